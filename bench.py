@@ -1,0 +1,496 @@
+"""Throughput of the mbarrier/TMA tile pipeline on one GB300 (or N, one per rank).
+
+One step = one pass of the whole hot path over one batch of input:
+  * tile_copy   fp16 16384 x 16384 (512 MiB), 128 x 64 tiles, seeded uniform[-1, 1)
+  * tile_rowsum bf16 8192 x 65536 (1 GiB), 64 x 256 tiles, seeded normal(0, 1)
+Metric: achieved HBM GB/s = algorithmic bytes (copy: read + write of the
+matrix; row sum: read of the matrix + write of the fp32 sums) / device time,
+1 GB = 1e9 B.  Inputs are far larger than the 129 MB L2, so no flush is needed
+between steps.
+
+Default (--impl mbtile) prints one JSON line on rank 0.  --impl reference times
+the CPU oracle (the plain restatement used by the tests) on a bounded sample of
+the same workload.  --sweep prints one extra line per stage / warp / CTA point.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+COPY = dict(name="copy", dtype="f16", M=16384, N=16384, tile_m=128, tile_n=64,
+            dist="uniform", seed=1003)
+ROWSUM = dict(name="rowsum", dtype="bf16", M=8192, N=65536, tile_m=64, tile_n=256,
+              dist="normal", seed=1004)
+ESIZE = {"f16": 2, "bf16": 2, "f32": 4}
+FALLBACK_HBM_GBS = 6800.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture
+# of each kernel on the full-size workload, keyed by the SHA-256 of the kernel
+# source it was taken on; reported only while the source is unchanged.
+NCU_TRAFFIC: dict = {}
+
+
+def copy_bytes(c=COPY):
+    return 2 * c["M"] * c["N"] * ESIZE[c["dtype"]]
+
+
+def rowsum_bytes(c=ROWSUM):
+    return c["M"] * c["N"] * ESIZE[c["dtype"]] + 4 * c["M"]
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("mbtile_kernels.cu", "internal.h"):
+        with open(os.path.join(ROOT, "mbarrier_async_tile_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples: list[tuple[float, list[str]]] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not inside and self.samples:
+            # timed region shorter than the sampling period: nearest samples
+            near = sorted(self.samples, key=lambda ts: abs(ts[0] - (t0 + t1) / 2))[:3]
+            inside, window = [s for _, s in near], "nearest"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(s[1]) for s in inside if num(s[1]) is not None]
+        mx = [num(s[2]) for s in inside if num(s[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4)
+                          if len(s) > 5 + i and s[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def make_inputs(device):
+    import synthetic
+
+    x3 = synthetic.make_matrix(COPY["M"], COPY["N"], COPY["dtype"], COPY["dist"],
+                               COPY["seed"], draw_on=str(device))
+    d3 = torch.empty_like(x3)
+    x4 = synthetic.make_matrix(ROWSUM["M"], ROWSUM["N"], ROWSUM["dtype"], ROWSUM["dist"],
+                               ROWSUM["seed"], draw_on=str(device))
+    o4 = torch.empty(ROWSUM["M"], dtype=torch.float32, device=device)
+    return x3, d3, x4, o4
+
+
+def cpu_baseline(x3, d3, x4, o4, budget_s: float = 12.0) -> dict:
+    """Time the CPU oracle on a bounded sample of the same workload (row
+    blocks of both matrices, alternated in proportion to their bytes, until
+    about ``budget_s`` of CPU time), and check the GPU's outputs on exactly
+    those rows against the oracle's."""
+    import oracle
+
+    oracle.build()
+    threads = 1   # the oracle is a plain single-threaded C loop
+    blk3, blk4 = 256, ROWSUM["tile_m"]
+    n3 = n4 = 0
+    t_cpu = 0.0
+    bytes_done = 0
+    mismatches = 0
+    worst = 0.0
+    r3 = r4 = 0
+    while t_cpu < budget_s and (r3 < COPY["M"] or r4 < ROWSUM["M"]):
+        # copy block
+        if r3 < COPY["M"] and (n3 * blk3 * COPY["N"] * 4 <= n4 * blk4 * ROWSUM["N"] * 2 + 1
+                               or r4 >= ROWSUM["M"]):
+            src = x3[r3:r3 + blk3].cpu()
+            want = torch.empty_like(src)
+            t = time.perf_counter()
+            oracle.copy(src, want)
+            t_cpu += time.perf_counter() - t
+            got = d3[r3:r3 + blk3].cpu()
+            mismatches += int((got.view(torch.int16) != want.view(torch.int16)).sum())
+            bytes_done += 2 * src.numel() * src.element_size()
+            r3 += blk3
+            n3 += 1
+        else:
+            src = x4[r4:r4 + blk4].cpu()
+            t = time.perf_counter()
+            ref, sq = oracle.rowsum(src, with_sumsq=True)
+            t_cpu += time.perf_counter() - t
+            got = o4[r4:r4 + blk4].cpu().double()
+            err = ((got - ref).abs() / torch.maximum(ref.abs(), sq.sqrt())).max().item()
+            worst = max(worst, err)
+            bytes_done += src.numel() * src.element_size() + 4 * src.shape[0]
+            r4 += blk4
+            n4 += 1
+    return {
+        "value": round(bytes_done / t_cpu / 1e9, 4), "unit": "GB/s", "cores": threads,
+        "kind": "oracle",
+        "sample": (f"{r3} of {COPY['M']} rows of the copy and {r4} of {ROWSUM['M']} rows "
+                   f"of the row sum ({bytes_done / 1e9:.3f} GB algorithmic, "
+                   f"{t_cpu:.1f} s on 1 host core)"),
+        "parity_on_sample": {"copy_mismatched_elements": mismatches,
+                             "rowsum_worst_scaled_error": worst},
+    }
+
+
+def bench_gpu(args, rank, world):
+    import mbarrier_async_tile_gb300 as mbt
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    mbt.tile_device_info()  # loads the library, fails loudly if it is missing
+    x3, d3, x4, o4 = make_inputs(dev)
+    stream = torch.cuda.current_stream()
+    ws_bytes = mbt.tile_rowsum_workspace_bytes(ROWSUM["M"], ROWSUM["N"], ROWSUM["tile_m"],
+                                               ROWSUM["tile_n"], args.rowsum_stages,
+                                               torch.bfloat16)
+    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        mbt.tile_copy(x3, d3, COPY["tile_m"], COPY["tile_n"], args.copy_stages, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        mbt.tile_rowsum(x4, o4, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
+                        workspace=ws, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    code, info = mbt.tile_status(stream)
+    if code != 0:
+        raise RuntimeError(f"pipeline status {code} {info}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    time.sleep(0.15)
+    clocks.stop()
+    code, info = mbt.tile_status(stream)
+    if code != 0:
+        raise RuntimeError(f"pipeline status {code} {info}")
+
+    ms_total = start.elapsed_time(end)
+    ms_copy = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    ms_rowsum = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    ms_max = reduce_max(ms_total, world)
+    step_bytes = copy_bytes() + rowsum_bytes()
+    value = world * step_bytes * args.steps / (ms_max / 1e3) / 1e9
+
+    # end to end through the public API with host buffers
+    e2e = bench_e2e(args, mbt, x3, x4, ws, stream, world)
+
+    peak, peak_kind = measured_peak()
+    kernels = {
+        "copy": {"ms": round(ms_copy, 4), "bytes": copy_bytes(),
+                 "gbs": round(copy_bytes() / ms_copy / 1e6, 1),
+                 "stages": args.copy_stages, "tile": [COPY["tile_m"], COPY["tile_n"]]},
+        "rowsum": {"ms": round(ms_rowsum, 4), "bytes": rowsum_bytes(),
+                   "gbs": round(rowsum_bytes() / ms_rowsum / 1e6, 1),
+                   "stages": args.rowsum_stages, "tile": [ROWSUM["tile_m"], ROWSUM["tile_n"]]},
+    }
+    dom_name = "copy" if ms_copy >= ms_rowsum else "rowsum"
+    dom = kernels[dom_name]
+    traffic = None
+    entry = NCU_TRAFFIC.get(dom_name)
+    if entry and entry.get("src_sha") == kernel_source_sha():
+        traffic = entry["bytes_per_launch"]
+    roofline = {"bound": "hbm", "kernel": f"mbt_{dom_name}_kernel",
+                "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
+                "frac": round(dom["gbs"] / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_kind} hbm_gbs (copy read+write)"}
+    out = {
+        "metric": "achieved HBM GB/s (read+write) for pipelined tile copy + rowsum",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 copy + bf16->f32 rowsum", "data": "synthetic (seeded, drawn on device)",
+        "config": {"workload": ("tile_copy fp16 16384x16384 tile 128x64 + tile_rowsum "
+                                "bf16 8192x65536 tile 64x256"),
+                   "copy_stages": args.copy_stages, "rowsum_stages": args.rowsum_stages,
+                   "l2": "inputs (512 MiB, 1 GiB) larger than L2; no flush",
+                   "parallelism": f"independent replica per GPU x{world}"},
+        "frac_of_peak": round(value / world / peak, 4),
+        "kernels": kernels,
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(t0, t1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(x3, d3, x4, o4, args.cpu_budget)
+    return out
+
+
+def bench_e2e(args, mbt, x3, x4, ws, stream, world):
+    """Same metric, through the public API, with host buffers: every step
+    copies the inputs from pinned host memory, runs both calls and reads the
+    results back."""
+    steps = max(1, min(args.steps, args.e2e_steps))
+    h3 = torch.empty(x3.shape, dtype=x3.dtype, pin_memory=True)
+    h3.copy_(x3)
+    h4 = torch.empty(x4.shape, dtype=x4.dtype, pin_memory=True)
+    h4.copy_(x4)
+    r3 = torch.empty_like(h3, pin_memory=True)
+    r4 = torch.empty(x4.shape[0], dtype=torch.float32, pin_memory=True)
+    g3, g3o = torch.empty_like(x3), torch.empty_like(x3)
+    g4, g4o = torch.empty_like(x4), torch.empty(x4.shape[0], dtype=torch.float32,
+                                                device=x4.device)
+
+    def step():
+        g3.copy_(h3, non_blocking=True)
+        mbt.tile_copy(g3, g3o, COPY["tile_m"], COPY["tile_n"], args.copy_stages, stream=stream)
+        r3.copy_(g3o, non_blocking=True)
+        g4.copy_(h4, non_blocking=True)
+        mbt.tile_rowsum(g4, g4o, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
+                        workspace=ws, stream=stream)
+        r4.copy_(g4o, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = reduce_max(s.elapsed_time(e), world)
+    value = world * (copy_bytes() + rowsum_bytes()) * steps / (ms / 1e3) / 1e9
+    return {"value": round(value, 1), "unit": "GB/s", "steps": steps,
+            "h2d_bytes_per_step": h3.numel() * h3.element_size() + h4.numel() * h4.element_size(),
+            "d2h_bytes_per_step": r3.numel() * r3.element_size() + r4.numel() * r4.element_size()}
+
+
+def bench_sweep(args):
+    """One line per (op, stages, consumer warps, CTAs per SM) point."""
+    import mbarrier_async_tile_gb300 as mbt
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    x3, d3, x4, o4 = make_inputs(dev)
+    ws = torch.zeros(1 << 22, dtype=torch.uint8, device=dev)
+    reps = 20
+
+    def timeit(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(reps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        assert mbt.tile_status()[0] == 0
+        return s.elapsed_time(e) / reps
+
+    for st in args.sweep_stages:
+        for w in args.sweep_warps:
+            for cps in args.sweep_ctas:
+                try:
+                    ms = timeit(lambda: mbt.tile_copy(x3, d3, COPY["tile_m"], COPY["tile_n"], st,
+                                                      consumer_warps=w, ctas_per_sm=cps))
+                    print(json.dumps({"sweep": "copy", "stages": st, "consumer_warps": w,
+                                      "ctas_per_sm": cps, "ms": round(ms, 4),
+                                      "gbs": round(copy_bytes() / ms / 1e6, 1)}), flush=True)
+                except mbt.MbtError as exc:
+                    print(json.dumps({"sweep": "copy", "stages": st, "consumer_warps": w,
+                                      "ctas_per_sm": cps, "error": str(exc)}), flush=True)
+                if st < 2 or st > 6:
+                    continue
+                try:
+                    ms = timeit(lambda: mbt.tile_rowsum(x4, o4, ROWSUM["tile_m"], ROWSUM["tile_n"],
+                                                        st, consumer_warps=w, ctas_per_sm=cps,
+                                                        workspace=ws))
+                    print(json.dumps({"sweep": "rowsum", "stages": st, "consumer_warps": w,
+                                      "ctas_per_sm": cps, "ms": round(ms, 4),
+                                      "gbs": round(rowsum_bytes() / ms / 1e6, 1)}), flush=True)
+                except mbt.MbtError as exc:
+                    print(json.dumps({"sweep": "rowsum", "stages": st, "consumer_warps": w,
+                                      "ctas_per_sm": cps, "error": str(exc)}), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+def bench_reference(args):
+    """Time the CPU oracle as it stands, one bounded sample of the workload
+    per step (row blocks of both matrices in proportion to their bytes)."""
+    import oracle
+    import synthetic
+
+    oracle.build()
+    rows3, rows4 = 512, 128   # about 16 + 16 MiB of input per step
+    x3 = synthetic.make_matrix(rows3, COPY["N"], COPY["dtype"], COPY["dist"], COPY["seed"])
+    x4 = synthetic.make_matrix(rows4, ROWSUM["N"], ROWSUM["dtype"], ROWSUM["dist"],
+                               ROWSUM["seed"])
+    d3 = torch.empty_like(x3)
+
+    def step():
+        oracle.copy(x3, d3)
+        oracle.rowsum(x4)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    sec = time.perf_counter() - t
+    nbytes = 2 * x3.numel() * 2 + x4.numel() * 2 + 4 * rows4
+    value = nbytes * args.steps / sec / 1e9
+    sample = (f"each step: oracle copy of {rows3} rows of the fp16 16384x16384 matrix and "
+              f"oracle row sum of {rows4} rows of the bf16 8192x65536 matrix "
+              f"({nbytes / 1e6:.1f} MB algorithmic), 1 host core")
+    return {
+        "impl": "reference",
+        "metric": "achieved HBM GB/s (read+write) for pipelined tile copy + rowsum",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(sec / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 copy + bf16->f64 rowsum", "data": "synthetic (seeded)",
+        "config": {"workload": ("tile_copy fp16 16384x16384 tile 128x64 + tile_rowsum "
+                                "bf16 8192x65536 tile 64x256 (row-block sample per step)")},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def reduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.distributed.get_backend() == "nccl" else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mbtile", "reference"], default="mbtile")
+    ap.add_argument("--copy-stages", type=int, default=4)
+    ap.add_argument("--rowsum-stages", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--sweep-stages", type=int, nargs="*", default=[1, 2, 3, 4, 6])
+    ap.add_argument("--sweep-warps", type=int, nargs="*", default=[3, 4, 7])
+    ap.add_argument("--sweep-ctas", type=int, nargs="*", default=[1, 2, 0])
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(bench_reference(args)), flush=True)
+        return 0
+    if args.sweep:
+        bench_sweep(args)
+        return 0
+    if world > 1:
+        torch.distributed.init_process_group(
+            backend="nccl" if torch.cuda.is_available() else "gloo")
+    out = bench_gpu(args, rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

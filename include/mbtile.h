@@ -1,0 +1,217 @@
+/*
+ * mbtile.h -- C ABI of the multi-stage mbarrier / bulk-tensor tile pipeline
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The library streams a 2-D row-major matrix from device memory through a ring
+ * of shared-memory stages.  One elected thread of a producer warp loads each
+ * tile with a single bulk tensor copy (TMA) into a 128-byte-swizzled stage and
+ * registers the expected bytes on the stage's "full" mbarrier; consumer warps
+ * wait on that barrier, use the tile, and arrive on the stage's "empty"
+ * mbarrier so the producer may refill it.  The consumers either write the tile
+ * back out (tile_copy) or reduce it to fp32 row sums (tile_rowsum).
+ *
+ * Where the operations are defined:
+ *   - "cute(11) Hopper TMA copy": §1 and §3 (a single thread issues one bulk
+ *     tensor load of a whole tile; the mbarrier expects the tile's bytes; the
+ *     tile is written back and must equal the input, §4); §2.2 (128-byte
+ *     swizzle atom, 16-byte units); §6 (proxy visibility: a load by the copy
+ *     engine followed by an mbarrier wait needs no extra fence).
+ *   - "cute(12) async_pipeline": §1 (a full/empty barrier pair per stage, the
+ *     producer at most S tiles ahead), §2 (the (index, phase, count) cursor,
+ *     producer start phase 1), §3 and §6.6-6.10 (acquire, wait, release, tail).
+ *   - "异步协作：mbarrier" (Async coordination: mbarrier): a phase completes
+ *     when both the owed arrivals and the tx-count reach zero; waits use the
+ *     phase parity and must be retried.
+ *   - "CUDA features 10: Pipelines" (§4.10.4-4.10.5): warp-uniform control of
+ *     the pipeline and completing every acquired stage before exit.
+ *   The row sum is not on the pages (their consumer only "uses" the tile); it
+ *   is the plain definition out[i] = sum_j src[i][j].
+ *
+ * Conventions common to every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates or frees device memory; it keeps only per-device caches
+ *     (SM count, shared-memory limit, the driver's tensor-map encoder) and a
+ *     small per-device status word (see tile_status).
+ *   - Matrices are row-major: element (i, j) is at ptr[i * ld + j], with the
+ *     row pitch ld in elements.  The logical shape is M rows by N columns.
+ *     ld * element size must be a multiple of 16 bytes and the base pointer
+ *     16-byte aligned (a bulk tensor copy's global stride rule); a dense
+ *     matrix whose rows are not a multiple of 16 bytes must be stored pitched.
+ *   - A tile is tile_m rows by tile_n columns.  tile_n * element size must be
+ *     128, 256, 512 or 1024 bytes (1, 2, 4 or 8 side-by-side 128-byte boxes,
+ *     each one bulk copy with the 128-byte swizzle); 1 <= tile_m <= 256;
+ *     1 <= stages <= 8.  Tiles that run past row M or column N are loaded
+ *     with zero fill and never written past the logical shape.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream) of the
+ *     current device.  Calls are asynchronous on it, like any CUDA library.
+ *   - Return value: MBT_OK, or a negative mbt_status.  Argument errors are
+ *     detected on the host before anything is launched.  A pipeline wait that
+ *     runs past its time budget on the device does not hang: the kernel
+ *     records MBT_ERR_TIMEOUT in the status word and returns; tile_status
+ *     reports it.
+ *   - Thread safety: entry points may be called from several host threads.
+ *     Concurrent calls must not share a workspace.
+ */
+#ifndef MBTILE_H
+#define MBTILE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types.  Copies move raw bits; row sums widen exactly to fp32. */
+typedef enum mbt_dtype { MBT_F16 = 0, MBT_BF16 = 1, MBT_F32 = 2 } mbt_dtype;
+
+typedef enum mbt_status {
+    MBT_OK = 0,
+    MBT_ERR_ARG = -1,          /* null pointer, bad size, shape or enum */
+    MBT_ERR_ALIGN = -2,        /* base or row pitch not 16-byte aligned */
+    MBT_ERR_UNSUPPORTED = -3,  /* tile shape / warp count outside the supported set */
+    MBT_ERR_SMEM = -4,         /* stages x tile exceed the shared memory of one CTA */
+    MBT_ERR_CUDA = -5,         /* a CUDA runtime call or the launch failed */
+    MBT_ERR_TIMEOUT = -6,      /* a pipeline wait ran out of its time budget */
+    MBT_ERR_DRIVER = -7,       /* tensor-map encoder unavailable or it refused */
+    MBT_ERR_WORKSPACE = -8     /* workspace given but smaller than required */
+} mbt_status;
+
+/* Optional settings.  A zero-filled struct (or a NULL pointer) selects every
+ * default. */
+typedef struct mbt_opts {
+    int64_t ld_src;          /* row pitch of src in elements; 0 => N */
+    int64_t ld_dst;          /* row pitch of dst in elements (copy); 0 => N */
+    int32_t max_ctas;        /* upper bound on the grid; 0 => no bound */
+    int32_t ctas_per_sm;     /* CTAs per SM of the persistent grid;
+                                0 => as many as fit */
+    int32_t consumer_warps;  /* consumer warps per CTA, 1..8; 0 => 4.  The
+                                CTA has one more warp, the producer. */
+    int32_t store_mode;      /* reserved; must be 0 */
+    uint64_t wait_budget_ns; /* time bound of every mbarrier wait; 0 => 1 s */
+    int32_t *log;            /* optional device buffer of int32 records, see
+                                below; NULL => no log */
+    int64_t log_capacity;    /* records per role in `log` */
+    void *workspace;         /* tile_rowsum only: device scratch that lets
+                                several CTAs share one row band; NULL => every
+                                band is reduced by a single CTA */
+    size_t workspace_bytes;  /* size of `workspace` */
+    int32_t fault;           /* test hook, 0 = none.  1: the producer starts at
+                                phase 0; 2: consumers never release a stage.
+                                Both make the pipeline stall by design, so the
+                                call ends with MBT_ERR_TIMEOUT after about
+                                (stages + 2) x wait_budget_ns; no bulk copy is
+                                in flight when the kernel returns. */
+    int32_t reserved[7];     /* must be 0 */
+} mbt_opts;
+
+/* Launch plan, as computed by tile_plan (host only, no CUDA calls). */
+typedef struct mbt_plan {
+    int32_t grid;            /* CTAs launched */
+    int32_t threads;         /* threads per CTA = 32 x (1 + consumer_warps) */
+    int32_t consumer_warps;
+    int32_t smem_bytes;      /* dynamic shared memory per CTA */
+    int32_t boxes;           /* 128-byte boxes per tile row */
+    int32_t box_inner;       /* elements per box row (128 / element size) */
+    int32_t box_rows;        /* rows per box (= tile_m) */
+    int32_t tx_bytes;        /* bytes registered on a full barrier per tile */
+    int32_t stage_bytes;     /* shared-memory bytes of one stage */
+    int32_t split;           /* row sum: 1 if a band may span several CTAs */
+    int32_t kmax;            /* row sum: most CTAs contributing to one band */
+    int32_t reserved0;
+    int64_t tiles_m;         /* tiles down the rows (row bands) */
+    int64_t tiles_n;         /* tiles across the columns */
+    int64_t num_tiles;
+    size_t workspace_bytes;  /* row sum: workspace bytes this plan needs */
+} mbt_plan;
+
+enum { MBT_OP_COPY = 0, MBT_OP_ROWSUM = 1 };
+
+/*
+ * tile_copy -- dst[i][j] = src[i][j], bit for bit, for 0 <= i < M, 0 <= j < N.
+ *
+ * Defined by "cute(11) Hopper TMA copy" §4 and "cute(12) async_pipeline" §3:
+ * every tile is loaded by one bulk tensor copy into a swizzled stage and the
+ * consumer warps store it back with 16-byte coalesced stores.
+ *   src, dst   device pointers, dense (ld = N) or pitched (see opts);
+ *              src and dst must not overlap unless equal.
+ *   M, N       logical shape, >= 0 (M == 0 or N == 0: nothing to do).
+ *   tile_m, tile_n, stages, dtype: see the conventions above.
+ * Elements of dst outside the logical shape (pad columns) are not written.
+ */
+int tile_copy(const void *src, void *dst, int64_t M, int64_t N, int tile_m,
+              int tile_n, int stages, int dtype, void *stream);
+int tile_copy_ex(const void *src, void *dst, int64_t M, int64_t N, int tile_m,
+                 int tile_n, int stages, int dtype, void *stream,
+                 const mbt_opts *opts);
+
+/*
+ * tile_rowsum -- out[i] = sum over j < N of src[i][j], for 0 <= i < M.
+ *
+ * Elements are widened exactly to fp32 and summed in fp32 in a fixed order
+ * (per thread: the 16-byte chunks of a tile in column order; then the tiles
+ * of a band in column order; then the threads of a row; then, with a
+ * workspace, the CTAs of a band in CTA order), so repeated calls with the same
+ * plan give identical bits.
+ *   src        device pointer, dense or pitched (opts->ld_src).
+ *   out        device pointer to M floats (dense).
+ *   M, N       >= 0.  N == 0 writes zeros; M == 0 does nothing.
+ * Without a workspace each row band (tile_m rows) is reduced by one CTA;
+ * with one (size from tile_rowsum_workspace_bytes, zero-filled before its
+ * first use, and left zero-filled by every call that completes without a
+ * timeout) the bands are split evenly over a persistent grid and the last
+ * CTA of each band combines the partial sums.
+ */
+int tile_rowsum(const void *src, float *out, int64_t M, int64_t N, int tile_m,
+                int tile_n, int stages, int dtype, void *stream);
+int tile_rowsum_ex(const void *src, float *out, int64_t M, int64_t N,
+                   int tile_m, int tile_n, int stages, int dtype, void *stream,
+                   const mbt_opts *opts);
+
+/* Workspace bytes tile_rowsum_ex needs on the current device for this shape
+ * and these options (opts->workspace is ignored).  0 when no split helps. */
+int tile_rowsum_workspace_bytes(int64_t M, int64_t N, int tile_m, int tile_n,
+                                int stages, int dtype, const mbt_opts *opts,
+                                size_t *bytes);
+
+/*
+ * tile_plan -- the launch plan for op (MBT_OP_COPY or MBT_OP_ROWSUM), from
+ * the device figures given as arguments; makes no CUDA call.
+ *   num_sms        SMs of the device (> 0).
+ *   smem_optin     opt-in dynamic shared memory limit per CTA, bytes.
+ *   fit_per_sm     CTAs of this plan that fit on one SM (> 0).
+ *   with_workspace row sum: plan for a split band (1) or whole bands (0).
+ * Returns the same argument errors as the entry points.
+ */
+int tile_plan(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages,
+              int dtype, const mbt_opts *opts, int num_sms, int smem_optin,
+              int fit_per_sm, int with_workspace, mbt_plan *plan);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word.  info (may be NULL) receives {code, block, stage, role * 2 + parity}
+ * of the first wait that timed out (role 0 = producer, 1 = consumer).
+ * Returns MBT_OK, MBT_ERR_TIMEOUT, or MBT_ERR_CUDA. */
+int tile_status(void *stream, int32_t info[4]);
+
+/* Static description of a status code; never NULL. */
+const char *tile_strerror(int code);
+
+/* Figures of device `device`: SM count, opt-in shared memory per CTA and the
+ * theoretical memory bandwidth 2 x memory clock x bus width (GB/s = 1e9 B/s).
+ * Any output pointer may be NULL. */
+int tile_device_info(int device, int *num_sms, int *smem_optin,
+                     double *hbm_gbs_theoretical);
+
+/*
+ * Log records (opts->log).  Only CTA 0 records.  The buffer holds
+ * 2 x log_capacity records of 4 int32 each: records [0, cap) belong to the
+ * producer, [cap, 2 cap) to consumer warp 0.  Record k of a role is
+ * {k, stage index, phase parity waited on, tile number}; tiles past the
+ * capacity are not recorded.  The caller zero-fills the buffer beforehand.
+ */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MBTILE_H */

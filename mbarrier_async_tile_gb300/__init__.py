@@ -1,0 +1,291 @@
+"""Python binding of libmbtile, the sm_103a mbarrier/TMA tile pipeline.
+
+Argument marshalling only: every step of ``tile_copy`` and ``tile_rowsum``
+runs in the library's CUDA kernels.  PyTorch supplies device memory and
+streams.  If the compiled library is missing, every call raises; there is no
+fallback path.
+
+The C entry points are reachable with the header's names through ``C`` (a
+ctypes handle); the functions below take ``torch.Tensor`` arguments.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "MbtError", "C", "library_path", "tile_copy", "tile_rowsum", "tile_status",
+    "tile_plan", "tile_device_info", "tile_strerror", "tile_rowsum_workspace_bytes",
+    "Opts", "Plan", "DTYPE_CODE", "OP_COPY", "OP_ROWSUM",
+]
+
+MBT_OK = 0
+MBT_ERR_TIMEOUT = -6
+OP_COPY, OP_ROWSUM = 0, 1
+DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
+
+
+class Opts(ctypes.Structure):
+    """Mirror of ``mbt_opts`` in include/mbtile.h."""
+    _fields_ = [
+        ("ld_src", ctypes.c_int64),
+        ("ld_dst", ctypes.c_int64),
+        ("max_ctas", ctypes.c_int32),
+        ("ctas_per_sm", ctypes.c_int32),
+        ("consumer_warps", ctypes.c_int32),
+        ("store_mode", ctypes.c_int32),
+        ("wait_budget_ns", ctypes.c_uint64),
+        ("log", ctypes.c_void_p),
+        ("log_capacity", ctypes.c_int64),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("fault", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 7),
+    ]
+
+
+class Plan(ctypes.Structure):
+    """Mirror of ``mbt_plan`` in include/mbtile.h."""
+    _fields_ = [
+        ("grid", ctypes.c_int32),
+        ("threads", ctypes.c_int32),
+        ("consumer_warps", ctypes.c_int32),
+        ("smem_bytes", ctypes.c_int32),
+        ("boxes", ctypes.c_int32),
+        ("box_inner", ctypes.c_int32),
+        ("box_rows", ctypes.c_int32),
+        ("tx_bytes", ctypes.c_int32),
+        ("stage_bytes", ctypes.c_int32),
+        ("split", ctypes.c_int32),
+        ("kmax", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("tiles_m", ctypes.c_int64),
+        ("tiles_n", ctypes.c_int64),
+        ("num_tiles", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved0"}
+
+
+class MbtError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {tile_strerror(code)} (status {code})" if what
+                         else f"{tile_strerror(code)} (status {code})")
+
+
+_lock = threading.Lock()
+_C = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def _load():
+    global _C
+    with _lock:
+        if _C is not None:
+            return _C
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libmbtile.so is not built ({path}); run __graft_entry__.build() "
+                "or mbarrier_async_tile_gb300._build.build()")
+        lib = ctypes.CDLL(path)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        sig = [vp, vp, i64, i64, i32, i32, i32, i32, vp]
+        lib.tile_copy.argtypes = sig
+        lib.tile_copy_ex.argtypes = sig + [ctypes.POINTER(Opts)]
+        lib.tile_rowsum.argtypes = sig
+        lib.tile_rowsum_ex.argtypes = sig + [ctypes.POINTER(Opts)]
+        lib.tile_rowsum_workspace_bytes.argtypes = [i64, i64, i32, i32, i32, i32,
+                                                    ctypes.POINTER(Opts),
+                                                    ctypes.POINTER(ctypes.c_size_t)]
+        lib.tile_plan.argtypes = [i32, i64, i64, i32, i32, i32, i32, ctypes.POINTER(Opts),
+                                  i32, i32, i32, i32, ctypes.POINTER(Plan)]
+        lib.tile_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+        lib.tile_strerror.argtypes = [i32]
+        lib.tile_strerror.restype = ctypes.c_char_p
+        lib.tile_device_info.argtypes = [i32, ctypes.POINTER(ctypes.c_int),
+                                         ctypes.POINTER(ctypes.c_int),
+                                         ctypes.POINTER(ctypes.c_double)]
+        for name in ("tile_copy", "tile_copy_ex", "tile_rowsum", "tile_rowsum_ex",
+                     "tile_rowsum_workspace_bytes", "tile_plan", "tile_status",
+                     "tile_device_info"):
+            getattr(lib, name).restype = ctypes.c_int
+        _C = lib
+        return lib
+
+
+class _LazyC:
+    """``C.tile_copy(...)`` etc.: the raw C entry points, loaded on first use."""
+
+    def __getattr__(self, name):
+        return getattr(_load(), name)
+
+
+C = _LazyC()
+
+
+def tile_strerror(code: int) -> str:
+    return _load().tile_strerror(code).decode()
+
+
+def _check(code: int, what: str) -> None:
+    if code != MBT_OK:
+        raise MbtError(code, what)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _matrix(t: torch.Tensor, name: str) -> tuple[int, int, int]:
+    if not isinstance(t, torch.Tensor) or t.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in DTYPE_CODE:
+        raise ValueError(f"{name} has unsupported dtype {t.dtype}")
+    M, N = t.shape
+    if M > 0 and N > 0 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major (unit column stride)")
+    ld = t.stride(0) if M > 1 else max(N, t.stride(0))
+    return M, N, ld
+
+
+def _opts(**kw) -> Opts:
+    o = Opts()
+    for k, v in kw.items():
+        if v is not None:
+            setattr(o, k, v)
+    return o
+
+
+def tile_copy(src: torch.Tensor, dst: torch.Tensor, tile_m: int = 128, tile_n: int = 64,
+              stages: int = 4, *, consumer_warps: int = 0, max_ctas: int = 0,
+              ctas_per_sm: int = 0, wait_budget_ns: int = 0, log: torch.Tensor | None = None,
+              fault: int = 0, stream=None) -> torch.Tensor:
+    """dst[i, j] = src[i, j] (bit-exact) through the tile pipeline.
+
+    ``src`` and ``dst`` are 2-D CUDA views of the same shape and dtype with
+    unit column stride; their row strides may differ (pitched storage)."""
+    M, N, ld_s = _matrix(src, "src")
+    Md, Nd, ld_d = _matrix(dst, "dst")
+    if (M, N) != (Md, Nd) or src.dtype != dst.dtype:
+        raise ValueError("src and dst must have the same shape and dtype")
+    o = _opts(ld_src=ld_s, ld_dst=ld_d, consumer_warps=consumer_warps, max_ctas=max_ctas,
+              ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault)
+    if log is not None:
+        o.log = log.data_ptr()
+        o.log_capacity = log.numel() // 8
+    rc = _load().tile_copy_ex(src.data_ptr(), dst.data_ptr(), M, N, tile_m, tile_n, stages,
+                              DTYPE_CODE[src.dtype], _stream_handle(stream), ctypes.byref(o))
+    _check(rc, "tile_copy")
+    return dst
+
+
+_ws_lock = threading.Lock()
+_ws_cache: dict[int, torch.Tensor] = {}
+
+
+def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    """A zero-filled byte buffer of at least ``nbytes`` on ``device``, reused
+    across calls (the kernels leave it zero-filled)."""
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    with _ws_lock:
+        buf = _ws_cache.get(idx)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
+            _ws_cache[idx] = buf
+        return buf
+
+
+def _reset_workspaces() -> None:
+    with _ws_lock:
+        for buf in _ws_cache.values():
+            buf.zero_()
+
+
+def tile_rowsum_workspace_bytes(M: int, N: int, tile_m: int, tile_n: int, stages: int,
+                                dtype: torch.dtype, **opt) -> int:
+    o = _opts(**opt)
+    out = ctypes.c_size_t(0)
+    rc = _load().tile_rowsum_workspace_bytes(M, N, tile_m, tile_n, stages, DTYPE_CODE[dtype],
+                                             ctypes.byref(o), ctypes.byref(out))
+    _check(rc, "tile_rowsum_workspace_bytes")
+    return out.value
+
+
+def tile_rowsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int = 64,
+                tile_n: int = 256, stages: int = 4, *, split: bool = True,
+                consumer_warps: int = 0, max_ctas: int = 0, ctas_per_sm: int = 0,
+                wait_budget_ns: int = 0, log: torch.Tensor | None = None, fault: int = 0,
+                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[i] = sum_j src[i, j] in fp32 through the tile pipeline.
+
+    With ``split`` (default) row bands may be shared by several CTAs, using a
+    zero-filled workspace (cached per device unless one is given)."""
+    M, N, ld_s = _matrix(src, "src")
+    if out is None:
+        out = torch.empty(M, dtype=torch.float32, device=src.device)
+    if out.dtype != torch.float32 or out.numel() != M or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor of M elements")
+    o = _opts(ld_src=ld_s, consumer_warps=consumer_warps, max_ctas=max_ctas,
+              ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault)
+    if log is not None:
+        o.log = log.data_ptr()
+        o.log_capacity = log.numel() // 8
+    if split and M > 0 and N > 0:
+        need = tile_rowsum_workspace_bytes(M, N, tile_m, tile_n, stages, src.dtype,
+                                           ld_src=ld_s, consumer_warps=consumer_warps,
+                                           max_ctas=max_ctas, ctas_per_sm=ctas_per_sm)
+        if need:
+            ws = workspace if workspace is not None else _workspace(src.device, need)
+            o.workspace = ws.data_ptr()
+            o.workspace_bytes = ws.numel() * ws.element_size()
+    rc = _load().tile_rowsum_ex(src.data_ptr(), out.data_ptr(), M, N, tile_m, tile_n, stages,
+                                DTYPE_CODE[src.dtype], _stream_handle(stream), ctypes.byref(o))
+    _check(rc, "tile_rowsum")
+    return out
+
+
+def tile_status(stream=None) -> tuple[int, list[int]]:
+    """Synchronise ``stream`` and read-and-clear the device status word.
+    Returns (code, [code, block, stage, role * 2 + parity])."""
+    info = (ctypes.c_int32 * 4)()
+    rc = _load().tile_status(_stream_handle(stream), info)
+    if rc == MBT_ERR_TIMEOUT:
+        _reset_workspaces()
+    return rc, list(info)
+
+
+def tile_plan(op: int, M: int, N: int, tile_m: int, tile_n: int, stages: int,
+              dtype: torch.dtype, *, num_sms: int, smem_optin: int, fit_per_sm: int,
+              with_workspace: bool = False, **opt) -> dict:
+    o = _opts(**opt)
+    p = Plan()
+    rc = _load().tile_plan(op, M, N, tile_m, tile_n, stages, DTYPE_CODE[dtype],
+                           ctypes.byref(o), num_sms, smem_optin, fit_per_sm,
+                           int(with_workspace), ctypes.byref(p))
+    _check(rc, "tile_plan")
+    return p.as_dict()
+
+
+def tile_device_info(device: int | None = None) -> dict:
+    dev = torch.cuda.current_device() if device is None else device
+    sms, smem = ctypes.c_int(0), ctypes.c_int(0)
+    gbs = ctypes.c_double(0.0)
+    rc = _load().tile_device_info(dev, ctypes.byref(sms), ctypes.byref(smem), ctypes.byref(gbs))
+    _check(rc, "tile_device_info")
+    return {"num_sms": sms.value, "smem_optin": smem.value, "hbm_gbs_theoretical": gbs.value}

@@ -1,0 +1,72 @@
+// Internal interface between the host side of libmbtile (mbtile_host.cpp) and
+// its kernels (mbtile_kernels.cu).  Not installed; the public ABI is mbtile.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mbtile.h"
+
+namespace mbt {
+
+constexpr int kMaxStages = 8;
+constexpr int kMaxConsumerWarps = 8;
+constexpr int kMaxThreads = 32 * (1 + kMaxConsumerWarps);
+constexpr int kBoxRowBytes = 128;      // one 128-byte swizzle span per box row
+constexpr int kSwizzleAtomBytes = 1024;
+constexpr uint64_t kDefaultWaitBudgetNs = 1000000000ull;  // 1 s
+
+// Fields every pipeline kernel needs.  Sizes in elements unless named *_bytes.
+struct PipeArgs {
+    int64_t M, N;              // logical shape
+    int64_t tiles_n;           // tiles across the columns
+    int64_t num_tiles;         // tiles_m * tiles_n
+    int32_t tile_m;            // rows per tile (= rows per box)
+    int32_t boxes;             // 128-byte boxes per tile row: 1, 2, 4 or 8
+    int32_t box_inner;         // elements per box row (128 / esize)
+    int32_t esize;             // bytes per element
+    int32_t stages;
+    int32_t consumer_warps;
+    uint32_t box_stride;       // shared-memory bytes between box buffers
+    uint32_t stage_stride;     // shared-memory bytes between stages
+    uint32_t tx_bytes;         // bytes one tile delivers to its full barrier
+    int32_t fault;             // test hook, see mbt_opts.fault
+    uint64_t wait_budget_ns;
+    int32_t *log;
+    int64_t log_cap;
+};
+
+struct CopyArgs {
+    PipeArgs p;
+    char *dst;
+    int64_t ld_dst_bytes;
+};
+
+struct RowsumArgs {
+    PipeArgs p;
+    float *out;
+    float *partial;            // [bands][kmax][tile_m], used when kmax > 1
+    int32_t *ticket;           // [bands], zero between calls
+    int64_t units;             // scheduling units = num_tiles / gran
+    int64_t gran;              // tiles per scheduling unit (1 or tiles_n)
+    int32_t kmax;
+    int32_t pad_;
+};
+
+// Launchers (mbtile_kernels.cu).  They only enqueue work on `stream`.
+cudaError_t launch_copy(const CUtensorMap &map, const CopyArgs &a, int grid,
+                        int threads, int smem, cudaStream_t stream);
+cudaError_t launch_rowsum(int dtype, const CUtensorMap &map,
+                          const RowsumArgs &a, int grid, int threads, int smem,
+                          cudaStream_t stream);
+cudaError_t launch_fill_zero(float *out, int64_t n, cudaStream_t stream);
+// Raise every kernel's dynamic shared-memory limit as far as the device's
+// opt-in limit allows; `usable` receives the limit common to all kernels.
+cudaError_t set_kernel_smem_limit(int optin, int *usable);
+// CTAs of a kernel with this block/smem shape that fit on one SM.
+cudaError_t kernel_fit_per_sm(int op, int dtype, int threads, int smem, int *fit);
+// Read the device status word and clear it (synchronous).
+cudaError_t read_and_clear_status(int32_t info[4]);
+
+}  // namespace mbt

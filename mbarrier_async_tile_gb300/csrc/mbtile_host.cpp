@@ -1,0 +1,420 @@
+// Host side of libmbtile: argument checks, launch planning, tensor-map
+// encoding and the extern "C" entry points declared in mbtile.h.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace {
+
+using mbt::CopyArgs;
+using mbt::PipeArgs;
+using mbt::RowsumArgs;
+
+constexpr int kDefaultConsumerWarps = 4;
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxCoord = 0x7fffffff;  // bulk-copy coordinates are int32
+
+struct DeviceFigures {
+    bool ready = false;
+    int num_sms = 0;
+    int smem_optin = 0;   // dynamic shared memory every kernel may use
+};
+
+std::mutex g_mutex;
+DeviceFigures g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int esize_of(int dtype) {
+    switch (dtype) {
+        case MBT_F16:
+        case MBT_BF16: return 2;
+        case MBT_F32: return 4;
+        default: return 0;
+    }
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t m) { return ceil_div(a, m) * m; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks that need no device.  Fills the effective row pitches.
+int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, int tile_m,
+               int tile_n, int stages, int dtype, const mbt_opts &o, int64_t *ld_src,
+               int64_t *ld_dst) {
+    const int es = esize_of(dtype);
+    if (es == 0) return MBT_ERR_ARG;
+    if (op != MBT_OP_COPY && op != MBT_OP_ROWSUM) return MBT_ERR_ARG;
+    if (M < 0 || N < 0) return MBT_ERR_ARG;
+    if (tile_m < 1 || tile_m > 256 || tile_n < 1 || stages < 1 || stages > mbt::kMaxStages)
+        return MBT_ERR_ARG;
+    const int64_t row_bytes = static_cast<int64_t>(tile_n) * es;
+    if (row_bytes != 128 && row_bytes != 256 && row_bytes != 512 && row_bytes != 1024)
+        return MBT_ERR_UNSUPPORTED;
+    if (o.consumer_warps < 0 || o.consumer_warps > mbt::kMaxConsumerWarps) return MBT_ERR_ARG;
+    if (o.ctas_per_sm < 0 || o.max_ctas < 0 || o.log_capacity < 0) return MBT_ERR_ARG;
+    if (o.fault < 0 || o.fault > 2) return MBT_ERR_ARG;
+    if (o.store_mode != 0) return MBT_ERR_UNSUPPORTED;
+    for (int r : o.reserved)
+        if (r != 0) return MBT_ERR_ARG;
+    if (o.log != nullptr && o.log_capacity == 0) return MBT_ERR_ARG;
+    if (o.workspace == nullptr && o.workspace_bytes != 0) return MBT_ERR_ARG;
+    if (M > kMaxCoord || N > kMaxCoord) return MBT_ERR_UNSUPPORTED;
+    *ld_src = o.ld_src ? o.ld_src : N;
+    *ld_dst = o.ld_dst ? o.ld_dst : N;
+    if (*ld_src < N || *ld_dst < N || *ld_src < 0 || *ld_dst < 0) return MBT_ERR_ARG;
+    if (op == MBT_OP_ROWSUM && o.ld_dst != 0) return MBT_ERR_ARG;
+    const bool empty = (M == 0 || N == 0);
+    if (empty) {
+        // Nothing is read; a row sum of empty rows still writes M zeros.
+        if (op == MBT_OP_ROWSUM && M > 0 && dst == nullptr) return MBT_ERR_ARG;
+        return MBT_OK;
+    }
+    if (src == nullptr || dst == nullptr) return MBT_ERR_ARG;
+    if (!aligned16(src) || (*ld_src * es) % 16 != 0) return MBT_ERR_ALIGN;
+    if (op == MBT_OP_COPY && (!aligned16(dst) || (*ld_dst * es) % 16 != 0)) return MBT_ERR_ALIGN;
+    if (op == MBT_OP_ROWSUM && (reinterpret_cast<uintptr_t>(dst) & 3u) != 0) return MBT_ERR_ALIGN;
+    if (static_cast<uint64_t>(*ld_src) * es >= (1ull << 40)) return MBT_ERR_UNSUPPORTED;
+    return MBT_OK;
+}
+
+// CTA that owns tile x in a split of `units` units of `gran` tiles over G CTAs.
+int64_t unit_owner(int64_t x, int64_t gran, int64_t units, int64_t G) {
+    return ((x / gran + 1) * G - 1) / units;
+}
+
+// Most CTAs that share one band when `num_tiles` tiles are split tile by tile.
+int32_t most_contributors(int64_t tiles_n, int64_t num_tiles, int64_t G) {
+    int64_t kmax = 1;
+    for (int64_t b = 1; b < G; ++b) {
+        const int64_t start = b * num_tiles / G;
+        if (start % tiles_n == 0) continue;   // boundary between bands
+        const int64_t band = start / tiles_n;
+        const int64_t x0 = band * tiles_n;
+        const int64_t k = unit_owner(x0 + tiles_n - 1, 1, num_tiles, G) -
+                          unit_owner(x0, 1, num_tiles, G) + 1;
+        kmax = std::max(kmax, k);
+    }
+    return static_cast<int32_t>(kmax);
+}
+
+int consumer_warps_for(int op, int tile_m, const mbt_opts &o) {
+    if (o.consumer_warps) return o.consumer_warps;
+    if (op == MBT_OP_ROWSUM)
+        return std::max(kDefaultConsumerWarps, static_cast<int>(ceil_div(tile_m, 32)));
+    return kDefaultConsumerWarps;
+}
+
+int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, int dtype,
+              const mbt_opts &o, int num_sms, int smem_optin, int fit_per_sm,
+              int with_workspace, mbt_plan *plan) {
+    if (plan == nullptr || num_sms < 1 || fit_per_sm < 1) return MBT_ERR_ARG;
+    const int es = esize_of(dtype);
+    std::memset(plan, 0, sizeof *plan);
+    const int W = consumer_warps_for(op, tile_m, o);
+    if (op == MBT_OP_ROWSUM && W * 32 < tile_m) return MBT_ERR_UNSUPPORTED;
+    plan->consumer_warps = W;
+    plan->threads = 32 * (1 + W);
+    plan->box_inner = mbt::kBoxRowBytes / es;
+    plan->boxes = tile_n * es / mbt::kBoxRowBytes;
+    plan->box_rows = tile_m;
+    const int64_t box_stride = round_up(static_cast<int64_t>(tile_m) * mbt::kBoxRowBytes,
+                                        mbt::kSwizzleAtomBytes);
+    plan->stage_bytes = static_cast<int32_t>(plan->boxes * box_stride);
+    plan->tx_bytes = plan->boxes * tile_m * mbt::kBoxRowBytes;
+    const int64_t smem = static_cast<int64_t>(stages) * plan->stage_bytes + mbt::kSwizzleAtomBytes;
+    if (smem > smem_optin) return MBT_ERR_SMEM;
+    plan->smem_bytes = static_cast<int32_t>(smem);
+    plan->tiles_m = ceil_div(M, tile_m);
+    plan->tiles_n = ceil_div(N, tile_n);
+    plan->num_tiles = plan->tiles_m * plan->tiles_n;
+    int64_t per_sm = o.ctas_per_sm ? std::min(o.ctas_per_sm, fit_per_sm) : fit_per_sm;
+    int64_t cap = per_sm * num_sms;
+    if (o.max_ctas) cap = std::min<int64_t>(cap, o.max_ctas);
+    if (plan->num_tiles == 0) return MBT_OK;
+    if (op == MBT_OP_COPY) {
+        plan->grid = static_cast<int32_t>(std::min<int64_t>(plan->num_tiles, cap));
+        plan->kmax = 1;
+        return MBT_OK;
+    }
+    if (with_workspace) {
+        const int64_t G = std::min<int64_t>(plan->num_tiles, cap);
+        const int32_t kmax = most_contributors(plan->tiles_n, plan->num_tiles, G);
+        if (kmax > 1) {
+            plan->grid = static_cast<int32_t>(G);
+            plan->split = 1;
+            plan->kmax = kmax;
+            plan->workspace_bytes =
+                static_cast<size_t>(round_up(plan->tiles_m * 4, 256) +
+                                    plan->tiles_m * kmax * static_cast<int64_t>(tile_m) * 4);
+            return MBT_OK;
+        }
+    }
+    plan->grid = static_cast<int32_t>(std::min<int64_t>(plan->tiles_m, cap));
+    plan->split = 0;
+    plan->kmax = 1;
+    return MBT_OK;
+}
+
+int device_figures(DeviceFigures *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MBT_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceFigures &d = g_devices[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
+            return MBT_ERR_CUDA;
+        int usable = 0;
+        if (mbt::set_kernel_smem_limit(d.smem_optin, &usable) != cudaSuccess) return MBT_ERR_CUDA;
+        d.smem_optin = usable;
+        d.ready = true;
+    }
+    *out = d;
+    return MBT_OK;
+}
+
+int encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_encode == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                               cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || p == nullptr)
+            return MBT_ERR_DRIVER;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    *fn = g_encode;
+    return MBT_OK;
+}
+
+// 2-D tiled map over the logical M x N matrix: box = 128 bytes x tile_m rows,
+// 128-byte swizzle, zero fill outside the matrix.
+int encode_map(CUtensorMap *map, const void *src, int64_t M, int64_t N, int64_t ld, int dtype,
+               int tile_m) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    int rc = encoder(&fn);
+    if (rc != MBT_OK) return rc;
+    const int es = esize_of(dtype);
+    const CUtensorMapDataType type = dtype == MBT_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                     : dtype == MBT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * es};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(mbt::kBoxRowBytes / es),
+                               static_cast<cuuint32_t>(tile_m)};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    const CUresult r = fn(map, type, 2, const_cast<void *>(src), dims, strides, box, elem_strides,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MBT_OK : MBT_ERR_DRIVER;
+}
+
+// Plan for the current device (occupancy included).
+int plan_on_device(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, int dtype,
+                   const mbt_opts &o, int with_workspace, mbt_plan *plan) {
+    DeviceFigures d;
+    int rc = device_figures(&d);
+    if (rc != MBT_OK) return rc;
+    rc = plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, d.num_sms, d.smem_optin, 1,
+                   with_workspace, plan);
+    if (rc != MBT_OK) return rc;
+    int fit = 0;
+    if (mbt::kernel_fit_per_sm(op, dtype, plan->threads, plan->smem_bytes, &fit) != cudaSuccess)
+        return MBT_ERR_CUDA;
+    if (fit < 1) return MBT_ERR_SMEM;
+    return plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, d.num_sms, d.smem_optin, fit,
+                     with_workspace, plan);
+}
+
+PipeArgs pipe_args(const mbt_plan &plan, int64_t M, int64_t N, int tile_m, int stages, int dtype,
+                   const mbt_opts &o) {
+    PipeArgs p{};
+    p.M = M;
+    p.N = N;
+    p.tiles_n = plan.tiles_n;
+    p.num_tiles = plan.num_tiles;
+    p.tile_m = tile_m;
+    p.boxes = plan.boxes;
+    p.box_inner = plan.box_inner;
+    p.esize = esize_of(dtype);
+    p.stages = stages;
+    p.consumer_warps = plan.consumer_warps;
+    p.box_stride = static_cast<uint32_t>(plan.stage_bytes / plan.boxes);
+    p.stage_stride = static_cast<uint32_t>(plan.stage_bytes);
+    p.tx_bytes = static_cast<uint32_t>(plan.tx_bytes);
+    p.fault = o.fault;
+    p.wait_budget_ns = o.wait_budget_ns ? o.wait_budget_ns : mbt::kDefaultWaitBudgetNs;
+    p.log = o.log;
+    p.log_cap = o.log_capacity;
+    return p;
+}
+
+mbt_opts opts_or_default(const mbt_opts *opts) {
+    mbt_opts o;
+    std::memset(&o, 0, sizeof o);
+    if (opts) o = *opts;
+    return o;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tile_plan(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, int dtype,
+              const mbt_opts *opts, int num_sms, int smem_optin, int fit_per_sm,
+              int with_workspace, mbt_plan *plan) {
+    const mbt_opts o = opts_or_default(opts);
+    int64_t ld_src = 0, ld_dst = 0;
+    // Shape checks only: pointers are not part of a plan.
+    static const char dummy[16] __attribute__((aligned(16))) = {0};
+    int rc = check_args(op, dummy, dummy, M, N, tile_m, tile_n, stages, dtype, o, &ld_src, &ld_dst);
+    if (rc != MBT_OK) return rc;
+    return plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, num_sms, smem_optin, fit_per_sm,
+                     with_workspace, plan);
+}
+
+int tile_copy_ex(const void *src, void *dst, int64_t M, int64_t N, int tile_m, int tile_n,
+                 int stages, int dtype, void *stream, const mbt_opts *opts) {
+    const mbt_opts o = opts_or_default(opts);
+    int64_t ld_src = 0, ld_dst = 0;
+    int rc = check_args(MBT_OP_COPY, src, dst, M, N, tile_m, tile_n, stages, dtype, o, &ld_src,
+                        &ld_dst);
+    if (rc != MBT_OK) return rc;
+    if (M == 0 || N == 0) return MBT_OK;
+    mbt_plan plan;
+    rc = plan_on_device(MBT_OP_COPY, M, N, tile_m, tile_n, stages, dtype, o, 0, &plan);
+    if (rc != MBT_OK) return rc;
+    alignas(64) CUtensorMap map;
+    rc = encode_map(&map, src, M, N, ld_src, dtype, tile_m);
+    if (rc != MBT_OK) return rc;
+    CopyArgs a{};
+    a.p = pipe_args(plan, M, N, tile_m, stages, dtype, o);
+    a.dst = static_cast<char *>(dst);
+    a.ld_dst_bytes = ld_dst * esize_of(dtype);
+    const cudaError_t e = mbt::launch_copy(map, a, plan.grid, plan.threads, plan.smem_bytes,
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
+}
+
+int tile_copy(const void *src, void *dst, int64_t M, int64_t N, int tile_m, int tile_n,
+              int stages, int dtype, void *stream) {
+    return tile_copy_ex(src, dst, M, N, tile_m, tile_n, stages, dtype, stream, nullptr);
+}
+
+int tile_rowsum_ex(const void *src, float *out, int64_t M, int64_t N, int tile_m, int tile_n,
+                   int stages, int dtype, void *stream, const mbt_opts *opts) {
+    const mbt_opts o = opts_or_default(opts);
+    int64_t ld_src = 0, ld_dst = 0;
+    int rc = check_args(MBT_OP_ROWSUM, src, out, M, N, tile_m, tile_n, stages, dtype, o, &ld_src,
+                        &ld_dst);
+    if (rc != MBT_OK) return rc;
+    if (M == 0) return MBT_OK;
+    if (N == 0) {
+        return mbt::launch_fill_zero(out, M, static_cast<cudaStream_t>(stream)) == cudaSuccess
+                   ? MBT_OK
+                   : MBT_ERR_CUDA;
+    }
+    mbt_plan plan;
+    rc = plan_on_device(MBT_OP_ROWSUM, M, N, tile_m, tile_n, stages, dtype, o,
+                        o.workspace != nullptr, &plan);
+    if (rc != MBT_OK) return rc;
+    if (plan.split && o.workspace_bytes < plan.workspace_bytes) return MBT_ERR_WORKSPACE;
+    if (plan.split && (reinterpret_cast<uintptr_t>(o.workspace) & 255u) != 0) return MBT_ERR_ALIGN;
+    alignas(64) CUtensorMap map;
+    rc = encode_map(&map, src, M, N, ld_src, dtype, tile_m);
+    if (rc != MBT_OK) return rc;
+    RowsumArgs a{};
+    a.p = pipe_args(plan, M, N, tile_m, stages, dtype, o);
+    a.out = out;
+    if (plan.split) {
+        char *ws = static_cast<char *>(o.workspace);
+        a.ticket = reinterpret_cast<int32_t *>(ws);
+        a.partial = reinterpret_cast<float *>(ws + round_up(plan.tiles_m * 4, 256));
+        a.gran = 1;
+        a.units = plan.num_tiles;
+    } else {
+        a.gran = plan.tiles_n;
+        a.units = plan.tiles_m;
+    }
+    a.kmax = plan.kmax;
+    const cudaError_t e = mbt::launch_rowsum(dtype, map, a, plan.grid, plan.threads,
+                                             plan.smem_bytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
+}
+
+int tile_rowsum(const void *src, float *out, int64_t M, int64_t N, int tile_m, int tile_n,
+                int stages, int dtype, void *stream) {
+    return tile_rowsum_ex(src, out, M, N, tile_m, tile_n, stages, dtype, stream, nullptr);
+}
+
+int tile_rowsum_workspace_bytes(int64_t M, int64_t N, int tile_m, int tile_n, int stages,
+                                int dtype, const mbt_opts *opts, size_t *bytes) {
+    if (bytes == nullptr) return MBT_ERR_ARG;
+    mbt_opts o = opts_or_default(opts);
+    o.workspace = nullptr;
+    o.workspace_bytes = 0;
+    int64_t ld_src = 0, ld_dst = 0;
+    static const char dummy[16] __attribute__((aligned(16))) = {0};
+    int rc = check_args(MBT_OP_ROWSUM, dummy, dummy, M, N, tile_m, tile_n, stages, dtype, o,
+                        &ld_src, &ld_dst);
+    if (rc != MBT_OK) return rc;
+    *bytes = 0;
+    if (M == 0 || N == 0) return MBT_OK;
+    mbt_plan plan;
+    rc = plan_on_device(MBT_OP_ROWSUM, M, N, tile_m, tile_n, stages, dtype, o, 1, &plan);
+    if (rc != MBT_OK) return rc;
+    *bytes = plan.workspace_bytes;
+    return MBT_OK;
+}
+
+int tile_status(void *stream, int32_t info[4]) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MBT_ERR_CUDA;
+    int32_t local[4];
+    if (mbt::read_and_clear_status(local) != cudaSuccess) return MBT_ERR_CUDA;
+    if (info)
+        for (int i = 0; i < 4; ++i) info[i] = local[i];
+    return local[0] == 0 ? MBT_OK : local[0];
+}
+
+const char *tile_strerror(int code) {
+    switch (code) {
+        case MBT_OK: return "success";
+        case MBT_ERR_ARG: return "invalid argument (pointer, size, shape, enum or option)";
+        case MBT_ERR_ALIGN: return "base pointer or row pitch not 16-byte aligned";
+        case MBT_ERR_UNSUPPORTED: return "tile shape, size or warp count not supported";
+        case MBT_ERR_SMEM: return "stages x tile exceed the shared memory of one CTA";
+        case MBT_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
+        case MBT_ERR_TIMEOUT: return "an mbarrier wait exceeded its time budget";
+        case MBT_ERR_DRIVER: return "tensor-map encoder unavailable or rejected the map";
+        case MBT_ERR_WORKSPACE: return "workspace smaller than required";
+        default: return "unknown status code";
+    }
+}
+
+int tile_device_info(int device, int *num_sms, int *smem_optin, double *hbm_gbs_theoretical) {
+    int sms = 0, optin = 0, mem_khz = 0, bus_bits = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+            cudaSuccess)
+        return MBT_ERR_CUDA;
+    // Memory clock and bus width may be unreported; then the figure is 0.
+    if (cudaDeviceGetAttribute(&mem_khz, cudaDevAttrMemoryClockRate, device) != cudaSuccess)
+        mem_khz = 0;
+    if (cudaDeviceGetAttribute(&bus_bits, cudaDevAttrGlobalMemoryBusWidth, device) != cudaSuccess)
+        bus_bits = 0;
+    cudaGetLastError();
+    if (num_sms) *num_sms = sms;
+    if (smem_optin) *smem_optin = optin;
+    if (hbm_gbs_theoretical)
+        *hbm_gbs_theoretical = 2.0 * mem_khz * 1e3 * (bus_bits / 8.0) / 1e9;
+    return MBT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,624 @@
+// Kernels of libmbtile: a warp-specialised, mbarrier-synchronised bulk-tensor
+// tile pipeline for sm_103a, with a copy consumer and a row-sum consumer.
+//
+// CTA layout: warp 0 is the producer (one elected lane issues every bulk
+// tensor copy); warps 1..W are consumers.  Shared memory holds S stages; a
+// stage is `boxes` box buffers of tile_m rows x 128 bytes, each aligned to
+// 1024 bytes so that the hardware's 128-byte swizzle (16-byte chunk c of row r
+// stored at chunk c ^ (r mod 8)) is relative to the buffer start.
+//
+// Per stage s there is a full barrier (expects 1 arrival + the tile's bytes)
+// and an empty barrier (expects one arrival per consumer warp).  The producer
+// waits on empty[s] with its cursor parity (starting at 1, because every
+// buffer is free at the start), registers the bytes with arrive.expect_tx and
+// issues the copies; consumers wait on full[s] with their parity (starting at
+// 0), read the stage, and one lane per warp arrives on empty[s] once the whole
+// warp has finished its shared-memory reads.  Sources: "cute(12)
+// async_pipeline" §1-§3, §6 and §7; "cute(11) Hopper TMA copy" §3 and §6;
+// "异步协作：mbarrier"; "CUDA features 10: Pipelines" §4.10.4-4.10.5.
+//
+// Every wait is bounded (time budget from the host).  A wait that runs out
+// records MBT_ERR_TIMEOUT in g_status, raises a CTA-local abort flag that makes
+// the CTA's other waits give up early, and the producer then waits (again
+// bounded) for the bulk copies it still has in flight before the CTA exits.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace mbt {
+
+__device__ int32_t g_status[4];
+
+namespace {
+
+constexpr int kVec = 8;  // 16-byte chunks a consumer thread holds per round
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count)
+                 : "memory");
+}
+
+// Make barrier initialisation visible to the copy engine before first use.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// One probe of the barrier: true once the phase with parity `parity` is over.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bulk tensor copy of one 2-D box at element coordinates (x = column, y = row)
+// into shared memory; completion is counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map,
+                                            int32_t x, int32_t y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void stg128(void *ptr, const uint4 &v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Byte offset of 16-byte chunk q (counted across all boxes of a tile row) of
+// tile row `row`, relative to the stage base.
+__device__ __forceinline__ uint32_t chunk_offset(int row, int q, uint32_t box_stride) {
+    return static_cast<uint32_t>(q >> 3) * box_stride +
+           static_cast<uint32_t>(row) * kBoxRowBytes +
+           (static_cast<uint32_t>((q & 7) ^ (row & 7)) << 4);
+}
+
+// ---------------------------------------------------------------------------
+// Bounded waits and the failure record
+// ---------------------------------------------------------------------------
+struct WaitCtl {
+    uint64_t budget_ns;
+    volatile int *abort;
+};
+
+__device__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl &w,
+                             bool heed_abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    // Each probe costs well over 8 ns, so this iteration cap is reached only
+    // if the timer itself stalls; it keeps the loop finite regardless.
+    const uint64_t max_iter = w.budget_ns / 8 + 4096;
+    for (uint64_t it = 0; it < max_iter; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 7) == 7) {
+            if (heed_abort && *w.abort) return false;
+            if (global_ns() - t0 > w.budget_ns) return false;
+        }
+    }
+    return false;
+}
+
+__device__ void report_timeout(int role, uint32_t stage, uint32_t parity) {
+    if (atomicCAS(&g_status[0], 0, static_cast<int32_t>(MBT_ERR_TIMEOUT)) == 0) {
+        g_status[1] = static_cast<int32_t>(blockIdx.x);
+        g_status[2] = static_cast<int32_t>(stage);
+        g_status[3] = role * 2 + static_cast<int32_t>(parity);
+    }
+}
+
+__device__ __forceinline__ void log_record(const PipeArgs &p, int role, int64_t k,
+                                           uint32_t stage, uint32_t parity,
+                                           int64_t tile) {
+    if (p.log != nullptr && blockIdx.x == 0 && k < p.log_cap) {
+        int32_t *r = p.log + 4 * (role * p.log_cap + k);
+        r[0] = static_cast<int32_t>(k);
+        r[1] = static_cast<int32_t>(stage);
+        r[2] = static_cast<int32_t>(parity);
+        r[3] = static_cast<int32_t>(tile);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Shared pipeline skeleton
+// ---------------------------------------------------------------------------
+struct Smem {
+    uint32_t base;    // 1024-aligned start of stage 0
+    uint32_t full0;   // full barrier of stage 0 (stage s at + 8 s)
+    uint32_t empty0;  // empty barrier of stage 0
+};
+
+// Producer: one elected lane.  Loads `count` tiles, tile j being
+// first + j * step in row-major tile order, then drains (producer tail).
+__device__ void produce(const CUtensorMap *map, const PipeArgs &p, const Smem &sm,
+                        const WaitCtl &w, int64_t first, int64_t step, int64_t count) {
+    uint32_t stage = 0;
+    uint32_t phase = (p.fault == 1) ? 0u : 1u;  // free buffers: start at phase 1
+    int64_t issued = 0;
+    bool ok = true;
+    for (int64_t j = 0; j < count; ++j) {
+        const uint32_t empty_bar = sm.empty0 + 8u * stage;
+        if (!wait_bounded(empty_bar, phase, w, true)) {
+            report_timeout(0, stage, phase);
+            *w.abort = 1;
+            ok = false;
+            break;
+        }
+        const int64_t tile = first + j * step;
+        const int64_t tm = tile / p.tiles_n;
+        const int64_t tn = tile - tm * p.tiles_n;
+        const int32_t y = static_cast<int32_t>(tm * p.tile_m);
+        const int32_t x0 = static_cast<int32_t>(tn * p.boxes * p.box_inner);
+        const uint32_t full_bar = sm.full0 + 8u * stage;
+        const uint32_t dst = sm.base + stage * p.stage_stride;
+        mbar_arrive_expect_tx(full_bar, p.tx_bytes);
+        for (int b = 0; b < p.boxes; ++b)
+            tma_load_2d(dst + b * p.box_stride, map, x0 + b * p.box_inner, y, full_bar);
+        log_record(p, 0, j, stage, phase, tile);
+        ++issued;
+        if (++stage == static_cast<uint32_t>(p.stages)) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+    if (ok) {
+        // Tail: wait until the consumers have released every stage once more,
+        // so the CTA never exits with a stage still being read or filled.
+        for (int s = 0; s < p.stages; ++s) {
+            if (!wait_bounded(sm.empty0 + 8u * stage, phase, w, true)) {
+                report_timeout(0, stage, phase);
+                *w.abort = 1;
+                ok = false;
+                break;
+            }
+            if (++stage == static_cast<uint32_t>(p.stages)) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        // Abort: wait (bounded) for the copies this CTA may still have in
+        // flight -- the last min(issued, S) tiles -- before leaving.
+        const int64_t from = issued > p.stages ? issued - p.stages : 0;
+        for (int64_t t = from; t < issued; ++t) {
+            const uint32_t s = static_cast<uint32_t>(t % p.stages);
+            const uint32_t par = static_cast<uint32_t>((t / p.stages) & 1);
+            wait_bounded(sm.full0 + 8u * s, par, w, false);
+        }
+    }
+}
+
+__device__ __forceinline__ void init_pipeline(const PipeArgs &p, Smem &sm,
+                                              uint64_t *bars, volatile int *abort_flag,
+                                              uint64_t *extra_bar, uint32_t extra_count,
+                                              unsigned char *dyn) {
+    sm.base = (smem_u32(dyn) + (kSwizzleAtomBytes - 1)) & ~uint32_t(kSwizzleAtomBytes - 1);
+    sm.full0 = smem_u32(&bars[0]);
+    sm.empty0 = smem_u32(&bars[kMaxStages]);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(sm.full0 + 8u * s, 1);
+            mbar_init(sm.empty0 + 8u * s, static_cast<uint32_t>(p.consumer_warps));
+        }
+        if (extra_bar != nullptr) mbar_init(smem_u32(extra_bar), extra_count);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Copy
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void store_tail(char *d, const uint4 &v, int nbytes, int esize) {
+    // A 16-byte chunk that straddles column N: store only its in-bounds elements.
+    auto word = [&v](int k) { return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w; };
+    if (esize == 4) {
+        for (int k = 0; k < nbytes / 4; ++k) reinterpret_cast<uint32_t *>(d)[k] = word(k);
+    } else {
+        for (int k = 0; k < nbytes / 2; ++k)
+            reinterpret_cast<uint16_t *>(d)[k] =
+                static_cast<uint16_t>(word(k >> 1) >> ((k & 1) * 16));
+    }
+}
+
+__device__ void consume_copy(const CopyArgs &a, const Smem &sm, const WaitCtl &w,
+                             int64_t first, int64_t step, int64_t count) {
+    const PipeArgs &p = a.p;
+    const int ctid = static_cast<int>(threadIdx.x) - 32;
+    const int lane = threadIdx.x & 31;
+    const int nthr = p.consumer_warps * 32;
+    const int cpr = p.boxes * 8;                    // 16-byte chunks per tile row
+    const int cpr_log2 = __ffs(cpr) - 1;
+    const int items = p.tile_m * cpr;
+    const int rounds = (items + nthr * kVec - 1) / (nthr * kVec);
+    const int vec_elems = 16 / p.esize;
+    uint32_t stage = 0, phase = 0;
+    for (int64_t j = 0; j < count; ++j) {
+        const uint32_t full_bar = sm.full0 + 8u * stage;
+        bool ok = wait_bounded(full_bar, phase, w, true);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            if (lane == 0) {
+                report_timeout(1, stage, phase);
+                *w.abort = 1;
+            }
+            break;
+        }
+        const int64_t tile = first + j * step;
+        if (threadIdx.x == 32) log_record(p, 1, j, stage, phase, tile);
+        const int64_t tm = tile / p.tiles_n;
+        const int64_t row0 = tm * p.tile_m;
+        const int64_t col0 = (tile - tm * p.tiles_n) * p.boxes * p.box_inner;
+        const uint32_t sbase = sm.base + stage * p.stage_stride;
+        for (int r = 0; r < rounds; ++r) {
+            uint4 v[kVec];
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                const int i = ctid + (r * kVec + u) * nthr;
+                if (i < items) v[u] = lds128(sbase + chunk_offset(i >> cpr_log2, i & (cpr - 1), p.box_stride));
+            }
+            if (r == rounds - 1) {
+                // Every lane's reads of this stage are done: release it.
+                __syncwarp();
+                if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+            }
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                const int i = ctid + (r * kVec + u) * nthr;
+                if (i >= items) continue;
+                const int64_t grow = row0 + (i >> cpr_log2);
+                const int64_t gcol = col0 + static_cast<int64_t>(i & (cpr - 1)) * vec_elems;
+                if (grow >= p.M || gcol >= p.N) continue;
+                char *d = a.dst + grow * a.ld_dst_bytes + gcol * p.esize;
+                if (gcol + vec_elems <= p.N)
+                    stg128(d, v[u]);
+                else
+                    store_tail(d, v[u], static_cast<int>(p.N - gcol) * p.esize, p.esize);
+            }
+        }
+        if (++stage == static_cast<uint32_t>(p.stages)) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kMaxThreads, 2)
+    mbt_copy_kernel(const __grid_constant__ CUtensorMap map, const CopyArgs a) {
+    extern __shared__ __align__(1024) unsigned char dyn_smem[];
+    __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
+    __shared__ int abort_flag;
+    Smem sm;
+    init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);
+    WaitCtl w{a.p.wait_budget_ns, &abort_flag};
+    // Tiles b, b + G, b + 2G, ... in row-major tile order.
+    const int64_t G = gridDim.x;
+    const int64_t first = blockIdx.x;
+    const int64_t count = first < a.p.num_tiles ? (a.p.num_tiles - first + G - 1) / G : 0;
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0) produce(&map, a.p, sm, w, first, G, count);
+        return;
+    }
+    consume_copy(a, sm, w, first, G, count);
+}
+
+// ---------------------------------------------------------------------------
+// Row sum
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ float chunk_sum(const uint4 &v) {
+    if constexpr (DT == MBT_F32) {
+        return (__uint_as_float(v.x) + __uint_as_float(v.y)) +
+               (__uint_as_float(v.z) + __uint_as_float(v.w));
+    } else if constexpr (DT == MBT_BF16) {
+        // bf16 -> fp32 is exact: the 16 bits are the top half of the fp32.
+        auto pair = [](uint32_t u) {
+            return __uint_as_float(u << 16) + __uint_as_float(u & 0xffff0000u);
+        };
+        return (pair(v.x) + pair(v.y)) + (pair(v.z) + pair(v.w));
+    } else {
+        auto pair = [](uint32_t u) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u));
+            return f.x + f.y;
+        };
+        return (pair(v.x) + pair(v.y)) + (pair(v.z) + pair(v.w));
+    }
+}
+
+// CTA that owns tile x when `units` units of `gran` tiles are split evenly
+// over G CTAs (CTA b owns units [b U / G, (b + 1) U / G)).
+__device__ __forceinline__ int64_t unit_owner(int64_t x, int64_t gran, int64_t units, int64_t G) {
+    return ((x / gran + 1) * G - 1) / units;
+}
+
+struct FlushCtl {
+    uint32_t bar;       // mbarrier counting consumer warps
+    uint32_t parity;    // next phase parity to wait for
+};
+
+// Bounded rendezvous of all consumer warps (replaces a named barrier so that a
+// consumer warp which gave up cannot leave the others blocked forever).
+__device__ bool consumers_sync(FlushCtl &f, const WaitCtl &w) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(f.bar);
+    bool ok = wait_bounded(f.bar, f.parity, w, true);
+    ok = __all_sync(0xffffffffu, ok);
+    f.parity ^= 1u;
+    if (!ok && (threadIdx.x & 31) == 0) {
+        report_timeout(1, kMaxStages, f.parity ^ 1u);
+        *w.abort = 1;
+    }
+    return ok;
+}
+
+// Finish one band segment: combine the threads of each row, then either write
+// the row sums (sole contributor) or deposit the CTA's partials and let the
+// last contributing CTA add the partials of all contributors in CTA order.
+__device__ bool flush_band(const RowsumArgs &a, int64_t band, float acc, bool active,
+                           int row, int sub, int tpr, float *red, int *last_flag,
+                           FlushCtl &f, const WaitCtl &w) {
+    const PipeArgs &p = a.p;
+    const int ctid = static_cast<int>(threadIdx.x) - 32;
+    red[ctid] = acc;
+    if (!consumers_sync(f, w)) return false;
+    const int64_t G = gridDim.x;
+    const int64_t x0 = band * p.tiles_n;
+    const int64_t b_first = unit_owner(x0, a.gran, a.units, G);
+    const int64_t b_last = unit_owner(x0 + p.tiles_n - 1, a.gran, a.units, G);
+    const int64_t K = b_last - b_first + 1;
+    const int64_t grow = band * p.tile_m + row;
+    float v = 0.f;
+    if (active && sub == 0) {
+        v = red[row];
+        for (int s = 1; s < tpr; ++s) v += red[row + s * p.tile_m];
+    }
+    if (K == 1) {
+        if (active && sub == 0 && grow < p.M) a.out[grow] = v;
+        return consumers_sync(f, w);   // red[] may be rewritten after this
+    }
+    float *slot = a.partial + (band * a.kmax + (blockIdx.x - b_first)) * p.tile_m;
+    if (active && sub == 0) {
+        slot[row] = v;
+        __threadfence();
+    }
+    if (!consumers_sync(f, w)) return false;
+    if (ctid == 0) {
+        const int old = atomicAdd(&a.ticket[band], 1);
+        *last_flag = (old == K - 1);
+    }
+    if (!consumers_sync(f, w)) return false;
+    if (*last_flag) {
+        __threadfence();
+        if (active && sub == 0) {
+            float *base = a.partial + band * a.kmax * p.tile_m + row;
+            float total = 0.f;
+            for (int64_t k = 0; k < K; ++k) {
+                total += __ldcg(base + k * p.tile_m);
+                base[k * p.tile_m] = 0.f;   // leave the workspace zero-filled
+            }
+            if (grow < p.M) a.out[grow] = total;
+        }
+        if (ctid == 0) a.ticket[band] = 0;
+    }
+    return true;
+}
+
+template <int DT>
+__device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCtl &w,
+                               int64_t first, int64_t count, float *red, int *last_flag,
+                               FlushCtl &f) {
+    const PipeArgs &p = a.p;
+    const int ctid = static_cast<int>(threadIdx.x) - 32;
+    const int lane = threadIdx.x & 31;
+    const int nthr = p.consumer_warps * 32;
+    const int tpr = nthr / p.tile_m;                 // threads per row (>= 1)
+    const bool active = ctid < p.tile_m * tpr;
+    const int row = active ? ctid % p.tile_m : 0;
+    const int sub = active ? ctid / p.tile_m : 0;
+    const int cpr = p.boxes * 8;
+    // This thread reads chunks q = sub, sub + tpr, ... of its row.
+    const int mine = active ? (cpr - sub + tpr - 1) / tpr : 0;
+    const int most = (cpr + tpr - 1) / tpr;
+    const int rounds = (most + kVec - 1) / kVec;
+    float acc = 0.f;
+    int64_t band = -1;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    for (int64_t j = 0; j < count; ++j) {
+        const int64_t tile = first + j;
+        const int64_t tb = tile / p.tiles_n;
+        if (tb != band) {
+            if (band >= 0 && !flush_band(a, band, acc, active, row, sub, tpr, red,
+                                         last_flag, f, w)) {
+                ok = false;
+                break;
+            }
+            band = tb;
+            acc = 0.f;
+        }
+        const uint32_t full_bar = sm.full0 + 8u * stage;
+        bool got = wait_bounded(full_bar, phase, w, true);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) {
+            if (lane == 0) {
+                report_timeout(1, stage, phase);
+                *w.abort = 1;
+            }
+            ok = false;
+            break;
+        }
+        if (threadIdx.x == 32) log_record(p, 1, j, stage, phase, tile);
+        const uint32_t rbase = sm.base + stage * p.stage_stride;
+        float tsum = 0.f;
+        for (int r = 0; r < rounds; ++r) {
+            uint4 v[kVec];
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                const int k = r * kVec + u;
+                if (k < mine) v[u] = lds128(rbase + chunk_offset(row, sub + k * tpr, p.box_stride));
+            }
+            if (r == rounds - 1) {
+                __syncwarp();
+                if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+            }
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                const int k = r * kVec + u;
+                if (k < mine) tsum += chunk_sum<DT>(v[u]);
+            }
+        }
+        acc += tsum;
+        if (++stage == static_cast<uint32_t>(p.stages)) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+    if (ok && band >= 0)
+        flush_band(a, band, acc, active, row, sub, tpr, red, last_flag, f, w);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads, 2)
+    mbt_rowsum_kernel(const __grid_constant__ CUtensorMap map, const RowsumArgs a) {
+    extern __shared__ __align__(1024) unsigned char dyn_smem[];
+    __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
+    __shared__ __align__(8) uint64_t flush_bar;
+    __shared__ float red[kMaxThreads];
+    __shared__ int abort_flag;
+    __shared__ int last_flag;
+    Smem sm;
+    init_pipeline(a.p, sm, bars, &abort_flag, &flush_bar,
+                  static_cast<uint32_t>(a.p.consumer_warps), dyn_smem);
+    WaitCtl w{a.p.wait_budget_ns, &abort_flag};
+    // Contiguous, evenly split range of scheduling units, in band-major order.
+    const int64_t G = gridDim.x;
+    const int64_t b = blockIdx.x;
+    const int64_t first = (b * a.units / G) * a.gran;
+    const int64_t last = ((b + 1) * a.units / G) * a.gran;
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0) produce(&map, a.p, sm, w, first, 1, last - first);
+        return;
+    }
+    FlushCtl f{smem_u32(&flush_bar), 0u};
+    consume_rowsum<DT>(a, sm, w, first, last - first, red, &last_flag, f);
+}
+
+__global__ void mbt_fill_zero_kernel(float *out, int64_t n) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        out[i] = 0.f;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Host-side launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_copy(const CUtensorMap &map, const CopyArgs &a, int grid, int threads,
+                        int smem, cudaStream_t stream) {
+    mbt_copy_kernel<<<grid, threads, smem, stream>>>(map, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rowsum(int dtype, const CUtensorMap &map, const RowsumArgs &a, int grid,
+                          int threads, int smem, cudaStream_t stream) {
+    switch (dtype) {
+        case MBT_F16: mbt_rowsum_kernel<MBT_F16><<<grid, threads, smem, stream>>>(map, a); break;
+        case MBT_BF16: mbt_rowsum_kernel<MBT_BF16><<<grid, threads, smem, stream>>>(map, a); break;
+        default: mbt_rowsum_kernel<MBT_F32><<<grid, threads, smem, stream>>>(map, a); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fill_zero(float *out, int64_t n, cudaStream_t stream) {
+    const int threads = 256;
+    const int64_t blocks64 = (n + threads - 1) / threads;
+    const int blocks = static_cast<int>(blocks64 < 1024 ? (blocks64 < 1 ? 1 : blocks64) : 1024);
+    mbt_fill_zero_kernel<<<blocks, threads, 0, stream>>>(out, n);
+    return cudaGetLastError();
+}
+
+cudaError_t set_kernel_smem_limit(int optin, int *usable) {
+    // Each kernel may use the opt-in limit minus its own static shared memory;
+    // the plan uses the smallest of these so that any kernel can launch it.
+    const void *fns[] = {reinterpret_cast<const void *>(mbt_copy_kernel),
+                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16>),
+                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16>),
+                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32>)};
+    int least = optin;
+    for (const void *fn : fns) {
+        cudaFuncAttributes attr{};
+        cudaError_t e = cudaFuncGetAttributes(&attr, fn);
+        if (e != cudaSuccess) return e;
+        const int dyn = optin - static_cast<int>(attr.sharedSizeBytes);
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+        if (e != cudaSuccess) return e;
+        if (dyn < least) least = dyn;
+    }
+    *usable = least;
+    return cudaSuccess;
+}
+
+cudaError_t kernel_fit_per_sm(int op, int dtype, int threads, int smem, int *fit) {
+    const void *fn = reinterpret_cast<const void *>(mbt_copy_kernel);
+    if (op == MBT_OP_ROWSUM) {
+        fn = dtype == MBT_F16    ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16>)
+             : dtype == MBT_BF16 ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16>)
+                                 : reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32>);
+    }
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(fit, fn, threads, smem);
+}
+
+cudaError_t read_and_clear_status(int32_t info[4]) {
+    int32_t host[4] = {0, 0, 0, 0};
+    cudaError_t e = cudaMemcpyFromSymbol(host, g_status, sizeof host);
+    if (e != cudaSuccess) return e;
+    const int32_t zero[4] = {0, 0, 0, 0};
+    e = cudaMemcpyToSymbol(g_status, zero, sizeof zero);
+    for (int i = 0; i < 4; ++i) info[i] = host[i];
+    return e;
+}
+
+}  // namespace mbt

@@ -61,31 +61,40 @@ def fill_bits(t: torch.Tensor, bits: int) -> torch.Tensor:
 
 
 def make_matrix(M: int, N: int, dtype: str, dist: str, seed: int,
-                ld: int | None = None, device: str = "cpu") -> torch.Tensor:
+                ld: int | None = None, device: str | None = None,
+                draw_on: str = "cpu") -> torch.Tensor:
     """Return a (M, ld) tensor whose first N columns hold the seeded values.
 
-    The logical matrix is ``t[:, :N]``; ``t.stride(0) == ld``.
+    The logical matrix is ``t[:, :N]``; ``t.stride(0) == ld``.  ``draw_on``
+    selects the generator: "cpu" (the bits every test uses) or a CUDA device
+    (same distribution, different bits, much faster for GiB-sized inputs).
+    The result lives on ``device`` (default: where it was drawn).
     """
     if dtype not in DTYPES:
         raise ValueError(f"unknown dtype {dtype!r}")
     ld = N if ld is None else ld
     if ld < N:
         raise ValueError("ld must be >= N")
-    g = torch.Generator(device="cpu")
+    where = torch.device(draw_on)
+    g = torch.Generator(device=where)
     g.manual_seed(seed)
-    if dist == "uniform":
-        vals = torch.rand(M, N, generator=g, dtype=torch.float32)
-        vals.mul_(2.0).sub_(1.0)
-    elif dist == "normal":
-        vals = torch.randn(M, N, generator=g, dtype=torch.float32)
-    else:
-        raise ValueError(f"unknown distribution {dist!r}")
-    out = torch.empty(M, ld, dtype=DTYPES[dtype])
+    out = torch.empty(M, ld, dtype=DTYPES[dtype], device=where)
     if ld > N:
         fill_bits(out[:, N:], PAD_BITS[dtype])
-    out[:, :N].copy_(vals)
-    del vals
-    if device != "cpu":
+    # draw in row blocks of at most 2^26 values to bound the float32 scratch
+    rows = max(1, (1 << 26) // max(N, 1))
+    for r0 in range(0, M, rows):
+        r1 = min(M, r0 + rows)
+        if dist == "uniform":
+            vals = torch.rand(r1 - r0, N, generator=g, dtype=torch.float32, device=where)
+            vals.mul_(2.0).sub_(1.0)
+        elif dist == "normal":
+            vals = torch.randn(r1 - r0, N, generator=g, dtype=torch.float32, device=where)
+        else:
+            raise ValueError(f"unknown distribution {dist!r}")
+        out[r0:r1, :N].copy_(vals)
+        del vals
+    if device is not None and torch.device(device) != where:
         out = out.to(device)
     return out
 

@@ -1,0 +1,171 @@
+"""C ABI checks that need no GPU: the library loads, exports every entry point
+declared in include/mbtile.h, rejects bad arguments on the host before any
+CUDA call, and plans launches as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import mbarrier_async_tile_gb300 as mbt
+from mbarrier_async_tile_gb300 import C, Opts, _build
+from conftest import ROOT, read_golden
+
+HEADER = os.path.join(ROOT, "include", "mbtile.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    _build.build()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tile_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert {"tile_copy", "tile_rowsum", "tile_copy_ex", "tile_rowsum_ex", "tile_status",
+            "tile_plan", "tile_strerror"} <= set(names)
+    lib = ctypes.CDLL(_build.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror_covers_codes():
+    for code in range(0, -9, -1):
+        s = mbt.tile_strerror(code)
+        assert s and "unknown" not in s
+    assert "unknown" in mbt.tile_strerror(-99)
+
+
+def _copy(src, dst, M, N, tm=128, tn=64, st=3, dt=0, opts=None):
+    return C.tile_copy_ex(src, dst, M, N, tm, tn, st, dt, None,
+                          ctypes.byref(opts) if opts is not None else None)
+
+
+A = 0x10000          # fake, 16-byte aligned "device" addresses: never dereferenced
+B = 0x20000
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, B, 8, 64), -1),                         # null src
+    ((A, 0, 8, 64), -1),                         # null dst
+    ((A, B, -1, 64), -1),                        # negative M
+    ((A + 8, B, 8, 64), -2),                     # misaligned src
+    ((A, B + 2, 8, 64), -2),                     # misaligned dst
+    ((A, B, 8, 63), -2),                         # dense fp16 row of 126 bytes
+])
+def test_copy_argument_errors(args, code):
+    assert _copy(*args) == code
+
+
+def test_copy_tile_and_stage_errors():
+    assert _copy(A, B, 8, 64, tm=0) == -1
+    assert _copy(A, B, 8, 64, tm=257) == -1
+    assert _copy(A, B, 8, 64, tn=32) == -3       # 64-byte box rows: unsupported
+    assert _copy(A, B, 8, 64, tn=96) == -3       # 192 bytes: not 1/2/4/8 boxes
+    assert _copy(A, B, 8, 64, st=0) == -1
+    assert _copy(A, B, 8, 64, st=9) == -1
+    assert _copy(A, B, 8, 64, dt=7) == -1
+
+
+def test_option_errors():
+    o = Opts()
+    o.reserved[3] = 1
+    assert _copy(A, B, 8, 64, opts=o) == -1
+    o = Opts(); o.consumer_warps = 9
+    assert _copy(A, B, 8, 64, opts=o) == -1
+    o = Opts(); o.fault = 3
+    assert _copy(A, B, 8, 64, opts=o) == -1
+    o = Opts(); o.store_mode = 1
+    assert _copy(A, B, 8, 64, opts=o) == -3
+    o = Opts(); o.ld_src = 60                    # pitch below N
+    assert _copy(A, B, 8, 64, opts=o) == -1
+    o = Opts(); o.ld_dst = 68                    # 136-byte pitch: not a 16-byte multiple
+    assert _copy(A, B, 8, 64, opts=o) == -2
+
+
+def test_empty_shapes_are_noops_without_device():
+    assert _copy(0, 0, 0, 64) == 0
+    assert _copy(0, 0, 5, 0) == 0
+    # a row sum of rows with no columns must still write M zeros: out required
+    assert C.tile_rowsum(A, None, 5, 0, 64, 256, 3, 1, None) == -1
+    assert C.tile_rowsum(0, None, 0, 0, 64, 256, 3, 1, None) == 0
+
+
+def _plan(op, M, N, tm, tn, st, dtype, sms=152, smem=232448, fit=1, ws=False, **opt):
+    return mbt.tile_plan(op, M, N, tm, tn, st, dtype, num_sms=sms, smem_optin=smem,
+                         fit_per_sm=fit, with_workspace=ws, **opt)
+
+
+def test_plan_single_tile_lesson_shape():
+    sizes = {r[0]: int(r[-1]) for r in read_golden("lesson_sizes.txt")}
+    p = _plan(mbt.OP_COPY, 256, 128, 128, 64, 1, torch.float16, fit=4)
+    assert p["tx_bytes"] == sizes["tx_bytes"]
+    assert p["box_inner"] == sizes["tma_box_inner"] and p["box_rows"] == sizes["tma_box_outer"]
+    assert p["grid"] == 4 and p["num_tiles"] == 4 and p["boxes"] == 1
+    # one 16 KiB stage plus 1 KiB of alignment slack for the swizzle atom
+    assert p["smem_bytes"] == 16384 + 1024
+
+
+def test_plan_pipeline_lesson_shape():
+    p = _plan(mbt.OP_COPY, 128, 512, 128, 64, 3, torch.float16, max_ctas=1, consumer_warps=3)
+    assert p["grid"] == 1 and p["threads"] == 128 and p["num_tiles"] == 8
+    assert p["smem_bytes"] == 3 * 16384 + 1024
+
+
+def test_plan_errors_and_limits():
+    with pytest.raises(mbt.MbtError) as e:
+        _plan(mbt.OP_COPY, 1024, 1024, 256, 64, 8, torch.float16, smem=200000)
+    assert e.value.code == -4
+    with pytest.raises(mbt.MbtError) as e:
+        _plan(mbt.OP_ROWSUM, 1024, 1024, 256, 64, 2, torch.float16, consumer_warps=4)
+    assert e.value.code == -3
+    p = _plan(mbt.OP_ROWSUM, 1024, 1024, 256, 64, 2, torch.float16)
+    assert p["consumer_warps"] == 8
+
+
+def test_plan_rowsum_multibox_tile():
+    p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 3, torch.bfloat16, fit=1)
+    assert p["boxes"] == 4 and p["tx_bytes"] == 32768 and p["stage_bytes"] == 32768
+    assert p["grid"] == 128 and p["split"] == 0      # whole bands, one CTA each
+
+
+def _ranges(G, units, gran):
+    return [((b * units // G) * gran, ((b + 1) * units // G) * gran) for b in range(G)]
+
+
+@pytest.mark.parametrize("M,N,tm,tn,dt,sms,fit", [
+    (8192, 65536, 64, 256, torch.bfloat16, 152, 1),
+    (8192, 65536, 64, 256, torch.bfloat16, 152, 2),
+    (12289, 8191, 128, 32, torch.float32, 152, 2),
+    (24577, 16383, 128, 64, torch.float16, 152, 3),
+    (1000, 300, 16, 64, torch.float16, 7, 1),
+    (64, 64, 64, 64, torch.float16, 152, 4),
+])
+def test_plan_rowsum_split_covers_every_tile_once(M, N, tm, tn, dt, sms, fit):
+    es = torch.empty(0, dtype=dt).element_size()
+    ld = -(-N * es // 16) * 16 // es                    # pitched rows
+    p = _plan(mbt.OP_ROWSUM, M, N, tm, tn, 3, dt, sms=sms, fit=fit, ws=True, ld_src=ld)
+    tiles_n, T = p["tiles_n"], p["num_tiles"]
+    if not p["split"]:
+        assert p["workspace_bytes"] == 0
+        return
+    G = p["grid"]
+    assert G == min(T, sms * fit)
+    rng = _ranges(G, T, 1)
+    assert rng[0][0] == 0 and rng[-1][1] == T
+    assert all(a[1] == b[0] for a, b in zip(rng, rng[1:]))
+    # brute-force contributors per band
+    contrib = {}
+    for b, (lo, hi) in enumerate(rng):
+        for band in range(lo // tiles_n, (hi - 1) // tiles_n + 1) if hi > lo else []:
+            contrib.setdefault(band, []).append(b)
+    kmax = max(len(v) for v in contrib.values())
+    assert p["kmax"] == kmax
+    bands = p["tiles_m"]
+    assert p["workspace_bytes"] == ((bands * 4 + 255) // 256) * 256 + bands * kmax * tm * 4

@@ -1,0 +1,117 @@
+"""GPU parity of tile_rowsum against the binary64 CPU oracle, through the C
+ABI: fp32 sums within 1e-5 x max(|sum|, sqrt(sum of squares)) per row, exact
+on exactly representable cases, run-to-run bit-identical."""
+import pytest
+import torch
+
+import mbarrier_async_tile_gb300 as mbt
+import oracle
+import synthetic
+from helpers import ROWSUM_RTOL, rowsum_errors
+from oracle.pipeline_state import sequence
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def setup():
+    mbt._build.build()
+    oracle.build()
+    torch.cuda.set_device(0)
+
+
+def run_rowsum(x_h, N, *args, **kw):
+    x = x_h.cuda()
+    out = mbt.tile_rowsum(x[:, :N], None, *args, **kw)
+    code, info = mbt.tile_status()
+    assert code == 0, info
+    return out
+
+
+CASES = [
+    # dtype, dist, M, N, tile_m, tile_n, stages, split
+    ("bf16", "normal", 200, 1000, 64, 256, 3, True),
+    ("bf16", "normal", 200, 1000, 64, 256, 3, False),
+    ("f16", "uniform", 1, 1, 128, 64, 1, True),
+    ("f16", "uniform", 300, 4100, 128, 64, 4, True),
+    ("f32", "uniform", 257, 8191, 128, 32, 3, True),
+    ("f32", "normal", 1000, 33, 16, 64, 2, True),
+    ("f16", "normal", 65, 20000, 8, 512, 2, True),
+    ("bf16", "uniform", 4097, 300, 256, 64, 5, True),
+    ("f16", "uniform", 37, 70000, 32, 128, 6, False),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
+def test_rowsum_matches_oracle(case):
+    dtype, dist, M, N, tm, tn, st, split = case
+    ld = synthetic.pitched_ld(N, dtype) + 16 // synthetic.ESIZE[dtype]
+    x = synthetic.make_matrix(M, N, dtype, dist, seed=M + N, ld=ld)
+    out = run_rowsum(x, N, tm, tn, st, split=split)
+    worst, rel, _ = rowsum_errors(out, x[:, :N])
+    assert worst <= ROWSUM_RTOL, (worst, rel)
+
+
+def test_all_ones_exact_and_empty_rows():
+    x = torch.ones(300, 5000, dtype=torch.bfloat16)
+    out = run_rowsum(x, 5000, 64, 256, 3)
+    assert out.cpu().tolist() == [5000.0] * 300
+    z = mbt.tile_rowsum(torch.empty(7, 0, dtype=torch.float16, device="cuda"), None, 64, 64, 2)
+    assert mbt.tile_status()[0] == 0
+    assert z.cpu().tolist() == [0.0] * 7
+
+
+def test_repeat_calls_bit_identical_and_workspace_reuse():
+    x = synthetic.make_matrix(1000, 30000, "bf16", "normal", seed=4)
+    xd = x.cuda()
+    a = mbt.tile_rowsum(xd, None, 64, 256, 3)
+    b = mbt.tile_rowsum(xd, None, 64, 256, 3)
+    c = mbt.tile_rowsum(xd, None, 64, 256, 4)
+    assert mbt.tile_status()[0] == 0
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert rowsum_errors(c, x)[0] <= ROWSUM_RTOL
+
+
+def test_one_workspace_shared_by_different_shapes():
+    """A workspace is reused across calls whose ticket and partial regions
+    differ in size; every call must leave all of it zero-filled."""
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    shapes = [(300, 40000, 64, 256), (8192, 4096, 64, 256), (1000, 30000, 64, 256),
+              (5000, 9000, 128, 64)]
+    for M, N, tm, tn in shapes:
+        x = synthetic.make_matrix(M, N, "bf16", "normal", seed=M)
+        out = mbt.tile_rowsum(x.cuda(), None, tm, tn, 3, workspace=ws)
+        assert mbt.tile_status()[0] == 0
+        assert rowsum_errors(out, x)[0] <= ROWSUM_RTOL, (M, N)
+        assert int(ws.count_nonzero()) == 0
+
+
+def test_log_of_one_cta_pipeline():
+    x = synthetic.make_matrix(128, 512, "f16", "uniform", seed=12)
+    log = torch.zeros(2 * 16 * 4, dtype=torch.int32, device="cuda")
+    out = run_rowsum(x, 512, 128, 64, 3, consumer_warps=4, max_ctas=1, split=False, log=log)
+    assert rowsum_errors(out, x)[0] <= ROWSUM_RTOL
+    rec = log.view(2, 16, 4).cpu()
+    assert [(s, p) for _, s, p, _ in rec[0, :8].tolist()] == sequence(3, 1, 8)
+    assert [(s, p) for _, s, p, _ in rec[1, :8].tolist()] == sequence(3, 0, 8)
+
+
+FULL = [
+    # pipelined row reduction: bf16 8192 x 65536, normal(0,1), 64 x 256 tiles
+    ("bf16", "normal", 8192, 65536, 64, 256, (2, 3, 4), 1004),
+    # ragged fp32 12289 x 8191 and fp16 24577 x 16383, pitched rows
+    ("f32", "uniform", 12289, 8191, 128, 32, (3,), 1005),
+    ("f16", "uniform", 24577, 16383, 128, 64, (3,), 1006),
+]
+
+
+@pytest.mark.parametrize("case", FULL, ids=lambda c: f"{c[0]}-{c[2]}x{c[3]}")
+def test_full_size_configs(case):
+    dtype, dist, M, N, tm, tn, stage_list, seed = case
+    x = synthetic.make_matrix(M, N, dtype, dist, seed, ld=synthetic.pitched_ld(N, dtype))
+    xd = x.cuda()
+    for st in stage_list:
+        out = mbt.tile_rowsum(xd[:, :N], None, tm, tn, st)
+        assert mbt.tile_status()[0] == 0
+        worst, rel, _ = rowsum_errors(out, x[:, :N])
+        assert worst <= ROWSUM_RTOL, (st, worst, rel)
