@@ -175,6 +175,42 @@ int tile_rowsum_workspace_bytes(int64_t M, int64_t N, int tile_m, int tile_n,
                                 size_t *bytes);
 
 /*
+ * tile_rowsum_noalloc -- tile_rowsum_ex for callers that cannot allocate
+ * device memory.
+ *
+ * Some callers may not call cudaMalloc: code whose device memory is all owned
+ * by another allocator (a framework's pool, an embedding host), where a new
+ * allocation would fail or fragment it, and latency-critical paths that must
+ * not allocate or free because cudaMalloc / cudaFree can synchronise the
+ * device.  This entry point computes exactly what tile_rowsum_ex computes but
+ * allocates nothing: the band-split workspace is a static device array inside
+ * the library, MBT_NOALLOC_SCRATCH_BYTES (1 MiB) per device that loads the
+ * library, held until the process exits.  The caller still passes src and
+ * out.  opts->workspace and opts->workspace_bytes must be 0 (MBT_ERR_ARG
+ * otherwise).
+ *
+ * Errors: a shape whose plan needs more workspace than the array holds is
+ * rejected with MBT_ERR_WORKSPACE before anything is launched (shapes that
+ * need no workspace are always accepted).  Otherwise as tile_rowsum_ex.
+ *
+ * Set-up: the first call on a device looks up the array's device address
+ * (with that device current) and keeps it; make that first call before any
+ * stream capture begins.  Every call clears the part of the array it uses
+ * (an asynchronous memset on `stream`) before launching.
+ *
+ * Sharing: every call on a device uses the same array, so calls whose work
+ * overlaps on the GPU (different streams, or different host threads) race
+ * with each other and may return wrong sums; serialise them, e.g. on one
+ * stream.
+ *
+ * The pages have no counterpart of this entry point.
+ */
+#define MBT_NOALLOC_SCRATCH_BYTES (1u << 20)
+int tile_rowsum_noalloc(const void *src, float *out, int64_t M, int64_t N,
+                        int tile_m, int tile_n, int stages, int dtype,
+                        void *stream, const mbt_opts *opts);
+
+/*
  * tile_plan -- the launch plan for op (MBT_OP_COPY or MBT_OP_ROWSUM), from
  * the device figures given as arguments; makes no CUDA call.
  *   num_sms        SMs of the device (> 0).

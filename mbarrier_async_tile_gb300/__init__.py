@@ -21,7 +21,7 @@ from . import _build
 __all__ = [
     "MbtError", "C", "library_path", "tile_copy", "tile_rowsum", "tile_status",
     "tile_plan", "tile_device_info", "tile_strerror", "tile_rowsum_workspace_bytes",
-    "Opts", "Plan", "DTYPE_CODE", "OP_COPY", "OP_ROWSUM",
+    "Opts", "Plan", "DTYPE_CODE", "OP_COPY", "OP_ROWSUM", "tile_rowsum_noalloc",
 ]
 
 MBT_OK = 0
@@ -289,3 +289,25 @@ def tile_device_info(device: int | None = None) -> dict:
     rc = _load().tile_device_info(dev, ctypes.byref(sms), ctypes.byref(smem), ctypes.byref(gbs))
     _check(rc, "tile_device_info")
     return {"num_sms": sms.value, "smem_optin": smem.value, "hbm_gbs_theoretical": gbs.value}
+
+
+def tile_rowsum_noalloc(src: torch.Tensor, out: torch.Tensor, tile_m: int = 64,
+                        tile_n: int = 256, stages: int = 4, *, stream=None,
+                        **opt) -> torch.Tensor:
+    """Row sums through ``tile_rowsum_noalloc``: for callers that cannot
+    allocate device memory, the library uses its own static scratch array
+    instead of a workspace (see include/mbtile.h).  ``out`` must be given."""
+    lib = _load()
+    fn = lib.tile_rowsum_noalloc
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                   ctypes.POINTER(Opts)]
+    fn.restype = ctypes.c_int
+    M, N, ld_s = _matrix(src, "src")
+    if out.dtype != torch.float32 or out.numel() != M or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor of M elements")
+    o = _opts(ld_src=ld_s, **opt)
+    rc = fn(src.data_ptr(), out.data_ptr(), M, N, tile_m, tile_n, stages,
+            DTYPE_CODE[src.dtype], _stream_handle(stream), ctypes.byref(o))
+    _check(rc, "tile_rowsum_noalloc")
+    return out
