@@ -39,7 +39,10 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture
 # of each kernel on the full-size workload, keyed by the SHA-256 of the kernel
 # source it was taken on; reported only while the source is unchanged.
-NCU_TRAFFIC: dict = {}
+NCU_TRAFFIC: dict = {
+    "copy": {"src_sha": "7403ea850626a692", "bytes_per_launch": 536966912 + 485191936},
+    "rowsum": {"src_sha": "7403ea850626a692", "bytes_per_launch": 1073857024 + 3035136},
+}
 
 
 def copy_bytes(c=COPY):
@@ -215,7 +218,8 @@ def bench_gpu(args, rank, world):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        mbt.tile_copy(x3, d3, COPY["tile_m"], COPY["tile_n"], args.copy_stages, stream=stream)
+        mbt.tile_copy(x3, d3, COPY["tile_m"], COPY["tile_n"], args.copy_stages,
+                      store_mode=args.store_mode, stream=stream)
         if ev is not None:
             ev[1].record(stream)
         mbt.tile_rowsum(x4, o4, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
@@ -288,6 +292,7 @@ def bench_gpu(args, rank, world):
         "config": {"workload": ("tile_copy fp16 16384x16384 tile 128x64 + tile_rowsum "
                                 "bf16 8192x65536 tile 64x256"),
                    "copy_stages": args.copy_stages, "rowsum_stages": args.rowsum_stages,
+                   "copy_store_mode": args.store_mode,
                    "l2": "inputs (512 MiB, 1 GiB) larger than L2; no flush",
                    "parallelism": f"independent replica per GPU x{world}"},
         "frac_of_peak": round(value / world / peak, 4),
@@ -319,7 +324,8 @@ def bench_e2e(args, mbt, x3, x4, ws, stream, world):
 
     def step():
         g3.copy_(h3, non_blocking=True)
-        mbt.tile_copy(g3, g3o, COPY["tile_m"], COPY["tile_n"], args.copy_stages, stream=stream)
+        mbt.tile_copy(g3, g3o, COPY["tile_m"], COPY["tile_n"], args.copy_stages,
+                      store_mode=args.store_mode, stream=stream)
         r3.copy_(g3o, non_blocking=True)
         g4.copy_(h4, non_blocking=True)
         mbt.tile_rowsum(g4, g4o, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
@@ -340,6 +346,47 @@ def bench_e2e(args, mbt, x3, x4, ws, stream, world):
     return {"value": round(value, 1), "unit": "GB/s", "steps": steps,
             "h2d_bytes_per_step": h3.numel() * h3.element_size() + h4.numel() * h4.element_size(),
             "d2h_bytes_per_step": r3.numel() * r3.element_size() + r4.numel() * r4.element_size()}
+
+
+def bench_only(args):
+    """Run one kernel ``args.steps`` times on the first ``args.rows`` rows of
+    its workload (for profiling a smaller case under ncu), and print its GB/s."""
+    import mbarrier_async_tile_gb300 as mbt
+    import synthetic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    c = COPY if args.only == "copy" else ROWSUM
+    rows = min(args.rows or c["M"], c["M"])
+    x = synthetic.make_matrix(rows, c["N"], c["dtype"], c["dist"], c["seed"], draw_on=str(dev))
+    if args.only == "copy":
+        y = torch.empty_like(x)
+        fn = lambda: mbt.tile_copy(x, y, c["tile_m"], c["tile_n"], args.copy_stages,  # noqa: E731
+                                   consumer_warps=args.consumer_warps,
+                                   ctas_per_sm=args.ctas_per_sm, store_mode=args.store_mode)
+        nbytes = 2 * x.numel() * x.element_size()
+    else:
+        y = torch.empty(rows, dtype=torch.float32, device=dev)
+        ws = torch.zeros(1 << 22, dtype=torch.uint8, device=dev)
+        fn = lambda: mbt.tile_rowsum(x, y, c["tile_m"], c["tile_n"], args.rowsum_stages,  # noqa: E731
+                                     consumer_warps=args.consumer_warps,
+                                     ctas_per_sm=args.ctas_per_sm, workspace=ws)
+        nbytes = x.numel() * x.element_size() + 4 * rows
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    code, info = mbt.tile_status()
+    if code != 0:
+        raise RuntimeError(f"pipeline status {code} {info}")
+    ms = s.elapsed_time(e) / args.steps
+    print(json.dumps({"only": args.only, "rows": rows, "ms": round(ms, 4),
+                      "gbs": round(nbytes / ms / 1e6, 1)}), flush=True)
 
 
 def bench_sweep(args):
@@ -370,8 +417,10 @@ def bench_sweep(args):
             for cps in args.sweep_ctas:
                 try:
                     ms = timeit(lambda: mbt.tile_copy(x3, d3, COPY["tile_m"], COPY["tile_n"], st,
-                                                      consumer_warps=w, ctas_per_sm=cps))
-                    print(json.dumps({"sweep": "copy", "stages": st, "consumer_warps": w,
+                                                      consumer_warps=w, ctas_per_sm=cps,
+                                                      store_mode=args.store_mode))
+                    print(json.dumps({"sweep": "copy", "store_mode": args.store_mode,
+                                      "stages": st, "consumer_warps": w,
                                       "ctas_per_sm": cps, "ms": round(ms, 4),
                                       "gbs": round(copy_bytes() / ms / 1e6, 1)}), flush=True)
                 except mbt.MbtError as exc:
@@ -456,15 +505,20 @@ def reduce_max(x: float, world: int) -> float:
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mbtile", "reference"], default="mbtile")
-    ap.add_argument("--copy-stages", type=int, default=4)
-    ap.add_argument("--rowsum-stages", type=int, default=3)
+    ap.add_argument("--copy-stages", type=int, default=3)
+    ap.add_argument("--rowsum-stages", type=int, default=2)
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--only", choices=["copy", "rowsum"])
+    ap.add_argument("--store-mode", type=int, default=0, choices=[0, 1])
+    ap.add_argument("--rows", type=int, default=0)
+    ap.add_argument("--consumer-warps", type=int, default=0)
+    ap.add_argument("--ctas-per-sm", type=int, default=0)
     ap.add_argument("--sweep-stages", type=int, nargs="*", default=[1, 2, 3, 4, 6])
     ap.add_argument("--sweep-warps", type=int, nargs="*", default=[3, 4, 7])
     ap.add_argument("--sweep-ctas", type=int, nargs="*", default=[1, 2, 0])
@@ -480,6 +534,9 @@ def main(argv=None):
         return 0
     if args.sweep:
         bench_sweep(args)
+        return 0
+    if args.only:
+        bench_only(args)
         return 0
     if world > 1:
         torch.distributed.init_process_group(

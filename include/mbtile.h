@@ -83,11 +83,20 @@ typedef struct mbt_opts {
     int64_t ld_src;          /* row pitch of src in elements; 0 => N */
     int64_t ld_dst;          /* row pitch of dst in elements (copy); 0 => N */
     int32_t max_ctas;        /* upper bound on the grid; 0 => no bound */
-    int32_t ctas_per_sm;     /* CTAs per SM of the persistent grid;
-                                0 => as many as fit */
-    int32_t consumer_warps;  /* consumer warps per CTA, 1..8; 0 => 4.  The
-                                CTA has one more warp, the producer. */
-    int32_t store_mode;      /* reserved; must be 0 */
+    int32_t ctas_per_sm;     /* CTAs per SM of the persistent grid (capped
+                                at what fits); 0 => 2 */
+    int32_t consumer_warps;  /* consumer warps per CTA, 1..8; 0 => 4 for
+                                tile_copy, 8 for tile_rowsum.  The CTA has one
+                                more warp, the producer. */
+    int32_t store_mode;      /* tile_copy only.  0: the consumer warps store
+                                each tile with 16-byte st.global (default);
+                                1: one consumer thread writes each landed
+                                stage back with bulk tensor stores (same
+                                swizzled box layout, out-of-bounds elements
+                                clipped by the copy engine); the CTA then has
+                                one consumer warp and consumer_warps is
+                                ignored.  Source of the store recipe: "cute(11)
+                                Hopper TMA copy" §6.3-6.4. */
     uint64_t wait_budget_ns; /* time bound of every mbarrier wait; 0 => 1 s */
     int32_t *log;            /* optional device buffer of int32 records, see
                                 below; NULL => no log */

@@ -41,6 +41,9 @@ struct CopyArgs {
     PipeArgs p;
     char *dst;
     int64_t ld_dst_bytes;
+    int32_t store_mode;        // 0: consumer warps store with st.global.v4;
+                               // 1: one consumer thread issues bulk tensor stores
+    int32_t pad_;
 };
 
 struct RowsumArgs {
@@ -55,8 +58,9 @@ struct RowsumArgs {
 };
 
 // Launchers (mbtile_kernels.cu).  They only enqueue work on `stream`.
-cudaError_t launch_copy(const CUtensorMap &map, const CopyArgs &a, int grid,
-                        int threads, int smem, cudaStream_t stream);
+cudaError_t launch_copy(const CUtensorMap &map, const CUtensorMap &dst_map,
+                        const CopyArgs &a, int grid, int threads, int smem,
+                        cudaStream_t stream);
 cudaError_t launch_rowsum(int dtype, const CUtensorMap &map,
                           const RowsumArgs &a, int grid, int threads, int smem,
                           cudaStream_t stream);

@@ -4,7 +4,9 @@
 
 #include <algorithm>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "internal.h"
 
@@ -14,7 +16,14 @@ using mbt::CopyArgs;
 using mbt::PipeArgs;
 using mbt::RowsumArgs;
 
-constexpr int kDefaultConsumerWarps = 4;
+constexpr int kDefaultConsumerWarps = 4;         // copy
+constexpr int kDefaultRowsumConsumerWarps = 8;   // 256 threads: an even split of any
+                                                 // power-of-two tile_m <= 256
+// Default CTAs per SM of the persistent grid (fewer if fewer fit).  Measured
+// on GB300 with 128 x 64 fp16 copy tiles and 64 x 256 bf16 row-sum tiles: two
+// CTAs per SM with 2-4 stages beat both one CTA (consumer-bound) and three or
+// more (lower DRAM efficiency).
+constexpr int kDefaultCtasPerSm = 2;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxCoord = 0x7fffffff;  // bulk-copy coordinates are int32
 
@@ -26,6 +35,9 @@ struct DeviceFigures {
 
 std::mutex g_mutex;
 DeviceFigures g_devices[kMaxDevices];
+// CTAs per SM from the occupancy calculator, keyed by
+// (device, op, dtype, threads, dynamic smem); the query is slow next to a launch.
+std::map<std::tuple<int, int, int, int, int>, int> g_fit_cache;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int esize_of(int dtype) {
@@ -58,7 +70,8 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
     if (o.consumer_warps < 0 || o.consumer_warps > mbt::kMaxConsumerWarps) return MBT_ERR_ARG;
     if (o.ctas_per_sm < 0 || o.max_ctas < 0 || o.log_capacity < 0) return MBT_ERR_ARG;
     if (o.fault < 0 || o.fault > 2) return MBT_ERR_ARG;
-    if (o.store_mode != 0) return MBT_ERR_UNSUPPORTED;
+    if (o.store_mode < 0 || o.store_mode > 1) return MBT_ERR_UNSUPPORTED;
+    if (o.store_mode != 0 && op != MBT_OP_COPY) return MBT_ERR_ARG;
     for (int r : o.reserved)
         if (r != 0) return MBT_ERR_ARG;
     if (o.log != nullptr && o.log_capacity == 0) return MBT_ERR_ARG;
@@ -103,9 +116,9 @@ int32_t most_contributors(int64_t tiles_n, int64_t num_tiles, int64_t G) {
 }
 
 int consumer_warps_for(int op, int tile_m, const mbt_opts &o) {
+    if (op == MBT_OP_COPY && o.store_mode == 1) return 1;   // one thread issues the stores
     if (o.consumer_warps) return o.consumer_warps;
-    if (op == MBT_OP_ROWSUM)
-        return std::max(kDefaultConsumerWarps, static_cast<int>(ceil_div(tile_m, 32)));
+    if (op == MBT_OP_ROWSUM) return kDefaultRowsumConsumerWarps;
     return kDefaultConsumerWarps;
 }
 
@@ -132,7 +145,7 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     plan->tiles_m = ceil_div(M, tile_m);
     plan->tiles_n = ceil_div(N, tile_n);
     plan->num_tiles = plan->tiles_m * plan->tiles_n;
-    int64_t per_sm = o.ctas_per_sm ? std::min(o.ctas_per_sm, fit_per_sm) : fit_per_sm;
+    int64_t per_sm = std::min(o.ctas_per_sm ? o.ctas_per_sm : kDefaultCtasPerSm, fit_per_sm);
     int64_t cap = per_sm * num_sms;
     if (o.max_ctas) cap = std::min<int64_t>(cap, o.max_ctas);
     if (plan->num_tiles == 0) return MBT_OK;
@@ -225,10 +238,24 @@ int plan_on_device(int op, int64_t M, int64_t N, int tile_m, int tile_n, int sta
     rc = plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, d.num_sms, d.smem_optin, 1,
                    with_workspace, plan);
     if (rc != MBT_OK) return rc;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MBT_ERR_CUDA;
+    const auto key = std::make_tuple(dev, op, op == MBT_OP_ROWSUM ? dtype : 0, plan->threads,
+                                     plan->smem_bytes);
     int fit = 0;
-    if (mbt::kernel_fit_per_sm(op, dtype, plan->threads, plan->smem_bytes, &fit) != cudaSuccess)
-        return MBT_ERR_CUDA;
-    if (fit < 1) return MBT_ERR_SMEM;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        auto it = g_fit_cache.find(key);
+        if (it != g_fit_cache.end()) fit = it->second;
+    }
+    if (fit == 0) {
+        if (mbt::kernel_fit_per_sm(op, dtype, plan->threads, plan->smem_bytes, &fit) !=
+            cudaSuccess)
+            return MBT_ERR_CUDA;
+        if (fit < 1) return MBT_ERR_SMEM;
+        std::lock_guard<std::mutex> lock(g_mutex);
+        g_fit_cache[key] = fit;
+    }
     return plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, d.num_sms, d.smem_optin, fit,
                      with_workspace, plan);
 }
@@ -294,12 +321,19 @@ int tile_copy_ex(const void *src, void *dst, int64_t M, int64_t N, int tile_m, i
     alignas(64) CUtensorMap map;
     rc = encode_map(&map, src, M, N, ld_src, dtype, tile_m);
     if (rc != MBT_OK) return rc;
+    alignas(64) CUtensorMap dst_map;
+    std::memset(&dst_map, 0, sizeof dst_map);
+    if (o.store_mode == 1) {
+        rc = encode_map(&dst_map, dst, M, N, ld_dst, dtype, tile_m);
+        if (rc != MBT_OK) return rc;
+    }
     CopyArgs a{};
     a.p = pipe_args(plan, M, N, tile_m, stages, dtype, o);
     a.dst = static_cast<char *>(dst);
     a.ld_dst_bytes = ld_dst * esize_of(dtype);
-    const cudaError_t e = mbt::launch_copy(map, a, plan.grid, plan.threads, plan.smem_bytes,
-                                           static_cast<cudaStream_t>(stream));
+    a.store_mode = o.store_mode;
+    const cudaError_t e = mbt::launch_copy(map, dst_map, a, plan.grid, plan.threads,
+                                           plan.smem_bytes, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
 }
 

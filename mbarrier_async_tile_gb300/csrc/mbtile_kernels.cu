@@ -91,6 +91,34 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Bulk tensor copy of one 2-D box from shared memory to global memory at
+// element coordinates (x, y); elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x,
+                                             int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most one committed bulk store group still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_allow1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -263,17 +291,54 @@ __device__ __forceinline__ void store_tail(char *d, const uint4 &v, int nbytes, 
     }
 }
 
+// Copy one landed stage to the destination with 16-byte LSU stores, using
+// `nthr` threads (ctid = 0 .. nthr-1, whole warps).  Every warp releases the
+// stage (one arrive on `release_bar` per warp, unless release_bar == 0) right
+// after its last shared-memory loads, before its global stores.
+__device__ __forceinline__ void copy_tile_lsu(const CopyArgs &a, uint32_t sbase, int64_t row0,
+                                              int64_t col0, int ctid, int nthr,
+                                              uint32_t release_bar) {
+    const PipeArgs &p = a.p;
+    const int lane = threadIdx.x & 31;
+    const int cpr = p.boxes * 8;                    // 16-byte chunks per tile row
+    const int cpr_log2 = __ffs(cpr) - 1;
+    const int items = p.tile_m * cpr;
+    const int rounds = (items + nthr * kVec - 1) / (nthr * kVec);
+    const int vec_elems = 16 / p.esize;
+    for (int r = 0; r < rounds; ++r) {
+        uint4 v[kVec];
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            const int i = ctid + (r * kVec + u) * nthr;
+            if (i < items) v[u] = lds128(sbase + chunk_offset(i >> cpr_log2, i & (cpr - 1), p.box_stride));
+        }
+        if (r == rounds - 1) {
+            // Every lane's reads of this stage are done: release it.
+            __syncwarp();
+            if (lane == 0 && release_bar != 0) mbar_arrive(release_bar);
+        }
+#pragma unroll
+        for (int u = 0; u < kVec; ++u) {
+            const int i = ctid + (r * kVec + u) * nthr;
+            if (i >= items) continue;
+            const int64_t grow = row0 + (i >> cpr_log2);
+            const int64_t gcol = col0 + static_cast<int64_t>(i & (cpr - 1)) * vec_elems;
+            if (grow >= p.M || gcol >= p.N) continue;
+            char *d = a.dst + grow * a.ld_dst_bytes + gcol * p.esize;
+            if (gcol + vec_elems <= p.N)
+                stg128(d, v[u]);
+            else
+                store_tail(d, v[u], static_cast<int>(p.N - gcol) * p.esize, p.esize);
+        }
+    }
+}
+
 __device__ void consume_copy(const CopyArgs &a, const Smem &sm, const WaitCtl &w,
                              int64_t first, int64_t step, int64_t count) {
     const PipeArgs &p = a.p;
     const int ctid = static_cast<int>(threadIdx.x) - 32;
     const int lane = threadIdx.x & 31;
     const int nthr = p.consumer_warps * 32;
-    const int cpr = p.boxes * 8;                    // 16-byte chunks per tile row
-    const int cpr_log2 = __ffs(cpr) - 1;
-    const int items = p.tile_m * cpr;
-    const int rounds = (items + nthr * kVec - 1) / (nthr * kVec);
-    const int vec_elems = 16 / p.esize;
     uint32_t stage = 0, phase = 0;
     for (int64_t j = 0; j < count; ++j) {
         const uint32_t full_bar = sm.full0 + 8u * stage;
@@ -291,33 +356,8 @@ __device__ void consume_copy(const CopyArgs &a, const Smem &sm, const WaitCtl &w
         const int64_t tm = tile / p.tiles_n;
         const int64_t row0 = tm * p.tile_m;
         const int64_t col0 = (tile - tm * p.tiles_n) * p.boxes * p.box_inner;
-        const uint32_t sbase = sm.base + stage * p.stage_stride;
-        for (int r = 0; r < rounds; ++r) {
-            uint4 v[kVec];
-#pragma unroll
-            for (int u = 0; u < kVec; ++u) {
-                const int i = ctid + (r * kVec + u) * nthr;
-                if (i < items) v[u] = lds128(sbase + chunk_offset(i >> cpr_log2, i & (cpr - 1), p.box_stride));
-            }
-            if (r == rounds - 1) {
-                // Every lane's reads of this stage are done: release it.
-                __syncwarp();
-                if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
-            }
-#pragma unroll
-            for (int u = 0; u < kVec; ++u) {
-                const int i = ctid + (r * kVec + u) * nthr;
-                if (i >= items) continue;
-                const int64_t grow = row0 + (i >> cpr_log2);
-                const int64_t gcol = col0 + static_cast<int64_t>(i & (cpr - 1)) * vec_elems;
-                if (grow >= p.M || gcol >= p.N) continue;
-                char *d = a.dst + grow * a.ld_dst_bytes + gcol * p.esize;
-                if (gcol + vec_elems <= p.N)
-                    stg128(d, v[u]);
-                else
-                    store_tail(d, v[u], static_cast<int>(p.N - gcol) * p.esize, p.esize);
-            }
-        }
+        copy_tile_lsu(a, sm.base + stage * p.stage_stride, row0, col0, ctid, nthr,
+                      p.fault != 2 ? sm.empty0 + 8u * stage : 0u);
         if (++stage == static_cast<uint32_t>(p.stages)) {
             stage = 0;
             phase ^= 1u;
@@ -325,8 +365,89 @@ __device__ void consume_copy(const CopyArgs &a, const Smem &sm, const WaitCtl &w
     }
 }
 
+// Copy consumer with bulk tensor stores (one consumer warp): lane 0 stores
+// each landed stage straight from shared memory (same swizzled box layout) to
+// the destination, and releases the stage once that store has finished
+// reading shared memory.  Loads and stores both run in the async proxy; the
+// proxy fence orders the lane's view of the completed phase before the
+// store's reads.  The copy engine clips a store's innermost dimension only at
+// 16-byte granularity, so a tile holding a partial 16-byte chunk at column N
+// is written by the warp with LSU stores instead.
+__device__ void consume_copy_bulk(const CUtensorMap *dst_map, const CopyArgs &a, const Smem &sm,
+                                  const WaitCtl &w, int64_t first, int64_t step, int64_t count) {
+    const PipeArgs &p = a.p;
+    const int lane = threadIdx.x & 31;
+    const int vec_elems = 16 / p.esize;
+    const int64_t n_whole = p.N - p.N % vec_elems;   // columns in whole 16-byte chunks
+    const int64_t tile_n = static_cast<int64_t>(p.boxes) * p.box_inner;
+    uint32_t stage = 0, phase = 0;
+    uint32_t prev_stage = 0;
+    bool pending = false;          // a committed store whose stage is not released yet
+    for (int64_t j = 0; j < count; ++j) {
+        bool ok = wait_bounded(sm.full0 + 8u * stage, phase, w, true);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            if (lane == 0) {
+                report_timeout(1, stage, phase);
+                *w.abort = 1;
+            }
+            break;
+        }
+        const int64_t tile = first + j * step;
+        if (lane == 0) log_record(p, 1, j, stage, phase, tile);
+        const int64_t tm = tile / p.tiles_n;
+        const int64_t row0 = tm * p.tile_m;
+        const int64_t col0 = (tile - tm * p.tiles_n) * tile_n;
+        const uint32_t sbase = sm.base + stage * p.stage_stride;
+        if (col0 + tile_n > n_whole && n_whole != p.N) {
+            if (pending) {
+                // Free the stage held by the last store first: the producer's
+                // next tile may need it, and no further store will release it.
+                if (lane == 0) {
+                    bulk_wait_read_all();
+                    if (p.fault != 2) mbar_arrive(sm.empty0 + 8u * prev_stage);
+                }
+                pending = false;
+            }
+            copy_tile_lsu(a, sbase, row0, col0, lane, 32,
+                          p.fault != 2 ? sm.empty0 + 8u * stage : 0u);
+        } else {
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                for (int b = 0; b < p.boxes; ++b)
+                    tma_store_2d(dst_map, sbase + b * p.box_stride,
+                                 static_cast<int32_t>(col0) + b * p.box_inner,
+                                 static_cast<int32_t>(row0));
+                bulk_commit_group();
+                if (p.stages == 1) {
+                    // A single stage cannot wait for the next tile: release it
+                    // as soon as this store has read it.
+                    bulk_wait_read_all();
+                    if (p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+                } else if (pending) {
+                    // The previous store has read its stage: release it.
+                    bulk_wait_read_allow1();
+                    if (p.fault != 2) mbar_arrive(sm.empty0 + 8u * prev_stage);
+                }
+            }
+            pending = p.stages > 1;
+            prev_stage = stage;
+        }
+        if (++stage == static_cast<uint32_t>(p.stages)) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+    if (lane == 0) {
+        bulk_wait_read_all();
+        if (pending && p.fault != 2 && !*w.abort) mbar_arrive(sm.empty0 + 8u * prev_stage);
+        bulk_wait_all();
+    }
+}
+
 __global__ void __launch_bounds__(kMaxThreads, 2)
-    mbt_copy_kernel(const __grid_constant__ CUtensorMap map, const CopyArgs a) {
+    mbt_copy_kernel(const __grid_constant__ CUtensorMap map,
+                    const __grid_constant__ CUtensorMap dst_map, const CopyArgs a) {
     extern __shared__ __align__(1024) unsigned char dyn_smem[];
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
     __shared__ int abort_flag;
@@ -339,6 +460,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     const int64_t count = first < a.p.num_tiles ? (a.p.num_tiles - first + G - 1) / G : 0;
     if (threadIdx.x < 32) {
         if (threadIdx.x == 0) produce(&map, a.p, sm, w, first, G, count);
+        return;
+    }
+    if (a.store_mode == 1) {
+        consume_copy_bulk(&dst_map, a, sm, w, first, G, count);   // one consumer warp
         return;
     }
     consume_copy(a, sm, w, first, G, count);
@@ -556,9 +681,9 @@ __global__ void mbt_fill_zero_kernel(float *out, int64_t n) {
 // ---------------------------------------------------------------------------
 // Host-side launchers
 // ---------------------------------------------------------------------------
-cudaError_t launch_copy(const CUtensorMap &map, const CopyArgs &a, int grid, int threads,
-                        int smem, cudaStream_t stream) {
-    mbt_copy_kernel<<<grid, threads, smem, stream>>>(map, a);
+cudaError_t launch_copy(const CUtensorMap &map, const CUtensorMap &dst_map, const CopyArgs &a,
+                        int grid, int threads, int smem, cudaStream_t stream) {
+    mbt_copy_kernel<<<grid, threads, smem, stream>>>(map, dst_map, a);
     return cudaGetLastError();
 }
 

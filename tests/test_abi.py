@@ -81,8 +81,10 @@ def test_option_errors():
     assert _copy(A, B, 8, 64, opts=o) == -1
     o = Opts(); o.fault = 3
     assert _copy(A, B, 8, 64, opts=o) == -1
-    o = Opts(); o.store_mode = 1
+    o = Opts(); o.store_mode = 2
     assert _copy(A, B, 8, 64, opts=o) == -3
+    o = Opts(); o.store_mode = 1                 # bulk stores: a copy-only option
+    assert C.tile_rowsum_ex(A, B, 8, 64, 128, 64, 3, 0, None, ctypes.byref(o)) == -1
     o = Opts(); o.ld_src = 60                    # pitch below N
     assert _copy(A, B, 8, 64, opts=o) == -1
     o = Opts(); o.ld_dst = 68                    # 136-byte pitch: not a 16-byte multiple
@@ -116,6 +118,12 @@ def test_plan_pipeline_lesson_shape():
     p = _plan(mbt.OP_COPY, 128, 512, 128, 64, 3, torch.float16, max_ctas=1, consumer_warps=3)
     assert p["grid"] == 1 and p["threads"] == 128 and p["num_tiles"] == 8
     assert p["smem_bytes"] == 3 * 16384 + 1024
+
+
+def test_plan_bulk_store_mode_uses_one_consumer_warp():
+    p = _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 4, torch.float16, store_mode=1,
+              consumer_warps=7)
+    assert p["consumer_warps"] == 1 and p["threads"] == 64
 
 
 def test_plan_errors_and_limits():
@@ -156,7 +164,7 @@ def test_plan_rowsum_split_covers_every_tile_once(M, N, tm, tn, dt, sms, fit):
         assert p["workspace_bytes"] == 0
         return
     G = p["grid"]
-    assert G == min(T, sms * fit)
+    assert G == min(T, sms * min(fit, 2))        # default: at most 2 CTAs per SM
     rng = _ranges(G, T, 1)
     assert rng[0][0] == 0 and rng[-1][1] == T
     assert all(a[1] == b[0] for a, b in zip(rng, rng[1:]))

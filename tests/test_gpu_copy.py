@@ -71,13 +71,55 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("store_mode", [0, 1])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
-def test_copy_matches_oracle(case):
+def test_copy_matches_oracle(case, store_mode):
     dtype, M, N, tm, tn, st, w = case
     es = synthetic.ESIZE[dtype]
     src, dst, want = copy_case(dtype, M, N, seed=M * 7 + N, src_pad=16 // es, dst_pad=32 // es)
-    got = run_copy(src, dst, N, tm, tn, st, consumer_warps=w)
+    got = run_copy(src, dst, N, tm, tn, st, consumer_warps=w, store_mode=store_mode)
     assert torch.equal(bits(got), bits(want))
+
+
+@pytest.mark.parametrize("store_mode", [0, 1])
+@pytest.mark.parametrize("dtype,M,N,tm,tn", [("f16", 200, 1000, 128, 64), ("f32", 77, 70, 64, 32),
+                                             ("bf16", 5, 3, 128, 64)])
+def test_nothing_written_outside_the_logical_region(dtype, M, N, tm, tn, store_mode):
+    """Destination views into a larger poisoned buffer: rows past M and
+    columns past N (up to the buffer's pitch) must keep their poison."""
+    es = synthetic.ESIZE[dtype]
+    src = synthetic.make_matrix(M, N, dtype, "uniform", seed=M + N,
+                                ld=synthetic.pitched_ld(N, dtype))
+    buf = torch.empty(M + 130, synthetic.pitched_ld(N, dtype) + 64 // es,
+                      dtype=synthetic.DTYPES[dtype])
+    synthetic.fill_bits(buf, synthetic.POISON_BITS[dtype])
+    want = buf.clone()
+    oracle.copy(src[:, :N], want[:M, :N])
+    d = buf.cuda()
+    mbt.tile_copy(src.cuda()[:, :N], d[:M, :N], tm, tn, 2, store_mode=store_mode)
+    assert mbt.tile_status()[0] == 0
+    assert torch.equal(bits(d.cpu()), bits(want))
+
+
+@pytest.mark.parametrize("stages", [1, 2, 3])
+def test_bulk_store_mode_many_tiles_per_cta(stages):
+    """Each CTA streams many tiles through its ring, including a single-stage
+    ring (whose stage must be released as soon as its store has read it)."""
+    src, dst, want = copy_case("f16", 1000, 700, seed=41, src_pad=8)
+    got = run_copy(src, dst, 700, 128, 64, stages, max_ctas=3, store_mode=1)
+    assert torch.equal(bits(got), bits(want))
+
+
+def test_bulk_store_mode_lesson_shapes_and_log():
+    src, dst, want = copy_case("f16", 256, 128, seed=1001)
+    assert torch.equal(bits(run_copy(src, dst, 128, 128, 64, 1, store_mode=1)), bits(want))
+    src, dst, want = copy_case("f16", 128, 512, seed=1002)
+    log = torch.zeros(2 * 16 * 4, dtype=torch.int32, device="cuda")
+    got = run_copy(src, dst, 512, 128, 64, 3, max_ctas=1, log=log, store_mode=1)
+    assert torch.equal(bits(got), bits(want))
+    rec = log.view(2, 16, 4).cpu()
+    assert [(s, p) for _, s, p, _ in rec[0, :8].tolist()] == sequence(3, 1, 8)
+    assert [(s, p) for _, s, p, _ in rec[1, :8].tolist()] == sequence(3, 0, 8)
 
 
 @pytest.mark.parametrize("max_ctas,ctas_per_sm", [(1, 0), (3, 0), (0, 1), (0, 2)])
@@ -139,9 +181,10 @@ def test_full_size_configs(case):
     src, dst, want = copy_case(dtype, M, N, seed=seed)
     s = src.cuda()
     wb = bits(want)
-    for st in stage_list:
+    runs = [(st, 0) for st in stage_list] + [(stage_list[-1], 1)]
+    for st, mode in runs:
         d = dst.cuda()
-        mbt.tile_copy(s[:, :N], d[:, :N], tm, tn, st)
+        mbt.tile_copy(s[:, :N], d[:, :N], tm, tn, st, store_mode=mode)
         assert mbt.tile_status()[0] == 0
-        assert torch.equal(bits(d.cpu()), wb), f"stages={st}"
+        assert torch.equal(bits(d.cpu()), wb), f"stages={st} store_mode={mode}"
         del d

@@ -22,12 +22,13 @@ def setup():
 
 
 @pytest.mark.parametrize("fault", [1, 2])
-@pytest.mark.parametrize("op", ["copy", "rowsum"])
+@pytest.mark.parametrize("op", ["copy", "copy_bulk", "rowsum"])
 def test_stalled_pipeline_reports_timeout(fault, op):
     src, dst, want = copy_case("f16", 512, 1024, seed=3)
     s, d = src.cuda(), dst.cuda()
-    if op == "copy":
-        mbt.tile_copy(s, d, 128, 64, 3, max_ctas=4, fault=fault, wait_budget_ns=BUDGET_NS)
+    if op.startswith("copy"):
+        mbt.tile_copy(s, d, 128, 64, 3, max_ctas=4, fault=fault, wait_budget_ns=BUDGET_NS,
+                      store_mode=1 if op == "copy_bulk" else 0)
     else:
         mbt.tile_rowsum(s, None, 128, 64, 3, max_ctas=4, fault=fault, wait_budget_ns=BUDGET_NS)
     code, info = mbt.tile_status()
