@@ -258,8 +258,7 @@ def bench_gpu(args, rank, world):
     ms_copy = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     ms_rowsum = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
     ms_max = reduce_max(ms_total, world)
-    step_bytes = copy_bytes() + rowsum_bytes()
-    value = world * step_bytes * args.steps / (ms_max / 1e3) / 1e9
+    value = aggregate_gbs(copy_bytes() + rowsum_bytes(), args.steps, world, ms_max)
 
     # end to end through the public API with host buffers
     e2e = bench_e2e(args, mbt, x3, x4, ws, stream, world)
@@ -342,7 +341,7 @@ def bench_e2e(args, mbt, x3, x4, ws, stream, world):
     e.record(stream)
     torch.cuda.synchronize()
     ms = reduce_max(s.elapsed_time(e), world)
-    value = world * (copy_bytes() + rowsum_bytes()) * steps / (ms / 1e3) / 1e9
+    value = aggregate_gbs(copy_bytes() + rowsum_bytes(), steps, world, ms)
     return {"value": round(value, 1), "unit": "GB/s", "steps": steps,
             "h2d_bytes_per_step": h3.numel() * h3.element_size() + h4.numel() * h4.element_size(),
             "d2h_bytes_per_step": r3.numel() * r3.element_size() + r4.numel() * r4.element_size()}
@@ -488,6 +487,12 @@ def bench_reference(args):
 
 
 # ---------------------------------------------------------------------------
+def aggregate_gbs(step_bytes: int, steps: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank processed `steps` steps of `step_bytes`
+    (independent replicas); the job took the slowest rank's time."""
+    return world * step_bytes * steps / (ms_max / 1e3) / 1e9
+
+
 def barrier(world):
     if world > 1:
         torch.distributed.barrier()
