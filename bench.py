@@ -388,6 +388,111 @@ def bench_only(args):
                       "gbs": round(nbytes / ms / 1e6, 1)}), flush=True)
 
 
+def bench_configs(args):
+    """One line per configuration of the task's table: latency for the two
+    lesson shapes, GB/s (algorithmic bytes / device time) for the streaming
+    and ragged ones, each the median of 5 rounds of `reps` back-to-back calls."""
+    import mbarrier_async_tile_gb300 as mbt
+    import synthetic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = measured_peak()
+    theo = mbt.tile_device_info()["hbm_gbs_theoretical"]
+
+    def med_ms(fn, reps):
+        vals = []
+        for _ in range(5):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            for _ in range(reps):
+                fn()
+            e.record()
+            torch.cuda.synchronize()
+            vals.append(s.elapsed_time(e) / reps)
+        code, info = mbt.tile_status()
+        if code != 0:
+            raise RuntimeError(f"pipeline status {code} {info}")
+        return statistics.median(vals)
+
+    def line(d):
+        if "gbs" in d:
+            d["frac_of_peak"] = round(d["gbs"] / peak, 4)
+            d["frac_of_theoretical"] = round(d["gbs"] / theo, 4) if theo else None
+        print(json.dumps(d), flush=True)
+
+    def graph_us(call, n=100):
+        """Device time per call: n calls captured in one CUDA graph, replayed."""
+        call(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(n):
+                    call(side)
+        torch.cuda.synchronize()
+        return med_ms(g.replay, 5) / n * 1e3
+
+    # 1: single-tile copy, fp16 256 x 128, 128 x 64 tiles, 1 stage, 4 CTAs
+    x = synthetic.make_matrix(256, 128, "f16", "uniform", 1001, draw_on=str(dev))
+    y = torch.empty_like(x)
+    ms = med_ms(lambda: mbt.tile_copy(x, y, 128, 64, 1), 200)
+    us = graph_us(lambda st: mbt.tile_copy(x, y, 128, 64, 1, stream=st))
+    line({"config": 1, "op": "copy", "shape": [256, 128], "tile": [128, 64], "stages": 1,
+          "us_per_call_host_bound": round(ms * 1e3, 2), "us_per_call_device": round(us, 2),
+          "bytes": 2 * x.numel() * 2})
+    # 2: 3-stage pipeline, fp16 128 x 512, 1 CTA, 1 producer + 3 consumer warps
+    x = synthetic.make_matrix(128, 512, "f16", "uniform", 1002, draw_on=str(dev))
+    y = torch.empty_like(x)
+    ms = med_ms(lambda: mbt.tile_copy(x, y, 128, 64, 3, consumer_warps=3, max_ctas=1), 200)
+    us = graph_us(lambda st: mbt.tile_copy(x, y, 128, 64, 3, consumer_warps=3, max_ctas=1,
+                                           stream=st))
+    line({"config": 2, "op": "copy", "shape": [128, 512], "tile": [128, 64], "stages": 3,
+          "us_per_call_host_bound": round(ms * 1e3, 2), "us_per_call_device": round(us, 2),
+          "bytes": 2 * x.numel() * 2})
+    # 3: streaming copy, stage sweep, both store paths
+    x = synthetic.make_matrix(16384, 16384, "f16", "uniform", 1003, draw_on=str(dev))
+    y = torch.empty_like(x)
+    for mode in (0, 1):
+        for st in (1, 2, 3, 4, 6):
+            ms = med_ms(lambda: mbt.tile_copy(x, y, 128, 64, st, store_mode=mode), 20)
+            line({"config": 3, "op": "copy", "store_mode": mode, "shape": [16384, 16384],
+                  "tile": [128, 64], "stages": st, "ms": round(ms, 4),
+                  "gbs": round(copy_bytes() / ms / 1e6, 1)})
+    del x, y
+    # 4: row sums, stage sweep
+    x = synthetic.make_matrix(8192, 65536, "bf16", "normal", 1004, draw_on=str(dev))
+    o = torch.empty(8192, dtype=torch.float32, device=dev)
+    ws = torch.zeros(1 << 22, dtype=torch.uint8, device=dev)
+    for st in (2, 3, 4):
+        ms = med_ms(lambda: mbt.tile_rowsum(x, o, 64, 256, st, workspace=ws), 20)
+        line({"config": 4, "op": "rowsum", "shape": [8192, 65536], "tile": [64, 256],
+              "stages": st, "ms": round(ms, 4), "gbs": round(rowsum_bytes() / ms / 1e6, 1)})
+    del x
+    # 5a / 5b: ragged, pitched rows, copy and row sum, 3 stages
+    for cfg, dt, M, N, tm, tn, seed in (("5a", "f32", 12289, 8191, 128, 32, 1005),
+                                        ("5b", "f16", 24577, 16383, 128, 64, 1006)):
+        ld = synthetic.pitched_ld(N, dt)
+        es = ESIZE[dt]
+        x = synthetic.make_matrix(M, N, dt, "uniform", seed, ld=ld, draw_on=str(dev))
+        y = torch.empty_like(x)
+        o = torch.empty(M, dtype=torch.float32, device=dev)
+        for mode in (0, 1):
+            ms = med_ms(lambda: mbt.tile_copy(x[:, :N], y[:, :N], tm, tn, 3, store_mode=mode), 20)
+            line({"config": cfg, "op": "copy", "store_mode": mode, "shape": [M, N], "ld": ld,
+                  "tile": [tm, tn], "stages": 3, "ms": round(ms, 4),
+                  "gbs": round(2 * M * N * es / ms / 1e6, 1)})
+        ms = med_ms(lambda: mbt.tile_rowsum(x[:, :N], o, tm, tn, 3, workspace=ws), 20)
+        line({"config": cfg, "op": "rowsum", "shape": [M, N], "ld": ld, "tile": [tm, tn],
+              "stages": 3, "ms": round(ms, 4), "gbs": round((M * N * es + 4 * M) / ms / 1e6, 1)})
+        del x, y
+    line({"peak_gbs": peak, "peak_source": peak_kind, "theoretical_gbs": round(theo, 1)})
+
+
 def bench_sweep(args):
     """One line per (op, stages, consumer warps, CTAs per SM) point."""
     import mbarrier_async_tile_gb300 as mbt
@@ -519,6 +624,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--all-configs", action="store_true")
     ap.add_argument("--only", choices=["copy", "rowsum"])
     ap.add_argument("--store-mode", type=int, default=0, choices=[0, 1])
     ap.add_argument("--rows", type=int, default=0)
@@ -542,6 +648,9 @@ def main(argv=None):
         return 0
     if args.only:
         bench_only(args)
+        return 0
+    if args.all_configs:
+        bench_configs(args)
         return 0
     if world > 1:
         torch.distributed.init_process_group(

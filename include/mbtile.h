@@ -84,10 +84,14 @@ typedef struct mbt_opts {
     int64_t ld_dst;          /* row pitch of dst in elements (copy); 0 => N */
     int32_t max_ctas;        /* upper bound on the grid; 0 => no bound */
     int32_t ctas_per_sm;     /* CTAs per SM of the persistent grid (capped
-                                at what fits); 0 => 2 */
+                                at what fits); 0 => at least 2, and enough
+                                that the stages on one SM hold ~64 KB (copy)
+                                or ~128 KB (row sum) */
     int32_t consumer_warps;  /* consumer warps per CTA, 1..8; 0 => 4 for
-                                tile_copy, 8 for tile_rowsum.  The CTA has one
-                                more warp, the producer. */
+                                tile_copy; for tile_rowsum 8, or 4 when the
+                                default grid puts 3+ CTAs on an SM and
+                                tile_m <= 128.  The CTA has one more warp,
+                                the producer. */
     int32_t store_mode;      /* tile_copy only.  0: the consumer warps store
                                 each tile with 16-byte st.global (default);
                                 1: one consumer thread writes each landed

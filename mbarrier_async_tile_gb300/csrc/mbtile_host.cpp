@@ -17,13 +17,14 @@ using mbt::PipeArgs;
 using mbt::RowsumArgs;
 
 constexpr int kDefaultConsumerWarps = 4;         // copy
-constexpr int kDefaultRowsumConsumerWarps = 8;   // 256 threads: an even split of any
-                                                 // power-of-two tile_m <= 256
-// Default CTAs per SM of the persistent grid (fewer if fewer fit).  Measured
-// on GB300 with 128 x 64 fp16 copy tiles and 64 x 256 bf16 row-sum tiles: two
-// CTAs per SM with 2-4 stages beat both one CTA (consumer-bound) and three or
-// more (lower DRAM efficiency).
-constexpr int kDefaultCtasPerSm = 2;
+// Default CTAs per SM: enough that the stages of all CTAs on an SM hold about
+// this many bytes, and never fewer than two.  Measured on GB300: one CTA per SM
+// is consumer-bound; the copy (reads and writes share the DRAM) peaks with
+// ~64 KB of stages per SM, the row sum (reads only) with ~128 KB; more data in
+// flight lowers DRAM efficiency.  With bulk stores one stage per CTA is held by
+// the store in progress, so it does not count.
+constexpr int64_t kCopyBytesPerSm = 64 * 1024;
+constexpr int64_t kRowsumBytesPerSm = 128 * 1024;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxCoord = 0x7fffffff;  // bulk-copy coordinates are int32
 
@@ -115,10 +116,22 @@ int32_t most_contributors(int64_t tiles_n, int64_t num_tiles, int64_t G) {
     return static_cast<int32_t>(kmax);
 }
 
-int consumer_warps_for(int op, int tile_m, const mbt_opts &o) {
+int wanted_ctas_per_sm(int op, const mbt_opts &o, int stages, int64_t stage_bytes) {
+    if (o.ctas_per_sm) return o.ctas_per_sm;
+    const int64_t held = (op == MBT_OP_COPY && o.store_mode == 1) ? 1 : 0;
+    const int64_t live = std::max<int64_t>(1, stages - held);
+    const int64_t target = op == MBT_OP_ROWSUM ? kRowsumBytesPerSm : kCopyBytesPerSm;
+    return static_cast<int>(std::max<int64_t>(2, ceil_div(target, live * stage_bytes)));
+}
+
+// Row sums: 8 consumer warps (256 threads: an even split of any power-of-two
+// tile_m <= 256) when at most two CTAs share an SM; 4 warps when three or more
+// do (then registers would not fit 8), unless the tile has more rows than 128
+// threads can own.
+int consumer_warps_for(int op, int tile_m, const mbt_opts &o, int wanted_ctas) {
     if (op == MBT_OP_COPY && o.store_mode == 1) return 1;   // one thread issues the stores
     if (o.consumer_warps) return o.consumer_warps;
-    if (op == MBT_OP_ROWSUM) return kDefaultRowsumConsumerWarps;
+    if (op == MBT_OP_ROWSUM) return (wanted_ctas <= 2 || tile_m > 128) ? 8 : 4;
     return kDefaultConsumerWarps;
 }
 
@@ -128,16 +141,17 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     if (plan == nullptr || num_sms < 1 || fit_per_sm < 1) return MBT_ERR_ARG;
     const int es = esize_of(dtype);
     std::memset(plan, 0, sizeof *plan);
-    const int W = consumer_warps_for(op, tile_m, o);
-    if (op == MBT_OP_ROWSUM && W * 32 < tile_m) return MBT_ERR_UNSUPPORTED;
-    plan->consumer_warps = W;
-    plan->threads = 32 * (1 + W);
     plan->box_inner = mbt::kBoxRowBytes / es;
     plan->boxes = tile_n * es / mbt::kBoxRowBytes;
     plan->box_rows = tile_m;
     const int64_t box_stride = round_up(static_cast<int64_t>(tile_m) * mbt::kBoxRowBytes,
                                         mbt::kSwizzleAtomBytes);
     plan->stage_bytes = static_cast<int32_t>(plan->boxes * box_stride);
+    const int wanted = wanted_ctas_per_sm(op, o, stages, plan->stage_bytes);
+    const int W = consumer_warps_for(op, tile_m, o, wanted);
+    if (op == MBT_OP_ROWSUM && W * 32 < tile_m) return MBT_ERR_UNSUPPORTED;
+    plan->consumer_warps = W;
+    plan->threads = 32 * (1 + W);
     plan->tx_bytes = plan->boxes * tile_m * mbt::kBoxRowBytes;
     const int64_t smem = static_cast<int64_t>(stages) * plan->stage_bytes + mbt::kSwizzleAtomBytes;
     if (smem > smem_optin) return MBT_ERR_SMEM;
@@ -145,7 +159,7 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     plan->tiles_m = ceil_div(M, tile_m);
     plan->tiles_n = ceil_div(N, tile_n);
     plan->num_tiles = plan->tiles_m * plan->tiles_n;
-    int64_t per_sm = std::min(o.ctas_per_sm ? o.ctas_per_sm : kDefaultCtasPerSm, fit_per_sm);
+    int64_t per_sm = std::min(wanted, fit_per_sm);
     int64_t cap = per_sm * num_sms;
     if (o.max_ctas) cap = std::min<int64_t>(cap, o.max_ctas);
     if (plan->num_tiles == 0) return MBT_OK;

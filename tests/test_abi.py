@@ -120,6 +120,25 @@ def test_plan_pipeline_lesson_shape():
     assert p["smem_bytes"] == 3 * 16384 + 1024
 
 
+def test_plan_default_grid_follows_bytes_in_flight():
+    # row sum, 64 x 256 bf16 (32 KB stages): 2 stages x 2 CTAs = 128 KB per SM, 8 warps
+    p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16, fit=4, ws=True)
+    assert p["grid"] == 304 and p["consumer_warps"] == 8
+    # row sum, 128 x 64 fp16 (16 KB stages), 3 stages: 3 CTAs per SM with 4 warps
+    p = _plan(mbt.OP_ROWSUM, 24577, 16383, 128, 64, 3, torch.float16, fit=4, ws=True,
+              ld_src=16384)
+    assert p["grid"] == 456 and p["consumer_warps"] == 4
+    # copy, 16 KB stages: 3 stages -> 2 CTAs, 1 stage -> 4 CTAs
+    assert _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 3, torch.float16, fit=4)["grid"] == 304
+    assert _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 1, torch.float16, fit=6)["grid"] == 608
+    # bulk stores hold one stage: 2 stages count as 1 -> 4 CTAs
+    assert _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 2, torch.float16, fit=8,
+                 store_mode=1)["grid"] == 608
+    # an explicit value wins, capped by what fits
+    assert _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 3, torch.float16, fit=3,
+                 ctas_per_sm=5)["grid"] == 456
+
+
 def test_plan_bulk_store_mode_uses_one_consumer_warp():
     p = _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 4, torch.float16, store_mode=1,
               consumer_warps=7)
@@ -164,7 +183,7 @@ def test_plan_rowsum_split_covers_every_tile_once(M, N, tm, tn, dt, sms, fit):
         assert p["workspace_bytes"] == 0
         return
     G = p["grid"]
-    assert G == min(T, sms * min(fit, 2))        # default: at most 2 CTAs per SM
+    assert G <= min(T, sms * fit) and G >= min(T, sms * min(fit, 2))
     rng = _ranges(G, T, 1)
     assert rng[0][0] == 0 and rng[-1][1] == T
     assert all(a[1] == b[0] for a, b in zip(rng, rng[1:]))
