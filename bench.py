@@ -489,6 +489,12 @@ def bench_configs(args):
         ms = med_ms(lambda: mbt.tile_rowsum(x[:, :N], o, tm, tn, 3, workspace=ws), 20)
         line({"config": cfg, "op": "rowsum", "shape": [M, N], "ld": ld, "tile": [tm, tn],
               "stages": 3, "ms": round(ms, 4), "gbs": round((M * N * es + 4 * M) / ms / 1e6, 1)})
+        ms_sep = ms
+        ms = med_ms(lambda: mbt.tile_copy_rowsum(x[:, :N], y[:, :N], o, tm, tn, 3,
+                                                 workspace=ws), 20)
+        line({"config": cfg, "op": "copy_rowsum (fused)", "shape": [M, N], "ld": ld,
+              "tile": [tm, tn], "stages": 3, "ms": round(ms, 4),
+              "gbs": round((2 * M * N * es + 4 * M) / ms / 1e6, 1)})
         del x, y
     line({"peak_gbs": peak, "peak_source": peak_kind, "theoretical_gbs": round(theo, 1)})
 

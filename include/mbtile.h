@@ -138,7 +138,7 @@ typedef struct mbt_plan {
     size_t workspace_bytes;  /* row sum: workspace bytes this plan needs */
 } mbt_plan;
 
-enum { MBT_OP_COPY = 0, MBT_OP_ROWSUM = 1 };
+enum { MBT_OP_COPY = 0, MBT_OP_ROWSUM = 1, MBT_OP_COPY_ROWSUM = 2 };
 
 /*
  * tile_copy -- dst[i][j] = src[i][j], bit for bit, for 0 <= i < M, 0 <= j < N.
@@ -181,11 +181,38 @@ int tile_rowsum_ex(const void *src, float *out, int64_t M, int64_t N,
                    int tile_m, int tile_n, int stages, int dtype, void *stream,
                    const mbt_opts *opts);
 
+/*
+ * tile_copy_rowsum -- both results in one pass over src:
+ *   dst[i][j] = src[i][j] (bit for bit) and out[i] = sum over j < N of src[i][j].
+ *
+ * The fused form of the two consumers the pages' pipeline feeds ("cute(12)
+ * async_pipeline" §3: the consumer uses each landed tile): each tile is read
+ * from device memory once; one consumer thread writes the landed stage back
+ * with bulk tensor stores ("cute(11) Hopper TMA copy" §6.3-6.4) while the
+ * consumer warps reduce it.  The CTA has a producer warp, a store warp (bulk
+ * tensor stores; LSU stores for tiles holding a partial 16-byte chunk at
+ * column N) and the row-sum warps; each stage is released when both the store
+ * and the row-sum warps are done with it.  Row sums follow tile_rowsum's
+ * order and tolerance.  Workspace: tile_copy_rowsum_workspace_bytes.
+ *   src, dst   as in tile_copy (opts->ld_src, opts->ld_dst; must not overlap
+ *              unless equal); out as in tile_rowsum.
+ * opts->store_mode must be 0.
+ */
+int tile_copy_rowsum(const void *src, void *dst, float *out, int64_t M, int64_t N,
+                     int tile_m, int tile_n, int stages, int dtype, void *stream);
+int tile_copy_rowsum_ex(const void *src, void *dst, float *out, int64_t M, int64_t N,
+                        int tile_m, int tile_n, int stages, int dtype, void *stream,
+                        const mbt_opts *opts);
+
 /* Workspace bytes tile_rowsum_ex needs on the current device for this shape
  * and these options (opts->workspace is ignored).  0 when no split helps. */
 int tile_rowsum_workspace_bytes(int64_t M, int64_t N, int tile_m, int tile_n,
                                 int stages, int dtype, const mbt_opts *opts,
                                 size_t *bytes);
+/* The same for tile_copy_rowsum_ex (its grid differs from tile_rowsum's). */
+int tile_copy_rowsum_workspace_bytes(int64_t M, int64_t N, int tile_m, int tile_n,
+                                     int stages, int dtype, const mbt_opts *opts,
+                                     size_t *bytes);
 
 /*
  * tile_rowsum_noalloc -- tile_rowsum_ex for callers that cannot allocate
@@ -224,7 +251,8 @@ int tile_rowsum_noalloc(const void *src, float *out, int64_t M, int64_t N,
                         void *stream, const mbt_opts *opts);
 
 /*
- * tile_plan -- the launch plan for op (MBT_OP_COPY or MBT_OP_ROWSUM), from
+ * tile_plan -- the launch plan for op (MBT_OP_COPY, MBT_OP_ROWSUM or
+ * MBT_OP_COPY_ROWSUM), from
  * the device figures given as arguments; makes no CUDA call.
  *   num_sms        SMs of the device (> 0).
  *   smem_optin     opt-in dynamic shared memory limit per CTA, bytes.

@@ -22,11 +22,12 @@ __all__ = [
     "MbtError", "C", "library_path", "tile_copy", "tile_rowsum", "tile_status",
     "tile_plan", "tile_device_info", "tile_strerror", "tile_rowsum_workspace_bytes",
     "Opts", "Plan", "DTYPE_CODE", "OP_COPY", "OP_ROWSUM", "tile_rowsum_noalloc",
+    "tile_copy_rowsum",
 ]
 
 MBT_OK = 0
 MBT_ERR_TIMEOUT = -6
-OP_COPY, OP_ROWSUM = 0, 1
+OP_COPY, OP_ROWSUM, OP_COPY_ROWSUM = 0, 1, 2
 DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
 
 
@@ -106,9 +107,15 @@ def _load():
         lib.tile_copy_ex.argtypes = sig + [ctypes.POINTER(Opts)]
         lib.tile_rowsum.argtypes = sig
         lib.tile_rowsum_ex.argtypes = sig + [ctypes.POINTER(Opts)]
+        lib.tile_copy_rowsum.argtypes = [vp, vp, vp, i64, i64, i32, i32, i32, i32, vp]
+        lib.tile_copy_rowsum_ex.argtypes = [vp, vp, vp, i64, i64, i32, i32, i32, i32, vp,
+                                            ctypes.POINTER(Opts)]
         lib.tile_rowsum_workspace_bytes.argtypes = [i64, i64, i32, i32, i32, i32,
                                                     ctypes.POINTER(Opts),
                                                     ctypes.POINTER(ctypes.c_size_t)]
+        lib.tile_copy_rowsum_workspace_bytes.argtypes = [i64, i64, i32, i32, i32, i32,
+                                                         ctypes.POINTER(Opts),
+                                                         ctypes.POINTER(ctypes.c_size_t)]
         lib.tile_plan.argtypes = [i32, i64, i64, i32, i32, i32, i32, ctypes.POINTER(Opts),
                                   i32, i32, i32, i32, ctypes.POINTER(Plan)]
         lib.tile_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
@@ -118,7 +125,9 @@ def _load():
                                          ctypes.POINTER(ctypes.c_int),
                                          ctypes.POINTER(ctypes.c_double)]
         for name in ("tile_copy", "tile_copy_ex", "tile_rowsum", "tile_rowsum_ex",
-                     "tile_rowsum_workspace_bytes", "tile_plan", "tile_status",
+                     "tile_copy_rowsum", "tile_copy_rowsum_ex",
+                     "tile_rowsum_workspace_bytes", "tile_copy_rowsum_workspace_bytes",
+                     "tile_plan", "tile_status",
                      "tile_device_info"):
             getattr(lib, name).restype = ctypes.c_int
         _C = lib
@@ -219,11 +228,13 @@ def _reset_workspaces() -> None:
 
 
 def tile_rowsum_workspace_bytes(M: int, N: int, tile_m: int, tile_n: int, stages: int,
-                                dtype: torch.dtype, **opt) -> int:
+                                dtype: torch.dtype, fused: bool = False, **opt) -> int:
+    """Workspace bytes of tile_rowsum (or, with ``fused``, tile_copy_rowsum)."""
     o = _opts(**opt)
     out = ctypes.c_size_t(0)
-    rc = _load().tile_rowsum_workspace_bytes(M, N, tile_m, tile_n, stages, DTYPE_CODE[dtype],
-                                             ctypes.byref(o), ctypes.byref(out))
+    fn = (_load().tile_copy_rowsum_workspace_bytes if fused
+          else _load().tile_rowsum_workspace_bytes)
+    rc = fn(M, N, tile_m, tile_n, stages, DTYPE_CODE[dtype], ctypes.byref(o), ctypes.byref(out))
     _check(rc, "tile_rowsum_workspace_bytes")
     return out.value
 
@@ -258,6 +269,42 @@ def tile_rowsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int 
     rc = _load().tile_rowsum_ex(src.data_ptr(), out.data_ptr(), M, N, tile_m, tile_n, stages,
                                 DTYPE_CODE[src.dtype], _stream_handle(stream), ctypes.byref(o))
     _check(rc, "tile_rowsum")
+    return out
+
+
+def tile_copy_rowsum(src: torch.Tensor, dst: torch.Tensor, out: torch.Tensor | None = None,
+                     tile_m: int = 128, tile_n: int = 64, stages: int = 3, *,
+                     split: bool = True, consumer_warps: int = 0, max_ctas: int = 0,
+                     ctas_per_sm: int = 0, wait_budget_ns: int = 0,
+                     log: torch.Tensor | None = None, fault: int = 0,
+                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """dst[i, j] = src[i, j] and out[i] = sum_j src[i, j] in one pass; returns out."""
+    M, N, ld_s = _matrix(src, "src")
+    Md, Nd, ld_d = _matrix(dst, "dst")
+    if (M, N) != (Md, Nd) or src.dtype != dst.dtype:
+        raise ValueError("src and dst must have the same shape and dtype")
+    if out is None:
+        out = torch.empty(M, dtype=torch.float32, device=src.device)
+    if out.dtype != torch.float32 or out.numel() != M or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor of M elements")
+    o = _opts(ld_src=ld_s, ld_dst=ld_d, consumer_warps=consumer_warps, max_ctas=max_ctas,
+              ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault)
+    if log is not None:
+        o.log = log.data_ptr()
+        o.log_capacity = log.numel() // 8
+    if split and M > 0 and N > 0:
+        need = tile_rowsum_workspace_bytes(M, N, tile_m, tile_n, stages, src.dtype, fused=True,
+                                           ld_src=ld_s, ld_dst=ld_d,
+                                           consumer_warps=consumer_warps,
+                                           max_ctas=max_ctas, ctas_per_sm=ctas_per_sm)
+        if need:
+            ws = workspace if workspace is not None else _workspace(src.device, need)
+            o.workspace = ws.data_ptr()
+            o.workspace_bytes = ws.numel() * ws.element_size()
+    rc = _load().tile_copy_rowsum_ex(src.data_ptr(), dst.data_ptr(), out.data_ptr(), M, N,
+                                     tile_m, tile_n, stages, DTYPE_CODE[src.dtype],
+                                     _stream_handle(stream), ctypes.byref(o))
+    _check(rc, "tile_copy_rowsum")
     return out
 
 

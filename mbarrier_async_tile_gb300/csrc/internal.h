@@ -32,6 +32,9 @@ struct PipeArgs {
     uint32_t stage_stride;     // shared-memory bytes between stages
     uint32_t tx_bytes;         // bytes one tile delivers to its full barrier
     int32_t fault;             // test hook, see mbt_opts.fault
+    int32_t empty_extra;       // arrivals on an empty barrier beyond one per
+                               // consumer warp (1 when a bulk store also reads
+                               // the stage)
     uint64_t wait_budget_ns;
     int32_t *log;
     int64_t log_cap;
@@ -54,14 +57,16 @@ struct RowsumArgs {
     int64_t units;             // scheduling units = num_tiles / gran
     int64_t gran;              // tiles per scheduling unit (1 or tiles_n)
     int32_t kmax;
-    int32_t pad_;
+    int32_t fused;             // 1: also copy every tile to dst (bulk stores)
+    char *dst;                 // fused copy destination
+    int64_t ld_dst_bytes;
 };
 
 // Launchers (mbtile_kernels.cu).  They only enqueue work on `stream`.
 cudaError_t launch_copy(const CUtensorMap &map, const CUtensorMap &dst_map,
                         const CopyArgs &a, int grid, int threads, int smem,
                         cudaStream_t stream);
-cudaError_t launch_rowsum(int dtype, const CUtensorMap &map,
+cudaError_t launch_rowsum(int dtype, const CUtensorMap &map, const CUtensorMap &dst_map,
                           const RowsumArgs &a, int grid, int threads, int smem,
                           cudaStream_t stream);
 cudaError_t launch_fill_zero(float *out, int64_t n, cudaStream_t stream);

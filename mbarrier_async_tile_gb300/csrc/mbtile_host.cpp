@@ -61,7 +61,8 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
                int64_t *ld_dst) {
     const int es = esize_of(dtype);
     if (es == 0) return MBT_ERR_ARG;
-    if (op != MBT_OP_COPY && op != MBT_OP_ROWSUM) return MBT_ERR_ARG;
+    if (op != MBT_OP_COPY && op != MBT_OP_ROWSUM && op != MBT_OP_COPY_ROWSUM) return MBT_ERR_ARG;
+    const bool writes_dst = op != MBT_OP_ROWSUM;
     if (M < 0 || N < 0) return MBT_ERR_ARG;
     if (tile_m < 1 || tile_m > 256 || tile_n < 1 || stages < 1 || stages > mbt::kMaxStages)
         return MBT_ERR_ARG;
@@ -73,6 +74,7 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
     if (o.fault < 0 || o.fault > 2) return MBT_ERR_ARG;
     if (o.store_mode < 0 || o.store_mode > 1) return MBT_ERR_UNSUPPORTED;
     if (o.store_mode != 0 && op != MBT_OP_COPY) return MBT_ERR_ARG;
+    (void)writes_dst;
     for (int r : o.reserved)
         if (r != 0) return MBT_ERR_ARG;
     if (o.log != nullptr && o.log_capacity == 0) return MBT_ERR_ARG;
@@ -90,7 +92,7 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
     }
     if (src == nullptr || dst == nullptr) return MBT_ERR_ARG;
     if (!aligned16(src) || (*ld_src * es) % 16 != 0) return MBT_ERR_ALIGN;
-    if (op == MBT_OP_COPY && (!aligned16(dst) || (*ld_dst * es) % 16 != 0)) return MBT_ERR_ALIGN;
+    if (writes_dst && (!aligned16(dst) || (*ld_dst * es) % 16 != 0)) return MBT_ERR_ALIGN;
     if (op == MBT_OP_ROWSUM && (reinterpret_cast<uintptr_t>(dst) & 3u) != 0) return MBT_ERR_ALIGN;
     if (static_cast<uint64_t>(*ld_src) * es >= (1ull << 40)) return MBT_ERR_UNSUPPORTED;
     return MBT_OK;
@@ -118,9 +120,10 @@ int32_t most_contributors(int64_t tiles_n, int64_t num_tiles, int64_t G) {
 
 int wanted_ctas_per_sm(int op, const mbt_opts &o, int stages, int64_t stage_bytes) {
     if (o.ctas_per_sm) return o.ctas_per_sm;
-    const int64_t held = (op == MBT_OP_COPY && o.store_mode == 1) ? 1 : 0;
+    const bool bulk = (op == MBT_OP_COPY && o.store_mode == 1) || op == MBT_OP_COPY_ROWSUM;
+    const int64_t held = bulk ? 1 : 0;
     const int64_t live = std::max<int64_t>(1, stages - held);
-    const int64_t target = op == MBT_OP_ROWSUM ? kRowsumBytesPerSm : kCopyBytesPerSm;
+    const int64_t target = op == MBT_OP_ROWSUM ? kRowsumBytesPerSm : kCopyBytesPerSm;  // fused writes too
     return static_cast<int>(std::max<int64_t>(2, ceil_div(target, live * stage_bytes)));
 }
 
@@ -131,7 +134,7 @@ int wanted_ctas_per_sm(int op, const mbt_opts &o, int stages, int64_t stage_byte
 int consumer_warps_for(int op, int tile_m, const mbt_opts &o, int wanted_ctas) {
     if (op == MBT_OP_COPY && o.store_mode == 1) return 1;   // one thread issues the stores
     if (o.consumer_warps) return o.consumer_warps;
-    if (op == MBT_OP_ROWSUM) return (wanted_ctas <= 2 || tile_m > 128) ? 8 : 4;
+    if (op != MBT_OP_COPY) return (wanted_ctas <= 2 || tile_m > 128) ? 8 : 4;
     return kDefaultConsumerWarps;
 }
 
@@ -149,9 +152,10 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     plan->stage_bytes = static_cast<int32_t>(plan->boxes * box_stride);
     const int wanted = wanted_ctas_per_sm(op, o, stages, plan->stage_bytes);
     const int W = consumer_warps_for(op, tile_m, o, wanted);
-    if (op == MBT_OP_ROWSUM && W * 32 < tile_m) return MBT_ERR_UNSUPPORTED;
+    if (op != MBT_OP_COPY && W * 32 < tile_m) return MBT_ERR_UNSUPPORTED;
     plan->consumer_warps = W;
-    plan->threads = 32 * (1 + W);
+    // producer warp + consumer warps (+ the fused operation's store warp)
+    plan->threads = 32 * (1 + W + (op == MBT_OP_COPY_ROWSUM ? 1 : 0));
     plan->tx_bytes = plan->boxes * tile_m * mbt::kBoxRowBytes;
     const int64_t smem = static_cast<int64_t>(stages) * plan->stage_bytes + mbt::kSwizzleAtomBytes;
     if (smem > smem_optin) return MBT_ERR_SMEM;
@@ -254,7 +258,7 @@ int plan_on_device(int op, int64_t M, int64_t N, int tile_m, int tile_n, int sta
     if (rc != MBT_OK) return rc;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MBT_ERR_CUDA;
-    const auto key = std::make_tuple(dev, op, op == MBT_OP_ROWSUM ? dtype : 0, plan->threads,
+    const auto key = std::make_tuple(dev, op, op != MBT_OP_COPY ? dtype : 0, plan->threads,
                                      plan->smem_bytes);
     int fit = 0;
     {
@@ -302,6 +306,77 @@ mbt_opts opts_or_default(const mbt_opts *opts) {
     std::memset(&o, 0, sizeof o);
     if (opts) o = *opts;
     return o;
+}
+
+// Row sums (and, with dst != nullptr, the fused copy) after argument checks.
+int rowsum_launch(const void *src, void *dst, float *out, int64_t M, int64_t N, int64_t ld_src,
+                  int64_t ld_dst, int tile_m, int tile_n, int stages, int dtype, void *stream,
+                  const mbt_opts &o) {
+    const int op = dst != nullptr ? MBT_OP_COPY_ROWSUM : MBT_OP_ROWSUM;
+    if (M == 0) return MBT_OK;
+    if (N == 0) {
+        return mbt::launch_fill_zero(out, M, static_cast<cudaStream_t>(stream)) == cudaSuccess
+                   ? MBT_OK
+                   : MBT_ERR_CUDA;
+    }
+    mbt_plan plan;
+    int rc = plan_on_device(op, M, N, tile_m, tile_n, stages, dtype, o, o.workspace != nullptr,
+                            &plan);
+    if (rc != MBT_OK) return rc;
+    if (plan.split && o.workspace_bytes < plan.workspace_bytes) return MBT_ERR_WORKSPACE;
+    if (plan.split && (reinterpret_cast<uintptr_t>(o.workspace) & 255u) != 0) return MBT_ERR_ALIGN;
+    alignas(64) CUtensorMap map;
+    rc = encode_map(&map, src, M, N, ld_src, dtype, tile_m);
+    if (rc != MBT_OK) return rc;
+    alignas(64) CUtensorMap dst_map;
+    std::memset(&dst_map, 0, sizeof dst_map);
+    if (dst != nullptr) {
+        rc = encode_map(&dst_map, dst, M, N, ld_dst, dtype, tile_m);
+        if (rc != MBT_OK) return rc;
+    }
+    RowsumArgs a{};
+    a.p = pipe_args(plan, M, N, tile_m, stages, dtype, o);
+    a.out = out;
+    if (plan.split) {
+        char *ws = static_cast<char *>(o.workspace);
+        a.ticket = reinterpret_cast<int32_t *>(ws);
+        a.partial = reinterpret_cast<float *>(ws + round_up(plan.tiles_m * 4, 256));
+        a.gran = 1;
+        a.units = plan.num_tiles;
+    } else {
+        a.gran = plan.tiles_n;
+        a.units = plan.tiles_m;
+    }
+    a.kmax = plan.kmax;
+    if (dst != nullptr) {
+        a.fused = 1;
+        a.dst = static_cast<char *>(dst);
+        a.ld_dst_bytes = ld_dst * esize_of(dtype);
+        a.p.empty_extra = 1;   // the bulk store's reads of each stage
+    }
+    const cudaError_t e = mbt::launch_rowsum(dtype, map, dst_map, a, plan.grid, plan.threads,
+                                             plan.smem_bytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
+}
+
+int workspace_bytes(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, int dtype,
+                    const mbt_opts *opts, size_t *bytes) {
+    if (bytes == nullptr) return MBT_ERR_ARG;
+    mbt_opts o = opts_or_default(opts);
+    o.workspace = nullptr;
+    o.workspace_bytes = 0;
+    int64_t ld_src = 0, ld_dst = 0;
+    static const char dummy[16] __attribute__((aligned(16))) = {0};
+    int rc = check_args(op, dummy, dummy, M, N, tile_m, tile_n, stages, dtype, o, &ld_src,
+                        &ld_dst);
+    if (rc != MBT_OK) return rc;
+    *bytes = 0;
+    if (M == 0 || N == 0) return MBT_OK;
+    mbt_plan plan;
+    rc = plan_on_device(op, M, N, tile_m, tile_n, stages, dtype, o, 1, &plan);
+    if (rc != MBT_OK) return rc;
+    *bytes = plan.workspace_bytes;
+    return MBT_OK;
 }
 
 }  // namespace
@@ -363,38 +438,28 @@ int tile_rowsum_ex(const void *src, float *out, int64_t M, int64_t N, int tile_m
     int rc = check_args(MBT_OP_ROWSUM, src, out, M, N, tile_m, tile_n, stages, dtype, o, &ld_src,
                         &ld_dst);
     if (rc != MBT_OK) return rc;
-    if (M == 0) return MBT_OK;
-    if (N == 0) {
-        return mbt::launch_fill_zero(out, M, static_cast<cudaStream_t>(stream)) == cudaSuccess
-                   ? MBT_OK
-                   : MBT_ERR_CUDA;
-    }
-    mbt_plan plan;
-    rc = plan_on_device(MBT_OP_ROWSUM, M, N, tile_m, tile_n, stages, dtype, o,
-                        o.workspace != nullptr, &plan);
+    return rowsum_launch(src, nullptr, out, M, N, ld_src, 0, tile_m, tile_n, stages, dtype,
+                         stream, o);
+}
+
+int tile_copy_rowsum_ex(const void *src, void *dst, float *out, int64_t M, int64_t N, int tile_m,
+                        int tile_n, int stages, int dtype, void *stream, const mbt_opts *opts) {
+    const mbt_opts o = opts_or_default(opts);
+    if (o.store_mode != 0) return MBT_ERR_ARG;
+    int64_t ld_src = 0, ld_dst = 0;
+    int rc = check_args(MBT_OP_COPY_ROWSUM, src, dst, M, N, tile_m, tile_n, stages, dtype, o,
+                        &ld_src, &ld_dst);
     if (rc != MBT_OK) return rc;
-    if (plan.split && o.workspace_bytes < plan.workspace_bytes) return MBT_ERR_WORKSPACE;
-    if (plan.split && (reinterpret_cast<uintptr_t>(o.workspace) & 255u) != 0) return MBT_ERR_ALIGN;
-    alignas(64) CUtensorMap map;
-    rc = encode_map(&map, src, M, N, ld_src, dtype, tile_m);
-    if (rc != MBT_OK) return rc;
-    RowsumArgs a{};
-    a.p = pipe_args(plan, M, N, tile_m, stages, dtype, o);
-    a.out = out;
-    if (plan.split) {
-        char *ws = static_cast<char *>(o.workspace);
-        a.ticket = reinterpret_cast<int32_t *>(ws);
-        a.partial = reinterpret_cast<float *>(ws + round_up(plan.tiles_m * 4, 256));
-        a.gran = 1;
-        a.units = plan.num_tiles;
-    } else {
-        a.gran = plan.tiles_n;
-        a.units = plan.tiles_m;
-    }
-    a.kmax = plan.kmax;
-    const cudaError_t e = mbt::launch_rowsum(dtype, map, a, plan.grid, plan.threads,
-                                             plan.smem_bytes, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
+    if (M > 0 && out == nullptr) return MBT_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(out) & 3u) != 0) return MBT_ERR_ALIGN;
+    return rowsum_launch(src, dst, out, M, N, ld_src, ld_dst, tile_m, tile_n, stages, dtype,
+                         stream, o);
+}
+
+int tile_copy_rowsum(const void *src, void *dst, float *out, int64_t M, int64_t N, int tile_m,
+                     int tile_n, int stages, int dtype, void *stream) {
+    return tile_copy_rowsum_ex(src, dst, out, M, N, tile_m, tile_n, stages, dtype, stream,
+                               nullptr);
 }
 
 int tile_rowsum(const void *src, float *out, int64_t M, int64_t N, int tile_m, int tile_n,
@@ -404,22 +469,12 @@ int tile_rowsum(const void *src, float *out, int64_t M, int64_t N, int tile_m, i
 
 int tile_rowsum_workspace_bytes(int64_t M, int64_t N, int tile_m, int tile_n, int stages,
                                 int dtype, const mbt_opts *opts, size_t *bytes) {
-    if (bytes == nullptr) return MBT_ERR_ARG;
-    mbt_opts o = opts_or_default(opts);
-    o.workspace = nullptr;
-    o.workspace_bytes = 0;
-    int64_t ld_src = 0, ld_dst = 0;
-    static const char dummy[16] __attribute__((aligned(16))) = {0};
-    int rc = check_args(MBT_OP_ROWSUM, dummy, dummy, M, N, tile_m, tile_n, stages, dtype, o,
-                        &ld_src, &ld_dst);
-    if (rc != MBT_OK) return rc;
-    *bytes = 0;
-    if (M == 0 || N == 0) return MBT_OK;
-    mbt_plan plan;
-    rc = plan_on_device(MBT_OP_ROWSUM, M, N, tile_m, tile_n, stages, dtype, o, 1, &plan);
-    if (rc != MBT_OK) return rc;
-    *bytes = plan.workspace_bytes;
-    return MBT_OK;
+    return workspace_bytes(MBT_OP_ROWSUM, M, N, tile_m, tile_n, stages, dtype, opts, bytes);
+}
+
+int tile_copy_rowsum_workspace_bytes(int64_t M, int64_t N, int tile_m, int tile_n, int stages,
+                                     int dtype, const mbt_opts *opts, size_t *bytes) {
+    return workspace_bytes(MBT_OP_COPY_ROWSUM, M, N, tile_m, tile_n, stages, dtype, opts, bytes);
 }
 
 int tile_status(void *stream, int32_t info[4]) {

@@ -267,7 +267,8 @@ __device__ __forceinline__ void init_pipeline(const PipeArgs &p, Smem &sm,
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(sm.full0 + 8u * s, 1);
-            mbar_init(sm.empty0 + 8u * s, static_cast<uint32_t>(p.consumer_warps));
+            mbar_init(sm.empty0 + 8u * s,
+                      static_cast<uint32_t>(p.consumer_warps + p.empty_extra));
         }
         if (extra_bar != nullptr) mbar_init(smem_u32(extra_bar), extra_count);
         *abort_flag = 0;
@@ -295,10 +296,9 @@ __device__ __forceinline__ void store_tail(char *d, const uint4 &v, int nbytes, 
 // `nthr` threads (ctid = 0 .. nthr-1, whole warps).  Every warp releases the
 // stage (one arrive on `release_bar` per warp, unless release_bar == 0) right
 // after its last shared-memory loads, before its global stores.
-__device__ __forceinline__ void copy_tile_lsu(const CopyArgs &a, uint32_t sbase, int64_t row0,
-                                              int64_t col0, int ctid, int nthr,
-                                              uint32_t release_bar) {
-    const PipeArgs &p = a.p;
+__device__ __forceinline__ void copy_tile_lsu(const PipeArgs &p, char *dst, int64_t ld_dst_bytes,
+                                              uint32_t sbase, int64_t row0, int64_t col0,
+                                              int ctid, int nthr, uint32_t release_bar) {
     const int lane = threadIdx.x & 31;
     const int cpr = p.boxes * 8;                    // 16-byte chunks per tile row
     const int cpr_log2 = __ffs(cpr) - 1;
@@ -324,7 +324,7 @@ __device__ __forceinline__ void copy_tile_lsu(const CopyArgs &a, uint32_t sbase,
             const int64_t grow = row0 + (i >> cpr_log2);
             const int64_t gcol = col0 + static_cast<int64_t>(i & (cpr - 1)) * vec_elems;
             if (grow >= p.M || gcol >= p.N) continue;
-            char *d = a.dst + grow * a.ld_dst_bytes + gcol * p.esize;
+            char *d = dst + grow * ld_dst_bytes + gcol * p.esize;
             if (gcol + vec_elems <= p.N)
                 stg128(d, v[u]);
             else
@@ -356,8 +356,8 @@ __device__ void consume_copy(const CopyArgs &a, const Smem &sm, const WaitCtl &w
         const int64_t tm = tile / p.tiles_n;
         const int64_t row0 = tm * p.tile_m;
         const int64_t col0 = (tile - tm * p.tiles_n) * p.boxes * p.box_inner;
-        copy_tile_lsu(a, sm.base + stage * p.stage_stride, row0, col0, ctid, nthr,
-                      p.fault != 2 ? sm.empty0 + 8u * stage : 0u);
+        copy_tile_lsu(p, a.dst, a.ld_dst_bytes, sm.base + stage * p.stage_stride, row0, col0,
+                      ctid, nthr, p.fault != 2 ? sm.empty0 + 8u * stage : 0u);
         if (++stage == static_cast<uint32_t>(p.stages)) {
             stage = 0;
             phase ^= 1u;
@@ -365,24 +365,70 @@ __device__ void consume_copy(const CopyArgs &a, const Smem &sm, const WaitCtl &w
     }
 }
 
+// Bulk tensor stores of landed stages, issued by one thread.  A stage is
+// released (one arrival on its empty barrier) once its store has finished
+// reading shared memory: with two or more stages one store is left in flight
+// and its stage released after the next store is issued; a single stage is
+// released right away.  Loads and stores both run in the async proxy; the
+// proxy fence orders the thread's view of the completed phase before the
+// store's reads.
+struct BulkStores {
+    bool pending = false;      // a committed store whose stage is not released yet
+    uint32_t prev_stage = 0;
+
+    __device__ void store_tile(const CUtensorMap *dst_map, const PipeArgs &p, const Smem &sm,
+                               uint32_t stage, int64_t row0, int64_t col0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const uint32_t sbase = sm.base + stage * p.stage_stride;
+        for (int b = 0; b < p.boxes; ++b)
+            tma_store_2d(dst_map, sbase + b * p.box_stride,
+                         static_cast<int32_t>(col0) + b * p.box_inner, static_cast<int32_t>(row0));
+        bulk_commit_group();
+        if (p.stages == 1) {
+            bulk_wait_read_all();
+            if (p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+            return;
+        }
+        if (pending) {
+            bulk_wait_read_allow1();
+            if (p.fault != 2) mbar_arrive(sm.empty0 + 8u * prev_stage);
+        }
+        pending = true;
+        prev_stage = stage;
+    }
+
+    // Release the stage of the store in flight now (before a tile that no
+    // store will follow soon: the producer may need that stage next).
+    __device__ void release_pending(const PipeArgs &p, const Smem &sm) {
+        if (!pending) return;
+        bulk_wait_read_all();
+        if (p.fault != 2) mbar_arrive(sm.empty0 + 8u * prev_stage);
+        pending = false;
+    }
+
+    __device__ void finish(const PipeArgs &p, const Smem &sm, bool aborted) {
+        bulk_wait_read_all();
+        if (pending && !aborted && p.fault != 2) mbar_arrive(sm.empty0 + 8u * prev_stage);
+        pending = false;
+        bulk_wait_all();
+    }
+};
+
 // Copy consumer with bulk tensor stores (one consumer warp): lane 0 stores
 // each landed stage straight from shared memory (same swizzled box layout) to
-// the destination, and releases the stage once that store has finished
-// reading shared memory.  Loads and stores both run in the async proxy; the
-// proxy fence orders the lane's view of the completed phase before the
-// store's reads.  The copy engine clips a store's innermost dimension only at
-// 16-byte granularity, so a tile holding a partial 16-byte chunk at column N
-// is written by the warp with LSU stores instead.
+// the destination.  The copy engine clips a store's innermost dimension only
+// at 16-byte granularity, so a tile holding a partial 16-byte chunk at column
+// N is written by the warp with LSU stores instead.
 __device__ void consume_copy_bulk(const CUtensorMap *dst_map, const CopyArgs &a, const Smem &sm,
-                                  const WaitCtl &w, int64_t first, int64_t step, int64_t count) {
+                                  const WaitCtl &w, int64_t first, int64_t step, int64_t count,
+                                  bool do_log = true) {
     const PipeArgs &p = a.p;
     const int lane = threadIdx.x & 31;
     const int vec_elems = 16 / p.esize;
     const int64_t n_whole = p.N - p.N % vec_elems;   // columns in whole 16-byte chunks
     const int64_t tile_n = static_cast<int64_t>(p.boxes) * p.box_inner;
+    BulkStores bs;
     uint32_t stage = 0, phase = 0;
-    uint32_t prev_stage = 0;
-    bool pending = false;          // a committed store whose stage is not released yet
     for (int64_t j = 0; j < count; ++j) {
         bool ok = wait_bounded(sm.full0 + 8u * stage, phase, w, true);
         ok = __all_sync(0xffffffffu, ok);
@@ -394,55 +440,23 @@ __device__ void consume_copy_bulk(const CUtensorMap *dst_map, const CopyArgs &a,
             break;
         }
         const int64_t tile = first + j * step;
-        if (lane == 0) log_record(p, 1, j, stage, phase, tile);
+        if (do_log && lane == 0) log_record(p, 1, j, stage, phase, tile);
         const int64_t tm = tile / p.tiles_n;
         const int64_t row0 = tm * p.tile_m;
         const int64_t col0 = (tile - tm * p.tiles_n) * tile_n;
-        const uint32_t sbase = sm.base + stage * p.stage_stride;
         if (col0 + tile_n > n_whole && n_whole != p.N) {
-            if (pending) {
-                // Free the stage held by the last store first: the producer's
-                // next tile may need it, and no further store will release it.
-                if (lane == 0) {
-                    bulk_wait_read_all();
-                    if (p.fault != 2) mbar_arrive(sm.empty0 + 8u * prev_stage);
-                }
-                pending = false;
-            }
-            copy_tile_lsu(a, sbase, row0, col0, lane, 32,
-                          p.fault != 2 ? sm.empty0 + 8u * stage : 0u);
-        } else {
-            if (lane == 0) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                for (int b = 0; b < p.boxes; ++b)
-                    tma_store_2d(dst_map, sbase + b * p.box_stride,
-                                 static_cast<int32_t>(col0) + b * p.box_inner,
-                                 static_cast<int32_t>(row0));
-                bulk_commit_group();
-                if (p.stages == 1) {
-                    // A single stage cannot wait for the next tile: release it
-                    // as soon as this store has read it.
-                    bulk_wait_read_all();
-                    if (p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
-                } else if (pending) {
-                    // The previous store has read its stage: release it.
-                    bulk_wait_read_allow1();
-                    if (p.fault != 2) mbar_arrive(sm.empty0 + 8u * prev_stage);
-                }
-            }
-            pending = p.stages > 1;
-            prev_stage = stage;
+            if (lane == 0) bs.release_pending(p, sm);
+            copy_tile_lsu(p, a.dst, a.ld_dst_bytes, sm.base + stage * p.stage_stride, row0, col0,
+                          lane, 32, p.fault != 2 ? sm.empty0 + 8u * stage : 0u);
+        } else if (lane == 0) {
+            bs.store_tile(dst_map, p, sm, stage, row0, col0);
         }
         if (++stage == static_cast<uint32_t>(p.stages)) {
             stage = 0;
             phase ^= 1u;
         }
     }
-    if (lane == 0) {
-        bulk_wait_read_all();
-        if (pending && p.fault != 2 && !*w.abort) mbar_arrive(sm.empty0 + 8u * prev_stage);
-        bulk_wait_all();
-    }
+    if (lane == 0) bs.finish(p, sm, *w.abort != 0);
 }
 
 __global__ void __launch_bounds__(kMaxThreads, 2)
@@ -523,9 +537,8 @@ __device__ bool consumers_sync(FlushCtl &f, const WaitCtl &w) {
 // last contributing CTA add the partials of all contributors in CTA order.
 __device__ bool flush_band(const RowsumArgs &a, int64_t band, float acc, bool active,
                            int row, int sub, int tpr, float *red, int *last_flag,
-                           FlushCtl &f, const WaitCtl &w) {
+                           FlushCtl &f, const WaitCtl &w, int ctid) {
     const PipeArgs &p = a.p;
-    const int ctid = static_cast<int>(threadIdx.x) - 32;
     red[ctid] = acc;
     if (!consumers_sync(f, w)) return false;
     const int64_t G = gridDim.x;
@@ -570,12 +583,13 @@ __device__ bool flush_band(const RowsumArgs &a, int64_t band, float acc, bool ac
     return true;
 }
 
+// Row-sum consumer warps; the first of them is warp `cwarp0` of the CTA.
 template <int DT>
 __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCtl &w,
                                int64_t first, int64_t count, float *red, int *last_flag,
-                               FlushCtl &f) {
+                               FlushCtl &f, int cwarp0) {
     const PipeArgs &p = a.p;
-    const int ctid = static_cast<int>(threadIdx.x) - 32;
+    const int ctid = static_cast<int>(threadIdx.x) - 32 * cwarp0;
     const int lane = threadIdx.x & 31;
     const int nthr = p.consumer_warps * 32;
     const int tpr = nthr / p.tile_m;                 // threads per row (>= 1)
@@ -596,7 +610,7 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
         const int64_t tb = tile / p.tiles_n;
         if (tb != band) {
             if (band >= 0 && !flush_band(a, band, acc, active, row, sub, tpr, red,
-                                         last_flag, f, w)) {
+                                         last_flag, f, w, ctid)) {
                 ok = false;
                 break;
             }
@@ -614,7 +628,7 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
             ok = false;
             break;
         }
-        if (threadIdx.x == 32) log_record(p, 1, j, stage, phase, tile);
+        if (ctid == 0) log_record(p, 1, j, stage, phase, tile);
         const uint32_t rbase = sm.base + stage * p.stage_stride;
         float tsum = 0.f;
         for (int r = 0; r < rounds; ++r) {
@@ -641,16 +655,20 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
         }
     }
     if (ok && band >= 0)
-        flush_band(a, band, acc, active, row, sub, tpr, red, last_flag, f, w);
+        flush_band(a, band, acc, active, row, sub, tpr, red, last_flag, f, w, ctid);
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kMaxThreads, 2)
-    mbt_rowsum_kernel(const __grid_constant__ CUtensorMap map, const RowsumArgs a) {
+// FUSED: warp 1 writes every landed stage to dst (bulk tensor stores; LSU
+// stores for tiles with a partial 16-byte chunk at column N) and is the one
+// extra arrival on each empty barrier; the row-sum warps follow it.
+template <int DT, bool FUSED>
+__global__ void __launch_bounds__(FUSED ? kMaxThreads + 32 : kMaxThreads, 2)
+    mbt_rowsum_kernel(const __grid_constant__ CUtensorMap map,
+                      const __grid_constant__ CUtensorMap dst_map, const RowsumArgs a) {
     extern __shared__ __align__(1024) unsigned char dyn_smem[];
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
     __shared__ __align__(8) uint64_t flush_bar;
-    __shared__ float red[kMaxThreads];
+    __shared__ float red[kMaxThreads];      // indexed by row-sum consumer thread
     __shared__ int abort_flag;
     __shared__ int last_flag;
     Smem sm;
@@ -666,8 +684,19 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
         if (threadIdx.x == 0) produce(&map, a.p, sm, w, first, 1, last - first);
         return;
     }
+    if constexpr (FUSED) {
+        if (threadIdx.x < 64) {
+            CopyArgs c{};
+            c.p = a.p;
+            c.dst = a.dst;
+            c.ld_dst_bytes = a.ld_dst_bytes;
+            c.store_mode = 1;
+            consume_copy_bulk(&dst_map, c, sm, w, first, 1, last - first, false);
+            return;
+        }
+    }
     FlushCtl f{smem_u32(&flush_bar), 0u};
-    consume_rowsum<DT>(a, sm, w, first, last - first, red, &last_flag, f);
+    consume_rowsum<DT>(a, sm, w, first, last - first, red, &last_flag, f, FUSED ? 2 : 1);
 }
 
 __global__ void mbt_fill_zero_kernel(float *out, int64_t n) {
@@ -687,14 +716,29 @@ cudaError_t launch_copy(const CUtensorMap &map, const CUtensorMap &dst_map, cons
     return cudaGetLastError();
 }
 
-cudaError_t launch_rowsum(int dtype, const CUtensorMap &map, const RowsumArgs &a, int grid,
-                          int threads, int smem, cudaStream_t stream) {
+template <bool FUSED>
+cudaError_t launch_rowsum_t(int dtype, const CUtensorMap &map, const CUtensorMap &dst_map,
+                            const RowsumArgs &a, int grid, int threads, int smem,
+                            cudaStream_t stream) {
     switch (dtype) {
-        case MBT_F16: mbt_rowsum_kernel<MBT_F16><<<grid, threads, smem, stream>>>(map, a); break;
-        case MBT_BF16: mbt_rowsum_kernel<MBT_BF16><<<grid, threads, smem, stream>>>(map, a); break;
-        default: mbt_rowsum_kernel<MBT_F32><<<grid, threads, smem, stream>>>(map, a); break;
+        case MBT_F16:
+            mbt_rowsum_kernel<MBT_F16, FUSED><<<grid, threads, smem, stream>>>(map, dst_map, a);
+            break;
+        case MBT_BF16:
+            mbt_rowsum_kernel<MBT_BF16, FUSED><<<grid, threads, smem, stream>>>(map, dst_map, a);
+            break;
+        default:
+            mbt_rowsum_kernel<MBT_F32, FUSED><<<grid, threads, smem, stream>>>(map, dst_map, a);
+            break;
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_rowsum(int dtype, const CUtensorMap &map, const CUtensorMap &dst_map,
+                          const RowsumArgs &a, int grid, int threads, int smem,
+                          cudaStream_t stream) {
+    return a.fused ? launch_rowsum_t<true>(dtype, map, dst_map, a, grid, threads, smem, stream)
+                   : launch_rowsum_t<false>(dtype, map, dst_map, a, grid, threads, smem, stream);
 }
 
 cudaError_t launch_fill_zero(float *out, int64_t n, cudaStream_t stream) {
@@ -709,9 +753,12 @@ cudaError_t set_kernel_smem_limit(int optin, int *usable) {
     // Each kernel may use the opt-in limit minus its own static shared memory;
     // the plan uses the smallest of these so that any kernel can launch it.
     const void *fns[] = {reinterpret_cast<const void *>(mbt_copy_kernel),
-                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16>),
-                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16>),
-                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32>)};
+                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16, false>),
+                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16, false>),
+                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32, false>),
+                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16, true>),
+                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16, true>),
+                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32, true>)};
     int least = optin;
     for (const void *fn : fns) {
         cudaFuncAttributes attr{};
@@ -728,11 +775,14 @@ cudaError_t set_kernel_smem_limit(int optin, int *usable) {
 
 cudaError_t kernel_fit_per_sm(int op, int dtype, int threads, int smem, int *fit) {
     const void *fn = reinterpret_cast<const void *>(mbt_copy_kernel);
-    if (op == MBT_OP_ROWSUM) {
-        fn = dtype == MBT_F16    ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16>)
-             : dtype == MBT_BF16 ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16>)
-                                 : reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32>);
-    }
+    if (op == MBT_OP_ROWSUM)
+        fn = dtype == MBT_F16    ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16, false>)
+             : dtype == MBT_BF16 ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16, false>)
+                                 : reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32, false>);
+    if (op == MBT_OP_COPY_ROWSUM)
+        fn = dtype == MBT_F16    ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16, true>)
+             : dtype == MBT_BF16 ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16, true>)
+                                 : reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32, true>);
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(fit, fn, threads, smem);
 }
 

@@ -91,6 +91,16 @@ def test_option_errors():
     assert _copy(A, B, 8, 64, opts=o) == -2
 
 
+def test_fused_argument_errors():
+    fn = C.tile_copy_rowsum_ex
+    assert fn(A, B, None, 8, 64, 128, 64, 3, 0, None, None) == -1          # out missing
+    assert fn(A, B, B + 2, 8, 64, 128, 64, 3, 0, None, None) == -2         # out misaligned
+    assert fn(A, B + 8, B, 8, 64, 128, 64, 3, 0, None, None) == -2         # dst misaligned
+    o = Opts(); o.store_mode = 1
+    assert fn(A, B, B, 8, 64, 128, 64, 3, 0, None, ctypes.byref(o)) == -1
+    assert fn(0, 0, None, 0, 64, 128, 64, 3, 0, None, None) == 0
+
+
 def test_empty_shapes_are_noops_without_device():
     assert _copy(0, 0, 0, 64) == 0
     assert _copy(0, 0, 5, 0) == 0
@@ -137,6 +147,13 @@ def test_plan_default_grid_follows_bytes_in_flight():
     # an explicit value wins, capped by what fits
     assert _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 3, torch.float16, fit=3,
                  ctas_per_sm=5)["grid"] == 456
+
+
+def test_plan_fused_adds_a_store_warp():
+    p = _plan(mbt.OP_COPY_ROWSUM, 24577, 16383, 128, 64, 3, torch.float16, fit=2, ws=True,
+              ld_src=16384, ld_dst=16384)
+    # 16 KB stages, one held by the store in flight: 2 live x 2 CTAs = 64 KB per SM
+    assert p["grid"] == 304 and p["consumer_warps"] == 8 and p["threads"] == 32 * 10
 
 
 def test_plan_bulk_store_mode_uses_one_consumer_warp():
