@@ -115,7 +115,16 @@ typedef struct mbt_opts {
                                 call ends with MBT_ERR_TIMEOUT after about
                                 (stages + 2) x wait_budget_ns; no bulk copy is
                                 in flight when the kernel returns. */
-    int32_t reserved[7];     /* must be 0 */
+    int32_t pipeline;        /* tile_copy only.  0: warp-specialised (a
+                                producer warp and consumer warps, full/empty
+                                barrier pair per stage; default).  1: unified
+                                -- every warp consumes; one elected thread
+                                issues each tile S-1 tiles ahead; a CTA-wide
+                                barrier releases a stage ("CUDA features 10:
+                                Pipelines" §4.10.7 prologue / steady state /
+                                epilogue).  Kept as a measured comparison
+                                point; consumer_warps counts all warps. */
+    int32_t reserved[6];     /* must be 0 */
 } mbt_opts;
 
 /* Launch plan, as computed by tile_plan (host only, no CUDA calls). */

@@ -46,7 +46,8 @@ class Opts(ctypes.Structure):
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("fault", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 7),
+        ("pipeline", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 6),
     ]
 
 
@@ -184,7 +185,8 @@ def _opts(**kw) -> Opts:
 def tile_copy(src: torch.Tensor, dst: torch.Tensor, tile_m: int = 128, tile_n: int = 64,
               stages: int = 4, *, consumer_warps: int = 0, max_ctas: int = 0,
               ctas_per_sm: int = 0, wait_budget_ns: int = 0, log: torch.Tensor | None = None,
-              fault: int = 0, store_mode: int = 0, stream=None) -> torch.Tensor:
+              fault: int = 0, store_mode: int = 0, pipeline: int = 0,
+              stream=None) -> torch.Tensor:
     """dst[i, j] = src[i, j] (bit-exact) through the tile pipeline.
 
     ``src`` and ``dst`` are 2-D CUDA views of the same shape and dtype with
@@ -195,7 +197,7 @@ def tile_copy(src: torch.Tensor, dst: torch.Tensor, tile_m: int = 128, tile_n: i
         raise ValueError("src and dst must have the same shape and dtype")
     o = _opts(ld_src=ld_s, ld_dst=ld_d, consumer_warps=consumer_warps, max_ctas=max_ctas,
               ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault,
-              store_mode=store_mode)
+              store_mode=store_mode, pipeline=pipeline)
     if log is not None:
         o.log = log.data_ptr()
         o.log_capacity = log.numel() // 8

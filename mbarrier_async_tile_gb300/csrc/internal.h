@@ -69,11 +69,14 @@ cudaError_t launch_copy(const CUtensorMap &map, const CUtensorMap &dst_map,
 cudaError_t launch_rowsum(int dtype, const CUtensorMap &map, const CUtensorMap &dst_map,
                           const RowsumArgs &a, int grid, int threads, int smem,
                           cudaStream_t stream);
+cudaError_t launch_copy_unified(const CUtensorMap &map, const CopyArgs &a, int grid,
+                                int threads, int smem, cudaStream_t stream);
 cudaError_t launch_fill_zero(float *out, int64_t n, cudaStream_t stream);
 // Raise every kernel's dynamic shared-memory limit as far as the device's
 // opt-in limit allows; `usable` receives the limit common to all kernels.
 cudaError_t set_kernel_smem_limit(int optin, int *usable);
-// CTAs of a kernel with this block/smem shape that fit on one SM.
+// CTAs of a kernel with this block/smem shape that fit on one SM; kernel
+// MBT_OP_COPY, MBT_OP_ROWSUM, MBT_OP_COPY_ROWSUM, or 3 = unified copy.
 cudaError_t kernel_fit_per_sm(int op, int dtype, int threads, int smem, int *fit);
 // Read the device status word and clear it (synchronous).
 cudaError_t read_and_clear_status(int32_t info[4]);

@@ -73,6 +73,9 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
     if (o.ctas_per_sm < 0 || o.max_ctas < 0 || o.log_capacity < 0) return MBT_ERR_ARG;
     if (o.fault < 0 || o.fault > 2) return MBT_ERR_ARG;
     if (o.store_mode < 0 || o.store_mode > 1) return MBT_ERR_UNSUPPORTED;
+    if (o.pipeline < 0 || o.pipeline > 1) return MBT_ERR_UNSUPPORTED;
+    if (o.pipeline == 1 && op != MBT_OP_COPY) return MBT_ERR_ARG;
+    if (o.pipeline == 1 && o.store_mode != 0) return MBT_ERR_UNSUPPORTED;
     if (o.store_mode != 0 && op != MBT_OP_COPY) return MBT_ERR_ARG;
     (void)writes_dst;
     for (int r : o.reserved)
@@ -154,8 +157,9 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     const int W = consumer_warps_for(op, tile_m, o, wanted);
     if (op != MBT_OP_COPY && W * 32 < tile_m) return MBT_ERR_UNSUPPORTED;
     plan->consumer_warps = W;
-    // producer warp + consumer warps (+ the fused operation's store warp)
-    plan->threads = 32 * (1 + W + (op == MBT_OP_COPY_ROWSUM ? 1 : 0));
+    // producer warp + consumer warps (+ the fused operation's store warp);
+    // the unified pipeline has no producer warp
+    plan->threads = 32 * ((o.pipeline == 1 ? 0 : 1) + W + (op == MBT_OP_COPY_ROWSUM ? 1 : 0));
     plan->tx_bytes = plan->boxes * tile_m * mbt::kBoxRowBytes;
     const int64_t smem = static_cast<int64_t>(stages) * plan->stage_bytes + mbt::kSwizzleAtomBytes;
     if (smem > smem_optin) return MBT_ERR_SMEM;
@@ -258,8 +262,9 @@ int plan_on_device(int op, int64_t M, int64_t N, int tile_m, int tile_n, int sta
     if (rc != MBT_OK) return rc;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MBT_ERR_CUDA;
-    const auto key = std::make_tuple(dev, op, op != MBT_OP_COPY ? dtype : 0, plan->threads,
-                                     plan->smem_bytes);
+    const int kernel_id = op == MBT_OP_COPY && o.pipeline == 1 ? 3 : op;
+    const auto key = std::make_tuple(dev, kernel_id, op != MBT_OP_COPY ? dtype : 0,
+                                     plan->threads, plan->smem_bytes);
     int fit = 0;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
@@ -267,7 +272,7 @@ int plan_on_device(int op, int64_t M, int64_t N, int tile_m, int tile_n, int sta
         if (it != g_fit_cache.end()) fit = it->second;
     }
     if (fit == 0) {
-        if (mbt::kernel_fit_per_sm(op, dtype, plan->threads, plan->smem_bytes, &fit) !=
+        if (mbt::kernel_fit_per_sm(kernel_id, dtype, plan->threads, plan->smem_bytes, &fit) !=
             cudaSuccess)
             return MBT_ERR_CUDA;
         if (fit < 1) return MBT_ERR_SMEM;
@@ -421,8 +426,12 @@ int tile_copy_ex(const void *src, void *dst, int64_t M, int64_t N, int tile_m, i
     a.dst = static_cast<char *>(dst);
     a.ld_dst_bytes = ld_dst * esize_of(dtype);
     a.store_mode = o.store_mode;
-    const cudaError_t e = mbt::launch_copy(map, dst_map, a, plan.grid, plan.threads,
-                                           plan.smem_bytes, static_cast<cudaStream_t>(stream));
+    const cudaError_t e =
+        o.pipeline == 1
+            ? mbt::launch_copy_unified(map, a, plan.grid, plan.threads, plan.smem_bytes,
+                                       static_cast<cudaStream_t>(stream))
+            : mbt::launch_copy(map, dst_map, a, plan.grid, plan.threads, plan.smem_bytes,
+                               static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
 }
 

@@ -484,6 +484,75 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
 }
 
 // ---------------------------------------------------------------------------
+// Unified (not warp-specialised) copy pipeline
+// ---------------------------------------------------------------------------
+// Every warp consumes.  Thread 0 issues tile j + S - 1 at the top of
+// iteration j (prologue: tiles 0 .. S-2 before the loop); all threads wait on
+// full[j mod S], copy the stage out, and a CTA-wide barrier -- which also
+// votes on whether any wait gave up -- marks the stage free for the issue at
+// the top of the next iteration.  No empty barriers.  Source: "CUDA features
+// 10: Pipelines" §4.10.7 (prologue fills S-1 stages; steady state issues the
+// next tile, waits for and uses the current one, releases it; epilogue).
+__global__ void __launch_bounds__(kMaxThreads, 2)
+    mbt_copy_unified_kernel(const __grid_constant__ CUtensorMap map, const CopyArgs a) {
+    extern __shared__ __align__(1024) unsigned char dyn_smem[];
+    __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
+    __shared__ int abort_flag;
+    Smem sm;
+    init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);
+    const PipeArgs &p = a.p;
+    WaitCtl w{p.wait_budget_ns, &abort_flag};
+    const int64_t G = gridDim.x;
+    const int64_t first = blockIdx.x;
+    const int64_t count = first < p.num_tiles ? (p.num_tiles - first + G - 1) / G : 0;
+    const int nthr = static_cast<int>(blockDim.x);
+    const int64_t ahead = p.stages - 1;
+    auto issue = [&](int64_t j) {
+        const uint32_t s = static_cast<uint32_t>(j % p.stages);
+        const int64_t tile = first + j * G;
+        const int64_t tm = tile / p.tiles_n;
+        const int32_t y = static_cast<int32_t>(tm * p.tile_m);
+        const int32_t x0 = static_cast<int32_t>((tile - tm * p.tiles_n) * p.boxes * p.box_inner);
+        const uint32_t full_bar = sm.full0 + 8u * s;
+        mbar_arrive_expect_tx(full_bar, p.tx_bytes);
+        for (int b = 0; b < p.boxes; ++b)
+            tma_load_2d(sm.base + s * p.stage_stride + b * p.box_stride, &map,
+                        x0 + b * p.box_inner, y, full_bar);
+        log_record(p, 0, j, s, 0, tile);
+    };
+    int64_t issued = 0;
+    if (threadIdx.x == 0)
+        for (; issued < ahead && issued < count; ++issued) issue(issued);
+    for (int64_t j = 0; j < count; ++j) {
+        const uint32_t s = static_cast<uint32_t>(j % p.stages);
+        const uint32_t par = static_cast<uint32_t>((j / p.stages) & 1);
+        // The stage of tile j + S - 1 held tile j - 1, released by the
+        // barrier that ended the previous iteration.
+        if (threadIdx.x == 0 && issued == j + ahead && issued < count) issue(issued++);
+        const bool ok = wait_bounded(sm.full0 + 8u * s, par, w, true);
+        if (ok) {
+            if (threadIdx.x == 0) log_record(p, 1, j, s, par, first + j * G);
+            const int64_t tile = first + j * G;
+            const int64_t tm = tile / p.tiles_n;
+            copy_tile_lsu(p, a.dst, a.ld_dst_bytes, sm.base + s * p.stage_stride, tm * p.tile_m,
+                          (tile - tm * p.tiles_n) * p.boxes * p.box_inner,
+                          static_cast<int>(threadIdx.x), nthr, 0u);
+        } else if ((threadIdx.x & 31) == 0) {
+            report_timeout(1, s, par);
+            *w.abort = 1;
+        }
+        if (__syncthreads_or(!ok)) break;
+    }
+    if (threadIdx.x == 0 && *w.abort) {
+        // Wait (bounded) for loads still in flight before the CTA exits.
+        const int64_t from = issued > p.stages ? issued - p.stages : 0;
+        for (int64_t t = from; t < issued; ++t)
+            wait_bounded(sm.full0 + 8u * static_cast<uint32_t>(t % p.stages),
+                         static_cast<uint32_t>((t / p.stages) & 1), w, false);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Row sum
 // ---------------------------------------------------------------------------
 template <int DT>
@@ -741,6 +810,12 @@ cudaError_t launch_rowsum(int dtype, const CUtensorMap &map, const CUtensorMap &
                    : launch_rowsum_t<false>(dtype, map, dst_map, a, grid, threads, smem, stream);
 }
 
+cudaError_t launch_copy_unified(const CUtensorMap &map, const CopyArgs &a, int grid, int threads,
+                                int smem, cudaStream_t stream) {
+    mbt_copy_unified_kernel<<<grid, threads, smem, stream>>>(map, a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fill_zero(float *out, int64_t n, cudaStream_t stream) {
     const int threads = 256;
     const int64_t blocks64 = (n + threads - 1) / threads;
@@ -753,6 +828,7 @@ cudaError_t set_kernel_smem_limit(int optin, int *usable) {
     // Each kernel may use the opt-in limit minus its own static shared memory;
     // the plan uses the smallest of these so that any kernel can launch it.
     const void *fns[] = {reinterpret_cast<const void *>(mbt_copy_kernel),
+                         reinterpret_cast<const void *>(mbt_copy_unified_kernel),
                          reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16, false>),
                          reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16, false>),
                          reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32, false>),
@@ -775,6 +851,7 @@ cudaError_t set_kernel_smem_limit(int optin, int *usable) {
 
 cudaError_t kernel_fit_per_sm(int op, int dtype, int threads, int smem, int *fit) {
     const void *fn = reinterpret_cast<const void *>(mbt_copy_kernel);
+    if (op == 3) fn = reinterpret_cast<const void *>(mbt_copy_unified_kernel);
     if (op == MBT_OP_ROWSUM)
         fn = dtype == MBT_F16    ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16, false>)
              : dtype == MBT_BF16 ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16, false>)

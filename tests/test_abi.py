@@ -75,12 +75,18 @@ def test_copy_tile_and_stage_errors():
 
 def test_option_errors():
     o = Opts()
-    o.reserved[3] = 1
+    o.reserved[2] = 1
     assert _copy(A, B, 8, 64, opts=o) == -1
     o = Opts(); o.consumer_warps = 9
     assert _copy(A, B, 8, 64, opts=o) == -1
     o = Opts(); o.fault = 3
     assert _copy(A, B, 8, 64, opts=o) == -1
+    o = Opts(); o.pipeline = 2
+    assert _copy(A, B, 8, 64, opts=o) == -3
+    o = Opts(); o.pipeline = 1; o.store_mode = 1   # unified pipeline: LSU stores only
+    assert _copy(A, B, 8, 64, opts=o) == -3
+    o = Opts(); o.pipeline = 1                     # copy only
+    assert C.tile_rowsum_ex(A, B, 8, 64, 128, 64, 3, 0, None, ctypes.byref(o)) == -1
     o = Opts(); o.store_mode = 2
     assert _copy(A, B, 8, 64, opts=o) == -3
     o = Opts(); o.store_mode = 1                 # bulk stores: a copy-only option

@@ -101,6 +101,28 @@ def test_nothing_written_outside_the_logical_region(dtype, M, N, tm, tn, store_m
     assert torch.equal(bits(d.cpu()), bits(want))
 
 
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
+def test_unified_pipeline_matches_oracle(case):
+    """The non-specialised pipeline (every warp consumes, one thread issues
+    S-1 tiles ahead, a CTA barrier releases each stage)."""
+    dtype, M, N, tm, tn, st, w = case
+    es = synthetic.ESIZE[dtype]
+    src, dst, want = copy_case(dtype, M, N, seed=M * 5 + N, src_pad=16 // es, dst_pad=32 // es)
+    got = run_copy(src, dst, N, tm, tn, st, consumer_warps=w, pipeline=1)
+    assert torch.equal(bits(got), bits(want))
+
+
+def test_unified_pipeline_full_size_and_one_cta():
+    src, dst, want = copy_case("f16", 16384, 16384, seed=1003)
+    s = src.cuda()
+    for st, kw in ((3, {}), (1, {}), (4, dict(max_ctas=1))):
+        d = dst.cuda() if not kw else dst[:512].cuda()
+        sv = s if not kw else s[:512]
+        mbt.tile_copy(sv, d, 128, 64, st, pipeline=1, **kw)
+        assert mbt.tile_status()[0] == 0
+        assert torch.equal(bits(d.cpu()), bits(want if not kw else want[:512])), (st, kw)
+
+
 @pytest.mark.parametrize("stages", [1, 2, 3])
 def test_bulk_store_mode_many_tiles_per_cta(stages):
     """Each CTA streams many tiles through its ring, including a single-stage
