@@ -34,9 +34,14 @@
  *     small per-device status word (see tile_status).
  *   - Matrices are row-major: element (i, j) is at ptr[i * ld + j], with the
  *     row pitch ld in elements.  The logical shape is M rows by N columns.
- *     ld * element size must be a multiple of 16 bytes and the base pointer
- *     16-byte aligned (a bulk tensor copy's global stride rule); a dense
- *     matrix whose rows are not a multiple of 16 bytes must be stored pitched.
+ *     Base pointers must be 16-byte aligned.  When ld * element size is a
+ *     multiple of 16 bytes the tiles are moved by 2-D bulk tensor copies into
+ *     128-byte-swizzled stages.  Otherwise (a bulk tensor copy needs 16-byte
+ *     global strides) the stages are filled by 1-D bulk copies of 16-byte-
+ *     aligned windows of the matrix's bytes: supported for tile_rowsum at any
+ *     pitch and for tile_copy when src and dst are both dense (ld = N); other
+ *     cases return MBT_ERR_ALIGN.  The stage then holds tile_m x tile_n
+ *     elements' worth of bytes.
  *   - A tile is tile_m rows by tile_n columns.  tile_n * element size must be
  *     128, 256, 512 or 1024 bytes (1, 2, 4 or 8 side-by-side 128-byte boxes,
  *     each one bulk copy with the 128-byte swizzle); 1 <= tile_m <= 256;
@@ -140,7 +145,9 @@ typedef struct mbt_plan {
     int32_t stage_bytes;     /* shared-memory bytes of one stage */
     int32_t split;           /* row sum: 1 if a band may span several CTAs */
     int32_t kmax;            /* row sum: most CTAs contributing to one band */
-    int32_t reserved0;
+    int32_t flat;            /* 1: row pitch not a multiple of 16 bytes; the
+                                1-D bulk-copy kernels run, num_tiles counts
+                                their windows */
     int64_t tiles_m;         /* tiles down the rows (row bands) */
     int64_t tiles_n;         /* tiles across the columns */
     int64_t num_tiles;

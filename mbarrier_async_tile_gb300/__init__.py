@@ -65,7 +65,7 @@ class Plan(ctypes.Structure):
         ("stage_bytes", ctypes.c_int32),
         ("split", ctypes.c_int32),
         ("kmax", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32),
+        ("flat", ctypes.c_int32),
         ("tiles_m", ctypes.c_int64),
         ("tiles_n", ctypes.c_int64),
         ("num_tiles", ctypes.c_int64),
@@ -73,7 +73,7 @@ class Plan(ctypes.Structure):
     ]
 
     def as_dict(self) -> dict:
-        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved0"}
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 class MbtError(RuntimeError):

@@ -62,6 +62,21 @@ struct RowsumArgs {
     int64_t ld_dst_bytes;
 };
 
+// Matrices whose row pitch is not a multiple of 16 bytes (mbtile_flat.cuh).
+struct FlatArgs {
+    PipeArgs p;                // M, N, esize, stages, consumer_warps, stage_stride, ...
+    const char *src;
+    char *dst;                 // copy
+    float *out;                // row sum
+    int64_t ld;                // row pitch (elements)
+    int64_t total_bytes;       // ((M - 1) ld + N) * esize
+    int64_t t_floor;           // total_bytes rounded down to 16
+    int64_t cap_bytes;         // bytes one stage can take (multiple of 16)
+    int64_t rows_per_window;   // row sum: whole rows per window, 0 => long rows
+    int64_t piece_elems;       // row sum, long rows: elements per piece
+    int64_t pieces_per_row;
+};
+
 // Launchers (mbtile_kernels.cu).  They only enqueue work on `stream`.
 cudaError_t launch_copy(const CUtensorMap &map, const CUtensorMap &dst_map,
                         const CopyArgs &a, int grid, int threads, int smem,
@@ -71,12 +86,17 @@ cudaError_t launch_rowsum(int dtype, const CUtensorMap &map, const CUtensorMap &
                           cudaStream_t stream);
 cudaError_t launch_copy_unified(const CUtensorMap &map, const CopyArgs &a, int grid,
                                 int threads, int smem, cudaStream_t stream);
+cudaError_t launch_copy_flat(const FlatArgs &a, int grid, int threads, int smem,
+                             cudaStream_t stream);
+cudaError_t launch_rowsum_flat(int dtype, const FlatArgs &a, int grid, int threads, int smem,
+                               cudaStream_t stream);
 cudaError_t launch_fill_zero(float *out, int64_t n, cudaStream_t stream);
 // Raise every kernel's dynamic shared-memory limit as far as the device's
 // opt-in limit allows; `usable` receives the limit common to all kernels.
 cudaError_t set_kernel_smem_limit(int optin, int *usable);
 // CTAs of a kernel with this block/smem shape that fit on one SM; kernel
-// MBT_OP_COPY, MBT_OP_ROWSUM, MBT_OP_COPY_ROWSUM, or 3 = unified copy.
+// MBT_OP_COPY, MBT_OP_ROWSUM, MBT_OP_COPY_ROWSUM, 3 = unified copy,
+// 4 = flat copy, 5 = flat row sum.
 cudaError_t kernel_fit_per_sm(int op, int dtype, int threads, int smem, int *fit);
 // Read the device status word and clear it (synchronous).
 cudaError_t read_and_clear_status(int32_t info[4]);

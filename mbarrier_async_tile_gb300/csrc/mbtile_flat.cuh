@@ -1,0 +1,471 @@
+// Pipelines over matrices whose row pitch is not a multiple of 16 bytes.
+//
+// A bulk tensor copy needs 16-byte global strides, so such a matrix cannot be
+// described by a 2-D tensor map.  Here the stages are filled with 1-D bulk
+// copies (cp.async.bulk, 16-byte-aligned address and size) of windows of the
+// matrix's bytes: the same producer / consumer ring, full and empty barriers,
+// expect_tx byte counts and parity cursors as the tiled kernels, but linear
+// (unswizzled) stages.  A window starts at the 16-byte boundary at or below its
+// first byte and ends at the one at or above its last byte, clipped to the
+// last 16-byte boundary of the array; bytes past that clip (at most 15, at the
+// very end of the array) are read from global memory directly.
+//
+// Included by mbtile_kernels.cu inside its anonymous namespace: it uses that
+// file's PTX wrappers, bounded waits and status word.
+
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void *src, uint32_t bytes,
+                                             uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+struct Window {
+    int64_t ws;     // first byte (16-byte aligned) loaded into the stage
+    int64_t size;   // bytes loaded (multiple of 16, may be 0)
+};
+
+__device__ __forceinline__ Window make_window(int64_t b0, int64_t b1, int64_t t_floor) {
+    Window w;
+    w.ws = b0 & ~int64_t(15);
+    int64_t we = (b1 + 15) & ~int64_t(15);
+    if (we > t_floor) we = t_floor;
+    w.size = we > w.ws ? we - w.ws : 0;
+    return w;
+}
+
+// Element range [e0, e1) of window j of this CTA (row-sum schedule).
+struct RowWindow {
+    int64_t r0, r1;     // rows [r0, r1) -- whole rows (short rows) or one row
+    int64_t e0, e1;     // element indices covered (global, counted along the pitch)
+    int64_t piece;      // long rows: which piece of row r0
+};
+
+__device__ __forceinline__ RowWindow rowsum_window(const FlatArgs &a, int64_t ra, int64_t rb,
+                                                   int64_t j) {
+    RowWindow w;
+    if (a.rows_per_window > 0) {
+        w.r0 = ra + j * a.rows_per_window;
+        w.r1 = w.r0 + a.rows_per_window < rb ? w.r0 + a.rows_per_window : rb;
+        w.piece = 0;
+        w.e0 = w.r0 * a.ld;
+        w.e1 = (w.r1 - 1) * a.ld + a.p.N;
+    } else {
+        w.r0 = ra + j / a.pieces_per_row;
+        w.r1 = w.r0 + 1;
+        w.piece = j % a.pieces_per_row;
+        const int64_t c0 = w.piece * a.piece_elems;
+        const int64_t c1 = c0 + a.piece_elems < a.p.N ? c0 + a.piece_elems : a.p.N;
+        w.e0 = w.r0 * a.ld + c0;
+        w.e1 = w.r0 * a.ld + c1;
+    }
+    return w;
+}
+
+__device__ __forceinline__ int64_t flat_rowsum_windows(const FlatArgs &a, int64_t ra, int64_t rb) {
+    if (rb <= ra) return 0;
+    if (a.rows_per_window > 0) return (rb - ra + a.rows_per_window - 1) / a.rows_per_window;
+    return (rb - ra) * a.pieces_per_row;
+}
+
+// Window of the copy schedule: bytes [w C, (w + 1) C) of the 16-byte-aligned
+// part of the array.
+__device__ __forceinline__ Window copy_window(const FlatArgs &a, int64_t w) {
+    Window win;
+    win.ws = w * a.cap_bytes;
+    const int64_t end = win.ws + a.cap_bytes < a.t_floor ? win.ws + a.cap_bytes : a.t_floor;
+    win.size = end - win.ws;
+    return win;
+}
+
+// Producer of the flat pipelines: loads `count` windows (window j given by
+// `win(j)`) into the ring, then drains it.  A window of size 0 (all of it in
+// the unaligned tail) completes its phase with a plain arrive.
+template <class WinFn>
+__device__ void produce_flat(const FlatArgs &a, const Smem &sm, const WaitCtl &w, int64_t count,
+                             WinFn win) {
+    const PipeArgs &p = a.p;
+    uint32_t stage = 0;
+    uint32_t phase = (p.fault == 1) ? 0u : 1u;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int64_t j = 0; j < count; ++j) {
+        if (!wait_bounded(sm.empty0 + 8u * stage, phase, w, true)) {
+            report_timeout(0, stage, phase);
+            *w.abort = 1;
+            ok = false;
+            break;
+        }
+        const Window wj = win(j);
+        const uint32_t full_bar = sm.full0 + 8u * stage;
+        if (wj.size > 0) {
+            mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(wj.size));
+            bulk_load_1d(sm.base + stage * p.stage_stride, a.src + wj.ws,
+                         static_cast<uint32_t>(wj.size), full_bar);
+        } else {
+            mbar_arrive(full_bar);
+        }
+        log_record(p, 0, j, stage, phase, j);
+        ++issued;
+        if (++stage == static_cast<uint32_t>(p.stages)) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+    if (ok) {
+        for (int s = 0; s < p.stages; ++s) {
+            if (!wait_bounded(sm.empty0 + 8u * stage, phase, w, true)) {
+                report_timeout(0, stage, phase);
+                *w.abort = 1;
+                ok = false;
+                break;
+            }
+            if (++stage == static_cast<uint32_t>(p.stages)) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        const int64_t from = issued > p.stages ? issued - p.stages : 0;
+        for (int64_t t = from; t < issued; ++t)
+            wait_bounded(sm.full0 + 8u * static_cast<uint32_t>(t % p.stages),
+                         static_cast<uint32_t>((t / p.stages) & 1), w, false);
+    }
+}
+
+__device__ __forceinline__ void copy_element(char *d, const char *s, int esize) {
+    if (esize == 4)
+        *reinterpret_cast<uint32_t *>(d) = *reinterpret_cast<const uint32_t *>(s);
+    else
+        *reinterpret_cast<uint16_t *>(d) = *reinterpret_cast<const uint16_t *>(s);
+}
+
+// ---------------------------------------------------------------------------
+// Flat copy (dense source and destination, ld = N, row bytes not a multiple
+// of 16): the matrix is one contiguous byte array; CTA b copies windows
+// b, b + G, ... with 16-byte LSU stores at the same offsets.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kMaxThreads, 2)
+    mbt_copy_flat_kernel(const FlatArgs a) {
+    extern __shared__ __align__(1024) unsigned char dyn_smem[];
+    __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
+    __shared__ int abort_flag;
+    Smem sm;
+    init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);
+    const PipeArgs &p = a.p;
+    WaitCtl w{p.wait_budget_ns, &abort_flag};
+    const int64_t G = gridDim.x;
+    const int64_t nwin = (a.t_floor + a.cap_bytes - 1) / a.cap_bytes;
+    const int64_t first = blockIdx.x;
+    const int64_t count = first < nwin ? (nwin - first + G - 1) / G : 0;
+    auto win = [&](int64_t j) { return copy_window(a, first + j * G); };
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0) produce_flat(a, sm, w, count, win);
+        return;
+    }
+    const int ctid = static_cast<int>(threadIdx.x) - 32;
+    const int lane = threadIdx.x & 31;
+    const int nthr = p.consumer_warps * 32;
+    if (blockIdx.x == 0) {
+        // The unaligned tail of the array (fewer than 16 bytes).
+        for (int64_t b = a.t_floor + ctid * p.esize; b < a.total_bytes; b += nthr * p.esize)
+            copy_element(a.dst + b, a.src + b, p.esize);
+    }
+    uint32_t stage = 0, phase = 0;
+    for (int64_t j = 0; j < count; ++j) {
+        bool ok = wait_bounded(sm.full0 + 8u * stage, phase, w, true);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            if (lane == 0) {
+                report_timeout(1, stage, phase);
+                *w.abort = 1;
+            }
+            break;
+        }
+        if (ctid == 0) log_record(p, 1, j, stage, phase, first + j * G);
+        const Window wj = win(j);
+        const uint32_t sbase = sm.base + stage * p.stage_stride;
+        const int chunks = static_cast<int>(wj.size >> 4);
+        const int rounds = (chunks + nthr * kVec - 1) / (nthr * kVec);
+        for (int r = 0; r < rounds; ++r) {
+            uint4 v[kVec];
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                const int c = ctid + (r * kVec + u) * nthr;
+                if (c < chunks) v[u] = lds128(sbase + 16u * c);
+            }
+            if (r == rounds - 1) {
+                __syncwarp();
+                if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+            }
+#pragma unroll
+            for (int u = 0; u < kVec; ++u) {
+                const int c = ctid + (r * kVec + u) * nthr;
+                if (c < chunks) stg128(a.dst + wj.ws + 16 * static_cast<int64_t>(c), v[u]);
+            }
+        }
+        if (rounds == 0) {
+            __syncwarp();
+            if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+        }
+        if (++stage == static_cast<uint32_t>(p.stages)) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Flat row sum (any row pitch): CTA b owns rows [b M / G, (b + 1) M / G).
+// Short rows: a window holds several whole rows; every thread splits its
+// 16-byte chunks into the part of the chunk's first row and of the next row,
+// then one thread per row adds its chunks' parts in chunk order (rows shorter
+// than a chunk: one thread per row, element by element).  Long rows: a window
+// holds one piece of one row; every thread keeps its share of the row across
+// the row's pieces, and at the row's last piece a warp tree and an ordered sum
+// over warps give the row's sum.  Each row is summed by one CTA, so no
+// workspace is needed.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ float element_value(uint32_t bits) {
+    if constexpr (DT == MBT_F32) {
+        return __uint_as_float(bits);
+    } else if constexpr (DT == MBT_BF16) {
+        return __uint_as_float(bits << 16);
+    } else {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t element_bits(const unsigned char *p) {
+    if constexpr (DT == MBT_F32)
+        return *reinterpret_cast<const uint32_t *>(p);
+    else
+        return *reinterpret_cast<const uint16_t *>(p);
+}
+
+// Sum of the elements of chunk `v` (starting at element index `g0`) whose
+// index lies in [e0, e1), in element order.
+template <int DT>
+__device__ __forceinline__ float masked_chunk_sum(const uint4 &v, int64_t g0, int64_t e0,
+                                                  int64_t e1) {
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    float s = 0.f;
+    if constexpr (DT == MBT_F32) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (g0 + k >= e0 && g0 + k < e1) s += __uint_as_float(w4[k]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t bits = (w4[k >> 1] >> ((k & 1) * 16)) & 0xffffu;
+            if (g0 + k >= e0 && g0 + k < e1) s += element_value<DT>(bits);
+        }
+    }
+    return s;
+}
+
+// Windows of the flat row sum hold at most this many 16-byte chunks.
+constexpr int kFlatChunks = 1024;
+constexpr int kFlatVec = 4;   // chunks a thread holds per round (register budget)
+
+template <int DT>
+__global__ void __launch_bounds__(kMaxThreads, 2)
+    mbt_rowsum_flat_kernel(const FlatArgs a) {
+    extern __shared__ __align__(1024) unsigned char dyn_smem[];
+    __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
+    __shared__ __align__(8) uint64_t flush_bar;
+    __shared__ float red[2][kMaxConsumerWarps];
+    // Short rows: per chunk, the sums of its elements in its first row (0)
+    // and in the next row (1); double-buffered by window parity.
+    __shared__ float part[2][2][kFlatChunks];
+    __shared__ int abort_flag;
+    Smem sm;
+    init_pipeline(a.p, sm, bars, &abort_flag, &flush_bar,
+                  static_cast<uint32_t>(a.p.consumer_warps), dyn_smem);
+    const PipeArgs &p = a.p;
+    WaitCtl w{p.wait_budget_ns, &abort_flag};
+    const int64_t G = gridDim.x;
+    const int64_t ra = static_cast<int64_t>(blockIdx.x) * p.M / G;
+    const int64_t rb = (static_cast<int64_t>(blockIdx.x) + 1) * p.M / G;
+    const int64_t count = flat_rowsum_windows(a, ra, rb);
+    auto win = [&](int64_t j) {
+        const RowWindow rw = rowsum_window(a, ra, rb, j);
+        return make_window(rw.e0 * p.esize, rw.e1 * p.esize, a.t_floor);
+    };
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0) produce_flat(a, sm, w, count, win);
+        return;
+    }
+    const int ctid = static_cast<int>(threadIdx.x) - 32;
+    const int lane = threadIdx.x & 31;
+    const int warp = ctid >> 5;
+    const int nthr = p.consumer_warps * 32;
+    constexpr int per = DT == MBT_F32 ? 4 : 8;      // elements per 16-byte chunk
+    const unsigned char *gsrc = reinterpret_cast<const unsigned char *>(a.src);
+    const unsigned char *stage_ptr0 = dyn_smem + (sm.base - smem_u32(dyn_smem));
+    // Chunked short-row path needs rows of at least one chunk (then a chunk
+    // touches at most two rows); shorter rows are summed element by element.
+    const bool chunked = a.rows_per_window > 0 && a.ld >= per;
+    FlushCtl f{smem_u32(&flush_bar), 0u};
+    float row_acc = 0.f;            // long rows: this thread's share of the current row
+    uint32_t stage = 0, phase = 0;
+    for (int64_t j = 0; j < count; ++j) {
+        bool ok = wait_bounded(sm.full0 + 8u * stage, phase, w, true);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            if (lane == 0) {
+                report_timeout(1, stage, phase);
+                *w.abort = 1;
+            }
+            break;
+        }
+        if (ctid == 0) log_record(p, 1, j, stage, phase, j);
+        const RowWindow rw = rowsum_window(a, ra, rb, j);
+        const Window wj = make_window(rw.e0 * p.esize, rw.e1 * p.esize, a.t_floor);
+        const int64_t we = wj.ws + wj.size;
+        const int chunks = static_cast<int>(wj.size >> 4);
+        const uint32_t sbase = sm.base + stage * p.stage_stride;
+        const int64_t g_ws = wj.ws / p.esize;        // element index of the window's first byte
+        if (chunked) {
+            // Phase 1: split every chunk into its first row's and next row's part.
+            const int buf = static_cast<int>(j & 1);
+            const int64_t row0_elem = rw.r0 * a.ld;
+            const int nrows = static_cast<int>(rw.r1 - rw.r0);
+            const uint32_t ld32 = static_cast<uint32_t>(a.ld);
+            const int n32 = static_cast<int>(p.N);
+            for (int c0 = 0; c0 < chunks; c0 += nthr * kFlatVec) {
+                uint4 v[kFlatVec];
+#pragma unroll
+                for (int u = 0; u < kFlatVec; ++u) {
+                    const int c = c0 + ctid + u * nthr;
+                    if (c < chunks) v[u] = lds128(sbase + 16u * c);
+                }
+                if (c0 + nthr * kFlatVec >= chunks) {
+                    __syncwarp();
+                    if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+                }
+#pragma unroll
+                for (int u = 0; u < kFlatVec; ++u) {
+                    const int c = c0 + ctid + u * nthr;
+                    if (c >= chunks) continue;
+                    // Element k of the chunk is element local0 + k counted from row
+                    // r0's start (the window is < 2^16 elements, so 32 bits do).
+                    const int local0 = static_cast<int>(g_ws - row0_elem) + c * per;
+                    const int fr = local0 >= 0 ? static_cast<int>(static_cast<uint32_t>(local0) / ld32)
+                                               : -1;            // row of element 0 (or before r0)
+                    const int kb = (fr + 1) * static_cast<int>(ld32) - local0;  // first k of row fr+1
+                    const int col0 = local0 - fr * static_cast<int>(ld32);      // column of element 0
+                    // row fr owns k in [0, a_end); row fr+1 owns k in [kb, b_end)
+                    const int a_end = (fr >= 0 && fr < nrows) ? min(kb, n32 - col0) : 0;
+                    const int b_end = (fr + 1 < nrows) ? kb + n32 : 0;
+                    const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                    float sa = 0.f, sb = 0.f;
+#pragma unroll
+                    for (int k = 0; k < per; ++k) {
+                        const uint32_t bits = DT == MBT_F32 ? wv[k & 3]
+                                                            : (wv[k >> 1] >> ((k & 1) * 16)) & 0xffffu;
+                        const float x = element_value<DT>(bits);
+                        if (k < a_end) sa += x;
+                        if (k >= kb && k < b_end) sb += x;
+                    }
+                    part[buf][0][c] = sa;
+                    part[buf][1][c] = sb;
+                }
+            }
+            if (chunks == 0) {
+                __syncwarp();
+                if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+            }
+            if (!consumers_sync(f, w)) break;
+            // Phase 2: one thread per row adds its chunks' parts in order.
+            const int64_t off0 = row0_elem * p.esize - wj.ws;   // row r0's start in the window
+            for (int lr = ctid; lr < nrows; lr += nthr) {
+                const int64_t rel0 = off0 + static_cast<int64_t>(lr) * a.ld * p.esize;
+                const int64_t rel1 = rel0 + p.N * p.esize;
+                const int64_t loaded_end = rel1 < wj.size ? rel1 : wj.size;
+                float s = 0.f;
+                if (loaded_end > rel0) {
+                    const int cs = static_cast<int>(rel0 >> 4);
+                    const int ce = static_cast<int>((loaded_end - 1) >> 4);
+                    for (int c = cs; c <= ce; ++c)
+                        s += (c == cs && (rel0 & 15) != 0) ? part[buf][1][c] : part[buf][0][c];
+                }
+                for (int64_t b = (loaded_end > rel0 ? loaded_end : rel0); b < rel1; b += p.esize)
+                    s += element_value<DT>(element_bits<DT>(gsrc + wj.ws + b));
+                a.out[rw.r0 + lr] = s;
+            }
+        } else if (a.rows_per_window > 0) {
+            // Rows shorter than one chunk: one thread per row, element by element.
+            const unsigned char *sp = stage_ptr0 + static_cast<size_t>(stage) * p.stage_stride;
+            for (int64_t r = rw.r0 + ctid; r < rw.r1; r += nthr) {
+                float s = 0.f;
+                const int64_t b0 = r * a.ld * p.esize;
+                for (int64_t i = 0; i < p.N; ++i) {
+                    const int64_t b = b0 + i * p.esize;
+                    const uint32_t bits = b < we ? element_bits<DT>(sp + (b - wj.ws))
+                                                 : element_bits<DT>(gsrc + b);
+                    s += element_value<DT>(bits);
+                }
+                a.out[r] = s;
+            }
+            __syncwarp();
+            if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+        } else {
+            // Long rows: the window is one piece of row r0; threads keep their
+            // share of the row across its pieces and reduce once per row.
+            for (int c0 = 0; c0 < chunks; c0 += nthr * kFlatVec) {
+                uint4 v[kFlatVec];
+#pragma unroll
+                for (int u = 0; u < kFlatVec; ++u) {
+                    const int c = c0 + ctid + u * nthr;
+                    if (c < chunks) v[u] = lds128(sbase + 16u * c);
+                }
+                if (c0 + nthr * kFlatVec >= chunks) {
+                    __syncwarp();
+                    if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+                }
+#pragma unroll
+                for (int u = 0; u < kFlatVec; ++u) {
+                    const int c = c0 + ctid + u * nthr;
+                    if (c >= chunks) continue;
+                    const int64_t g0 = g_ws + static_cast<int64_t>(c) * per;
+                    row_acc += (g0 >= rw.e0 && g0 + per <= rw.e1)
+                                   ? chunk_sum<DT>(v[u])
+                                   : masked_chunk_sum<DT>(v[u], g0, rw.e0, rw.e1);
+                }
+            }
+            if (chunks == 0) {
+                __syncwarp();
+                if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+            }
+            if (ctid == 0) {
+                // Elements past the array's last 16-byte boundary.
+                for (int64_t g = (we > rw.e0 * p.esize ? we / p.esize : rw.e0); g < rw.e1; ++g)
+                    row_acc += element_value<DT>(element_bits<DT>(gsrc + g * p.esize));
+            }
+            if (rw.piece == a.pieces_per_row - 1) {
+                float s = row_acc;
+                row_acc = 0.f;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+                const int buf = static_cast<int>(rw.r0 & 1);
+                if (lane == 0) red[buf][warp] = s;
+                if (!consumers_sync(f, w)) break;
+                if (ctid == 0) {
+                    float total = 0.f;
+                    for (int k = 0; k < p.consumer_warps; ++k) total += red[buf][k];
+                    a.out[rw.r0] = total;
+                }
+            }
+        }
+        if (++stage == static_cast<uint32_t>(p.stages)) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+}

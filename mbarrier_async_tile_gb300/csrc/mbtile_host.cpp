@@ -56,9 +56,12 @@ int64_t round_up(int64_t a, int64_t m) { return ceil_div(a, m) * m; }
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Checks that need no device.  Fills the effective row pitches.
+// *flat is set when the row pitch is not a multiple of 16 bytes and the
+// operation can still run (through the 1-D bulk-copy kernels).
 int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, int tile_m,
                int tile_n, int stages, int dtype, const mbt_opts &o, int64_t *ld_src,
-               int64_t *ld_dst) {
+               int64_t *ld_dst, bool *flat = nullptr) {
+    if (flat) *flat = false;
     const int es = esize_of(dtype);
     if (es == 0) return MBT_ERR_ARG;
     if (op != MBT_OP_COPY && op != MBT_OP_ROWSUM && op != MBT_OP_COPY_ROWSUM) return MBT_ERR_ARG;
@@ -94,9 +97,21 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
         return MBT_OK;
     }
     if (src == nullptr || dst == nullptr) return MBT_ERR_ARG;
-    if (!aligned16(src) || (*ld_src * es) % 16 != 0) return MBT_ERR_ALIGN;
-    if (writes_dst && (!aligned16(dst) || (*ld_dst * es) % 16 != 0)) return MBT_ERR_ALIGN;
+    if (!aligned16(src)) return MBT_ERR_ALIGN;
+    if (writes_dst && !aligned16(dst)) return MBT_ERR_ALIGN;
     if (op == MBT_OP_ROWSUM && (reinterpret_cast<uintptr_t>(dst) & 3u) != 0) return MBT_ERR_ALIGN;
+    const bool pitch_ok = (*ld_src * es) % 16 == 0 && (!writes_dst || (*ld_dst * es) % 16 == 0);
+    if (!pitch_ok) {
+        // Unaligned pitch: a row sum of any pitch, or a copy of a dense matrix
+        // into a dense matrix (one contiguous byte array), through 1-D bulk copies.
+        const bool flat_ok =
+            op == MBT_OP_ROWSUM ||
+            (op == MBT_OP_COPY && *ld_src == N && *ld_dst == N && o.store_mode == 0 &&
+             o.pipeline == 0);
+        if (!flat_ok) return MBT_ERR_ALIGN;
+        if (flat) *flat = true;
+        return MBT_OK;
+    }
     if (static_cast<uint64_t>(*ld_src) * es >= (1ull << 40)) return MBT_ERR_UNSUPPORTED;
     return MBT_OK;
 }
@@ -141,9 +156,44 @@ int consumer_warps_for(int op, int tile_m, const mbt_opts &o, int wanted_ctas) {
     return kDefaultConsumerWarps;
 }
 
+// Window schedule of the 1-D bulk-copy kernels (pure; shared by planning and launch).
+void flat_setup(int op, int64_t M, int64_t N, int64_t ld, int es, int tile_m, int tile_n,
+                mbt::FlatArgs *f) {
+    f->ld = ld;
+    f->total_bytes = M > 0 ? ((M - 1) * ld + N) * es : 0;
+    f->t_floor = f->total_bytes & ~int64_t(15);
+    f->cap_bytes = static_cast<int64_t>(tile_m) * tile_n * es;
+    // The flat row sum splits a window into at most 1024 16-byte chunks.
+    if (op == MBT_OP_ROWSUM) f->cap_bytes = std::min<int64_t>(f->cap_bytes, 16 * 1024);
+    f->rows_per_window = 0;
+    f->piece_elems = 0;
+    f->pieces_per_row = 0;
+    if (op == MBT_OP_ROWSUM) {
+        const int64_t row_bytes = N * es, pitch = ld * es, room = f->cap_bytes - 32;
+        if (room >= row_bytes) {
+            f->rows_per_window = (room - row_bytes) / pitch + 1;
+        } else {
+            const int64_t most = room / es;
+            f->pieces_per_row = ceil_div(N, most);
+            f->piece_elems = ceil_div(N, f->pieces_per_row);
+        }
+    }
+}
+
+int64_t flat_windows(int op, const mbt::FlatArgs &f, int64_t M, int64_t G) {
+    if (op == MBT_OP_COPY) return ceil_div(f.t_floor, f.cap_bytes);
+    int64_t n = 0;
+    for (int64_t b = 0; b < G; ++b) {
+        const int64_t rows = (b + 1) * M / G - b * M / G;
+        n += f.rows_per_window > 0 ? ceil_div(rows, f.rows_per_window)
+                                   : rows * f.pieces_per_row;
+    }
+    return n;
+}
+
 int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, int dtype,
               const mbt_opts &o, int num_sms, int smem_optin, int fit_per_sm,
-              int with_workspace, mbt_plan *plan) {
+              int with_workspace, mbt_plan *plan, bool flat = false) {
     if (plan == nullptr || num_sms < 1 || fit_per_sm < 1) return MBT_ERR_ARG;
     const int es = esize_of(dtype);
     std::memset(plan, 0, sizeof *plan);
@@ -170,7 +220,23 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     int64_t per_sm = std::min(wanted, fit_per_sm);
     int64_t cap = per_sm * num_sms;
     if (o.max_ctas) cap = std::min<int64_t>(cap, o.max_ctas);
+    plan->flat = flat ? 1 : 0;
     if (plan->num_tiles == 0) return MBT_OK;
+    if (flat) {
+        mbt::FlatArgs f{};
+        const int64_t ld = o.ld_src ? o.ld_src : N;
+        flat_setup(op, M, N, ld, es, tile_m, tile_n, &f);
+        int64_t G = 1;
+        if (op == MBT_OP_COPY) {
+            G = std::max<int64_t>(1, std::min<int64_t>(ceil_div(f.t_floor, f.cap_bytes), cap));
+        } else {
+            G = std::min<int64_t>(M, cap);
+        }
+        plan->grid = static_cast<int32_t>(G);
+        plan->num_tiles = flat_windows(op, f, M, G);
+        plan->kmax = 1;
+        return MBT_OK;
+    }
     if (op == MBT_OP_COPY) {
         plan->grid = static_cast<int32_t>(std::min<int64_t>(plan->num_tiles, cap));
         plan->kmax = 1;
@@ -253,16 +319,17 @@ int encode_map(CUtensorMap *map, const void *src, int64_t M, int64_t N, int64_t 
 
 // Plan for the current device (occupancy included).
 int plan_on_device(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, int dtype,
-                   const mbt_opts &o, int with_workspace, mbt_plan *plan) {
+                   const mbt_opts &o, int with_workspace, mbt_plan *plan, bool flat = false) {
     DeviceFigures d;
     int rc = device_figures(&d);
     if (rc != MBT_OK) return rc;
     rc = plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, d.num_sms, d.smem_optin, 1,
-                   with_workspace, plan);
+                   with_workspace, plan, flat);
     if (rc != MBT_OK) return rc;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MBT_ERR_CUDA;
-    const int kernel_id = op == MBT_OP_COPY && o.pipeline == 1 ? 3 : op;
+    const int kernel_id = flat ? (op == MBT_OP_COPY ? 4 : 5)
+                          : (op == MBT_OP_COPY && o.pipeline == 1 ? 3 : op);
     const auto key = std::make_tuple(dev, kernel_id, op != MBT_OP_COPY ? dtype : 0,
                                      plan->threads, plan->smem_bytes);
     int fit = 0;
@@ -280,8 +347,10 @@ int plan_on_device(int op, int64_t M, int64_t N, int tile_m, int tile_n, int sta
         g_fit_cache[key] = fit;
     }
     return plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, d.num_sms, d.smem_optin, fit,
-                     with_workspace, plan);
+                     with_workspace, plan, flat);
 }
+
+
 
 PipeArgs pipe_args(const mbt_plan &plan, int64_t M, int64_t N, int tile_m, int stages, int dtype,
                    const mbt_opts &o) {
@@ -311,6 +380,27 @@ mbt_opts opts_or_default(const mbt_opts *opts) {
     std::memset(&o, 0, sizeof o);
     if (opts) o = *opts;
     return o;
+}
+
+// Launch of the 1-D bulk-copy kernels (pitch not a multiple of 16 bytes).
+int flat_launch(int op, const void *src, void *dst, float *out, int64_t M, int64_t N, int64_t ld,
+                int tile_m, int tile_n, int stages, int dtype, void *stream, const mbt_opts &o) {
+    mbt_plan plan;
+    int rc = plan_on_device(op, M, N, tile_m, tile_n, stages, dtype, o, 0, &plan, true);
+    if (rc != MBT_OK) return rc;
+    mbt::FlatArgs f{};
+    f.p = pipe_args(plan, M, N, tile_m, stages, dtype, o);
+    f.src = static_cast<const char *>(src);
+    f.dst = static_cast<char *>(dst);
+    f.out = out;
+    flat_setup(op, M, N, ld, esize_of(dtype), tile_m, tile_n, &f);
+    const cudaError_t e =
+        op == MBT_OP_COPY
+            ? mbt::launch_copy_flat(f, plan.grid, plan.threads, plan.smem_bytes,
+                                    static_cast<cudaStream_t>(stream))
+            : mbt::launch_rowsum_flat(dtype, f, plan.grid, plan.threads, plan.smem_bytes,
+                                      static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
 }
 
 // Row sums (and, with dst != nullptr, the fused copy) after argument checks.
@@ -372,11 +462,12 @@ int workspace_bytes(int op, int64_t M, int64_t N, int tile_m, int tile_n, int st
     o.workspace_bytes = 0;
     int64_t ld_src = 0, ld_dst = 0;
     static const char dummy[16] __attribute__((aligned(16))) = {0};
+    bool flat = false;
     int rc = check_args(op, dummy, dummy, M, N, tile_m, tile_n, stages, dtype, o, &ld_src,
-                        &ld_dst);
+                        &ld_dst, &flat);
     if (rc != MBT_OK) return rc;
     *bytes = 0;
-    if (M == 0 || N == 0) return MBT_OK;
+    if (M == 0 || N == 0 || flat) return MBT_OK;   // flat row sums need no workspace
     mbt_plan plan;
     rc = plan_on_device(op, M, N, tile_m, tile_n, stages, dtype, o, 1, &plan);
     if (rc != MBT_OK) return rc;
@@ -395,20 +486,26 @@ int tile_plan(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     int64_t ld_src = 0, ld_dst = 0;
     // Shape checks only: pointers are not part of a plan.
     static const char dummy[16] __attribute__((aligned(16))) = {0};
-    int rc = check_args(op, dummy, dummy, M, N, tile_m, tile_n, stages, dtype, o, &ld_src, &ld_dst);
+    bool flat = false;
+    int rc = check_args(op, dummy, dummy, M, N, tile_m, tile_n, stages, dtype, o, &ld_src, &ld_dst,
+                        &flat);
     if (rc != MBT_OK) return rc;
     return plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, num_sms, smem_optin, fit_per_sm,
-                     with_workspace, plan);
+                     with_workspace, plan, flat);
 }
 
 int tile_copy_ex(const void *src, void *dst, int64_t M, int64_t N, int tile_m, int tile_n,
                  int stages, int dtype, void *stream, const mbt_opts *opts) {
     const mbt_opts o = opts_or_default(opts);
     int64_t ld_src = 0, ld_dst = 0;
+    bool flat = false;
     int rc = check_args(MBT_OP_COPY, src, dst, M, N, tile_m, tile_n, stages, dtype, o, &ld_src,
-                        &ld_dst);
+                        &ld_dst, &flat);
     if (rc != MBT_OK) return rc;
     if (M == 0 || N == 0) return MBT_OK;
+    if (flat)
+        return flat_launch(MBT_OP_COPY, src, dst, nullptr, M, N, ld_src, tile_m, tile_n, stages,
+                           dtype, stream, o);
     mbt_plan plan;
     rc = plan_on_device(MBT_OP_COPY, M, N, tile_m, tile_n, stages, dtype, o, 0, &plan);
     if (rc != MBT_OK) return rc;
@@ -444,9 +541,13 @@ int tile_rowsum_ex(const void *src, float *out, int64_t M, int64_t N, int tile_m
                    int stages, int dtype, void *stream, const mbt_opts *opts) {
     const mbt_opts o = opts_or_default(opts);
     int64_t ld_src = 0, ld_dst = 0;
+    bool flat = false;
     int rc = check_args(MBT_OP_ROWSUM, src, out, M, N, tile_m, tile_n, stages, dtype, o, &ld_src,
-                        &ld_dst);
+                        &ld_dst, &flat);
     if (rc != MBT_OK) return rc;
+    if (flat && M > 0 && N > 0)
+        return flat_launch(MBT_OP_ROWSUM, src, nullptr, out, M, N, ld_src, tile_m, tile_n, stages,
+                           dtype, stream, o);
     return rowsum_launch(src, nullptr, out, M, N, ld_src, 0, tile_m, tile_n, stages, dtype,
                          stream, o);
 }

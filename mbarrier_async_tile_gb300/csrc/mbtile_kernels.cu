@@ -774,6 +774,8 @@ __global__ void mbt_fill_zero_kernel(float *out, int64_t n) {
         out[i] = 0.f;
 }
 
+#include "mbtile_flat.cuh"
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -816,6 +818,22 @@ cudaError_t launch_copy_unified(const CUtensorMap &map, const CopyArgs &a, int g
     return cudaGetLastError();
 }
 
+cudaError_t launch_copy_flat(const FlatArgs &a, int grid, int threads, int smem,
+                             cudaStream_t stream) {
+    mbt_copy_flat_kernel<<<grid, threads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rowsum_flat(int dtype, const FlatArgs &a, int grid, int threads, int smem,
+                               cudaStream_t stream) {
+    switch (dtype) {
+        case MBT_F16: mbt_rowsum_flat_kernel<MBT_F16><<<grid, threads, smem, stream>>>(a); break;
+        case MBT_BF16: mbt_rowsum_flat_kernel<MBT_BF16><<<grid, threads, smem, stream>>>(a); break;
+        default: mbt_rowsum_flat_kernel<MBT_F32><<<grid, threads, smem, stream>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fill_zero(float *out, int64_t n, cudaStream_t stream) {
     const int threads = 256;
     const int64_t blocks64 = (n + threads - 1) / threads;
@@ -829,6 +847,10 @@ cudaError_t set_kernel_smem_limit(int optin, int *usable) {
     // the plan uses the smallest of these so that any kernel can launch it.
     const void *fns[] = {reinterpret_cast<const void *>(mbt_copy_kernel),
                          reinterpret_cast<const void *>(mbt_copy_unified_kernel),
+                         reinterpret_cast<const void *>(mbt_copy_flat_kernel),
+                         reinterpret_cast<const void *>(mbt_rowsum_flat_kernel<MBT_F16>),
+                         reinterpret_cast<const void *>(mbt_rowsum_flat_kernel<MBT_BF16>),
+                         reinterpret_cast<const void *>(mbt_rowsum_flat_kernel<MBT_F32>),
                          reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16, false>),
                          reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16, false>),
                          reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32, false>),
@@ -852,6 +874,11 @@ cudaError_t set_kernel_smem_limit(int optin, int *usable) {
 cudaError_t kernel_fit_per_sm(int op, int dtype, int threads, int smem, int *fit) {
     const void *fn = reinterpret_cast<const void *>(mbt_copy_kernel);
     if (op == 3) fn = reinterpret_cast<const void *>(mbt_copy_unified_kernel);
+    if (op == 4) fn = reinterpret_cast<const void *>(mbt_copy_flat_kernel);
+    if (op == 5)
+        fn = dtype == MBT_F16    ? reinterpret_cast<const void *>(mbt_rowsum_flat_kernel<MBT_F16>)
+             : dtype == MBT_BF16 ? reinterpret_cast<const void *>(mbt_rowsum_flat_kernel<MBT_BF16>)
+                                 : reinterpret_cast<const void *>(mbt_rowsum_flat_kernel<MBT_F32>);
     if (op == MBT_OP_ROWSUM)
         fn = dtype == MBT_F16    ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16, false>)
              : dtype == MBT_BF16 ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16, false>)

@@ -57,10 +57,29 @@ B = 0x20000
     ((A, B, -1, 64), -1),                        # negative M
     ((A + 8, B, 8, 64), -2),                     # misaligned src
     ((A, B + 2, 8, 64), -2),                     # misaligned dst
-    ((A, B, 8, 63), -2),                         # dense fp16 row of 126 bytes
 ])
 def test_copy_argument_errors(args, code):
     assert _copy(*args) == code
+
+
+def test_unaligned_pitch_routes_and_refusals():
+    # dense fp16 rows of 126 bytes: the 1-D bulk-copy path (no 2-D tensor map)
+    p = _plan(mbt.OP_COPY, 1000, 63, 128, 64, 3, torch.float16, fit=2)
+    assert p["flat"] == 1 and p["num_tiles"] == -(-(1000 * 63 * 2 // 16 * 16) // 16384)
+    p = _plan(mbt.OP_ROWSUM, 1000, 63, 128, 64, 3, torch.float16, fit=2, ws=True)
+    assert p["flat"] == 1 and p["workspace_bytes"] == 0 and p["grid"] == 304
+    # row sum with a pitch of 70 elements (140 bytes): allowed
+    assert _plan(mbt.OP_ROWSUM, 10, 63, 128, 64, 3, torch.float16, ld_src=70)["flat"] == 1
+    # copies whose src and dst are not both dense, or bulk-store / unified copies: refused
+    o = Opts(); o.ld_src = 70                    # 140-byte pitch, dst dense
+    assert _copy(A, B, 8, 63, opts=o) == -2
+    o = Opts(); o.store_mode = 1
+    assert _copy(A, B, 8, 63, opts=o) == -2
+    o = Opts(); o.pipeline = 1
+    assert _copy(A, B, 8, 63, opts=o) == -2
+    assert C.tile_copy_rowsum_ex(A, B, B, 8, 63, 128, 64, 3, 0, None, None) == -2
+    # aligned shapes keep the tiled path
+    assert _plan(mbt.OP_COPY, 1000, 64, 128, 64, 3, torch.float16)["flat"] == 0
 
 
 def test_copy_tile_and_stage_errors():

@@ -1,0 +1,97 @@
+"""GPU parity of the unaligned-pitch path (row pitch not a multiple of 16
+bytes, e.g. dense fp16 rows of 16383 elements): 1-D bulk copies of
+16-byte-aligned windows through the same mbarrier ring.  Copies bit-exact
+(dense src and dst; bytes past the matrix untouched), row sums at any pitch
+within 1e-5 of the binary64 oracle, short rows (several per stage) and long
+rows (pieces of a row per stage)."""
+import pytest
+import torch
+
+import mbarrier_async_tile_gb300 as mbt
+import oracle
+import synthetic
+from helpers import ROWSUM_RTOL, bits, rowsum_errors
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def setup():
+    mbt._build.build()
+    oracle.build()
+    torch.cuda.set_device(0)
+
+
+def dense_in_poisoned(dtype, M, N, extra=40):
+    """A dense (M, N) view at the start of a poisoned flat buffer, so writes
+    past the matrix's last byte are caught."""
+    es = synthetic.ESIZE[dtype]
+    flat = torch.empty(M * N + extra, dtype=synthetic.DTYPES[dtype])
+    synthetic.fill_bits(flat, synthetic.POISON_BITS[dtype])
+    return flat
+
+
+@pytest.mark.parametrize("dtype,M,N,tm,tn,st", [
+    ("f16", 1, 1, 128, 64, 2),          # 2 bytes: all tail
+    ("f16", 3, 5, 128, 64, 1),
+    ("f16", 1000, 63, 128, 64, 3),
+    ("bf16", 513, 4099, 64, 256, 2),
+    ("f32", 777, 8191, 128, 32, 4),
+    ("f16", 37, 16383, 128, 64, 3),
+])
+def test_flat_copy_matches_oracle(dtype, M, N, tm, tn, st):
+    src = synthetic.make_matrix(M, N, dtype, "uniform", seed=M + 7 * N)
+    assert (N * synthetic.ESIZE[dtype]) % 16 != 0 or M * N < 8
+    dflat = dense_in_poisoned(dtype, M, N)
+    want = dflat.clone()
+    oracle.copy(src, want[:M * N].view(M, N))
+    d = dflat.cuda()
+    mbt.tile_copy(src.cuda(), d[:M * N].view(M, N), tm, tn, st)
+    code, info = mbt.tile_status()
+    assert code == 0, info
+    assert torch.equal(bits(d.cpu()), bits(want))
+
+
+@pytest.mark.parametrize("dtype,dist,M,N,ld,tm,tn,st", [
+    ("f16", "uniform", 1000, 63, 63, 128, 64, 3),       # short rows, dense
+    ("f16", "normal", 300, 63, 70, 128, 64, 2),         # short rows, pitched (140 B)
+    ("bf16", "normal", 2000, 33, 33, 64, 256, 2),
+    ("f32", "uniform", 5, 3, 3, 128, 32, 1),
+    ("f16", "uniform", 501, 16383, 16383, 128, 64, 3),  # long rows: 3 pieces each
+    ("bf16", "normal", 40, 100003, 100003, 64, 256, 2),
+    ("f32", "normal", 123, 8191, 8191, 128, 32, 4),
+])
+def test_flat_rowsum_matches_oracle(dtype, dist, M, N, ld, tm, tn, st):
+    x = synthetic.make_matrix(M, N, dtype, dist, seed=M + N, ld=ld)
+    out = mbt.tile_rowsum(x.cuda()[:, :N], None, tm, tn, st)
+    code, info = mbt.tile_status()
+    assert code == 0, info
+    worst, rel, _ = rowsum_errors(out, x[:, :N])
+    assert worst <= ROWSUM_RTOL, (worst, rel)
+
+
+def test_flat_full_size_dense_ragged_configs():
+    """The ragged shapes of the task, stored dense (no pitch padding)."""
+    for dtype, M, N, tm, tn, seed in (("f32", 12289, 8191, 128, 32, 1005),
+                                      ("f16", 24577, 16383, 128, 64, 1006)):
+        x = synthetic.make_matrix(M, N, dtype, "uniform", seed)
+        xd = x.cuda()
+        y = torch.empty_like(xd)
+        mbt.tile_copy(xd, y, tm, tn, 3)
+        out = mbt.tile_rowsum(xd, None, tm, tn, 3)
+        assert mbt.tile_status()[0] == 0
+        assert torch.equal(bits(y.cpu()), bits(x))
+        assert rowsum_errors(out, x)[0] <= ROWSUM_RTOL
+
+
+@pytest.mark.parametrize("fault", [1, 2])
+def test_flat_stall_reports_timeout(fault):
+    x = synthetic.make_matrix(512, 1001, "f16", "uniform", seed=2).cuda()
+    y = torch.empty_like(x)
+    mbt.tile_copy(x, y, 128, 64, 3, max_ctas=4, fault=fault, wait_budget_ns=20_000_000)
+    assert mbt.tile_status()[0] == mbt.MBT_ERR_TIMEOUT
+    mbt.tile_rowsum(x, None, 128, 64, 3, max_ctas=4, fault=fault, wait_budget_ns=20_000_000)
+    assert mbt.tile_status()[0] == mbt.MBT_ERR_TIMEOUT
+    mbt.tile_copy(x, y, 128, 64, 3)
+    assert mbt.tile_status()[0] == 0
+    assert torch.equal(y.view(torch.int16), x.view(torch.int16))
