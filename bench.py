@@ -209,59 +209,92 @@ def bench_gpu(args, rank, world):
     torch.cuda.set_device(dev)
     mbt.tile_device_info()  # loads the library, fails loudly if it is missing
     x3, d3, x4, o4 = make_inputs(dev)
-    stream = torch.cuda.current_stream()
+    main = torch.cuda.current_stream()
     ws_bytes = mbt.tile_rowsum_workspace_bytes(ROWSUM["M"], ROWSUM["N"], ROWSUM["tile_m"],
                                                ROWSUM["tile_n"], args.rowsum_stages,
                                                torch.bfloat16)
     ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    side = (torch.cuda.Stream(), torch.cuda.Stream())
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        mbt.tile_copy(x3, d3, COPY["tile_m"], COPY["tile_n"], args.copy_stages,
-                      store_mode=args.store_mode, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        mbt.tile_rowsum(x4, o4, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
-                        workspace=ws, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
+    def run_pass(two_streams: bool, record: bool):
+        """Warm up, then time args.steps steps.  One stream: copy then row sum,
+        per-kernel events on it.  Two streams: each operation on its own
+        stream (independent calls, so one kernel's tail overlaps the next
+        one's start).  Returns (total ms, mean copy ms, mean rowsum ms)."""
+        s_copy, s_rowsum = side if two_streams else (main, main)
 
-    for _ in range(args.warmup):
-        step()
-    code, info = mbt.tile_status(stream)
-    if code != 0:
-        raise RuntimeError(f"pipeline status {code} {info}")
+        def step(ev=None):
+            if ev is not None:
+                ev[0].record(s_copy)
+            mbt.tile_copy(x3, d3, COPY["tile_m"], COPY["tile_n"], args.copy_stages,
+                          store_mode=args.store_mode, stream=s_copy)
+            if ev is not None:
+                ev[1].record(s_copy)
+                ev[2].record(s_rowsum)
+            mbt.tile_rowsum(x4, o4, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
+                            workspace=ws, stream=s_rowsum)
+            if ev is not None:
+                ev[3].record(s_rowsum)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        def fork():
+            s_copy.wait_stream(main)
+            s_rowsum.wait_stream(main)
+
+        def join():
+            main.wait_stream(s_copy)
+            main.wait_stream(s_rowsum)
+
+        fork()
+        for _ in range(args.warmup):
+            step()
+        join()
+        code, info = mbt.tile_status(main)
+        if code != 0:
+            raise RuntimeError(f"pipeline status {code} {info}")
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+               for _ in range(args.steps)] if record else [None] * args.steps
+        barrier(world)
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(main)
+        fork()
+        for k in range(args.steps):
+            step(evs[k])
+        join()
+        end.record(main)
+        torch.cuda.synchronize()
+        barrier(world)
+        code, info = mbt.tile_status(main)
+        if code != 0:
+            raise RuntimeError(f"pipeline status {code} {info}")
+        ms_c = ms_r = None
+        if record:
+            ms_c = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+            ms_r = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+        return start.elapsed_time(end), ms_c, ms_r
+
     clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.time()
-    start.record(stream)
-    for k in range(args.steps):
-        step(evs[k])
-    end.record(stream)
-    torch.cuda.synchronize()
+    # sequential pass: per-kernel durations for the roofline
+    ms_seq, ms_copy, ms_rowsum = run_pass(False, True)
+    # the headline pass
+    if args.streams == 2:
+        ms_total, _, _ = run_pass(True, False)
+    else:
+        ms_total = ms_seq
     t1 = time.time()
-    barrier(world)
     time.sleep(0.15)
     clocks.stop()
-    code, info = mbt.tile_status(stream)
-    if code != 0:
-        raise RuntimeError(f"pipeline status {code} {info}")
-
-    ms_total = start.elapsed_time(end)
-    ms_copy = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
-    ms_rowsum = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    step_bytes = copy_bytes() + rowsum_bytes()
+    value_one_stream = aggregate_gbs(step_bytes, args.steps, world, reduce_max(ms_seq, world))
     ms_max = reduce_max(ms_total, world)
-    value = aggregate_gbs(copy_bytes() + rowsum_bytes(), args.steps, world, ms_max)
+    value = aggregate_gbs(step_bytes, args.steps, world, ms_max)
 
     # end to end through the public API with host buffers
-    e2e = bench_e2e(args, mbt, x3, x4, ws, stream, world)
+    e2e = bench_e2e(args, mbt, x3, x4, ws,
+                    (side[0], side[1], main) if args.streams == 2 else (main, main, main), world)
 
     peak, peak_kind = measured_peak()
     kernels = {
@@ -281,7 +314,9 @@ def bench_gpu(args, rank, world):
     roofline = {"bound": "hbm", "kernel": f"mbt_{dom_name}_kernel",
                 "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": round(dom["gbs"] / peak, 4), "traffic": traffic,
-                "peak_source": f"{peak_kind} hbm_gbs (copy read+write)"}
+                "peak_source": f"{peak_kind} hbm_gbs (copy read+write)",
+                "timing": "per-kernel CUDA events on the launching stream, sequential pass "
+                          "(in the two-stream pass the kernels share the DRAM)"}
     out = {
         "metric": "achieved HBM GB/s (read+write) for pipelined tile copy + rowsum",
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -292,9 +327,13 @@ def bench_gpu(args, rank, world):
                                 "bf16 8192x65536 tile 64x256"),
                    "copy_stages": args.copy_stages, "rowsum_stages": args.rowsum_stages,
                    "copy_store_mode": args.store_mode,
+                   "streams": ("copy and rowsum each on its own stream (independent calls, "
+                               "so the kernels overlap); value_one_stream: both on one stream"
+                               if args.streams == 2 else "one stream"),
                    "l2": "inputs (512 MiB, 1 GiB) larger than L2; no flush",
                    "parallelism": f"independent replica per GPU x{world}"},
         "frac_of_peak": round(value / world / peak, 4),
+        "value_one_stream": round(value_one_stream, 1),
         "kernels": kernels,
         "roofline": roofline,
         "e2e": e2e,
@@ -306,10 +345,11 @@ def bench_gpu(args, rank, world):
     return out
 
 
-def bench_e2e(args, mbt, x3, x4, ws, stream, world):
+def bench_e2e(args, mbt, x3, x4, ws, streams, world):
     """Same metric, through the public API, with host buffers: every step
     copies the inputs from pinned host memory, runs both calls and reads the
-    results back."""
+    results back (each operation's copies and kernel on its own stream)."""
+    s_copy, s_rowsum, main = streams
     steps = max(1, min(args.steps, args.e2e_steps))
     h3 = torch.empty(x3.shape, dtype=x3.dtype, pin_memory=True)
     h3.copy_(x3)
@@ -320,72 +360,38 @@ def bench_e2e(args, mbt, x3, x4, ws, stream, world):
     g3, g3o = torch.empty_like(x3), torch.empty_like(x3)
     g4, g4o = torch.empty_like(x4), torch.empty(x4.shape[0], dtype=torch.float32,
                                                 device=x4.device)
+    torch.cuda.synchronize()
 
     def step():
-        g3.copy_(h3, non_blocking=True)
-        mbt.tile_copy(g3, g3o, COPY["tile_m"], COPY["tile_n"], args.copy_stages,
-                      store_mode=args.store_mode, stream=stream)
-        r3.copy_(g3o, non_blocking=True)
-        g4.copy_(h4, non_blocking=True)
-        mbt.tile_rowsum(g4, g4o, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
-                        workspace=ws, stream=stream)
-        r4.copy_(g4o, non_blocking=True)
+        with torch.cuda.stream(s_copy):
+            g3.copy_(h3, non_blocking=True)
+            mbt.tile_copy(g3, g3o, COPY["tile_m"], COPY["tile_n"], args.copy_stages,
+                          store_mode=args.store_mode, stream=s_copy)
+            r3.copy_(g3o, non_blocking=True)
+        with torch.cuda.stream(s_rowsum):
+            g4.copy_(h4, non_blocking=True)
+            mbt.tile_rowsum(g4, g4o, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
+                            workspace=ws, stream=s_rowsum)
+            r4.copy_(g4o, non_blocking=True)
 
     step()
     torch.cuda.synchronize()
     barrier(world)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
+    s.record(main)
+    s_copy.wait_stream(main)
+    s_rowsum.wait_stream(main)
     for _ in range(steps):
         step()
-    e.record(stream)
+    main.wait_stream(s_copy)
+    main.wait_stream(s_rowsum)
+    e.record(main)
     torch.cuda.synchronize()
     ms = reduce_max(s.elapsed_time(e), world)
     value = aggregate_gbs(copy_bytes() + rowsum_bytes(), steps, world, ms)
     return {"value": round(value, 1), "unit": "GB/s", "steps": steps,
             "h2d_bytes_per_step": h3.numel() * h3.element_size() + h4.numel() * h4.element_size(),
             "d2h_bytes_per_step": r3.numel() * r3.element_size() + r4.numel() * r4.element_size()}
-
-
-def bench_only(args):
-    """Run one kernel ``args.steps`` times on the first ``args.rows`` rows of
-    its workload (for profiling a smaller case under ncu), and print its GB/s."""
-    import mbarrier_async_tile_gb300 as mbt
-    import synthetic
-
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    c = COPY if args.only == "copy" else ROWSUM
-    rows = min(args.rows or c["M"], c["M"])
-    x = synthetic.make_matrix(rows, c["N"], c["dtype"], c["dist"], c["seed"], draw_on=str(dev))
-    if args.only == "copy":
-        y = torch.empty_like(x)
-        fn = lambda: mbt.tile_copy(x, y, c["tile_m"], c["tile_n"], args.copy_stages,  # noqa: E731
-                                   consumer_warps=args.consumer_warps,
-                                   ctas_per_sm=args.ctas_per_sm, store_mode=args.store_mode)
-        nbytes = 2 * x.numel() * x.element_size()
-    else:
-        y = torch.empty(rows, dtype=torch.float32, device=dev)
-        ws = torch.zeros(1 << 22, dtype=torch.uint8, device=dev)
-        fn = lambda: mbt.tile_rowsum(x, y, c["tile_m"], c["tile_n"], args.rowsum_stages,  # noqa: E731
-                                     consumer_warps=args.consumer_warps,
-                                     ctas_per_sm=args.ctas_per_sm, workspace=ws)
-        nbytes = x.numel() * x.element_size() + 4 * rows
-    for _ in range(args.warmup):
-        fn()
-    torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(args.steps):
-        fn()
-    e.record()
-    torch.cuda.synchronize()
-    code, info = mbt.tile_status()
-    if code != 0:
-        raise RuntimeError(f"pipeline status {code} {info}")
-    ms = s.elapsed_time(e) / args.steps
-    print(json.dumps({"only": args.only, "rows": rows, "ms": round(ms, 4),
-                      "gbs": round(nbytes / ms / 1e6, 1)}), flush=True)
 
 
 def bench_configs(args):
@@ -624,6 +630,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mbtile", "reference"], default="mbtile")
+    ap.add_argument("--streams", type=int, default=2, choices=[1, 2])
     ap.add_argument("--copy-stages", type=int, default=3)
     ap.add_argument("--rowsum-stages", type=int, default=2)
     ap.add_argument("--e2e-steps", type=int, default=5)
