@@ -40,8 +40,8 @@ FALLBACK_HBM_GBS = 6800.0
 # of each kernel on the full-size workload, keyed by the SHA-256 of the kernel
 # source it was taken on; reported only while the source is unchanged.
 NCU_TRAFFIC: dict = {
-    "copy": {"src_sha": "7403ea850626a692", "bytes_per_launch": 536966912 + 485191936},
-    "rowsum": {"src_sha": "7403ea850626a692", "bytes_per_launch": 1073857024 + 3035136},
+    "copy": {"src_sha": "c076ca3ec5cb0be1", "bytes_per_launch": 536959232 + 484882176},
+    "rowsum": {"src_sha": "c076ca3ec5cb0be1", "bytes_per_launch": 1073833216 + 3353088},
 }
 
 
@@ -55,7 +55,7 @@ def rowsum_bytes(c=ROWSUM):
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for f in ("mbtile_kernels.cu", "internal.h"):
+    for f in ("mbtile_kernels.cu", "mbtile_flat.cuh", "internal.h"):
         with open(os.path.join(ROOT, "mbarrier_async_tile_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -394,6 +394,55 @@ def bench_e2e(args, mbt, x3, x4, ws, streams, world):
             "d2h_bytes_per_step": r3.numel() * r3.element_size() + r4.numel() * r4.element_size()}
 
 
+def bench_only(args):
+    """Run one kernel ``args.steps`` times on the first ``args.rows`` rows of
+    its workload (for profiling a smaller case under ncu), and print its GB/s."""
+    import mbarrier_async_tile_gb300 as mbt
+    import synthetic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    c = ROWSUM if args.only == "rowsum" else COPY
+    rows = min(args.rows or c["M"], c["M"])
+    cols = c["N"] - args.trim_cols
+    x = synthetic.make_matrix(rows, cols, c["dtype"], c["dist"], c["seed"], draw_on=str(dev))
+    if args.only == "copy_rowsum":
+        y = torch.empty_like(x)
+        o = torch.empty(rows, dtype=torch.float32, device=dev)
+        ws = torch.zeros(1 << 22, dtype=torch.uint8, device=dev)
+        fn = lambda: mbt.tile_copy_rowsum(x, y, o, c["tile_m"], c["tile_n"],  # noqa: E731
+                                          args.copy_stages, workspace=ws)
+        nbytes = 2 * x.numel() * x.element_size() + 4 * rows
+    elif args.only == "copy":
+        y = torch.empty_like(x)
+        fn = lambda: mbt.tile_copy(x, y, c["tile_m"], c["tile_n"], args.copy_stages,  # noqa: E731
+                                   consumer_warps=args.consumer_warps,
+                                   ctas_per_sm=args.ctas_per_sm, store_mode=args.store_mode)
+        nbytes = 2 * x.numel() * x.element_size()
+    else:
+        y = torch.empty(rows, dtype=torch.float32, device=dev)
+        ws = torch.zeros(1 << 22, dtype=torch.uint8, device=dev)
+        fn = lambda: mbt.tile_rowsum(x, y, c["tile_m"], c["tile_n"], args.rowsum_stages,  # noqa: E731
+                                     consumer_warps=args.consumer_warps,
+                                     ctas_per_sm=args.ctas_per_sm, workspace=ws)
+        nbytes = x.numel() * x.element_size() + 4 * rows
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    code, info = mbt.tile_status()
+    if code != 0:
+        raise RuntimeError(f"pipeline status {code} {info}")
+    ms = s.elapsed_time(e) / args.steps
+    print(json.dumps({"only": args.only, "rows": rows, "cols": cols, "ms": round(ms, 4),
+                      "gbs": round(nbytes / ms / 1e6, 1)}), flush=True)
+
+
 def bench_configs(args):
     """One line per configuration of the task's table: latency for the two
     lesson shapes, GB/s (algorithmic bytes / device time) for the streaming
@@ -638,7 +687,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--all-configs", action="store_true")
-    ap.add_argument("--only", choices=["copy", "rowsum"])
+    ap.add_argument("--only", choices=["copy", "rowsum", "copy_rowsum"])
+    ap.add_argument("--trim-cols", type=int, default=0,
+                    help="--only: drop this many columns (an odd count gives a dense matrix "
+                         "whose rows are not a multiple of 16 bytes: the 1-D bulk-copy path)")
     ap.add_argument("--store-mode", type=int, default=0, choices=[0, 1])
     ap.add_argument("--rows", type=int, default=0)
     ap.add_argument("--consumer-warps", type=int, default=0)

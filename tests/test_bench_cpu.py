@@ -30,3 +30,10 @@ def test_warmup_below_three_is_refused():
                           "--steps", "1", "--warmup", "2"], capture_output=True, text=True,
                          timeout=300, cwd=ROOT)
     assert res.returncode != 0
+
+
+def test_every_mode_has_its_function():
+    import bench
+    for name in ("bench_gpu", "bench_e2e", "bench_only", "bench_configs", "bench_sweep",
+                 "bench_reference", "cpu_baseline", "aggregate_gbs"):
+        assert callable(getattr(bench, name, None)), name
