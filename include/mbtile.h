@@ -280,6 +280,21 @@ int tile_plan(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages,
               int dtype, const mbt_opts *opts, int num_sms, int smem_optin,
               int fit_per_sm, int with_workspace, mbt_plan *plan);
 
+/*
+ * tile_stage_image -- debug: the raw shared-memory image of one staged tile.
+ *
+ * Loads tile (tile_row, tile_col) of src (M x N, row pitch ld elements, which
+ * must be a multiple of 16 bytes) exactly as the pipelines do -- one 2-D bulk
+ * tensor copy per 128-byte box with the 128-byte swizzle, completion counted
+ * on an mbarrier -- and writes the stage's bytes to the device buffer `image`
+ * (boxes x tile_m x 128 bytes, box after box, unswizzling nothing).  Used to
+ * check the swizzle against "cute(11) Hopper TMA copy" §2.2.  One CTA, 1 KB
+ * of slack plus the tile in shared memory.
+ */
+int tile_stage_image(const void *src, int64_t M, int64_t N, int64_t ld, int tile_m,
+                     int tile_n, int dtype, int64_t tile_row, int64_t tile_col,
+                     void *image, void *stream);
+
 /* Synchronises `stream`, then reads and clears the current device's status
  * word.  info (may be NULL) receives {code, block, stage, role * 2 + parity}
  * of the first wait that timed out (role 0 = producer, 1 = consumer).

@@ -22,7 +22,7 @@ __all__ = [
     "MbtError", "C", "library_path", "tile_copy", "tile_rowsum", "tile_status",
     "tile_plan", "tile_device_info", "tile_strerror", "tile_rowsum_workspace_bytes",
     "Opts", "Plan", "DTYPE_CODE", "OP_COPY", "OP_ROWSUM", "tile_rowsum_noalloc",
-    "tile_copy_rowsum",
+    "tile_copy_rowsum", "tile_stage_image",
 ]
 
 MBT_OK = 0
@@ -308,6 +308,24 @@ def tile_copy_rowsum(src: torch.Tensor, dst: torch.Tensor, out: torch.Tensor | N
                                      _stream_handle(stream), ctypes.byref(o))
     _check(rc, "tile_copy_rowsum")
     return out
+
+
+def tile_stage_image(src: torch.Tensor, tile_m: int, tile_n: int, tile_row: int = 0,
+                     tile_col: int = 0, stream=None) -> torch.Tensor:
+    """Raw shared-memory bytes of one staged tile (debug; see include/mbtile.h)."""
+    lib = _load()
+    fn = lib.tile_stage_image
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                   ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    M, N, ld = _matrix(src, "src")
+    boxes = tile_n * src.element_size() // 128
+    image = torch.zeros(boxes * tile_m * 128, dtype=torch.uint8, device=src.device)
+    rc = fn(src.data_ptr(), M, N, ld, tile_m, tile_n, DTYPE_CODE[src.dtype], tile_row, tile_col,
+            image.data_ptr(), _stream_handle(stream))
+    _check(rc, "tile_stage_image")
+    return image
 
 
 def tile_status(stream=None) -> tuple[int, list[int]]:

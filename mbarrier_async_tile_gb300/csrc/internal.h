@@ -90,6 +90,9 @@ cudaError_t launch_copy_flat(const FlatArgs &a, int grid, int threads, int smem,
                              cudaStream_t stream);
 cudaError_t launch_rowsum_flat(int dtype, const FlatArgs &a, int grid, int threads, int smem,
                                cudaStream_t stream);
+cudaError_t launch_stage_image(const CUtensorMap &map, int32_t row0, int32_t col0, int32_t boxes,
+                               int32_t box_inner, uint32_t box_bytes, uint32_t box_stride,
+                               unsigned char *image, cudaStream_t stream);
 cudaError_t launch_fill_zero(float *out, int64_t n, cudaStream_t stream);
 // Raise every kernel's dynamic shared-memory limit as far as the device's
 // opt-in limit allows; `usable` receives the limit common to all kernels.

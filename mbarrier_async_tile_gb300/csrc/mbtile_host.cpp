@@ -587,6 +587,37 @@ int tile_copy_rowsum_workspace_bytes(int64_t M, int64_t N, int tile_m, int tile_
     return workspace_bytes(MBT_OP_COPY_ROWSUM, M, N, tile_m, tile_n, stages, dtype, opts, bytes);
 }
 
+int tile_stage_image(const void *src, int64_t M, int64_t N, int64_t ld, int tile_m, int tile_n,
+                     int dtype, int64_t tile_row, int64_t tile_col, void *image, void *stream) {
+    mbt_opts o;
+    std::memset(&o, 0, sizeof o);
+    o.ld_src = ld;
+    int64_t ld_src = 0, ld_dst = 0;
+    bool flat = false;
+    int rc = check_args(MBT_OP_ROWSUM, src, image, M, N, tile_m, tile_n, 1, dtype, o, &ld_src,
+                        &ld_dst, &flat);
+    if (rc != MBT_OK) return rc;
+    if (flat || M == 0 || N == 0 || image == nullptr) return MBT_ERR_ARG;
+    if (tile_row < 0 || tile_col < 0 || tile_row * tile_m >= M || tile_col * tile_n >= N)
+        return MBT_ERR_ARG;
+    const int es = esize_of(dtype);
+    const int boxes = tile_n * es / mbt::kBoxRowBytes;
+    const uint32_t box_bytes = static_cast<uint32_t>(tile_m) * mbt::kBoxRowBytes;
+    const uint32_t box_stride = static_cast<uint32_t>(round_up(box_bytes, mbt::kSwizzleAtomBytes));
+    DeviceFigures d;
+    rc = device_figures(&d);
+    if (rc != MBT_OK) return rc;
+    if (static_cast<int64_t>(boxes) * box_stride + 1024 > d.smem_optin) return MBT_ERR_SMEM;
+    alignas(64) CUtensorMap map;
+    rc = encode_map(&map, src, M, N, ld_src, dtype, tile_m);
+    if (rc != MBT_OK) return rc;
+    const cudaError_t e = mbt::launch_stage_image(
+        map, static_cast<int32_t>(tile_row * tile_m), static_cast<int32_t>(tile_col * tile_n),
+        boxes, mbt::kBoxRowBytes / es, box_bytes, box_stride, static_cast<unsigned char *>(image),
+        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
+}
+
 int tile_status(void *stream, int32_t info[4]) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MBT_ERR_CUDA;
     int32_t local[4];

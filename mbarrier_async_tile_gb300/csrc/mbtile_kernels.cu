@@ -776,6 +776,41 @@ __global__ void mbt_fill_zero_kernel(float *out, int64_t n) {
 
 #include "mbtile_flat.cuh"
 
+// Debug: one CTA loads tile (row0, col0) exactly as the pipelines do (one
+// bulk tensor copy per 128-byte box, completion on an mbarrier with the
+// tile's bytes registered) and writes the stage's raw shared-memory bytes,
+// box after box, to `image` -- the swizzled layout the copy engine produced.
+__global__ void mbt_stage_image_kernel(const __grid_constant__ CUtensorMap map, int32_t row0,
+                                       int32_t col0, int32_t boxes, int32_t box_inner,
+                                       uint32_t box_bytes, uint32_t box_stride,
+                                       uint64_t budget_ns, unsigned char *image) {
+    extern __shared__ __align__(1024) unsigned char dyn_smem[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    const uint32_t base = (smem_u32(dyn_smem) + 1023u) & ~1023u;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(b, box_bytes * boxes);
+        for (int k = 0; k < boxes; ++k)
+            tma_load_2d(base + k * box_stride, &map, col0 + k * box_inner, row0, b);
+    }
+    WaitCtl w{budget_ns, &abort_flag};
+    const bool ok = wait_bounded(b, 0, w, false);
+    if (!ok && threadIdx.x == 0) report_timeout(1, 0, 0);
+    const unsigned char *stage = dyn_smem + (base - smem_u32(dyn_smem));
+    if (ok)
+        for (uint32_t i = threadIdx.x; i < box_bytes * boxes; i += blockDim.x) {
+            const uint32_t k = i / box_bytes, off = i - k * box_bytes;
+            image[i] = stage[k * box_stride + off];
+        }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -831,6 +866,18 @@ cudaError_t launch_rowsum_flat(int dtype, const FlatArgs &a, int grid, int threa
         case MBT_BF16: mbt_rowsum_flat_kernel<MBT_BF16><<<grid, threads, smem, stream>>>(a); break;
         default: mbt_rowsum_flat_kernel<MBT_F32><<<grid, threads, smem, stream>>>(a); break;
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stage_image(const CUtensorMap &map, int32_t row0, int32_t col0, int32_t boxes,
+                               int32_t box_inner, uint32_t box_bytes, uint32_t box_stride,
+                               unsigned char *image, cudaStream_t stream) {
+    const int smem = static_cast<int>(boxes * box_stride + 1024);
+    cudaError_t e = cudaFuncSetAttribute(mbt_stage_image_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    mbt_stage_image_kernel<<<1, 128, smem, stream>>>(map, row0, col0, boxes, box_inner, box_bytes,
+                                                     box_stride, kDefaultWaitBudgetNs, image);
     return cudaGetLastError();
 }
 
