@@ -21,7 +21,7 @@ from . import _build
 __all__ = [
     "MbtError", "C", "library_path", "tile_copy", "tile_rowsum", "tile_status",
     "tile_plan", "tile_device_info", "tile_strerror", "tile_rowsum_workspace_bytes",
-    "Opts", "Plan", "DTYPE_CODE", "OP_COPY", "OP_ROWSUM", "tile_rowsum_noalloc",
+    "Opts", "Plan", "DTYPE_CODE", "OP_COPY", "OP_ROWSUM", "OP_COPY_ROWSUM", "tile_rowsum_noalloc",
     "tile_copy_rowsum", "tile_stage_image",
 ]
 

@@ -80,7 +80,6 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
     if (o.pipeline == 1 && op != MBT_OP_COPY) return MBT_ERR_ARG;
     if (o.pipeline == 1 && o.store_mode != 0) return MBT_ERR_UNSUPPORTED;
     if (o.store_mode != 0 && op != MBT_OP_COPY) return MBT_ERR_ARG;
-    (void)writes_dst;
     for (int r : o.reserved)
         if (r != 0) return MBT_ERR_ARG;
     if (o.log != nullptr && o.log_capacity == 0) return MBT_ERR_ARG;

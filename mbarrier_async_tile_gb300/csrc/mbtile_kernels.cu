@@ -21,6 +21,13 @@
 // records MBT_ERR_TIMEOUT in g_status, raises a CTA-local abort flag that makes
 // the CTA's other waits give up early, and the producer then waits (again
 // bounded) for the bulk copies it still has in flight before the CTA exits.
+//
+// Kernels: mbt_copy_kernel (LSU stores, or bulk tensor stores from one
+// consumer warp), mbt_copy_unified_kernel (no warp specialisation; a CTA
+// barrier releases each stage), mbt_rowsum_kernel<dtype, fused> (row sums;
+// fused adds a store warp that also writes the tile out), and, in
+// mbtile_flat.cuh, the 1-D bulk-copy kernels for row pitches that are not a
+// multiple of 16 bytes.
 #include <cuda_fp16.h>
 
 #include "internal.h"

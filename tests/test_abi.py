@@ -238,3 +238,28 @@ def test_plan_rowsum_split_covers_every_tile_once(M, N, tm, tn, dt, sms, fit):
     assert p["kmax"] == kmax
     bands = p["tiles_m"]
     assert p["workspace_bytes"] == ((bands * 4 + 255) // 256) * 256 + bands * kmax * tm * 4
+
+
+def test_ctypes_mirrors_match_the_c_structs(tmp_path):
+    """Sizes and field offsets of mbt_opts / mbt_plan as the C compiler lays
+    them out, against the binding's ctypes mirrors."""
+    import subprocess
+    fields = {"mbt_opts": [n for n, _ in Opts._fields_],
+              "mbt_plan": [n for n, _ in mbt.Plan._fields_]}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "mbtile.h"', "int main(void) {"]
+    for struct, names in fields.items():
+        lines.append(f'printf("{struct} %zu\\n", sizeof({struct}));')
+        for n in names:
+            lines.append(f'printf("{struct}.{n} %zu\\n", offsetof({struct}, {n}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                    str(exe)], check=True)
+    out = dict(l.split() for l in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                 check=True).stdout.splitlines())
+    for struct, cls in (("mbt_opts", Opts), ("mbt_plan", mbt.Plan)):
+        assert int(out[struct]) == ctypes.sizeof(cls), struct
+        for n, _ in cls._fields_:
+            assert int(out[f"{struct}.{n}"]) == getattr(cls, n).offset, (struct, n)
