@@ -25,6 +25,7 @@ constexpr int kDefaultConsumerWarps = 4;         // copy
 // the store in progress, so it does not count.
 constexpr int64_t kCopyBytesPerSm = 64 * 1024;
 constexpr int64_t kRowsumBytesPerSm = 128 * 1024;
+constexpr int64_t kFlatRowsumWindowBytes = 16 * 1024;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxCoord = 0x7fffffff;  // bulk-copy coordinates are int32
 
@@ -163,7 +164,7 @@ void flat_setup(int op, int64_t M, int64_t N, int64_t ld, int es, int tile_m, in
     f->t_floor = f->total_bytes & ~int64_t(15);
     f->cap_bytes = static_cast<int64_t>(tile_m) * tile_n * es;
     // The flat row sum splits a window into at most 1024 16-byte chunks.
-    if (op == MBT_OP_ROWSUM) f->cap_bytes = std::min<int64_t>(f->cap_bytes, 16 * 1024);
+    if (op == MBT_OP_ROWSUM) f->cap_bytes = std::min<int64_t>(f->cap_bytes, kFlatRowsumWindowBytes);
     f->rows_per_window = 0;
     f->piece_elems = 0;
     f->pieces_per_row = 0;
@@ -202,6 +203,14 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     const int64_t box_stride = round_up(static_cast<int64_t>(tile_m) * mbt::kBoxRowBytes,
                                         mbt::kSwizzleAtomBytes);
     plan->stage_bytes = static_cast<int32_t>(plan->boxes * box_stride);
+    if (flat && op == MBT_OP_ROWSUM) {
+        // The flat row sum's windows hold at most 16 KB (its chunk bookkeeping
+        // is sized for 1024 chunks): stages of that size, and a grid sized by
+        // what they really keep in flight.
+        plan->stage_bytes = static_cast<int32_t>(
+            round_up(std::min<int64_t>(plan->stage_bytes, kFlatRowsumWindowBytes),
+                     mbt::kSwizzleAtomBytes));
+    }
     const int wanted = wanted_ctas_per_sm(op, o, stages, plan->stage_bytes);
     const int W = consumer_warps_for(op, tile_m, o, wanted);
     if (op != MBT_OP_COPY && W * 32 < tile_m) return MBT_ERR_UNSUPPORTED;
