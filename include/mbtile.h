@@ -128,7 +128,15 @@ typedef struct mbt_opts {
                                 barrier releases a stage ("CUDA features 10:
                                 Pipelines" §4.10.7 prologue / steady state /
                                 epilogue).  Kept as a measured comparison
-                                point; consumer_warps counts all warps. */
+                                point; consumer_warps counts all warps.
+                                tile_rowsum only (same sums, bit for bit):
+                                2: one full/empty pair per stage;
+                                3: a pair per 128-byte box of a stage
+                                wherever the tile allows it (see
+                                mbt_plan.box_barriers); 0 chooses 3 for at
+                                most 2 stages, else 2 (per-box pairs gain at
+                                2 stages and lose at 3 on the bf16 64 x 256
+                                row sum). */
     int32_t reserved[6];     /* must be 0 */
 } mbt_opts;
 
@@ -148,6 +156,16 @@ typedef struct mbt_plan {
     int32_t flat;            /* 1: row pitch not a multiple of 16 bytes; the
                                 1-D bulk-copy kernels run, num_tiles counts
                                 their windows */
+    int32_t box_barriers;    /* row sum: 1 if every 128-byte box of a stage
+                                has its own full/empty barrier pair, so the
+                                consumer warps of one box start on it, and
+                                release it, independently of the other boxes.
+                                Possible when each consumer warp reads a
+                                single box: 32 x consumer_warps = tile_m x
+                                tpr with tpr a multiple of boxes and tile_m x
+                                tpr / boxes a multiple of 32; see
+                                mbt_opts.pipeline for when it is chosen */
+    int32_t reserved0;
     int64_t tiles_m;         /* tiles down the rows (row bands) */
     int64_t tiles_n;         /* tiles across the columns */
     int64_t num_tiles;

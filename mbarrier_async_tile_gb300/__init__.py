@@ -66,6 +66,8 @@ class Plan(ctypes.Structure):
         ("split", ctypes.c_int32),
         ("kmax", ctypes.c_int32),
         ("flat", ctypes.c_int32),
+        ("box_barriers", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
         ("tiles_m", ctypes.c_int64),
         ("tiles_n", ctypes.c_int64),
         ("num_tiles", ctypes.c_int64),
@@ -245,18 +247,24 @@ def tile_rowsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int 
                 tile_n: int = 256, stages: int = 4, *, split: bool = True,
                 consumer_warps: int = 0, max_ctas: int = 0, ctas_per_sm: int = 0,
                 wait_budget_ns: int = 0, log: torch.Tensor | None = None, fault: int = 0,
-                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                workspace: torch.Tensor | None = None, pipeline: int = 0,
+                stream=None) -> torch.Tensor:
     """out[i] = sum_j src[i, j] in fp32 through the tile pipeline.
 
     With ``split`` (default) row bands may be shared by several CTAs, using a
-    zero-filled workspace (cached per device unless one is given)."""
+    zero-filled workspace (cached per device unless one is given).
+    ``pipeline=2`` keeps one barrier pair per stage, ``pipeline=3`` gives
+    every box of a stage its own pair where the tile allows it
+    (``Plan.box_barriers``), 0 picks 3 for at most 2 stages; the sums are the
+    same in all three."""
     M, N, ld_s = _matrix(src, "src")
     if out is None:
         out = torch.empty(M, dtype=torch.float32, device=src.device)
     if out.dtype != torch.float32 or out.numel() != M or not out.is_contiguous():
         raise ValueError("out must be a contiguous float32 tensor of M elements")
     o = _opts(ld_src=ld_s, consumer_warps=consumer_warps, max_ctas=max_ctas,
-              ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault)
+              ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault,
+              pipeline=pipeline)
     if log is not None:
         o.log = log.data_ptr()
         o.log_capacity = log.numel() // 8

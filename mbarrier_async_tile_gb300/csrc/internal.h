@@ -58,6 +58,9 @@ struct RowsumArgs {
     int64_t gran;              // tiles per scheduling unit (1 or tiles_n)
     int32_t kmax;
     int32_t fused;             // 1: also copy every tile to dst (bulk stores)
+    int32_t boxed;             // 1: a full/empty barrier pair per (stage, box); the
+                               // consumer warps of box b use only box b's pair
+    int32_t pad2_;
     char *dst;                 // fused copy destination
     int64_t ld_dst_bytes;
 };

@@ -77,8 +77,9 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
     if (o.ctas_per_sm < 0 || o.max_ctas < 0 || o.log_capacity < 0) return MBT_ERR_ARG;
     if (o.fault < 0 || o.fault > 2) return MBT_ERR_ARG;
     if (o.store_mode < 0 || o.store_mode > 1) return MBT_ERR_UNSUPPORTED;
-    if (o.pipeline < 0 || o.pipeline > 1) return MBT_ERR_UNSUPPORTED;
+    if (o.pipeline < 0 || o.pipeline > 3) return MBT_ERR_UNSUPPORTED;
     if (o.pipeline == 1 && op != MBT_OP_COPY) return MBT_ERR_ARG;
+    if (o.pipeline >= 2 && op != MBT_OP_ROWSUM) return MBT_ERR_ARG;
     if (o.pipeline == 1 && o.store_mode != 0) return MBT_ERR_UNSUPPORTED;
     if (o.store_mode != 0 && op != MBT_OP_COPY) return MBT_ERR_ARG;
     for (int r : o.reserved)
@@ -191,6 +192,28 @@ int64_t flat_windows(int op, const mbt::FlatArgs &f, int64_t M, int64_t G) {
     return n;
 }
 
+// Row sum with a full/empty barrier pair per (stage, box): each consumer warp
+// must read a single box.  The threads of a row split its boxes * 8 chunks
+// into tpr = 32 W / tile_m contiguous blocks; that holds when every thread
+// is active (tile_m divides 32 W), tpr is a multiple of the box count, and
+// the threads serving one box, tile_m tpr / boxes of them, are whole warps.
+// By default only with at most kBoxBarrierMaxStages stages: measured on the
+// bf16 64 x 256 row sum, per-box pairs gain ~0.4% at 2 stages and lose ~1.6%
+// at 3 (the boxes of one tile are then issued at different times, so the
+// 512-byte row segments of a tile no longer reach DRAM together).
+constexpr int kBoxBarrierMaxStages = 2;
+
+bool box_barriers_apply(int op, int tile_m, int boxes, int W, int stages, const mbt_opts &o,
+                        bool flat) {
+    if (op != MBT_OP_ROWSUM || flat || boxes < 2 || boxes > 8) return false;
+    if (o.pipeline == 2 || (o.pipeline == 0 && stages > kBoxBarrierMaxStages)) return false;
+    const int nthr = 32 * W;
+    if (nthr % tile_m != 0) return false;
+    const int tpr = nthr / tile_m;
+    if (tpr % boxes != 0) return false;
+    return (tile_m * (tpr / boxes)) % 32 == 0;
+}
+
 int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, int dtype,
               const mbt_opts &o, int num_sms, int smem_optin, int fit_per_sm,
               int with_workspace, mbt_plan *plan, bool flat = false) {
@@ -229,6 +252,7 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     int64_t cap = per_sm * num_sms;
     if (o.max_ctas) cap = std::min<int64_t>(cap, o.max_ctas);
     plan->flat = flat ? 1 : 0;
+    plan->box_barriers = box_barriers_apply(op, tile_m, plan->boxes, W, stages, o, flat) ? 1 : 0;
     if (plan->num_tiles == 0) return MBT_OK;
     if (flat) {
         mbt::FlatArgs f{};
@@ -451,6 +475,7 @@ int rowsum_launch(const void *src, void *dst, float *out, int64_t M, int64_t N, 
         a.units = plan.tiles_m;
     }
     a.kmax = plan.kmax;
+    a.boxed = plan.box_barriers;
     if (dst != nullptr) {
         a.fused = 1;
         a.dst = static_cast<char *>(dst);

@@ -201,34 +201,64 @@ struct Smem {
     uint32_t base;    // 1024-aligned start of stage 0
     uint32_t full0;   // full barrier of stage 0 (stage s at + 8 s)
     uint32_t empty0;  // empty barrier of stage 0
+    // Per-box barriers (row sum, boxed mode): box b of stage s at + 8 (8 s + b).
+    uint32_t fullb0 = 0;
+    uint32_t emptyb0 = 0;
 };
+
+__device__ __forceinline__ uint32_t box_bar(uint32_t base, uint32_t stage, int box) {
+    return base + 8u * (stage * 8u + static_cast<uint32_t>(box));
+}
 
 // Producer: one elected lane.  Loads `count` tiles, tile j being
 // first + j * step in row-major tile order, then drains (producer tail).
+// With `boxed`, every box of a stage has its own full/empty barrier pair: the
+// producer refills box b as soon as box b's consumers have released it.
 __device__ void produce(const CUtensorMap *map, const PipeArgs &p, const Smem &sm,
-                        const WaitCtl &w, int64_t first, int64_t step, int64_t count) {
+                        const WaitCtl &w, int64_t first, int64_t step, int64_t count,
+                        bool boxed = false) {
     uint32_t stage = 0;
     uint32_t phase = (p.fault == 1) ? 0u : 1u;  // free buffers: start at phase 1
     int64_t issued = 0;
+    int last_boxes = p.boxes;   // boxes issued of tile issued - 1
     bool ok = true;
+    const uint32_t box_tx = p.tx_bytes / static_cast<uint32_t>(p.boxes);
     for (int64_t j = 0; j < count; ++j) {
-        const uint32_t empty_bar = sm.empty0 + 8u * stage;
-        if (!wait_bounded(empty_bar, phase, w, true)) {
-            report_timeout(0, stage, phase);
-            *w.abort = 1;
-            ok = false;
-            break;
-        }
         const int64_t tile = first + j * step;
         const int64_t tm = tile / p.tiles_n;
         const int64_t tn = tile - tm * p.tiles_n;
         const int32_t y = static_cast<int32_t>(tm * p.tile_m);
         const int32_t x0 = static_cast<int32_t>(tn * p.boxes * p.box_inner);
-        const uint32_t full_bar = sm.full0 + 8u * stage;
         const uint32_t dst = sm.base + stage * p.stage_stride;
-        mbar_arrive_expect_tx(full_bar, p.tx_bytes);
-        for (int b = 0; b < p.boxes; ++b)
-            tma_load_2d(dst + b * p.box_stride, map, x0 + b * p.box_inner, y, full_bar);
+        if (boxed) {
+            for (int b = 0; b < p.boxes; ++b) {
+                if (!wait_bounded(box_bar(sm.emptyb0, stage, b), phase, w, true)) {
+                    report_timeout(0, stage, phase);
+                    *w.abort = 1;
+                    ok = false;
+                    if (b > 0) {   // boxes 0 .. b-1 of this tile are in flight
+                        ++issued;
+                        last_boxes = b;
+                    }
+                    break;
+                }
+                const uint32_t full_bar = box_bar(sm.fullb0, stage, b);
+                mbar_arrive_expect_tx(full_bar, box_tx);
+                tma_load_2d(dst + b * p.box_stride, map, x0 + b * p.box_inner, y, full_bar);
+            }
+            if (!ok) break;
+        } else {
+            if (!wait_bounded(sm.empty0 + 8u * stage, phase, w, true)) {
+                report_timeout(0, stage, phase);
+                *w.abort = 1;
+                ok = false;
+                break;
+            }
+            const uint32_t full_bar = sm.full0 + 8u * stage;
+            mbar_arrive_expect_tx(full_bar, p.tx_bytes);
+            for (int b = 0; b < p.boxes; ++b)
+                tma_load_2d(dst + b * p.box_stride, map, x0 + b * p.box_inner, y, full_bar);
+        }
         log_record(p, 0, j, stage, phase, tile);
         ++issued;
         if (++stage == static_cast<uint32_t>(p.stages)) {
@@ -239,12 +269,16 @@ __device__ void produce(const CUtensorMap *map, const PipeArgs &p, const Smem &s
     if (ok) {
         // Tail: wait until the consumers have released every stage once more,
         // so the CTA never exits with a stage still being read or filled.
-        for (int s = 0; s < p.stages; ++s) {
-            if (!wait_bounded(sm.empty0 + 8u * stage, phase, w, true)) {
-                report_timeout(0, stage, phase);
-                *w.abort = 1;
-                ok = false;
-                break;
+        for (int s = 0; s < p.stages && ok; ++s) {
+            const int nb = boxed ? p.boxes : 1;
+            for (int b = 0; b < nb; ++b) {
+                const uint32_t bar = boxed ? box_bar(sm.emptyb0, stage, b) : sm.empty0 + 8u * stage;
+                if (!wait_bounded(bar, phase, w, true)) {
+                    report_timeout(0, stage, phase);
+                    *w.abort = 1;
+                    ok = false;
+                    break;
+                }
             }
             if (++stage == static_cast<uint32_t>(p.stages)) {
                 stage = 0;
@@ -259,20 +293,41 @@ __device__ void produce(const CUtensorMap *map, const PipeArgs &p, const Smem &s
         for (int64_t t = from; t < issued; ++t) {
             const uint32_t s = static_cast<uint32_t>(t % p.stages);
             const uint32_t par = static_cast<uint32_t>((t / p.stages) & 1);
-            wait_bounded(sm.full0 + 8u * s, par, w, false);
+            if (boxed) {
+                const int nb = t == issued - 1 ? last_boxes : p.boxes;
+                for (int b = 0; b < nb; ++b) wait_bounded(box_bar(sm.fullb0, s, b), par, w, false);
+            } else {
+                wait_bounded(sm.full0 + 8u * s, par, w, false);
+            }
         }
     }
 }
 
+// `bars` holds 2 kMaxStages barriers, or 16 kMaxStages when `boxed`: then
+// each (stage, box) gets a full barrier (one arrival + the box's bytes) and an
+// empty barrier that the box's consumer warps -- consumer_warps / boxes of
+// them -- release.
 __device__ __forceinline__ void init_pipeline(const PipeArgs &p, Smem &sm,
                                               uint64_t *bars, volatile int *abort_flag,
                                               uint64_t *extra_bar, uint32_t extra_count,
-                                              unsigned char *dyn) {
+                                              unsigned char *dyn, bool boxed = false) {
     sm.base = (smem_u32(dyn) + (kSwizzleAtomBytes - 1)) & ~uint32_t(kSwizzleAtomBytes - 1);
     sm.full0 = smem_u32(&bars[0]);
     sm.empty0 = smem_u32(&bars[kMaxStages]);
+    if (boxed) {
+        sm.fullb0 = smem_u32(&bars[0]);
+        sm.emptyb0 = smem_u32(&bars[8 * kMaxStages]);
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
+            if (boxed) {
+                for (int b = 0; b < p.boxes; ++b) {
+                    mbar_init(box_bar(sm.fullb0, s, b), 1);
+                    mbar_init(box_bar(sm.emptyb0, s, b),
+                              static_cast<uint32_t>(p.consumer_warps / p.boxes + p.empty_extra));
+                }
+                continue;
+            }
             mbar_init(sm.full0 + 8u * s, 1);
             mbar_init(sm.empty0 + 8u * s,
                       static_cast<uint32_t>(p.consumer_warps + p.empty_extra));
@@ -660,10 +715,17 @@ __device__ bool flush_band(const RowsumArgs &a, int64_t band, float acc, bool ac
 }
 
 // Row-sum consumer warps; the first of them is warp `cwarp0` of the CTA.
+// Thread (row, sub) of the tpr threads per row sums the contiguous block of
+// 16-byte chunks [sub cpr / tpr, (sub + 1) cpr / tpr) of its row (cpr chunks
+// per tile row), in chunk order; the per-thread sums are combined in `sub`
+// order.  This order does not depend on the barrier layout, so the fused and
+// the per-box kernels give bit-identical sums.  With `boxed` (host-checked:
+// tpr a multiple of boxes, and the threads of one box whole warps) every warp
+// reads one box only, and waits for and releases that box alone.
 template <int DT>
 __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCtl &w,
                                int64_t first, int64_t count, float *red, int *last_flag,
-                               FlushCtl &f, int cwarp0) {
+                               FlushCtl &f, int cwarp0, bool boxed) {
     const PipeArgs &p = a.p;
     const int ctid = static_cast<int>(threadIdx.x) - 32 * cwarp0;
     const int lane = threadIdx.x & 31;
@@ -673,10 +735,11 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
     const int row = active ? ctid % p.tile_m : 0;
     const int sub = active ? ctid / p.tile_m : 0;
     const int cpr = p.boxes * 8;
-    // This thread reads chunks q = sub, sub + tpr, ... of its row.
-    const int mine = active ? (cpr - sub + tpr - 1) / tpr : 0;
+    const int lo = sub * cpr / tpr;
+    const int mine = active ? (sub + 1) * cpr / tpr - lo : 0;
     const int most = (cpr + tpr - 1) / tpr;
     const int rounds = (most + kVec - 1) / kVec;
+    const int box = boxed ? (ctid / p.tile_m) / (tpr / p.boxes) : 0;
     float acc = 0.f;
     int64_t band = -1;
     uint32_t stage = 0, phase = 0;
@@ -693,7 +756,7 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
             band = tb;
             acc = 0.f;
         }
-        const uint32_t full_bar = sm.full0 + 8u * stage;
+        const uint32_t full_bar = boxed ? box_bar(sm.fullb0, stage, box) : sm.full0 + 8u * stage;
         bool got = wait_bounded(full_bar, phase, w, true);
         got = __all_sync(0xffffffffu, got);
         if (!got) {
@@ -712,11 +775,12 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
 #pragma unroll
             for (int u = 0; u < kVec; ++u) {
                 const int k = r * kVec + u;
-                if (k < mine) v[u] = lds128(rbase + chunk_offset(row, sub + k * tpr, p.box_stride));
+                if (k < mine) v[u] = lds128(rbase + chunk_offset(row, lo + k, p.box_stride));
             }
             if (r == rounds - 1) {
                 __syncwarp();
-                if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+                if (lane == 0 && p.fault != 2)
+                    mbar_arrive(boxed ? box_bar(sm.emptyb0, stage, box) : sm.empty0 + 8u * stage);
             }
 #pragma unroll
             for (int u = 0; u < kVec; ++u) {
@@ -742,14 +806,16 @@ __global__ void __launch_bounds__(FUSED ? kMaxThreads + 32 : kMaxThreads, 2)
     mbt_rowsum_kernel(const __grid_constant__ CUtensorMap map,
                       const __grid_constant__ CUtensorMap dst_map, const RowsumArgs a) {
     extern __shared__ __align__(1024) unsigned char dyn_smem[];
-    __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
+    // Per-box barrier pairs only without the store warp (which reads whole stages).
+    __shared__ __align__(8) uint64_t bars[FUSED ? 2 * kMaxStages : 16 * kMaxStages];
     __shared__ __align__(8) uint64_t flush_bar;
     __shared__ float red[kMaxThreads];      // indexed by row-sum consumer thread
     __shared__ int abort_flag;
     __shared__ int last_flag;
     Smem sm;
+    const bool boxed = !FUSED && a.boxed != 0;
     init_pipeline(a.p, sm, bars, &abort_flag, &flush_bar,
-                  static_cast<uint32_t>(a.p.consumer_warps), dyn_smem);
+                  static_cast<uint32_t>(a.p.consumer_warps), dyn_smem, boxed);
     WaitCtl w{a.p.wait_budget_ns, &abort_flag};
     // Contiguous, evenly split range of scheduling units, in band-major order.
     const int64_t G = gridDim.x;
@@ -757,7 +823,7 @@ __global__ void __launch_bounds__(FUSED ? kMaxThreads + 32 : kMaxThreads, 2)
     const int64_t first = (b * a.units / G) * a.gran;
     const int64_t last = ((b + 1) * a.units / G) * a.gran;
     if (threadIdx.x < 32) {
-        if (threadIdx.x == 0) produce(&map, a.p, sm, w, first, 1, last - first);
+        if (threadIdx.x == 0) produce(&map, a.p, sm, w, first, 1, last - first, boxed);
         return;
     }
     if constexpr (FUSED) {
@@ -772,7 +838,7 @@ __global__ void __launch_bounds__(FUSED ? kMaxThreads + 32 : kMaxThreads, 2)
         }
     }
     FlushCtl f{smem_u32(&flush_bar), 0u};
-    consume_rowsum<DT>(a, sm, w, first, last - first, red, &last_flag, f, FUSED ? 2 : 1);
+    consume_rowsum<DT>(a, sm, w, first, last - first, red, &last_flag, f, FUSED ? 2 : 1, boxed);
 }
 
 __global__ void mbt_fill_zero_kernel(float *out, int64_t n) {

@@ -100,8 +100,13 @@ def test_option_errors():
     assert _copy(A, B, 8, 64, opts=o) == -1
     o = Opts(); o.fault = 3
     assert _copy(A, B, 8, 64, opts=o) == -1
-    o = Opts(); o.pipeline = 2
+    o = Opts(); o.pipeline = 4
     assert _copy(A, B, 8, 64, opts=o) == -3
+    for pipe in (2, 3):                            # barrier layouts: row sum only
+        o = Opts(); o.pipeline = pipe
+        assert _copy(A, B, 8, 64, opts=o) == -1
+        assert C.tile_copy_rowsum_ex(A, B, B, 8, 64, 128, 64, 3, 0, None,
+                                     ctypes.byref(o)) == -1
     o = Opts(); o.pipeline = 1; o.store_mode = 1   # unified pipeline: LSU stores only
     assert _copy(A, B, 8, 64, opts=o) == -3
     o = Opts(); o.pipeline = 1                     # copy only
@@ -202,6 +207,58 @@ def test_plan_rowsum_multibox_tile():
     p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 3, torch.bfloat16, fit=1)
     assert p["boxes"] == 4 and p["tx_bytes"] == 32768 and p["stage_bytes"] == 32768
     assert p["grid"] == 128 and p["split"] == 0      # whole bands, one CTA each
+
+
+def _warp_boxes(tile_m, boxes, W):
+    """Boxes each consumer warp reads when thread t of 32 W sums chunks
+    [sub cpr / tpr, (sub + 1) cpr / tpr) of row t % tile_m (sub = t // tile_m)."""
+    tpr, cpr = 32 * W // tile_m, 8 * boxes
+    out = []
+    for w in range(W):
+        seen = set()
+        for t in range(32 * w, 32 * w + 32):
+            if t >= tile_m * tpr:
+                continue
+            sub = t // tile_m
+            seen |= {q // 8 for q in range(sub * cpr // tpr, (sub + 1) * cpr // tpr)}
+        out.append(seen)
+    return out
+
+
+@pytest.mark.parametrize("tm,tn,dt,W", [
+    (64, 256, torch.bfloat16, 8), (64, 256, torch.bfloat16, 4), (128, 128, torch.float16, 8),
+    (128, 256, torch.bfloat16, 8), (64, 512, torch.float16, 8), (32, 256, torch.float32, 8),
+    (96, 256, torch.bfloat16, 8), (128, 64, torch.float16, 4), (16, 512, torch.bfloat16, 1),
+    (64, 128, torch.float32, 2), (256, 128, torch.float16, 8), (48, 128, torch.float16, 3),
+])
+def test_plan_box_barriers_only_where_each_warp_reads_one_box(tm, tn, dt, W):
+    p = _plan(mbt.OP_ROWSUM, 4096, 8192, tm, tn, 2, dt, consumer_warps=W)
+    # forced per-box pairs at 3 stages follow the same geometric rule;
+    # the default keeps stage-wide pairs there
+    p3 = _plan(mbt.OP_ROWSUM, 4096, 8192, tm, tn, 3, dt, consumer_warps=W, pipeline=3)
+    assert p3["box_barriers"] == p["box_barriers"]
+    assert _plan(mbt.OP_ROWSUM, 4096, 8192, tm, tn, 3, dt, consumer_warps=W)[
+        "box_barriers"] == 0
+    per_warp = _warp_boxes(tm, p["boxes"], W)
+    every_thread_busy = (32 * W) % tm == 0
+    one_box = all(len(b) == 1 for b in per_warp)
+    assert p["box_barriers"] == int(p["boxes"] > 1 and every_thread_busy and one_box)
+    if p["box_barriers"]:
+        # the barrier counts: every box is read by the same number of warps
+        counts = [sum(1 for b in per_warp if b == {k}) for k in range(p["boxes"])]
+        assert counts == [W // p["boxes"]] * p["boxes"]
+    # never for the fused operation, the flat kernels, or with pipeline=2
+    assert _plan(mbt.OP_COPY_ROWSUM, 4096, 8192, tm, tn, 2, dt, consumer_warps=W)[
+        "box_barriers"] == 0
+    assert _plan(mbt.OP_ROWSUM, 4096, 8192, tm, tn, 2, dt, consumer_warps=W,
+                 pipeline=2)["box_barriers"] == 0
+    flat = _plan(mbt.OP_ROWSUM, 4096, 8191, tm, tn, 2, dt, consumer_warps=W)  # odd pitch
+    assert flat["flat"] == 1 and flat["box_barriers"] == 0
+
+
+def test_plan_box_barriers_in_the_bench_row_sum():
+    p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16, fit=4, ws=True)
+    assert p["boxes"] == 4 and p["consumer_warps"] == 8 and p["box_barriers"] == 1
 
 
 def _ranges(G, units, gran):
