@@ -326,8 +326,7 @@ def bench_gpu(args, rank, world):
     value = aggregate_gbs(step_bytes, args.steps, world, ms_max)
 
     # end to end through the public API with host buffers
-    e2e = bench_e2e(args, mbt, x3, x4, ws,
-                    (side[0], side[1], main) if args.streams == 2 else (main, main, main), world)
+    e2e = bench_e2e(args, mbt, x3, x4, world)
 
     peak, peak_kind = measured_peak()
     kernels = {
@@ -382,11 +381,18 @@ def bench_gpu(args, rank, world):
     return out
 
 
-def bench_e2e(args, mbt, x3, x4, ws, streams, world):
-    """Same metric, through the public API, with host buffers: every step
-    copies the inputs from pinned host memory, runs both calls and reads the
-    results back (each operation's copies and kernel on its own stream)."""
-    s_copy, s_rowsum, main = streams
+def bench_e2e(args, mbt, x3, x4, world):
+    """Same metric through the host-buffer C-ABI calls: every step runs
+    tile_copy_host on the fp16 matrix and tile_rowsum_host on the bf16 matrix,
+    both in pinned host memory; each call copies its input in, runs the tile
+    pipeline and copies the result out, slab by slab with the three
+    overlapped, and returns when the result is in host memory.  With
+    args.e2e_threads == 2 the two calls of a step run on two host threads
+    (independent calls; the copy's device-to-host traffic then shares the
+    link with the row sum's host-to-device traffic).  Host wall-clock time,
+    max over ranks."""
+    import threading
+
     steps = max(1, min(args.steps, args.e2e_steps))
     h3 = torch.empty(x3.shape, dtype=x3.dtype, pin_memory=True)
     h3.copy_(x3)
@@ -394,39 +400,36 @@ def bench_e2e(args, mbt, x3, x4, ws, streams, world):
     h4.copy_(x4)
     r3 = torch.empty_like(h3, pin_memory=True)
     r4 = torch.empty(x4.shape[0], dtype=torch.float32, pin_memory=True)
-    g3, g3o = torch.empty_like(x3), torch.empty_like(x3)
-    g4, g4o = torch.empty_like(x4), torch.empty(x4.shape[0], dtype=torch.float32,
-                                                device=x4.device)
-    torch.cuda.synchronize()
+
+    def run_copy():
+        mbt.tile_copy_host(h3, r3, COPY["tile_m"], COPY["tile_n"], args.copy_stages,
+                           store_mode=args.store_mode)
+
+    def run_rowsum():
+        mbt.tile_rowsum_host(h4, r4, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages)
 
     def step():
-        with torch.cuda.stream(s_copy):
-            g3.copy_(h3, non_blocking=True)
-            mbt.tile_copy(g3, g3o, COPY["tile_m"], COPY["tile_n"], args.copy_stages,
-                          store_mode=args.store_mode, stream=s_copy)
-            r3.copy_(g3o, non_blocking=True)
-        with torch.cuda.stream(s_rowsum):
-            g4.copy_(h4, non_blocking=True)
-            mbt.tile_rowsum(g4, g4o, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
-                            workspace=ws, stream=s_rowsum)
-            r4.copy_(g4o, non_blocking=True)
+        if args.e2e_threads == 2:
+            t = threading.Thread(target=run_copy)
+            t.start()
+            run_rowsum()
+            t.join()
+        else:
+            run_copy()
+            run_rowsum()
 
-    step()
-    torch.cuda.synchronize()
+    step()   # warm-up: staging sets allocated, plans cached
+    if not torch.equal(r3.view(torch.int16), h3.view(torch.int16)):
+        raise RuntimeError("tile_copy_host result differs from its input")
     barrier(world)
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(main)
-    s_copy.wait_stream(main)
-    s_rowsum.wait_stream(main)
+    t0 = time.perf_counter()
     for _ in range(steps):
         step()
-    main.wait_stream(s_copy)
-    main.wait_stream(s_rowsum)
-    e.record(main)
-    torch.cuda.synchronize()
-    ms = reduce_max(s.elapsed_time(e), world)
+    ms = reduce_max((time.perf_counter() - t0) * 1e3, world)
     value = aggregate_gbs(copy_bytes() + rowsum_bytes(), steps, world, ms)
     return {"value": round(value, 1), "unit": "GB/s", "steps": steps,
+            "api": "tile_copy_host + tile_rowsum_host (host buffers, pinned)",
+            "host_threads": args.e2e_threads,
             "h2d_bytes_per_step": h3.numel() * h3.element_size() + h4.numel() * h4.element_size(),
             "d2h_bytes_per_step": r3.numel() * r3.element_size() + r4.numel() * r4.element_size()}
 
@@ -720,6 +723,8 @@ def main(argv=None):
     ap.add_argument("--copy-stages", type=int, default=3)
     ap.add_argument("--rowsum-stages", type=int, default=2)
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-threads", type=int, default=2, choices=(1, 2),
+                    help="host threads running the two host-buffer calls of an e2e step")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true")

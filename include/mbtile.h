@@ -28,10 +28,12 @@
  *   is the plain definition out[i] = sum_j src[i][j].
  *
  * Conventions common to every entry point:
- *   - All data pointers are DEVICE pointers owned by the caller.  The library
- *     never allocates or frees device memory; it keeps only per-device caches
- *     (SM count, shared-memory limit, the driver's tensor-map encoder) and a
- *     small per-device status word (see tile_status).
+ *   - All data pointers are DEVICE pointers owned by the caller, except in
+ *     the host-buffer forms (tile_copy_host, tile_rowsum_host).  Apart from
+ *     those forms' staging pool, the library never allocates or frees device
+ *     memory; it keeps only per-device caches (SM count, shared-memory limit,
+ *     the driver's tensor-map encoder) and a small per-device status word
+ *     (see tile_status).
  *   - Matrices are row-major: element (i, j) is at ptr[i * ld + j], with the
  *     row pitch ld in elements.  The logical shape is M rows by N columns.
  *     Base pointers must be 16-byte aligned.  When ld * element size is a
@@ -137,7 +139,11 @@ typedef struct mbt_opts {
                                 most 2 stages, else 2 (per-box pairs gain at
                                 2 stages and lose at 3 on the bf16 64 x 256
                                 row sum). */
-    int32_t reserved[6];     /* must be 0 */
+    int32_t host_slab_rows;  /* tile_copy_host / tile_rowsum_host only: rows
+                                per slab; 0 => whole row bands of about
+                                MBT_HOST_SLAB_BYTES.  Must be 0 for the
+                                device calls. */
+    int32_t reserved[5];     /* must be 0 */
 } mbt_opts;
 
 /* Launch plan, as computed by tile_plan (host only, no CUDA calls). */
@@ -312,6 +318,37 @@ int tile_plan(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages,
 int tile_stage_image(const void *src, int64_t M, int64_t N, int64_t ld, int tile_m,
                      int tile_n, int dtype, int64_t tile_row, int64_t tile_col,
                      void *image, void *stream);
+
+/*
+ * Host-buffer forms: src, dst and out are HOST pointers (pinned memory from
+ * cudaHostAlloc / cudaHostRegister lets the copies overlap; pageable memory
+ * works but the driver then stages it).  The result is that of tile_copy_ex /
+ * tile_rowsum_ex on the same matrix (row sums: within the same error bound,
+ * not necessarily bit-identical, since a band may be split differently).
+ * The call is synchronous: on return every copy and kernel has finished.
+ *
+ * The matrix moves through the current device in slabs of whole row bands of
+ * about MBT_HOST_SLAB_BYTES each, repacked there with a 16-byte row pitch (so
+ * ld_src / ld_dst, in elements, may be any value >= N and host pointers need
+ * no alignment).  Three slab slots and three streams pipeline the host-to-
+ * device copy of slab k + 1, the kernel of slab k and the device-to-host copy
+ * of slab k - 1.  The staging memory (3 x 2 slabs, plus a row-sum workspace)
+ * comes from a per-device pool that the library owns; concurrent calls use
+ * separate staging sets; tile_host_release frees the idle ones.
+ *
+ * opts: as for the device calls, except that log, workspace and
+ * workspace_bytes must be NULL / 0 (the slab schedule owns them).  Returns
+ * MBT_OK, an argument error before anything is copied, MBT_ERR_CUDA, or
+ * MBT_ERR_TIMEOUT when a pipeline wait ran out of its budget (the status word
+ * is read and cleared by the call, see tile_status).
+ */
+#define MBT_HOST_SLAB_BYTES (64ll << 20)
+int tile_copy_host(const void *src, void *dst, int64_t M, int64_t N, int tile_m, int tile_n,
+                   int stages, int dtype, const mbt_opts *opts);
+int tile_rowsum_host(const void *src, float *out, int64_t M, int64_t N, int tile_m,
+                     int tile_n, int stages, int dtype, const mbt_opts *opts);
+/* Frees the current device's idle staging sets of the host-buffer forms. */
+int tile_host_release(void);
 
 /* Synchronises `stream`, then reads and clears the current device's status
  * word.  info (may be NULL) receives {code, block, stage, role * 2 + parity}

@@ -47,7 +47,8 @@ class Opts(ctypes.Structure):
         ("workspace_bytes", ctypes.c_size_t),
         ("fault", ctypes.c_int32),
         ("pipeline", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 6),
+        ("host_slab_rows", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 5),
     ]
 
 
@@ -127,11 +128,15 @@ def _load():
         lib.tile_device_info.argtypes = [i32, ctypes.POINTER(ctypes.c_int),
                                          ctypes.POINTER(ctypes.c_int),
                                          ctypes.POINTER(ctypes.c_double)]
+        host_sig = [vp, vp, i64, i64, i32, i32, i32, i32, ctypes.POINTER(Opts)]
+        lib.tile_copy_host.argtypes = host_sig
+        lib.tile_rowsum_host.argtypes = host_sig
+        lib.tile_host_release.argtypes = []
         for name in ("tile_copy", "tile_copy_ex", "tile_rowsum", "tile_rowsum_ex",
                      "tile_copy_rowsum", "tile_copy_rowsum_ex",
                      "tile_rowsum_workspace_bytes", "tile_copy_rowsum_workspace_bytes",
-                     "tile_plan", "tile_status",
-                     "tile_device_info"):
+                     "tile_plan", "tile_status", "tile_device_info",
+                     "tile_copy_host", "tile_rowsum_host", "tile_host_release"):
             getattr(lib, name).restype = ctypes.c_int
         _C = lib
         return lib
@@ -167,6 +172,20 @@ def _matrix(t: torch.Tensor, name: str) -> tuple[int, int, int]:
         raise ValueError(f"{name} must be a 2-D tensor")
     if t.device.type != "cuda":
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in DTYPE_CODE:
+        raise ValueError(f"{name} has unsupported dtype {t.dtype}")
+    M, N = t.shape
+    if M > 0 and N > 0 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major (unit column stride)")
+    ld = t.stride(0) if M > 1 else max(N, t.stride(0))
+    return M, N, ld
+
+
+def _host_matrix(t: torch.Tensor, name: str) -> tuple[int, int, int]:
+    if not isinstance(t, torch.Tensor) or t.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D tensor")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor")
     if t.dtype not in DTYPE_CODE:
         raise ValueError(f"{name} has unsupported dtype {t.dtype}")
     M, N = t.shape
@@ -387,3 +406,42 @@ def tile_rowsum_noalloc(src: torch.Tensor, out: torch.Tensor, tile_m: int = 64,
             DTYPE_CODE[src.dtype], _stream_handle(stream), ctypes.byref(o))
     _check(rc, "tile_rowsum_noalloc")
     return out
+
+
+def tile_copy_host(src: torch.Tensor, dst: torch.Tensor, tile_m: int = 128, tile_n: int = 64,
+                   stages: int = 3, *, slab_rows: int = 0, **opt) -> torch.Tensor:
+    """dst[i, j] = src[i, j] for HOST tensors: the library streams row slabs
+    through the current device (copy in, tile pipeline, copy out, overlapped).
+    Pinned tensors (``pin_memory=True``) let the copies overlap.  Synchronous."""
+    M, N, ld_s = _host_matrix(src, "src")
+    Md, Nd, ld_d = _host_matrix(dst, "dst")
+    if (M, N) != (Md, Nd) or src.dtype != dst.dtype:
+        raise ValueError("src and dst must have the same shape and dtype")
+    o = _opts(ld_src=ld_s, ld_dst=ld_d, host_slab_rows=slab_rows, **opt)
+    rc = _load().tile_copy_host(src.data_ptr(), dst.data_ptr(), M, N, tile_m, tile_n, stages,
+                                DTYPE_CODE[src.dtype], ctypes.byref(o))
+    _check(rc, "tile_copy_host")
+    return dst
+
+
+def tile_rowsum_host(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int = 64,
+                     tile_n: int = 256, stages: int = 2, *, slab_rows: int = 0,
+                     **opt) -> torch.Tensor:
+    """out[i] = sum_j src[i, j] in fp32 for a HOST tensor (out on the host
+    too), streamed through the current device in row slabs.  Synchronous."""
+    M, N, ld_s = _host_matrix(src, "src")
+    if out is None:
+        out = torch.empty(M, dtype=torch.float32, pin_memory=src.is_pinned())
+    if (out.device.type != "cpu" or out.dtype != torch.float32 or out.numel() != M
+            or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous float32 host tensor of M elements")
+    o = _opts(ld_src=ld_s, host_slab_rows=slab_rows, **opt)
+    rc = _load().tile_rowsum_host(src.data_ptr(), out.data_ptr(), M, N, tile_m, tile_n, stages,
+                                  DTYPE_CODE[src.dtype], ctypes.byref(o))
+    _check(rc, "tile_rowsum_host")
+    return out
+
+
+def tile_host_release() -> None:
+    """Free the current device's idle staging memory of the host-buffer forms."""
+    _check(_load().tile_host_release(), "tile_host_release")

@@ -84,6 +84,7 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
     if (o.store_mode != 0 && op != MBT_OP_COPY) return MBT_ERR_ARG;
     for (int r : o.reserved)
         if (r != 0) return MBT_ERR_ARG;
+    if (o.host_slab_rows != 0) return MBT_ERR_ARG;   // host-buffer forms only
     if (o.log != nullptr && o.log_capacity == 0) return MBT_ERR_ARG;
     if (o.workspace == nullptr && o.workspace_bytes != 0) return MBT_ERR_ARG;
     if (M > kMaxCoord || N > kMaxCoord) return MBT_ERR_UNSUPPORTED;

@@ -139,6 +139,31 @@ def test_empty_shapes_are_noops_without_device():
     assert C.tile_rowsum(0, None, 0, 0, 64, 256, 3, 1, None) == 0
 
 
+def test_host_forms_argument_errors_before_any_cuda_call():
+    """The host-buffer forms check their arguments before touching the
+    device, so these run without a GPU."""
+    src = (ctypes.c_uint16 * 64)()
+    out = (ctypes.c_float * 8)(*([7.0] * 8))
+    p = ctypes.addressof
+    assert C.tile_copy_host(p(src), p(src), 0, 64, 128, 64, 3, 0, None) == 0
+    assert C.tile_rowsum_host(p(src), p(out), 8, 0, 64, 64, 2, 0, None) == 0
+    assert list(out) == [0.0] * 8                       # empty rows sum to 0
+    assert C.tile_rowsum_host(p(src), None, 8, 0, 64, 64, 2, 0, None) == -1
+    assert C.tile_rowsum_host(None, p(out), 8, 8, 64, 64, 2, 0, None) == -1
+    assert C.tile_copy_host(p(src), None, 8, 8, 64, 64, 2, 0, None) == -1
+    assert C.tile_copy_host(p(src), p(src), 8, 8, 64, 64, 2, 7, None) == -1   # dtype
+    for field, value in (("log", 16), ("workspace", 16), ("workspace_bytes", 4),
+                         ("host_slab_rows", -1), ("ld_src", 4)):
+        o = Opts()
+        setattr(o, field, value)
+        assert C.tile_copy_host(p(src), p(src), 8, 8, 64, 64, 2, 0, ctypes.byref(o)) == -1, field
+    o = Opts(); o.ld_dst = 8                             # a row sum has no dst pitch
+    assert C.tile_rowsum_host(p(src), p(out), 8, 8, 64, 64, 2, 0, ctypes.byref(o)) == -1
+    o = Opts(); o.host_slab_rows = 4                     # host-buffer forms only
+    assert _copy(A, B, 8, 64, opts=o) == -1
+    assert C.tile_rowsum_ex(A, B, 8, 64, 128, 64, 3, 0, None, ctypes.byref(o)) == -1
+
+
 def _plan(op, M, N, tm, tn, st, dtype, sms=152, smem=232448, fit=1, ws=False, **opt):
     return mbt.tile_plan(op, M, N, tm, tn, st, dtype, num_sms=sms, smem_optin=smem,
                          fit_per_sm=fit, with_workspace=ws, **opt)
