@@ -15,6 +15,7 @@ the same workload.  --sweep prints one extra line per stage / warp / CTA point.
 from __future__ import annotations
 
 import argparse
+import concurrent.futures
 import hashlib
 import json
 import os
@@ -149,55 +150,127 @@ def make_inputs(device):
     return x3, d3, x4, o4
 
 
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+def oracle_blocks_parallel(jobs, pool) -> float:
+    """Run independent oracle calls (closures over disjoint row blocks) on a
+    thread pool; the oracle's C loops release the GIL.  Returns the
+    wall-clock seconds."""
+    t = time.perf_counter()
+    for f in [pool.submit(j) for j in jobs]:
+        f.result()
+    return time.perf_counter() - t
+
+
+def host_memcpy_gbs(nbytes: int = 256 << 20) -> float:
+    """Context: a plain single-thread memcpy of nbytes on the host, read +
+    write bytes over the best of 3."""
+    import ctypes
+
+    a = torch.ones(nbytes, dtype=torch.uint8)
+    b = torch.empty_like(a)
+    best = float("inf")
+    for _ in range(3):
+        t = time.perf_counter()
+        ctypes.memmove(b.data_ptr(), a.data_ptr(), nbytes)
+        best = min(best, time.perf_counter() - t)
+    return 2 * nbytes / best / 1e9
+
+
 def cpu_baseline(x3, d3, x4, o4, budget_s: float = 12.0) -> dict:
-    """Time the CPU oracle on a bounded sample of the same workload (row
-    blocks of both matrices, alternated in proportion to their bytes, until
-    about ``budget_s`` of CPU time), and check the GPU's outputs on exactly
-    those rows against the oracle's."""
+    """Time the CPU oracle, as it stands, on a bounded sample of the same
+    workload: row blocks of both matrices in proportion to their bytes, first
+    on one host core (about budget_s / 2 of CPU time), then on all host
+    cores (disjoint row blocks on as many threads, about budget_s / 2 of wall
+    time).  The GPU's outputs on every sampled row are checked against the
+    oracle's."""
     import oracle
 
     oracle.build()
-    threads = 1   # the oracle is a plain single-threaded C loop
+    cores = host_cores()
     blk3, blk4 = 256, ROWSUM["tile_m"]
-    n3 = n4 = 0
-    t_cpu = 0.0
-    bytes_done = 0
-    mismatches = 0
-    worst = 0.0
-    r3 = r4 = 0
-    while t_cpu < budget_s and (r3 < COPY["M"] or r4 < ROWSUM["M"]):
-        # copy block
-        if r3 < COPY["M"] and (n3 * blk3 * COPY["N"] * 4 <= n4 * blk4 * ROWSUM["N"] * 2 + 1
-                               or r4 >= ROWSUM["M"]):
+    state = {}
+    checks = {"mismatches": 0, "worst": 0.0}
+
+    def next_block():
+        """(job, check, bytes) of the next row block, or None when both
+        matrices are exhausted."""
+        r3, r4 = state["r3"], state["r4"]
+        take_copy = r3 < COPY["M"] and (state["b3"] <= state["b4"] or r4 >= ROWSUM["M"])
+        if take_copy:
             src = x3[r3:r3 + blk3].cpu()
             want = torch.empty_like(src)
-            t = time.perf_counter()
-            oracle.copy(src, want)
-            t_cpu += time.perf_counter() - t
             got = d3[r3:r3 + blk3].cpu()
-            mismatches += int((got.view(torch.int16) != want.view(torch.int16)).sum())
-            bytes_done += 2 * src.numel() * src.element_size()
-            r3 += blk3
-            n3 += 1
-        else:
+            state["r3"] += blk3
+            nbytes = 2 * src.numel() * src.element_size()
+            state["b3"] += nbytes
+
+            def check():
+                checks["mismatches"] += int((got.view(torch.int16) != want.view(torch.int16)).sum())
+            return (lambda: oracle.copy(src, want)), check, nbytes
+        if r4 < ROWSUM["M"]:
             src = x4[r4:r4 + blk4].cpu()
-            t = time.perf_counter()
-            ref, sq = oracle.rowsum(src, with_sumsq=True)
-            t_cpu += time.perf_counter() - t
             got = o4[r4:r4 + blk4].cpu().double()
-            err = ((got - ref).abs() / torch.maximum(ref.abs(), sq.sqrt())).max().item()
-            worst = max(worst, err)
-            bytes_done += src.numel() * src.element_size() + 4 * src.shape[0]
-            r4 += blk4
-            n4 += 1
+            res = {}
+            state["r4"] += blk4
+            nbytes = src.numel() * src.element_size() + 4 * src.shape[0]
+            state["b4"] += nbytes
+
+            def job():
+                res["ref"], res["sq"] = oracle.rowsum(src, with_sumsq=True)
+
+            def check():
+                err = ((got - res["ref"]).abs() / torch.maximum(res["ref"].abs(),
+                                                                res["sq"].sqrt())).max().item()
+                checks["worst"] = max(checks["worst"], err)
+            return job, check, nbytes
+        return None
+
+    # one core, from the first row of both matrices
+    state.update(r3=0, r4=0, b3=0, b4=0)
+    t1 = 0.0
+    bytes1 = 0
+    while t1 < budget_s / 2:
+        blk = next_block()
+        if blk is None:
+            break
+        job, check, nbytes = blk
+        t = time.perf_counter()
+        job()
+        t1 += time.perf_counter() - t
+        check()
+        bytes1 += nbytes
+    rows1 = (state["r3"], state["r4"])
+    # all cores, again from the first row: rounds of `cores` blocks
+    state.update(r3=0, r4=0, b3=0, b4=0)
+    tn = 0.0
+    bytesn = 0
+    with concurrent.futures.ThreadPoolExecutor(max_workers=cores) as pool:
+        while tn < budget_s / 2:
+            blocks = [b for b in (next_block() for _ in range(cores)) if b is not None]
+            if not blocks:
+                break
+            tn += oracle_blocks_parallel([b[0] for b in blocks], pool)
+            for _, check, nbytes in blocks:
+                check()
+                bytesn += nbytes
+    one = bytes1 / t1 / 1e9 if t1 > 0 else None
+    alln = bytesn / tn / 1e9 if tn > 0 else None
     return {
-        "value": round(bytes_done / t_cpu / 1e9, 4), "unit": "GB/s", "cores": threads,
-        "kind": "oracle",
-        "sample": (f"{r3} of {COPY['M']} rows of the copy and {r4} of {ROWSUM['M']} rows "
-                   f"of the row sum ({bytes_done / 1e9:.3f} GB algorithmic, "
-                   f"{t_cpu:.1f} s on 1 host core)"),
-        "parity_on_sample": {"copy_mismatched_elements": mismatches,
-                             "rowsum_worst_scaled_error": worst},
+        "value": round(alln if alln is not None else one, 4), "unit": "GB/s",
+        "cores": cores if alln is not None else 1, "kind": "oracle",
+        "sample": (f"row blocks of {blk3} (copy) / {blk4} (row sum) rows, in proportion "
+                   f"to their bytes: on 1 core {rows1[0]} of {COPY['M']} copy rows and "
+                   f"{rows1[1]} of {ROWSUM['M']} row-sum rows ({bytes1 / 1e9:.3f} GB "
+                   f"algorithmic, {t1:.2f} s); on {cores} cores, one block per thread, "
+                   f"{state['r3']} and {state['r4']} rows ({bytesn / 1e9:.3f} GB, "
+                   f"{tn:.2f} s)"),
+        "single_core": {"value": round(one, 4) if one else None, "unit": "GB/s", "cores": 1},
+        "host_memcpy_gbs_1_thread": round(host_memcpy_gbs(), 2),
+        "parity_on_sample": {"copy_mismatched_elements": checks["mismatches"],
+                             "rowsum_worst_scaled_error": checks["worst"]},
     }
 
 
@@ -649,33 +722,38 @@ def bench_sweep(args):
 # the reference arm: the CPU oracle
 # ---------------------------------------------------------------------------
 def bench_reference(args):
-    """Time the CPU oracle as it stands, one bounded sample of the workload
-    per step (row blocks of both matrices in proportion to their bytes)."""
+    """Time the CPU oracle as it stands on the host's cores: each step is one
+    bounded sample of the workload (row blocks of both matrices in
+    proportion to their bytes), split into disjoint row blocks that run on
+    as many host threads as there are cores."""
     import oracle
     import synthetic
 
     oracle.build()
-    rows3, rows4 = 512, 128   # about 16 + 16 MiB of input per step
+    cores = host_cores()
+    rows3, rows4 = 32 * cores, 8 * cores   # 1 + 1 MiB of input per thread per step
     x3 = synthetic.make_matrix(rows3, COPY["N"], COPY["dtype"], COPY["dist"], COPY["seed"])
     x4 = synthetic.make_matrix(rows4, ROWSUM["N"], ROWSUM["dtype"], ROWSUM["dist"],
                                ROWSUM["seed"])
     d3 = torch.empty_like(x3)
+    jobs = []
+    for i in range(cores):
+        a3, a4 = slice(32 * i, 32 * (i + 1)), slice(8 * i, 8 * (i + 1))
+        jobs.append(lambda a3=a3, a4=a4: (oracle.copy(x3[a3], d3[a3]), oracle.rowsum(x4[a4])))
 
-    def step():
-        oracle.copy(x3, d3)
-        oracle.rowsum(x4)
-
-    for _ in range(args.warmup):
-        step()
-    t = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    sec = time.perf_counter() - t
+    with concurrent.futures.ThreadPoolExecutor(max_workers=cores) as pool:
+        for _ in range(args.warmup):
+            oracle_blocks_parallel(jobs, pool)
+        sec = 0.0
+        for _ in range(args.steps):
+            sec += oracle_blocks_parallel(jobs, pool)
+    if not torch.equal(d3.view(torch.int16), x3.view(torch.int16)):
+        raise RuntimeError("oracle copy differs from its input")
     nbytes = 2 * x3.numel() * 2 + x4.numel() * 2 + 4 * rows4
     value = nbytes * args.steps / sec / 1e9
     sample = (f"each step: oracle copy of {rows3} rows of the fp16 16384x16384 matrix and "
               f"oracle row sum of {rows4} rows of the bf16 8192x65536 matrix "
-              f"({nbytes / 1e6:.1f} MB algorithmic), 1 host core")
+              f"({nbytes / 1e6:.1f} MB algorithmic), split over {cores} host threads")
     return {
         "impl": "reference",
         "metric": "achieved HBM GB/s (read+write) for pipelined tile copy + rowsum",
@@ -685,7 +763,7 @@ def bench_reference(args):
         "dtype": "f16 copy + bf16->f64 rowsum", "data": "synthetic (seeded)",
         "config": {"workload": ("tile_copy fp16 16384x16384 tile 128x64 + tile_rowsum "
                                 "bf16 8192x65536 tile 64x256 (row-block sample per step)")},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
