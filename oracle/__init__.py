@@ -9,6 +9,7 @@ Contents, each pinned by ``tests/test_oracle_*.py`` against what the pages fix:
 
 * ``copy``            -- the tile copy's result (plain C, ``oracle_ref.c``).
 * ``rowsum``          -- binary64 row sums (plain C, ``oracle_ref.c``).
+* ``colsum``          -- binary64 column sums (plain C, ``oracle_ref.c``).
 * ``f16_to_f64`` ...  -- exact element widening (plain C).
 * ``pipeline_state``  -- the (index, phase, count) ring cursor.
 * ``mbarrier``        -- the mbarrier phase / arrival / tx-count model.
@@ -77,6 +78,8 @@ def _load():
                                           ctypes.c_void_p, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
             lib.oracle_rowsum.restype = None
+            lib.oracle_colsum.argtypes = lib.oracle_rowsum.argtypes
+            lib.oracle_colsum.restype = None
             _lib = lib
     return _lib
 
@@ -123,6 +126,20 @@ def rowsum(src: torch.Tensor, with_sumsq: bool = False):
     sums = torch.empty(M, dtype=torch.float64)
     sumsq = torch.empty(M, dtype=torch.float64) if with_sumsq else None
     _load().oracle_rowsum(src.data_ptr(), sums.data_ptr(),
+                          sumsq.data_ptr() if with_sumsq else None,
+                          M, N, src.stride(0), _DTYPE_CODE[src.dtype])
+    return (sums, sumsq) if with_sumsq else sums
+
+
+def colsum(src: torch.Tensor, with_sumsq: bool = False):
+    """Binary64 column sums of the logical matrix ``src`` (a CPU view)."""
+    _check_2d(src, "src")
+    if src.dtype not in _DTYPE_CODE:
+        raise ValueError("unsupported dtype")
+    M, N = src.shape
+    sums = torch.empty(N, dtype=torch.float64)
+    sumsq = torch.empty(N, dtype=torch.float64) if with_sumsq else None
+    _load().oracle_colsum(src.data_ptr(), sums.data_ptr(),
                           sumsq.data_ptr() if with_sumsq else None,
                           M, N, src.stride(0), _DTYPE_CODE[src.dtype])
     return (sums, sumsq) if with_sumsq else sums

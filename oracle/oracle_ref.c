@@ -17,6 +17,12 @@
  *                      element widened exactly to binary64 and added in column
  *                      order in binary64.  Optionally also sum of squares, used
  *                      by the tests to scale the row-sum tolerance.
+ *   oracle_colsum      Column-sum result: out[j] = sum over i < M of x[i][j],
+ *                      every element widened exactly to binary64 and added in
+ *                      row order in binary64; optionally also the sum of
+ *                      squares of each column.  Like the row sum, not on the
+ *                      pages (their consumer only "uses" the tile): the plain
+ *                      definition of a second reduction of the same tiles.
  *   oracle_f16_to_f64  Exact widening of IEEE binary16 (sign, 5-bit exponent
  *                      with bias 15, 10-bit fraction; exponent 0 = subnormal,
  *                      exponent 31 = infinity or NaN).
@@ -103,5 +109,24 @@ void oracle_rowsum(const void *src, double *sums, double *sumsq, int64_t M,
         sums[i] = s;
         if (sumsq)
             sumsq[i] = q;
+    }
+}
+
+/* Column sums of the logical M x N matrix in binary64.  sums[j] receives the
+ * sum of column j; sumsq (may be NULL) receives the sum of squares of column
+ * j.  The loop walks each column from row 0 to row M - 1. */
+void oracle_colsum(const void *src, double *sums, double *sumsq, int64_t M,
+                   int64_t N, int64_t ld, int dtype)
+{
+    for (int64_t j = 0; j < N; ++j) {
+        double s = 0.0, q = 0.0;
+        for (int64_t i = 0; i < M; ++i) {
+            double x = element(src, i * ld + j, dtype);
+            s += x;
+            q += x * x;
+        }
+        sums[j] = s;
+        if (sumsq)
+            sumsq[j] = q;
     }
 }
