@@ -114,19 +114,23 @@ void oracle_rowsum(const void *src, double *sums, double *sumsq, int64_t M,
 
 /* Column sums of the logical M x N matrix in binary64.  sums[j] receives the
  * sum of column j; sumsq (may be NULL) receives the sum of squares of column
- * j.  The loop walks each column from row 0 to row M - 1. */
+ * j.  Every column's elements are added from row 0 to row M - 1; the rows
+ * are visited one after the other (each row updates all N running sums), so
+ * memory is read in its row-major order. */
 void oracle_colsum(const void *src, double *sums, double *sumsq, int64_t M,
                    int64_t N, int64_t ld, int dtype)
 {
     for (int64_t j = 0; j < N; ++j) {
-        double s = 0.0, q = 0.0;
-        for (int64_t i = 0; i < M; ++i) {
-            double x = element(src, i * ld + j, dtype);
-            s += x;
-            q += x * x;
-        }
-        sums[j] = s;
+        sums[j] = 0.0;
         if (sumsq)
-            sumsq[j] = q;
+            sumsq[j] = 0.0;
+    }
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double x = element(src, i * ld + j, dtype);
+            sums[j] += x;
+            if (sumsq)
+                sumsq[j] += x * x;
+        }
     }
 }

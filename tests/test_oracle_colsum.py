@@ -85,3 +85,14 @@ def test_colsum_special_values_and_empty():
     assert s[3] == 0.0
     assert oracle.colsum(torch.empty(0, 4, dtype=torch.float16)).tolist() == [0.0] * 4
     assert oracle.colsum(torch.empty(4, 0, dtype=torch.float16)).tolist() == []
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+def test_colsum_equals_rowsum_of_the_transpose_bitwise(dtype):
+    """Column j of x is row j of x^T, and both functions add in index order,
+    so the two binary64 results must agree bit for bit."""
+    M, N = 301, 77
+    x = make_matrix(M, N, dtype, "normal", seed=9, ld=pitched_ld(N, dtype) + 8)[:, :N]
+    s, q = oracle.colsum(x, with_sumsq=True)
+    r, rq = oracle.rowsum(x.t().contiguous(), with_sumsq=True)
+    assert torch.equal(s, r) and torch.equal(q, rq)
