@@ -515,7 +515,7 @@ def bench_only(args):
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    c = ROWSUM if args.only == "rowsum" else COPY
+    c = ROWSUM if args.only in ("rowsum", "colsum") else COPY
     rows = min(args.rows or c["M"], c["M"])
     cols = c["N"] - args.trim_cols
     x = synthetic.make_matrix(rows, cols, c["dtype"], c["dist"], c["seed"], draw_on=str(dev))
@@ -532,6 +532,13 @@ def bench_only(args):
                                    consumer_warps=args.consumer_warps,
                                    ctas_per_sm=args.ctas_per_sm, store_mode=args.store_mode)
         nbytes = 2 * x.numel() * x.element_size()
+    elif args.only == "colsum":
+        y = torch.empty(cols, dtype=torch.float32, device=dev)
+        ws = torch.zeros(1 << 22, dtype=torch.uint8, device=dev)
+        fn = lambda: mbt.tile_colsum(x, y, c["tile_m"], c["tile_n"], args.rowsum_stages,  # noqa: E731
+                                     consumer_warps=args.consumer_warps,
+                                     ctas_per_sm=args.ctas_per_sm, workspace=ws)
+        nbytes = x.numel() * x.element_size() + 4 * cols
     else:
         y = torch.empty(rows, dtype=torch.float32, device=dev)
         ws = torch.zeros(1 << 22, dtype=torch.uint8, device=dev)
@@ -640,6 +647,13 @@ def bench_configs(args):
         ms = med_ms(lambda: mbt.tile_rowsum(x, o, 64, 256, st, workspace=ws), 20)
         line({"config": 4, "op": "rowsum", "shape": [8192, 65536], "tile": [64, 256],
               "stages": st, "ms": round(ms, 4), "gbs": round(rowsum_bytes() / ms / 1e6, 1)})
+    # the second reduction of the same matrix: column sums
+    oc = torch.empty(65536, dtype=torch.float32, device=dev)
+    for st in (2, 3, 4):
+        ms = med_ms(lambda: mbt.tile_colsum(x, oc, 64, 256, st, workspace=ws), 20)
+        line({"config": 4, "op": "colsum", "shape": [8192, 65536], "tile": [64, 256],
+              "stages": st, "ms": round(ms, 4),
+              "gbs": round((8192 * 65536 * 2 + 4 * 65536) / ms / 1e6, 1)})
     del x
     # 5a / 5b: ragged, pitched rows, copy and row sum, 3 stages
     for cfg, dt, M, N, tm, tn, seed in (("5a", "f32", 12289, 8191, 128, 32, 1005),
@@ -657,7 +671,10 @@ def bench_configs(args):
         ms = med_ms(lambda: mbt.tile_rowsum(x[:, :N], o, tm, tn, 3, workspace=ws), 20)
         line({"config": cfg, "op": "rowsum", "shape": [M, N], "ld": ld, "tile": [tm, tn],
               "stages": 3, "ms": round(ms, 4), "gbs": round((M * N * es + 4 * M) / ms / 1e6, 1)})
-        ms_sep = ms
+        oc = torch.empty(N, dtype=torch.float32, device=dev)
+        ms = med_ms(lambda: mbt.tile_colsum(x[:, :N], oc, tm, tn, 3, workspace=ws), 20)
+        line({"config": cfg, "op": "colsum", "shape": [M, N], "ld": ld, "tile": [tm, tn],
+              "stages": 3, "ms": round(ms, 4), "gbs": round((M * N * es + 4 * N) / ms / 1e6, 1)})
         ms = med_ms(lambda: mbt.tile_copy_rowsum(x[:, :N], y[:, :N], o, tm, tn, 3,
                                                  workspace=ws), 20)
         line({"config": cfg, "op": "copy_rowsum (fused)", "shape": [M, N], "ld": ld,
@@ -807,7 +824,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--all-configs", action="store_true")
-    ap.add_argument("--only", choices=["copy", "rowsum", "copy_rowsum"])
+    ap.add_argument("--only", choices=["copy", "rowsum", "copy_rowsum", "colsum"])
     ap.add_argument("--trim-cols", type=int, default=0,
                     help="--only: drop this many columns (an odd count gives a dense matrix "
                          "whose rows are not a multiple of 16 bytes: the 1-D bulk-copy path)")

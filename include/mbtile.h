@@ -171,14 +171,17 @@ typedef struct mbt_plan {
                                 tpr with tpr a multiple of boxes and tile_m x
                                 tpr / boxes a multiple of 32; see
                                 mbt_opts.pipeline for when it is chosen */
-    int32_t reserved0;
+    int32_t col_group;       /* column sum: adjacent column strips taken
+                                together, band by band (2 where the tile row
+                                is 128 bytes and strips are split over CTAs,
+                                else 1); 0 for the other operations */
     int64_t tiles_m;         /* tiles down the rows (row bands) */
     int64_t tiles_n;         /* tiles across the columns */
     int64_t num_tiles;
     size_t workspace_bytes;  /* row sum: workspace bytes this plan needs */
 } mbt_plan;
 
-enum { MBT_OP_COPY = 0, MBT_OP_ROWSUM = 1, MBT_OP_COPY_ROWSUM = 2 };
+enum { MBT_OP_COPY = 0, MBT_OP_ROWSUM = 1, MBT_OP_COPY_ROWSUM = 2, MBT_OP_COLSUM = 3 };
 
 /*
  * tile_copy -- dst[i][j] = src[i][j], bit for bit, for 0 <= i < M, 0 <= j < N.
@@ -243,6 +246,37 @@ int tile_copy_rowsum(const void *src, void *dst, float *out, int64_t M, int64_t 
 int tile_copy_rowsum_ex(const void *src, void *dst, float *out, int64_t M, int64_t N,
                         int tile_m, int tile_n, int stages, int dtype, void *stream,
                         const mbt_opts *opts);
+
+/*
+ * tile_colsum -- out[j] = sum over i < M of src[i][j] in fp32, 0 <= j < N.
+ *
+ * A second reduction of the same pipeline's tiles ("cute(12) async_pipeline"
+ * §3: the consumer uses each landed tile; the pages name no reduction, this is
+ * the plain definition).  The producer takes the tiles in strip-major order --
+ * down each column strip of tile_n columns -- so the consumer threads keep
+ * their columns' sums in registers across a strip; 32 x consumer_warps
+ * threads are split over the tile row's 16-byte chunks (at least one thread
+ * per chunk: tile_n * element size <= 32 x consumer_warps x 16 bytes, else
+ * MBT_ERR_UNSUPPORTED).  out: device fp32[N], 4-byte aligned.  Elements are
+ * widened exactly; each thread adds its rows in order, the threads of a
+ * column and the CTAs sharing a strip are combined in a fixed order, so
+ * repeated calls with the same plan give bit-identical sums.  The row pitch
+ * must be a multiple of 16 bytes (MBT_ERR_ALIGN otherwise).
+ *
+ * opts: as for tile_rowsum_ex.  With a workspace (see
+ * tile_colsum_workspace_bytes: tickets and partial sums per strip,
+ * zero-filled, 256-byte aligned, left zero-filled) a strip may be split over
+ * several CTAs; without one, each strip is reduced by a single CTA.  M = 0
+ * writes N zeros; N = 0 writes nothing.
+ */
+int tile_colsum(const void *src, float *out, int64_t M, int64_t N, int tile_m,
+                int tile_n, int stages, int dtype, void *stream);
+int tile_colsum_ex(const void *src, float *out, int64_t M, int64_t N, int tile_m,
+                   int tile_n, int stages, int dtype, void *stream,
+                   const mbt_opts *opts);
+int tile_colsum_workspace_bytes(int64_t M, int64_t N, int tile_m, int tile_n,
+                                int stages, int dtype, const mbt_opts *opts,
+                                size_t *bytes);
 
 /* Workspace bytes tile_rowsum_ex needs on the current device for this shape
  * and these options (opts->workspace is ignored).  0 when no split helps. */

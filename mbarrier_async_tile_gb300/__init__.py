@@ -27,7 +27,7 @@ __all__ = [
 
 MBT_OK = 0
 MBT_ERR_TIMEOUT = -6
-OP_COPY, OP_ROWSUM, OP_COPY_ROWSUM = 0, 1, 2
+OP_COPY, OP_ROWSUM, OP_COPY_ROWSUM, OP_COLSUM = 0, 1, 2, 3
 DTYPE_CODE = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
 
 
@@ -68,7 +68,7 @@ class Plan(ctypes.Structure):
         ("kmax", ctypes.c_int32),
         ("flat", ctypes.c_int32),
         ("box_barriers", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32),
+        ("col_group", ctypes.c_int32),
         ("tiles_m", ctypes.c_int64),
         ("tiles_n", ctypes.c_int64),
         ("num_tiles", ctypes.c_int64),
@@ -128,6 +128,11 @@ def _load():
         lib.tile_device_info.argtypes = [i32, ctypes.POINTER(ctypes.c_int),
                                          ctypes.POINTER(ctypes.c_int),
                                          ctypes.POINTER(ctypes.c_double)]
+        lib.tile_colsum.argtypes = sig
+        lib.tile_colsum_ex.argtypes = sig + [ctypes.POINTER(Opts)]
+        lib.tile_colsum_workspace_bytes.argtypes = [i64, i64, i32, i32, i32, i32,
+                                                    ctypes.POINTER(Opts),
+                                                    ctypes.POINTER(ctypes.c_size_t)]
         host_sig = [vp, vp, i64, i64, i32, i32, i32, i32, ctypes.POINTER(Opts)]
         lib.tile_copy_host.argtypes = host_sig
         lib.tile_rowsum_host.argtypes = host_sig
@@ -136,7 +141,8 @@ def _load():
                      "tile_copy_rowsum", "tile_copy_rowsum_ex",
                      "tile_rowsum_workspace_bytes", "tile_copy_rowsum_workspace_bytes",
                      "tile_plan", "tile_status", "tile_device_info",
-                     "tile_copy_host", "tile_rowsum_host", "tile_host_release"):
+                     "tile_copy_host", "tile_rowsum_host", "tile_host_release",
+                     "tile_colsum", "tile_colsum_ex", "tile_colsum_workspace_bytes"):
             getattr(lib, name).restype = ctypes.c_int
         _C = lib
         return lib
@@ -232,15 +238,17 @@ _ws_lock = threading.Lock()
 _ws_cache: dict[int, torch.Tensor] = {}
 
 
-def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+def _workspace(device: torch.device, nbytes: int, stream=None) -> torch.Tensor:
     """A zero-filled byte buffer of at least ``nbytes`` on ``device``, reused
-    across calls (the kernels leave it zero-filled)."""
+    across calls on the same stream (the kernels leave it zero-filled; calls
+    on different streams may overlap, so each stream has its own)."""
     idx = device.index if device.index is not None else torch.cuda.current_device()
+    key = (idx, _stream_handle(stream))
     with _ws_lock:
-        buf = _ws_cache.get(idx)
+        buf = _ws_cache.get(key)
         if buf is None or buf.numel() < nbytes:
             buf = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
-            _ws_cache[idx] = buf
+            _ws_cache[key] = buf
         return buf
 
 
@@ -260,6 +268,50 @@ def tile_rowsum_workspace_bytes(M: int, N: int, tile_m: int, tile_n: int, stages
     rc = fn(M, N, tile_m, tile_n, stages, DTYPE_CODE[dtype], ctypes.byref(o), ctypes.byref(out))
     _check(rc, "tile_rowsum_workspace_bytes")
     return out.value
+
+
+def tile_colsum_workspace_bytes(M: int, N: int, tile_m: int, tile_n: int, stages: int,
+                                dtype: torch.dtype, **opt) -> int:
+    """Workspace bytes of tile_colsum."""
+    o = _opts(**opt)
+    out = ctypes.c_size_t(0)
+    rc = _load().tile_colsum_workspace_bytes(M, N, tile_m, tile_n, stages, DTYPE_CODE[dtype],
+                                             ctypes.byref(o), ctypes.byref(out))
+    _check(rc, "tile_colsum_workspace_bytes")
+    return out.value
+
+
+def tile_colsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int = 64,
+                tile_n: int = 256, stages: int = 2, *, split: bool = True,
+                consumer_warps: int = 0, max_ctas: int = 0, ctas_per_sm: int = 0,
+                wait_budget_ns: int = 0, log: torch.Tensor | None = None, fault: int = 0,
+                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[j] = sum_i src[i, j] in fp32 through the tile pipeline (tiles taken
+    down each column strip).  With ``split`` (default) strips may be shared by
+    several CTAs, using a zero-filled workspace (cached per device and stream
+    unless one is given)."""
+    M, N, ld_s = _matrix(src, "src")
+    if out is None:
+        out = torch.empty(N, dtype=torch.float32, device=src.device)
+    if out.dtype != torch.float32 or out.numel() != N or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor of N elements")
+    o = _opts(ld_src=ld_s, consumer_warps=consumer_warps, max_ctas=max_ctas,
+              ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault)
+    if log is not None:
+        o.log = log.data_ptr()
+        o.log_capacity = log.numel() // 8
+    if split and M > 0 and N > 0:
+        need = tile_colsum_workspace_bytes(M, N, tile_m, tile_n, stages, src.dtype,
+                                           ld_src=ld_s, consumer_warps=consumer_warps,
+                                           max_ctas=max_ctas, ctas_per_sm=ctas_per_sm)
+        if need:
+            ws = workspace if workspace is not None else _workspace(src.device, need, stream)
+            o.workspace = ws.data_ptr()
+            o.workspace_bytes = ws.numel() * ws.element_size()
+    rc = _load().tile_colsum_ex(src.data_ptr(), out.data_ptr(), M, N, tile_m, tile_n, stages,
+                                DTYPE_CODE[src.dtype], _stream_handle(stream), ctypes.byref(o))
+    _check(rc, "tile_colsum")
+    return out
 
 
 def tile_rowsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int = 64,
@@ -292,7 +344,7 @@ def tile_rowsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int 
                                            ld_src=ld_s, consumer_warps=consumer_warps,
                                            max_ctas=max_ctas, ctas_per_sm=ctas_per_sm)
         if need:
-            ws = workspace if workspace is not None else _workspace(src.device, need)
+            ws = workspace if workspace is not None else _workspace(src.device, need, stream)
             o.workspace = ws.data_ptr()
             o.workspace_bytes = ws.numel() * ws.element_size()
     rc = _load().tile_rowsum_ex(src.data_ptr(), out.data_ptr(), M, N, tile_m, tile_n, stages,
@@ -327,7 +379,7 @@ def tile_copy_rowsum(src: torch.Tensor, dst: torch.Tensor, out: torch.Tensor | N
                                            consumer_warps=consumer_warps,
                                            max_ctas=max_ctas, ctas_per_sm=ctas_per_sm)
         if need:
-            ws = workspace if workspace is not None else _workspace(src.device, need)
+            ws = workspace if workspace is not None else _workspace(src.device, need, stream)
             o.workspace = ws.data_ptr()
             o.workspace_bytes = ws.numel() * ws.element_size()
     rc = _load().tile_copy_rowsum_ex(src.data_ptr(), dst.data_ptr(), out.data_ptr(), M, N,

@@ -21,7 +21,14 @@ constexpr uint64_t kDefaultWaitBudgetNs = 1000000000ull;  // 1 s
 struct PipeArgs {
     int64_t M, N;              // logical shape
     int64_t tiles_n;           // tiles across the columns
+    int64_t tiles_m;           // tiles down the rows
     int64_t num_tiles;         // tiles_m * tiles_n
+    int32_t col_group;         // tile order of the producer.  0: row-major (tile t
+                               // is (t / tiles_n, t % tiles_n)).  g >= 1: column
+                               // strips in groups of g adjacent strips (the last
+                               // group may be narrower); a group's tiles are taken
+                               // band by band, left to right within a band
+    int32_t pad_pipe_;
     int32_t tile_m;            // rows per tile (= rows per box)
     int32_t boxes;             // 128-byte boxes per tile row: 1, 2, 4 or 8
     int32_t box_inner;         // elements per box row (128 / esize)
@@ -65,6 +72,62 @@ struct RowsumArgs {
     int64_t ld_dst_bytes;
 };
 
+// Column sums (mbtile_colsum.cuh): tiles in strip-major order, each column
+// strip (tile_n columns) reduced down the rows.
+constexpr int kMaxColGroup = 2;
+
+// Position of tile t in the strip-group order (PipeArgs.col_group = g >= 1).
+struct ColPos {
+    int64_t gstart;            // order position of the group's first tile
+    int32_t gi;                // group index
+    int32_t band;              // tile row (row band)
+    int32_t kloc, wg;          // strip within its group, strips in the group
+    // (M, N < 2^31, so bands and strips fit 32 bits; order positions need 64)
+};
+
+__host__ __device__ inline ColPos col_pos(int64_t t, int64_t tiles_m, int64_t tiles_n, int g) {
+    ColPos c;
+    const int64_t per = tiles_m * g;
+    const int64_t gi = t / per;
+    c.gi = static_cast<int32_t>(gi);
+    c.gstart = gi * per;
+    const int64_t left = tiles_n - gi * g;
+    c.wg = static_cast<int32_t>(left < g ? left : g);
+    const int64_t local = t - c.gstart;
+    c.band = static_cast<int32_t>(local / c.wg);
+    c.kloc = static_cast<int32_t>(local - static_cast<int64_t>(c.band) * c.wg);
+    return c;
+}
+
+__host__ __device__ inline int64_t col_strip(const ColPos &c, int g) {
+    return static_cast<int64_t>(c.gi) * g + c.kloc;
+}
+
+// The position of the next tile in the same order (no divisions).
+__host__ __device__ inline void col_next(ColPos &c, int64_t tiles_m, int64_t tiles_n, int g) {
+    if (++c.kloc == c.wg) {
+        c.kloc = 0;
+        if (++c.band == tiles_m) {
+            c.band = 0;
+            ++c.gi;
+            c.gstart += tiles_m * g;
+            const int64_t left = tiles_n - static_cast<int64_t>(c.gi) * g;
+            c.wg = static_cast<int32_t>(left < g ? left : g);
+        }
+    }
+}
+
+struct ColsumArgs {
+    PipeArgs p;                // col_group >= 1
+    float *out;                // [N]
+    float *partial;            // [strips][kmax][tile_n], used when kmax > 1
+    int32_t *ticket;           // [strips], zero between calls
+    int64_t units;             // scheduling units = num_tiles / gran
+    int64_t gran;              // tiles per scheduling unit (1 or tiles_m)
+    int32_t kmax;
+    int32_t tile_n;            // columns per tile
+};
+
 // Matrices whose row pitch is not a multiple of 16 bytes (mbtile_flat.cuh).
 struct FlatArgs {
     PipeArgs p;                // M, N, esize, stages, consumer_warps, stage_stride, ...
@@ -87,6 +150,8 @@ cudaError_t launch_copy(const CUtensorMap &map, const CUtensorMap &dst_map,
 cudaError_t launch_rowsum(int dtype, const CUtensorMap &map, const CUtensorMap &dst_map,
                           const RowsumArgs &a, int grid, int threads, int smem,
                           cudaStream_t stream);
+cudaError_t launch_colsum(int dtype, const CUtensorMap &map, const ColsumArgs &a, int grid,
+                          int threads, int smem, cudaStream_t stream);
 cudaError_t launch_copy_unified(const CUtensorMap &map, const CopyArgs &a, int grid,
                                 int threads, int smem, cudaStream_t stream);
 cudaError_t launch_copy_flat(const FlatArgs &a, int grid, int threads, int smem,
@@ -102,7 +167,7 @@ cudaError_t launch_fill_zero(float *out, int64_t n, cudaStream_t stream);
 cudaError_t set_kernel_smem_limit(int optin, int *usable);
 // CTAs of a kernel with this block/smem shape that fit on one SM; kernel
 // MBT_OP_COPY, MBT_OP_ROWSUM, MBT_OP_COPY_ROWSUM, 3 = unified copy,
-// 4 = flat copy, 5 = flat row sum.
+// 4 = flat copy, 5 = flat row sum, 6 = column sum.
 cudaError_t kernel_fit_per_sm(int op, int dtype, int threads, int smem, int *fit);
 // Read the device status word and clear it (synchronous).
 cudaError_t read_and_clear_status(int32_t info[4]);

@@ -1,0 +1,251 @@
+// Column sums through the tile pipeline: out[j] = sum over rows i < M of
+// x[i][j], fp32.
+//
+// The same producer / consumer ring as the row sum (one elected producer
+// thread issues each tile's bulk tensor copies against the stage's full
+// barrier, consumer warps wait on it, read the swizzled stage and release it
+// with one arrive per warp), but the tiles are taken down the column strips
+// (tile_n columns each), so each consumer thread keeps its columns' sums in
+// registers across a strip's tiles.
+//
+// Order.  The column strips are taken in groups of col_group adjacent strips
+// (2 strips where a tile row is 128 bytes, so that the copies in flight read
+// 256 contiguous bytes of each row, not scattered 128-byte pieces); within a group the
+// tiles go band by band, left to right.  Each consumer thread keeps one set of
+// accumulators per strip of the group.
+//
+// Consumer mapping.  A tile row holds cpr = boxes x 8 chunks of 16 bytes;
+// tpc = 32 W / cpr threads share each chunk column: thread (q, g) with
+// q = ctid / tpc, g = ctid % tpc sums rows g, g + tpc, ... of chunk column q
+// into EPC fp32 accumulators (EPC = elements per chunk: 8, or 4 for fp32).
+// Eight consecutive threads read eight consecutive rows of the same chunk,
+// which the 128-byte swizzle spreads over all banks.  When a CTA leaves a
+// group, the tpc partial sums of each column are added in g order; a strip
+// that several CTAs share is combined by the last of them in CTA order
+// (tickets and partials in the caller's workspace, left zeroed).
+//
+// Included by mbtile_kernels.cu inside its anonymous namespace: it uses that
+// file's PTX wrappers, bounded waits, producer, status word and log.
+
+constexpr int kColsumRedFloats = 32 * kMaxConsumerWarps * 8;   // threads x EPC (max)
+
+template <int DT>
+__device__ __forceinline__ void chunk_accumulate(float *acc, const uint4 &v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (DT == MBT_F32) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] += __uint_as_float(w[k]);
+    } else if constexpr (DT == MBT_BF16) {
+        // bf16 -> fp32 is exact: the 16 bits are the top half of the fp32.
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            acc[2 * k] += __uint_as_float(w[k] << 16);
+            acc[2 * k + 1] += __uint_as_float(w[k] & 0xffff0000u);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+            acc[2 * k] += f.x;
+            acc[2 * k + 1] += f.y;
+        }
+    }
+}
+
+// Finish this CTA's share of one strip: add the tpc partials of each column
+// in g order, then write out (sole contributor) or deposit the CTA's partials
+// and let the last contributing CTA add those of all contributors in CTA
+// order.  pos_first / pos_last: order positions of the strip's first and last
+// tile; the contributors are the CTAs owning them and every CTA in between.
+template <int EPC>
+__device__ __forceinline__ bool flush_strip(const ColsumArgs &a, int64_t strip, int64_t pos_first,
+                            int64_t pos_last, const float *acc, bool active, int q, int g,
+                            int tpc, float *red, int *last_flag, FlushCtl &f, const WaitCtl &w,
+                            int ctid, int nthr) {
+    const PipeArgs &p = a.p;
+    const int tn = a.tile_n;
+    const int64_t G = gridDim.x;
+    const int64_t b_first = unit_owner(pos_first, a.gran, a.units, G);
+    const int64_t b_last = unit_owner(pos_last, a.gran, a.units, G);
+    if (static_cast<int64_t>(blockIdx.x) < b_first || static_cast<int64_t>(blockIdx.x) > b_last)
+        return true;   // not a contributor of this strip
+    if (active) {
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) red[g * tn + q * EPC + e] = acc[e];
+    }
+    if (!consumers_sync(f, w)) return false;
+    const int64_t K = b_last - b_first + 1;
+    const int64_t col0 = strip * tn;
+    float *slot = a.partial + (strip * a.kmax + (blockIdx.x - b_first)) * tn;
+    for (int c = ctid; c < tn; c += nthr) {
+        float v = red[c];
+        for (int s = 1; s < tpc; ++s) v += red[s * tn + c];
+        if (K == 1) {
+            if (col0 + c < p.N) a.out[col0 + c] = v;
+        } else {
+            slot[c] = v;
+        }
+    }
+    if (K == 1) return consumers_sync(f, w);   // red[] may be rewritten after this
+    __threadfence();
+    if (!consumers_sync(f, w)) return false;
+    if (ctid == 0) {
+        const int old = atomicAdd(&a.ticket[strip], 1);
+        *last_flag = (old == K - 1);
+    }
+    if (!consumers_sync(f, w)) return false;
+    if (*last_flag) {
+        __threadfence();
+        float *base = a.partial + strip * a.kmax * tn;
+        for (int c = ctid; c < tn; c += nthr) {
+            float total = 0.f;
+            for (int64_t k = 0; k < K; ++k) {
+                total += __ldcg(base + k * tn + c);
+                base[k * tn + c] = 0.f;   // leave the workspace zero-filled
+            }
+            if (col0 + c < p.N) a.out[col0 + c] = total;
+        }
+        if (ctid == 0) a.ticket[strip] = 0;
+    }
+    return true;
+}
+
+// Flush every strip of the group that starts at order position gstart.
+template <int EPC, int GMAX>
+__device__ __forceinline__ bool flush_group(const ColsumArgs &a, int64_t gstart, float (*acc)[EPC],
+                            bool active, int q, int g, int tpc, float *red, int *last_flag,
+                            FlushCtl &f, const WaitCtl &w, int ctid, int nthr) {
+    const PipeArgs &p = a.p;
+    const ColPos c0 = col_pos(gstart, p.tiles_m, p.tiles_n, GMAX);
+#pragma unroll
+    for (int k = 0; k < GMAX; ++k) {
+        if (k >= c0.wg) break;
+        const int64_t first = gstart + k;
+        const int64_t last = gstart + (p.tiles_m - 1) * c0.wg + k;
+        if (!flush_strip<EPC>(a, col_strip(c0, GMAX) + k, first, last, acc[k], active,
+                              q, g, tpc, red,
+                              last_flag, f, w, ctid, nthr))
+            return false;
+    }
+    return true;
+}
+
+// GMAX: strips per group (= p.col_group; the launch picks the instantiation).
+template <int DT, int GMAX>
+__device__ void consume_colsum(const ColsumArgs &a, const Smem &sm, const WaitCtl &w,
+                               int64_t first, int64_t count, float *red, int *last_flag,
+                               FlushCtl &f) {
+    constexpr int EPC = DT == MBT_F32 ? 4 : 8;
+    const PipeArgs &p = a.p;
+    const int ctid = static_cast<int>(threadIdx.x) - 32;
+    const int lane = threadIdx.x & 31;
+    const int nthr = p.consumer_warps * 32;
+    const int cpr = p.boxes * 8;
+    const int tpc = nthr / cpr;                      // threads per chunk column (>= 1)
+    const bool active = ctid < cpr * tpc;
+    const int q = active ? ctid / tpc : 0;
+    const int g = active ? ctid % tpc : 0;
+    float acc[GMAX][EPC];
+#pragma unroll
+    for (int k = 0; k < GMAX; ++k)
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) acc[k][e] = 0.f;
+    // 16-byte loads in flight per thread and round (fewer when a thread keeps
+    // two strips' accumulators, to stay within the registers of 2 CTAs/SM).
+    constexpr int CV = GMAX == 1 ? kVec : kVec / 2;
+    int64_t group = -1;   // order position of the current group's first tile
+    const int most = (p.tile_m + tpc - 1) / tpc;
+    const int rounds = (most + CV - 1) / CV;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    // The launch picks GMAX = p.col_group, so the group width is a constant here.
+    ColPos c = col_pos(first, p.tiles_m, p.tiles_n, GMAX);
+    for (int64_t j = 0; j < count; ++j, col_next(c, p.tiles_m, p.tiles_n, GMAX)) {
+        const int64_t tile = first + j;
+        if (c.gstart != group) {
+            if (group >= 0 && !flush_group<EPC, GMAX>(a, group, acc, active, q, g, tpc, red,
+                                                      last_flag, f, w, ctid, nthr)) {
+                ok = false;
+                break;
+            }
+            group = c.gstart;
+#pragma unroll
+            for (int k = 0; k < GMAX; ++k)
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) acc[k][e] = 0.f;
+        }
+        const uint32_t full_bar = sm.full0 + 8u * stage;
+        bool got = wait_bounded(full_bar, phase, w, true);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) {
+            if (lane == 0) {
+                report_timeout(1, stage, phase);
+                *w.abort = 1;
+            }
+            ok = false;
+            break;
+        }
+        if (ctid == 0) log_record(p, 1, j, stage, phase, tile);
+        // Rows of this tile inside the matrix (the copy engine zero-fills the
+        // rest; skipping them saves the reads).
+        const int64_t left = p.M - static_cast<int64_t>(c.band) * p.tile_m;
+        const int rows = left < p.tile_m ? static_cast<int>(left) : p.tile_m;
+        const int mine = active && g < rows ? (rows - g + tpc - 1) / tpc : 0;
+        const uint32_t rbase = sm.base + stage * p.stage_stride;
+        for (int r = 0; r < rounds; ++r) {
+            uint4 v[CV];
+#pragma unroll
+            for (int u = 0; u < CV; ++u) {
+                const int k = r * CV + u;
+                if (k < mine) v[u] = lds128(rbase + chunk_offset(g + k * tpc, q, p.box_stride));
+            }
+            if (r == rounds - 1) {
+                __syncwarp();
+                if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+            }
+            // The strip's accumulators, selected without indexing registers
+            // by a run-time value.
+#pragma unroll
+            for (int s = 0; s < GMAX; ++s) {
+                if (s != c.kloc) continue;
+#pragma unroll
+                for (int u = 0; u < CV; ++u) {
+                    const int k = r * CV + u;
+                    if (k < mine) chunk_accumulate<DT>(acc[s], v[u]);
+                }
+            }
+        }
+        if (++stage == static_cast<uint32_t>(p.stages)) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+    if (ok && group >= 0)
+        flush_group<EPC, GMAX>(a, group, acc, active, q, g, tpc, red, last_flag, f, w, ctid, nthr);
+}
+
+template <int DT, int GMAX>
+__global__ void __launch_bounds__(kMaxThreads, 2)
+    mbt_colsum_kernel(const __grid_constant__ CUtensorMap map, const ColsumArgs a) {
+    extern __shared__ __align__(1024) unsigned char dyn_smem[];
+    __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
+    __shared__ __align__(8) uint64_t flush_bar;
+    __shared__ float red[kColsumRedFloats];   // [tpc][tile_n] partial column sums
+    __shared__ int abort_flag;
+    __shared__ int last_flag;
+    Smem sm;
+    init_pipeline(a.p, sm, bars, &abort_flag, &flush_bar,
+                  static_cast<uint32_t>(a.p.consumer_warps), dyn_smem);
+    WaitCtl w{a.p.wait_budget_ns, &abort_flag};
+    // Contiguous, evenly split range of scheduling units, in strip-major order.
+    const int64_t G = gridDim.x;
+    const int64_t b = blockIdx.x;
+    const int64_t first = (b * a.units / G) * a.gran;
+    const int64_t last = ((b + 1) * a.units / G) * a.gran;
+    if (threadIdx.x < 32) {
+        if (threadIdx.x == 0) produce(&map, a.p, sm, w, first, 1, last - first);
+        return;
+    }
+    FlushCtl f{smem_u32(&flush_bar), 0u};
+    consume_colsum<DT, GMAX>(a, sm, w, first, last - first, red, &last_flag, f);
+}

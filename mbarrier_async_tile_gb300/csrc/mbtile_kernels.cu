@@ -225,8 +225,15 @@ __device__ void produce(const CUtensorMap *map, const PipeArgs &p, const Smem &s
     const uint32_t box_tx = p.tx_bytes / static_cast<uint32_t>(p.boxes);
     for (int64_t j = 0; j < count; ++j) {
         const int64_t tile = first + j * step;
-        const int64_t tm = tile / p.tiles_n;
-        const int64_t tn = tile - tm * p.tiles_n;
+        int64_t tm, tn;
+        if (p.col_group) {
+            const ColPos c = col_pos(tile, p.tiles_m, p.tiles_n, p.col_group);
+            tm = c.band;
+            tn = col_strip(c, p.col_group);
+        } else {
+            tm = tile / p.tiles_n;
+            tn = tile - tm * p.tiles_n;
+        }
         const int32_t y = static_cast<int32_t>(tm * p.tile_m);
         const int32_t x0 = static_cast<int32_t>(tn * p.boxes * p.box_inner);
         const uint32_t dst = sm.base + stage * p.stage_stride;
@@ -848,6 +855,7 @@ __global__ void mbt_fill_zero_kernel(float *out, int64_t n) {
 }
 
 #include "mbtile_flat.cuh"
+#include "mbtile_colsum.cuh"
 
 // Debug: one CTA loads tile (row0, col0) exactly as the pipelines do (one
 // bulk tensor copy per 128-byte box, completion on an mbarrier with the
@@ -920,6 +928,32 @@ cudaError_t launch_rowsum(int dtype, const CUtensorMap &map, const CUtensorMap &
                    : launch_rowsum_t<false>(dtype, map, dst_map, a, grid, threads, smem, stream);
 }
 
+template <int GMAX>
+void launch_colsum_t(int dtype, const CUtensorMap &map, const ColsumArgs &a, int grid,
+                     int threads, int smem, cudaStream_t stream) {
+    switch (dtype) {
+        case MBT_F16:
+            mbt_colsum_kernel<MBT_F16, GMAX><<<grid, threads, smem, stream>>>(map, a);
+            break;
+        case MBT_BF16:
+            mbt_colsum_kernel<MBT_BF16, GMAX><<<grid, threads, smem, stream>>>(map, a);
+            break;
+        default:
+            mbt_colsum_kernel<MBT_F32, GMAX><<<grid, threads, smem, stream>>>(map, a);
+            break;
+    }
+}
+
+cudaError_t launch_colsum(int dtype, const CUtensorMap &map, const ColsumArgs &a, int grid,
+                          int threads, int smem, cudaStream_t stream) {
+    if (a.p.col_group < 1 || a.p.col_group > kMaxColGroup) return cudaErrorInvalidValue;
+    if (a.p.col_group == 1)
+        launch_colsum_t<1>(dtype, map, a, grid, threads, smem, stream);
+    else
+        launch_colsum_t<2>(dtype, map, a, grid, threads, smem, stream);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_copy_unified(const CUtensorMap &map, const CopyArgs &a, int grid, int threads,
                                 int smem, cudaStream_t stream) {
     mbt_copy_unified_kernel<<<grid, threads, smem, stream>>>(map, a);
@@ -976,7 +1010,13 @@ cudaError_t set_kernel_smem_limit(int optin, int *usable) {
                          reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32, false>),
                          reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16, true>),
                          reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16, true>),
-                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32, true>)};
+                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32, true>),
+                         reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F16, 1>),
+                         reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_BF16, 1>),
+                         reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F32, 1>),
+                         reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F16, 2>),
+                         reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_BF16, 2>),
+                         reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F32, 2>)};
     int least = optin;
     for (const void *fn : fns) {
         cudaFuncAttributes attr{};
@@ -1007,6 +1047,10 @@ cudaError_t kernel_fit_per_sm(int op, int dtype, int threads, int smem, int *fit
         fn = dtype == MBT_F16    ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16, true>)
              : dtype == MBT_BF16 ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16, true>)
                                  : reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32, true>);
+    if (op == 6)   // both group widths have the same block shape and limits
+        fn = dtype == MBT_F16    ? reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F16, 2>)
+             : dtype == MBT_BF16 ? reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_BF16, 2>)
+                                 : reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F32, 2>);
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(fit, fn, threads, smem);
 }
 

@@ -41,3 +41,17 @@ def rowsum_errors(got: torch.Tensor, x_cpu: torch.Tensor):
     big = ref.abs() >= sq.sqrt()
     rel = (err[big] / ref.abs()[big]).max().item() if bool(big.any()) else 0.0
     return worst, rel, ref
+
+
+def colsum_errors(got: torch.Tensor, x_cpu: torch.Tensor):
+    """(worst |got - ref| / scale, worst relative error on columns with
+    |ref| >= sqrt(sum of squares), ref) for a logical CPU matrix x_cpu; the
+    column-sum counterpart of rowsum_errors, same tolerance."""
+    ref, sq = oracle.colsum(x_cpu, with_sumsq=True)
+    g = got.detach().cpu().double()
+    scale = torch.maximum(ref.abs(), sq.sqrt()).clamp_min(1e-300)
+    err = (g - ref).abs()
+    worst = (err / scale).max().item() if len(ref) else 0.0
+    big = ref.abs() >= sq.sqrt()
+    rel = (err[big] / ref.abs()[big]).max().item() if bool(big.any()) else 0.0
+    return worst, rel, ref

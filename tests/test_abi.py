@@ -322,6 +322,87 @@ def test_plan_rowsum_split_covers_every_tile_once(M, N, tm, tn, dt, sms, fit):
     assert p["workspace_bytes"] == ((bands * 4 + 255) // 256) * 256 + bands * kmax * tm * 4
 
 
+@pytest.mark.parametrize("M,N,tm,tn,dt,sms,fit", [
+    (8192, 65536, 64, 256, torch.bfloat16, 152, 2),
+    (65536, 8192, 64, 256, torch.bfloat16, 152, 2),
+    (12289, 8191, 128, 32, torch.float32, 152, 3),
+    (24577, 16383, 128, 64, torch.float16, 152, 3),
+    (300, 1000, 16, 64, torch.float16, 7, 1),
+    (64, 64, 64, 64, torch.float16, 152, 4),
+])
+def test_plan_colsum_split_covers_every_tile_once(M, N, tm, tn, dt, sms, fit):
+    """Column sums take tiles in strip-group order: groups of col_group
+    adjacent strips, band by band inside a group.  CTA b owns an even,
+    contiguous range of that order; every tile is owned once, and a strip's
+    contributors are the CTAs from the owner of its first tile to the owner
+    of its last."""
+    es = torch.empty(0, dtype=dt).element_size()
+    ld = -(-N * es // 16) * 16 // es
+    p = _plan(mbt.OP_COLSUM, M, N, tm, tn, 3, dt, sms=sms, fit=fit, ws=True, ld_src=ld)
+    tiles_m, strips, T = p["tiles_m"], p["tiles_n"], p["num_tiles"]
+    if not p["split"]:
+        assert p["workspace_bytes"] == 0 and p["grid"] == min(strips, sms * fit)
+        assert p["col_group"] == 1
+        return
+    g = p["col_group"]
+    assert g == (2 if tn * es == 128 else 1)
+    # order position of every tile, built band by band inside each group
+    pos = {}
+    t = 0
+    for g0 in range(0, strips, g):
+        wg = min(g, strips - g0)
+        for band in range(tiles_m):
+            for k in range(wg):
+                pos[(band, g0 + k)] = t
+                t += 1
+    assert t == T and len(set(pos.values())) == T
+    G = p["grid"]
+    owner = [None] * T
+    for b, (lo, hi) in enumerate(_ranges(G, T, 1)):
+        for x in range(lo, hi):
+            owner[x] = b
+    assert None not in owner
+    kmax = 1
+    for s_ in range(strips):
+        own = [owner[pos[(band, s_)]] for band in range(tiles_m)]
+        assert own == sorted(own)
+        kmax = max(kmax, own[-1] - own[0] + 1)
+    assert p["kmax"] == kmax
+    assert p["workspace_bytes"] == ((strips * 4 + 255) // 256) * 256 + strips * kmax * tn * 4
+
+
+def test_plan_colsum_limits_and_errors():
+    # one thread per 16-byte chunk column: 1024-byte rows (64 chunks) need 2 warps
+    with pytest.raises(mbt.MbtError) as e:
+        _plan(mbt.OP_COLSUM, 1024, 4096, 64, 512, 2, torch.float16, consumer_warps=1)
+    assert e.value.code == -3
+    assert _plan(mbt.OP_COLSUM, 1024, 4096, 64, 512, 2, torch.float16,
+                 consumer_warps=2)["consumer_warps"] == 2
+    # a 16-byte row pitch is required (no flat column sum)
+    with pytest.raises(mbt.MbtError) as e:
+        _plan(mbt.OP_COLSUM, 100, 4095, 64, 256, 2, torch.bfloat16)
+    assert e.value.code == -2
+    # barrier layouts and bulk stores belong to other operations
+    for kw in ({"pipeline": 1}, {"pipeline": 2}, {"pipeline": 3}, {"store_mode": 1}):
+        with pytest.raises(mbt.MbtError) as e:
+            _plan(mbt.OP_COLSUM, 1024, 4096, 64, 256, 2, torch.bfloat16, **kw)
+        assert e.value.code in (-1, -3), kw
+    p = _plan(mbt.OP_COLSUM, 8192, 65536, 64, 256, 2, torch.bfloat16, fit=4, ws=True)
+    assert p["consumer_warps"] == 8 and p["threads"] == 288 and p["box_barriers"] == 0
+    assert p["grid"] == 304 and p["split"] == 1
+
+
+def test_colsum_argument_errors():
+    assert C.tile_colsum(A, B + 2, 8, 64, 64, 64, 2, 0, None) == -2      # out not 4-aligned
+    assert C.tile_colsum(A, None, 8, 64, 64, 64, 2, 0, None) == -1
+    assert C.tile_colsum(A + 8, B, 8, 64, 64, 64, 2, 0, None) == -2      # src not 16-aligned
+    assert C.tile_colsum(A, B, 8, 64, 0, 64, 2, 0, None) == -1
+    assert C.tile_colsum(A, B, 8, 64, 64, 32, 2, 0, None) == -3          # 64-byte rows
+    assert C.tile_colsum(None, None, 0, 0, 64, 64, 2, 0, None) == 0
+    o = Opts(); o.ld_dst = 64                                             # sums have no dst pitch
+    assert C.tile_colsum_ex(A, B, 8, 64, 64, 64, 2, 0, None, ctypes.byref(o)) == -1
+
+
 def test_ctypes_mirrors_match_the_c_structs(tmp_path):
     """Sizes and field offsets of mbt_opts / mbt_plan as the C compiler lays
     them out, against the binding's ctypes mirrors."""
