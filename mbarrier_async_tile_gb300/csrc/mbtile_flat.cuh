@@ -220,13 +220,14 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
 
 // ---------------------------------------------------------------------------
 // Flat row sum (any row pitch): CTA b owns rows [b M / G, (b + 1) M / G).
-// Short rows: a window holds several whole rows; every thread splits its
-// 16-byte chunks into the part of the chunk's first row and of the next row,
-// then one thread per row adds its chunks' parts in chunk order (rows shorter
-// than a chunk: one thread per row, element by element).  Long rows: a window
+// Short rows: a window holds several whole rows; each row goes to a group of
+// L lanes of one warp (as many lanes per row as the CTA's threads allow, a
+// power of two up to 32), which add the row's 16-byte chunks masked to the
+// row and finish with a shuffle tree: no rendezvous per window.  Long rows: a window
 // holds one piece of one row; every thread keeps its share of the row across
-// the row's pieces, and at the row's last piece a warp tree and an ordered sum
-// over warps give the row's sum.  Each row is summed by one CTA, so no
+// the row's pieces; at the row's last piece each warp's shuffle tree deposits
+// a partial, and warp 0 adds the partials in warp order (the other warps do
+// not wait for it).  Each row is summed by one CTA, so no
 // workspace is needed.
 // ---------------------------------------------------------------------------
 template <int DT>
@@ -248,29 +249,51 @@ __device__ __forceinline__ uint32_t element_bits(const unsigned char *p) {
         return *reinterpret_cast<const uint16_t *>(p);
 }
 
-// Sum of the elements of chunk `v` (starting at element index `g0`) whose
-// index lies in [e0, e1), in element order.
+// Sum of the elements of the 16-byte chunk `v` at window byte offset cb whose
+// bytes lie in [b0, b1) (window-relative offsets, so 32 bits do), in element order.
 template <int DT>
-__device__ __forceinline__ float masked_chunk_sum(const uint4 &v, int64_t g0, int64_t e0,
-                                                  int64_t e1) {
+__device__ __forceinline__ float masked_chunk_sum_rel(const uint4 &v, int cb, int b0, int b1) {
     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
     float s = 0.f;
     if constexpr (DT == MBT_F32) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            if (g0 + k >= e0 && g0 + k < e1) s += __uint_as_float(w4[k]);
+            if (cb + 4 * k >= b0 && cb + 4 * k < b1) s += __uint_as_float(w4[k]);
     } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const uint32_t bits = (w4[k >> 1] >> ((k & 1) * 16)) & 0xffffu;
-            if (g0 + k >= e0 && g0 + k < e1) s += element_value<DT>(bits);
+            if (cb + 2 * k >= b0 && cb + 2 * k < b1) s += element_value<DT>(bits);
         }
     }
     return s;
 }
 
-// Windows of the flat row sum hold at most this many 16-byte chunks.
-constexpr int kFlatChunks = 1024;
+// Window j + 1 of the row-sum schedule from window j (no divisions).
+__device__ __forceinline__ void next_row_window(const FlatArgs &a, int64_t rb, RowWindow &w) {
+    if (a.rows_per_window > 0) {
+        w.r0 += a.rows_per_window;
+        w.r1 = w.r0 + a.rows_per_window < rb ? w.r0 + a.rows_per_window : rb;
+        w.e0 = w.r0 * a.ld;
+        w.e1 = (w.r1 - 1) * a.ld + a.p.N;
+    } else {
+        if (++w.piece == a.pieces_per_row) {
+            w.piece = 0;
+            ++w.r0;
+            w.r1 = w.r0 + 1;
+        }
+        const int64_t c0 = w.piece * a.piece_elems;
+        const int64_t c1 = c0 + a.piece_elems < a.p.N ? c0 + a.piece_elems : a.p.N;
+        w.e0 = w.r0 * a.ld + c0;
+        w.e1 = w.r0 * a.ld + c1;
+    }
+}
+
+// Long rows: slots for the warp partials of rows still being combined.  A
+// window is reloaded only after every warp released it, so another warp can
+// finish row lr + K before warp 0 has read row lr's partials only if
+// K P <= stages (P pieces per row, P >= 1): 16 slots hold for up to 15 stages.
+constexpr int kFlatRowSlots = 16;
 constexpr int kFlatVec = 4;   // chunks a thread holds per round (register budget)
 
 template <int DT>
@@ -278,15 +301,16 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     mbt_rowsum_flat_kernel(const FlatArgs a) {
     extern __shared__ __align__(1024) unsigned char dyn_smem[];
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
-    __shared__ __align__(8) uint64_t flush_bar;
-    __shared__ float red[2][kMaxConsumerWarps];
-    // Short rows: per chunk, the sums of its elements in its first row (0)
-    // and in the next row (1); double-buffered by window parity.
-    __shared__ float part[2][2][kFlatChunks];
+    // Long rows: warp partials of row lr in red[lr % 8]; row_bar[lr % 8]
+    // completes when every consumer warp has deposited its partial.
+    __shared__ __align__(8) uint64_t row_bar[kFlatRowSlots];
+    __shared__ float red[kFlatRowSlots][kMaxConsumerWarps];
     __shared__ int abort_flag;
     Smem sm;
-    init_pipeline(a.p, sm, bars, &abort_flag, &flush_bar,
-                  static_cast<uint32_t>(a.p.consumer_warps), dyn_smem);
+    if (threadIdx.x == 0)
+        for (int k = 0; k < kFlatRowSlots; ++k)
+            mbar_init(smem_u32(&row_bar[k]), static_cast<uint32_t>(a.p.consumer_warps));
+    init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);   // fences the inits
     const PipeArgs &p = a.p;
     WaitCtl w{p.wait_budget_ns, &abort_flag};
     const int64_t G = gridDim.x;
@@ -305,16 +329,11 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     const int lane = threadIdx.x & 31;
     const int warp = ctid >> 5;
     const int nthr = p.consumer_warps * 32;
-    constexpr int per = DT == MBT_F32 ? 4 : 8;      // elements per 16-byte chunk
     const unsigned char *gsrc = reinterpret_cast<const unsigned char *>(a.src);
-    const unsigned char *stage_ptr0 = dyn_smem + (sm.base - smem_u32(dyn_smem));
-    // Chunked short-row path needs rows of at least one chunk (then a chunk
-    // touches at most two rows); shorter rows are summed element by element.
-    const bool chunked = a.rows_per_window > 0 && a.ld >= per;
-    FlushCtl f{smem_u32(&flush_bar), 0u};
     float row_acc = 0.f;            // long rows: this thread's share of the current row
     uint32_t stage = 0, phase = 0;
-    for (int64_t j = 0; j < count; ++j) {
+    RowWindow rw = rowsum_window(a, ra, rb, 0);
+    for (int64_t j = 0; j < count; ++j, next_row_window(a, rb, rw)) {
         bool ok = wait_bounded(sm.full0 + 8u * stage, phase, w, true);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
@@ -325,99 +344,55 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
             break;
         }
         if (ctid == 0) log_record(p, 1, j, stage, phase, j);
-        const RowWindow rw = rowsum_window(a, ra, rb, j);
         const Window wj = make_window(rw.e0 * p.esize, rw.e1 * p.esize, a.t_floor);
         const int64_t we = wj.ws + wj.size;
         const int chunks = static_cast<int>(wj.size >> 4);
         const uint32_t sbase = sm.base + stage * p.stage_stride;
-        const int64_t g_ws = wj.ws / p.esize;        // element index of the window's first byte
-        if (chunked) {
-            // Phase 1: split every chunk into its first row's and next row's part.
-            const int buf = static_cast<int>(j & 1);
-            const int64_t row0_elem = rw.r0 * a.ld;
+        if (a.rows_per_window > 0) {
+            // Short rows: every row of the window goes to a group of L lanes of
+            // one warp (L = 32 W / rows of the window, a power of two, 1..32);
+            // the group's lanes add the row's chunks, masked to the row, and a
+            // shuffle tree inside the group gives the row's sum.  No thread
+            // needs another warp's results, so the window needs no rendezvous.
             const int nrows = static_cast<int>(rw.r1 - rw.r0);
-            const uint32_t ld32 = static_cast<uint32_t>(a.ld);
-            const int n32 = static_cast<int>(p.N);
-            for (int c0 = 0; c0 < chunks; c0 += nthr * kFlatVec) {
-                uint4 v[kFlatVec];
-#pragma unroll
-                for (int u = 0; u < kFlatVec; ++u) {
-                    const int c = c0 + ctid + u * nthr;
-                    if (c < chunks) v[u] = lds128(sbase + 16u * c);
-                }
-                if (c0 + nthr * kFlatVec >= chunks) {
-                    __syncwarp();
-                    if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
-                }
-#pragma unroll
-                for (int u = 0; u < kFlatVec; ++u) {
-                    const int c = c0 + ctid + u * nthr;
-                    if (c >= chunks) continue;
-                    // Element k of the chunk is element local0 + k counted from row
-                    // r0's start (the window is < 2^16 elements, so 32 bits do).
-                    const int local0 = static_cast<int>(g_ws - row0_elem) + c * per;
-                    const int fr = local0 >= 0 ? static_cast<int>(static_cast<uint32_t>(local0) / ld32)
-                                               : -1;            // row of element 0 (or before r0)
-                    const int kb = (fr + 1) * static_cast<int>(ld32) - local0;  // first k of row fr+1
-                    const int col0 = local0 - fr * static_cast<int>(ld32);      // column of element 0
-                    // row fr owns k in [0, a_end); row fr+1 owns k in [kb, b_end)
-                    const int a_end = (fr >= 0 && fr < nrows) ? min(kb, n32 - col0) : 0;
-                    const int b_end = (fr + 1 < nrows) ? kb + n32 : 0;
-                    const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-                    float sa = 0.f, sb = 0.f;
-#pragma unroll
-                    for (int k = 0; k < per; ++k) {
-                        const uint32_t bits = DT == MBT_F32 ? wv[k & 3]
-                                                            : (wv[k >> 1] >> ((k & 1) * 16)) & 0xffffu;
-                        const float x = element_value<DT>(bits);
-                        if (k < a_end) sa += x;
-                        if (k >= kb && k < b_end) sb += x;
+            int L = 1;
+            while (L < 32 && 2 * L * nrows <= nthr) L <<= 1;
+            const int groups = nthr / L;
+            const int gidx = ctid / L, gl = ctid % L;
+            const int iters = (nrows + groups - 1) / groups;
+            for (int it = 0; it < iters; ++it) {
+                const int lr = gidx + it * groups;
+                float s = 0.f;
+                if (lr < nrows) {
+                    const int64_t e0 = (rw.r0 + lr) * a.ld, e1 = e0 + p.N;
+                    const int64_t b0 = e0 * p.esize - wj.ws, b1 = e1 * p.esize - wj.ws;
+                    const int64_t loaded = b1 < wj.size ? b1 : wj.size;
+                    if (loaded > b0) {
+                        const int rb0 = static_cast<int>(b0), rb1 = static_cast<int>(b1);
+                        const int cs = rb0 >> 4;
+                        const int ce = static_cast<int>((loaded - 1) >> 4);
+                        for (int c = cs + gl; c <= ce; c += L) {
+                            const uint4 v = lds128(sbase + 16u * c);
+                            const int cb = 16 * c;
+                            s += (cb >= rb0 && cb + 16 <= rb1) ? chunk_sum<DT>(v)
+                                                               : masked_chunk_sum_rel<DT>(v, cb, rb0, rb1);
+                        }
                     }
-                    part[buf][0][c] = sa;
-                    part[buf][1][c] = sb;
+                    // Bytes past the array's last 16-byte boundary (never loaded).
+                    if (gl == 0)
+                        for (int64_t bb = loaded > b0 ? loaded : b0; bb < b1; bb += p.esize)
+                            s += element_value<DT>(element_bits<DT>(gsrc + wj.ws + bb));
                 }
-            }
-            if (chunks == 0) {
-                __syncwarp();
-                if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
-            }
-            if (!consumers_sync(f, w)) break;
-            // Phase 2: one thread per row adds its chunks' parts in order.
-            const int64_t off0 = row0_elem * p.esize - wj.ws;   // row r0's start in the window
-            for (int lr = ctid; lr < nrows; lr += nthr) {
-                const int64_t rel0 = off0 + static_cast<int64_t>(lr) * a.ld * p.esize;
-                const int64_t rel1 = rel0 + p.N * p.esize;
-                const int64_t loaded_end = rel1 < wj.size ? rel1 : wj.size;
-                float s = 0.f;
-                if (loaded_end > rel0) {
-                    const int cs = static_cast<int>(rel0 >> 4);
-                    const int ce = static_cast<int>((loaded_end - 1) >> 4);
-                    for (int c = cs; c <= ce; ++c)
-                        s += (c == cs && (rel0 & 15) != 0) ? part[buf][1][c] : part[buf][0][c];
-                }
-                for (int64_t b = (loaded_end > rel0 ? loaded_end : rel0); b < rel1; b += p.esize)
-                    s += element_value<DT>(element_bits<DT>(gsrc + wj.ws + b));
-                a.out[rw.r0 + lr] = s;
-            }
-        } else if (a.rows_per_window > 0) {
-            // Rows shorter than one chunk: one thread per row, element by element.
-            const unsigned char *sp = stage_ptr0 + static_cast<size_t>(stage) * p.stage_stride;
-            for (int64_t r = rw.r0 + ctid; r < rw.r1; r += nthr) {
-                float s = 0.f;
-                const int64_t b0 = r * a.ld * p.esize;
-                for (int64_t i = 0; i < p.N; ++i) {
-                    const int64_t b = b0 + i * p.esize;
-                    const uint32_t bits = b < we ? element_bits<DT>(sp + (b - wj.ws))
-                                                 : element_bits<DT>(gsrc + b);
-                    s += element_value<DT>(bits);
-                }
-                a.out[r] = s;
+                for (int off = L >> 1; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+                if (lr < nrows && gl == 0) a.out[rw.r0 + lr] = s;
             }
             __syncwarp();
             if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
         } else {
             // Long rows: the window is one piece of row r0; threads keep their
             // share of the row across its pieces and reduce once per row.
+            const int pb0 = static_cast<int>(rw.e0 * p.esize - wj.ws);   // piece bytes in
+            const int pb1 = static_cast<int>(rw.e1 * p.esize - wj.ws);   // the window
             for (int c0 = 0; c0 < chunks; c0 += nthr * kFlatVec) {
                 uint4 v[kFlatVec];
 #pragma unroll
@@ -433,10 +408,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
                 for (int u = 0; u < kFlatVec; ++u) {
                     const int c = c0 + ctid + u * nthr;
                     if (c >= chunks) continue;
-                    const int64_t g0 = g_ws + static_cast<int64_t>(c) * per;
-                    row_acc += (g0 >= rw.e0 && g0 + per <= rw.e1)
+                    const int cb = 16 * c;
+                    row_acc += (cb >= pb0 && cb + 16 <= pb1)
                                    ? chunk_sum<DT>(v[u])
-                                   : masked_chunk_sum<DT>(v[u], g0, rw.e0, rw.e1);
+                                   : masked_chunk_sum_rel<DT>(v[u], cb, pb0, pb1);
                 }
             }
             if (chunks == 0) {
@@ -453,13 +428,32 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
                 row_acc = 0.f;
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-                const int buf = static_cast<int>(rw.r0 & 1);
-                if (lane == 0) red[buf][warp] = s;
-                if (!consumers_sync(f, w)) break;
-                if (ctid == 0) {
-                    float total = 0.f;
-                    for (int k = 0; k < p.consumer_warps; ++k) total += red[buf][k];
-                    a.out[rw.r0] = total;
+                // Deposit the warp's partial; warp 0 alone waits for the row's
+                // other partials and adds them in warp order, so the other
+                // warps go on to the next row at once.
+                const int64_t lr = rw.r0 - ra;
+                const int slot = static_cast<int>(lr % kFlatRowSlots);
+                const uint32_t bar = smem_u32(&row_bar[slot]);
+                if (lane == 0) {
+                    red[slot][warp] = s;
+                    mbar_arrive(bar);
+                }
+                if (warp == 0) {
+                    bool got = wait_bounded(bar, static_cast<uint32_t>((lr / kFlatRowSlots) & 1),
+                                            w, true);
+                    got = __all_sync(0xffffffffu, got);
+                    if (!got) {
+                        if (lane == 0) {
+                            report_timeout(1, kMaxStages, static_cast<uint32_t>(slot));
+                            *w.abort = 1;
+                        }
+                        break;
+                    }
+                    if (lane == 0) {
+                        float total = 0.f;
+                        for (int k = 0; k < p.consumer_warps; ++k) total += red[slot][k];
+                        a.out[rw.r0] = total;
+                    }
                 }
             }
         }

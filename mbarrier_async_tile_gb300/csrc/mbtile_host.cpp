@@ -25,7 +25,10 @@ constexpr int kDefaultConsumerWarps = 4;         // copy
 // the store in progress, so it does not count.
 constexpr int64_t kCopyBytesPerSm = 64 * 1024;
 constexpr int64_t kRowsumBytesPerSm = 128 * 1024;
-constexpr int64_t kFlatRowsumWindowBytes = 16 * 1024;
+// Flat row sum: windows of at most this many bytes (the tile's bytes below it),
+// holding whole rows only if at least kFlatMinRowsPerWindow fit.
+constexpr int64_t kFlatRowsumWindowBytes = 64 * 1024;
+constexpr int64_t kFlatMinRowsPerWindow = 8;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxCoord = 0x7fffffff;  // bulk-copy coordinates are int32
 
@@ -211,8 +214,12 @@ void flat_setup(int op, int64_t M, int64_t N, int64_t ld, int es, int tile_m, in
     f->pieces_per_row = 0;
     if (op == MBT_OP_ROWSUM) {
         const int64_t row_bytes = N * es, pitch = ld * es, room = f->cap_bytes - 32;
-        if (room >= row_bytes) {
-            f->rows_per_window = (room - row_bytes) / pitch + 1;
+        // Whole rows per window only when every consumer warp gets rows to
+        // sum (a row's lanes stay inside one warp); else pieces of each row,
+        // which all threads share.
+        const int64_t rows = room >= row_bytes ? (room - row_bytes) / pitch + 1 : 0;
+        if (rows >= kFlatMinRowsPerWindow) {
+            f->rows_per_window = rows;
         } else {
             const int64_t most = room / es;
             f->pieces_per_row = ceil_div(N, most);
@@ -267,12 +274,19 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
                                         mbt::kSwizzleAtomBytes);
     plan->stage_bytes = static_cast<int32_t>(plan->boxes * box_stride);
     if (flat && op == MBT_OP_ROWSUM) {
-        // The flat row sum's windows hold at most 16 KB (its chunk bookkeeping
-        // is sized for 1024 chunks): stages of that size, and a grid sized by
-        // what they really keep in flight.
+        // The flat row sum loads windows of at most the tile's bytes (at most
+        // kFlatRowsumWindowBytes): whole rows, or equal pieces of a long row.
+        // Stages are sized to the largest window it really loads (+ 16-byte
+        // rounding at both ends), and the grid by those bytes in flight.
+        mbt::FlatArgs f{};
+        flat_setup(op, M, N, o.ld_src ? o.ld_src : N, es, tile_m, tile_n, &f);
+        const int64_t pitch = (o.ld_src ? o.ld_src : N) * es;
+        const int64_t window = f.rows_per_window > 0
+                                   ? (std::min(f.rows_per_window, std::max<int64_t>(M, 1)) - 1) *
+                                             pitch + N * es
+                                   : f.piece_elems * es;
         plan->stage_bytes = static_cast<int32_t>(
-            round_up(std::min<int64_t>(plan->stage_bytes, kFlatRowsumWindowBytes),
-                     mbt::kSwizzleAtomBytes));
+            round_up(std::min<int64_t>(window + 32, f.cap_bytes), mbt::kSwizzleAtomBytes));
     }
     const int wanted = wanted_ctas_per_sm(op, o, stages, plan->stage_bytes);
     const int W = consumer_warps_for(op, tile_m, o, wanted);
