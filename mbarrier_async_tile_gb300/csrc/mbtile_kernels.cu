@@ -25,9 +25,11 @@
 // Kernels: mbt_copy_kernel (LSU stores, or bulk tensor stores from one
 // consumer warp), mbt_copy_unified_kernel (no warp specialisation; a CTA
 // barrier releases each stage), mbt_rowsum_kernel<dtype, fused> (row sums;
-// fused adds a store warp that also writes the tile out), and, in
-// mbtile_flat.cuh, the 1-D bulk-copy kernels for row pitches that are not a
-// multiple of 16 bytes.
+// fused adds a store warp that also writes the tile out; without it, where
+// each consumer warp reads one 128-byte box, every box of a stage may have
+// its own full/empty pair); in mbtile_flat.cuh, the 1-D bulk-copy kernels for
+// row pitches that are not a multiple of 16 bytes; in mbtile_colsum.cuh,
+// mbt_colsum_kernel (column sums, tiles taken down the column strips).
 #include <cuda_fp16.h>
 
 #include "internal.h"
