@@ -96,10 +96,11 @@ def test_log_of_one_cta_pipeline_walks_down_the_strips():
 
 
 @pytest.mark.parametrize("fault", [1, 2])
-def test_stalled_pipeline_reports_timeout(fault):
+@pytest.mark.parametrize("tile", [(64, 256), (128, 64)], ids=["one-strip", "strip-pairs"])
+def test_stalled_pipeline_reports_timeout(fault, tile):
     x = synthetic.make_matrix(512, 4096, "bf16", "normal", seed=5)
     xd = x.cuda()
-    mbt.tile_colsum(xd, None, 64, 256, 3, max_ctas=4, fault=fault, wait_budget_ns=BUDGET_NS)
+    mbt.tile_colsum(xd, None, *tile, 3, max_ctas=4, fault=fault, wait_budget_ns=BUDGET_NS)
     code, info = mbt.tile_status()
     assert code == mbt.MBT_ERR_TIMEOUT, info
     assert 0 <= info[1] < 4
@@ -108,6 +109,34 @@ def test_stalled_pipeline_reports_timeout(fault):
     out = mbt.tile_colsum(xd, None, 64, 256, 3)
     assert mbt.tile_status()[0] == 0
     assert colsum_errors(out, x)[0] <= ROWSUM_RTOL
+
+
+def test_log_of_strip_pairs_walks_band_by_band():
+    """128-byte tiles with a workspace: strips are taken in pairs, band by
+    band (5 strips: the last group is a single strip).  The sums are right
+    whichever CTA ends where in a pair, and CTA 0's producer and consumer
+    walk the same order positions."""
+    M, N, tm, tn = 512, 320, 128, 64            # 4 bands x 5 strips (last pair: one strip)
+    x = synthetic.make_matrix(M, N, "f16", "uniform", seed=14)
+    info = mbt.tile_device_info()
+    plan = mbt.tile_plan(mbt.OP_COLSUM, M, N, tm, tn, 2, torch.float16,
+                         num_sms=info["num_sms"], smem_optin=info["smem_optin"], fit_per_sm=1,
+                         with_workspace=True, max_ctas=3)
+    assert plan["split"] == 1 and plan["col_group"] == 2 and plan["grid"] == 3
+    log = torch.zeros(2 * 32 * 4, dtype=torch.int32, device="cuda")
+    out = mbt.tile_colsum(x.cuda(), None, tm, tn, 2, max_ctas=3, log=log)
+    assert mbt.tile_status()[0] == 0
+    assert colsum_errors(out, x)[0] <= ROWSUM_RTOL
+    rec = log.view(2, 32, 4).cpu()
+    T = 20                                       # CTA 0 owns positions [0, 20 / 3)
+    mine = [t for *_, t in rec[0].tolist()][:T // 3]
+    assert mine == list(range(T // 3))
+    assert [t for *_, t in rec[1].tolist()][:T // 3] == mine
+    # every CTA count splits the pairs differently; all give the same sums
+    for ctas in (1, 2, 4, 7, 20):
+        o2 = mbt.tile_colsum(x.cuda(), None, tm, tn, 2, max_ctas=ctas)
+        assert mbt.tile_status()[0] == 0
+        assert colsum_errors(o2, x)[0] <= ROWSUM_RTOL, ctas
 
 
 def test_full_size_sampled_columns_and_totals():
