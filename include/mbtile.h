@@ -357,8 +357,9 @@ int tile_stage_image(const void *src, int64_t M, int64_t N, int64_t ld, int tile
  * Host-buffer forms: src, dst and out are HOST pointers (pinned memory from
  * cudaHostAlloc / cudaHostRegister lets the copies overlap; pageable memory
  * works but the driver then stages it).  The result is that of tile_copy_ex /
- * tile_rowsum_ex on the same matrix (row sums: within the same error bound,
- * not necessarily bit-identical, since a band may be split differently).
+ * tile_rowsum_ex / tile_colsum_ex on the same matrix (sums: within the same
+ * error bound, not necessarily bit-identical, since the work is split
+ * differently).
  * The call is synchronous: on return every copy and kernel has finished.
  *
  * The matrix moves through the current device in slabs of whole row bands of
@@ -380,6 +381,11 @@ int tile_stage_image(const void *src, int64_t M, int64_t N, int64_t ld, int tile
 int tile_copy_host(const void *src, void *dst, int64_t M, int64_t N, int tile_m, int tile_n,
                    int stages, int dtype, const mbt_opts *opts);
 int tile_rowsum_host(const void *src, float *out, int64_t M, int64_t N, int tile_m,
+                     int tile_n, int stages, int dtype, const mbt_opts *opts);
+/* Column sums of a host matrix (out: host fp32[N]).  Each slab's column sums
+ * are added on the device in slab order, then copied out once; any host row
+ * pitch (the slabs are repacked to a 16-byte pitch on the device). */
+int tile_colsum_host(const void *src, float *out, int64_t M, int64_t N, int tile_m,
                      int tile_n, int stages, int dtype, const mbt_opts *opts);
 /* Frees the current device's idle staging sets of the host-buffer forms. */
 int tile_host_release(void);

@@ -136,12 +136,14 @@ def _load():
         host_sig = [vp, vp, i64, i64, i32, i32, i32, i32, ctypes.POINTER(Opts)]
         lib.tile_copy_host.argtypes = host_sig
         lib.tile_rowsum_host.argtypes = host_sig
+        lib.tile_colsum_host.argtypes = host_sig
         lib.tile_host_release.argtypes = []
         for name in ("tile_copy", "tile_copy_ex", "tile_rowsum", "tile_rowsum_ex",
                      "tile_copy_rowsum", "tile_copy_rowsum_ex",
                      "tile_rowsum_workspace_bytes", "tile_copy_rowsum_workspace_bytes",
                      "tile_plan", "tile_status", "tile_device_info",
-                     "tile_copy_host", "tile_rowsum_host", "tile_host_release",
+                     "tile_copy_host", "tile_rowsum_host", "tile_colsum_host",
+                     "tile_host_release",
                      "tile_colsum", "tile_colsum_ex", "tile_colsum_workspace_bytes"):
             getattr(lib, name).restype = ctypes.c_int
         _C = lib
@@ -491,6 +493,25 @@ def tile_rowsum_host(src: torch.Tensor, out: torch.Tensor | None = None, tile_m:
     rc = _load().tile_rowsum_host(src.data_ptr(), out.data_ptr(), M, N, tile_m, tile_n, stages,
                                   DTYPE_CODE[src.dtype], ctypes.byref(o))
     _check(rc, "tile_rowsum_host")
+    return out
+
+
+def tile_colsum_host(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int = 64,
+                     tile_n: int = 256, stages: int = 2, *, slab_rows: int = 0,
+                     **opt) -> torch.Tensor:
+    """out[j] = sum_i src[i, j] in fp32 for a HOST tensor (out on the host too),
+    streamed through the current device in row slabs whose column sums are
+    added on the device in slab order.  Any row pitch.  Synchronous."""
+    M, N, ld_s = _host_matrix(src, "src")
+    if out is None:
+        out = torch.empty(N, dtype=torch.float32, pin_memory=src.is_pinned())
+    if (out.device.type != "cpu" or out.dtype != torch.float32 or out.numel() != N
+            or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous float32 host tensor of N elements")
+    o = _opts(ld_src=ld_s, host_slab_rows=slab_rows, **opt)
+    rc = _load().tile_colsum_host(src.data_ptr(), out.data_ptr(), M, N, tile_m, tile_n, stages,
+                                  DTYPE_CODE[src.dtype], ctypes.byref(o))
+    _check(rc, "tile_colsum_host")
     return out
 
 

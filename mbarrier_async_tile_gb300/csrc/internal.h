@@ -162,6 +162,9 @@ cudaError_t launch_stage_image(const CUtensorMap &map, int32_t row0, int32_t col
                                int32_t box_inner, uint32_t box_bytes, uint32_t box_stride,
                                unsigned char *image, cudaStream_t stream);
 cudaError_t launch_fill_zero(float *out, int64_t n, cudaStream_t stream);
+// acc[i] = part[i] (first) or acc[i] + part[i], 0 <= i < n.
+cudaError_t launch_accumulate(float *acc, const float *part, int64_t n, bool first,
+                              cudaStream_t stream);
 // Raise every kernel's dynamic shared-memory limit as far as the device's
 // opt-in limit allows; `usable` receives the limit common to all kernels.
 cudaError_t set_kernel_smem_limit(int optin, int *usable);

@@ -1,5 +1,5 @@
-// Host-buffer forms of tile_copy and tile_rowsum: the matrix lives in host
-// memory, the library moves it through the device in row slabs.
+// Host-buffer forms of tile_copy, tile_rowsum and tile_colsum: the matrix
+// lives in host memory, the library moves it through the device in row slabs.
 //
 // Each call takes a staging set from a per-device pool: kSlots slab-sized
 // device buffers plus three streams (host-to-device copies, kernels,
@@ -12,8 +12,9 @@
 // once.  The slabs are repacked on the device with a 16-byte row pitch, so the
 // 2-D bulk tensor copies of the pipeline apply whatever the host pitch is.
 //
-// The operations are those of tile_copy_ex / tile_rowsum_ex (see mbtile.h);
-// this file only schedules copies and calls those entry points.
+// The operations are those of tile_copy_ex / tile_rowsum_ex / tile_colsum_ex
+// (see mbtile.h); this file schedules copies and calls those entry points, and
+// for column sums adds the slabs' sums on the device in slab order.
 
 #include <cuda_runtime.h>
 
@@ -24,7 +25,7 @@
 #include <mutex>
 #include <vector>
 
-#include "mbtile.h"
+#include "internal.h"
 
 namespace {
 
@@ -134,11 +135,13 @@ mbt_opts opts_or_default(const mbt_opts *opts) {
     return o;
 }
 
-// Copy (dst != nullptr) or row sums (out != nullptr) of a host matrix.
-int host_run(bool is_copy, const void *src, void *dst, float *out, int64_t M, int64_t N,
-             int tile_m, int tile_n, int stages, int dtype, const mbt_opts *opts) {
+// op: MBT_OP_COPY (src -> dst), MBT_OP_ROWSUM (out[M]) or MBT_OP_COLSUM
+// (out[N]: each slab's column sums, added on the device in slab order).
+int host_run(int op, const void *src, void *dst, float *out, int64_t M, int64_t N, int tile_m,
+             int tile_n, int stages, int dtype, const mbt_opts *opts) {
     const mbt_opts o = opts_or_default(opts);
     const int es = esize_of(dtype);
+    const bool is_copy = op == MBT_OP_COPY, cols = op == MBT_OP_COLSUM;
     if (es == 0 || M < 0 || N < 0) return MBT_ERR_ARG;
     // Device-side options that the slab schedule owns.
     if (o.log != nullptr || o.workspace != nullptr || o.workspace_bytes != 0) return MBT_ERR_ARG;
@@ -146,10 +149,10 @@ int host_run(bool is_copy, const void *src, void *dst, float *out, int64_t M, in
     const int64_t ld_dst = o.ld_dst ? o.ld_dst : N;
     if (ld_src < N || ld_dst < N || (!is_copy && o.ld_dst != 0)) return MBT_ERR_ARG;
     if (o.host_slab_rows < 0) return MBT_ERR_ARG;
-    if (M == 0) return MBT_OK;
-    if (!is_copy && out == nullptr) return MBT_ERR_ARG;
-    if (N == 0) {   // empty rows: nothing to copy, zero sums
-        if (!is_copy) std::fill(out, out + M, 0.f);
+    const int64_t nsums = cols ? N : M;
+    if (!is_copy && nsums > 0 && out == nullptr) return MBT_ERR_ARG;
+    if (M == 0 || N == 0) {   // nothing to read: no copy, zero sums
+        if (!is_copy) std::fill(out, out + nsums, 0.f);
         return MBT_OK;
     }
     if (src == nullptr || (is_copy && dst == nullptr)) return MBT_ERR_ARG;
@@ -170,32 +173,39 @@ int host_run(bool is_copy, const void *src, void *dst, float *out, int64_t M, in
     dev_o.ld_src = static_cast<int64_t>(dpitch / es);
     dev_o.ld_dst = is_copy ? dev_o.ld_src : 0;
     mbt_plan plan;
-    int rc = tile_plan(is_copy ? MBT_OP_COPY : MBT_OP_ROWSUM, R, N, tile_m, tile_n, stages,
-                       dtype, &dev_o, 1, 1 << 30, 1, 0, &plan);
+    int rc = tile_plan(op, R, N, tile_m, tile_n, stages, dtype, &dev_o, 1, 1 << 30, 1, 0, &plan);
     if (rc != MBT_OK) return rc;
-    // Row-sum workspace: the larger of what a full slab and the last slab need.
+    // Sum workspace: the larger of what a full slab and the last slab need.
     size_t ws_bytes = 0;
     if (!is_copy) {
         const int64_t tail = M % R;
         for (int64_t rows : {R, tail}) {
             if (rows == 0) continue;
             size_t b = 0;
-            rc = tile_rowsum_workspace_bytes(rows, N, tile_m, tile_n, stages, dtype, &dev_o, &b);
+            rc = cols ? tile_colsum_workspace_bytes(rows, N, tile_m, tile_n, stages, dtype, &dev_o,
+                                                    &b)
+                      : tile_rowsum_workspace_bytes(rows, N, tile_m, tile_n, stages, dtype, &dev_o,
+                                                    &b);
             if (rc != MBT_OK) return rc;
             ws_bytes = std::max(ws_bytes, b);
         }
     }
     const size_t slab_in = round_up(static_cast<size_t>(R) * dpitch, kAlign);
     const size_t slab_out =
-        is_copy ? slab_in : round_up(static_cast<size_t>(R) * sizeof(float), kAlign);
+        is_copy ? slab_in
+                : round_up(static_cast<size_t>(cols ? N : R) * sizeof(float), kAlign);
+    const size_t acc_bytes = cols ? round_up(static_cast<size_t>(N) * sizeof(float), kAlign) : 0;
     const size_t ws_region = round_up(ws_bytes, kAlign);
-    const size_t need = ws_region + kSlots * (slab_in + slab_out);
+    const size_t need = ws_region + acc_bytes + kSlots * (slab_in + slab_out);
 
     Staging *st = nullptr;
     rc = acquire(need, &st);
     if (rc != MBT_OK) return rc;
     char *ws = st->base;
-    auto slot_in = [&](int s) { return st->base + ws_region + s * (slab_in + slab_out); };
+    float *acc = reinterpret_cast<float *>(st->base + ws_region);
+    auto slot_in = [&](int s) {
+        return st->base + ws_region + acc_bytes + s * (slab_in + slab_out);
+    };
     auto slot_out = [&](int s) { return slot_in(s) + slab_in; };
     if (ws_bytes > 0 && cudaMemsetAsync(ws, 0, ws_bytes, st->comp) != cudaSuccess)
         rc = MBT_ERR_CUDA;
@@ -210,8 +220,10 @@ int host_run(bool is_copy, const void *src, void *dst, float *out, int64_t M, in
         const int s = static_cast<int>(k % kSlots);
         const int64_t r0 = k * R;
         const int64_t rows = std::min<int64_t>(R, M - r0);
-        // Slot s is free once slab k - kSlots has been copied out.
-        if (k >= kSlots && cudaStreamWaitEvent(st->h2d, st->out[s], 0) != cudaSuccess) {
+        // Slot s is free once slab k - kSlots has been copied out (column
+        // sums: once its kernel and the addition of its sums have run).
+        if (k >= kSlots &&
+            cudaStreamWaitEvent(st->h2d, cols ? st->kdone[s] : st->out[s], 0) != cudaSuccess) {
             rc = MBT_ERR_CUDA;
             break;
         }
@@ -223,13 +235,27 @@ int host_run(bool is_copy, const void *src, void *dst, float *out, int64_t M, in
             rc = MBT_ERR_CUDA;
             break;
         }
-        rc = is_copy ? tile_copy_ex(slot_in(s), slot_out(s), rows, N, tile_m, tile_n, stages,
-                                    dtype, st->comp, &dev_o)
-                     : tile_rowsum_ex(slot_in(s), reinterpret_cast<float *>(slot_out(s)), rows,
-                                      N, tile_m, tile_n, stages, dtype, st->comp, &dev_o);
+        float *sums = reinterpret_cast<float *>(slot_out(s));
+        if (is_copy)
+            rc = tile_copy_ex(slot_in(s), slot_out(s), rows, N, tile_m, tile_n, stages, dtype,
+                              st->comp, &dev_o);
+        else if (cols)
+            rc = tile_colsum_ex(slot_in(s), sums, rows, N, tile_m, tile_n, stages, dtype,
+                                st->comp, &dev_o);
+        else
+            rc = tile_rowsum_ex(slot_in(s), sums, rows, N, tile_m, tile_n, stages, dtype,
+                                st->comp, &dev_o);
         if (rc != MBT_OK) break;
-        if (cudaEventRecord(st->kdone[s], st->comp) != cudaSuccess ||
-            cudaStreamWaitEvent(st->d2h, st->kdone[s], 0) != cudaSuccess) {
+        if (cols && mbt::launch_accumulate(acc, sums, N, k == 0, st->comp) != cudaSuccess) {
+            rc = MBT_ERR_CUDA;
+            break;
+        }
+        if (cudaEventRecord(st->kdone[s], st->comp) != cudaSuccess) {
+            rc = MBT_ERR_CUDA;
+            break;
+        }
+        if (cols) continue;   // copied out once, after the last slab
+        if (cudaStreamWaitEvent(st->d2h, st->kdone[s], 0) != cudaSuccess) {
             rc = MBT_ERR_CUDA;
             break;
         }
@@ -238,13 +264,17 @@ int host_run(bool is_copy, const void *src, void *dst, float *out, int64_t M, in
                                         slot_out(s), dpitch, row_bytes,
                                         static_cast<size_t>(rows), cudaMemcpyDeviceToHost,
                                         st->d2h)
-                    : cudaMemcpyAsync(out + r0, slot_out(s), static_cast<size_t>(rows) * 4,
+                    : cudaMemcpyAsync(out + r0, sums, static_cast<size_t>(rows) * 4,
                                       cudaMemcpyDeviceToHost, st->d2h);
         if (e != cudaSuccess || cudaEventRecord(st->out[s], st->d2h) != cudaSuccess) {
             rc = MBT_ERR_CUDA;
             break;
         }
     }
+    if (cols && rc == MBT_OK &&
+        cudaMemcpyAsync(out, acc, static_cast<size_t>(N) * 4, cudaMemcpyDeviceToHost,
+                        st->comp) != cudaSuccess)
+        rc = MBT_ERR_CUDA;
     // Nothing may still read or write the caller's host memory after return.
     const bool synced = cudaStreamSynchronize(st->h2d) == cudaSuccess &&
                         cudaStreamSynchronize(st->comp) == cudaSuccess &&
@@ -254,7 +284,7 @@ int host_run(bool is_copy, const void *src, void *dst, float *out, int64_t M, in
     const int status = tile_status(st->comp, info);
     if (rc == MBT_OK) rc = status;
     if (status == MBT_ERR_TIMEOUT && ws_bytes > 0) {
-        // A stalled row sum may leave tickets or partials behind.
+        // A stalled sum may leave tickets or partials behind.
         cudaMemsetAsync(ws, 0, ws_bytes, st->comp);
         cudaStreamSynchronize(st->comp);
     }
@@ -268,12 +298,17 @@ extern "C" {
 
 int tile_copy_host(const void *src, void *dst, int64_t M, int64_t N, int tile_m, int tile_n,
                    int stages, int dtype, const mbt_opts *opts) {
-    return host_run(true, src, dst, nullptr, M, N, tile_m, tile_n, stages, dtype, opts);
+    return host_run(MBT_OP_COPY, src, dst, nullptr, M, N, tile_m, tile_n, stages, dtype, opts);
 }
 
 int tile_rowsum_host(const void *src, float *out, int64_t M, int64_t N, int tile_m, int tile_n,
                      int stages, int dtype, const mbt_opts *opts) {
-    return host_run(false, src, nullptr, out, M, N, tile_m, tile_n, stages, dtype, opts);
+    return host_run(MBT_OP_ROWSUM, src, nullptr, out, M, N, tile_m, tile_n, stages, dtype, opts);
+}
+
+int tile_colsum_host(const void *src, float *out, int64_t M, int64_t N, int tile_m, int tile_n,
+                     int stages, int dtype, const mbt_opts *opts) {
+    return host_run(MBT_OP_COLSUM, src, nullptr, out, M, N, tile_m, tile_n, stages, dtype, opts);
 }
 
 int tile_host_release(void) {

@@ -850,6 +850,12 @@ __global__ void __launch_bounds__(FUSED ? kMaxThreads + 32 : kMaxThreads, 2)
     consume_rowsum<DT>(a, sm, w, first, last - first, red, &last_flag, f, FUSED ? 2 : 1, boxed);
 }
 
+__global__ void mbt_accumulate_kernel(float *acc, const float *part, int64_t n, int first) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        acc[i] = first ? part[i] : acc[i] + part[i];
+}
+
 __global__ void mbt_fill_zero_kernel(float *out, int64_t n) {
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
@@ -995,6 +1001,15 @@ cudaError_t launch_fill_zero(float *out, int64_t n, cudaStream_t stream) {
     const int64_t blocks64 = (n + threads - 1) / threads;
     const int blocks = static_cast<int>(blocks64 < 1024 ? (blocks64 < 1 ? 1 : blocks64) : 1024);
     mbt_fill_zero_kernel<<<blocks, threads, 0, stream>>>(out, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_accumulate(float *acc, const float *part, int64_t n, bool first,
+                              cudaStream_t stream) {
+    const int threads = 256;
+    const int64_t blocks64 = (n + threads - 1) / threads;
+    const int blocks = static_cast<int>(blocks64 < 1024 ? (blocks64 < 1 ? 1 : blocks64) : 1024);
+    mbt_accumulate_kernel<<<blocks, threads, 0, stream>>>(acc, part, n, first ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -159,6 +159,11 @@ def test_host_forms_argument_errors_before_any_cuda_call():
         assert C.tile_copy_host(p(src), p(src), 8, 8, 64, 64, 2, 0, ctypes.byref(o)) == -1, field
     o = Opts(); o.ld_dst = 8                             # a row sum has no dst pitch
     assert C.tile_rowsum_host(p(src), p(out), 8, 8, 64, 64, 2, 0, ctypes.byref(o)) == -1
+    cout = (ctypes.c_float * 4)(*([5.0] * 4))
+    assert C.tile_colsum_host(p(src), p(cout), 0, 4, 64, 64, 2, 0, None) == 0
+    assert list(cout) == [0.0] * 4                      # no rows: zero column sums
+    assert C.tile_colsum_host(p(src), None, 8, 0, 64, 64, 2, 0, None) == 0   # no columns
+    assert C.tile_colsum_host(p(src), None, 8, 4, 64, 64, 2, 0, None) == -1
     o = Opts(); o.host_slab_rows = 4                     # host-buffer forms only
     assert _copy(A, B, 8, 64, opts=o) == -1
     assert C.tile_rowsum_ex(A, B, 8, 64, 128, 64, 3, 0, None, ctypes.byref(o)) == -1

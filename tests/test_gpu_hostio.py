@@ -1,8 +1,9 @@
-"""Host-buffer forms (tile_copy_host, tile_rowsum_host): HOST matrices moved
-through the device in row slabs with the copies in, the tile pipeline and
-the copies out overlapped on three streams.  Copies are bit-exact against the
-oracle (pads of dst untouched), row sums within the fp32 bound; any host
-pitch, ragged slab counts, pinned and pageable memory, stalls, threads."""
+"""Host-buffer forms (tile_copy_host, tile_rowsum_host, tile_colsum_host):
+HOST matrices moved through the device in row slabs with the copies in, the
+tile pipeline and the copies out overlapped on three streams.  Copies are
+bit-exact against the oracle (pads of dst untouched), row and column sums
+within the fp32 bound; any host pitch, ragged slab counts, pinned and
+pageable memory, stalls, threads."""
 import threading
 
 import pytest
@@ -11,7 +12,7 @@ import torch
 import mbarrier_async_tile_gb300 as mbt
 import oracle
 import synthetic
-from helpers import DTYPES, ROWSUM_RTOL, bits, rowsum_errors
+from helpers import DTYPES, ROWSUM_RTOL, bits, colsum_errors, rowsum_errors
 
 pytestmark = pytest.mark.gpu
 
@@ -75,6 +76,28 @@ def test_rowsum_host_matches_oracle(case):
     assert worst <= ROWSUM_RTOL, (worst, rel)
 
 
+COLSUM_CASES = [
+    # dtype, M, N, host ld_src, slab rows (0 = default), pinned
+    ("bf16", 3000, 20000, 20000, 256, True),       # 12 slabs added in order
+    ("f32", 1234, 8191, 8193, 300, True),          # odd pitch (repacked), ragged last slab
+    ("f16", 4097, 777, 781, 0, False),             # pageable, one slab
+    ("f16", 70, 4000, 4000, 1, True),              # one row per slab
+]
+
+
+@pytest.mark.parametrize("case", COLSUM_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_colsum_host_matches_oracle(case):
+    dtype, M, N, ld_s, slab, pinned = case
+    x = synthetic.make_matrix(M, N, dtype, "normal", seed=M + N, ld=ld_s)
+    if pinned:
+        x = x.pin_memory()
+    tn = 128 if dtype == "f32" else 256
+    out = mbt.tile_colsum_host(x[:, :N], None, 64, tn, 2, slab_rows=slab)
+    assert out.device.type == "cpu" and out.numel() == N
+    worst, rel, _ = colsum_errors(out, x[:, :N])
+    assert worst <= ROWSUM_RTOL, (worst, rel)
+
+
 def test_default_slabs_of_a_quarter_gigabyte_matrix():
     """bf16 8192 x 16384 (256 MiB): four default slabs of 64 MiB each way."""
     M, N = 8192, 16384
@@ -84,6 +107,8 @@ def test_default_slabs_of_a_quarter_gigabyte_matrix():
     assert torch.equal(bits(y), bits(x))
     out = mbt.tile_rowsum_host(x, None, 64, 256, 2)
     assert rowsum_errors(out, x)[0] <= ROWSUM_RTOL
+    cols = mbt.tile_colsum_host(x, None, 64, 256, 2)
+    assert colsum_errors(cols, x)[0] <= ROWSUM_RTOL
 
 
 def test_empty_shapes():
@@ -91,6 +116,7 @@ def test_empty_shapes():
     assert out.tolist() == [0.0] * 5
     mbt.tile_copy_host(torch.empty(0, 9, dtype=torch.float16),
                        torch.empty(0, 9, dtype=torch.float16))
+    assert mbt.tile_colsum_host(torch.empty(0, 6, dtype=torch.bfloat16)).tolist() == [0.0] * 6
 
 
 def test_stall_reports_timeout_and_pool_recovers():
