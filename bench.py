@@ -36,6 +36,7 @@ ROWSUM = dict(name="rowsum", dtype="bf16", M=8192, N=65536, tile_m=64, tile_n=25
               dist="normal", seed=1004)
 ESIZE = {"f16": 2, "bf16": 2, "f32": 4}
 FALLBACK_HBM_GBS = 6800.0
+MODE_NAME = {0: "default", 1: "bulk tensor stores", 2: "LSU stores"}
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture
 # of each kernel on the full-size workload, keyed by the SHA-256 of the kernel
@@ -634,10 +635,10 @@ def bench_configs(args):
     # 3: streaming copy, stage sweep, both store paths
     x = synthetic.make_matrix(16384, 16384, "f16", "uniform", 1003, draw_on=str(dev))
     y = torch.empty_like(x)
-    for mode in (0, 1):
+    for mode in (2, 1):
         for st in (1, 2, 3, 4, 6):
             ms = med_ms(lambda: mbt.tile_copy(x, y, 128, 64, st, store_mode=mode), 20)
-            line({"config": 3, "op": "copy", "store_mode": mode, "shape": [16384, 16384],
+            line({"config": 3, "op": "copy", "store_mode": MODE_NAME[mode], "shape": [16384, 16384],
                   "tile": [128, 64], "stages": st, "ms": round(ms, 4),
                   "gbs": round(copy_bytes() / ms / 1e6, 1)})
     del x, y
@@ -665,9 +666,9 @@ def bench_configs(args):
         x = synthetic.make_matrix(M, N, dt, "uniform", seed, ld=ld, draw_on=str(dev))
         y = torch.empty_like(x)
         o = torch.empty(M, dtype=torch.float32, device=dev)
-        for mode in (0, 1):
+        for mode in (2, 1):
             ms = med_ms(lambda: mbt.tile_copy(x[:, :N], y[:, :N], tm, tn, 3, store_mode=mode), 20)
-            line({"config": cfg, "op": "copy", "store_mode": mode, "shape": [M, N], "ld": ld,
+            line({"config": cfg, "op": "copy", "store_mode": MODE_NAME[mode], "shape": [M, N], "ld": ld,
                   "tile": [tm, tn], "stages": 3, "ms": round(ms, 4),
                   "gbs": round(2 * M * N * es / ms / 1e6, 1)})
         ms = med_ms(lambda: mbt.tile_rowsum(x[:, :N], o, tm, tn, 3, workspace=ws), 20)
@@ -830,7 +831,7 @@ def main(argv=None):
     ap.add_argument("--trim-cols", type=int, default=0,
                     help="--only: drop this many columns (an odd count gives a dense matrix "
                          "whose rows are not a multiple of 16 bytes: the 1-D bulk-copy path)")
-    ap.add_argument("--store-mode", type=int, default=0, choices=[0, 1])
+    ap.add_argument("--store-mode", type=int, default=0, choices=[0, 1, 2])
     ap.add_argument("--rows", type=int, default=0)
     ap.add_argument("--consumer-warps", type=int, default=0)
     ap.add_argument("--ctas-per-sm", type=int, default=0)

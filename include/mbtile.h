@@ -99,15 +99,21 @@ typedef struct mbt_opts {
                                 default grid puts 3+ CTAs on an SM and
                                 tile_m <= 128.  The CTA has one more warp,
                                 the producer. */
-    int32_t store_mode;      /* tile_copy only.  0: the consumer warps store
-                                each tile with 16-byte st.global (default);
+    int32_t store_mode;      /* tile_copy only (same result in every mode).
                                 1: one consumer thread writes each landed
                                 stage back with bulk tensor stores (same
-                                swizzled box layout, out-of-bounds elements
-                                clipped by the copy engine); the CTA then has
-                                one consumer warp and consumer_warps is
-                                ignored.  Source of the store recipe: "cute(11)
-                                Hopper TMA copy" §6.3-6.4. */
+                                swizzled box layout; the store map ends at the
+                                last whole 16-byte chunk of a row, and a
+                                row's partial last chunk is stored by the
+                                warp's lanes); the CTA has one consumer warp
+                                and consumer_warps is ignored.  2: the
+                                consumer warps store with 16-byte st.global.
+                                0 (default): 1 when rows end inside a 16-byte
+                                chunk (LSU stores would leave a partly written
+                                last sector per row), else 2; always 2 with
+                                the unified pipeline.  mbt_plan.bulk_stores
+                                tells which.  Source of the store recipe:
+                                "cute(11) Hopper TMA copy" §6.3-6.4. */
     uint64_t wait_budget_ns; /* time bound of every mbarrier wait; 0 => 1 s */
     int32_t *log;            /* optional device buffer of int32 records, see
                                 below; NULL => no log */
@@ -175,6 +181,10 @@ typedef struct mbt_plan {
                                 together, band by band (2 where the tile row
                                 is 128 bytes and strips are split over CTAs,
                                 else 1); 0 for the other operations */
+    int32_t bulk_stores;     /* copy: 1 if stages are written back with bulk
+                                tensor stores (see mbt_opts.store_mode; always
+                                1 for tile_copy_rowsum) */
+    int32_t reserved1;
     int64_t tiles_m;         /* tiles down the rows (row bands) */
     int64_t tiles_n;         /* tiles across the columns */
     int64_t num_tiles;

@@ -69,6 +69,8 @@ class Plan(ctypes.Structure):
         ("flat", ctypes.c_int32),
         ("box_barriers", ctypes.c_int32),
         ("col_group", ctypes.c_int32),
+        ("bulk_stores", ctypes.c_int32),
+        ("reserved1", ctypes.c_int32),
         ("tiles_m", ctypes.c_int64),
         ("tiles_n", ctypes.c_int64),
         ("num_tiles", ctypes.c_int64),
@@ -219,7 +221,9 @@ def tile_copy(src: torch.Tensor, dst: torch.Tensor, tile_m: int = 128, tile_n: i
     """dst[i, j] = src[i, j] (bit-exact) through the tile pipeline.
 
     ``src`` and ``dst`` are 2-D CUDA views of the same shape and dtype with
-    unit column stride; their row strides may differ (pitched storage)."""
+    unit column stride; their row strides may differ (pitched storage).
+    ``store_mode``: 1 bulk tensor stores, 2 16-byte LSU stores, 0 (default)
+    bulk where rows end inside a 16-byte chunk, else LSU."""
     M, N, ld_s = _matrix(src, "src")
     Md, Nd, ld_d = _matrix(dst, "dst")
     if (M, N) != (Md, Nd) or src.dtype != dst.dtype:

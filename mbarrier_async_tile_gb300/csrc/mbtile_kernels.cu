@@ -447,13 +447,18 @@ struct BulkStores {
     bool pending = false;      // a committed store whose stage is not released yet
     uint32_t prev_stage = 0;
 
+    // Store the tile's boxes that start before column n_map (the extent of
+    // dst_map: the columns held in whole 16-byte chunks); the copy engine
+    // clips each box there.
     __device__ void store_tile(const CUtensorMap *dst_map, const PipeArgs &p, const Smem &sm,
-                               uint32_t stage, int64_t row0, int64_t col0) {
+                               uint32_t stage, int64_t row0, int64_t col0, int64_t n_map) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         const uint32_t sbase = sm.base + stage * p.stage_stride;
         for (int b = 0; b < p.boxes; ++b)
-            tma_store_2d(dst_map, sbase + b * p.box_stride,
-                         static_cast<int32_t>(col0) + b * p.box_inner, static_cast<int32_t>(row0));
+            if (col0 + static_cast<int64_t>(b) * p.box_inner < n_map)
+                tma_store_2d(dst_map, sbase + b * p.box_stride,
+                             static_cast<int32_t>(col0) + b * p.box_inner,
+                             static_cast<int32_t>(row0));
         bulk_commit_group();
         if (p.stages == 1) {
             bulk_wait_read_all();
@@ -485,11 +490,30 @@ struct BulkStores {
     }
 };
 
+// The partial 16-byte chunk that ends each row of the tile at column N
+// (columns [n_whole, N), fewer than 16 bytes), stored element by element by
+// the 32 lanes of one warp.
+__device__ __forceinline__ void store_partial_chunks(const PipeArgs &p, char *dst,
+                                                     int64_t ld_dst_bytes, uint32_t sbase,
+                                                     int64_t row0, int64_t col0,
+                                                     int64_t n_whole, int lane) {
+    const int64_t c_lo = n_whole > col0 ? n_whole : col0;
+    const int q = static_cast<int>((c_lo - col0) * p.esize / 16);   // chunk in the tile row
+    const int nbytes = static_cast<int>((p.N - c_lo) * p.esize);
+    const int64_t left = p.M - row0;
+    const int rows = left < p.tile_m ? static_cast<int>(left) : p.tile_m;
+    for (int r = lane; r < rows; r += 32) {
+        const uint4 v = lds128(sbase + chunk_offset(r, q, p.box_stride));
+        store_tail(dst + (row0 + r) * ld_dst_bytes + c_lo * p.esize, v, nbytes, p.esize);
+    }
+}
+
 // Copy consumer with bulk tensor stores (one consumer warp): lane 0 stores
 // each landed stage straight from shared memory (same swizzled box layout) to
 // the destination.  The copy engine clips a store's innermost dimension only
-// at 16-byte granularity, so a tile holding a partial 16-byte chunk at column
-// N is written by the warp with LSU stores instead.
+// at 16-byte granularity, so dst_map ends at the last whole 16-byte chunk of a
+// row (n_whole columns): a tile holding the partial chunk at column N has its
+// whole chunks stored in bulk and that chunk stored by the warp's lanes.
 __device__ void consume_copy_bulk(const CUtensorMap *dst_map, const CopyArgs &a, const Smem &sm,
                                   const WaitCtl &w, int64_t first, int64_t step, int64_t count,
                                   bool do_log = true) {
@@ -516,11 +540,19 @@ __device__ void consume_copy_bulk(const CUtensorMap *dst_map, const CopyArgs &a,
         const int64_t row0 = tm * p.tile_m;
         const int64_t col0 = (tile - tm * p.tiles_n) * tile_n;
         if (col0 + tile_n > n_whole && n_whole != p.N) {
-            if (lane == 0) bs.release_pending(p, sm);
-            copy_tile_lsu(p, a.dst, a.ld_dst_bytes, sm.base + stage * p.stage_stride, row0, col0,
-                          lane, 32, p.fault != 2 ? sm.empty0 + 8u * stage : 0u);
+            store_partial_chunks(p, a.dst, a.ld_dst_bytes, sm.base + stage * p.stage_stride,
+                                 row0, col0, n_whole, lane);
+            __syncwarp();   // every lane's reads of the stage are done
+            if (lane == 0) {
+                if (col0 < n_whole) {
+                    bs.store_tile(dst_map, p, sm, stage, row0, col0, n_whole);
+                } else {    // nothing in whole chunks: release the stage now
+                    bs.release_pending(p, sm);
+                    if (p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+                }
+            }
         } else if (lane == 0) {
-            bs.store_tile(dst_map, p, sm, stage, row0, col0);
+            bs.store_tile(dst_map, p, sm, stage, row0, col0, n_whole);
         }
         if (++stage == static_cast<uint32_t>(p.stages)) {
             stage = 0;

@@ -111,8 +111,10 @@ def test_option_errors():
     assert _copy(A, B, 8, 64, opts=o) == -3
     o = Opts(); o.pipeline = 1                     # copy only
     assert C.tile_rowsum_ex(A, B, 8, 64, 128, 64, 3, 0, None, ctypes.byref(o)) == -1
-    o = Opts(); o.store_mode = 2
+    o = Opts(); o.store_mode = 3
     assert _copy(A, B, 8, 64, opts=o) == -3
+    o = Opts(); o.store_mode = 2                 # LSU stores: a copy-only option
+    assert C.tile_rowsum_ex(A, B, 8, 64, 128, 64, 3, 0, None, ctypes.byref(o)) == -1
     o = Opts(); o.store_mode = 1                 # bulk stores: a copy-only option
     assert C.tile_rowsum_ex(A, B, 8, 64, 128, 64, 3, 0, None, ctypes.byref(o)) == -1
     o = Opts(); o.ld_src = 60                    # pitch below N
@@ -214,6 +216,25 @@ def test_plan_fused_adds_a_store_warp():
               ld_src=16384, ld_dst=16384)
     # 16 KB stages, one held by the store in flight: 2 live x 2 CTAs = 64 KB per SM
     assert p["grid"] == 304 and p["consumer_warps"] == 8 and p["threads"] == 32 * 10
+
+
+def test_plan_store_mode_default_follows_the_row_end():
+    """0 picks bulk stores where rows end inside a 16-byte chunk, LSU stores
+    otherwise (and always LSU with the unified pipeline)."""
+    ragged = _plan(mbt.OP_COPY, 24577, 16383, 128, 64, 3, torch.float16, ld_src=16384,
+                   ld_dst=16384)
+    assert ragged["bulk_stores"] == 1 and ragged["consumer_warps"] == 1
+    aligned = _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 3, torch.float16)
+    assert aligned["bulk_stores"] == 0 and aligned["consumer_warps"] == 4
+    assert _plan(mbt.OP_COPY, 24577, 16383, 128, 64, 3, torch.float16, ld_src=16384,
+                 ld_dst=16384, store_mode=2)["bulk_stores"] == 0
+    assert _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 3, torch.float16,
+                 store_mode=1)["bulk_stores"] == 1
+    assert _plan(mbt.OP_COPY, 24577, 16383, 128, 64, 3, torch.float16, ld_src=16384,
+                 ld_dst=16384, pipeline=1)["bulk_stores"] == 0
+    assert _plan(mbt.OP_COPY_ROWSUM, 1024, 4096, 64, 256, 2, torch.bfloat16)["bulk_stores"] == 1
+    assert _plan(mbt.OP_ROWSUM, 1024, 4095, 64, 256, 2, torch.bfloat16,
+                 ld_src=4096)["bulk_stores"] == 0
 
 
 def test_plan_bulk_store_mode_uses_one_consumer_warp():

@@ -68,10 +68,12 @@ CASES = [
     ("f16", 2048, 2048, 128, 64, 6, 7),
     ("f16", 65, 8, 1, 64, 8, 1),
     ("f32", 4099, 1025, 256, 32, 3, 5),
+    ("bf16", 300, 1001, 64, 256, 3, 4),   # last tile: 4 boxes in whole chunks + a partial one
+    ("bf16", 77, 803, 64, 256, 2, 2),     # last tile: boxes 2-4 start past the whole chunks
 ]
 
 
-@pytest.mark.parametrize("store_mode", [0, 1])
+@pytest.mark.parametrize("store_mode", [0, 1, 2])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
 def test_copy_matches_oracle(case, store_mode):
     dtype, M, N, tm, tn, st, w = case
@@ -81,7 +83,7 @@ def test_copy_matches_oracle(case, store_mode):
     assert torch.equal(bits(got), bits(want))
 
 
-@pytest.mark.parametrize("store_mode", [0, 1])
+@pytest.mark.parametrize("store_mode", [0, 1, 2])
 @pytest.mark.parametrize("dtype,M,N,tm,tn", [("f16", 200, 1000, 128, 64), ("f32", 77, 70, 64, 32),
                                              ("bf16", 5, 3, 128, 64)])
 def test_nothing_written_outside_the_logical_region(dtype, M, N, tm, tn, store_mode):
