@@ -228,7 +228,10 @@ void flat_setup(int op, int64_t M, int64_t N, int64_t ld, int es, int tile_m, in
         // Whole rows per window only when every consumer warp gets rows to
         // sum (a row's lanes stay inside one warp); else pieces of each row,
         // which all threads share.
-        const int64_t rows = room >= row_bytes ? (room - row_bytes) / pitch + 1 : 0;
+        int64_t rows = room >= row_bytes ? (room - row_bytes) / pitch + 1 : 0;
+        // A multiple of 32 rows spreads evenly over the consumer threads (129
+        // rows on 128 threads would take two passes, the second for one row).
+        if (rows >= 32) rows -= rows % 32;
         if (rows >= kFlatMinRowsPerWindow) {
             f->rows_per_window = rows;
         } else {
