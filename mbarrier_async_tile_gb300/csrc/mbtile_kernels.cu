@@ -22,7 +22,7 @@
 // the CTA's other waits give up early, and the producer then waits (again
 // bounded) for the bulk copies it still has in flight before the CTA exits.
 //
-// Kernels: mbt_copy_kernel (LSU stores, or bulk tensor stores from one
+// Kernels: mbt_copy_kernel<bulk> (LSU stores, or bulk tensor stores from one
 // consumer warp), mbt_copy_unified_kernel (no warp specialisation; a CTA
 // barrier releases each stage), mbt_rowsum_kernel<dtype, fused> (row sums;
 // fused adds a store warp that also writes the tile out; without it, where
@@ -562,6 +562,10 @@ __device__ void consume_copy_bulk(const CUtensorMap *dst_map, const CopyArgs &a,
     if (lane == 0) bs.finish(p, sm, *w.abort != 0);
 }
 
+// BULK: bulk tensor stores from one consumer warp; else the consumer warps'
+// 16-byte LSU stores.  Two instantiations, so that neither carries the other's
+// code (one kernel with both paths ran the LSU copy 1.5% slower).
+template <bool BULK>
 __global__ void __launch_bounds__(kMaxThreads, 2)
     mbt_copy_kernel(const __grid_constant__ CUtensorMap map,
                     const __grid_constant__ CUtensorMap dst_map, const CopyArgs a) {
@@ -579,11 +583,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
         if (threadIdx.x == 0) produce(&map, a.p, sm, w, first, G, count);
         return;
     }
-    if (a.store_mode == 1) {
+    if constexpr (BULK)
         consume_copy_bulk(&dst_map, a, sm, w, first, G, count);   // one consumer warp
-        return;
-    }
-    consume_copy(a, sm, w, first, G, count);
+    else
+        consume_copy(a, sm, w, first, G, count);
 }
 
 // ---------------------------------------------------------------------------
@@ -939,7 +942,10 @@ __global__ void mbt_stage_image_kernel(const __grid_constant__ CUtensorMap map, 
 // ---------------------------------------------------------------------------
 cudaError_t launch_copy(const CUtensorMap &map, const CUtensorMap &dst_map, const CopyArgs &a,
                         int grid, int threads, int smem, cudaStream_t stream) {
-    mbt_copy_kernel<<<grid, threads, smem, stream>>>(map, dst_map, a);
+    if (a.store_mode == 1)
+        mbt_copy_kernel<true><<<grid, threads, smem, stream>>>(map, dst_map, a);
+    else
+        mbt_copy_kernel<false><<<grid, threads, smem, stream>>>(map, dst_map, a);
     return cudaGetLastError();
 }
 
@@ -1048,7 +1054,8 @@ cudaError_t launch_accumulate(float *acc, const float *part, int64_t n, bool fir
 cudaError_t set_kernel_smem_limit(int optin, int *usable) {
     // Each kernel may use the opt-in limit minus its own static shared memory;
     // the plan uses the smallest of these so that any kernel can launch it.
-    const void *fns[] = {reinterpret_cast<const void *>(mbt_copy_kernel),
+    const void *fns[] = {reinterpret_cast<const void *>(mbt_copy_kernel<false>),
+                         reinterpret_cast<const void *>(mbt_copy_kernel<true>),
                          reinterpret_cast<const void *>(mbt_copy_unified_kernel),
                          reinterpret_cast<const void *>(mbt_copy_flat_kernel),
                          reinterpret_cast<const void *>(mbt_rowsum_flat_kernel<MBT_F16>),
@@ -1081,7 +1088,8 @@ cudaError_t set_kernel_smem_limit(int optin, int *usable) {
 }
 
 cudaError_t kernel_fit_per_sm(int op, int dtype, int threads, int smem, int *fit) {
-    const void *fn = reinterpret_cast<const void *>(mbt_copy_kernel);
+    const void *fn = reinterpret_cast<const void *>(mbt_copy_kernel<false>);
+    if (op == 7) fn = reinterpret_cast<const void *>(mbt_copy_kernel<true>);
     if (op == 3) fn = reinterpret_cast<const void *>(mbt_copy_unified_kernel);
     if (op == 4) fn = reinterpret_cast<const void *>(mbt_copy_flat_kernel);
     if (op == 5)
