@@ -170,7 +170,8 @@ cudaError_t launch_accumulate(float *acc, const float *part, int64_t n, bool fir
 cudaError_t set_kernel_smem_limit(int optin, int *usable);
 // CTAs of a kernel with this block/smem shape that fit on one SM; kernel
 // MBT_OP_COPY, MBT_OP_ROWSUM, MBT_OP_COPY_ROWSUM, 3 = unified copy,
-// 4 = flat copy, 5 = flat row sum, 6 = column sum, 7 = copy with bulk stores.
+// 4 = flat copy, 5 = flat row sum, 6 = column sum, 7 = copy with bulk stores,
+// 8 = row sum with a barrier pair per box.
 cudaError_t kernel_fit_per_sm(int op, int dtype, int threads, int smem, int *fit);
 // Read the device status word and clear it (synchronous).
 cudaError_t read_and_clear_status(int32_t info[4]);

@@ -461,6 +461,7 @@ int plan_on_device(int op, int64_t M, int64_t N, int tile_m, int tile_n, int sta
                           : op == MBT_OP_COLSUM                 ? 6
                           : op == MBT_OP_COPY && o.pipeline == 1 ? 3
                           : op == MBT_OP_COPY && plan->bulk_stores ? 7
+                          : op == MBT_OP_ROWSUM && plan->box_barriers ? 8
                                                                 : op;
     const auto key = std::make_tuple(dev, kernel_id, op != MBT_OP_COPY ? dtype : 0,
                                      plan->threads, plan->smem_bytes);
