@@ -243,10 +243,11 @@ int tile_rowsum_ex(const void *src, float *out, int64_t M, int64_t N,
  * from device memory once; one consumer thread writes the landed stage back
  * with bulk tensor stores ("cute(11) Hopper TMA copy" §6.3-6.4) while the
  * consumer warps reduce it.  The CTA has a producer warp, a store warp (bulk
- * tensor stores; LSU stores for tiles holding a partial 16-byte chunk at
- * column N) and the row-sum warps; each stage is released when both the store
- * and the row-sum warps are done with it.  Row sums follow tile_rowsum's
- * order and tolerance.  Workspace: tile_copy_rowsum_workspace_bytes.
+ * tensor stores of each row's whole 16-byte chunks; its lanes store a row's
+ * partial chunk at column N) and the row-sum warps; each stage is released
+ * when both the store and the row-sum warps are done with it.  Row sums are
+ * bit-identical to tile_rowsum's with the same plan.  Workspace:
+ * tile_copy_rowsum_workspace_bytes.
  *   src, dst   as in tile_copy (opts->ld_src, opts->ld_dst; must not overlap
  *              unless equal); out as in tile_rowsum.
  * opts->store_mode must be 0.
