@@ -11,6 +11,7 @@ ctypes handle); the functions below take ``torch.Tensor`` arguments.
 from __future__ import annotations
 
 import ctypes
+from collections import OrderedDict
 import os
 import threading
 
@@ -241,7 +242,8 @@ def tile_copy(src: torch.Tensor, dst: torch.Tensor, tile_m: int = 128, tile_n: i
 
 
 _ws_lock = threading.Lock()
-_ws_cache: dict[int, torch.Tensor] = {}
+_ws_cache: "OrderedDict[tuple[int, int], torch.Tensor]" = OrderedDict()
+_WS_CACHE_MAX = 16   # (device, stream) pairs kept; the least recently used goes first
 
 
 def _workspace(device: torch.device, nbytes: int, stream=None) -> torch.Tensor:
@@ -253,15 +255,25 @@ def _workspace(device: torch.device, nbytes: int, stream=None) -> torch.Tensor:
     with _ws_lock:
         buf = _ws_cache.get(key)
         if buf is None or buf.numel() < nbytes:
-            buf = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
+            # Allocated and zero-filled on the stream that will use it: the fill
+            # is ordered before the kernels, and once evicted the block is
+            # reused only by later work on that same stream.
+            with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
+                buf = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
             _ws_cache[key] = buf
+        _ws_cache.move_to_end(key)
+        while len(_ws_cache) > _WS_CACHE_MAX:
+            _ws_cache.popitem(last=False)
         return buf
 
 
 def _reset_workspaces() -> None:
+    """Zero every cached workspace (after a stalled call may have left tickets
+    or partials behind), finished before any later launch on any stream."""
     with _ws_lock:
         for buf in _ws_cache.values():
             buf.zero_()
+    torch.cuda.synchronize()
 
 
 def tile_rowsum_workspace_bytes(M: int, N: int, tile_m: int, tile_n: int, stages: int,

@@ -115,3 +115,24 @@ def test_full_size_configs(case):
         assert mbt.tile_status()[0] == 0
         worst, rel, _ = rowsum_errors(out, x[:, :N])
         assert worst <= ROWSUM_RTOL, (st, worst, rel)
+
+
+def test_cached_workspaces_per_stream_are_ordered_and_bounded():
+    """The binding's cached workspace is allocated and zero-filled on the
+    stream that uses it (so the fill precedes the kernels there), one per
+    (device, stream), at most 16 kept."""
+    x = synthetic.make_matrix(3000, 20000, "bf16", "normal", seed=17)
+    xd = x.cuda()
+    torch.cuda.synchronize()
+    mbt._ws_cache.clear()
+    streams = [torch.cuda.Stream() for _ in range(20)]
+    outs = []
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+        outs.append(mbt.tile_rowsum(xd, None, 64, 256, 2, stream=s))
+    torch.cuda.synchronize()
+    assert mbt.tile_status()[0] == 0
+    assert len(mbt._ws_cache) == 16
+    for o in outs:
+        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
+    assert rowsum_errors(outs[0], x)[0] <= ROWSUM_RTOL
