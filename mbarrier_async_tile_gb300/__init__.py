@@ -1,9 +1,10 @@
 """Python binding of libmbtile, the sm_103a mbarrier/TMA tile pipeline.
 
-Argument marshalling only: every step of ``tile_copy`` and ``tile_rowsum``
-runs in the library's CUDA kernels.  PyTorch supplies device memory and
-streams.  If the compiled library is missing, every call raises; there is no
-fallback path.
+Argument marshalling only: every step of ``tile_copy``, ``tile_rowsum``,
+``tile_colsum`` and ``tile_copy_rowsum`` runs in the library's CUDA kernels,
+and the host-buffer forms (``tile_*_host``) are the library's own slab
+pipeline.  PyTorch supplies device memory and streams.  If the compiled
+library is missing, every call raises; there is no fallback path.
 
 The C entry points are reachable with the header's names through ``C`` (a
 ctypes handle); the functions below take ``torch.Tensor`` arguments.
@@ -20,10 +21,12 @@ import torch
 from . import _build
 
 __all__ = [
-    "MbtError", "C", "library_path", "tile_copy", "tile_rowsum", "tile_status",
-    "tile_plan", "tile_device_info", "tile_strerror", "tile_rowsum_workspace_bytes",
-    "Opts", "Plan", "DTYPE_CODE", "OP_COPY", "OP_ROWSUM", "OP_COPY_ROWSUM", "tile_rowsum_noalloc",
-    "tile_copy_rowsum", "tile_stage_image",
+    "MbtError", "C", "library_path", "Opts", "Plan", "DTYPE_CODE",
+    "OP_COPY", "OP_ROWSUM", "OP_COPY_ROWSUM", "OP_COLSUM", "MBT_OK", "MBT_ERR_TIMEOUT",
+    "tile_copy", "tile_rowsum", "tile_colsum", "tile_copy_rowsum", "tile_rowsum_noalloc",
+    "tile_rowsum_workspace_bytes", "tile_colsum_workspace_bytes",
+    "tile_copy_host", "tile_rowsum_host", "tile_colsum_host", "tile_host_release",
+    "tile_status", "tile_plan", "tile_device_info", "tile_strerror", "tile_stage_image",
 ]
 
 MBT_OK = 0
@@ -246,6 +249,13 @@ _ws_cache: "OrderedDict[tuple[int, int], torch.Tensor]" = OrderedDict()
 _WS_CACHE_MAX = 16   # (device, stream) pairs kept; the least recently used goes first
 
 
+def _device_empty(n: int, device: torch.device, stream=None) -> torch.Tensor:
+    """fp32[n] for a result, allocated on the stream that will write it (so the
+    caching allocator orders any later reuse of the block after that work)."""
+    with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
+        return torch.empty(n, dtype=torch.float32, device=device)
+
+
 def _workspace(device: torch.device, nbytes: int, stream=None) -> torch.Tensor:
     """A zero-filled byte buffer of at least ``nbytes`` on ``device``, reused
     across calls on the same stream (the kernels leave it zero-filled; calls
@@ -310,7 +320,7 @@ def tile_colsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int 
     unless one is given)."""
     M, N, ld_s = _matrix(src, "src")
     if out is None:
-        out = torch.empty(N, dtype=torch.float32, device=src.device)
+        out = _device_empty(N, src.device, stream)
     if out.dtype != torch.float32 or out.numel() != N or not out.is_contiguous():
         raise ValueError("out must be a contiguous float32 tensor of N elements")
     o = _opts(ld_src=ld_s, consumer_warps=consumer_warps, max_ctas=max_ctas,
@@ -348,7 +358,7 @@ def tile_rowsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int 
     same in all three."""
     M, N, ld_s = _matrix(src, "src")
     if out is None:
-        out = torch.empty(M, dtype=torch.float32, device=src.device)
+        out = _device_empty(M, src.device, stream)
     if out.dtype != torch.float32 or out.numel() != M or not out.is_contiguous():
         raise ValueError("out must be a contiguous float32 tensor of M elements")
     o = _opts(ld_src=ld_s, consumer_warps=consumer_warps, max_ctas=max_ctas,
@@ -383,7 +393,7 @@ def tile_copy_rowsum(src: torch.Tensor, dst: torch.Tensor, out: torch.Tensor | N
     if (M, N) != (Md, Nd) or src.dtype != dst.dtype:
         raise ValueError("src and dst must have the same shape and dtype")
     if out is None:
-        out = torch.empty(M, dtype=torch.float32, device=src.device)
+        out = _device_empty(M, src.device, stream)
     if out.dtype != torch.float32 or out.numel() != M or not out.is_contiguous():
         raise ValueError("out must be a contiguous float32 tensor of M elements")
     o = _opts(ld_src=ld_s, ld_dst=ld_d, consumer_warps=consumer_warps, max_ctas=max_ctas,

@@ -452,3 +452,9 @@ def test_ctypes_mirrors_match_the_c_structs(tmp_path):
         assert int(out[struct]) == ctypes.sizeof(cls), struct
         for n, _ in cls._fields_:
             assert int(out[f"{struct}.{n}"]) == getattr(cls, n).offset, (struct, n)
+
+
+def test_binding_exports_what_it_lists():
+    assert all(hasattr(mbt, name) for name in mbt.__all__)
+    for name in ("tile_colsum", "tile_copy_host", "tile_rowsum_host", "tile_colsum_host"):
+        assert name in mbt.__all__
