@@ -54,8 +54,9 @@
  *   - Return value: MBT_OK, or a negative mbt_status.  Argument errors are
  *     detected on the host before anything is launched.  A pipeline wait that
  *     runs past its time budget on the device does not hang: the kernel
- *     records MBT_ERR_TIMEOUT in the status word and returns; tile_status
- *     reports it.
+ *     records MBT_ERR_TIMEOUT in the per-device status word (or in the call's
+ *     own buffer, mbt_opts.status) and returns; tile_status reports the
+ *     word.
  *   - Thread safety: entry points may be called from several host threads.
  *     Concurrent calls must not share a workspace.
  */
@@ -149,7 +150,19 @@ typedef struct mbt_opts {
                                 per slab; 0 => whole row bands of about
                                 MBT_HOST_SLAB_BYTES.  Must be 0 for the
                                 device calls. */
-    int32_t reserved[5];     /* must be 0 */
+    int32_t reserved0;       /* must be 0 */
+    int32_t *status;         /* optional device int32[4], zero on entry: a
+                                pipeline wait of this call that runs out of
+                                its budget is recorded here ({code, block,
+                                stage, role * 2 + parity}, as tile_status
+                                reports it) instead of in the per-device
+                                status word, so that calls on concurrent
+                                streams can tell whose wait stalled.  The
+                                caller reads it after the stream has
+                                finished and clears it before reuse.  NULL =>
+                                the per-device word.  Must be 4-byte
+                                aligned. */
+    int32_t reserved[2];     /* must be 0 */
 } mbt_opts;
 
 /* Launch plan, as computed by tile_plan (host only, no CUDA calls). */
@@ -385,8 +398,10 @@ int tile_stage_image(const void *src, int64_t M, int64_t N, int64_t ld, int tile
  * opts: as for the device calls, except that log, workspace and
  * workspace_bytes must be NULL / 0 (the slab schedule owns them).  Returns
  * MBT_OK, an argument error before anything is copied, MBT_ERR_CUDA, or
- * MBT_ERR_TIMEOUT when a pipeline wait ran out of its budget (the status word
- * is read and cleared by the call, see tile_status).
+ * MBT_ERR_TIMEOUT when a pipeline wait of this call ran out of its budget
+ * (each staging set has its own device status buffer, so concurrent calls and
+ * the per-device word do not see one another's timeouts).  opts->status must
+ * be NULL.
  */
 #define MBT_HOST_SLAB_BYTES (64ll << 20)
 int tile_copy_host(const void *src, void *dst, int64_t M, int64_t N, int tile_m, int tile_n,

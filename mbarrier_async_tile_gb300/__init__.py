@@ -52,7 +52,9 @@ class Opts(ctypes.Structure):
         ("fault", ctypes.c_int32),
         ("pipeline", ctypes.c_int32),
         ("host_slab_rows", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 5),
+        ("reserved0", ctypes.c_int32),
+        ("status", ctypes.c_void_p),
+        ("reserved", ctypes.c_int32 * 2),
     ]
 
 
@@ -217,17 +219,34 @@ def _opts(**kw) -> Opts:
     return o
 
 
+def _set_log_status(o: Opts, log: torch.Tensor | None, status: torch.Tensor | None,
+                    device: torch.device) -> None:
+    """Point ``o`` at the caller's log records and per-call status buffer."""
+    if log is not None:
+        o.log = log.data_ptr()
+        o.log_capacity = log.numel() // 8
+    if status is not None:
+        if (status.dtype != torch.int32 or status.device != device or status.numel() < 4
+                or not status.is_contiguous()):
+            raise ValueError("status must be a contiguous int32 tensor of at least 4 "
+                             "elements on the matrix's device")
+        o.status = status.data_ptr()
+
+
 def tile_copy(src: torch.Tensor, dst: torch.Tensor, tile_m: int = 128, tile_n: int = 64,
               stages: int = 4, *, consumer_warps: int = 0, max_ctas: int = 0,
               ctas_per_sm: int = 0, wait_budget_ns: int = 0, log: torch.Tensor | None = None,
               fault: int = 0, store_mode: int = 0, pipeline: int = 0,
-              stream=None) -> torch.Tensor:
+              status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """dst[i, j] = src[i, j] (bit-exact) through the tile pipeline.
 
     ``src`` and ``dst`` are 2-D CUDA views of the same shape and dtype with
     unit column stride; their row strides may differ (pitched storage).
     ``store_mode``: 1 bulk tensor stores, 2 16-byte LSU stores, 0 (default)
-    bulk where rows end inside a 16-byte chunk, else LSU."""
+    bulk where rows end inside a 16-byte chunk, else LSU.  ``status``: an
+    optional zero-filled CUDA int32[4] that records this call's timed-out
+    wait (as :func:`tile_status` reports it) instead of the per-device word;
+    the sums and the fused call take it too."""
     M, N, ld_s = _matrix(src, "src")
     Md, Nd, ld_d = _matrix(dst, "dst")
     if (M, N) != (Md, Nd) or src.dtype != dst.dtype:
@@ -235,9 +254,7 @@ def tile_copy(src: torch.Tensor, dst: torch.Tensor, tile_m: int = 128, tile_n: i
     o = _opts(ld_src=ld_s, ld_dst=ld_d, consumer_warps=consumer_warps, max_ctas=max_ctas,
               ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault,
               store_mode=store_mode, pipeline=pipeline)
-    if log is not None:
-        o.log = log.data_ptr()
-        o.log_capacity = log.numel() // 8
+    _set_log_status(o, log, status, src.device)
     rc = _load().tile_copy_ex(src.data_ptr(), dst.data_ptr(), M, N, tile_m, tile_n, stages,
                               DTYPE_CODE[src.dtype], _stream_handle(stream), ctypes.byref(o))
     _check(rc, "tile_copy")
@@ -313,7 +330,8 @@ def tile_colsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int 
                 tile_n: int = 256, stages: int = 2, *, split: bool = True,
                 consumer_warps: int = 0, max_ctas: int = 0, ctas_per_sm: int = 0,
                 wait_budget_ns: int = 0, log: torch.Tensor | None = None, fault: int = 0,
-                workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
     """out[j] = sum_i src[i, j] in fp32 through the tile pipeline (tiles taken
     down each column strip).  With ``split`` (default) strips may be shared by
     several CTAs, using a zero-filled workspace (cached per device and stream
@@ -325,9 +343,7 @@ def tile_colsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int 
         raise ValueError("out must be a contiguous float32 tensor of N elements")
     o = _opts(ld_src=ld_s, consumer_warps=consumer_warps, max_ctas=max_ctas,
               ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault)
-    if log is not None:
-        o.log = log.data_ptr()
-        o.log_capacity = log.numel() // 8
+    _set_log_status(o, log, status, src.device)
     if split and M > 0 and N > 0:
         need = tile_colsum_workspace_bytes(M, N, tile_m, tile_n, stages, src.dtype,
                                            ld_src=ld_s, consumer_warps=consumer_warps,
@@ -347,7 +363,7 @@ def tile_rowsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int 
                 consumer_warps: int = 0, max_ctas: int = 0, ctas_per_sm: int = 0,
                 wait_budget_ns: int = 0, log: torch.Tensor | None = None, fault: int = 0,
                 workspace: torch.Tensor | None = None, pipeline: int = 0,
-                stream=None) -> torch.Tensor:
+                status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """out[i] = sum_j src[i, j] in fp32 through the tile pipeline.
 
     With ``split`` (default) row bands may be shared by several CTAs, using a
@@ -364,9 +380,7 @@ def tile_rowsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int 
     o = _opts(ld_src=ld_s, consumer_warps=consumer_warps, max_ctas=max_ctas,
               ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault,
               pipeline=pipeline)
-    if log is not None:
-        o.log = log.data_ptr()
-        o.log_capacity = log.numel() // 8
+    _set_log_status(o, log, status, src.device)
     if split and M > 0 and N > 0:
         need = tile_rowsum_workspace_bytes(M, N, tile_m, tile_n, stages, src.dtype,
                                            ld_src=ld_s, consumer_warps=consumer_warps,
@@ -386,7 +400,8 @@ def tile_copy_rowsum(src: torch.Tensor, dst: torch.Tensor, out: torch.Tensor | N
                      split: bool = True, consumer_warps: int = 0, max_ctas: int = 0,
                      ctas_per_sm: int = 0, wait_budget_ns: int = 0,
                      log: torch.Tensor | None = None, fault: int = 0,
-                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                     workspace: torch.Tensor | None = None,
+                     status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """dst[i, j] = src[i, j] and out[i] = sum_j src[i, j] in one pass; returns out."""
     M, N, ld_s = _matrix(src, "src")
     Md, Nd, ld_d = _matrix(dst, "dst")
@@ -398,9 +413,7 @@ def tile_copy_rowsum(src: torch.Tensor, dst: torch.Tensor, out: torch.Tensor | N
         raise ValueError("out must be a contiguous float32 tensor of M elements")
     o = _opts(ld_src=ld_s, ld_dst=ld_d, consumer_warps=consumer_warps, max_ctas=max_ctas,
               ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault)
-    if log is not None:
-        o.log = log.data_ptr()
-        o.log_capacity = log.numel() // 8
+    _set_log_status(o, log, status, src.device)
     if split and M > 0 and N > 0:
         need = tile_rowsum_workspace_bytes(M, N, tile_m, tile_n, stages, src.dtype, fused=True,
                                            ld_src=ld_s, ld_dst=ld_d,

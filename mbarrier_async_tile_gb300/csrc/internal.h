@@ -45,6 +45,7 @@ struct PipeArgs {
     uint64_t wait_budget_ns;
     int32_t *log;
     int64_t log_cap;
+    int32_t *status;           // the call's status buffer, or nullptr (g_status)
 };
 
 struct CopyArgs {

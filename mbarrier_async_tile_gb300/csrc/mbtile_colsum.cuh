@@ -179,7 +179,7 @@ __device__ void consume_colsum(const ColsumArgs &a, const Smem &sm, const WaitCt
         got = __all_sync(0xffffffffu, got);
         if (!got) {
             if (lane == 0) {
-                report_timeout(1, stage, phase);
+                report_timeout(w, 1, stage, phase);
                 *w.abort = 1;
             }
             ok = false;
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     Smem sm;
     init_pipeline(a.p, sm, bars, &abort_flag, &flush_bar,
                   static_cast<uint32_t>(a.p.consumer_warps), dyn_smem);
-    WaitCtl w{a.p.wait_budget_ns, &abort_flag};
+    WaitCtl w{a.p.wait_budget_ns, &abort_flag, status_of(a.p)};
     // Contiguous, evenly split range of scheduling units, in strip-major order.
     const int64_t G = gridDim.x;
     const int64_t b = blockIdx.x;

@@ -93,7 +93,7 @@ __device__ void produce_flat(const FlatArgs &a, const Smem &sm, const WaitCtl &w
     bool ok = true;
     for (int64_t j = 0; j < count; ++j) {
         if (!wait_bounded(sm.empty0 + 8u * stage, phase, w, true)) {
-            report_timeout(0, stage, phase);
+            report_timeout(w, 0, stage, phase);
             *w.abort = 1;
             ok = false;
             break;
@@ -117,7 +117,7 @@ __device__ void produce_flat(const FlatArgs &a, const Smem &sm, const WaitCtl &w
     if (ok) {
         for (int s = 0; s < p.stages; ++s) {
             if (!wait_bounded(sm.empty0 + 8u * stage, phase, w, true)) {
-                report_timeout(0, stage, phase);
+                report_timeout(w, 0, stage, phase);
                 *w.abort = 1;
                 ok = false;
                 break;
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     Smem sm;
     init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);
     const PipeArgs &p = a.p;
-    WaitCtl w{p.wait_budget_ns, &abort_flag};
+    WaitCtl w{p.wait_budget_ns, &abort_flag, status_of(p)};
     const int64_t G = gridDim.x;
     const int64_t nwin = (a.t_floor + a.cap_bytes - 1) / a.cap_bytes;
     const int64_t first = blockIdx.x;
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
             if (lane == 0) {
-                report_timeout(1, stage, phase);
+                report_timeout(w, 1, stage, phase);
                 *w.abort = 1;
             }
             break;
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
             mbar_init(smem_u32(&row_bar[k]), static_cast<uint32_t>(a.p.consumer_warps));
     init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);   // fences the inits
     const PipeArgs &p = a.p;
-    WaitCtl w{p.wait_budget_ns, &abort_flag};
+    WaitCtl w{p.wait_budget_ns, &abort_flag, status_of(p)};
     const int64_t G = gridDim.x;
     const int64_t ra = static_cast<int64_t>(blockIdx.x) * p.M / G;
     const int64_t rb = (static_cast<int64_t>(blockIdx.x) + 1) * p.M / G;
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
             if (lane == 0) {
-                report_timeout(1, stage, phase);
+                report_timeout(w, 1, stage, phase);
                 *w.abort = 1;
             }
             break;
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
                     got = __all_sync(0xffffffffu, got);
                     if (!got) {
                         if (lane == 0) {
-                            report_timeout(1, kMaxStages, static_cast<uint32_t>(slot));
+                            report_timeout(w, 1, kMaxStages, static_cast<uint32_t>(slot));
                             *w.abort = 1;
                         }
                         break;

@@ -90,6 +90,8 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
     if (o.store_mode != 0 && op != MBT_OP_COPY) return MBT_ERR_ARG;
     for (int r : o.reserved)
         if (r != 0) return MBT_ERR_ARG;
+    if (o.reserved0 != 0) return MBT_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(o.status) % 4 != 0) return MBT_ERR_ALIGN;
     if (o.host_slab_rows != 0) return MBT_ERR_ARG;   // host-buffer forms only
     if (o.log != nullptr && o.log_capacity == 0) return MBT_ERR_ARG;
     if (o.workspace == nullptr && o.workspace_bytes != 0) return MBT_ERR_ARG;
@@ -506,6 +508,7 @@ PipeArgs pipe_args(const mbt_plan &plan, int64_t M, int64_t N, int tile_m, int s
     p.wait_budget_ns = o.wait_budget_ns ? o.wait_budget_ns : mbt::kDefaultWaitBudgetNs;
     p.log = o.log;
     p.log_cap = o.log_capacity;
+    p.status = o.status;
     return p;
 }
 

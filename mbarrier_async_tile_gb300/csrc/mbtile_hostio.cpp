@@ -144,7 +144,9 @@ int host_run(int op, const void *src, void *dst, float *out, int64_t M, int64_t 
     const bool is_copy = op == MBT_OP_COPY, cols = op == MBT_OP_COLSUM;
     if (es == 0 || M < 0 || N < 0) return MBT_ERR_ARG;
     // Device-side options that the slab schedule owns.
-    if (o.log != nullptr || o.workspace != nullptr || o.workspace_bytes != 0) return MBT_ERR_ARG;
+    if (o.log != nullptr || o.workspace != nullptr || o.workspace_bytes != 0 ||
+        o.status != nullptr)
+        return MBT_ERR_ARG;
     const int64_t ld_src = o.ld_src ? o.ld_src : N;
     const int64_t ld_dst = o.ld_dst ? o.ld_dst : N;
     if (ld_src < N || ld_dst < N || (!is_copy && o.ld_dst != 0)) return MBT_ERR_ARG;
@@ -196,21 +198,26 @@ int host_run(int op, const void *src, void *dst, float *out, int64_t M, int64_t 
                 : round_up(static_cast<size_t>(cols ? N : R) * sizeof(float), kAlign);
     const size_t acc_bytes = cols ? round_up(static_cast<size_t>(N) * sizeof(float), kAlign) : 0;
     const size_t ws_region = round_up(ws_bytes, kAlign);
-    const size_t need = ws_region + acc_bytes + kSlots * (slab_in + slab_out);
+    // Layout: the call's status buffer (int32[4]), the sum workspace, the
+    // column-sum accumulator, then the slab slots.
+    const size_t status_region = kAlign;
+    const size_t need = status_region + ws_region + acc_bytes + kSlots * (slab_in + slab_out);
 
     Staging *st = nullptr;
     rc = acquire(need, &st);
     if (rc != MBT_OK) return rc;
-    char *ws = st->base;
-    float *acc = reinterpret_cast<float *>(st->base + ws_region);
+    int32_t *status = reinterpret_cast<int32_t *>(st->base);
+    char *ws = st->base + status_region;
+    float *acc = reinterpret_cast<float *>(ws + ws_region);
     auto slot_in = [&](int s) {
-        return st->base + ws_region + acc_bytes + s * (slab_in + slab_out);
+        return ws + ws_region + acc_bytes + s * (slab_in + slab_out);
     };
     auto slot_out = [&](int s) { return slot_in(s) + slab_in; };
-    if (ws_bytes > 0 && cudaMemsetAsync(ws, 0, ws_bytes, st->comp) != cudaSuccess)
+    if (cudaMemsetAsync(st->base, 0, status_region + ws_bytes, st->comp) != cudaSuccess)
         rc = MBT_ERR_CUDA;
     dev_o.workspace = ws_bytes > 0 ? ws : nullptr;
     dev_o.workspace_bytes = ws_bytes;
+    dev_o.status = status;   // this call's timeouts only
 
     const char *hsrc = static_cast<const char *>(src);
     const size_t spitch = static_cast<size_t>(ld_src) * es;
@@ -280,13 +287,13 @@ int host_run(int op, const void *src, void *dst, float *out, int64_t M, int64_t 
                         cudaStreamSynchronize(st->comp) == cudaSuccess &&
                         cudaStreamSynchronize(st->d2h) == cudaSuccess;
     if (!synced && rc == MBT_OK) rc = MBT_ERR_CUDA;
-    int32_t info[4];
-    const int status = tile_status(st->comp, info);
-    if (rc == MBT_OK) rc = status;
-    if (status == MBT_ERR_TIMEOUT && ws_bytes > 0) {
-        // A stalled sum may leave tickets or partials behind.
-        cudaMemsetAsync(ws, 0, ws_bytes, st->comp);
-        cudaStreamSynchronize(st->comp);
+    int32_t info[4] = {0, 0, 0, 0};
+    if (cudaMemcpyAsync(info, status, sizeof info, cudaMemcpyDeviceToHost, st->comp) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st->comp) != cudaSuccess) {
+        if (rc == MBT_OK) rc = MBT_ERR_CUDA;
+    } else if (info[0] != 0 && rc == MBT_OK) {
+        rc = info[0];   // MBT_ERR_TIMEOUT
     }
     release(st);
     return rc;

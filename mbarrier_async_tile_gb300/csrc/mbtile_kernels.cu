@@ -18,8 +18,9 @@
 // "异步协作：mbarrier"; "CUDA features 10: Pipelines" §4.10.4-4.10.5.
 //
 // Every wait is bounded (time budget from the host).  A wait that runs out
-// records MBT_ERR_TIMEOUT in g_status, raises a CTA-local abort flag that makes
-// the CTA's other waits give up early, and the producer then waits (again
+// records MBT_ERR_TIMEOUT in the call's status buffer (or, without one, in
+// g_status), raises a CTA-local abort flag that makes the CTA's other waits
+// give up early, and the producer then waits (again
 // bounded) for the bulk copies it still has in flight before the CTA exits.
 //
 // Kernels: mbt_copy_kernel<bulk> (LSU stores, or bulk tensor stores from one
@@ -157,7 +158,13 @@ __device__ __forceinline__ uint32_t chunk_offset(int row, int q, uint32_t box_st
 struct WaitCtl {
     uint64_t budget_ns;
     volatile int *abort;
+    int32_t *status;    // where a timed-out wait is recorded: the call's own
+                        // status buffer (mbt_opts.status) or g_status
 };
+
+__device__ __forceinline__ int32_t *status_of(const PipeArgs &p) {
+    return p.status != nullptr ? p.status : g_status;
+}
 
 __device__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl &w,
                              bool heed_abort) {
@@ -176,11 +183,12 @@ __device__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtl &w,
     return false;
 }
 
-__device__ void report_timeout(int role, uint32_t stage, uint32_t parity) {
-    if (atomicCAS(&g_status[0], 0, static_cast<int32_t>(MBT_ERR_TIMEOUT)) == 0) {
-        g_status[1] = static_cast<int32_t>(blockIdx.x);
-        g_status[2] = static_cast<int32_t>(stage);
-        g_status[3] = role * 2 + static_cast<int32_t>(parity);
+__device__ void report_timeout(const WaitCtl &w, int role, uint32_t stage, uint32_t parity) {
+    int32_t *st = w.status;
+    if (atomicCAS(&st[0], 0, static_cast<int32_t>(MBT_ERR_TIMEOUT)) == 0) {
+        st[1] = static_cast<int32_t>(blockIdx.x);
+        st[2] = static_cast<int32_t>(stage);
+        st[3] = role * 2 + static_cast<int32_t>(parity);
     }
 }
 
@@ -230,7 +238,7 @@ __device__ void produce(const CUtensorMap *map, const PipeArgs &p, const Smem &s
         // (measured: this order keeps the 3-stage row sum 1.3% faster than
         // computing the coordinates ahead of the wait).
         if (!boxed && !wait_bounded(sm.empty0 + 8u * stage, phase, w, true)) {
-            report_timeout(0, stage, phase);
+            report_timeout(w, 0, stage, phase);
             *w.abort = 1;
             ok = false;
             break;
@@ -251,7 +259,7 @@ __device__ void produce(const CUtensorMap *map, const PipeArgs &p, const Smem &s
         if (boxed) {
             for (int b = 0; b < p.boxes; ++b) {
                 if (!wait_bounded(box_bar(sm.emptyb0, stage, b), phase, w, true)) {
-                    report_timeout(0, stage, phase);
+                    report_timeout(w, 0, stage, phase);
                     *w.abort = 1;
                     ok = false;
                     if (b > 0) {   // boxes 0 .. b-1 of this tile are in flight
@@ -286,7 +294,7 @@ __device__ void produce(const CUtensorMap *map, const PipeArgs &p, const Smem &s
             for (int b = 0; b < nb; ++b) {
                 const uint32_t bar = boxed ? box_bar(sm.emptyb0, stage, b) : sm.empty0 + 8u * stage;
                 if (!wait_bounded(bar, phase, w, true)) {
-                    report_timeout(0, stage, phase);
+                    report_timeout(w, 0, stage, phase);
                     *w.abort = 1;
                     ok = false;
                     break;
@@ -420,7 +428,7 @@ __device__ void consume_copy(const CopyArgs &a, const Smem &sm, const WaitCtl &w
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
             if (lane == 0) {
-                report_timeout(1, stage, phase);
+                report_timeout(w, 1, stage, phase);
                 *w.abort = 1;
             }
             break;
@@ -532,7 +540,7 @@ __device__ void consume_copy_bulk(const CUtensorMap *dst_map, const CopyArgs &a,
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
             if (lane == 0) {
-                report_timeout(1, stage, phase);
+                report_timeout(w, 1, stage, phase);
                 *w.abort = 1;
             }
             break;
@@ -577,7 +585,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     __shared__ int abort_flag;
     Smem sm;
     init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);
-    WaitCtl w{a.p.wait_budget_ns, &abort_flag};
+    WaitCtl w{a.p.wait_budget_ns, &abort_flag, status_of(a.p)};
     // Tiles b, b + G, b + 2G, ... in row-major tile order.
     const int64_t G = gridDim.x;
     const int64_t first = blockIdx.x;
@@ -610,7 +618,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     Smem sm;
     init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);
     const PipeArgs &p = a.p;
-    WaitCtl w{p.wait_budget_ns, &abort_flag};
+    WaitCtl w{p.wait_budget_ns, &abort_flag, status_of(p)};
     const int64_t G = gridDim.x;
     const int64_t first = blockIdx.x;
     const int64_t count = first < p.num_tiles ? (p.num_tiles - first + G - 1) / G : 0;
@@ -647,7 +655,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
                           (tile - tm * p.tiles_n) * p.boxes * p.box_inner,
                           static_cast<int>(threadIdx.x), nthr, 0u);
         } else if ((threadIdx.x & 31) == 0) {
-            report_timeout(1, s, par);
+            report_timeout(w, 1, s, par);
             *w.abort = 1;
         }
         if (__syncthreads_or(!ok)) break;
@@ -704,7 +712,7 @@ __device__ bool consumers_sync(FlushCtl &f, const WaitCtl &w) {
     ok = __all_sync(0xffffffffu, ok);
     f.parity ^= 1u;
     if (!ok && (threadIdx.x & 31) == 0) {
-        report_timeout(1, kMaxStages, f.parity ^ 1u);
+        report_timeout(w, 1, kMaxStages, f.parity ^ 1u);
         *w.abort = 1;
     }
     return ok;
@@ -808,7 +816,7 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
         got = __all_sync(0xffffffffu, got);
         if (!got) {
             if (lane == 0) {
-                report_timeout(1, stage, phase);
+                report_timeout(w, 1, stage, phase);
                 *w.abort = 1;
             }
             ok = false;
@@ -866,7 +874,7 @@ __global__ void __launch_bounds__(FUSED ? kMaxThreads + 32 : kMaxThreads, 2)
     constexpr bool boxed = BOXED;
     init_pipeline(a.p, sm, bars, &abort_flag, &flush_bar,
                   static_cast<uint32_t>(a.p.consumer_warps), dyn_smem, boxed);
-    WaitCtl w{a.p.wait_budget_ns, &abort_flag};
+    WaitCtl w{a.p.wait_budget_ns, &abort_flag, status_of(a.p)};
     // Contiguous, evenly split range of scheduling units, in band-major order.
     const int64_t G = gridDim.x;
     const int64_t b = blockIdx.x;
@@ -930,9 +938,9 @@ __global__ void mbt_stage_image_kernel(const __grid_constant__ CUtensorMap map, 
         for (int k = 0; k < boxes; ++k)
             tma_load_2d(base + k * box_stride, &map, col0 + k * box_inner, row0, b);
     }
-    WaitCtl w{budget_ns, &abort_flag};
+    WaitCtl w{budget_ns, &abort_flag, g_status};
     const bool ok = wait_bounded(b, 0, w, false);
-    if (!ok && threadIdx.x == 0) report_timeout(1, 0, 0);
+    if (!ok && threadIdx.x == 0) report_timeout(w, 1, 0, 0);
     const unsigned char *stage = dyn_smem + (base - smem_u32(dyn_smem));
     if (ok)
         for (uint32_t i = threadIdx.x; i < box_bytes * boxes; i += blockDim.x) {

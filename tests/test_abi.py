@@ -94,8 +94,13 @@ def test_copy_tile_and_stage_errors():
 
 def test_option_errors():
     o = Opts()
-    o.reserved[2] = 1
+    o.reserved[1] = 1
     assert _copy(A, B, 8, 64, opts=o) == -1
+    o = Opts(); o.reserved0 = 1
+    assert _copy(A, B, 8, 64, opts=o) == -1
+    o = Opts(); o.status = B + 2                   # a status buffer must be 4-byte aligned
+    assert _copy(A, B, 8, 64, opts=o) == -2
+    assert C.tile_rowsum_ex(A, B, 8, 64, 128, 64, 3, 0, None, ctypes.byref(o)) == -2
     o = Opts(); o.consumer_warps = 9
     assert _copy(A, B, 8, 64, opts=o) == -1
     o = Opts(); o.fault = 3
@@ -155,7 +160,7 @@ def test_host_forms_argument_errors_before_any_cuda_call():
     assert C.tile_copy_host(p(src), None, 8, 8, 64, 64, 2, 0, None) == -1
     assert C.tile_copy_host(p(src), p(src), 8, 8, 64, 64, 2, 7, None) == -1   # dtype
     for field, value in (("log", 16), ("workspace", 16), ("workspace_bytes", 4),
-                         ("host_slab_rows", -1), ("ld_src", 4)):
+                         ("host_slab_rows", -1), ("ld_src", 4), ("status", 16)):
         o = Opts()
         setattr(o, field, value)
         assert C.tile_copy_host(p(src), p(src), 8, 8, 64, 64, 2, 0, ctypes.byref(o)) == -1, field
