@@ -37,6 +37,7 @@ ROWSUM = dict(name="rowsum", dtype="bf16", M=8192, N=65536, tile_m=64, tile_n=25
 ESIZE = {"f16": 2, "bf16": 2, "f32": 4}
 FALLBACK_HBM_GBS = 6800.0
 MODE_NAME = {0: "default", 1: "bulk tensor stores", 2: "LSU stores"}
+GRAPH_CHUNK = 50   # steps per captured CUDA graph
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture
 # of each kernel on the full-size workload, keyed by the SHA-256 of the kernel
@@ -350,9 +351,13 @@ def bench_gpu(args, rank, world):
 
     def run_kernel_pass(which: str):
         """Time args.steps back-to-back launches of one kernel on the main
-        stream, an event pair around each; returns the mean ms per launch.
-        In the one-stream pass a row sum starts while L2 still writes back
-        the dirty lines the copy before it left (up to ~126 MB), so that
+        stream, twice: with one event pair around the whole series (the mean
+        launch duration, gaps between launches included: the roofline's
+        figure) and with an event pair around each launch (each launch then
+        also pays its own start-up, which back-to-back launches overlap with
+        the previous launch's tail).  Returns (ms back to back, ms per event
+        pair).  In the one-stream pass a row sum starts while L2 still writes
+        back the dirty lines the copy before it left (up to ~126 MB), so that
         pass charges part of the copy's writes to the row sum; here every
         launch follows one of its own kind (steady state)."""
         def launch():
@@ -362,8 +367,25 @@ def bench_gpu(args, rank, world):
             else:
                 mbt.tile_rowsum(x4, o4, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
                                 workspace=ws, stream=main)
+
+        def check():
+            code, info = mbt.tile_status(main)
+            if code != 0:
+                raise RuntimeError(f"pipeline status {code} {info}")
+
         for _ in range(args.warmup):
             launch()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(main)
+        for _ in range(args.steps):
+            launch()
+        end.record(main)
+        torch.cuda.synchronize()
+        barrier(world)
+        check()
+        ms_b2b = reduce_max(start.elapsed_time(end) / args.steps, world)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
         barrier(world)
@@ -374,25 +396,106 @@ def bench_gpu(args, rank, world):
             b.record(main)
         torch.cuda.synchronize()
         barrier(world)
+        check()
+        ms_pairs = reduce_max(sum(a.elapsed_time(b) for a, b in evs) / args.steps, world)
+        return ms_b2b, ms_pairs
+
+    def copy_on(stream):
+        mbt.tile_copy(x3, d3, COPY["tile_m"], COPY["tile_n"], args.copy_stages,
+                      store_mode=args.store_mode, stream=stream)
+
+    def rowsum_on(stream):
+        mbt.tile_rowsum(x4, o4, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
+                        workspace=ws, stream=stream)
+
+    def graphed(chunk_body, steps: int):
+        """CUDA graphs that together replay `steps` steps: chunk_body(origin,
+        n) launches n steps from the capturing stream `origin` (forking to
+        and joining back from side streams itself).  Returns a function that
+        replays them on the current stream."""
+        full, rem = divmod(steps, GRAPH_CHUNK)
+        graphs = []
+        for n, times in ((GRAPH_CHUNK, full), (rem, 1)):
+            if n == 0 or times == 0:
+                continue
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            cap.wait_stream(main)
+            with torch.cuda.graph(g, stream=cap):
+                chunk_body(cap, n)
+            graphs.append((g, times))
+
+        def replay():
+            for g, times in graphs:
+                for _ in range(times):
+                    g.replay()
+        return replay
+
+    def time_graphed(replay) -> float:
+        """Mean ms per step of the replayed graphs (one event pair around all
+        of them), after one untimed replay of the whole set."""
+        replay()
+        torch.cuda.synchronize()
         code, info = mbt.tile_status(main)
         if code != 0:
             raise RuntimeError(f"pipeline status {code} {info}")
-        return reduce_max(sum(a.elapsed_time(b) for a, b in evs) / args.steps, world)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(main)
+        replay()
+        end.record(main)
+        torch.cuda.synchronize()
+        barrier(world)
+        code, info = mbt.tile_status(main)
+        if code != 0:
+            raise RuntimeError(f"pipeline status {code} {info}")
+        return reduce_max(start.elapsed_time(end), world)
+
+    def kernel_chunk(which):
+        def body(origin, n):
+            for _ in range(n):
+                (copy_on if which == "copy" else rowsum_on)(origin)
+        return body
+
+    def step_chunk(two_streams):
+        def body(origin, n):
+            s_copy, s_rowsum = side if two_streams else (origin, origin)
+            s_copy.wait_stream(origin)
+            s_rowsum.wait_stream(origin)
+            for _ in range(n):
+                copy_on(s_copy)
+                rowsum_on(s_rowsum)
+            origin.wait_stream(s_copy)
+            origin.wait_stream(s_rowsum)
+        return body
 
     clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.3)
     t0 = time.time()
-    # per-kernel passes: steady-state launch durations for the roofline
-    ms_copy = run_kernel_pass("copy")
-    ms_rowsum = run_kernel_pass("rowsum")
-    # sequential pass: both operations on one stream, per-kernel events
-    ms_seq, ms_copy_seq, ms_rowsum_seq = run_pass(False, True)
-    # the headline pass
+    # per-kernel passes: steady-state launch durations for the roofline,
+    # launched one by one from the host (back to back, and with an event pair
+    # around each launch), then replayed from CUDA graphs
+    ms_copy_stream, ms_copy_pairs = run_kernel_pass("copy")
+    ms_rowsum_stream, ms_rowsum_pairs = run_kernel_pass("rowsum")
+    ms_copy_graph = time_graphed(graphed(kernel_chunk("copy"), args.steps)) / args.steps
+    ms_rowsum_graph = time_graphed(graphed(kernel_chunk("rowsum"), args.steps)) / args.steps
+    # sequential passes: both operations on one stream, then again with
+    # per-kernel events (which add gaps, so they do not time value_one_stream)
+    ms_seq, _, _ = run_pass(False, False)
+    _, ms_copy_seq, ms_rowsum_seq = run_pass(False, True)
+    # the headline pass: the steps launched from the host, then the same
+    # steps replayed from CUDA graphs
     if args.streams == 2:
-        ms_total, _, _ = run_pass(True, False)
+        ms_total_stream, _, _ = run_pass(True, False)
     else:
-        ms_total = ms_seq
+        ms_total_stream = ms_seq
+    ms_total_graph = time_graphed(graphed(step_chunk(args.streams == 2), args.steps))
+    graph = args.launch == "graph"
+    ms_copy = ms_copy_graph if graph else ms_copy_stream
+    ms_rowsum = ms_rowsum_graph if graph else ms_rowsum_stream
+    ms_total = ms_total_graph if graph else ms_total_stream
     t1 = time.time()
     time.sleep(0.15)
     clocks.stop()
@@ -400,6 +503,8 @@ def bench_gpu(args, rank, world):
     value_one_stream = aggregate_gbs(step_bytes, args.steps, world, reduce_max(ms_seq, world))
     ms_max = reduce_max(ms_total, world)
     value = aggregate_gbs(step_bytes, args.steps, world, ms_max)
+    value_other_launch = aggregate_gbs(step_bytes, args.steps, world, reduce_max(
+        ms_total_stream if graph else ms_total_graph, world))
 
     # end to end through the public API with host buffers
     e2e = bench_e2e(args, mbt, x3, x4, world)
@@ -408,10 +513,18 @@ def bench_gpu(args, rank, world):
     kernels = {
         "copy": {"ms": round(ms_copy, 4), "bytes": copy_bytes(),
                  "gbs": round(copy_bytes() / ms_copy / 1e6, 1),
+                 "ms_host_launched": round(ms_copy_stream, 4),
+                 "gbs_host_launched": round(copy_bytes() / ms_copy_stream / 1e6, 1),
+                 "ms_event_pairs": round(ms_copy_pairs, 4),
+                 "gbs_event_pairs": round(copy_bytes() / ms_copy_pairs / 1e6, 1),
                  "ms_in_one_stream_step": round(ms_copy_seq, 4),
                  "stages": args.copy_stages, "tile": [COPY["tile_m"], COPY["tile_n"]]},
         "rowsum": {"ms": round(ms_rowsum, 4), "bytes": rowsum_bytes(),
                    "gbs": round(rowsum_bytes() / ms_rowsum / 1e6, 1),
+                   "ms_host_launched": round(ms_rowsum_stream, 4),
+                   "gbs_host_launched": round(rowsum_bytes() / ms_rowsum_stream / 1e6, 1),
+                   "ms_event_pairs": round(ms_rowsum_pairs, 4),
+                   "gbs_event_pairs": round(rowsum_bytes() / ms_rowsum_pairs / 1e6, 1),
                    "ms_in_one_stream_step": round(ms_rowsum_seq, 4),
                    "stages": args.rowsum_stages, "tile": [ROWSUM["tile_m"], ROWSUM["tile_n"]]},
     }
@@ -425,10 +538,15 @@ def bench_gpu(args, rank, world):
                 "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": round(dom["gbs"] / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_kind} hbm_gbs (copy read+write)",
-                "timing": (f"CUDA events around each of {args.steps} back-to-back launches "
-                           "of this kernel on its stream (steady state); kernels.*."
-                           "ms_in_one_stream_step: the same kernels alternating on one "
-                           "stream, where each inherits the other's L2 write-back")}
+                "timing": ((f"{args.steps} launches of the kernel replayed from CUDA graphs "
+                            f"of {GRAPH_CHUNK} launches" if graph else
+                            f"{args.steps} launches of the kernel from the host") +
+                           ", back to back on one stream, one CUDA event pair around all "
+                           "of them: mean per launch, gaps included; kernels.*."
+                           "ms_host_launched: the same launches from the host; kernels.*."
+                           "ms_event_pairs: host launches with an event pair around each; "
+                           "kernels.*.ms_in_one_stream_step: the two kernels alternating "
+                           "on one stream, where each inherits the other's L2 write-back")}
     out = {
         "metric": "achieved HBM GB/s (read+write) for pipelined tile copy + rowsum",
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -442,10 +560,14 @@ def bench_gpu(args, rank, world):
                    "streams": ("copy and rowsum each on its own stream (independent calls, "
                                "so the kernels overlap); value_one_stream: both on one stream"
                                if args.streams == 2 else "one stream"),
+                   "launch": (f"steps replayed from CUDA graphs of {GRAPH_CHUNK} steps each "
+                              "(captured once before the timed region)" if graph else
+                              "each call launched from the host"),
                    "l2": "inputs (512 MiB, 1 GiB) larger than L2; no flush",
                    "parallelism": f"independent replica per GPU x{world}"},
         "frac_of_peak": round(value / world / peak, 4),
         "value_one_stream": round(value_one_stream, 1),
+        ("value_host_launched" if graph else "value_graph_replay"): round(value_other_launch, 1),
         "kernels": kernels,
         "roofline": roofline,
         "e2e": e2e,
@@ -818,6 +940,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mbtile", "reference"], default="mbtile")
     ap.add_argument("--streams", type=int, default=2, choices=[1, 2])
+    ap.add_argument("--launch", choices=["graph", "host"], default="graph",
+                    help="time steps replayed from CUDA graphs (default) or launched "
+                         "call by call from the host; the other is reported beside it")
     ap.add_argument("--copy-stages", type=int, default=3)
     ap.add_argument("--rowsum-stages", type=int, default=2)
     ap.add_argument("--e2e-steps", type=int, default=5)

@@ -42,8 +42,11 @@
  *     global strides) the stages are filled by 1-D bulk copies of 16-byte-
  *     aligned windows of the matrix's bytes: supported for tile_rowsum at any
  *     pitch and for tile_copy when src and dst are both dense (ld = N); other
- *     cases return MBT_ERR_ALIGN.  The stage then holds tile_m x tile_n
- *     elements' worth of bytes.
+ *     cases return MBT_ERR_ALIGN.  A copy's stage then holds tile_m x tile_n
+ *     elements' worth of bytes.  A row sum's window, whatever the tile, holds
+ *     whole rows -- at most 32 KB while 8 rows fit in that, else at most 64
+ *     KB -- or one of equal pieces (at most 64 KB) of a longer row, within
+ *     what `stages` stages leave of the shared memory.
  *   - A tile is tile_m rows by tile_n columns.  tile_n * element size must be
  *     128, 256, 512 or 1024 bytes (1, 2, 4 or 8 side-by-side 128-byte boxes,
  *     each one bulk copy with the 128-byte swizzle); 1 <= tile_m <= 256;

@@ -82,6 +82,31 @@ def test_unaligned_pitch_routes_and_refusals():
     assert _plan(mbt.OP_COPY, 1000, 64, 128, 64, 3, torch.float16)["flat"] == 0
 
 
+def test_flat_rowsum_windows_follow_the_rows_not_the_tile():
+    """Unaligned-pitch row sums load whole rows (32 KB windows while 8 rows
+    fit, else up to 64 KB) or equal pieces of longer rows, whatever the tile,
+    within what the stages leave of shared memory; the default grid keeps
+    about 192 KB of stages per SM."""
+    smem = 232448
+    plans = [_plan(mbt.OP_ROWSUM, 24577, 16383, tm, tn, 2, torch.float16, fit=8)
+             for tm, tn in ((128, 64), (64, 256), (256, 512))]
+    for p in plans:
+        # one window per 32766-byte row (+ up to 32 bytes of 16-byte rounding)
+        assert p["flat"] == 1 and p["num_tiles"] == 24577 and p["stage_bytes"] == 33 * 1024
+        assert p["grid"] == 3 * 152 and p["consumer_warps"] == 4
+    short = _plan(mbt.OP_ROWSUM, 4194304, 63, 128, 64, 2, torch.float16, fit=8)
+    assert short["stage_bytes"] == 32 * 1024                 # 256 rows of 126 bytes
+    # 200006-byte rows: four pieces of at most 64 KB at 2 stages; at 8 stages
+    # the pieces shrink so that the stages still fit
+    p2 = _plan(mbt.OP_ROWSUM, 2000, 100003, 128, 64, 2, torch.bfloat16, fit=8)
+    assert p2["num_tiles"] == 2000 * 4 and p2["stage_bytes"] <= 64 * 1024 + 1024
+    p8 = _plan(mbt.OP_ROWSUM, 2000, 100003, 128, 64, 8, torch.bfloat16, fit=8)
+    assert p8["smem_bytes"] <= smem and p8["num_tiles"] == 2000 * 7
+    # tile_m above 32 x consumer_warps does not matter without tile rows
+    assert _plan(mbt.OP_ROWSUM, 1000, 63, 256, 64, 2, torch.float16, consumer_warps=1,
+                 fit=8)["flat"] == 1
+
+
 def test_copy_tile_and_stage_errors():
     assert _copy(A, B, 8, 64, tm=0) == -1
     assert _copy(A, B, 8, 64, tm=257) == -1
