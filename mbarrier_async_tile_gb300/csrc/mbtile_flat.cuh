@@ -13,15 +13,6 @@
 // Included by mbtile_kernels.cu inside its anonymous namespace: it uses that
 // file's PTX wrappers, bounded waits and status word.
 
-__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void *src, uint32_t bytes,
-                                             uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
 struct Window {
     int64_t ws;     // first byte (16-byte aligned) loaded into the stage
     int64_t size;   // bytes loaded (multiple of 16, may be 0)

@@ -90,6 +90,17 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
+// 1-D bulk copy of `bytes` bytes (16-byte aligned address and size) from
+// global memory into shared memory; completion is counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void *src, uint32_t bytes,
+                                             uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 // Bulk tensor copy of one 2-D box at element coordinates (x = column, y = row)
 // into shared memory; completion is counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map,
@@ -323,6 +334,147 @@ __device__ void produce(const CUtensorMap *map, const PipeArgs &p, const Smem &s
     }
 }
 
+// What the row-sum producer publishes for each stage (each box with per-box
+// barriers): the band the tile belongs to (-1 marks the end) and the tile's
+// coordinates, so that the consumers do no division between a full barrier
+// and their first read.
+struct StageInfo {
+    int64_t key;
+    int32_t tm, tn;
+};
+
+// Producer of the row-sum kernels: loads the tiles [first, last) in order.
+// Besides loading, it publishes each stage's band and tile coordinates (each
+// box's, with `boxed`) in `info` before the stage's full barrier is armed --
+// the arrive releases them to the consumers, which then need no division of
+// their own between the barrier and their first read (measured: 1.5 % on the
+// bf16 8192 x 65536 row sum, 15-20 % on the fp32 / fp16 ragged ones, without a
+// workspace) -- and closes the ring with an end mark (key -1) on a stage whose
+// full barrier completes by a plain arrive.
+template <bool boxed>
+__device__ void produce_rows(const CUtensorMap *map, const RowsumArgs &a, const Smem &sm,
+                             const WaitCtl &w, int64_t first, int64_t last,
+                             volatile StageInfo *info) {
+    const PipeArgs &p = a.p;
+    uint32_t stage = 0;
+    uint32_t phase = (p.fault == 1) ? 0u : 1u;  // free buffers: start at phase 1
+    int64_t issued = 0;
+    int last_boxes = p.boxes;   // boxes issued of tile issued - 1
+    bool ok = true;
+    const uint32_t box_tx = p.tx_bytes / static_cast<uint32_t>(p.boxes);
+    // The run of tiles being issued: columns [tn, tn_end) of band tm (the
+    // band is the consumers' segment key), one run per band.
+    int64_t tm = 0, tn = 0, tn_end = 0, t_next = first;
+    auto open_run = [&]() {
+        if (t_next >= last) return false;
+        tm = t_next / p.tiles_n;
+        tn = t_next - tm * p.tiles_n;
+        tn_end = last - tm * p.tiles_n < p.tiles_n ? last - tm * p.tiles_n : p.tiles_n;
+        t_next = tm * p.tiles_n + tn_end;
+        return true;
+    };
+    bool more = open_run();
+    for (int64_t j = 0;; ++j) {
+        // Work out the next tile (or the end mark) before waiting for a stage.
+        const bool end = !more;
+        const int64_t ctm = tm, ctn = tn, ckey = end ? -1 : tm;
+        if (!end && ++tn == tn_end) more = open_run();
+        if (!boxed && !wait_bounded(sm.empty0 + 8u * stage, phase, w, true)) {
+            report_timeout(w, 0, stage, phase);
+            *w.abort = 1;
+            ok = false;
+            break;
+        }
+        const int64_t tile = end ? -1 : ctm * p.tiles_n + ctn;
+        const int32_t y = static_cast<int32_t>(ctm * p.tile_m);
+        const int32_t x0 = static_cast<int32_t>(ctn * p.boxes * p.box_inner);
+        const uint32_t dst = sm.base + stage * p.stage_stride;
+        if (boxed) {
+            for (int b = 0; b < p.boxes; ++b) {
+                if (!wait_bounded(box_bar(sm.emptyb0, stage, b), phase, w, true)) {
+                    report_timeout(w, 0, stage, phase);
+                    *w.abort = 1;
+                    ok = false;
+                    if (b > 0 && tile >= 0) {   // boxes 0 .. b-1 of this tile are in flight
+                        ++issued;
+                        last_boxes = b;
+                    }
+                    break;
+                }
+                info[stage * 8 + b].key = ckey;
+                info[stage * 8 + b].tm = static_cast<int32_t>(ctm);
+                info[stage * 8 + b].tn = static_cast<int32_t>(ctn);
+                const uint32_t full_bar = box_bar(sm.fullb0, stage, b);
+                if (tile < 0) {
+                    mbar_arrive(full_bar);
+                } else {
+                    mbar_arrive_expect_tx(full_bar, box_tx);
+                    tma_load_2d(dst + b * p.box_stride, map, x0 + b * p.box_inner, y, full_bar);
+                }
+            }
+            if (!ok) break;
+        } else {
+            info[stage * 8].key = ckey;
+            info[stage * 8].tm = static_cast<int32_t>(ctm);
+            info[stage * 8].tn = static_cast<int32_t>(ctn);
+            const uint32_t full_bar = sm.full0 + 8u * stage;
+            if (tile < 0) {
+                mbar_arrive(full_bar);
+            } else {
+                mbar_arrive_expect_tx(full_bar, p.tx_bytes);
+                for (int b = 0; b < p.boxes; ++b)
+                    tma_load_2d(dst + b * p.box_stride, map, x0 + b * p.box_inner, y, full_bar);
+            }
+        }
+        if (tile >= 0) {
+            log_record(p, 0, j, stage, phase, tile);
+            ++issued;
+        }
+        if (++stage == static_cast<uint32_t>(p.stages)) {
+            stage = 0;
+            phase ^= 1u;
+        }
+        if (tile < 0) break;
+    }
+    if (ok) {
+        // Tail: wait until the consumers have released every stage once more,
+        // so the CTA never exits with a stage still being read or filled.
+        for (int s = 0; s < p.stages && ok; ++s) {
+            const int nb = boxed ? p.boxes : 1;
+            for (int b = 0; b < nb; ++b) {
+                const uint32_t bar = boxed ? box_bar(sm.emptyb0, stage, b) : sm.empty0 + 8u * stage;
+                if (!wait_bounded(bar, phase, w, true)) {
+                    report_timeout(w, 0, stage, phase);
+                    *w.abort = 1;
+                    ok = false;
+                    break;
+                }
+            }
+            if (++stage == static_cast<uint32_t>(p.stages)) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        // Abort: wait (bounded) for the copies this CTA may still have in
+        // flight -- the last min(issued, S) tiles -- before leaving.  (Stages
+        // are used in order, the end mark after the last tile, so tile k went
+        // to stage k mod S.)
+        const int64_t from = issued > p.stages ? issued - p.stages : 0;
+        for (int64_t k = from; k < issued; ++k) {
+            const uint32_t s = static_cast<uint32_t>(k % p.stages);
+            const uint32_t par = static_cast<uint32_t>((k / p.stages) & 1);
+            if (boxed) {
+                const int nb = k == issued - 1 ? last_boxes : p.boxes;
+                for (int b = 0; b < nb; ++b) wait_bounded(box_bar(sm.fullb0, s, b), par, w, false);
+            } else {
+                wait_bounded(sm.full0 + 8u * s, par, w, false);
+            }
+        }
+    }
+}
+
 // `bars` holds 2 kMaxStages barriers, or 16 kMaxStages when `boxed`: then
 // each (stage, box) gets a full barrier (one arrival + the box's bytes) and an
 // empty barrier that the box's consumer warps -- consumer_warps / boxes of
@@ -525,9 +677,11 @@ __device__ __forceinline__ void store_partial_chunks(const PipeArgs &p, char *ds
 // at 16-byte granularity, so dst_map ends at the last whole 16-byte chunk of a
 // row (n_whole columns): a tile holding the partial chunk at column N has its
 // whole chunks stored in bulk and that chunk stored by the warp's lanes.
+// With `info` (the row-sum kernels' store warp) the tiles are those the
+// producer published per stage, up to its end mark; else first + j step, j < count.
 __device__ void consume_copy_bulk(const CUtensorMap *dst_map, const CopyArgs &a, const Smem &sm,
                                   const WaitCtl &w, int64_t first, int64_t step, int64_t count,
-                                  bool do_log = true) {
+                                  bool do_log = true, const volatile StageInfo *info = nullptr) {
     const PipeArgs &p = a.p;
     const int lane = threadIdx.x & 31;
     const int vec_elems = 16 / p.esize;
@@ -535,7 +689,7 @@ __device__ void consume_copy_bulk(const CUtensorMap *dst_map, const CopyArgs &a,
     const int64_t tile_n = static_cast<int64_t>(p.boxes) * p.box_inner;
     BulkStores bs;
     uint32_t stage = 0, phase = 0;
-    for (int64_t j = 0; j < count; ++j) {
+    for (int64_t j = 0; info != nullptr || j < count; ++j) {
         bool ok = wait_bounded(sm.full0 + 8u * stage, phase, w, true);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
@@ -545,11 +699,25 @@ __device__ void consume_copy_bulk(const CUtensorMap *dst_map, const CopyArgs &a,
             }
             break;
         }
-        const int64_t tile = first + j * step;
-        if (do_log && lane == 0) log_record(p, 1, j, stage, phase, tile);
-        const int64_t tm = tile / p.tiles_n;
+        int64_t tm, tn;
+        if (info != nullptr) {
+            if (info[stage * 8].key < 0) {   // end mark: release it after the stores in flight
+                if (lane == 0) {
+                    bs.release_pending(p, sm);
+                    if (p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+                }
+                break;
+            }
+            tm = info[stage * 8].tm;
+            tn = info[stage * 8].tn;
+        } else {
+            const int64_t tile = first + j * step;
+            tm = tile / p.tiles_n;
+            tn = tile - tm * p.tiles_n;
+        }
+        if (do_log && lane == 0) log_record(p, 1, j, stage, phase, tm * p.tiles_n + tn);
         const int64_t row0 = tm * p.tile_m;
-        const int64_t col0 = (tile - tm * p.tiles_n) * tile_n;
+        const int64_t col0 = tn * tile_n;
         if (col0 + tile_n > n_whole && n_whole != p.N) {
             store_partial_chunks(p, a.dst, a.ld_dst_bytes, sm.base + stage * p.stage_stride,
                                  row0, col0, n_whole, lane);
@@ -718,55 +886,193 @@ __device__ bool consumers_sync(FlushCtl &f, const WaitCtl &w) {
     return ok;
 }
 
-// Finish one band segment: combine the threads of each row, then either write
-// the row sums (sole contributor) or deposit the CTA's partials and let the
-// last contributing CTA add the partials of all contributors in CTA order.
-__device__ bool flush_band(const RowsumArgs &a, int64_t band, float acc, bool active,
+// Where a finished segment (a CTA's part of band `key`) goes: the band's K
+// contributors are the CTAs owning its units, this CTA's slot its rank among
+// them.
+struct FlushTarget {
+    int64_t band, K, slot;
+};
+
+__device__ __forceinline__ FlushTarget flush_target(const RowsumArgs &a, int64_t key) {
+    FlushTarget t;
+    const int64_t G = gridDim.x;
+    const int64_t x0 = key * a.p.tiles_n;
+    const int64_t b_first = unit_owner(x0, a.gran, a.units, G);
+    t.band = key;
+    t.K = unit_owner(x0 + a.p.tiles_n - 1, a.gran, a.units, G) - b_first + 1;
+    t.slot = blockIdx.x - b_first;
+    return t;
+}
+
+// Orders this thread's earlier memory accesses (and those it has synchronised
+// with) before its later ones at GPU scope: release before a ticket, acquire
+// after it.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// The band's K partial slots of one row, added in slot order; the loads are
+// issued B at a time so that their latencies overlap.  Leaves the slots
+// zero-filled (a workspace may next serve a shape whose tickets lie there).
+template <int B>
+__device__ __forceinline__ float combine_slots(float *base, int64_t K, int64_t stride) {
+    float total = 0.f;
+    for (int64_t k0 = 0; k0 < K; k0 += B) {
+        float v[B];
+#pragma unroll
+        for (int u = 0; u < B; ++u) v[u] = k0 + u < K ? __ldcg(base + (k0 + u) * stride) : 0.f;
+#pragma unroll
+        for (int u = 0; u < B; ++u)
+            if (k0 + u < K) total += v[u];
+    }
+    for (int64_t k = 0; k < K; ++k) base[k * stride] = 0.f;   // leave the workspace zero-filled
+    return total;
+}
+
+
+
+// Finish one segment: combine the threads of each row, then either write the
+// row sums (sole contributor) or deposit the partials in the segment's slot
+// and let the last contributor to arrive add the band's slots in slot order.
+__device__ bool flush_band(const RowsumArgs &a, int64_t key, float acc, bool active,
                            int row, int sub, int tpr, float *red, int *last_flag,
                            FlushCtl &f, const WaitCtl &w, int ctid) {
     const PipeArgs &p = a.p;
     red[ctid] = acc;
     if (!consumers_sync(f, w)) return false;
-    const int64_t G = gridDim.x;
-    const int64_t x0 = band * p.tiles_n;
-    const int64_t b_first = unit_owner(x0, a.gran, a.units, G);
-    const int64_t b_last = unit_owner(x0 + p.tiles_n - 1, a.gran, a.units, G);
-    const int64_t K = b_last - b_first + 1;
-    const int64_t grow = band * p.tile_m + row;
+    const FlushTarget ft = flush_target(a, key);
+    const int64_t grow = ft.band * p.tile_m + row;
     float v = 0.f;
     if (active && sub == 0) {
         v = red[row];
         for (int s = 1; s < tpr; ++s) v += red[row + s * p.tile_m];
     }
-    if (K == 1) {
+    if (ft.K == 1) {
         if (active && sub == 0 && grow < p.M) a.out[grow] = v;
         return consumers_sync(f, w);   // red[] may be rewritten after this
     }
-    float *slot = a.partial + (band * a.kmax + (blockIdx.x - b_first)) * p.tile_m;
+    float *slot = a.partial + (ft.band * a.kmax + ft.slot) * p.tile_m;
     if (active && sub == 0) {
         slot[row] = v;
-        __threadfence();
+        fence_acq_rel_gpu();
     }
     if (!consumers_sync(f, w)) return false;
     if (ctid == 0) {
-        const int old = atomicAdd(&a.ticket[band], 1);
-        *last_flag = (old == K - 1);
+        const int old = atomicAdd(&a.ticket[ft.band], 1);
+        *last_flag = (old == ft.K - 1);
     }
     if (!consumers_sync(f, w)) return false;
     if (*last_flag) {
-        __threadfence();
+        fence_acq_rel_gpu();
         if (active && sub == 0) {
-            float *base = a.partial + band * a.kmax * p.tile_m + row;
-            float total = 0.f;
-            for (int64_t k = 0; k < K; ++k) {
-                total += __ldcg(base + k * p.tile_m);
-                base[k * p.tile_m] = 0.f;   // leave the workspace zero-filled
-            }
+            const float total = combine_slots<4>(a.partial + ft.band * a.kmax * p.tile_m + row,
+                                                 ft.K, p.tile_m);
             if (grow < p.M) a.out[grow] = total;
         }
-        if (ctid == 0) a.ticket[band] = 0;
+        if (ctid == 0) a.ticket[ft.band] = 0;
     }
     return true;
+}
+
+// Flush ring of the row sum without the fused store warp: the consumers hand
+// each finished segment (the CTA's part of a band) -- one fp32 per
+// consumer thread and the segment's key -- to a flush warp through a ring of
+// shared-memory slots (full: all consumer warps arrived; empty: the flush
+// warp has read the slot), and go on with the next segment at once.  The
+// flush warp combines each row's threads in `sub` order and does the global
+// part (the row sums, or the segment's partials, the band's ticket and the
+// last contributor's ordered addition), so the global round trips of a
+// segment change no longer stall the pipeline.  Same arithmetic, same order
+// as flush_band.
+constexpr int kMaxConsumerThreads = 32 * kMaxConsumerWarps;
+constexpr int kFlushSlots = 2;   // segments the consumers may run ahead
+
+struct FlushRing {
+    uint32_t full0;    // full[slot] at + 8 slot, counts consumer warps
+    uint32_t empty0;   // empty[slot] at + 8 slot, counts the flush warp
+    uint32_t k;        // records posted (consumers) or taken (flush warp)
+    volatile int64_t *key;   // key[slot]: the segment's key, -1 = no more segments
+};
+
+__device__ __forceinline__ uint32_t ring_slot(uint32_t k) { return k % kFlushSlots; }
+__device__ __forceinline__ uint32_t ring_parity(uint32_t k) { return (k / kFlushSlots) & 1u; }
+
+// Post a segment (key >= 0, red: this thread's share) or the end (key < 0).
+__device__ bool flush_post(FlushRing &fr, float *red, float acc, int64_t key, int ctid,
+                           const WaitCtl &w) {
+    const uint32_t slot = ring_slot(fr.k);
+    bool ok = wait_bounded(fr.empty0 + 8u * slot, ring_parity(fr.k) ^ 1u, w, true);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) {
+        if ((threadIdx.x & 31) == 0) {
+            report_timeout(w, 1, kMaxStages + 1, slot);
+            *w.abort = 1;
+        }
+        return false;
+    }
+    red[slot * kMaxConsumerThreads + ctid] = acc;
+    if (ctid == 0) fr.key[slot] = key;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(fr.full0 + 8u * slot);
+    ++fr.k;
+    return true;
+}
+
+// The flush warp: takes the consumers' records in order until the end mark.
+// A band this CTA reduced alone gets its row sums written; otherwise the
+// CTA's partials go to its slot and the band's last contributor to arrive
+// adds the K slots in slot order (the order of flush_band).
+__device__ void flush_warp(const RowsumArgs &a, const float *red, FlushRing fr,
+                           const WaitCtl &w) {
+    const PipeArgs &p = a.p;
+    const int lane = threadIdx.x & 31;
+    const int tpr = p.consumer_warps * 32 / p.tile_m;
+    for (;;) {
+        const uint32_t slot = ring_slot(fr.k);
+        bool ok = wait_bounded(fr.full0 + 8u * slot, ring_parity(fr.k), w, true);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            if (lane == 0) {
+                report_timeout(w, 1, kMaxStages + 2, slot);
+                *w.abort = 1;
+            }
+            return;
+        }
+        const int64_t key = fr.key[slot];
+        if (key < 0) return;   // the consumers are done
+        const float *r = red + slot * kMaxConsumerThreads;
+        const FlushTarget ft = flush_target(a, key);
+        float *part = ft.K > 1 ? a.partial + (ft.band * a.kmax + ft.slot) * p.tile_m : nullptr;
+        for (int row = lane; row < p.tile_m; row += 32) {
+            float v = r[row];
+            for (int s = 1; s < tpr; ++s) v += r[row + s * p.tile_m];
+            const int64_t grow = ft.band * p.tile_m + row;
+            if (ft.K == 1) {
+                if (grow < p.M) a.out[grow] = v;
+            } else {
+                part[row] = v;
+            }
+        }
+        if (ft.K > 1) fence_acq_rel_gpu();   // partials visible before the ticket
+        __syncwarp();
+        if (lane == 0) mbar_arrive(fr.empty0 + 8u * slot);   // r[] is no longer read
+        ++fr.k;
+        if (ft.K == 1) continue;
+        int is_last = 0;
+        if (lane == 0) is_last = atomicAdd(&a.ticket[ft.band], 1) == ft.K - 1;
+        is_last = __shfl_sync(0xffffffffu, is_last, 0);
+        if (is_last) {
+            fence_acq_rel_gpu();   // the other contributors' partials, before reading them
+            for (int row = lane; row < p.tile_m; row += 32) {
+                const float total = combine_slots<8>(
+                    a.partial + ft.band * a.kmax * p.tile_m + row, ft.K, p.tile_m);
+                const int64_t grow = ft.band * p.tile_m + row;
+                if (grow < p.M) a.out[grow] = total;
+            }
+            __syncwarp();
+            if (lane == 0) a.ticket[ft.band] = 0;
+        }
+    }
 }
 
 // Row-sum consumer warps; the first of them is warp `cwarp0` of the CTA.
@@ -777,10 +1083,10 @@ __device__ bool flush_band(const RowsumArgs &a, int64_t band, float acc, bool ac
 // the per-box kernels give bit-identical sums.  With `boxed` (host-checked:
 // tpr a multiple of boxes, and the threads of one box whole warps) every warp
 // reads one box only, and waits for and releases that box alone.
-template <int DT, bool boxed>
+template <int DT, bool boxed, bool ring>
 __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCtl &w,
-                               int64_t first, int64_t count, float *red, int *last_flag,
-                               FlushCtl &f, int cwarp0) {
+                               const volatile StageInfo *info, float *red, int *last_flag,
+                               FlushCtl &f, FlushRing &fr, int cwarp0) {
     const PipeArgs &p = a.p;
     const int ctid = static_cast<int>(threadIdx.x) - 32 * cwarp0;
     const int lane = threadIdx.x & 31;
@@ -796,22 +1102,12 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
     const int rounds = (most + kVec - 1) / kVec;
     const int box = boxed ? (ctid / p.tile_m) / (tpr / p.boxes) : 0;
     float acc = 0.f;
-    int64_t band = -1;
+    int64_t key = -1;   // band being summed
     uint32_t stage = 0, phase = 0;
     bool ok = true;
-    for (int64_t j = 0; j < count; ++j) {
-        const int64_t tile = first + j;
-        const int64_t tb = tile / p.tiles_n;
-        if (tb != band) {
-            if (band >= 0 && !flush_band(a, band, acc, active, row, sub, tpr, red,
-                                         last_flag, f, w, ctid)) {
-                ok = false;
-                break;
-            }
-            band = tb;
-            acc = 0.f;
-        }
+    for (int64_t j = 0;; ++j) {
         const uint32_t full_bar = boxed ? box_bar(sm.fullb0, stage, box) : sm.full0 + 8u * stage;
+        const uint32_t empty_bar = boxed ? box_bar(sm.emptyb0, stage, box) : sm.empty0 + 8u * stage;
         bool got = wait_bounded(full_bar, phase, w, true);
         got = __all_sync(0xffffffffu, got);
         if (!got) {
@@ -822,25 +1118,44 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
             ok = false;
             break;
         }
-        if (ctid == 0) log_record(p, 1, j, stage, phase, tile);
+        const int64_t k = info[stage * 8 + box].key;
+        if (k < 0) {   // end mark: release its stage, no more tiles
+            __syncwarp();
+            if (lane == 0 && p.fault != 2) mbar_arrive(empty_bar);
+            break;
+        }
+        if (k != key) {
+            if (key >= 0 &&
+                !(ring ? flush_post(fr, red, acc, key, ctid, w)
+                       : flush_band(a, key, acc, active, row, sub, tpr, red, last_flag, f, w,
+                                    ctid))) {
+                ok = false;
+                break;
+            }
+            key = k;
+            acc = 0.f;
+        }
+        if (ctid == 0 && p.log != nullptr)
+            log_record(p, 1, j, stage, phase,
+                       static_cast<int64_t>(info[stage * 8 + box].tm) * p.tiles_n +
+                           info[stage * 8 + box].tn);
         const uint32_t rbase = sm.base + stage * p.stage_stride;
         float tsum = 0.f;
         for (int r = 0; r < rounds; ++r) {
             uint4 v[kVec];
 #pragma unroll
             for (int u = 0; u < kVec; ++u) {
-                const int k = r * kVec + u;
-                if (k < mine) v[u] = lds128(rbase + chunk_offset(row, lo + k, p.box_stride));
+                const int c = r * kVec + u;
+                if (c < mine) v[u] = lds128(rbase + chunk_offset(row, lo + c, p.box_stride));
             }
             if (r == rounds - 1) {
                 __syncwarp();
-                if (lane == 0 && p.fault != 2)
-                    mbar_arrive(boxed ? box_bar(sm.emptyb0, stage, box) : sm.empty0 + 8u * stage);
+                if (lane == 0 && p.fault != 2) mbar_arrive(empty_bar);
             }
 #pragma unroll
             for (int u = 0; u < kVec; ++u) {
-                const int k = r * kVec + u;
-                if (k < mine) tsum += chunk_sum<DT>(v[u]);
+                const int c = r * kVec + u;
+                if (c < mine) tsum += chunk_sum<DT>(v[u]);
             }
         }
         acc += tsum;
@@ -849,31 +1164,50 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
             phase ^= 1u;
         }
     }
-    if (ok && band >= 0)
-        flush_band(a, band, acc, active, row, sub, tpr, red, last_flag, f, w, ctid);
+    if (!ok) return;
+    if (key >= 0) {
+        if (ring)
+            ok = flush_post(fr, red, acc, key, ctid, w);
+        else
+            flush_band(a, key, acc, active, row, sub, tpr, red, last_flag, f, w, ctid);
+    }
+    if (ring && ok) flush_post(fr, red, 0.f, -1, ctid, w);   // end mark for the flush warp
 }
 
 // FUSED: warp 1 writes every landed stage to dst (bulk tensor stores; LSU
 // stores for tiles with a partial 16-byte chunk at column N) and is the one
-// extra arrival on each empty barrier; the row-sum warps follow it.
+// extra arrival on each empty barrier; the row-sum warps follow it.  Without
+// it, warp 1 is the flush warp (see flush_warp).
 // BOXED: a full/empty pair per (stage, box) (never with FUSED).  Each barrier
 // layout is its own instantiation, so neither carries the other's code.
 template <int DT, bool FUSED, bool BOXED>
-__global__ void __launch_bounds__(FUSED ? kMaxThreads + 32 : kMaxThreads, 2)
+__global__ void __launch_bounds__(kMaxThreads + 32, 2)
     mbt_rowsum_kernel(const __grid_constant__ CUtensorMap map,
                       const __grid_constant__ CUtensorMap dst_map, const RowsumArgs a) {
     extern __shared__ __align__(1024) unsigned char dyn_smem[];
     // Per-box barrier pairs only without the store warp (which reads whole stages).
     static_assert(!(FUSED && BOXED), "the store warp reads whole stages");
+    constexpr bool ring = !FUSED;
     __shared__ __align__(8) uint64_t bars[BOXED ? 16 * kMaxStages : 2 * kMaxStages];
     __shared__ __align__(8) uint64_t flush_bar;
-    __shared__ float red[kMaxThreads];      // indexed by row-sum consumer thread
+    __shared__ __align__(8) uint64_t ring_bars[2 * kFlushSlots];   // flush ring: full, empty
+    // By row-sum consumer thread (one block per flush-ring slot without FUSED).
+    __shared__ float red[ring ? kFlushSlots * kMaxConsumerThreads : kMaxConsumerThreads];
     __shared__ int abort_flag;
     __shared__ int last_flag;
+    __shared__ StageInfo info[8 * kMaxStages];   // per (stage, box), from the producer
+    __shared__ int64_t ring_key[kFlushSlots];
     Smem sm;
     constexpr bool boxed = BOXED;
+    FlushRing fr{smem_u32(&ring_bars[0]), smem_u32(&ring_bars[kFlushSlots]), 0u, ring_key};
+    if (ring && threadIdx.x == 0) {
+        for (int k = 0; k < kFlushSlots; ++k) {
+            mbar_init(fr.full0 + 8u * k, static_cast<uint32_t>(a.p.consumer_warps));
+            mbar_init(fr.empty0 + 8u * k, 1);
+        }
+    }
     init_pipeline(a.p, sm, bars, &abort_flag, &flush_bar,
-                  static_cast<uint32_t>(a.p.consumer_warps), dyn_smem, boxed);
+                  static_cast<uint32_t>(a.p.consumer_warps), dyn_smem, boxed);   // fences the inits
     WaitCtl w{a.p.wait_budget_ns, &abort_flag, status_of(a.p)};
     // Contiguous, evenly split range of scheduling units, in band-major order.
     const int64_t G = gridDim.x;
@@ -881,22 +1215,24 @@ __global__ void __launch_bounds__(FUSED ? kMaxThreads + 32 : kMaxThreads, 2)
     const int64_t first = (b * a.units / G) * a.gran;
     const int64_t last = ((b + 1) * a.units / G) * a.gran;
     if (threadIdx.x < 32) {
-        if (threadIdx.x == 0) produce<boxed>(&map, a.p, sm, w, first, 1, last - first);
+        if (threadIdx.x == 0) produce_rows<boxed>(&map, a, sm, w, first, last, info);
         return;
     }
-    if constexpr (FUSED) {
-        if (threadIdx.x < 64) {
+    if (threadIdx.x < 64) {
+        if constexpr (FUSED) {
             CopyArgs c{};
             c.p = a.p;
             c.dst = a.dst;
             c.ld_dst_bytes = a.ld_dst_bytes;
             c.store_mode = 1;
-            consume_copy_bulk(&dst_map, c, sm, w, first, 1, last - first, false);
-            return;
+            consume_copy_bulk(&dst_map, c, sm, w, 0, 0, 0, false, info);
+        } else {
+            flush_warp(a, red, fr, w);
         }
+        return;
     }
     FlushCtl f{smem_u32(&flush_bar), 0u};
-    consume_rowsum<DT, boxed>(a, sm, w, first, last - first, red, &last_flag, f, FUSED ? 2 : 1);
+    consume_rowsum<DT, boxed, ring>(a, sm, w, info, red, &last_flag, f, fr, 2);
 }
 
 __global__ void mbt_accumulate_kernel(float *acc, const float *part, int64_t n, int first) {

@@ -248,6 +248,18 @@ def test_plan_fused_adds_a_store_warp():
     assert p["grid"] == 304 and p["consumer_warps"] == 8 and p["threads"] == 32 * 10
 
 
+def test_plan_tiled_rowsum_adds_a_flush_warp():
+    """The tiled row sum runs a producer warp, a flush warp and the consumer
+    warps; the flat row sum has no flush warp."""
+    p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16, fit=2, ws=True)
+    assert p["consumer_warps"] == 8 and p["threads"] == 32 * 10
+    p = _plan(mbt.OP_ROWSUM, 24577, 16383, 128, 64, 3, torch.float16, fit=4, ws=True,
+              ld_src=16384)
+    assert p["threads"] == 32 * (2 + p["consumer_warps"])
+    f = _plan(mbt.OP_ROWSUM, 1000, 63, 128, 64, 2, torch.float16, fit=4)
+    assert f["flat"] == 1 and f["threads"] == 32 * (1 + f["consumer_warps"])
+
+
 def test_plan_store_mode_default_follows_the_row_end():
     """0 picks bulk stores where rows end inside a 16-byte chunk, LSU stores
     otherwise (and always LSU with the unified pipeline)."""
