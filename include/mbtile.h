@@ -173,10 +173,11 @@ typedef struct mbt_plan {
     int32_t grid;            /* CTAs launched */
     int32_t threads;         /* threads per CTA = 32 x (1 + consumer_warps),
                                 plus one warp for the fused operation's
-                                stores or the tiled row sum's flush warp
-                                (which finishes each band's row sums while the
-                                consumers go on); none without a producer
-                                warp (unified copy) */
+                                stores, or the flush warp of the tiled row
+                                sum and of the column sum (which finishes each
+                                band's / strip's sums while the consumers go
+                                on); none without a producer warp (unified
+                                copy) */
     int32_t consumer_warps;
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t boxes;           /* 128-byte boxes per tile row */

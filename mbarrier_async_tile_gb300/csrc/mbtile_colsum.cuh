@@ -52,92 +52,144 @@ __device__ __forceinline__ void chunk_accumulate(float *acc, const uint4 &v) {
     }
 }
 
-// Finish this CTA's share of one strip: add the tpc partials of each column
-// in g order, then write out (sole contributor) or deposit the CTA's partials
-// and let the last contributing CTA add those of all contributors in CTA
-// order.  pos_first / pos_last: order positions of the strip's first and last
-// tile; the contributors are the CTAs owning them and every CTA in between.
-template <int EPC>
-__device__ __forceinline__ bool flush_strip(const ColsumArgs &a, int64_t strip, int64_t pos_first,
-                            int64_t pos_last, const float *acc, bool active, int q, int g,
-                            int tpc, float *red, int *last_flag, FlushCtl &f, const WaitCtl &w,
-                            int ctid, int nthr) {
-    const PipeArgs &p = a.p;
+// Flush ring of the column sum: when a CTA leaves a group, its consumers add
+// the tpc partials of each column in g order (through red[]) and hand the
+// per-column sums of the group's strips -- with the group as key -- to the
+// flush warp, which does the global part: the column sums (sole contributor),
+// or the CTA's partials, fence, ticket, and for the last contributor the
+// addition of all contributors' partials in CTA order.  The consumers go on
+// at once.  (Measured on the row sum, whose flush works the same way: the
+// fence and ticket round trips of a band change had stalled the consumers of
+// the CTAs crossing one by ~3 us.)
+constexpr int kColsumSlotFloats = 512;   // group strips x tile_n, at most
+
+template <int EPC, int GMAX>
+__device__ bool post_group(const ColsumArgs &a, int64_t gstart, float (*acc)[EPC], bool active,
+                           int q, int g, int tpc, float *red, float *ring_data, FlushCtl &f,
+                           FlushRing &fr, const WaitCtl &w, int ctid, int nthr) {
     const int tn = a.tile_n;
-    const int64_t G = gridDim.x;
-    const int64_t b_first = unit_owner(pos_first, a.gran, a.units, G);
-    const int64_t b_last = unit_owner(pos_last, a.gran, a.units, G);
-    if (static_cast<int64_t>(blockIdx.x) < b_first || static_cast<int64_t>(blockIdx.x) > b_last)
-        return true;   // not a contributor of this strip
-    if (active) {
+    const uint32_t slot = ring_slot(fr.k);
+    bool ok = wait_bounded(fr.empty0 + 8u * slot, ring_parity(fr.k) ^ 1u, w, true);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) {
+        if ((threadIdx.x & 31) == 0) {
+            report_timeout(w, 1, kMaxStages + 1, slot);
+            *w.abort = 1;
+        }
+        return false;
+    }
+    float *data = ring_data + slot * kColsumSlotFloats;
+    if (gstart >= 0) {
+        const ColPos c0 = col_pos(gstart, a.p.tiles_m, a.p.tiles_n, GMAX);
 #pragma unroll
-        for (int e = 0; e < EPC; ++e) red[g * tn + q * EPC + e] = acc[e];
-    }
-    if (!consumers_sync(f, w)) return false;
-    const int64_t K = b_last - b_first + 1;
-    const int64_t col0 = strip * tn;
-    float *slot = a.partial + (strip * a.kmax + (blockIdx.x - b_first)) * tn;
-    for (int c = ctid; c < tn; c += nthr) {
-        float v = red[c];
-        for (int s = 1; s < tpc; ++s) v += red[s * tn + c];
-        if (K == 1) {
-            if (col0 + c < p.N) a.out[col0 + c] = v;
-        } else {
-            slot[c] = v;
-        }
-    }
-    if (K == 1) return consumers_sync(f, w);   // red[] may be rewritten after this
-    __threadfence();
-    if (!consumers_sync(f, w)) return false;
-    if (ctid == 0) {
-        const int old = atomicAdd(&a.ticket[strip], 1);
-        *last_flag = (old == K - 1);
-    }
-    if (!consumers_sync(f, w)) return false;
-    if (*last_flag) {
-        __threadfence();
-        float *base = a.partial + strip * a.kmax * tn;
-        for (int c = ctid; c < tn; c += nthr) {
-            float total = 0.f;
-            for (int64_t k = 0; k < K; ++k) {
-                total += __ldcg(base + k * tn + c);
-                base[k * tn + c] = 0.f;   // leave the workspace zero-filled
+        for (int k = 0; k < GMAX; ++k) {
+            if (k >= c0.wg) break;
+            if (active) {
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) red[g * tn + q * EPC + e] = acc[k][e];
             }
-            if (col0 + c < p.N) a.out[col0 + c] = total;
+            if (!consumers_sync(f, w)) return false;
+            for (int c = ctid; c < tn; c += nthr) {
+                float v = red[c];
+                for (int s = 1; s < tpc; ++s) v += red[s * tn + c];
+                data[k * tn + c] = v;
+            }
+            if (!consumers_sync(f, w)) return false;   // red[] may be rewritten after this
         }
-        if (ctid == 0) a.ticket[strip] = 0;
     }
+    if (ctid == 0) fr.key[slot] = gstart;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(fr.full0 + 8u * slot);
+    ++fr.k;
     return true;
 }
 
-// Flush every strip of the group that starts at order position gstart.
-template <int EPC, int GMAX>
-__device__ __forceinline__ bool flush_group(const ColsumArgs &a, int64_t gstart, float (*acc)[EPC],
-                            bool active, int q, int g, int tpc, float *red, int *last_flag,
-                            FlushCtl &f, const WaitCtl &w, int ctid, int nthr) {
+// The column sum's flush warp: takes the consumers' records in order until
+// the end mark (key -1).
+template <int GMAX>
+__device__ void colsum_flush_warp(const ColsumArgs &a, const float *ring_data, FlushRing fr,
+                                  const WaitCtl &w) {
     const PipeArgs &p = a.p;
-    const ColPos c0 = col_pos(gstart, p.tiles_m, p.tiles_n, GMAX);
+    const int lane = threadIdx.x & 31;
+    const int tn = a.tile_n;
+    const int64_t G = gridDim.x;
+    for (;;) {
+        const uint32_t slot = ring_slot(fr.k);
+        bool ok = wait_bounded(fr.full0 + 8u * slot, ring_parity(fr.k), w, true);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            if (lane == 0) {
+                report_timeout(w, 1, kMaxStages + 2, slot);
+                *w.abort = 1;
+            }
+            return;
+        }
+        const int64_t gstart = fr.key[slot];
+        if (gstart < 0) return;   // the consumers are done
+        const float *data = ring_data + slot * kColsumSlotFloats;
+        const ColPos c0 = col_pos(gstart, p.tiles_m, p.tiles_n, GMAX);
+        int64_t strip_k[GMAX], K_k[GMAX];
+        bool any_split = false;
 #pragma unroll
-    for (int k = 0; k < GMAX; ++k) {
-        if (k >= c0.wg) break;
-        const int64_t first = gstart + k;
-        const int64_t last = gstart + (p.tiles_m - 1) * c0.wg + k;
-        if (!flush_strip<EPC>(a, col_strip(c0, GMAX) + k, first, last, acc[k], active,
-                              q, g, tpc, red,
-                              last_flag, f, w, ctid, nthr))
-            return false;
+        for (int k = 0; k < GMAX; ++k) {
+            K_k[k] = 0;
+            if (k >= c0.wg) continue;
+            const int64_t pos_first = gstart + k;
+            const int64_t pos_last = gstart + (p.tiles_m - 1) * c0.wg + k;
+            const int64_t b_first = unit_owner(pos_first, a.gran, a.units, G);
+            const int64_t b_last = unit_owner(pos_last, a.gran, a.units, G);
+            if (static_cast<int64_t>(blockIdx.x) < b_first ||
+                static_cast<int64_t>(blockIdx.x) > b_last)
+                continue;   // not a contributor of this strip
+            const int64_t strip = col_strip(c0, GMAX) + k;
+            const int64_t K = b_last - b_first + 1;
+            strip_k[k] = strip;
+            K_k[k] = K;
+            const int64_t col0 = strip * tn;
+            float *part = a.partial + (strip * a.kmax + (blockIdx.x - b_first)) * tn;
+            for (int c = lane; c < tn; c += 32) {
+                const float v = data[k * tn + c];
+                if (K == 1) {
+                    if (col0 + c < p.N) a.out[col0 + c] = v;
+                } else {
+                    part[c] = v;
+                }
+            }
+            any_split |= K > 1;
+        }
+        if (any_split) fence_acq_rel_gpu();   // partials visible before the tickets
+        __syncwarp();
+        if (lane == 0) mbar_arrive(fr.empty0 + 8u * slot);   // data[] is no longer read
+        ++fr.k;
+#pragma unroll
+        for (int k = 0; k < GMAX; ++k) {
+            if (K_k[k] <= 1) continue;
+            const int64_t strip = strip_k[k], K = K_k[k];
+            int is_last = 0;
+            if (lane == 0) is_last = atomicAdd(&a.ticket[strip], 1) == K - 1;
+            is_last = __shfl_sync(0xffffffffu, is_last, 0);
+            if (!is_last) continue;
+            fence_acq_rel_gpu();   // the other contributors' partials, before reading them
+            float *base = a.partial + strip * a.kmax * tn;
+            const int64_t col0 = strip * tn;
+            for (int c = lane; c < tn; c += 32) {
+                const float total = combine_slots<8>(base + c, K, tn);
+                if (col0 + c < p.N) a.out[col0 + c] = total;
+            }
+            __syncwarp();
+            if (lane == 0) a.ticket[strip] = 0;
+        }
     }
-    return true;
 }
 
 // GMAX: strips per group (= p.col_group; the launch picks the instantiation).
 template <int DT, int GMAX>
 __device__ void consume_colsum(const ColsumArgs &a, const Smem &sm, const WaitCtl &w,
-                               int64_t first, int64_t count, float *red, int *last_flag,
-                               FlushCtl &f) {
+                               int64_t first, int64_t count, float *red, float *ring_data,
+                               FlushCtl &f, FlushRing &fr) {
     constexpr int EPC = DT == MBT_F32 ? 4 : 8;
     const PipeArgs &p = a.p;
-    const int ctid = static_cast<int>(threadIdx.x) - 32;
+    const int ctid = static_cast<int>(threadIdx.x) - 64;   // warp 0 produces, warp 1 flushes
     const int lane = threadIdx.x & 31;
     const int nthr = p.consumer_warps * 32;
     const int cpr = p.boxes * 8;
@@ -163,8 +215,8 @@ __device__ void consume_colsum(const ColsumArgs &a, const Smem &sm, const WaitCt
     for (int64_t j = 0; j < count; ++j, col_next(c, p.tiles_m, p.tiles_n, GMAX)) {
         const int64_t tile = first + j;
         if (c.gstart != group) {
-            if (group >= 0 && !flush_group<EPC, GMAX>(a, group, acc, active, q, g, tpc, red,
-                                                      last_flag, f, w, ctid, nthr)) {
+            if (group >= 0 && !post_group<EPC, GMAX>(a, group, acc, active, q, g, tpc, red,
+                                                     ring_data, f, fr, w, ctid, nthr)) {
                 ok = false;
                 break;
             }
@@ -221,21 +273,34 @@ __device__ void consume_colsum(const ColsumArgs &a, const Smem &sm, const WaitCt
         }
     }
     if (ok && group >= 0)
-        flush_group<EPC, GMAX>(a, group, acc, active, q, g, tpc, red, last_flag, f, w, ctid, nthr);
+        ok = post_group<EPC, GMAX>(a, group, acc, active, q, g, tpc, red, ring_data, f, fr, w,
+                                   ctid, nthr);
+    if (ok)   // the end mark for the flush warp
+        post_group<EPC, GMAX>(a, -1, acc, active, q, g, tpc, red, ring_data, f, fr, w, ctid,
+                              nthr);
 }
 
 template <int DT, int GMAX>
-__global__ void __launch_bounds__(kMaxThreads, 2)
+__global__ void __launch_bounds__(kMaxThreads + 32, 2)
     mbt_colsum_kernel(const __grid_constant__ CUtensorMap map, const ColsumArgs a) {
     extern __shared__ __align__(1024) unsigned char dyn_smem[];
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
     __shared__ __align__(8) uint64_t flush_bar;
+    __shared__ __align__(8) uint64_t ring_bars[2 * kFlushSlots];   // flush ring: full, empty
     __shared__ float red[kColsumRedFloats];   // [tpc][tile_n] partial column sums
+    __shared__ float ring_data[kFlushSlots * kColsumSlotFloats];
+    __shared__ int64_t ring_key[kFlushSlots];
     __shared__ int abort_flag;
-    __shared__ int last_flag;
     Smem sm;
+    FlushRing fr{smem_u32(&ring_bars[0]), smem_u32(&ring_bars[kFlushSlots]), 0u, ring_key};
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < kFlushSlots; ++k) {
+            mbar_init(fr.full0 + 8u * k, static_cast<uint32_t>(a.p.consumer_warps));
+            mbar_init(fr.empty0 + 8u * k, 1);
+        }
+    }
     init_pipeline(a.p, sm, bars, &abort_flag, &flush_bar,
-                  static_cast<uint32_t>(a.p.consumer_warps), dyn_smem);
+                  static_cast<uint32_t>(a.p.consumer_warps), dyn_smem);   // fences the inits
     WaitCtl w{a.p.wait_budget_ns, &abort_flag, status_of(a.p)};
     // Contiguous, evenly split range of scheduling units, in strip-major order.
     const int64_t G = gridDim.x;
@@ -246,6 +311,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
         if (threadIdx.x == 0) produce(&map, a.p, sm, w, first, 1, last - first);
         return;
     }
+    if (threadIdx.x < 64) {
+        colsum_flush_warp<GMAX>(a, ring_data, fr, w);
+        return;
+    }
     FlushCtl f{smem_u32(&flush_bar), 0u};
-    consume_colsum<DT, GMAX>(a, sm, w, first, last - first, red, &last_flag, f);
+    consume_colsum<DT, GMAX>(a, sm, w, first, last - first, red, ring_data, f, fr);
 }

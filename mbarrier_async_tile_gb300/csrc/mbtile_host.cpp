@@ -340,8 +340,10 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     }
     plan->consumer_warps = W;
     // producer warp + consumer warps (+ the fused operation's store warp, or
-    // the tiled row sum's flush warp); the unified pipeline has no producer warp
-    const bool second_warp = op == MBT_OP_COPY_ROWSUM || (op == MBT_OP_ROWSUM && !flat);
+    // the flush warp of the tiled row sum and the column sum); the unified
+    // pipeline has no producer warp
+    const bool second_warp = op == MBT_OP_COPY_ROWSUM || op == MBT_OP_COLSUM ||
+                             (op == MBT_OP_ROWSUM && !flat);
     plan->threads = 32 * ((o.pipeline == 1 ? 0 : 1) + W + (second_warp ? 1 : 0));
     plan->tx_bytes = plan->boxes * tile_m * mbt::kBoxRowBytes;
     const int64_t smem = static_cast<int64_t>(stages) * plan->stage_bytes + mbt::kSwizzleAtomBytes;
