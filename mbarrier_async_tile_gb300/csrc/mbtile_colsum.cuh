@@ -170,12 +170,9 @@ __device__ void colsum_flush_warp(const ColsumArgs &a, const float *ring_data, F
             is_last = __shfl_sync(0xffffffffu, is_last, 0);
             if (!is_last) continue;
             fence_acq_rel_gpu();   // the other contributors' partials, before reading them
-            float *base = a.partial + strip * a.kmax * tn;
             const int64_t col0 = strip * tn;
-            for (int c = lane; c < tn; c += 32) {
-                const float total = combine_slots<8>(base + c, K, tn);
-                if (col0 + c < p.N) a.out[col0 + c] = total;
-            }
+            warp_add_slots<16, 2>(a.partial + strip * a.kmax * tn, K, tn, tn, a.out + col0,
+                                  p.N - col0);
             __syncwarp();
             if (lane == 0) a.ticket[strip] = 0;
         }

@@ -907,6 +907,44 @@ __device__ __forceinline__ FlushTarget flush_target(const RowsumArgs &a, int64_t
     return t;
 }
 
+// One warp adds K partial slots (`stride` floats apart) for the entries
+// lane, lane + 32, ... < n: per entry in slot order, as combine_slots does,
+// so the same bits; writes dst[c] for c < valid and leaves the slots zero.
+// Each lane's entries (at most PL) and B slots are loaded together, so the
+// addition takes about K / B load round trips instead of one per entry.
+template <int PL, int B>
+__device__ __forceinline__ void warp_add_slots(float *base, int64_t K, int64_t stride, int n,
+                                               float *dst, int64_t valid) {
+    const int lane = threadIdx.x & 31;
+    float acc[PL];
+#pragma unroll
+    for (int i = 0; i < PL; ++i) acc[i] = 0.f;
+    for (int64_t k0 = 0; k0 < K; k0 += B) {
+        float v[B][PL];
+#pragma unroll
+        for (int u = 0; u < B; ++u)
+#pragma unroll
+            for (int i = 0; i < PL; ++i) {
+                const int c = lane + 32 * i;
+                v[u][i] = k0 + u < K && c < n ? __ldcg(base + (k0 + u) * stride + c) : 0.f;
+            }
+#pragma unroll
+        for (int u = 0; u < B; ++u)
+#pragma unroll
+            for (int i = 0; i < PL; ++i)
+                if (k0 + u < K && lane + 32 * i < n) acc[i] += v[u][i];
+    }
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+        const int c = lane + 32 * i;
+        if (c < n && c < valid) dst[c] = acc[i];
+    }
+    for (int64_t k = 0; k < K; ++k)
+#pragma unroll
+        for (int i = 0; i < PL; ++i)
+            if (lane + 32 * i < n) base[k * stride + lane + 32 * i] = 0.f;
+}
+
 // Orders this thread's earlier memory accesses (and those it has synchronised
 // with) before its later ones at GPU scope: release before a ticket, acquire
 // after it.
@@ -1066,12 +1104,9 @@ __device__ void flush_warp(const RowsumArgs &a, const float *red, FlushRing fr,
         is_last = __shfl_sync(0xffffffffu, is_last, 0);
         if (is_last) {
             fence_acq_rel_gpu();   // the other contributors' partials, before reading them
-            for (int row = lane; row < p.tile_m; row += 32) {
-                const float total = combine_slots<8>(
-                    a.partial + ft.band * a.kmax * p.tile_m + row, ft.K, p.tile_m);
-                const int64_t grow = ft.band * p.tile_m + row;
-                if (grow < p.M) a.out[grow] = total;
-            }
+            warp_add_slots<8, 4>(a.partial + ft.band * a.kmax * p.tile_m, ft.K, p.tile_m,
+                                 p.tile_m, a.out + ft.band * p.tile_m,
+                                 p.M - ft.band * p.tile_m);
             __syncwarp();
             if (lane == 0) a.ticket[ft.band] = 0;
         }
