@@ -231,27 +231,23 @@ __device__ __forceinline__ uint32_t box_bar(uint32_t base, uint32_t stage, int b
     return base + 8u * (stage * 8u + static_cast<uint32_t>(box));
 }
 
-// Producer: one elected lane.  Loads `count` tiles, tile j being
-// first + j * step in row-major tile order, then drains (producer tail).
-// With `boxed`, every box of a stage has its own full/empty barrier pair: the
-// producer refills box b as soon as box b's consumers have released it.
-template <bool boxed = false>
+// Producer of the copy and column-sum kernels: one elected lane.  Loads
+// `count` tiles, tile j being first + j * step in row-major tile order (or,
+// with p.col_group, in strip-group order), then drains (producer tail).
 __device__ void produce(const CUtensorMap *map, const PipeArgs &p, const Smem &sm,
                         const WaitCtl &w, int64_t first, int64_t step, int64_t count) {
     uint32_t stage = 0;
     uint32_t phase = (p.fault == 1) ? 0u : 1u;  // free buffers: start at phase 1
     int64_t issued = 0;
-    int last_boxes = p.boxes;   // boxes issued of tile issued - 1
     bool ok = true;
-    const uint32_t box_tx = p.tx_bytes / static_cast<uint32_t>(p.boxes);
     for (int64_t j = 0; j < count; ++j) {
-        // Stage-wide pairs: wait for the stage first, then work out the tile
-        // (measured: this order kept the 3-stage row sum 1.3% faster than
-        // computing the coordinates ahead of the wait, and the 3-stage column
-        // sum 3% faster than stepping its strip-group position incrementally
-        // after the wait -- a short gap between a stage's release and its
-        // next copy helps, though the incremental step does less work).
-        if (!boxed && !wait_bounded(sm.empty0 + 8u * stage, phase, w, true)) {
+        // Wait for the stage first, then work out the tile (measured: this
+        // order kept the 3-stage row sum 1.3% faster than computing the
+        // coordinates ahead of the wait, and the 3-stage column sum 3% faster
+        // than stepping its strip-group position incrementally after the wait
+        // -- a short gap between a stage's release and its next copy helps,
+        // though the incremental step does less work).
+        if (!wait_bounded(sm.empty0 + 8u * stage, phase, w, true)) {
             report_timeout(w, 0, stage, phase);
             *w.abort = 1;
             ok = false;
@@ -270,29 +266,10 @@ __device__ void produce(const CUtensorMap *map, const PipeArgs &p, const Smem &s
         const int32_t y = static_cast<int32_t>(tm * p.tile_m);
         const int32_t x0 = static_cast<int32_t>(tn * p.boxes * p.box_inner);
         const uint32_t dst = sm.base + stage * p.stage_stride;
-        if (boxed) {
-            for (int b = 0; b < p.boxes; ++b) {
-                if (!wait_bounded(box_bar(sm.emptyb0, stage, b), phase, w, true)) {
-                    report_timeout(w, 0, stage, phase);
-                    *w.abort = 1;
-                    ok = false;
-                    if (b > 0) {   // boxes 0 .. b-1 of this tile are in flight
-                        ++issued;
-                        last_boxes = b;
-                    }
-                    break;
-                }
-                const uint32_t full_bar = box_bar(sm.fullb0, stage, b);
-                mbar_arrive_expect_tx(full_bar, box_tx);
-                tma_load_2d(dst + b * p.box_stride, map, x0 + b * p.box_inner, y, full_bar);
-            }
-            if (!ok) break;
-        } else {
-            const uint32_t full_bar = sm.full0 + 8u * stage;
-            mbar_arrive_expect_tx(full_bar, p.tx_bytes);
-            for (int b = 0; b < p.boxes; ++b)
-                tma_load_2d(dst + b * p.box_stride, map, x0 + b * p.box_inner, y, full_bar);
-        }
+        const uint32_t full_bar = sm.full0 + 8u * stage;
+        mbar_arrive_expect_tx(full_bar, p.tx_bytes);
+        for (int b = 0; b < p.boxes; ++b)
+            tma_load_2d(dst + b * p.box_stride, map, x0 + b * p.box_inner, y, full_bar);
         log_record(p, 0, j, stage, phase, tile);
         ++issued;
         if (++stage == static_cast<uint32_t>(p.stages)) {
@@ -303,16 +280,12 @@ __device__ void produce(const CUtensorMap *map, const PipeArgs &p, const Smem &s
     if (ok) {
         // Tail: wait until the consumers have released every stage once more,
         // so the CTA never exits with a stage still being read or filled.
-        for (int s = 0; s < p.stages && ok; ++s) {
-            const int nb = boxed ? p.boxes : 1;
-            for (int b = 0; b < nb; ++b) {
-                const uint32_t bar = boxed ? box_bar(sm.emptyb0, stage, b) : sm.empty0 + 8u * stage;
-                if (!wait_bounded(bar, phase, w, true)) {
-                    report_timeout(w, 0, stage, phase);
-                    *w.abort = 1;
-                    ok = false;
-                    break;
-                }
+        for (int s = 0; s < p.stages; ++s) {
+            if (!wait_bounded(sm.empty0 + 8u * stage, phase, w, true)) {
+                report_timeout(w, 0, stage, phase);
+                *w.abort = 1;
+                ok = false;
+                break;
             }
             if (++stage == static_cast<uint32_t>(p.stages)) {
                 stage = 0;
@@ -327,12 +300,7 @@ __device__ void produce(const CUtensorMap *map, const PipeArgs &p, const Smem &s
         for (int64_t t = from; t < issued; ++t) {
             const uint32_t s = static_cast<uint32_t>(t % p.stages);
             const uint32_t par = static_cast<uint32_t>((t / p.stages) & 1);
-            if (boxed) {
-                const int nb = t == issued - 1 ? last_boxes : p.boxes;
-                for (int b = 0; b < nb; ++b) wait_bounded(box_bar(sm.fullb0, s, b), par, w, false);
-            } else {
-                wait_bounded(sm.full0 + 8u * s, par, w, false);
-            }
+            wait_bounded(sm.full0 + 8u * s, par, w, false);
         }
     }
 }
