@@ -641,8 +641,8 @@ def bench_only(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     c = ROWSUM if args.only in ("rowsum", "colsum") else COPY
-    rows = min(args.rows or c["M"], c["M"])
-    cols = c["N"] - args.trim_cols
+    rows = args.rows or c["M"]
+    cols = args.cols or c["N"] - args.trim_cols
     x = synthetic.make_matrix(rows, cols, c["dtype"], c["dist"], c["seed"], draw_on=str(dev))
     if args.only == "copy_rowsum":
         y = torch.empty_like(x)
@@ -958,6 +958,9 @@ def main(argv=None):
                          "whose rows are not a multiple of 16 bytes: the 1-D bulk-copy path)")
     ap.add_argument("--store-mode", type=int, default=0, choices=[0, 1, 2])
     ap.add_argument("--rows", type=int, default=0)
+    ap.add_argument("--cols", type=int, default=0,
+                    help="--only: columns of the matrix (dense rows; a pitch that is not a "
+                         "multiple of 16 bytes takes the 1-D bulk-copy kernels)")
     ap.add_argument("--consumer-warps", type=int, default=0)
     ap.add_argument("--ctas-per-sm", type=int, default=0)
     ap.add_argument("--sweep-stages", type=int, nargs="*", default=[1, 2, 3, 4, 6])

@@ -240,6 +240,27 @@ __device__ __forceinline__ uint32_t element_bits(const unsigned char *p) {
         return *reinterpret_cast<const uint16_t *>(p);
 }
 
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+// Sum of the elements of the 4-byte word `u` (at window byte offset wb) whose
+// bytes lie in [b0, b1).
+template <int DT>
+__device__ __forceinline__ float word_sum(uint32_t u, int wb, int b0, int b1) {
+    if constexpr (DT == MBT_F32) {
+        return wb >= b0 && wb < b1 ? __uint_as_float(u) : 0.f;
+    } else {
+        const float lo = element_value<DT>(u & 0xffffu);
+        const float hi = element_value<DT>(u >> 16);
+        const bool in_lo = wb >= b0 && wb < b1, in_hi = wb + 2 >= b0 && wb + 2 < b1;
+        if (in_lo && in_hi) return lo + hi;
+        return in_lo ? lo : in_hi ? hi : 0.f;
+    }
+}
+
 // Sum of the elements of the 16-byte chunk `v` at window byte offset cb whose
 // bytes lie in [b0, b1) (window-relative offsets, so 32 bits do), in element order.
 template <int DT>
@@ -346,6 +367,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
             // shuffle tree inside the group gives the row's sum.  No thread
             // needs another warp's results, so the window needs no rendezvous.
             const int nrows = static_cast<int>(rw.r1 - rw.r0);
+            const bool tiny = p.N * p.esize <= 16;
             int L = 1;
             while (L < 32 && 2 * L * nrows <= nthr) L <<= 1;
             const int groups = nthr / L;
@@ -360,13 +382,24 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
                     const int64_t loaded = b1 < wj.size ? b1 : wj.size;
                     if (loaded > b0) {
                         const int rb0 = static_cast<int>(b0), rb1 = static_cast<int>(b1);
-                        const int cs = rb0 >> 4;
-                        const int ce = static_cast<int>((loaded - 1) >> 4);
-                        for (int c = cs + gl; c <= ce; c += L) {
-                            const uint4 v = lds128(sbase + 16u * c);
-                            const int cb = 16 * c;
-                            s += (cb >= rb0 && cb + 16 <= rb1) ? chunk_sum<DT>(v)
-                                                               : masked_chunk_sum_rel<DT>(v, cb, rb0, rb1);
+                        if (tiny) {
+                            // Rows of at most 16 bytes: 4-byte reads (measured: rows of
+                            // 3 bf16 elements 1.23 -> 1.82 TB/s; rows of 17 elements or
+                            // more were 3-29 % slower this way, so they keep 16-byte
+                            // chunks despite the bank conflicts of rows ~128 bytes apart).
+                            const int we = static_cast<int>((loaded - 1) >> 2);
+                            for (int wd = (rb0 >> 2) + gl; wd <= we; wd += L)
+                                s += word_sum<DT>(lds32(sbase + 4u * wd), 4 * wd, rb0, rb1);
+                        } else {
+                            const int cs = rb0 >> 4;
+                            const int ce = static_cast<int>((loaded - 1) >> 4);
+                            for (int c = cs + gl; c <= ce; c += L) {
+                                const uint4 v = lds128(sbase + 16u * c);
+                                const int cb = 16 * c;
+                                s += (cb >= rb0 && cb + 16 <= rb1)
+                                         ? chunk_sum<DT>(v)
+                                         : masked_chunk_sum_rel<DT>(v, cb, rb0, rb1);
+                            }
                         }
                     }
                     // Bytes past the array's last 16-byte boundary (never loaded).

@@ -57,6 +57,10 @@ def test_flat_copy_matches_oracle(dtype, M, N, tm, tn, st):
     ("f16", "normal", 300, 63, 70, 128, 64, 2),         # short rows, pitched (140 B)
     ("bf16", "normal", 2000, 33, 33, 64, 256, 2),
     ("f32", "uniform", 5, 3, 3, 128, 32, 1),
+    ("bf16", "normal", 3000, 3, 3, 64, 256, 2),         # rows of <= 16 bytes: 4-byte reads
+    ("f16", "uniform", 2500, 7, 9, 128, 64, 3),         # 14-byte rows, odd pitch
+    ("f16", "normal", 777, 8, 11, 128, 64, 2),          # 16-byte rows starting mid-word
+    ("f32", "normal", 999, 4, 5, 128, 32, 2),
     ("f16", "uniform", 501, 16383, 16383, 128, 64, 3),  # long rows: 3 pieces each
     ("bf16", "normal", 40, 100003, 100003, 64, 256, 2),
     ("f32", "normal", 123, 8191, 8191, 128, 32, 4),
