@@ -177,3 +177,15 @@ def test_ragged_full_size_configs():
         assert mbt.tile_status()[0] == 0
         worst, rel, _ = colsum_errors(out, x[:, :N])
         assert worst <= ROWSUM_RTOL, (dtype, worst, rel)
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_flush_ring_wraps_many_times(split):
+    """Three CTAs over 1024 one-tile strips (and 512 strip pairs): each CTA's
+    consumers post hundreds of strip groups through the two-slot flush ring."""
+    for M, N, tm, tn in ((64, 262144, 64, 256), (100, 65536, 128, 64)):
+        x = synthetic.make_matrix(M, N, "bf16", "normal", seed=M + 5)
+        mbt._reset_workspaces()
+        out = mbt.tile_colsum(x.cuda(), None, tm, tn, 2, max_ctas=3, split=split)
+        assert mbt.tile_status()[0] == 0
+        assert colsum_errors(out, x)[0] <= ROWSUM_RTOL, (M, N)

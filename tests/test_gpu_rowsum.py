@@ -136,3 +136,15 @@ def test_cached_workspaces_per_stream_are_ordered_and_bounded():
     for o in outs:
         assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
     assert rowsum_errors(outs[0], x)[0] <= ROWSUM_RTOL
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_flush_ring_wraps_many_times(split):
+    """Three CTAs over 1563 single-tile bands: each CTA's consumers post ~520
+    segments through the two-slot flush ring (with a workspace, bands shared
+    by two CTAs add their partials through tickets)."""
+    M, N = 100003, 256
+    x = synthetic.make_matrix(M, N, "bf16", "normal", seed=77)
+    out = mbt.tile_rowsum(x.cuda(), None, 64, 256, 2, max_ctas=3, split=split)
+    assert mbt.tile_status()[0] == 0
+    assert rowsum_errors(out, x)[0] <= ROWSUM_RTOL
