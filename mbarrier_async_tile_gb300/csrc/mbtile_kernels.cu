@@ -318,10 +318,10 @@ struct StageInfo {
 // Besides loading, it publishes each stage's band and tile coordinates (each
 // box's, with `boxed`) in `info` before the stage's full barrier is armed --
 // the arrive releases them to the consumers, which then need no division of
-// their own between the barrier and their first read (measured: 1.5 % on the
-// bf16 8192 x 65536 row sum, 15-20 % on the fp32 / fp16 ragged ones, without a
-// workspace) -- and closes the ring with an end mark (key -1) on a stage whose
-// full barrier completes by a plain arrive.
+// their own between the barrier and their first read (measured without a
+// workspace: +5.6 % on the bf16 8192 x 65536 row sum, +21.6 / +16.9 % on the
+// fp32 12289 x 8191 / fp16 24577 x 16383 ones) -- and closes the ring with an
+// end mark (key -1) on a stage whose full barrier completes by a plain arrive.
 template <bool boxed>
 __device__ void produce_rows(const CUtensorMap *map, const RowsumArgs &a, const Smem &sm,
                              const WaitCtl &w, int64_t first, int64_t last,
