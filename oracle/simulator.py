@@ -266,3 +266,98 @@ def two_stage_parity_table(iterations: int = 4) -> list[tuple[int, int, int, int
         cur.step()
         rows.append((it, s, waited, bars[s].parity, cur.phase))
     return rows
+
+
+@dataclass
+class RingResult:
+    status: str                      # "done" | "deadlock" | "budget"
+    steps: int
+    taken: list = field(default_factory=list)        # keys in the order the reader took them
+    violations: list = field(default_factory=list)
+
+
+def simulate_flush_ring(slots: int, records: int, writers: int, *, seed: int = 0,
+                        writer_start_parity: int = 1, reader_start_parity: int = 0,
+                        full_count: int | None = None, max_steps: int | None = None
+                        ) -> RingResult:
+    """Discrete-event model of the sums' flush ring: ``writers`` consumer
+    warps hand ``records`` records to one flush warp through ``slots``
+    shared-memory slots, with the full/empty mbarrier protocol of the tile
+    ring ("cute(12) async_pipeline" §3, §6) run the other way round.
+
+    * writer w, record k (slot k mod slots, parity (k div slots) mod 2 XOR
+      writer_start_parity): wait empty[slot]; write its share of the slot
+      (tagged with k); arrive on full[slot].
+    * reader, record k (same slot, parity (k div slots) mod 2 XOR
+      reader_start_parity): wait full[slot]; read every writer's share; arrive
+      on empty[slot] (expected count 1).
+
+    full[slot] expects ``full_count`` arrivals (default: one per writer).
+    Checked: the reader takes records in order and finds every share of
+    record k tagged k (no share overwritten by record k + slots before it was
+    read, none missing)."""
+    rng = random.Random(seed)
+    fc = writers if full_count is None else full_count
+    full = [MBarrier(fc) for _ in range(slots)]
+    empty = [MBarrier(1) for _ in range(slots)]
+    share = [[None] * writers for _ in range(slots)]
+    wk = [0] * writers          # next record of each writer
+    wstate = ["wait"] * writers  # "wait" (empty) then "arrive" (full)
+    rk = 0
+    rstate = "wait"
+    res = RingResult(status="done", steps=0)
+    budget = max_steps or 100 * (records + 1) * (writers + 2) * slots
+    for step in range(budget):
+        acts = []
+        for w in range(writers):
+            if wk[w] >= records:
+                continue
+            s, par = wk[w] % slots, ((wk[w] // slots) & 1) ^ writer_start_parity
+            if wstate[w] == "wait":
+                if empty[s].test_wait_parity(par):
+                    acts.append(("w", w))
+            else:
+                acts.append(("w", w))
+        if rk < records:
+            s, par = rk % slots, ((rk // slots) & 1) ^ reader_start_parity
+            if rstate == "wait":
+                if full[s].test_wait_parity(par):
+                    acts.append(("r", 0))
+            else:
+                acts.append(("r", 0))
+        if not acts:
+            res.steps = step
+            if rk < records or any(k < records for k in wk):
+                res.status = "deadlock"
+            return res
+        who, i = rng.choice(acts)
+        try:
+            if who == "w":
+                s = wk[i] % slots
+                if wstate[i] == "wait":       # passed the empty wait: write the share
+                    share[s][i] = wk[i]
+                    wstate[i] = "arrive"
+                else:
+                    full[s].arrive()
+                    wstate[i] = "wait"
+                    wk[i] += 1
+            else:
+                s = rk % slots
+                if rstate == "wait":          # passed the full wait: read every share
+                    got = list(share[s])
+                    if got != [rk] * writers:
+                        res.violations.append((rk, got))
+                    res.taken.append(rk)
+                    rstate = "arrive"
+                else:
+                    empty[s].arrive()
+                    rstate = "wait"
+                    rk += 1
+        except ProtocolError as e:
+            res.violations.append(("protocol", str(e)))
+            res.status = "error"
+            res.steps = step
+            return res
+    res.status = "budget"
+    res.steps = budget
+    return res
