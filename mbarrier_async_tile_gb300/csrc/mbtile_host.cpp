@@ -216,12 +216,17 @@ int wanted_ctas_per_sm(int op, const mbt_opts &o, int stages, int64_t stage_byte
 // Row sums: 8 consumer warps (256 threads: an even split of any power-of-two
 // tile_m <= 256) when at most two CTAs share an SM; 4 warps when three or more
 // do (then registers would not fit 8), unless the tile has more rows than 128
-// threads can own.
-int consumer_warps_for(int op, int tile_m, const mbt_opts &o, int wanted_ctas, int64_t n_mod,
-                       bool flat) {
+// threads can own.  The tiled row sum also takes 4 at exactly 3 stages when
+// two CTAs share an SM: measured on 32 KB tiles (bf16 64x256 and 32x512, fp16
+// 128x128), 4 warps beat 8 there by 1.5-2.9 %, while at 2 stages 8 beat 4 by
+// up to 4 %, and at 4 stages (wanted_ctas is never below 2, but only one such
+// CTA fits an SM) 4 warps lose a third.
+int consumer_warps_for(int op, int tile_m, int stages, const mbt_opts &o, int wanted_ctas,
+                       int64_t n_mod, bool flat) {
     if (bulk_stores(op, o, n_mod)) return 1;   // one thread issues the stores
     if (o.consumer_warps) return o.consumer_warps;
     if (flat && op == MBT_OP_ROWSUM) return wanted_ctas <= 2 ? 8 : 4;   // no tile rows
+    if (op == MBT_OP_ROWSUM && wanted_ctas == 2 && stages == 3 && tile_m <= 128) return 4;
     if (op != MBT_OP_COPY) return (wanted_ctas <= 2 || tile_m > 128) ? 8 : 4;
     return kDefaultConsumerWarps;
 }
@@ -329,7 +334,7 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     }
     const int64_t n_mod = N % (16 / es);
     const int wanted = wanted_ctas_per_sm(op, o, stages, plan->stage_bytes, n_mod, flat);
-    const int W = consumer_warps_for(op, tile_m, o, wanted, n_mod, flat);
+    const int W = consumer_warps_for(op, tile_m, stages, o, wanted, n_mod, flat);
     plan->bulk_stores = bulk_stores(op, o, n_mod) || op == MBT_OP_COPY_ROWSUM ? 1 : 0;
     // Row sums: at least one thread per tile row; column sums: at least one
     // thread per 16-byte chunk column of a tile row.
