@@ -101,7 +101,9 @@ typedef struct mbt_opts {
     int32_t consumer_warps;  /* consumer warps per CTA, 1..8; 0 => 4 for
                                 tile_copy; for tile_rowsum 8, or 4 when the
                                 default grid puts 3+ CTAs on an SM and
-                                tile_m <= 128.  The CTA has one more warp,
+                                tile_m <= 128 (and, with a 2-D tensor map,
+                                when it puts 2 on an SM at exactly 3 stages
+                                and tile_m <= 128).  The CTA has one more warp,
                                 the producer. */
     int32_t store_mode;      /* tile_copy only (same result in every mode).
                                 1: one consumer thread writes each landed
@@ -206,7 +208,11 @@ typedef struct mbt_plan {
     int32_t bulk_stores;     /* copy: 1 if stages are written back with bulk
                                 tensor stores (see mbt_opts.store_mode; always
                                 1 for tile_copy_rowsum) */
-    int32_t reserved1;
+    int32_t phase_shift;     /* flat row sum with whole rows per window: the
+                                lane groups of one 8-lane shared-memory phase
+                                sum rows 2^phase_shift apart, which spreads
+                                their 16-byte reads over the bank groups; 0
+                                otherwise */
     int64_t tiles_m;         /* tiles down the rows (row bands) */
     int64_t tiles_n;         /* tiles across the columns */
     int64_t num_tiles;

@@ -76,7 +76,7 @@ class Plan(ctypes.Structure):
         ("box_barriers", ctypes.c_int32),
         ("col_group", ctypes.c_int32),
         ("bulk_stores", ctypes.c_int32),
-        ("reserved1", ctypes.c_int32),
+        ("phase_shift", ctypes.c_int32),
         ("tiles_m", ctypes.c_int64),
         ("tiles_n", ctypes.c_int64),
         ("num_tiles", ctypes.c_int64),

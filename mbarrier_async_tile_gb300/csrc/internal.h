@@ -142,6 +142,9 @@ struct FlatArgs {
     int64_t rows_per_window;   // row sum: whole rows per window, 0 => long rows
     int64_t piece_elems;       // row sum, long rows: elements per piece
     int64_t pieces_per_row;
+    int32_t phase_shift;       // row sum, short rows: the row groups of one 8-lane
+                               // shared-memory phase take rows 2^phase_shift apart
+    int32_t pad0;
 };
 
 // Launchers (mbtile_kernels.cu).  They only enqueue work on `stream`.

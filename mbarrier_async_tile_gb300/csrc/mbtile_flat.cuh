@@ -342,148 +342,172 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     const int warp = ctid >> 5;
     const int nthr = p.consumer_warps * 32;
     const unsigned char *gsrc = reinterpret_cast<const unsigned char *>(a.src);
-    float row_acc = 0.f;            // long rows: this thread's share of the current row
-    uint32_t stage = 0, phase = 0;
-    RowWindow rw = rowsum_window(a, ra, rb, 0);
-    for (int64_t j = 0; j < count; ++j, next_row_window(a, rb, rw)) {
-        bool ok = wait_bounded(sm.full0 + 8u * stage, phase, w, true);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) {
-            if (lane == 0) {
-                report_timeout(w, 1, stage, phase);
-                *w.abort = 1;
+    // One instantiation of the window loop for whole rows per window, one for
+    // pieces of long rows: neither carries the other's state.
+    auto run = [&](auto short_rows) {
+        constexpr bool kShort = decltype(short_rows)::value;
+        float row_acc = 0.f;            // long rows: this thread's share of the current row
+        // Short rows: every row of a window goes to a group of L lanes of one warp
+        // (a power of two, 1..32: as many lanes per row as the threads allow for
+        // this CTA's fullest window; a shorter last window leaves groups idle).
+        // The pp = 8 / L groups of one 8-lane shared-memory phase take rows
+        // 2^phase_shift apart (group g of a block of pp << phase_shift groups sums
+        // row h + q 2^phase_shift, q = g mod pp, h = g / pp), so that their 16-byte
+        // reads fall in different bank groups.
+        const int64_t full_rows = a.rows_per_window < rb - ra ? a.rows_per_window : rb - ra;
+        int L = 1;
+        while (L < 32 && 2 * L * full_rows <= nthr) L <<= 1;
+        const int groups = nthr / L;
+        const int gidx = ctid / L, gl = ctid % L;
+        const int pp_log = L < 8 ? 3 - (__ffs(L) - 1) : 0;
+        const int sh = pp_log > 0 ? a.phase_shift : 0;
+        const int blk = 1 << (pp_log + sh);
+        const bool tiny = p.N * p.esize <= 16;
+        uint32_t stage = 0, phase = 0;
+        RowWindow rw = rowsum_window(a, ra, rb, 0);
+        for (int64_t j = 0; j < count; ++j, next_row_window(a, rb, rw)) {
+            bool ok = wait_bounded(sm.full0 + 8u * stage, phase, w, true);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0) {
+                    report_timeout(w, 1, stage, phase);
+                    *w.abort = 1;
+                }
+                break;
             }
-            break;
-        }
-        if (ctid == 0) log_record(p, 1, j, stage, phase, j);
-        const Window wj = make_window(rw.e0 * p.esize, rw.e1 * p.esize, a.t_floor);
-        const int64_t we = wj.ws + wj.size;
-        const int chunks = static_cast<int>(wj.size >> 4);
-        const uint32_t sbase = sm.base + stage * p.stage_stride;
-        if (a.rows_per_window > 0) {
-            // Short rows: every row of the window goes to a group of L lanes of
-            // one warp (L = 32 W / rows of the window, a power of two, 1..32);
-            // the group's lanes add the row's chunks, masked to the row, and a
-            // shuffle tree inside the group gives the row's sum.  No thread
-            // needs another warp's results, so the window needs no rendezvous.
-            const int nrows = static_cast<int>(rw.r1 - rw.r0);
-            const bool tiny = p.N * p.esize <= 16;
-            int L = 1;
-            while (L < 32 && 2 * L * nrows <= nthr) L <<= 1;
-            const int groups = nthr / L;
-            const int gidx = ctid / L, gl = ctid % L;
-            const int iters = (nrows + groups - 1) / groups;
-            for (int it = 0; it < iters; ++it) {
-                const int lr = gidx + it * groups;
-                float s = 0.f;
-                if (lr < nrows) {
-                    const int64_t e0 = (rw.r0 + lr) * a.ld, e1 = e0 + p.N;
-                    const int64_t b0 = e0 * p.esize - wj.ws, b1 = e1 * p.esize - wj.ws;
-                    const int64_t loaded = b1 < wj.size ? b1 : wj.size;
-                    if (loaded > b0) {
-                        const int rb0 = static_cast<int>(b0), rb1 = static_cast<int>(b1);
-                        if (tiny) {
-                            // Rows of at most 16 bytes: 4-byte reads (measured: rows of
-                            // 3 bf16 elements 1.23 -> 1.82 TB/s; rows of 17 elements or
-                            // more were 3-29 % slower this way, so they keep 16-byte
-                            // chunks despite the bank conflicts of rows ~128 bytes apart).
-                            const int we = static_cast<int>((loaded - 1) >> 2);
-                            for (int wd = (rb0 >> 2) + gl; wd <= we; wd += L)
-                                s += word_sum<DT>(lds32(sbase + 4u * wd), 4 * wd, rb0, rb1);
-                        } else {
-                            const int cs = rb0 >> 4;
-                            const int ce = static_cast<int>((loaded - 1) >> 4);
-                            for (int c = cs + gl; c <= ce; c += L) {
-                                const uint4 v = lds128(sbase + 16u * c);
-                                const int cb = 16 * c;
-                                s += (cb >= rb0 && cb + 16 <= rb1)
-                                         ? chunk_sum<DT>(v)
-                                         : masked_chunk_sum_rel<DT>(v, cb, rb0, rb1);
+            if (ctid == 0) log_record(p, 1, j, stage, phase, j);
+            const Window wj = make_window(rw.e0 * p.esize, rw.e1 * p.esize, a.t_floor);
+            const int64_t we = wj.ws + wj.size;
+            const int chunks = static_cast<int>(wj.size >> 4);
+            const uint32_t sbase = sm.base + stage * p.stage_stride;
+            if constexpr (kShort) {
+                // Short rows: the group's lanes add the row's chunks, masked to
+                // the row, and a shuffle tree inside the group gives the row's sum.
+                // No thread needs another warp's results, so the window needs no
+                // rendezvous.  The rows are padded to whole blocks of the row map.
+                const int nrows = static_cast<int>(rw.r1 - rw.r0);
+                const int padded = (nrows + blk - 1) & ~(blk - 1);
+                const int iters = (padded + groups - 1) / groups;
+                for (int it = 0; it < iters; ++it) {
+                    int lr = gidx + it * groups;
+                    if (sh != 0) {
+                        const int gi = lr & (blk - 1);
+                        lr += (gi >> pp_log) + ((gi & ((1 << pp_log) - 1)) << sh) - gi;
+                    }
+                    float s = 0.f;
+                    if (lr < nrows) {
+                        const int64_t e0 = (rw.r0 + lr) * a.ld, e1 = e0 + p.N;
+                        const int64_t b0 = e0 * p.esize - wj.ws, b1 = e1 * p.esize - wj.ws;
+                        const int64_t loaded = b1 < wj.size ? b1 : wj.size;
+                        if (loaded > b0) {
+                            const int rb0 = static_cast<int>(b0), rb1 = static_cast<int>(b1);
+                            if (tiny) {
+                                // Rows of at most 16 bytes: 4-byte reads (measured: rows of
+                                // 3 bf16 elements 1.23 -> 1.82 TB/s; rows of 17 elements or
+                                // more were 3-29 % slower this way, so they keep 16-byte
+                                // chunks despite the bank conflicts of rows ~128 bytes apart).
+                                const int we = static_cast<int>((loaded - 1) >> 2);
+                                for (int wd = (rb0 >> 2) + gl; wd <= we; wd += L)
+                                    s += word_sum<DT>(lds32(sbase + 4u * wd), 4 * wd, rb0, rb1);
+                            } else {
+                                const int cs = rb0 >> 4;
+                                const int ce = static_cast<int>((loaded - 1) >> 4);
+                                for (int c = cs + gl; c <= ce; c += L) {
+                                    const uint4 v = lds128(sbase + 16u * c);
+                                    const int cb = 16 * c;
+                                    s += (cb >= rb0 && cb + 16 <= rb1)
+                                             ? chunk_sum<DT>(v)
+                                             : masked_chunk_sum_rel<DT>(v, cb, rb0, rb1);
+                                }
                             }
                         }
+                        // Bytes past the array's last 16-byte boundary (never loaded).
+                        if (gl == 0)
+                            for (int64_t bb = loaded > b0 ? loaded : b0; bb < b1; bb += p.esize)
+                                s += element_value<DT>(element_bits<DT>(gsrc + wj.ws + bb));
                     }
-                    // Bytes past the array's last 16-byte boundary (never loaded).
-                    if (gl == 0)
-                        for (int64_t bb = loaded > b0 ? loaded : b0; bb < b1; bb += p.esize)
-                            s += element_value<DT>(element_bits<DT>(gsrc + wj.ws + bb));
+                    for (int off = L >> 1; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+                    if (lr < nrows && gl == 0) a.out[rw.r0 + lr] = s;
                 }
-                for (int off = L >> 1; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-                if (lr < nrows && gl == 0) a.out[rw.r0 + lr] = s;
-            }
-            __syncwarp();
-            if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
-        } else {
-            // Long rows: the window is one piece of row r0; threads keep their
-            // share of the row across its pieces and reduce once per row.
-            const int pb0 = static_cast<int>(rw.e0 * p.esize - wj.ws);   // piece bytes in
-            const int pb1 = static_cast<int>(rw.e1 * p.esize - wj.ws);   // the window
-            for (int c0 = 0; c0 < chunks; c0 += nthr * kFlatVec) {
-                uint4 v[kFlatVec];
-#pragma unroll
-                for (int u = 0; u < kFlatVec; ++u) {
-                    const int c = c0 + ctid + u * nthr;
-                    if (c < chunks) v[u] = lds128(sbase + 16u * c);
+                __syncwarp();
+                if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+            } else {
+                // Long rows: the window is one piece of row r0; threads keep their
+                // share of the row across its pieces and reduce once per row.
+                const int pb0 = static_cast<int>(rw.e0 * p.esize - wj.ws);   // piece bytes in
+                const int pb1 = static_cast<int>(rw.e1 * p.esize - wj.ws);   // the window
+                for (int c0 = 0; c0 < chunks; c0 += nthr * kFlatVec) {
+                    uint4 v[kFlatVec];
+    #pragma unroll
+                    for (int u = 0; u < kFlatVec; ++u) {
+                        const int c = c0 + ctid + u * nthr;
+                        if (c < chunks) v[u] = lds128(sbase + 16u * c);
+                    }
+                    if (c0 + nthr * kFlatVec >= chunks) {
+                        __syncwarp();
+                        if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+                    }
+    #pragma unroll
+                    for (int u = 0; u < kFlatVec; ++u) {
+                        const int c = c0 + ctid + u * nthr;
+                        if (c >= chunks) continue;
+                        const int cb = 16 * c;
+                        row_acc += (cb >= pb0 && cb + 16 <= pb1)
+                                       ? chunk_sum<DT>(v[u])
+                                       : masked_chunk_sum_rel<DT>(v[u], cb, pb0, pb1);
+                    }
                 }
-                if (c0 + nthr * kFlatVec >= chunks) {
+                if (chunks == 0) {
                     __syncwarp();
                     if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
                 }
-#pragma unroll
-                for (int u = 0; u < kFlatVec; ++u) {
-                    const int c = c0 + ctid + u * nthr;
-                    if (c >= chunks) continue;
-                    const int cb = 16 * c;
-                    row_acc += (cb >= pb0 && cb + 16 <= pb1)
-                                   ? chunk_sum<DT>(v[u])
-                                   : masked_chunk_sum_rel<DT>(v[u], cb, pb0, pb1);
+                if (ctid == 0) {
+                    // Elements past the array's last 16-byte boundary.
+                    for (int64_t g = (we > rw.e0 * p.esize ? we / p.esize : rw.e0); g < rw.e1; ++g)
+                        row_acc += element_value<DT>(element_bits<DT>(gsrc + g * p.esize));
                 }
-            }
-            if (chunks == 0) {
-                __syncwarp();
-                if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
-            }
-            if (ctid == 0) {
-                // Elements past the array's last 16-byte boundary.
-                for (int64_t g = (we > rw.e0 * p.esize ? we / p.esize : rw.e0); g < rw.e1; ++g)
-                    row_acc += element_value<DT>(element_bits<DT>(gsrc + g * p.esize));
-            }
-            if (rw.piece == a.pieces_per_row - 1) {
-                float s = row_acc;
-                row_acc = 0.f;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-                // Deposit the warp's partial; warp 0 alone waits for the row's
-                // other partials and adds them in warp order, so the other
-                // warps go on to the next row at once.
-                const int64_t lr = rw.r0 - ra;
-                const int slot = static_cast<int>(lr % kFlatRowSlots);
-                const uint32_t bar = smem_u32(&row_bar[slot]);
-                if (lane == 0) {
-                    red[slot][warp] = s;
-                    mbar_arrive(bar);
-                }
-                if (warp == 0) {
-                    bool got = wait_bounded(bar, static_cast<uint32_t>((lr / kFlatRowSlots) & 1),
-                                            w, true);
-                    got = __all_sync(0xffffffffu, got);
-                    if (!got) {
-                        if (lane == 0) {
-                            report_timeout(w, 1, kMaxStages, static_cast<uint32_t>(slot));
-                            *w.abort = 1;
-                        }
-                        break;
-                    }
+                if (rw.piece == a.pieces_per_row - 1) {
+                    float s = row_acc;
+                    row_acc = 0.f;
+    #pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+                    // Deposit the warp's partial; warp 0 alone waits for the row's
+                    // other partials and adds them in warp order, so the other
+                    // warps go on to the next row at once.
+                    const int64_t lr = rw.r0 - ra;
+                    const int slot = static_cast<int>(lr % kFlatRowSlots);
+                    const uint32_t bar = smem_u32(&row_bar[slot]);
                     if (lane == 0) {
-                        float total = 0.f;
-                        for (int k = 0; k < p.consumer_warps; ++k) total += red[slot][k];
-                        a.out[rw.r0] = total;
+                        red[slot][warp] = s;
+                        mbar_arrive(bar);
+                    }
+                    if (warp == 0) {
+                        bool got = wait_bounded(bar, static_cast<uint32_t>((lr / kFlatRowSlots) & 1),
+                                                w, true);
+                        got = __all_sync(0xffffffffu, got);
+                        if (!got) {
+                            if (lane == 0) {
+                                report_timeout(w, 1, kMaxStages, static_cast<uint32_t>(slot));
+                                *w.abort = 1;
+                            }
+                            break;
+                        }
+                        if (lane == 0) {
+                            float total = 0.f;
+                            for (int k = 0; k < p.consumer_warps; ++k) total += red[slot][k];
+                            a.out[rw.r0] = total;
+                        }
                     }
                 }
             }
+            if (++stage == static_cast<uint32_t>(p.stages)) {
+                stage = 0;
+                phase ^= 1u;
+            }
         }
-        if (++stage == static_cast<uint32_t>(p.stages)) {
-            stage = 0;
-            phase ^= 1u;
-        }
-    }
+    };
+    if (a.rows_per_window > 0)
+        run(std::true_type{});
+    else
+        run(std::false_type{});
 }

@@ -272,6 +272,81 @@ void flat_setup(int op, int64_t M, int64_t N, int64_t ld, int es, int tile_m, in
     }
 }
 
+// Flat row sum, short rows: lanes per row L for a window of `rows` rows on
+// `nthr` consumer threads -- the kernel's rule (a power of two, as many lanes
+// per row as the threads allow, up to a warp).
+int flat_lanes_per_row(int64_t rows, int nthr) {
+    int L = 1;
+    while (L < 32 && 2 * L * rows <= nthr) L <<= 1;
+    return L;
+}
+
+// Flat row sum, short rows: a 16-byte shared-memory load is served in phases
+// of 8 lanes, one wavefront per 16-byte bank group (address / 16 mod 8) and
+// distinct address in it.  A phase holds 8 / L rows' groups of L lanes; rows
+// one pitch apart start in nearly the same bank group when the pitch is close
+// to a multiple of 128 bytes (126-byte rows: ~23 wavefronts per load instead
+// of 4).  The kernel therefore lets the groups of one phase take rows 2^shift
+// apart; this picks the shift whose first loads spread best, by counting the
+// wavefronts of sample phases (window start offsets 0, 4, 8, 12 mod 16, 8
+// phases each).  The kernel pads a window's rows to a whole block of
+// (8 / L) << shift rows, so a shift qualifies only if the padding adds no round
+// of rows per lane group.  A shift is taken only if it cuts the wavefronts at
+// least 3-fold: the row map costs a few instructions per row, and measured on
+// rows whose lanes met 2-way conflicts (34- and 606-byte rows) removing them
+// did not pay (-1.5 to -2.5 %), while 126-byte rows (~6 wavefronts per phase)
+// gained 21 %.  0 when L >= 8 (a phase reads one row's consecutive chunks) or
+// the rows are read 4 bytes at a time.
+int flat_phase_shift(const mbt::FlatArgs &f, int64_t N, int es, int W) {
+    if (f.rows_per_window <= 0 || N * es <= 16) return 0;
+    const int L = flat_lanes_per_row(f.rows_per_window, 32 * W);
+    if (L >= 8) return 0;
+    const int per_phase = 8 / L;
+    const int64_t pitch = f.ld * es;
+    auto wavefronts = [&](int shift) {
+        int64_t total = 0;
+        for (int off0 = 0; off0 < 16; off0 += 4) {
+            for (int h = 0; h < 8; ++h) {
+                int64_t chunks[8];
+                int n = 0;
+                for (int q = 0; q < per_phase; ++q) {
+                    const int64_t first =
+                        (off0 + (h + (static_cast<int64_t>(q) << shift)) * pitch) / 16;
+                    for (int gl = 0; gl < L; ++gl) chunks[n++] = first + gl;
+                }
+                int worst = 0;
+                for (int g = 0; g < 8; ++g) {
+                    int distinct = 0;
+                    for (int i = 0; i < n; ++i) {
+                        if (chunks[i] % 8 != g) continue;
+                        bool seen = false;
+                        for (int k = 0; k < i; ++k) seen = seen || chunks[k] == chunks[i];
+                        distinct += seen ? 0 : 1;
+                    }
+                    worst = std::max(worst, distinct);
+                }
+                total += worst;
+            }
+        }
+        return total;
+    };
+    const int64_t rows = f.rows_per_window, groups = 32 * W / L;
+    const int64_t rounds = ceil_div(rows, groups);
+    const int64_t base_cost = wavefronts(0);
+    int best = 0;
+    int64_t best_cost = base_cost;
+    for (int shift = 1; shift <= 6; ++shift) {
+        const int64_t blk = static_cast<int64_t>(per_phase) << shift;
+        if (ceil_div(round_up(rows, blk), groups) != rounds) continue;
+        const int64_t c = wavefronts(shift);
+        if (c < best_cost) {
+            best = shift;
+            best_cost = c;
+        }
+    }
+    return 3 * best_cost <= base_cost ? best : 0;
+}
+
 int64_t flat_windows(int op, const mbt::FlatArgs &f, int64_t M, int64_t G) {
     if (op == MBT_OP_COPY) return ceil_div(f.t_floor, f.cap_bytes);
     int64_t n = 0;
@@ -376,6 +451,7 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
         plan->grid = static_cast<int32_t>(G);
         plan->num_tiles = flat_windows(op, f, M, G);
         plan->kmax = 1;
+        plan->phase_shift = op == MBT_OP_ROWSUM ? flat_phase_shift(f, N, es, W) : 0;
         return MBT_OK;
     }
     if (op == MBT_OP_COPY) {
@@ -565,6 +641,7 @@ int flat_launch(int op, const void *src, void *dst, float *out, int64_t M, int64
     rc = device_figures(&d);
     if (rc != MBT_OK) return rc;
     flat_setup(op, M, N, ld, esize_of(dtype), tile_m, tile_n, stages, d.smem_optin, &f);
+    f.phase_shift = plan.phase_shift;
     const cudaError_t e =
         op == MBT_OP_COPY
             ? mbt::launch_copy_flat(f, plan.grid, plan.threads, plan.smem_bytes,

@@ -33,6 +33,8 @@
 // mbt_colsum_kernel (column sums, tiles taken down the column strips).
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 
 namespace mbt {

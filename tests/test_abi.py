@@ -107,6 +107,40 @@ def test_flat_rowsum_windows_follow_the_rows_not_the_tile():
                  fit=8)["flat"] == 1
 
 
+def test_flat_rowsum_phase_shift_spreads_bank_groups():
+    """Short unaligned rows: the 8 / L lane groups of one 8-lane shared-memory
+    phase sum rows 2^phase_shift apart.  A 16-byte read's bank group is its
+    window offset / 16 mod 8, so rows s apart start s * pitch / 16 groups
+    apart: with 8 rows of one lane each, s * pitch = 16 x odd (mod 128) puts the
+    phase's 8 lanes in 8 distinct groups; with 4 rows of 2 lanes each, s * pitch
+    = 32 x odd (mod 128) puts their 2-chunk spans side by side.  A shift is
+    taken only where it cuts a phase's wavefronts at least 3-fold."""
+    def shift(dtype, N, **kw):
+        return _plan(mbt.OP_ROWSUM, 2097152, N, 128, 64, 2, dtype, fit=3, **kw)["phase_shift"]
+    # one lane per row (4 consumer warps, 224-260 rows per window):
+    # 8 x 126 = 1008 = -16, 8 x 130 = 1040 = 16, 8 x 134 = 1072 = 48 (mod 128);
+    # a smaller power of two leaves two lanes of a phase in one group
+    assert shift(torch.bfloat16, 63) == 3
+    assert shift(torch.bfloat16, 65) == 3
+    assert shift(torch.bfloat16, 67) == 3
+    # 510-byte rows, 64 per window, 2 lanes per row: 16 x 510 = 8160 = 96 = 32 x 3
+    # (mod 128); 8 x 510 = 4080 = 112 would overlap two rows' spans
+    assert shift(torch.float16, 255) == 4
+    # two rows per phase (4 lanes each), or 34-byte rows 2.1 groups apart: at
+    # most 2-way conflicts, which a shift could only halve
+    assert shift(torch.bfloat16, 300) == 0
+    assert shift(torch.bfloat16, 17) == 0
+    # 2002-byte rows: 16 per window, a phase reads 8 chunks of one row
+    assert shift(torch.float16, 1001) == 0
+    # rows of at most 16 bytes are read 4 bytes at a time; long rows in pieces
+    assert shift(torch.bfloat16, 3) == 0
+    assert _plan(mbt.OP_ROWSUM, 2000, 100003, 128, 64, 2, torch.bfloat16,
+                 fit=8)["phase_shift"] == 0
+    # 2-D tensor-map path and the copy: no lane groups over rows
+    assert _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16)["phase_shift"] == 0
+    assert _plan(mbt.OP_COPY, 2097152, 63, 128, 64, 2, torch.bfloat16)["phase_shift"] == 0
+
+
 def test_copy_tile_and_stage_errors():
     assert _copy(A, B, 8, 64, tm=0) == -1
     assert _copy(A, B, 8, 64, tm=257) == -1

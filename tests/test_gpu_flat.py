@@ -74,6 +74,40 @@ def test_flat_rowsum_matches_oracle(dtype, dist, M, N, ld, tm, tn, st):
     assert worst <= ROWSUM_RTOL, (worst, rel)
 
 
+@pytest.mark.parametrize("dtype,M,N,warps,ctas", [
+    ("bf16", 5000, 65, 0, 16),      # 224 rows per window padded to blocks of 64
+    ("bf16", 4097, 67, 0, 16),
+    ("f16", 2049, 255, 0, 16),      # 2 lanes per row, rows 16 apart
+    ("f32", 7777, 31, 0, 16),
+    ("f16", 3001, 127, 0, 16),
+    ("bf16", 3000, 129, 0, 8),
+    ("bf16", 100000, 63, 0, 0),     # default grid, ~219 rows per CTA: one short window each
+    ("bf16", 5000, 63, 8, 16),      # 8 consumer warps
+])
+def test_flat_rowsum_permuted_rows_each_written_once(dtype, M, N, warps, ctas):
+    """Rows given to lane groups 2^phase_shift apart: every row is summed and
+    written (the output starts as NaN), on windows cut short at each CTA's
+    last rows as well as whole ones.  The grid is capped where the default
+    one would leave each CTA fewer rows than a window holds (its lane groups
+    would then take a row each, and no phase would hold several rows)."""
+    kw = {"consumer_warps": warps} if warps else {}
+    if ctas:
+        kw["max_ctas"] = ctas
+    info = mbt.tile_device_info()
+    plan = mbt.tile_plan(mbt.OP_ROWSUM, M, N, 128, 64, 2, synthetic.DTYPES[dtype],
+                         num_sms=info["num_sms"], smem_optin=info["smem_optin"],
+                         fit_per_sm=3, **kw)
+    assert plan["flat"] == 1 and plan["phase_shift"] > 0
+    x = synthetic.make_matrix(M, N, dtype, "normal", seed=31 * M + N)
+    out = torch.full((M,), float("nan"), device="cuda")
+    mbt.tile_rowsum(x.cuda(), out, 128, 64, 2, **kw)
+    code, info = mbt.tile_status()
+    assert code == 0, info
+    assert not bool(out.isnan().any())
+    worst, rel, _ = rowsum_errors(out, x)
+    assert worst <= ROWSUM_RTOL, (worst, rel)
+
+
 def test_flat_full_size_dense_ragged_configs():
     """The ragged shapes of the task, stored dense (no pitch padding)."""
     for dtype, M, N, tm, tn, seed in (("f32", 12289, 8191, 128, 32, 1005),
