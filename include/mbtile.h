@@ -54,6 +54,12 @@
  *     with zero fill and never written past the logical shape.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream) of the
  *     current device.  Calls are asynchronous on it, like any CUDA library.
+ *     The pipeline kernels are launched with programmatic stream
+ *     serialization: one may be launched, and set up its shared memory, while
+ *     the previous kernel of the stream completes, but it reads and writes
+ *     global memory only after that kernel has completed and its writes are
+ *     visible.  Stream order is therefore what it would be without it: a call
+ *     may read what the call before it wrote.
  *   - Return value: MBT_OK, or a negative mbt_status.  Argument errors are
  *     detected on the host before anything is launched.  A pipeline wait that
  *     runs past its time budget on the device does not hang: the kernel
