@@ -313,8 +313,8 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     mbt_rowsum_flat_kernel(const FlatArgs a) {
     extern __shared__ __align__(1024) unsigned char dyn_smem[];
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
-    // Long rows: warp partials of row lr in red[lr % 8]; row_bar[lr % 8]
-    // completes when every consumer warp has deposited its partial.
+    // Long rows: warp partials of row lr in red[lr % kFlatRowSlots]; its
+    // row_bar completes when every consumer warp has deposited its partial.
     __shared__ __align__(8) uint64_t row_bar[kFlatRowSlots];
     __shared__ float red[kFlatRowSlots][kMaxConsumerWarps];
     __shared__ int abort_flag;
