@@ -301,36 +301,40 @@ int flat_phase_shift(const mbt::FlatArgs &f, int64_t N, int es, int W) {
     if (f.rows_per_window <= 0 || N * es <= 16) return 0;
     const int L = flat_lanes_per_row(f.rows_per_window, 32 * W);
     if (L >= 8) return 0;
+    const int64_t pitch = f.ld * es, rows = f.rows_per_window;
+    // The answer depends on (pitch, rows per window, W) alone; callers repeat
+    // shapes, so each host thread keeps its last one (the search below costs
+    // a few microseconds).
+    thread_local int64_t last_pitch = -1, last_rows = -1;
+    thread_local int last_w = 0, last_shift = 0;
+    if (pitch == last_pitch && rows == last_rows && W == last_w) return last_shift;
     const int per_phase = 8 / L;
-    const int64_t pitch = f.ld * es;
+    // Wavefronts of the first 16-byte loads of sample phases: per phase, the
+    // most distinct chunks that share one bank group.
     auto wavefronts = [&](int shift) {
         int64_t total = 0;
         for (int off0 = 0; off0 < 16; off0 += 4) {
             for (int h = 0; h < 8; ++h) {
-                int64_t chunks[8];
-                int n = 0;
+                int64_t chunk[8];
+                int per_group[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                int n = 0, worst = 0;
                 for (int q = 0; q < per_phase; ++q) {
                     const int64_t first =
                         (off0 + (h + (static_cast<int64_t>(q) << shift)) * pitch) / 16;
-                    for (int gl = 0; gl < L; ++gl) chunks[n++] = first + gl;
-                }
-                int worst = 0;
-                for (int g = 0; g < 8; ++g) {
-                    int distinct = 0;
-                    for (int i = 0; i < n; ++i) {
-                        if (chunks[i] % 8 != g) continue;
+                    for (int gl = 0; gl < L; ++gl) {
+                        const int64_t c = first + gl;
                         bool seen = false;
-                        for (int k = 0; k < i; ++k) seen = seen || chunks[k] == chunks[i];
-                        distinct += seen ? 0 : 1;
+                        for (int k = 0; k < n; ++k) seen = seen || chunk[k] == c;
+                        chunk[n++] = c;
+                        if (!seen) worst = std::max(worst, ++per_group[c & 7]);
                     }
-                    worst = std::max(worst, distinct);
                 }
                 total += worst;
             }
         }
         return total;
     };
-    const int64_t rows = f.rows_per_window, groups = 32 * W / L;
+    const int64_t groups = 32 * W / L;
     const int64_t rounds = ceil_div(rows, groups);
     const int64_t base_cost = wavefronts(0);
     int best = 0;
@@ -344,7 +348,11 @@ int flat_phase_shift(const mbt::FlatArgs &f, int64_t N, int es, int W) {
             best_cost = c;
         }
     }
-    return 3 * best_cost <= base_cost ? best : 0;
+    last_pitch = pitch;
+    last_rows = rows;
+    last_w = W;
+    last_shift = 3 * best_cost <= base_cost ? best : 0;
+    return last_shift;
 }
 
 int64_t flat_windows(int op, const mbt::FlatArgs &f, int64_t M, int64_t G) {
