@@ -136,6 +136,11 @@ def test_flat_rowsum_phase_shift_spreads_bank_groups():
     assert shift(torch.bfloat16, 3) == 0
     assert _plan(mbt.OP_ROWSUM, 2000, 100003, 128, 64, 2, torch.bfloat16,
                  fit=8)["phase_shift"] == 0
+    # the same rows on 8 consumer warps: 4 lanes per row, two rows per phase
+    # (at most 2-way); the answer follows the warps, call after call
+    assert shift(torch.float16, 255, consumer_warps=8) == 0
+    assert shift(torch.float16, 255) == 4
+    assert shift(torch.float16, 255, consumer_warps=8) == 0
     # 2-D tensor-map path and the copy: no lane groups over rows
     assert _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16)["phase_shift"] == 0
     assert _plan(mbt.OP_COPY, 2097152, 63, 128, 64, 2, torch.bfloat16)["phase_shift"] == 0
