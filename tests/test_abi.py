@@ -265,6 +265,15 @@ def test_plan_default_grid_follows_bytes_in_flight():
     # row sum, 64 x 256 bf16 (32 KB stages): 2 stages x 2 CTAs = 128 KB per SM, 8 warps
     p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16, fit=4, ws=True)
     assert p["grid"] == 304 and p["consumer_warps"] == 8
+    # the same tiles at 3 stages (96 KB per CTA): still 2 CTAs, with 4 warps; at 4
+    # stages only one 128 KB CTA fits an SM, which keeps 8 warps
+    p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 3, torch.bfloat16, fit=2, ws=True)
+    assert p["grid"] == 304 and p["consumer_warps"] == 4
+    p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True)
+    assert p["grid"] == 152 and p["consumer_warps"] == 8
+    # 3 stages of 256-row tiles: 4 warps cannot give each row a thread
+    p = _plan(mbt.OP_ROWSUM, 16384, 32768, 256, 64, 3, torch.float16, fit=2, ws=True)
+    assert p["consumer_warps"] == 8
     # row sum, 128 x 64 fp16 (16 KB stages), 3 stages: 3 CTAs per SM with 4 warps
     p = _plan(mbt.OP_ROWSUM, 24577, 16383, 128, 64, 3, torch.float16, fit=4, ws=True,
               ld_src=16384)
