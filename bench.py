@@ -291,10 +291,6 @@ def bench_gpu(args, rank, world):
     mbt.tile_device_info()  # loads the library, fails loudly if it is missing
     x3, d3, x4, o4 = make_inputs(dev)
     main = torch.cuda.current_stream()
-    ws_bytes = mbt.tile_rowsum_workspace_bytes(ROWSUM["M"], ROWSUM["N"], ROWSUM["tile_m"],
-                                               ROWSUM["tile_n"], args.rowsum_stages,
-                                               torch.bfloat16)
-    ws = torch.zeros(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     side = (torch.cuda.Stream(), torch.cuda.Stream())
 
     def run_pass(two_streams: bool, record: bool):
@@ -313,7 +309,7 @@ def bench_gpu(args, rank, world):
                 ev[1].record(s_copy)
                 ev[2].record(s_rowsum)
             mbt.tile_rowsum(x4, o4, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
-                            workspace=ws, stream=s_rowsum)
+                            stream=s_rowsum)
             if ev is not None:
                 ev[3].record(s_rowsum)
 
@@ -371,7 +367,7 @@ def bench_gpu(args, rank, world):
                               store_mode=args.store_mode, stream=main)
             else:
                 mbt.tile_rowsum(x4, o4, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
-                                workspace=ws, stream=main)
+                                stream=main)
 
         def check():
             code, info = mbt.tile_status(main)
@@ -411,7 +407,7 @@ def bench_gpu(args, rank, world):
 
     def rowsum_on(stream):
         mbt.tile_rowsum(x4, o4, ROWSUM["tile_m"], ROWSUM["tile_n"], args.rowsum_stages,
-                        workspace=ws, stream=stream)
+                        stream=stream)
 
     def graphed(chunk_body, steps: int):
         """CUDA graphs that together replay `steps` steps: chunk_body(origin,
@@ -420,11 +416,14 @@ def bench_gpu(args, rank, world):
         replays them on the current stream."""
         full, rem = divmod(steps, GRAPH_CHUNK)
         graphs = []
+        cap = torch.cuda.Stream()
+        cap.wait_stream(main)
+        chunk_body(cap, 1)   # outside the capture: the library's workspace for cap
+        torch.cuda.synchronize()
         for n, times in ((GRAPH_CHUNK, full), (rem, 1)):
             if n == 0 or times == 0:
                 continue
             g = torch.cuda.CUDAGraph()
-            cap = torch.cuda.Stream()
             cap.wait_stream(main)
             with torch.cuda.graph(g, stream=cap):
                 chunk_body(cap, n)
@@ -502,6 +501,12 @@ def bench_gpu(args, rank, world):
     ms_rowsum = ms_rowsum_graph if graph else ms_rowsum_stream
     ms_total = ms_total_graph if graph else ms_total_stream
     t1 = time.time()
+    # every configuration of the task's table and the stage sweep, each point
+    # in its own clock window
+    sweep = None
+    if not args.no_sweep:
+        theo = mbt.tile_device_info()["hbm_gbs_theoretical"]
+        sweep = config_sweep(dev, clocks, measured_peak()[0], theo)
     time.sleep(0.15)
     clocks.stop()
     step_bytes = copy_bytes() + rowsum_bytes()
@@ -579,6 +584,17 @@ def bench_gpu(args, rank, world):
         "gpu_launches": 2 * args.steps,
         "clocks": clocks.summary(t0, t1),
     }
+    if sweep is not None:
+        out["sweep"] = sweep
+        out["sweep_note"] = (
+            "every configuration of the task's table (1, 2: latency; 3: copy at 1/2/3/4/6 "
+            "stages with LSU and bulk stores; 4: row and column sums at 2/3/4 stages with a "
+            "caller's workspace, and the plain calls with the library's own; 5a/5b: copy, "
+            "row sum, column sum and fused copy + row sum at 3 stages), each timed by "
+            f"replaying CUDA graphs of its calls for about {POINT_TARGET_S} s on one stream "
+            "(ms = mean per launch, gaps included; ms_host_launched: 20 host launches back "
+            "to back), clocks sampled during its replays, output checked on the device "
+            "before timing; frac = gbs / measured hbm_gbs")
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(x3, d3, x4, o4, args.cpu_budget)
     return out
@@ -693,125 +709,213 @@ def bench_only(args):
                       "gbs": round(nbytes / ms / 1e6, 1)}), flush=True)
 
 
-def bench_configs(args):
-    """One line per configuration of the task's table: latency for the two
-    lesson shapes, GB/s (algorithmic bytes / device time) for the streaming
-    and ragged ones, each the median of 5 rounds of `reps` back-to-back calls."""
+# Every configuration of the task's table, each point timed in its own window
+# with the SM clocks sampled there.  (config, op, dtype, M, N, tile_m, tile_n,
+# stages, extra) -- extra: store_mode for copies, "caller" / "library" for the
+# sums' workspace.
+CONFIG_POINTS = (
+    [("1", "copy", "f16", 256, 128, 128, 64, 1, {}),
+     ("2", "copy", "f16", 128, 512, 128, 64, 3, {"consumer_warps": 3, "max_ctas": 1})]
+    + [("3", "copy", "f16", 16384, 16384, 128, 64, st, {"store_mode": mode})
+       for mode in (2, 1) for st in (1, 2, 3, 4, 6)]
+    + [("4", op, "bf16", 8192, 65536, 64, 256, st, {"workspace": "caller"})
+       for op in ("rowsum", "colsum") for st in (2, 3, 4)]
+    + [("4", op, "bf16", 8192, 65536, 64, 256, 2, {"workspace": "library"})
+       for op in ("rowsum", "colsum")]
+    + [(cfg, op, dt, M, N, tm, tn, 3, extra)
+       for cfg, dt, M, N, tm, tn in (("5a", "f32", 12289, 8191, 128, 32),
+                                     ("5b", "f16", 24577, 16383, 128, 64))
+       for op, extra in (("copy", {"store_mode": 2}), ("copy", {"store_mode": 1}),
+                         ("rowsum", {"workspace": "caller"}),
+                         ("rowsum", {"workspace": "library"}),
+                         ("colsum", {"workspace": "caller"}),
+                         ("colsum", {"workspace": "library"}),
+                         ("copy_rowsum", {"workspace": "library"}))]
+)
+CONFIG_SEEDS = {"1": 1001, "2": 1002, "3": 1003, "4": 1004, "5a": 1005, "5b": 1006}
+CONFIG_DIST = {"4": "normal"}
+POINT_TARGET_S = 0.25     # device time of each point's timed graph replays
+
+
+def config_sweep(dev, clocks, peak: float, theo: float, target_s: float = POINT_TARGET_S,
+                 select=None):
+    """Time every CONFIG_POINTS entry (or those `select` keeps) on one side
+    stream: the calls captured in a CUDA graph (20 launches, 200 for the
+    latency-bound lesson shapes), replayed until about `target_s` of device
+    time, one event pair around the replays (mean per launch, gaps included);
+    then 20 launches from the host, back to back.  The SM clocks sampled
+    during each point's replays go with it.  Each point's output is checked
+    once on the device first (copies bit for bit, sums on sampled rows or
+    columns against a float64 reduction within 1e-5 of max(|sum|, sqrt(sum
+    of squares))).  Returns the list of point records."""
     import mbarrier_async_tile_gb300 as mbt
     import synthetic
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    out_points = []
+    cache = {}
+
+    def matrix(cfg, dt, M, N):
+        key = (cfg, dt, M, N)
+        if key not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            ld = synthetic.pitched_ld(N, dt) if cfg in ("5a", "5b") else N
+            x = synthetic.make_matrix(M, N, dt, CONFIG_DIST.get(cfg, "uniform"),
+                                      CONFIG_SEEDS[cfg], ld=ld, draw_on=str(dev))
+            cache[key] = (x, ld)
+        return cache[key]
+
+    def check_status(what):
+        code, info = mbt.tile_status(side)
+        if code != 0:
+            raise RuntimeError(f"{what}: pipeline status {code} {info}")
+
+    def sums_ok(got, x, dim, g):
+        n = x.shape[1 - dim]
+        idx = torch.randperm(n, generator=g)[:64].to(dev)
+        part = x.index_select(1 - dim, idx).double()
+        ref = part.sum(dim)
+        scale = torch.maximum(ref.abs(), part.pow(2).sum(dim).sqrt())
+        return bool(((got[idx].double() - ref).abs() <= 1e-5 * scale).all())
+
+    for (cfg, op, dt, M, N, tm, tn, st, extra) in CONFIG_POINTS:
+        if select is not None and not select(cfg, op, st, extra):
+            continue
+        x, ld = matrix(cfg, dt, M, N)
+        xs = x[:, :N]
+        es = ESIZE[dt]
+        ws_kind = extra.get("workspace")
+        kw = {k: v for k, v in extra.items() if k != "workspace"}
+        y = torch.empty_like(x)[:, :N] if op in ("copy", "copy_rowsum") else None
+        o = torch.empty(N if op == "colsum" else M, dtype=torch.float32, device=dev) \
+            if op != "copy" else None
+        ws = None
+        if ws_kind == "caller":
+            need = (mbt.tile_colsum_workspace_bytes if op == "colsum"
+                    else mbt.tile_rowsum_workspace_bytes)(M, N, tm, tn, st, xs.dtype, ld_src=ld)
+            ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+        if op == "copy":
+            call = lambda s: mbt.tile_copy(xs, y, tm, tn, st, stream=s, **kw)  # noqa: E731
+            nbytes = 2 * M * N * es
+        elif op == "rowsum":
+            call = lambda s: mbt.tile_rowsum(xs, o, tm, tn, st, workspace=ws,  # noqa: E731
+                                             stream=s, **kw)
+            nbytes = M * N * es + 4 * M
+        elif op == "colsum":
+            call = lambda s: mbt.tile_colsum(xs, o, tm, tn, st, workspace=ws,  # noqa: E731
+                                             stream=s, **kw)
+            nbytes = M * N * es + 4 * N
+        else:
+            call = lambda s: mbt.tile_copy_rowsum(xs, y, o, tm, tn, st, stream=s,  # noqa: E731
+                                                  **kw)
+            nbytes = 2 * M * N * es + 4 * M
+        latency = cfg in ("1", "2")
+        n_graph = 200 if latency else 20
+        # once, checked (this also plans, and allocates the library's workspace)
+        if y is not None:
+            y.fill_(float("nan"))
+        # inputs, poison and workspace were written on the current stream
+        side.wait_stream(torch.cuda.current_stream())
+        call(side)
+        torch.cuda.synchronize()
+        check_status(f"config {cfg} {op}")
+        g = torch.Generator().manual_seed(5)
+        ok = True
+        if y is not None:
+            iv = torch.int32 if es == 4 else torch.int16
+            ok = ok and torch.equal(y.contiguous().view(iv), xs.contiguous().view(iv))
+        if op in ("rowsum", "copy_rowsum"):
+            ok = ok and sums_ok(o, xs, 1, g)
+        if op == "colsum":
+            ok = ok and sums_ok(o, xs, 0, g)
+        # host-launched, back to back
+        for _ in range(3):
+            call(side)
+        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_host = 200 if latency else 20
+        torch.cuda.synchronize()
+        h0.record(side)
+        for _ in range(n_host):
+            call(side)
+        h1.record(side)
+        torch.cuda.synchronize()
+        check_status(f"config {cfg} {op}")
+        ms_host = h0.elapsed_time(h1) / n_host
+        # graph replays
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(n_graph):
+                call(side)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(side):
+            e0.record(side)
+            graph.replay()
+            e1.record(side)
+        torch.cuda.synchronize()
+        reps = max(3, int(target_s / max(e0.elapsed_time(e1) / 1e3, 1e-6)) + 1)
+        t0 = time.time()
+        with torch.cuda.stream(side):
+            e0.record(side)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(side)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        check_status(f"config {cfg} {op}")
+        ms = e0.elapsed_time(e1) / (reps * n_graph)
+        del graph
+        rec = {"config": cfg, "op": op, "dtype": dt, "shape": [M, N], "ld": ld,
+               "tile": [tm, tn], "stages": st}
+        if "store_mode" in extra:
+            rec["store"] = MODE_NAME[extra["store_mode"]]
+        if ws_kind:
+            rec["workspace"] = ws_kind
+        if "max_ctas" in extra:
+            rec["ctas"] = extra["max_ctas"]
+            rec["consumer_warps"] = extra["consumer_warps"]
+        rec["bytes"] = nbytes
+        if latency:
+            rec["us_per_call"] = round(ms * 1e3, 3)
+            rec["us_per_call_host_launched"] = round(ms_host * 1e3, 3)
+        else:
+            gbs = nbytes / ms / 1e6
+            rec.update(ms=round(ms, 4), gbs=round(gbs, 1), frac=round(gbs / peak, 4),
+                       frac_theoretical=round(gbs / theo, 4) if theo else None,
+                       ms_host_launched=round(ms_host, 4),
+                       gbs_host_launched=round(nbytes / ms_host / 1e6, 1))
+        rec["launches_timed"] = reps * n_graph
+        rec["parity_ok"] = bool(ok)
+        c = clocks.summary(t0, t1)
+        rec["clocks"] = {"sm_mhz": c.get("sm_mhz"), "sm_max_mhz": c.get("sm_max_mhz"),
+                         "reasons": c.get("reasons"), "samples": c.get("samples")}
+        out_points.append(rec)
+    cache.clear()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out_points
+
+
+def bench_configs(args):
+    """One JSON line per configuration point (see config_sweep), then the
+    denominators."""
+    import mbarrier_async_tile_gb300 as mbt
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     peak, peak_kind = measured_peak()
     theo = mbt.tile_device_info()["hbm_gbs_theoretical"]
-
-    def med_ms(fn, reps):
-        vals = []
-        for _ in range(5):
-            for _ in range(3):
-                fn()
-            torch.cuda.synchronize()
-            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s.record()
-            for _ in range(reps):
-                fn()
-            e.record()
-            torch.cuda.synchronize()
-            vals.append(s.elapsed_time(e) / reps)
-        code, info = mbt.tile_status()
-        if code != 0:
-            raise RuntimeError(f"pipeline status {code} {info}")
-        return statistics.median(vals)
-
-    def line(d):
-        if "gbs" in d:
-            d["frac_of_peak"] = round(d["gbs"] / peak, 4)
-            d["frac_of_theoretical"] = round(d["gbs"] / theo, 4) if theo else None
-        print(json.dumps(d), flush=True)
-
-    def graph_us(call, n=100):
-        """Device time per call: n calls captured in one CUDA graph, replayed."""
-        call(torch.cuda.current_stream())
-        torch.cuda.synchronize()
-        side = torch.cuda.Stream()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(side):
-            with torch.cuda.graph(g, stream=side):
-                for _ in range(n):
-                    call(side)
-        torch.cuda.synchronize()
-        return med_ms(g.replay, 5) / n * 1e3
-
-    # 1: single-tile copy, fp16 256 x 128, 128 x 64 tiles, 1 stage, 4 CTAs
-    x = synthetic.make_matrix(256, 128, "f16", "uniform", 1001, draw_on=str(dev))
-    y = torch.empty_like(x)
-    ms = med_ms(lambda: mbt.tile_copy(x, y, 128, 64, 1), 200)
-    us = graph_us(lambda st: mbt.tile_copy(x, y, 128, 64, 1, stream=st))
-    line({"config": 1, "op": "copy", "shape": [256, 128], "tile": [128, 64], "stages": 1,
-          "us_per_call_host_bound": round(ms * 1e3, 2), "us_per_call_device": round(us, 2),
-          "bytes": 2 * x.numel() * 2})
-    # 2: 3-stage pipeline, fp16 128 x 512, 1 CTA, 1 producer + 3 consumer warps
-    x = synthetic.make_matrix(128, 512, "f16", "uniform", 1002, draw_on=str(dev))
-    y = torch.empty_like(x)
-    ms = med_ms(lambda: mbt.tile_copy(x, y, 128, 64, 3, consumer_warps=3, max_ctas=1), 200)
-    us = graph_us(lambda st: mbt.tile_copy(x, y, 128, 64, 3, consumer_warps=3, max_ctas=1,
-                                           stream=st))
-    line({"config": 2, "op": "copy", "shape": [128, 512], "tile": [128, 64], "stages": 3,
-          "us_per_call_host_bound": round(ms * 1e3, 2), "us_per_call_device": round(us, 2),
-          "bytes": 2 * x.numel() * 2})
-    # 3: streaming copy, stage sweep, both store paths
-    x = synthetic.make_matrix(16384, 16384, "f16", "uniform", 1003, draw_on=str(dev))
-    y = torch.empty_like(x)
-    for mode in (2, 1):
-        for st in (1, 2, 3, 4, 6):
-            ms = med_ms(lambda: mbt.tile_copy(x, y, 128, 64, st, store_mode=mode), 20)
-            line({"config": 3, "op": "copy", "store_mode": MODE_NAME[mode], "shape": [16384, 16384],
-                  "tile": [128, 64], "stages": st, "ms": round(ms, 4),
-                  "gbs": round(copy_bytes() / ms / 1e6, 1)})
-    del x, y
-    # 4: row sums, stage sweep
-    x = synthetic.make_matrix(8192, 65536, "bf16", "normal", 1004, draw_on=str(dev))
-    o = torch.empty(8192, dtype=torch.float32, device=dev)
-    ws = torch.zeros(1 << 22, dtype=torch.uint8, device=dev)
-    for st in (2, 3, 4):
-        ms = med_ms(lambda: mbt.tile_rowsum(x, o, 64, 256, st, workspace=ws), 20)
-        line({"config": 4, "op": "rowsum", "shape": [8192, 65536], "tile": [64, 256],
-              "stages": st, "ms": round(ms, 4), "gbs": round(rowsum_bytes() / ms / 1e6, 1)})
-    # the second reduction of the same matrix: column sums
-    oc = torch.empty(65536, dtype=torch.float32, device=dev)
-    for st in (2, 3, 4):
-        ms = med_ms(lambda: mbt.tile_colsum(x, oc, 64, 256, st, workspace=ws), 20)
-        line({"config": 4, "op": "colsum", "shape": [8192, 65536], "tile": [64, 256],
-              "stages": st, "ms": round(ms, 4),
-              "gbs": round((8192 * 65536 * 2 + 4 * 65536) / ms / 1e6, 1)})
-    del x
-    # 5a / 5b: ragged, pitched rows, copy and row sum, 3 stages
-    for cfg, dt, M, N, tm, tn, seed in (("5a", "f32", 12289, 8191, 128, 32, 1005),
-                                        ("5b", "f16", 24577, 16383, 128, 64, 1006)):
-        ld = synthetic.pitched_ld(N, dt)
-        es = ESIZE[dt]
-        x = synthetic.make_matrix(M, N, dt, "uniform", seed, ld=ld, draw_on=str(dev))
-        y = torch.empty_like(x)
-        o = torch.empty(M, dtype=torch.float32, device=dev)
-        for mode in (2, 1):
-            ms = med_ms(lambda: mbt.tile_copy(x[:, :N], y[:, :N], tm, tn, 3, store_mode=mode), 20)
-            line({"config": cfg, "op": "copy", "store_mode": MODE_NAME[mode], "shape": [M, N], "ld": ld,
-                  "tile": [tm, tn], "stages": 3, "ms": round(ms, 4),
-                  "gbs": round(2 * M * N * es / ms / 1e6, 1)})
-        ms = med_ms(lambda: mbt.tile_rowsum(x[:, :N], o, tm, tn, 3, workspace=ws), 20)
-        line({"config": cfg, "op": "rowsum", "shape": [M, N], "ld": ld, "tile": [tm, tn],
-              "stages": 3, "ms": round(ms, 4), "gbs": round((M * N * es + 4 * M) / ms / 1e6, 1)})
-        oc = torch.empty(N, dtype=torch.float32, device=dev)
-        ms = med_ms(lambda: mbt.tile_colsum(x[:, :N], oc, tm, tn, 3, workspace=ws), 20)
-        line({"config": cfg, "op": "colsum", "shape": [M, N], "ld": ld, "tile": [tm, tn],
-              "stages": 3, "ms": round(ms, 4), "gbs": round((M * N * es + 4 * N) / ms / 1e6, 1)})
-        ms = med_ms(lambda: mbt.tile_copy_rowsum(x[:, :N], y[:, :N], o, tm, tn, 3,
-                                                 workspace=ws), 20)
-        line({"config": cfg, "op": "copy_rowsum (fused)", "shape": [M, N], "ld": ld,
-              "tile": [tm, tn], "stages": 3, "ms": round(ms, 4),
-              "gbs": round((2 * M * N * es + 4 * M) / ms / 1e6, 1)})
-        del x, y
-    line({"peak_gbs": peak, "peak_source": peak_kind, "theoretical_gbs": round(theo, 1)})
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    try:
+        for rec in config_sweep(dev, clocks, peak, theo):
+            print(json.dumps(rec), flush=True)
+    finally:
+        clocks.stop()
+    print(json.dumps({"peak_gbs": peak, "peak_source": peak_kind,
+                      "theoretical_gbs": round(theo, 1)}), flush=True)
 
 
 def bench_sweep(args):
@@ -957,6 +1061,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--all-configs", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="leave the per-configuration sweep out of the default line")
     ap.add_argument("--only", choices=["copy", "rowsum", "copy_rowsum", "colsum"])
     ap.add_argument("--trim-cols", type=int, default=0,
                     help="--only: drop this many columns (an odd count gives a dense matrix "

@@ -29,11 +29,15 @@
  *
  * Conventions common to every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller, except in
- *     the host-buffer forms (tile_copy_host, tile_rowsum_host).  Apart from
- *     those forms' staging pool, the library never allocates or frees device
- *     memory; it keeps only per-device caches (SM count, shared-memory limit,
- *     the driver's tensor-map encoder) and a small per-device status word
- *     (see tile_status).
+ *     the host-buffer forms (tile_copy_host, tile_rowsum_host).  The library
+ *     allocates device memory in two places only: the host-buffer forms'
+ *     staging pool, and the sum workspace it keeps per (device, stream) for
+ *     row and column sums called without a workspace of the caller's (see
+ *     tile_rowsum; allocated in stream order with cudaMallocAsync on the
+ *     first such call on a stream, freed by tile_workspace_release).  Besides
+ *     those it keeps per-device caches (SM count, shared-memory limit, the
+ *     driver's tensor-map encoder) and a small per-device status word (see
+ *     tile_status).  tile_rowsum_noalloc allocates nothing.
  *   - Matrices are row-major: element (i, j) is at ptr[i * ld + j], with the
  *     row pitch ld in elements.  The logical shape is M rows by N columns.
  *     Base pointers must be 16-byte aligned.  When ld * element size is a
@@ -91,7 +95,9 @@ typedef enum mbt_status {
     MBT_ERR_CUDA = -5,         /* a CUDA runtime call or the launch failed */
     MBT_ERR_TIMEOUT = -6,      /* a pipeline wait ran out of its time budget */
     MBT_ERR_DRIVER = -7,       /* tensor-map encoder unavailable or it refused */
-    MBT_ERR_WORKSPACE = -8     /* workspace given but smaller than required */
+    MBT_ERR_WORKSPACE = -8     /* workspace given but smaller than required, or
+                                  the library's own would have to be allocated
+                                  or grown during a stream capture */
 } mbt_status;
 
 /* Optional settings.  A zero-filled struct (or a NULL pointer) selects every
@@ -130,9 +136,10 @@ typedef struct mbt_opts {
     int32_t *log;            /* optional device buffer of int32 records, see
                                 below; NULL => no log */
     int64_t log_capacity;    /* records per role in `log` */
-    void *workspace;         /* tile_rowsum only: device scratch that lets
-                                several CTAs share one row band; NULL => every
-                                band is reduced by a single CTA */
+    void *workspace;         /* row and column sums: device scratch that lets
+                                several CTAs share one row band (column
+                                strip); NULL => the library's own workspace
+                                for (device, stream), unless no_split */
     size_t workspace_bytes;  /* size of `workspace` */
     int32_t fault;           /* test hook, 0 = none.  1: the producer starts at
                                 phase 0; 2: consumers never release a stage.
@@ -173,7 +180,13 @@ typedef struct mbt_opts {
                                 finished and clears it before reuse.  NULL =>
                                 the per-device word.  Must be 4-byte
                                 aligned. */
-    int32_t reserved[2];     /* must be 0 */
+    int32_t no_split;        /* row and column sums: 1 => every row band
+                                (column strip) is reduced by a single CTA and
+                                no workspace is used (workspace must be NULL);
+                                0 => bands (strips) may be split over several
+                                CTAs of a persistent grid.  Must be 0 for
+                                tile_copy. */
+    int32_t reserved1;       /* must be 0 */
 } mbt_opts;
 
 /* Launch plan, as computed by tile_plan (host only, no CUDA calls). */
@@ -256,11 +269,27 @@ int tile_copy_ex(const void *src, void *dst, int64_t M, int64_t N, int tile_m,
  *   src        device pointer, dense or pitched (opts->ld_src).
  *   out        device pointer to M floats (dense).
  *   M, N       >= 0.  N == 0 writes zeros; M == 0 does nothing.
- * Without a workspace each row band (tile_m rows) is reduced by one CTA;
- * with one (size from tile_rowsum_workspace_bytes, zero-filled before its
- * first use, and left zero-filled by every call that completes without a
- * timeout) the bands are split evenly over a persistent grid and the last
- * CTA of each band combines the partial sums.
+ * The bands' tiles are split evenly over a persistent grid and the last CTA
+ * to finish its part of a band adds the band's partial sums in CTA order.
+ * That needs a workspace (band tickets and partial sums).  tile_rowsum, and
+ * tile_rowsum_ex with opts->workspace NULL, use the library's own workspace
+ * for (current device, stream): allocated in stream order (cudaMallocAsync,
+ * then zero-filled) on the first such call on the stream, grown the same way
+ * when a larger plan needs more, and reused by every later call on that
+ * stream -- make the first call on a stream, for the largest shape, before
+ * any stream capture on it (an allocation during a capture would break the
+ * capture, so it returns MBT_ERR_WORKSPACE instead).  Calls on one stream are
+ * ordered, so they may share it; calls on different streams have their own.
+ * Free it with tile_workspace_release before destroying a stream whose
+ * handle a new stream could take while the old one's work is still running.
+ * A call that stops on a timed-out wait may leave band tickets set; the
+ * next call on the stream clears them (the workspace alternates two ticket
+ * sets, and each call zeroes the one it does not use).
+ * With a caller's workspace (opts->workspace; size from
+ * tile_rowsum_workspace_bytes, zero-filled before its first use, and left
+ * zero-filled by every call that completes without a timeout) the plan and
+ * the sums are the same, bit for bit.  opts->no_split = 1: each row band
+ * (tile_m rows) is reduced by one CTA, no workspace.
  */
 int tile_rowsum(const void *src, float *out, int64_t M, int64_t N, int tile_m,
                 int tile_n, int stages, int dtype, void *stream);
@@ -280,8 +309,9 @@ int tile_rowsum_ex(const void *src, float *out, int64_t M, int64_t N,
  * tensor stores of each row's whole 16-byte chunks; its lanes store a row's
  * partial chunk at column N) and the row-sum warps; each stage is released
  * when both the store and the row-sum warps are done with it.  Row sums are
- * bit-identical to tile_rowsum's with the same plan.  Workspace:
- * tile_copy_rowsum_workspace_bytes.
+ * bit-identical to tile_rowsum's with the same plan.  Workspace: as for
+ * tile_rowsum (the library's own unless opts->workspace is given; size for a
+ * caller's from tile_copy_rowsum_workspace_bytes).
  *   src, dst   as in tile_copy (opts->ld_src, opts->ld_dst; must not overlap
  *              unless equal); out as in tile_rowsum.
  * opts->store_mode must be 0.
@@ -308,11 +338,12 @@ int tile_copy_rowsum_ex(const void *src, void *dst, float *out, int64_t M, int64
  * repeated calls with the same plan give bit-identical sums.  The row pitch
  * must be a multiple of 16 bytes (MBT_ERR_ALIGN otherwise).
  *
- * opts: as for tile_rowsum_ex.  With a workspace (see
- * tile_colsum_workspace_bytes: tickets and partial sums per strip,
- * zero-filled, 256-byte aligned, left zero-filled) a strip may be split over
- * several CTAs; without one, each strip is reduced by a single CTA.  M = 0
- * writes N zeros; N = 0 writes nothing.
+ * opts: as for tile_rowsum_ex.  Strips may be split over several CTAs, with
+ * the caller's workspace (see tile_colsum_workspace_bytes: tickets and
+ * partial sums per strip, zero-filled, 256-byte aligned, left zero-filled)
+ * or, when opts->workspace is NULL, the library's own for (device, stream),
+ * exactly as tile_rowsum describes; opts->no_split = 1 reduces each strip
+ * on a single CTA.  M = 0 writes N zeros; N = 0 writes nothing.
  */
 int tile_colsum(const void *src, float *out, int64_t M, int64_t N, int tile_m,
                 int tile_n, int stages, int dtype, void *stream);
@@ -324,7 +355,8 @@ int tile_colsum_workspace_bytes(int64_t M, int64_t N, int tile_m, int tile_n,
                                 size_t *bytes);
 
 /* Workspace bytes tile_rowsum_ex needs on the current device for this shape
- * and these options (opts->workspace is ignored).  0 when no split helps. */
+ * and these options (opts->workspace is ignored).  0 when no split helps or
+ * opts->no_split is set. */
 int tile_rowsum_workspace_bytes(int64_t M, int64_t N, int tile_m, int tile_n,
                                 int stages, int dtype, const mbt_opts *opts,
                                 size_t *bytes);
@@ -353,9 +385,12 @@ int tile_copy_rowsum_workspace_bytes(int64_t M, int64_t N, int tile_m, int tile_
  * need no workspace are always accepted).  Otherwise as tile_rowsum_ex.
  *
  * Set-up: the first call on a device looks up the array's device address
- * (with that device current) and keeps it; make that first call before any
- * stream capture begins.  Every call clears the part of the array it uses
- * (an asynchronous memset on `stream`) before launching.
+ * (with that device current) and keeps it for the device's context (after
+ * cudaDeviceReset the next call looks it up again, and a call that fails
+ * with MBT_ERR_CUDA drops it); make that first call before any stream
+ * capture begins.  Every call clears the part of the array it uses (an
+ * asynchronous memset on `stream`) before launching, so a call after one
+ * that stopped on a timed-out wait starts clean.
  *
  * Sharing: every call on a device uses the same array, so calls whose work
  * overlaps on the GPU (different streams, or different host threads) race
@@ -436,6 +471,12 @@ int tile_colsum_host(const void *src, float *out, int64_t M, int64_t N, int tile
                      int tile_n, int stages, int dtype, const mbt_opts *opts);
 /* Frees the current device's idle staging sets of the host-buffer forms. */
 int tile_host_release(void);
+
+/* Frees, in stream order (cudaFreeAsync on `stream`), the sum workspace the
+ * library keeps for (current device, stream); the next row or column sum
+ * without a caller's workspace on that stream allocates a new one.  MBT_OK
+ * when there is none. */
+int tile_workspace_release(void *stream);
 
 /* Synchronises `stream`, then reads and clears the current device's status
  * word.  info (may be NULL) receives {code, block, stage, role * 2 + parity}

@@ -12,7 +12,6 @@ ctypes handle); the functions below take ``torch.Tensor`` arguments.
 from __future__ import annotations
 
 import ctypes
-from collections import OrderedDict
 import os
 import threading
 
@@ -26,6 +25,7 @@ __all__ = [
     "tile_copy", "tile_rowsum", "tile_colsum", "tile_copy_rowsum", "tile_rowsum_noalloc",
     "tile_rowsum_workspace_bytes", "tile_colsum_workspace_bytes",
     "tile_copy_host", "tile_rowsum_host", "tile_colsum_host", "tile_host_release",
+    "tile_workspace_release",
     "tile_status", "tile_plan", "tile_device_info", "tile_strerror", "tile_stage_image",
 ]
 
@@ -54,7 +54,8 @@ class Opts(ctypes.Structure):
         ("host_slab_rows", ctypes.c_int32),
         ("reserved0", ctypes.c_int32),
         ("status", ctypes.c_void_p),
-        ("reserved", ctypes.c_int32 * 2),
+        ("no_split", ctypes.c_int32),
+        ("reserved1", ctypes.c_int32),
     ]
 
 
@@ -146,12 +147,13 @@ def _load():
         lib.tile_rowsum_host.argtypes = host_sig
         lib.tile_colsum_host.argtypes = host_sig
         lib.tile_host_release.argtypes = []
+        lib.tile_workspace_release.argtypes = [vp]
         for name in ("tile_copy", "tile_copy_ex", "tile_rowsum", "tile_rowsum_ex",
                      "tile_copy_rowsum", "tile_copy_rowsum_ex",
                      "tile_rowsum_workspace_bytes", "tile_copy_rowsum_workspace_bytes",
                      "tile_plan", "tile_status", "tile_device_info",
                      "tile_copy_host", "tile_rowsum_host", "tile_colsum_host",
-                     "tile_host_release",
+                     "tile_host_release", "tile_workspace_release",
                      "tile_colsum", "tile_colsum_ex", "tile_colsum_workspace_bytes"):
             getattr(lib, name).restype = ctypes.c_int
         _C = lib
@@ -261,11 +263,6 @@ def tile_copy(src: torch.Tensor, dst: torch.Tensor, tile_m: int = 128, tile_n: i
     return dst
 
 
-_ws_lock = threading.Lock()
-_ws_cache: "OrderedDict[tuple[int, int], torch.Tensor]" = OrderedDict()
-_WS_CACHE_MAX = 16   # (device, stream) pairs kept; the least recently used goes first
-
-
 def _device_empty(n: int, device: torch.device, stream=None) -> torch.Tensor:
     """fp32[n] for a result, allocated on the stream that will write it (so the
     caching allocator orders any later reuse of the block after that work)."""
@@ -273,34 +270,16 @@ def _device_empty(n: int, device: torch.device, stream=None) -> torch.Tensor:
         return torch.empty(n, dtype=torch.float32, device=device)
 
 
-def _workspace(device: torch.device, nbytes: int, stream=None) -> torch.Tensor:
-    """A zero-filled byte buffer of at least ``nbytes`` on ``device``, reused
-    across calls on the same stream (the kernels leave it zero-filled; calls
-    on different streams may overlap, so each stream has its own)."""
-    idx = device.index if device.index is not None else torch.cuda.current_device()
-    key = (idx, _stream_handle(stream))
-    with _ws_lock:
-        buf = _ws_cache.get(key)
-        if buf is None or buf.numel() < nbytes:
-            # Allocated and zero-filled on the stream that will use it: the fill
-            # is ordered before the kernels, and once evicted the block is
-            # reused only by later work on that same stream.
-            with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
-                buf = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device)
-            _ws_cache[key] = buf
-        _ws_cache.move_to_end(key)
-        while len(_ws_cache) > _WS_CACHE_MAX:
-            _ws_cache.popitem(last=False)
-        return buf
-
-
-def _reset_workspaces() -> None:
-    """Zero every cached workspace (after a stalled call may have left tickets
-    or partials behind), finished before any later launch on any stream."""
-    with _ws_lock:
-        for buf in _ws_cache.values():
-            buf.zero_()
-    torch.cuda.synchronize()
+def _set_split(o: Opts, split: bool, workspace: torch.Tensor | None) -> None:
+    """Bands (strips) split over CTAs with the caller's workspace if given, else
+    with the library's own for (device, stream); ``split=False``: one CTA each."""
+    if not split:
+        if workspace is not None:
+            raise ValueError("workspace given with split=False")
+        o.no_split = 1
+    elif workspace is not None:
+        o.workspace = workspace.data_ptr()
+        o.workspace_bytes = workspace.numel() * workspace.element_size()
 
 
 def tile_rowsum_workspace_bytes(M: int, N: int, tile_m: int, tile_n: int, stages: int,
@@ -334,8 +313,9 @@ def tile_colsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int 
                 stream=None) -> torch.Tensor:
     """out[j] = sum_i src[i, j] in fp32 through the tile pipeline (tiles taken
     down each column strip).  With ``split`` (default) strips may be shared by
-    several CTAs, using a zero-filled workspace (cached per device and stream
-    unless one is given)."""
+    several CTAs, using ``workspace`` (zero-filled, see
+    :func:`tile_colsum_workspace_bytes`) or, if none is given, the library's
+    own for (device, stream)."""
     M, N, ld_s = _matrix(src, "src")
     if out is None:
         out = _device_empty(N, src.device, stream)
@@ -344,14 +324,7 @@ def tile_colsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int 
     o = _opts(ld_src=ld_s, consumer_warps=consumer_warps, max_ctas=max_ctas,
               ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault)
     _set_log_status(o, log, status, src.device)
-    if split and M > 0 and N > 0:
-        need = tile_colsum_workspace_bytes(M, N, tile_m, tile_n, stages, src.dtype,
-                                           ld_src=ld_s, consumer_warps=consumer_warps,
-                                           max_ctas=max_ctas, ctas_per_sm=ctas_per_sm)
-        if need:
-            ws = workspace if workspace is not None else _workspace(src.device, need, stream)
-            o.workspace = ws.data_ptr()
-            o.workspace_bytes = ws.numel() * ws.element_size()
+    _set_split(o, split, workspace)
     rc = _load().tile_colsum_ex(src.data_ptr(), out.data_ptr(), M, N, tile_m, tile_n, stages,
                                 DTYPE_CODE[src.dtype], _stream_handle(stream), ctypes.byref(o))
     _check(rc, "tile_colsum")
@@ -366,8 +339,9 @@ def tile_rowsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int 
                 status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """out[i] = sum_j src[i, j] in fp32 through the tile pipeline.
 
-    With ``split`` (default) row bands may be shared by several CTAs, using a
-    zero-filled workspace (cached per device unless one is given).
+    With ``split`` (default) row bands may be shared by several CTAs, using
+    ``workspace`` (zero-filled, see :func:`tile_rowsum_workspace_bytes`) or,
+    if none is given, the library's own for (device, stream).
     ``pipeline=2`` keeps one barrier pair per stage, ``pipeline=3`` gives
     every box of a stage its own pair where the tile allows it
     (``Plan.box_barriers``), 0 picks 3 for at most 2 stages; the sums are the
@@ -381,14 +355,7 @@ def tile_rowsum(src: torch.Tensor, out: torch.Tensor | None = None, tile_m: int 
               ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault,
               pipeline=pipeline)
     _set_log_status(o, log, status, src.device)
-    if split and M > 0 and N > 0:
-        need = tile_rowsum_workspace_bytes(M, N, tile_m, tile_n, stages, src.dtype,
-                                           ld_src=ld_s, consumer_warps=consumer_warps,
-                                           max_ctas=max_ctas, ctas_per_sm=ctas_per_sm)
-        if need:
-            ws = workspace if workspace is not None else _workspace(src.device, need, stream)
-            o.workspace = ws.data_ptr()
-            o.workspace_bytes = ws.numel() * ws.element_size()
+    _set_split(o, split, workspace)
     rc = _load().tile_rowsum_ex(src.data_ptr(), out.data_ptr(), M, N, tile_m, tile_n, stages,
                                 DTYPE_CODE[src.dtype], _stream_handle(stream), ctypes.byref(o))
     _check(rc, "tile_rowsum")
@@ -414,15 +381,7 @@ def tile_copy_rowsum(src: torch.Tensor, dst: torch.Tensor, out: torch.Tensor | N
     o = _opts(ld_src=ld_s, ld_dst=ld_d, consumer_warps=consumer_warps, max_ctas=max_ctas,
               ctas_per_sm=ctas_per_sm, wait_budget_ns=wait_budget_ns, fault=fault)
     _set_log_status(o, log, status, src.device)
-    if split and M > 0 and N > 0:
-        need = tile_rowsum_workspace_bytes(M, N, tile_m, tile_n, stages, src.dtype, fused=True,
-                                           ld_src=ld_s, ld_dst=ld_d,
-                                           consumer_warps=consumer_warps,
-                                           max_ctas=max_ctas, ctas_per_sm=ctas_per_sm)
-        if need:
-            ws = workspace if workspace is not None else _workspace(src.device, need, stream)
-            o.workspace = ws.data_ptr()
-            o.workspace_bytes = ws.numel() * ws.element_size()
+    _set_split(o, split, workspace)
     rc = _load().tile_copy_rowsum_ex(src.data_ptr(), dst.data_ptr(), out.data_ptr(), M, N,
                                      tile_m, tile_n, stages, DTYPE_CODE[src.dtype],
                                      _stream_handle(stream), ctypes.byref(o))
@@ -453,8 +412,6 @@ def tile_status(stream=None) -> tuple[int, list[int]]:
     Returns (code, [code, block, stage, role * 2 + parity])."""
     info = (ctypes.c_int32 * 4)()
     rc = _load().tile_status(_stream_handle(stream), info)
-    if rc == MBT_ERR_TIMEOUT:
-        _reset_workspaces()
     return rc, list(info)
 
 
@@ -557,3 +514,9 @@ def tile_colsum_host(src: torch.Tensor, out: torch.Tensor | None = None, tile_m:
 def tile_host_release() -> None:
     """Free the current device's idle staging memory of the host-buffer forms."""
     _check(_load().tile_host_release(), "tile_host_release")
+
+
+def tile_workspace_release(stream=None) -> None:
+    """Free (in stream order) the sum workspace the library keeps for the
+    current device and ``stream``."""
+    _check(_load().tile_workspace_release(_stream_handle(stream)), "tile_workspace_release")

@@ -62,6 +62,8 @@ struct RowsumArgs {
     float *out;
     float *partial;            // [bands][kmax][tile_m], used when kmax > 1
     int32_t *ticket;           // [bands], zero between calls
+    int32_t *clear_ticket;     // the library's own workspace: the other ticket
+    int64_t clear_n;           // set, zeroed by this call for the next (n words)
     int64_t units;             // scheduling units = num_tiles / gran
     int64_t gran;              // tiles per scheduling unit (1 or tiles_n)
     int32_t kmax;
@@ -123,6 +125,8 @@ struct ColsumArgs {
     float *out;                // [N]
     float *partial;            // [strips][kmax][tile_n], used when kmax > 1
     int32_t *ticket;           // [strips], zero between calls
+    int32_t *clear_ticket;     // as in RowsumArgs
+    int64_t clear_n;
     int64_t units;             // scheduling units = num_tiles / gran
     int64_t gran;              // tiles per scheduling unit (1 or tiles_m)
     int32_t kmax;

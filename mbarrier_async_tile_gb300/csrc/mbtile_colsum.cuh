@@ -298,6 +298,7 @@ __global__ void __launch_bounds__(kMaxThreads + 32, 2)
     }
     init_pipeline(a.p, sm, bars, &abort_flag, &flush_bar,
                   static_cast<uint32_t>(a.p.consumer_warps), dyn_smem);   // fences the inits
+    clear_next_tickets(a.clear_ticket, a.clear_n);
     WaitCtl w{a.p.wait_budget_ns, &abort_flag, status_of(a.p)};
     // Contiguous, evenly split range of scheduling units, in strip-major order.
     const int64_t G = gridDim.x;

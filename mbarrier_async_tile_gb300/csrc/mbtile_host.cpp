@@ -6,6 +6,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <thread>
 #include <tuple>
 
 #include "internal.h"
@@ -39,6 +40,9 @@ constexpr int64_t kFlatRowsumWindowBytes = 64 * 1024;
 constexpr int64_t kFlatRowsumBytesPerSm = 192 * 1024;
 constexpr int64_t kFlatMinRowsPerWindow = 8;
 constexpr int kMaxDevices = 64;
+// Smallest partial-sum area of the library's own workspace (most plans need
+// far less; growing it costs an allocation on the stream).
+constexpr int64_t kOwnedMinPartialBytes = 1 << 20;
 constexpr int64_t kMaxCoord = 0x7fffffff;  // bulk-copy coordinates are int32
 
 struct DeviceFigures {
@@ -97,9 +101,9 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
     if (o.pipeline >= 2 && op != MBT_OP_ROWSUM) return MBT_ERR_ARG;
     if (o.pipeline == 1 && o.store_mode == 1) return MBT_ERR_UNSUPPORTED;
     if (o.store_mode != 0 && op != MBT_OP_COPY) return MBT_ERR_ARG;
-    for (int r : o.reserved)
-        if (r != 0) return MBT_ERR_ARG;
-    if (o.reserved0 != 0) return MBT_ERR_ARG;
+    if (o.reserved0 != 0 || o.reserved1 != 0) return MBT_ERR_ARG;
+    if (o.no_split < 0 || o.no_split > 1) return MBT_ERR_ARG;
+    if (o.no_split && (op == MBT_OP_COPY || o.workspace != nullptr)) return MBT_ERR_ARG;
     if (reinterpret_cast<uintptr_t>(o.status) % 4 != 0) return MBT_ERR_ALIGN;
     if (o.host_slab_rows != 0) return MBT_ERR_ARG;   // host-buffer forms only
     if (o.log != nullptr && o.log_capacity == 0) return MBT_ERR_ARG;
@@ -659,6 +663,78 @@ int flat_launch(int op, const void *src, void *dst, float *out, int64_t M, int64
     return e == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
 }
 
+// The library's own sum workspace, for row and column sums called without one
+// (and without no_split): one buffer per (device, stream), allocated in stream
+// order on first use and grown when a plan needs more.  Layout: two ticket
+// sets of ticket_cap words each, then the partial sums.  Successive calls
+// alternate between the two sets; each call's kernel zeroes the set it does
+// not use (clear_next_tickets), so the next call on the stream starts from
+// zeroed tickets even if a call before it stopped on a timed-out wait.  The
+// partial slots need no clearing: a band's last contributor reads only slots
+// its co-contributors wrote in the same call.  The per-thread default stream
+// is a different stream in every host thread, so its key includes the thread.
+struct OwnedWorkspace {
+    char *base = nullptr;
+    int64_t ticket_cap = 0;     // words per ticket set (a multiple of 64)
+    size_t partial_bytes = 0;
+    uint64_t uses = 0;
+};
+
+std::mutex g_owned_mutex;
+std::map<std::tuple<int, uintptr_t, size_t>, OwnedWorkspace> g_owned;
+
+std::tuple<int, uintptr_t, size_t> owned_key(int dev, void *stream) {
+    const size_t thread =
+        stream == static_cast<void *>(cudaStreamPerThread)
+            ? std::hash<std::thread::id>()(std::this_thread::get_id())
+            : 0;
+    return std::make_tuple(dev, reinterpret_cast<uintptr_t>(stream), thread);
+}
+
+// Tickets for `groups` reduction groups and `partial_bytes` of partial sums
+// from the library's workspace for (current device, stream).
+int owned_workspace(void *stream, int64_t groups, size_t partial_bytes, int32_t **ticket,
+                    int32_t **clear, int64_t *clear_n, float **partial) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MBT_ERR_CUDA;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(g_owned_mutex);
+    OwnedWorkspace &w = g_owned[owned_key(dev, stream)];
+    if (w.base == nullptr || w.ticket_cap < groups || w.partial_bytes < partial_bytes) {
+        // Allocating inside a stream capture would end the capture with an error.
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return MBT_ERR_CUDA;
+        if (cap != cudaStreamCaptureStatusNone) return MBT_ERR_WORKSPACE;
+        OwnedWorkspace nw;
+        nw.ticket_cap = round_up(std::max<int64_t>({groups, w.ticket_cap, 64}), 64);
+        nw.partial_bytes = static_cast<size_t>(round_up(
+            static_cast<int64_t>(std::max({partial_bytes, w.partial_bytes,
+                                           static_cast<size_t>(kOwnedMinPartialBytes)})),
+            256));
+        const size_t total = static_cast<size_t>(2 * nw.ticket_cap * 4) + nw.partial_bytes;
+        void *p = nullptr;
+        if (cudaMallocAsync(&p, total, s) != cudaSuccess) return MBT_ERR_CUDA;
+        if (cudaMemsetAsync(p, 0, total, s) != cudaSuccess) {
+            cudaFreeAsync(p, s);
+            return MBT_ERR_CUDA;
+        }
+        // The old buffer served this stream only: freed after its last use.
+        if (w.base != nullptr && cudaFreeAsync(w.base, s) != cudaSuccess) {
+            cudaFreeAsync(p, s);
+            return MBT_ERR_CUDA;
+        }
+        nw.base = static_cast<char *>(p);
+        w = nw;
+    }
+    const int64_t parity = static_cast<int64_t>(w.uses++ & 1u);
+    int32_t *sets = reinterpret_cast<int32_t *>(w.base);
+    *ticket = sets + parity * w.ticket_cap;
+    *clear = sets + (1 - parity) * w.ticket_cap;
+    *clear_n = w.ticket_cap;
+    *partial = reinterpret_cast<float *>(w.base + 2 * w.ticket_cap * 4);
+    return MBT_OK;
+}
+
 // Row sums (and, with dst != nullptr, the fused copy) after argument checks.
 int rowsum_launch(const void *src, void *dst, float *out, int64_t M, int64_t N, int64_t ld_src,
                   int64_t ld_dst, int tile_m, int tile_n, int stages, int dtype, void *stream,
@@ -671,11 +747,13 @@ int rowsum_launch(const void *src, void *dst, float *out, int64_t M, int64_t N, 
                    : MBT_ERR_CUDA;
     }
     mbt_plan plan;
-    int rc = plan_on_device(op, M, N, tile_m, tile_n, stages, dtype, o, o.workspace != nullptr,
-                            &plan);
+    int rc = plan_on_device(op, M, N, tile_m, tile_n, stages, dtype, o, !o.no_split, &plan);
     if (rc != MBT_OK) return rc;
-    if (plan.split && o.workspace_bytes < plan.workspace_bytes) return MBT_ERR_WORKSPACE;
-    if (plan.split && (reinterpret_cast<uintptr_t>(o.workspace) & 255u) != 0) return MBT_ERR_ALIGN;
+    const bool own = plan.split && o.workspace == nullptr;
+    if (plan.split && !own) {
+        if (o.workspace_bytes < plan.workspace_bytes) return MBT_ERR_WORKSPACE;
+        if ((reinterpret_cast<uintptr_t>(o.workspace) & 255u) != 0) return MBT_ERR_ALIGN;
+    }
     alignas(64) CUtensorMap map;
     rc = encode_map(&map, src, M, N, ld_src, dtype, tile_m);
     if (rc != MBT_OK) return rc;
@@ -688,10 +766,17 @@ int rowsum_launch(const void *src, void *dst, float *out, int64_t M, int64_t N, 
     RowsumArgs a{};
     a.p = pipe_args(plan, M, N, tile_m, stages, dtype, o);
     a.out = out;
-    if (plan.split) {
+    if (own) {
+        rc = owned_workspace(stream, plan.tiles_m,
+                             plan.workspace_bytes - round_up(plan.tiles_m * 4, 256), &a.ticket,
+                             &a.clear_ticket, &a.clear_n, &a.partial);
+        if (rc != MBT_OK) return rc;
+    } else if (plan.split) {
         char *ws = static_cast<char *>(o.workspace);
         a.ticket = reinterpret_cast<int32_t *>(ws);
         a.partial = reinterpret_cast<float *>(ws + round_up(plan.tiles_m * 4, 256));
+    }
+    if (plan.split) {
         a.gran = 1;
         a.units = plan.num_tiles;
     } else {
@@ -721,11 +806,14 @@ int colsum_launch(const void *src, float *out, int64_t M, int64_t N, int64_t ld_
                    : MBT_ERR_CUDA;
     }
     mbt_plan plan;
-    int rc = plan_on_device(MBT_OP_COLSUM, M, N, tile_m, tile_n, stages, dtype, o,
-                            o.workspace != nullptr, &plan);
+    int rc = plan_on_device(MBT_OP_COLSUM, M, N, tile_m, tile_n, stages, dtype, o, !o.no_split,
+                            &plan);
     if (rc != MBT_OK) return rc;
-    if (plan.split && o.workspace_bytes < plan.workspace_bytes) return MBT_ERR_WORKSPACE;
-    if (plan.split && (reinterpret_cast<uintptr_t>(o.workspace) & 255u) != 0) return MBT_ERR_ALIGN;
+    const bool own = plan.split && o.workspace == nullptr;
+    if (plan.split && !own) {
+        if (o.workspace_bytes < plan.workspace_bytes) return MBT_ERR_WORKSPACE;
+        if ((reinterpret_cast<uintptr_t>(o.workspace) & 255u) != 0) return MBT_ERR_ALIGN;
+    }
     alignas(64) CUtensorMap map;
     rc = encode_map(&map, src, M, N, ld_src, dtype, tile_m);
     if (rc != MBT_OK) return rc;
@@ -733,10 +821,17 @@ int colsum_launch(const void *src, float *out, int64_t M, int64_t N, int64_t ld_
     a.p = pipe_args(plan, M, N, tile_m, stages, dtype, o);
     a.p.col_group = plan.col_group;
     a.out = out;
-    if (plan.split) {
+    if (own) {
+        rc = owned_workspace(stream, plan.tiles_n,
+                             plan.workspace_bytes - round_up(plan.tiles_n * 4, 256), &a.ticket,
+                             &a.clear_ticket, &a.clear_n, &a.partial);
+        if (rc != MBT_OK) return rc;
+    } else if (plan.split) {
         char *ws = static_cast<char *>(o.workspace);
         a.ticket = reinterpret_cast<int32_t *>(ws);
         a.partial = reinterpret_cast<float *>(ws + round_up(plan.tiles_n * 4, 256));
+    }
+    if (plan.split) {
         a.gran = 1;
         a.units = plan.num_tiles;
     } else {
@@ -763,7 +858,8 @@ int workspace_bytes(int op, int64_t M, int64_t N, int tile_m, int tile_n, int st
                         &ld_dst, &flat);
     if (rc != MBT_OK) return rc;
     *bytes = 0;
-    if (M == 0 || N == 0 || flat) return MBT_OK;   // flat row sums need no workspace
+    // flat row sums need no workspace, nor sums that are never split
+    if (M == 0 || N == 0 || flat || o.no_split) return MBT_OK;
     mbt_plan plan;
     rc = plan_on_device(op, M, N, tile_m, tile_n, stages, dtype, o, 1, &plan);
     if (rc != MBT_OK) return rc;
@@ -933,6 +1029,19 @@ int tile_stage_image(const void *src, int64_t M, int64_t N, int64_t ld, int tile
         map, static_cast<int32_t>(tile_row * tile_m), static_cast<int32_t>(tile_col * tile_n),
         boxes, mbt::kBoxRowBytes / es, box_bytes, box_stride, static_cast<unsigned char *>(image),
         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
+}
+
+int tile_workspace_release(void *stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MBT_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_owned_mutex);
+    auto it = g_owned.find(owned_key(dev, stream));
+    if (it == g_owned.end()) return MBT_OK;
+    const cudaError_t e =
+        it->second.base ? cudaFreeAsync(it->second.base, static_cast<cudaStream_t>(stream))
+                        : cudaSuccess;
+    g_owned.erase(it);
     return e == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;
 }
 

@@ -217,6 +217,7 @@ int host_run(int op, const void *src, void *dst, float *out, int64_t M, int64_t 
         rc = MBT_ERR_CUDA;
     dev_o.workspace = ws_bytes > 0 ? ws : nullptr;
     dev_o.workspace_bytes = ws_bytes;
+    if (ws_bytes == 0 && !is_copy) dev_o.no_split = 1;   // never the library's own workspace
     dev_o.status = status;   // this call's timeouts only
 
     const char *hsrc = static_cast<const char *>(src);

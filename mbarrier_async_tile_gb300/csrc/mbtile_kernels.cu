@@ -494,6 +494,19 @@ __device__ __forceinline__ void init_pipeline(const PipeArgs &p, Smem &sm,
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// The library's own sum workspace holds two ticket sets and successive calls
+// alternate between them: each call zeroes the set it does not use, spread
+// over every thread of its grid, right after init_pipeline (so before any wait
+// that could run out of time).  The next call, ordered after this one on the
+// stream, then starts from zeroed tickets even if a call before this one
+// stopped half way.  n == 0 (a caller's workspace, or none): nothing to do.
+__device__ __forceinline__ void clear_next_tickets(int32_t *t, int64_t n) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += stride)
+        t[i] = 0;
+}
+
 // ---------------------------------------------------------------------------
 // Copy
 // ---------------------------------------------------------------------------
@@ -1226,6 +1239,7 @@ __global__ void __launch_bounds__(kMaxThreads + 32, 2)
     }
     init_pipeline(a.p, sm, bars, &abort_flag, &flush_bar,
                   static_cast<uint32_t>(a.p.consumer_warps), dyn_smem, boxed);   // fences the inits
+    clear_next_tickets(a.clear_ticket, a.clear_n);
     WaitCtl w{a.p.wait_budget_ns, &abort_flag, status_of(a.p)};
     // Contiguous, evenly split range of scheduling units, in band-major order.
     const int64_t G = gridDim.x;

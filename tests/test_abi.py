@@ -158,10 +158,18 @@ def test_copy_tile_and_stage_errors():
 
 def test_option_errors():
     o = Opts()
-    o.reserved[1] = 1
+    o.reserved1 = 1
     assert _copy(A, B, 8, 64, opts=o) == -1
     o = Opts(); o.reserved0 = 1
     assert _copy(A, B, 8, 64, opts=o) == -1
+    # no_split: 0 or 1, row and column sums only, never with a workspace
+    o = Opts(); o.no_split = 1
+    assert _copy(A, B, 8, 64, opts=o) == -1
+    o = Opts(); o.no_split = 2
+    assert C.tile_rowsum_ex(A, B, 8, 64, 128, 64, 3, 0, None, ctypes.byref(o)) == -1
+    o = Opts(); o.no_split = 1; o.workspace = B; o.workspace_bytes = 256
+    assert C.tile_rowsum_ex(A, B, 8, 64, 128, 64, 3, 0, None, ctypes.byref(o)) == -1
+    assert C.tile_colsum_ex(A, B, 8, 64, 128, 64, 3, 0, None, ctypes.byref(o)) == -1
     o = Opts(); o.status = B + 2                   # a status buffer must be 4-byte aligned
     assert _copy(A, B, 8, 64, opts=o) == -2
     assert C.tile_rowsum_ex(A, B, 8, 64, 128, 64, 3, 0, None, ctypes.byref(o)) == -2

@@ -105,10 +105,12 @@ def test_stalled_pipeline_reports_timeout(fault, tile):
     assert code == mbt.MBT_ERR_TIMEOUT, info
     assert 0 <= info[1] < 4
     assert mbt.tile_status()[0] == 0
-    mbt._reset_workspaces()
-    out = mbt.tile_colsum(xd, None, 64, 256, 3)
-    assert mbt.tile_status()[0] == 0
-    assert colsum_errors(out, x)[0] <= ROWSUM_RTOL
+    # The stalled call used the library's own workspace of this stream and may
+    # have left strip tickets set; the calls after it start from zeroed ones.
+    for _ in range(3):
+        out = mbt.tile_colsum(xd, None, *tile, 3, max_ctas=4)
+        assert mbt.tile_status()[0] == 0
+        assert colsum_errors(out, x)[0] <= ROWSUM_RTOL
 
 
 def test_log_of_strip_pairs_walks_band_by_band():
@@ -185,7 +187,6 @@ def test_flush_ring_wraps_many_times(split):
     consumers post hundreds of strip groups through the two-slot flush ring."""
     for M, N, tm, tn in ((64, 262144, 64, 256), (100, 65536, 128, 64)):
         x = synthetic.make_matrix(M, N, "bf16", "normal", seed=M + 5)
-        mbt._reset_workspaces()
         out = mbt.tile_colsum(x.cuda(), None, tm, tn, 2, max_ctas=3, split=split)
         assert mbt.tile_status()[0] == 0
         assert colsum_errors(out, x)[0] <= ROWSUM_RTOL, (M, N)

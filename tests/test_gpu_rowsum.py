@@ -84,6 +84,35 @@ def test_one_workspace_shared_by_different_shapes():
         assert mbt.tile_status()[0] == 0
         assert rowsum_errors(out, x)[0] <= ROWSUM_RTOL, (M, N)
         assert int(ws.count_nonzero()) == 0
+        # the library's own workspace on a fresh stream, grown as the plans
+        # need more tickets or partial sums, gives the same bits
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        own = mbt.tile_rowsum(x.cuda(), None, tm, tn, 3, stream=s)
+        torch.cuda.synchronize()
+        assert mbt.tile_status()[0] == 0
+        assert torch.equal(own.view(torch.int32), out.view(torch.int32))
+
+
+def test_library_workspace_grows_across_shapes_on_one_stream():
+    """Shapes whose plans need more band tickets or partial sums than the
+    stream's workspace holds: it is replaced in stream order, and every call
+    (before and after the growth) gives the caller's-workspace bits."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    for M, N, tm, tn in [(300, 40000, 64, 256), (60000, 2048, 32, 256), (1000, 30000, 64, 256),
+                         (200000, 1024, 16, 512), (8192, 4096, 64, 256)]:
+        x = synthetic.make_matrix(M, N, "bf16", "normal", seed=M + 1)
+        xd = x.cuda()
+        need = mbt.tile_rowsum_workspace_bytes(M, N, tm, tn, 2, torch.bfloat16)
+        ws = torch.zeros(max(need, 256), dtype=torch.uint8, device="cuda")
+        want = mbt.tile_rowsum(xd, None, tm, tn, 2, workspace=ws)
+        torch.cuda.synchronize()
+        got = mbt.tile_rowsum(xd, None, tm, tn, 2, stream=s)
+        torch.cuda.synchronize()
+        assert mbt.tile_status()[0] == 0
+        assert torch.equal(got.view(torch.int32), want.view(torch.int32)), (M, N)
+        assert rowsum_errors(got, x)[0] <= ROWSUM_RTOL, (M, N)
 
 
 def test_log_of_one_cta_pipeline():
@@ -117,25 +146,90 @@ def test_full_size_configs(case):
         assert worst <= ROWSUM_RTOL, (st, worst, rel)
 
 
-def test_cached_workspaces_per_stream_are_ordered_and_bounded():
-    """The binding's cached workspace is allocated and zero-filled on the
-    stream that uses it (so the fill precedes the kernels there), one per
-    (device, stream), at most 16 kept."""
+def test_library_workspace_per_stream():
+    """Without a workspace of the caller's, each stream gets the library's
+    own (allocated and zero-filled in stream order on its first call): row
+    sums on 20 streams at once are right and bit-identical to the sums with a
+    caller's workspace; releasing a stream's workspace and calling again
+    allocates a fresh one."""
     x = synthetic.make_matrix(3000, 20000, "bf16", "normal", seed=17)
     xd = x.cuda()
+    need = mbt.tile_rowsum_workspace_bytes(3000, 20000, 64, 256, 2, torch.bfloat16)
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    want = mbt.tile_rowsum(xd, None, 64, 256, 2, workspace=ws)
     torch.cuda.synchronize()
-    mbt._ws_cache.clear()
     streams = [torch.cuda.Stream() for _ in range(20)]
     outs = []
-    for s in streams:
-        s.wait_stream(torch.cuda.current_stream())
-        outs.append(mbt.tile_rowsum(xd, None, 64, 256, 2, stream=s))
-    torch.cuda.synchronize()
+    for rep in range(2):
+        for s in streams:
+            s.wait_stream(torch.cuda.current_stream())
+            outs.append(mbt.tile_rowsum(xd, None, 64, 256, 2, stream=s))
+        torch.cuda.synchronize()
+        if rep == 0:
+            for s in streams[:5]:
+                mbt.tile_workspace_release(s)
     assert mbt.tile_status()[0] == 0
-    assert len(mbt._ws_cache) == 16
     for o in outs:
-        assert torch.equal(o.view(torch.int32), outs[0].view(torch.int32))
-    assert rowsum_errors(outs[0], x)[0] <= ROWSUM_RTOL
+        assert torch.equal(o.view(torch.int32), want.view(torch.int32))
+    assert rowsum_errors(want, x)[0] <= ROWSUM_RTOL
+    assert int(ws.count_nonzero()) == 0              # the caller's is left zero-filled
+
+
+def test_library_workspace_recovers_after_timeout():
+    """A stalled call on the library's workspace may leave band tickets set;
+    the workspace alternates two ticket sets and each call zeroes the one it
+    does not use, so every later call on the stream is right."""
+    M, N = 2048, 16384
+    x = synthetic.make_matrix(M, N, "bf16", "normal", seed=18)
+    xd = x.cuda()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    want = mbt.tile_rowsum(xd, None, 64, 256, 2, stream=s)
+    for fault in (2, 1, 2):
+        mbt.tile_rowsum(xd, None, 64, 256, 2, fault=fault, wait_budget_ns=20_000_000, stream=s)
+        code, info = mbt.tile_status(s)
+        assert code == mbt.MBT_ERR_TIMEOUT, info
+        for _ in range(3):
+            out = mbt.tile_rowsum(xd, None, 64, 256, 2, stream=s)
+            assert mbt.tile_status(s)[0] == 0
+            assert torch.equal(out.view(torch.int32), want.view(torch.int32))
+    assert rowsum_errors(want, x)[0] <= ROWSUM_RTOL
+
+
+def test_library_workspace_is_not_allocated_during_capture():
+    """The first call on a fresh stream inside a stream capture would have to
+    allocate: refused with MBT_ERR_WORKSPACE before anything is enqueued; after
+    a call outside the capture the same call captures and replays right."""
+    M, N = 1000, 20480
+    x = synthetic.make_matrix(M, N, "bf16", "normal", seed=19)
+    xd = x.cuda()
+    out = torch.empty(M, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        try:
+            rc = mbt.C.tile_rowsum(xd.data_ptr(), out.data_ptr(), M, N, 64, 256, 2,
+                                   mbt.DTYPE_CODE[xd.dtype], s.cuda_stream)
+        finally:
+            g.capture_end()
+    assert rc == -8
+    torch.cuda.synchronize()
+    mbt.tile_rowsum(xd, out, 64, 256, 2, stream=s)   # outside: allocates
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):                              # an odd count of calls
+            mbt.tile_rowsum(xd, out, 64, 256, 2, stream=s)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert mbt.tile_status()[0] == 0
+        assert rowsum_errors(out, x)[0] <= ROWSUM_RTOL
 
 
 @pytest.mark.parametrize("split", [False, True])
