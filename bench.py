@@ -35,6 +35,13 @@ COPY = dict(name="copy", dtype="f16", M=16384, N=16384, tile_m=128, tile_n=64,
 ROWSUM = dict(name="rowsum", dtype="bf16", M=8192, N=65536, tile_m=64, tile_n=256,
               dist="normal", seed=1004)
 ESIZE = {"f16": 2, "bf16": 2, "f32": 4}
+# The ragged task shapes, stored with a 16-byte row pitch (--only --config).
+RAGGED = {
+    "5a": dict(name="5a", dtype="f32", M=12289, N=8191, tile_m=128, tile_n=32, dist="uniform",
+               seed=1005),
+    "5b": dict(name="5b", dtype="f16", M=24577, N=16383, tile_m=128, tile_n=64,
+               dist="uniform", seed=1006),
+}
 FALLBACK_HBM_GBS = 6800.0
 MODE_NAME = {0: "default", 1: "bulk tensor stores", 2: "LSU stores"}
 GRAPH_CHUNK = 50   # steps per captured CUDA graph
@@ -662,35 +669,45 @@ def bench_only(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     c = ROWSUM if args.only in ("rowsum", "colsum") else COPY
+    if args.config:
+        c = RAGGED[args.config]
     rows = args.rows or c["M"]
     cols = args.cols or c["N"] - args.trim_cols
-    x = synthetic.make_matrix(rows, cols, c["dtype"], c["dist"], c["seed"], draw_on=str(dev))
+    ld = synthetic.pitched_ld(cols, c["dtype"]) if args.config else cols
+    x = synthetic.make_matrix(rows, cols, c["dtype"], c["dist"], c["seed"], ld=ld,
+                              draw_on=str(dev))[:, :cols]
+    def like_x():
+        return torch.empty(rows, ld, dtype=x.dtype, device=dev)[:, :cols]
+
     if args.only == "copy_rowsum":
-        y = torch.empty_like(x)
+        y = like_x()
         o = torch.empty(rows, dtype=torch.float32, device=dev)
         ws = torch.zeros(1 << 22, dtype=torch.uint8, device=dev)
         fn = lambda: mbt.tile_copy_rowsum(x, y, o, c["tile_m"], c["tile_n"],  # noqa: E731
                                           args.copy_stages, workspace=ws)
         nbytes = 2 * x.numel() * x.element_size() + 4 * rows
     elif args.only == "copy":
-        y = torch.empty_like(x)
+        y = like_x()
         fn = lambda: mbt.tile_copy(x, y, c["tile_m"], c["tile_n"], args.copy_stages,  # noqa: E731
                                    consumer_warps=args.consumer_warps,
-                                   ctas_per_sm=args.ctas_per_sm, store_mode=args.store_mode)
+                                   ctas_per_sm=args.ctas_per_sm, max_ctas=args.max_ctas,
+                                   store_mode=args.store_mode)
         nbytes = 2 * x.numel() * x.element_size()
     elif args.only == "colsum":
         y = torch.empty(cols, dtype=torch.float32, device=dev)
         ws = torch.zeros(1 << 22, dtype=torch.uint8, device=dev)
         fn = lambda: mbt.tile_colsum(x, y, c["tile_m"], c["tile_n"], args.rowsum_stages,  # noqa: E731
                                      consumer_warps=args.consumer_warps,
-                                     ctas_per_sm=args.ctas_per_sm, workspace=ws)
+                                     ctas_per_sm=args.ctas_per_sm, max_ctas=args.max_ctas,
+                                     workspace=ws)
         nbytes = x.numel() * x.element_size() + 4 * cols
     else:
         y = torch.empty(rows, dtype=torch.float32, device=dev)
         ws = torch.zeros(1 << 22, dtype=torch.uint8, device=dev)
         fn = lambda: mbt.tile_rowsum(x, y, c["tile_m"], c["tile_n"], args.rowsum_stages,  # noqa: E731
                                      consumer_warps=args.consumer_warps,
-                                     ctas_per_sm=args.ctas_per_sm, workspace=ws)
+                                     ctas_per_sm=args.ctas_per_sm, max_ctas=args.max_ctas,
+                                     workspace=ws)
         nbytes = x.numel() * x.element_size() + 4 * rows
     for _ in range(args.warmup):
         fn()
@@ -1064,6 +1081,9 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true",
                     help="leave the per-configuration sweep out of the default line")
     ap.add_argument("--only", choices=["copy", "rowsum", "copy_rowsum", "colsum"])
+    ap.add_argument("--config", choices=sorted(RAGGED),
+                    help="--only: one of the ragged task shapes (pitched rows) instead of "
+                         "the bench workload")
     ap.add_argument("--trim-cols", type=int, default=0,
                     help="--only: drop this many columns (an odd count gives a dense matrix "
                          "whose rows are not a multiple of 16 bytes: the 1-D bulk-copy path)")
@@ -1074,6 +1094,7 @@ def main(argv=None):
                          "multiple of 16 bytes takes the 1-D bulk-copy kernels)")
     ap.add_argument("--consumer-warps", type=int, default=0)
     ap.add_argument("--ctas-per-sm", type=int, default=0)
+    ap.add_argument("--max-ctas", type=int, default=0)
     ap.add_argument("--sweep-stages", type=int, nargs="*", default=[1, 2, 3, 4, 6])
     ap.add_argument("--sweep-warps", type=int, nargs="*", default=[3, 4, 7])
     ap.add_argument("--sweep-ctas", type=int, nargs="*", default=[1, 2, 0])

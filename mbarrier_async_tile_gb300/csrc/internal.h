@@ -13,6 +13,11 @@ namespace mbt {
 constexpr int kMaxStages = 8;
 constexpr int kMaxConsumerWarps = 8;
 constexpr int kMaxThreads = 32 * (1 + kMaxConsumerWarps);
+// Row and column sums with one CTA per SM (stages too large for two) run a
+// wide CTA instead: up to 16 consumer warps, in kernels built for one block
+// per SM (so the two-per-SM kernels keep their register budget).
+constexpr int kMaxWideConsumerWarps = 16;
+constexpr int kMaxWideThreads = 32 * (2 + kMaxWideConsumerWarps);
 constexpr int kBoxRowBytes = 128;      // one 128-byte swizzle span per box row
 constexpr int kSwizzleAtomBytes = 1024;
 constexpr uint64_t kDefaultWaitBudgetNs = 1000000000ull;  // 1 s
@@ -179,7 +184,8 @@ cudaError_t set_kernel_smem_limit(int optin, int *usable);
 // CTAs of a kernel with this block/smem shape that fit on one SM; kernel
 // MBT_OP_COPY, MBT_OP_ROWSUM, MBT_OP_COPY_ROWSUM, 3 = unified copy,
 // 4 = flat copy, 5 = flat row sum, 6 = column sum, 7 = copy with bulk stores,
-// 8 = row sum with a barrier pair per box.
+// 8 = row sum with a barrier pair per box, 9 = wide row sum, 10 = wide column
+// sum.
 cudaError_t kernel_fit_per_sm(int op, int dtype, int threads, int smem, int *fit);
 // Read the device status word and clear it (synchronous).
 cudaError_t read_and_clear_status(int32_t info[4]);

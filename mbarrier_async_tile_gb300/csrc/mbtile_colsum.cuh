@@ -28,6 +28,7 @@
 // file's PTX wrappers, bounded waits, producer, status word and log.
 
 constexpr int kColsumRedFloats = 32 * kMaxConsumerWarps * 8;   // threads x EPC (max)
+constexpr int kColsumWideRedFloats = 32 * kMaxWideConsumerWarps * 8;
 
 template <int DT>
 __device__ __forceinline__ void chunk_accumulate(float *acc, const uint4 &v) {
@@ -277,14 +278,16 @@ __device__ void consume_colsum(const ColsumArgs &a, const Smem &sm, const WaitCt
                               nthr);
 }
 
-template <int DT, int GMAX>
-__global__ void __launch_bounds__(kMaxThreads + 32, 2)
+// WIDE: up to 16 consumer warps, one CTA per SM.
+template <int DT, int GMAX, bool WIDE = false>
+__global__ void __launch_bounds__(WIDE ? kMaxWideThreads : kMaxThreads + 32, WIDE ? 1 : 2)
     mbt_colsum_kernel(const __grid_constant__ CUtensorMap map, const ColsumArgs a) {
     extern __shared__ __align__(1024) unsigned char dyn_smem[];
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
     __shared__ __align__(8) uint64_t flush_bar;
     __shared__ __align__(8) uint64_t ring_bars[2 * kFlushSlots];   // flush ring: full, empty
-    __shared__ float red[kColsumRedFloats];   // [tpc][tile_n] partial column sums
+    // [tpc][tile_n] partial column sums
+    __shared__ float red[WIDE ? kColsumWideRedFloats : kColsumRedFloats];
     __shared__ float ring_data[kFlushSlots * kColsumSlotFloats];
     __shared__ int64_t ring_key[kFlushSlots];
     __shared__ int abort_flag;

@@ -92,7 +92,10 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
     const int64_t row_bytes = static_cast<int64_t>(tile_n) * es;
     if (row_bytes != 128 && row_bytes != 256 && row_bytes != 512 && row_bytes != 1024)
         return MBT_ERR_UNSUPPORTED;
-    if (o.consumer_warps < 0 || o.consumer_warps > mbt::kMaxConsumerWarps) return MBT_ERR_ARG;
+    if (o.consumer_warps < 0 || o.consumer_warps > mbt::kMaxWideConsumerWarps) return MBT_ERR_ARG;
+    // more than 8 consumer warps: the wide row- and column-sum kernels only
+    if (o.consumer_warps > mbt::kMaxConsumerWarps && op != MBT_OP_ROWSUM && op != MBT_OP_COLSUM)
+        return MBT_ERR_ARG;
     if (o.ctas_per_sm < 0 || o.max_ctas < 0 || o.log_capacity < 0) return MBT_ERR_ARG;
     if (o.fault < 0 || o.fault > 2) return MBT_ERR_ARG;
     if (o.store_mode < 0 || o.store_mode > 2) return MBT_ERR_UNSUPPORTED;
@@ -134,6 +137,7 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
             (op == MBT_OP_COPY && *ld_src == N && *ld_dst == N && o.store_mode != 1 &&
              o.pipeline == 0);
         if (!flat_ok) return MBT_ERR_ALIGN;
+        if (o.consumer_warps > mbt::kMaxConsumerWarps) return MBT_ERR_ARG;   // 1-D kernels: <= 8
         if (flat) *flat = true;
         return MBT_OK;
     }
@@ -224,12 +228,20 @@ int wanted_ctas_per_sm(int op, const mbt_opts &o, int stages, int64_t stage_byte
 // two CTAs share an SM: measured on 32 KB tiles (bf16 64x256 and 32x512, fp16
 // 128x128), 4 warps beat 8 there by 1.5-2.9 %, while at 2 stages 8 beat 4 by
 // up to 4 %, and at 4 stages (wanted_ctas is never below 2, but only one such
-// CTA fits an SM) 4 warps lose a third.
+// CTA fits an SM) 4 warps lose a third.  Where only one CTA of the tiled row
+// sum runs on an SM (`one_per_sm`: its stages leave no room for a second, or
+// the caller asked for one), the wide kernel's 16 warps.  Measured on bf16
+// 64 x 256 tiles with one CTA per SM: the row sum runs at ~6.1 TB/s whatever
+// the stages (3 to 6) and 1 % faster with 16 warps than with 8; the column
+// sum at ~4.9 TB/s, 2 % slower with 16 (so it keeps 8 unless asked).  Two
+// CTAs of 8 at 2 stages: 6.6-6.8 TB/s for both.  The one-CTA ceiling does not
+// move with stages, consumer warps or the form of the barrier wait.
 int consumer_warps_for(int op, int tile_m, int stages, const mbt_opts &o, int wanted_ctas,
-                       int64_t n_mod, bool flat) {
+                       int64_t n_mod, bool flat, bool one_per_sm, bool wide_ok) {
     if (bulk_stores(op, o, n_mod)) return 1;   // one thread issues the stores
     if (o.consumer_warps) return o.consumer_warps;
     if (flat && op == MBT_OP_ROWSUM) return wanted_ctas <= 2 ? 8 : 4;   // no tile rows
+    if (op == MBT_OP_ROWSUM && one_per_sm && wide_ok) return mbt::kMaxWideConsumerWarps;
     if (op == MBT_OP_ROWSUM && wanted_ctas == 2 && stages == 3 && tile_m <= 128) return 4;
     if (op != MBT_OP_COPY) return (wanted_ctas <= 2 || tile_m > 128) ? 8 : 4;
     return kDefaultConsumerWarps;
@@ -384,6 +396,7 @@ constexpr int kBoxBarrierMaxStages = 2;
 bool box_barriers_apply(int op, int tile_m, int boxes, int W, int stages, const mbt_opts &o,
                         bool flat) {
     if (op != MBT_OP_ROWSUM || flat || boxes < 2 || boxes > 8) return false;
+    if (W > mbt::kMaxConsumerWarps) return false;   // the wide kernel has stage-wide pairs
     if (o.pipeline == 2 || (o.pipeline == 0 && stages > kBoxBarrierMaxStages)) return false;
     const int nthr = 32 * W;
     if (nthr % tile_m != 0) return false;
@@ -392,10 +405,12 @@ bool box_barriers_apply(int op, int tile_m, int boxes, int W, int stages, const 
     return (tile_m * (tpr / boxes)) % 32 == 0;
 }
 
+// fit_per_sm: CTAs of this plan's kernel that fit on one SM; 0 = not known yet
+// (a first pass, before the occupancy query: planned as if two fit).
 int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, int dtype,
               const mbt_opts &o, int num_sms, int smem_optin, int fit_per_sm,
               int with_workspace, mbt_plan *plan, bool flat = false) {
-    if (plan == nullptr || num_sms < 1 || fit_per_sm < 1) return MBT_ERR_ARG;
+    if (plan == nullptr || num_sms < 1 || fit_per_sm < 0) return MBT_ERR_ARG;
     const int es = esize_of(dtype);
     std::memset(plan, 0, sizeof *plan);
     plan->box_inner = mbt::kBoxRowBytes / es;
@@ -421,7 +436,12 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     }
     const int64_t n_mod = N % (16 / es);
     const int wanted = wanted_ctas_per_sm(op, o, stages, plan->stage_bytes, n_mod, flat);
-    const int W = consumer_warps_for(op, tile_m, stages, o, wanted, n_mod, flat);
+    const bool one_per_sm = wanted == 1 || fit_per_sm == 1;
+    // wide column sums walk one strip at a time (a split plan of 128-byte tiles
+    // walks two)
+    const bool wide_ok = op == MBT_OP_ROWSUM || !with_workspace || col_group_for(tile_n, es) == 1;
+    const int W = consumer_warps_for(op, tile_m, stages, o, wanted, n_mod, flat, one_per_sm,
+                                     wide_ok);
     plan->bulk_stores = bulk_stores(op, o, n_mod) || op == MBT_OP_COPY_ROWSUM ? 1 : 0;
     // Row sums: at least one thread per tile row; column sums: at least one
     // thread per 16-byte chunk column of a tile row.
@@ -444,7 +464,7 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     plan->tiles_m = ceil_div(M, tile_m);
     plan->tiles_n = ceil_div(N, tile_n);
     plan->num_tiles = plan->tiles_m * plan->tiles_n;
-    int64_t per_sm = std::min(wanted, fit_per_sm);
+    int64_t per_sm = fit_per_sm > 0 ? std::min(wanted, fit_per_sm) : wanted;
     int64_t cap = per_sm * num_sms;
     if (o.max_ctas) cap = std::min<int64_t>(cap, o.max_ctas);
     plan->flat = flat ? 1 : 0;
@@ -479,7 +499,8 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     const int64_t sums_per_group = cols ? tile_n : tile_m;
     if (with_workspace) {
         const int64_t G = std::min<int64_t>(plan->num_tiles, cap);
-        const int cg = cols ? col_group_for(tile_n, es) : 0;
+        // (the wide column sum walks one strip at a time)
+        const int cg = !cols ? 0 : W > mbt::kMaxConsumerWarps ? 1 : col_group_for(tile_n, es);
         const int32_t kmax =
             cols ? colsum_contributors(plan->tiles_m, plan->tiles_n, cg, plan->num_tiles, G)
                  : most_contributors(group_tiles, plan->num_tiles, G);
@@ -567,39 +588,61 @@ int encode_store_map(CUtensorMap *map, void *dst, int64_t M, int64_t N, int64_t 
     return encode_map(map, dst, M, n_whole, ld, dtype, tile_m);
 }
 
-// Plan for the current device (occupancy included).
+// Occupancy kernel id of a plan (see mbt::kernel_fit_per_sm).
+int kernel_id_of(int op, const mbt_opts &o, const mbt_plan &plan, bool flat) {
+    const bool wide = plan.consumer_warps > mbt::kMaxConsumerWarps;
+    return flat                                          ? (op == MBT_OP_COPY ? 4 : 5)
+           : op == MBT_OP_COLSUM                         ? (wide ? 10 : 6)
+           : op == MBT_OP_COPY && o.pipeline == 1        ? 3
+           : op == MBT_OP_COPY && plan.bulk_stores       ? 7
+           : op == MBT_OP_ROWSUM && wide                 ? 9
+           : op == MBT_OP_ROWSUM && plan.box_barriers    ? 8
+                                                         : op;
+}
+
+// Plan for the current device (occupancy included): a first pass without the
+// CTAs that fit an SM, the occupancy of its kernel, and the plan again with
+// it; when that picks another kernel (the wide sums where only one CTA fits),
+// its occupancy and a last pass.
 int plan_on_device(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, int dtype,
                    const mbt_opts &o, int with_workspace, mbt_plan *plan, bool flat = false) {
     DeviceFigures d;
     int rc = device_figures(&d);
     if (rc != MBT_OK) return rc;
-    rc = plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, d.num_sms, d.smem_optin, 1,
-                   with_workspace, plan, flat);
-    if (rc != MBT_OK) return rc;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MBT_ERR_CUDA;
-    const int kernel_id = flat                                  ? (op == MBT_OP_COPY ? 4 : 5)
-                          : op == MBT_OP_COLSUM                 ? 6
-                          : op == MBT_OP_COPY && o.pipeline == 1 ? 3
-                          : op == MBT_OP_COPY && plan->bulk_stores ? 7
-                          : op == MBT_OP_ROWSUM && plan->box_barriers ? 8
-                                                                : op;
-    const auto key = std::make_tuple(dev, kernel_id, op != MBT_OP_COPY ? dtype : 0,
-                                     plan->threads, plan->smem_bytes);
+    auto fit_of = [&](const mbt_plan &pl, int *fit) {
+        const int kernel_id = kernel_id_of(op, o, pl, flat);
+        const auto key = std::make_tuple(dev, kernel_id, op != MBT_OP_COPY ? dtype : 0,
+                                         pl.threads, pl.smem_bytes);
+        *fit = 0;
+        {
+            std::lock_guard<std::mutex> lock(g_mutex);
+            auto it = g_fit_cache.find(key);
+            if (it != g_fit_cache.end()) *fit = it->second;
+        }
+        if (*fit == 0) {
+            if (mbt::kernel_fit_per_sm(kernel_id, dtype, pl.threads, pl.smem_bytes, fit) !=
+                cudaSuccess)
+                return MBT_ERR_CUDA;
+            if (*fit < 1) return MBT_ERR_SMEM;
+            std::lock_guard<std::mutex> lock(g_mutex);
+            g_fit_cache[key] = *fit;
+        }
+        return MBT_OK;
+    };
+    rc = plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, d.num_sms, d.smem_optin, 0,
+                   with_workspace, plan, flat);
+    if (rc != MBT_OK) return rc;
     int fit = 0;
-    {
-        std::lock_guard<std::mutex> lock(g_mutex);
-        auto it = g_fit_cache.find(key);
-        if (it != g_fit_cache.end()) fit = it->second;
-    }
-    if (fit == 0) {
-        if (mbt::kernel_fit_per_sm(kernel_id, dtype, plan->threads, plan->smem_bytes, &fit) !=
-            cudaSuccess)
-            return MBT_ERR_CUDA;
-        if (fit < 1) return MBT_ERR_SMEM;
-        std::lock_guard<std::mutex> lock(g_mutex);
-        g_fit_cache[key] = fit;
-    }
+    rc = fit_of(*plan, &fit);
+    if (rc != MBT_OK) return rc;
+    const int threads = plan->threads;
+    rc = plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, d.num_sms, d.smem_optin, fit,
+                   with_workspace, plan, flat);
+    if (rc != MBT_OK || plan->threads == threads) return rc;
+    rc = fit_of(*plan, &fit);
+    if (rc != MBT_OK) return rc;
     return plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, d.num_sms, d.smem_optin, fit,
                      with_workspace, plan, flat);
 }

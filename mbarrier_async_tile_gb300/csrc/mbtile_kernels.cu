@@ -1019,6 +1019,7 @@ __device__ bool flush_band(const RowsumArgs &a, int64_t key, float acc, bool act
 // segment change no longer stall the pipeline.  Same arithmetic, same order
 // as flush_band.
 constexpr int kMaxConsumerThreads = 32 * kMaxConsumerWarps;
+constexpr int kMaxWideConsumerThreads = 32 * kMaxWideConsumerWarps;
 constexpr int kFlushSlots = 2;   // segments the consumers may run ahead
 
 struct FlushRing {
@@ -1032,6 +1033,8 @@ __device__ __forceinline__ uint32_t ring_slot(uint32_t k) { return k % kFlushSlo
 __device__ __forceinline__ uint32_t ring_parity(uint32_t k) { return (k / kFlushSlots) & 1u; }
 
 // Post a segment (key >= 0, red: this thread's share) or the end (key < 0).
+// CT: consumer threads a ring slot holds.
+template <int CT>
 __device__ bool flush_post(FlushRing &fr, float *red, float acc, int64_t key, int ctid,
                            const WaitCtl &w) {
     const uint32_t slot = ring_slot(fr.k);
@@ -1044,7 +1047,7 @@ __device__ bool flush_post(FlushRing &fr, float *red, float acc, int64_t key, in
         }
         return false;
     }
-    red[slot * kMaxConsumerThreads + ctid] = acc;
+    red[slot * CT + ctid] = acc;
     if (ctid == 0) fr.key[slot] = key;
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(fr.full0 + 8u * slot);
@@ -1056,6 +1059,7 @@ __device__ bool flush_post(FlushRing &fr, float *red, float acc, int64_t key, in
 // A band this CTA reduced alone gets its row sums written; otherwise the
 // CTA's partials go to its slot and the band's last contributor to arrive
 // adds the K slots in slot order (the order of flush_band).
+template <int CT>
 __device__ void flush_warp(const RowsumArgs &a, const float *red, FlushRing fr,
                            const WaitCtl &w) {
     const PipeArgs &p = a.p;
@@ -1074,7 +1078,7 @@ __device__ void flush_warp(const RowsumArgs &a, const float *red, FlushRing fr,
         }
         const int64_t key = fr.key[slot];
         if (key < 0) return;   // the consumers are done
-        const float *r = red + slot * kMaxConsumerThreads;
+        const float *r = red + slot * CT;
         const FlushTarget ft = flush_target(a, key);
         float *part = ft.K > 1 ? a.partial + (ft.band * a.kmax + ft.slot) * p.tile_m : nullptr;
         for (int row = lane; row < p.tile_m; row += 32) {
@@ -1114,7 +1118,7 @@ __device__ void flush_warp(const RowsumArgs &a, const float *red, FlushRing fr,
 // the per-box kernels give bit-identical sums.  With `boxed` (host-checked:
 // tpr a multiple of boxes, and the threads of one box whole warps) every warp
 // reads one box only, and waits for and releases that box alone.
-template <int DT, bool boxed, bool ring>
+template <int DT, bool boxed, bool ring, int CT>
 __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCtl &w,
                                const volatile StageInfo *info, float *red, int *last_flag,
                                FlushCtl &f, FlushRing &fr, int cwarp0) {
@@ -1157,7 +1161,7 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
         }
         if (k != key) {
             if (key >= 0 &&
-                !(ring ? flush_post(fr, red, acc, key, ctid, w)
+                !(ring ? flush_post<CT>(fr, red, acc, key, ctid, w)
                        : flush_band(a, key, acc, active, row, sub, tpr, red, last_flag, f, w,
                                     ctid))) {
                 ok = false;
@@ -1198,11 +1202,11 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
     if (!ok) return;
     if (key >= 0) {
         if (ring)
-            ok = flush_post(fr, red, acc, key, ctid, w);
+            ok = flush_post<CT>(fr, red, acc, key, ctid, w);
         else
             flush_band(a, key, acc, active, row, sub, tpr, red, last_flag, f, w, ctid);
     }
-    if (ring && ok) flush_post(fr, red, 0.f, -1, ctid, w);   // end mark for the flush warp
+    if (ring && ok) flush_post<CT>(fr, red, 0.f, -1, ctid, w);   // end mark for the flush warp
 }
 
 // FUSED: warp 1 writes every landed stage to dst (bulk tensor stores; LSU
@@ -1211,19 +1215,23 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
 // it, warp 1 is the flush warp (see flush_warp).
 // BOXED: a full/empty pair per (stage, box) (never with FUSED).  Each barrier
 // layout is its own instantiation, so neither carries the other's code.
-template <int DT, bool FUSED, bool BOXED>
-__global__ void __launch_bounds__(kMaxThreads + 32, 2)
+// WIDE: up to 16 consumer warps, one CTA per SM (stage-wide pairs, no store
+// warp).
+template <int DT, bool FUSED, bool BOXED, bool WIDE = false>
+__global__ void __launch_bounds__(WIDE ? kMaxWideThreads : kMaxThreads + 32, WIDE ? 1 : 2)
     mbt_rowsum_kernel(const __grid_constant__ CUtensorMap map,
                       const __grid_constant__ CUtensorMap dst_map, const RowsumArgs a) {
     extern __shared__ __align__(1024) unsigned char dyn_smem[];
     // Per-box barrier pairs only without the store warp (which reads whole stages).
     static_assert(!(FUSED && BOXED), "the store warp reads whole stages");
+    static_assert(!(WIDE && (FUSED || BOXED)), "wide CTAs: stage-wide pairs, no store warp");
     constexpr bool ring = !FUSED;
+    constexpr int CT = WIDE ? kMaxWideConsumerThreads : kMaxConsumerThreads;
     __shared__ __align__(8) uint64_t bars[BOXED ? 16 * kMaxStages : 2 * kMaxStages];
     __shared__ __align__(8) uint64_t flush_bar;
     __shared__ __align__(8) uint64_t ring_bars[2 * kFlushSlots];   // flush ring: full, empty
     // By row-sum consumer thread (one block per flush-ring slot without FUSED).
-    __shared__ float red[ring ? kFlushSlots * kMaxConsumerThreads : kMaxConsumerThreads];
+    __shared__ float red[ring ? kFlushSlots * CT : CT];
     __shared__ int abort_flag;
     __shared__ int last_flag;
     __shared__ StageInfo info[8 * kMaxStages];   // per (stage, box), from the producer
@@ -1259,12 +1267,12 @@ __global__ void __launch_bounds__(kMaxThreads + 32, 2)
             c.store_mode = 1;
             consume_copy_bulk(&dst_map, c, sm, w, 0, 0, 0, false, info);
         } else {
-            flush_warp(a, red, fr, w);
+            flush_warp<CT>(a, red, fr, w);
         }
         return;
     }
     FlushCtl f{smem_u32(&flush_bar), 0u};
-    consume_rowsum<DT, boxed, ring>(a, sm, w, info, red, &last_flag, f, fr, 2);
+    consume_rowsum<DT, boxed, ring, CT>(a, sm, w, info, red, &last_flag, f, fr, 2);
 }
 
 __global__ void mbt_accumulate_kernel(float *acc, const float *part, int64_t n, int first) {
@@ -1352,52 +1360,62 @@ cudaError_t launch_copy(const CUtensorMap &map, const CUtensorMap &dst_map, cons
     return launch_pipeline(mbt_copy_kernel<false>, grid, threads, smem, stream, map, dst_map, a);
 }
 
-template <bool FUSED, bool BOXED>
+template <bool FUSED, bool BOXED, bool WIDE = false>
 cudaError_t launch_rowsum_t(int dtype, const CUtensorMap &map, const CUtensorMap &dst_map,
                             const RowsumArgs &a, int grid, int threads, int smem,
                             cudaStream_t stream) {
     switch (dtype) {
         case MBT_F16:
-            return launch_pipeline(mbt_rowsum_kernel<MBT_F16, FUSED, BOXED>, grid, threads, smem,
-                                   stream, map, dst_map, a);
+            return launch_pipeline(mbt_rowsum_kernel<MBT_F16, FUSED, BOXED, WIDE>, grid, threads,
+                                   smem, stream, map, dst_map, a);
         case MBT_BF16:
-            return launch_pipeline(mbt_rowsum_kernel<MBT_BF16, FUSED, BOXED>, grid, threads, smem,
-                                   stream, map, dst_map, a);
+            return launch_pipeline(mbt_rowsum_kernel<MBT_BF16, FUSED, BOXED, WIDE>, grid, threads,
+                                   smem, stream, map, dst_map, a);
         default:
-            return launch_pipeline(mbt_rowsum_kernel<MBT_F32, FUSED, BOXED>, grid, threads, smem,
-                                   stream, map, dst_map, a);
+            return launch_pipeline(mbt_rowsum_kernel<MBT_F32, FUSED, BOXED, WIDE>, grid, threads,
+                                   smem, stream, map, dst_map, a);
     }
 }
 
 cudaError_t launch_rowsum(int dtype, const CUtensorMap &map, const CUtensorMap &dst_map,
                           const RowsumArgs &a, int grid, int threads, int smem,
                           cudaStream_t stream) {
+    const bool wide = a.p.consumer_warps > kMaxConsumerWarps;
+    if (wide && (a.fused || a.boxed)) return cudaErrorInvalidValue;
     if (a.fused)
         return launch_rowsum_t<true, false>(dtype, map, dst_map, a, grid, threads, smem, stream);
     if (a.boxed)
         return launch_rowsum_t<false, true>(dtype, map, dst_map, a, grid, threads, smem, stream);
+    if (wide)
+        return launch_rowsum_t<false, false, true>(dtype, map, dst_map, a, grid, threads, smem,
+                                                   stream);
     return launch_rowsum_t<false, false>(dtype, map, dst_map, a, grid, threads, smem, stream);
 }
 
-template <int GMAX>
+template <int GMAX, bool WIDE = false>
 cudaError_t launch_colsum_t(int dtype, const CUtensorMap &map, const ColsumArgs &a, int grid,
                             int threads, int smem, cudaStream_t stream) {
     switch (dtype) {
         case MBT_F16:
-            return launch_pipeline(mbt_colsum_kernel<MBT_F16, GMAX>, grid, threads, smem, stream,
-                                   map, a);
+            return launch_pipeline(mbt_colsum_kernel<MBT_F16, GMAX, WIDE>, grid, threads, smem,
+                                   stream, map, a);
         case MBT_BF16:
-            return launch_pipeline(mbt_colsum_kernel<MBT_BF16, GMAX>, grid, threads, smem, stream,
-                                   map, a);
+            return launch_pipeline(mbt_colsum_kernel<MBT_BF16, GMAX, WIDE>, grid, threads, smem,
+                                   stream, map, a);
         default:
-            return launch_pipeline(mbt_colsum_kernel<MBT_F32, GMAX>, grid, threads, smem, stream,
-                                   map, a);
+            return launch_pipeline(mbt_colsum_kernel<MBT_F32, GMAX, WIDE>, grid, threads, smem,
+                                   stream, map, a);
     }
 }
 
 cudaError_t launch_colsum(int dtype, const CUtensorMap &map, const ColsumArgs &a, int grid,
                           int threads, int smem, cudaStream_t stream) {
     if (a.p.col_group < 1 || a.p.col_group > kMaxColGroup) return cudaErrorInvalidValue;
+    const bool wide = a.p.consumer_warps > kMaxConsumerWarps;
+    if (wide) {   // planned for strips walked one at a time only
+        if (a.p.col_group != 1) return cudaErrorInvalidValue;
+        return launch_colsum_t<1, true>(dtype, map, a, grid, threads, smem, stream);
+    }
     if (a.p.col_group == 1) return launch_colsum_t<1>(dtype, map, a, grid, threads, smem, stream);
     return launch_colsum_t<2>(dtype, map, a, grid, threads, smem, stream);
 }
@@ -1478,7 +1496,13 @@ cudaError_t set_kernel_smem_limit(int optin, int *usable) {
                          reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F32, 1>),
                          reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F16, 2>),
                          reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_BF16, 2>),
-                         reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F32, 2>)};
+                         reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F32, 2>),
+                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16, false, false, true>),
+                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16, false, false, true>),
+                         reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32, false, false, true>),
+                         reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F16, 1, true>),
+                         reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_BF16, 1, true>),
+                         reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F32, 1, true>)};
     int least = optin;
     for (const void *fn : fns) {
         cudaFuncAttributes attr{};
@@ -1518,6 +1542,14 @@ cudaError_t kernel_fit_per_sm(int op, int dtype, int threads, int smem, int *fit
         fn = dtype == MBT_F16    ? reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F16, 2>)
              : dtype == MBT_BF16 ? reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_BF16, 2>)
                                  : reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F32, 2>);
+    if (op == 9)   // wide row sum
+        fn = dtype == MBT_F16    ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16, false, false, true>)
+             : dtype == MBT_BF16 ? reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16, false, false, true>)
+                                 : reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32, false, false, true>);
+    if (op == 10)  // wide column sum
+        fn = dtype == MBT_F16    ? reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F16, 1, true>)
+             : dtype == MBT_BF16 ? reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_BF16, 1, true>)
+                                 : reinterpret_cast<const void *>(mbt_colsum_kernel<MBT_F32, 1, true>);
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(fit, fn, threads, smem);
 }
 

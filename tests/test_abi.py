@@ -274,11 +274,41 @@ def test_plan_default_grid_follows_bytes_in_flight():
     p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16, fit=4, ws=True)
     assert p["grid"] == 304 and p["consumer_warps"] == 8
     # the same tiles at 3 stages (96 KB per CTA): still 2 CTAs, with 4 warps; at 4
-    # stages only one 128 KB CTA fits an SM, which keeps 8 warps
+    # stages only one 128 KB CTA fits an SM: the row sum's wide CTA of 16 consumer
+    # warps (+ producer and flush warps); the column sum keeps 8 unless asked
     p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 3, torch.bfloat16, fit=2, ws=True)
     assert p["grid"] == 304 and p["consumer_warps"] == 4
     p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True)
-    assert p["grid"] == 152 and p["consumer_warps"] == 8
+    assert p["grid"] == 152 and p["consumer_warps"] == 16 and p["threads"] == 32 * 18
+    assert p["box_barriers"] == 0
+    p = _plan(mbt.OP_COLSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True)
+    assert p["grid"] == 152 and p["consumer_warps"] == 8 and p["col_group"] == 1
+    p = _plan(mbt.OP_COLSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True,
+              consumer_warps=16)
+    assert p["threads"] == 32 * 18 and p["col_group"] == 1
+    # a caller's one CTA per SM gets the wide CTA too; 128-byte column-sum tiles
+    # walked in strip pairs, the fused operation and copies never do
+    p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16, fit=4, ws=True,
+              ctas_per_sm=1)
+    assert p["consumer_warps"] == 16
+    p = _plan(mbt.OP_COLSUM, 12289, 8191, 128, 32, 8, torch.float32, fit=1, ws=True,
+              ld_src=8192)
+    assert p["col_group"] == 2 and p["consumer_warps"] == 8
+    p = _plan(mbt.OP_COLSUM, 12289, 8191, 128, 32, 3, torch.float32, fit=1, ws=True,
+              ld_src=8192, consumer_warps=12)   # more than 8 warps: one strip at a time
+    assert p["col_group"] == 1 and p["consumer_warps"] == 12
+    p = _plan(mbt.OP_COPY_ROWSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True)
+    assert p["consumer_warps"] <= 8
+    assert _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 8, torch.float16)["consumer_warps"] == 4
+    # an explicit count above 8: row and column sums only, never the 1-D kernels
+    assert _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16, fit=1,
+                 consumer_warps=12)["threads"] == 32 * 14
+    with pytest.raises(mbt.MbtError):
+        _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 3, torch.float16, consumer_warps=9)
+    with pytest.raises(mbt.MbtError):
+        _plan(mbt.OP_ROWSUM, 1000, 63, 128, 64, 2, torch.float16, consumer_warps=9)
+    with pytest.raises(mbt.MbtError):
+        _plan(mbt.OP_ROWSUM, 100, 256, 64, 256, 2, torch.bfloat16, consumer_warps=17)
     # 3 stages of 256-row tiles: 4 warps cannot give each row a thread
     p = _plan(mbt.OP_ROWSUM, 16384, 32768, 256, 64, 3, torch.float16, fit=2, ws=True)
     assert p["consumer_warps"] == 8
@@ -348,8 +378,10 @@ def test_plan_errors_and_limits():
     with pytest.raises(mbt.MbtError) as e:
         _plan(mbt.OP_ROWSUM, 1024, 1024, 256, 64, 2, torch.float16, consumer_warps=4)
     assert e.value.code == -3
-    p = _plan(mbt.OP_ROWSUM, 1024, 1024, 256, 64, 2, torch.float16)
+    p = _plan(mbt.OP_ROWSUM, 1024, 1024, 256, 64, 2, torch.float16, fit=2)
     assert p["consumer_warps"] == 8
+    p = _plan(mbt.OP_ROWSUM, 1024, 1024, 256, 64, 2, torch.float16, fit=1)
+    assert p["consumer_warps"] == 16                 # one CTA per SM: the wide CTA
 
 
 def test_plan_rowsum_multibox_tile():

@@ -3,7 +3,8 @@ construction on one stream records its timed-out wait in its own buffer,
 while a clean call of the same kind on a second stream, running at the same
 time, finishes with its buffer and the per-device status word untouched.
 Covers every kernel family: LSU and bulk-store copies, the stage-wide and
-per-box row sums, the column sum, the fused copy + row sum, and the 1-D
+per-box row sums, the column sum, the wide (one CTA per SM) row and column
+sums, the fused copy + row sum, and the 1-D
 bulk-copy (unaligned pitch) copy and row sums.  The host-buffer forms use a
 buffer per staging set, so a stalled host call and clean host calls in other
 threads do not see one another's timeouts."""
@@ -43,6 +44,10 @@ CASES = {
         x, None, 64, 256, 3, consumer_warps=8, split=False, pipeline=3, **o), "rows"),
     "colsum": ("bf16", 512, 4096, lambda x, y, **o: mbt.tile_colsum(
         x, None, 64, 256, 3, split=False, **o), "cols"),
+    "rowsum_wide": ("bf16", 512, 4096, lambda x, y, **o: mbt.tile_rowsum(
+        x, None, 64, 256, 4, split=False, **o), "rows"),
+    "colsum_wide": ("bf16", 512, 4096, lambda x, y, **o: mbt.tile_colsum(
+        x, None, 64, 256, 4, split=False, **o), "cols"),
     "fused": ("bf16", 512, 4096, lambda x, y, **o: mbt.tile_copy_rowsum(
         x, y, None, 128, 64, 3, split=False, **o), "rows+copy"),
     "flat_copy": ("f16", 512, 1001, _copy(), "copy"),
