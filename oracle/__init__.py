@@ -10,6 +10,8 @@ Contents, each pinned by ``tests/test_oracle_*.py`` against what the pages fix:
 * ``copy``            -- the tile copy's result (plain C, ``oracle_ref.c``).
 * ``rowsum``          -- binary64 row sums (plain C, ``oracle_ref.c``).
 * ``colsum``          -- binary64 column sums (plain C, ``oracle_ref.c``).
+* ``xor_fold``        -- XOR of a buffer's 32-bit words (plain C): the result
+                         of the read-bandwidth reference.
 * ``f16_to_f64`` ...  -- exact element widening (plain C).
 * ``pipeline_state``  -- the (index, phase, count) ring cursor.
 * ``mbarrier``        -- the mbarrier phase / arrival / tx-count model.
@@ -80,6 +82,8 @@ def _load():
             lib.oracle_rowsum.restype = None
             lib.oracle_colsum.argtypes = lib.oracle_rowsum.argtypes
             lib.oracle_colsum.restype = None
+            lib.oracle_xor_fold.argtypes = [ctypes.c_void_p, ctypes.c_int64]
+            lib.oracle_xor_fold.restype = ctypes.c_uint32
             _lib = lib
     return _lib
 
@@ -143,3 +147,14 @@ def colsum(src: torch.Tensor, with_sumsq: bool = False):
                           sumsq.data_ptr() if with_sumsq else None,
                           M, N, src.stride(0), _DTYPE_CODE[src.dtype])
     return (sums, sumsq) if with_sumsq else sums
+
+
+def xor_fold(buf: torch.Tensor) -> int:
+    """XOR of all 32-bit little-endian words of a contiguous CPU tensor's
+    bytes (its byte count a multiple of 4)."""
+    if buf.device.type != "cpu" or not buf.is_contiguous():
+        raise ValueError("buf must be a contiguous CPU tensor")
+    nbytes = buf.numel() * buf.element_size()
+    if nbytes % 4:
+        raise ValueError("byte count must be a multiple of 4")
+    return int(_load().oracle_xor_fold(buf.data_ptr() if nbytes else None, nbytes // 4))

@@ -29,6 +29,11 @@
  *   oracle_bf16_to_f64 Exact widening of bfloat16: its 16 bits are the upper
  *                      half of an IEEE binary32 value.
  *   oracle_f32_to_f64  Exact widening of IEEE binary32.
+ *   oracle_xor_fold    Checksum of a byte buffer: the bitwise XOR of all its
+ *                      32-bit little-endian words.  Not on the pages: the
+ *                      result of the read-bandwidth reference that states the
+ *                      reductions' read-only roofline; XOR is associative and
+ *                      commutative, so any grouping gives this value.
  */
 #include <math.h>
 #include <stdint.h>
@@ -133,4 +138,17 @@ void oracle_colsum(const void *src, double *sums, double *sumsq, int64_t M,
                 sumsq[j] += x * x;
         }
     }
+}
+
+/* XOR of the n32 little-endian 32-bit words at src, one after the other. */
+uint32_t oracle_xor_fold(const unsigned char *src, int64_t n32)
+{
+    uint32_t x = 0;
+    for (int64_t k = 0; k < n32; ++k) {
+        const unsigned char *b = src + 4 * k;
+        uint32_t w = (uint32_t)b[0] | ((uint32_t)b[1] << 8) | ((uint32_t)b[2] << 16) |
+                     ((uint32_t)b[3] << 24);
+        x ^= w;
+    }
+    return x;
 }
