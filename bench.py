@@ -511,9 +511,10 @@ def bench_gpu(args, rank, world):
     # every configuration of the task's table and the stage sweep, each point
     # in its own clock window
     sweep = None
+    read_ref = read_reference(dev, clocks)
     if not args.no_sweep:
         theo = mbt.tile_device_info()["hbm_gbs_theoretical"]
-        sweep = config_sweep(dev, clocks, measured_peak()[0], theo)
+        sweep = config_sweep(dev, clocks, measured_peak()[0], theo, read_peak=read_ref["gbs"])
     time.sleep(0.15)
     clocks.stop()
     step_bytes = copy_bytes() + rowsum_bytes()
@@ -563,7 +564,10 @@ def bench_gpu(args, rank, world):
                            "ms_host_launched: the same launches from the host; kernels.*."
                            "ms_event_pairs: host launches with an event pair around each; "
                            "kernels.*.ms_in_one_stream_step: the two kernels alternating "
-                           "on one stream, where each inherits the other's L2 write-back")}
+                           "on one stream, where each inherits the other's L2 write-back"),
+                "read_peak": read_ref,
+                "frac_of_read_peak": (round(dom["gbs"] / read_ref["gbs"], 4)
+                                      if dom_name == "rowsum" else None)}
     out = {
         "metric": "achieved HBM GB/s (read+write) for pipelined tile copy + rowsum",
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -754,8 +758,60 @@ CONFIG_DIST = {"4": "normal"}
 POINT_TARGET_S = 0.25     # device time of each point's timed graph replays
 
 
+READ_REF_BYTES = 4 << 30   # the read reference's buffer: far larger than L2
+
+
+def read_reference(dev, clocks, target_s: float = POINT_TARGET_S) -> dict:
+    """The read-only ceiling of this device for the reductions: GB/s of
+    tile_read_checksum (one pass of 16-byte loads over a 4 GiB buffer, every
+    32-bit word folded into an XOR checksum), replayed from a CUDA graph of 10
+    launches for about `target_s`, one event pair around the replays, with
+    the clocks sampled meanwhile."""
+    import mbarrier_async_tile_gb300 as mbt
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    buf = torch.empty(READ_REF_BYTES, dtype=torch.uint8, device=dev)
+    out = torch.empty(1, dtype=torch.int32, device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    for _ in range(3):
+        mbt.tile_read_checksum(buf, out, stream=side)
+    torch.cuda.synchronize()
+    n = 10
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(n):
+            mbt.tile_read_checksum(buf, out, stream=side)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(side):
+        e0.record(side)
+        graph.replay()
+        e1.record(side)
+    torch.cuda.synchronize()
+    reps = max(3, int(target_s / max(e0.elapsed_time(e1) / 1e3, 1e-6)) + 1)
+    t0 = time.time()
+    with torch.cuda.stream(side):
+        e0.record(side)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(side)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    ms = e0.elapsed_time(e1) / (reps * n)
+    del graph, buf
+    torch.cuda.empty_cache()
+    c = clocks.summary(t0, t1)
+    return {"gbs": round(READ_REF_BYTES / ms / 1e6, 1), "ms": round(ms, 4),
+            "bytes": READ_REF_BYTES, "kernel": "mbt_read_checksum_kernel",
+            "what": ("tile_read_checksum: one pass of 16-byte loads over a 4 GiB device buffer "
+                     "(XOR of every 32-bit word), graph replay, mean per launch"),
+            "launches_timed": reps * n,
+            "clocks": {"sm_mhz": c.get("sm_mhz"), "sm_max_mhz": c.get("sm_max_mhz"),
+                       "reasons": c.get("reasons"), "samples": c.get("samples")}}
+
+
 def config_sweep(dev, clocks, peak: float, theo: float, target_s: float = POINT_TARGET_S,
-                 select=None):
+                 select=None, read_peak: float | None = None):
     """Time every CONFIG_POINTS entry (or those `select` keeps) on one side
     stream: the calls captured in a CUDA graph (20 launches, 200 for the
     latency-bound lesson shapes), replayed until about `target_s` of device
@@ -900,6 +956,8 @@ def config_sweep(dev, clocks, peak: float, theo: float, target_s: float = POINT_
             gbs = nbytes / ms / 1e6
             rec.update(ms=round(ms, 4), gbs=round(gbs, 1), frac=round(gbs / peak, 4),
                        frac_theoretical=round(gbs / theo, 4) if theo else None,
+                       frac_of_read_peak=(round(gbs / read_peak, 4)
+                                          if read_peak and op in ("rowsum", "colsum") else None),
                        ms_host_launched=round(ms_host, 4),
                        gbs_host_launched=round(nbytes / ms_host / 1e6, 1))
         rec["launches_timed"] = reps * n_graph
@@ -927,7 +985,9 @@ def bench_configs(args):
     clocks.start()
     time.sleep(0.3)
     try:
-        for rec in config_sweep(dev, clocks, peak, theo):
+        ref = read_reference(dev, clocks)
+        print(json.dumps({"read_reference": ref}), flush=True)
+        for rec in config_sweep(dev, clocks, peak, theo, read_peak=ref["gbs"]):
             print(json.dumps(rec), flush=True)
     finally:
         clocks.stop()

@@ -478,6 +478,24 @@ int tile_host_release(void);
  * when there is none. */
 int tile_workspace_release(void *stream);
 
+/*
+ * tile_read_checksum -- the read-bandwidth reference of the reductions:
+ * *out = the XOR of all 32-bit words of the `bytes` bytes at src (a device
+ * buffer, read once with 16-byte loads by a grid of whole CTAs per SM).
+ *
+ * Not an operation of the pages: row and column sums read their matrix and
+ * write only its sums, so the copy's read + write bandwidth is not their
+ * ceiling; the benchmark times this call on a buffer far larger than L2 and
+ * states the sums' fraction of it beside their fraction of the copy peak.
+ *   src    device pointer, 16-byte aligned; bytes a multiple of 16
+ *          (MBT_ERR_ALIGN otherwise).  bytes == 0 gives 0.
+ *   out    device pointer to one uint32, 4-byte aligned, overwritten (set to 0
+ *          on `stream`, then XORed into by the kernel).
+ * Asynchronous on `stream`.  Returns MBT_OK, MBT_ERR_ARG (out NULL or
+ * misaligned, src NULL with bytes > 0), MBT_ERR_ALIGN or MBT_ERR_CUDA.
+ */
+int tile_read_checksum(const void *src, size_t bytes, uint32_t *out, void *stream);
+
 /* Synchronises `stream`, then reads and clears the current device's status
  * word.  info (may be NULL) receives {code, block, stage, role * 2 + parity}
  * of the first wait that timed out (role 0 = producer, 1 = consumer).

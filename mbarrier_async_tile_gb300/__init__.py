@@ -25,7 +25,7 @@ __all__ = [
     "tile_copy", "tile_rowsum", "tile_colsum", "tile_copy_rowsum", "tile_rowsum_noalloc",
     "tile_rowsum_workspace_bytes", "tile_colsum_workspace_bytes",
     "tile_copy_host", "tile_rowsum_host", "tile_colsum_host", "tile_host_release",
-    "tile_workspace_release",
+    "tile_workspace_release", "tile_read_checksum",
     "tile_status", "tile_plan", "tile_device_info", "tile_strerror", "tile_stage_image",
 ]
 
@@ -148,12 +148,13 @@ def _load():
         lib.tile_colsum_host.argtypes = host_sig
         lib.tile_host_release.argtypes = []
         lib.tile_workspace_release.argtypes = [vp]
+        lib.tile_read_checksum.argtypes = [vp, ctypes.c_size_t, vp, vp]
         for name in ("tile_copy", "tile_copy_ex", "tile_rowsum", "tile_rowsum_ex",
                      "tile_copy_rowsum", "tile_copy_rowsum_ex",
                      "tile_rowsum_workspace_bytes", "tile_copy_rowsum_workspace_bytes",
                      "tile_plan", "tile_status", "tile_device_info",
                      "tile_copy_host", "tile_rowsum_host", "tile_colsum_host",
-                     "tile_host_release", "tile_workspace_release",
+                     "tile_host_release", "tile_workspace_release", "tile_read_checksum",
                      "tile_colsum", "tile_colsum_ex", "tile_colsum_workspace_bytes"):
             getattr(lib, name).restype = ctypes.c_int
         _C = lib
@@ -520,3 +521,19 @@ def tile_workspace_release(stream=None) -> None:
     """Free (in stream order) the sum workspace the library keeps for the
     current device and ``stream``."""
     _check(_load().tile_workspace_release(_stream_handle(stream)), "tile_workspace_release")
+
+
+def tile_read_checksum(buf: torch.Tensor, out: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """XOR of all 32-bit words of a contiguous CUDA tensor's bytes (the
+    read-bandwidth reference, see include/mbtile.h); returns an int32[1]
+    device tensor holding the checksum's bits."""
+    if buf.device.type != "cuda" or not buf.is_contiguous():
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    if out is None:
+        with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
+            out = torch.empty(1, dtype=torch.int32, device=buf.device)
+    rc = _load().tile_read_checksum(buf.data_ptr(), buf.numel() * buf.element_size(),
+                                    out.data_ptr(), _stream_handle(stream))
+    _check(rc, "tile_read_checksum")
+    return out

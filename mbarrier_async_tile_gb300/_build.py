@@ -15,7 +15,8 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libmbtile.so")
-SOURCES = ["mbtile_kernels.cu", "mbtile_host.cpp", "mbtile_noalloc.cu", "mbtile_hostio.cpp"]
+SOURCES = ["mbtile_kernels.cu", "mbtile_host.cpp", "mbtile_noalloc.cu", "mbtile_hostio.cpp",
+           "mbtile_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE]
 
