@@ -419,6 +419,17 @@ int tile_plan(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages,
               int fit_per_sm, int with_workspace, mbt_plan *plan);
 
 /*
+ * tile_plan_device -- the plan a call of op (MBT_OP_*) with these arguments
+ * runs on the current device: tile_plan with the device's SM count, shared
+ * memory and the occupancy of the kernel the plan picks; row and column sums
+ * planned as the call plans them (bands or strips split unless
+ * opts->no_split).  Returns the argument errors of the calls, or
+ * MBT_ERR_CUDA.
+ */
+int tile_plan_device(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages,
+                     int dtype, const mbt_opts *opts, mbt_plan *plan);
+
+/*
  * tile_stage_image -- debug: the raw shared-memory image of one staged tile.
  *
  * Loads tile (tile_row, tile_col) of src (M x N, row pitch ld elements, which

@@ -26,7 +26,8 @@ __all__ = [
     "tile_rowsum_workspace_bytes", "tile_colsum_workspace_bytes",
     "tile_copy_host", "tile_rowsum_host", "tile_colsum_host", "tile_host_release",
     "tile_workspace_release", "tile_read_checksum",
-    "tile_status", "tile_plan", "tile_device_info", "tile_strerror", "tile_stage_image",
+    "tile_status", "tile_plan", "tile_plan_device", "tile_device_info", "tile_strerror",
+    "tile_stage_image",
 ]
 
 MBT_OK = 0
@@ -131,6 +132,8 @@ def _load():
                                                          ctypes.POINTER(ctypes.c_size_t)]
         lib.tile_plan.argtypes = [i32, i64, i64, i32, i32, i32, i32, ctypes.POINTER(Opts),
                                   i32, i32, i32, i32, ctypes.POINTER(Plan)]
+        lib.tile_plan_device.argtypes = [i32, i64, i64, i32, i32, i32, i32,
+                                         ctypes.POINTER(Opts), ctypes.POINTER(Plan)]
         lib.tile_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
         lib.tile_strerror.argtypes = [i32]
         lib.tile_strerror.restype = ctypes.c_char_p
@@ -152,7 +155,7 @@ def _load():
         for name in ("tile_copy", "tile_copy_ex", "tile_rowsum", "tile_rowsum_ex",
                      "tile_copy_rowsum", "tile_copy_rowsum_ex",
                      "tile_rowsum_workspace_bytes", "tile_copy_rowsum_workspace_bytes",
-                     "tile_plan", "tile_status", "tile_device_info",
+                     "tile_plan", "tile_plan_device", "tile_status", "tile_device_info",
                      "tile_copy_host", "tile_rowsum_host", "tile_colsum_host",
                      "tile_host_release", "tile_workspace_release", "tile_read_checksum",
                      "tile_colsum", "tile_colsum_ex", "tile_colsum_workspace_bytes"):
@@ -425,6 +428,17 @@ def tile_plan(op: int, M: int, N: int, tile_m: int, tile_n: int, stages: int,
                            ctypes.byref(o), num_sms, smem_optin, fit_per_sm,
                            int(with_workspace), ctypes.byref(p))
     _check(rc, "tile_plan")
+    return p.as_dict()
+
+
+def tile_plan_device(op: int, M: int, N: int, tile_m: int, tile_n: int, stages: int,
+                     dtype: torch.dtype, **opt) -> dict:
+    """The plan the call would run on the current device (see include/mbtile.h)."""
+    o = _opts(**opt)
+    p = Plan()
+    rc = _load().tile_plan_device(op, M, N, tile_m, tile_n, stages, DTYPE_CODE[dtype],
+                                  ctypes.byref(o), ctypes.byref(p))
+    _check(rc, "tile_plan_device")
     return p.as_dict()
 
 

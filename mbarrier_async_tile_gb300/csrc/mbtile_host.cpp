@@ -929,6 +929,21 @@ int tile_plan(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
                      with_workspace, plan, flat);
 }
 
+int tile_plan_device(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages,
+                     int dtype, const mbt_opts *opts, mbt_plan *plan) {
+    if (plan == nullptr) return MBT_ERR_ARG;
+    const mbt_opts o = opts_or_default(opts);
+    int64_t ld_src = 0, ld_dst = 0;
+    static const char dummy[16] __attribute__((aligned(16))) = {0};
+    bool flat = false;
+    int rc = check_args(op, dummy, dummy, M, N, tile_m, tile_n, stages, dtype, o, &ld_src,
+                        &ld_dst, &flat);
+    if (rc != MBT_OK) return rc;
+    const bool sums = op != MBT_OP_COPY;
+    return plan_on_device(op, M, N, tile_m, tile_n, stages, dtype, o,
+                          sums && !o.no_split ? 1 : 0, plan, flat);
+}
+
 int tile_copy_ex(const void *src, void *dst, int64_t M, int64_t N, int tile_m, int tile_n,
                  int stages, int dtype, void *stream, const mbt_opts *opts) {
     const mbt_opts o = opts_or_default(opts);

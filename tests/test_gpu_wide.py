@@ -23,12 +23,9 @@ def setup():
 
 
 def _plan(op, M, N, tm, tn, st, dtype, **opt):
-    """The plan the device call makes (the real device's occupancy: a 4-stage
-    ring of 32 KB tiles leaves room for one CTA per SM)."""
-    info = mbt.tile_device_info()
-    return mbt.tile_plan(op, M, N, tm, tn, st, dtype, num_sms=info["num_sms"],
-                         smem_optin=info["smem_optin"], fit_per_sm=1, with_workspace=True,
-                         **opt)
+    """The plan the device call makes (tile_plan_device: the real device's
+    occupancy; a 4-stage ring of 32 KB tiles leaves room for one CTA per SM)."""
+    return mbt.tile_plan_device(op, M, N, tm, tn, st, dtype, **opt)
 
 
 CASES = [
@@ -96,3 +93,15 @@ def test_wide_full_size_colsum_sampled():
         w = 256 if c0 in (0, N - 256) else 8
         block = x[:, c0:c0 + w].cpu().contiguous()
         assert colsum_errors(out[c0:c0 + w], block)[0] <= ROWSUM_RTOL, c0
+
+
+def test_device_plan_of_the_sweep_points():
+    """tile_plan_device on the bench's row-sum tiles: 2 CTAs of 8 consumer
+    warps per SM at 2 stages (bands split), one wide CTA per SM at 4."""
+    sms = mbt.tile_device_info()["num_sms"]
+    p2 = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16)
+    assert p2["grid"] == 2 * sms and p2["consumer_warps"] == 8 and p2["split"] == 1
+    p4 = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 4, torch.bfloat16)
+    assert p4["grid"] == sms and p4["consumer_warps"] == 16
+    whole = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16, no_split=1)
+    assert whole["split"] == 0 and whole["grid"] == 128
