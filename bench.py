@@ -51,8 +51,8 @@ GRAPH_CHUNK = 50   # steps per captured CUDA graph
 # code it was taken on (kernel_source_sha); reported only while that code is
 # unchanged.
 NCU_TRAFFIC: dict = {
-    "copy": {"src_sha": "a0a3bd16d02bc554", "bytes_per_launch": 537033728 + 485258752},
-    "rowsum": {"src_sha": "a0a3bd16d02bc554", "bytes_per_launch": 1073842688 + 2991616},
+    "copy": {"src_sha": "7426ce850d4d255d", "bytes_per_launch": 537029632 + 484311296},
+    "rowsum": {"src_sha": "7426ce850d4d255d", "bytes_per_launch": 1073834240 + 3081472},
 }
 
 def copy_bytes(c=COPY):
@@ -511,10 +511,11 @@ def bench_gpu(args, rank, world):
     # every configuration of the task's table and the stage sweep, each point
     # in its own clock window
     sweep = None
-    read_ref = read_reference(dev, clocks)
+    read_ref = None if args.no_read_ref else read_reference(dev, clocks)
     if not args.no_sweep:
         theo = mbt.tile_device_info()["hbm_gbs_theoretical"]
-        sweep = config_sweep(dev, clocks, measured_peak()[0], theo, read_peak=read_ref["gbs"])
+        sweep = config_sweep(dev, clocks, measured_peak()[0], theo,
+                             read_peak=read_ref["gbs"] if read_ref else None)
     time.sleep(0.15)
     clocks.stop()
     step_bytes = copy_bytes() + rowsum_bytes()
@@ -567,7 +568,9 @@ def bench_gpu(args, rank, world):
                            "on one stream, where each inherits the other's L2 write-back"),
                 "read_peak": read_ref,
                 "frac_of_read_peak": (round(dom["gbs"] / read_ref["gbs"], 4)
-                                      if dom_name == "rowsum" else None)}
+                                      if dom_name == "rowsum" and read_ref else None),
+                "rowsum_frac_of_read_peak": (round(kernels["rowsum"]["gbs"] / read_ref["gbs"], 4)
+                                             if read_ref else None)}
     out = {
         "metric": "achieved HBM GB/s (read+write) for pipelined tile copy + rowsum",
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -1140,6 +1143,8 @@ def main(argv=None):
     ap.add_argument("--all-configs", action="store_true")
     ap.add_argument("--no-sweep", action="store_true",
                     help="leave the per-configuration sweep out of the default line")
+    ap.add_argument("--no-read-ref", action="store_true",
+                    help="leave the read-bandwidth reference out of the default line")
     ap.add_argument("--only", choices=["copy", "rowsum", "copy_rowsum", "colsum"])
     ap.add_argument("--config", choices=sorted(RAGGED),
                     help="--only: one of the ragged task shapes (pitched rows) instead of "
