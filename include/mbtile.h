@@ -46,7 +46,9 @@
  *     global strides) the stages are filled by 1-D bulk copies of 16-byte-
  *     aligned windows of the matrix's bytes: supported for tile_rowsum at any
  *     pitch and for tile_copy when src and dst are both dense (ld = N); other
- *     cases return MBT_ERR_ALIGN.  A copy's stage then holds tile_m x tile_n
+ *     cases return MBT_ERR_ALIGN.  Row sums of rows of at most 64 bytes take
+ *     the 1-D path whatever the pitch (one thread sums a whole row), unless
+ *     more than 8 consumer warps are asked for.  A copy's stage then holds tile_m x tile_n
  *     elements' worth of bytes.  A row sum's window, whatever the tile, holds
  *     whole rows -- at most 32 KB while 8 rows fit in that, else at most 64
  *     KB -- or one of equal pieces (at most 64 KB) of a longer row, within

@@ -21,6 +21,9 @@ constexpr int kMaxWideThreads = 32 * (2 + kMaxWideConsumerWarps);
 constexpr int kBoxRowBytes = 128;      // one 128-byte swizzle span per box row
 constexpr int kSwizzleAtomBytes = 1024;
 constexpr uint64_t kDefaultWaitBudgetNs = 1000000000ull;  // 1 s
+// Flat row sum: rows of at most this many bytes are summed one thread per row,
+// element by element (fewer instructions per row than masked 16-byte chunks).
+constexpr int kFlatElemRowBytes = 64;
 
 // Fields every pipeline kernel needs.  Sizes in elements unless named *_bytes.
 struct PipeArgs {
@@ -153,6 +156,11 @@ struct FlatArgs {
     int64_t pieces_per_row;
     int32_t phase_shift;       // row sum, short rows: the row groups of one 8-lane
                                // shared-memory phase take rows 2^phase_shift apart
+    int32_t elem_rows;         // row sum, rows of at most kFlatElemRowBytes: each
+                               // thread sums whole rows element by element
+    int32_t elem_period;       // ... lanes this many apart read rows whose starts
+                               // share a shared-memory bank (0: no such lanes);
+                               // lane l starts its row (l / elem_period) words in
     int32_t pad0;
 };
 

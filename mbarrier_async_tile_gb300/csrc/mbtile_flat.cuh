@@ -211,10 +211,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
 
 // ---------------------------------------------------------------------------
 // Flat row sum (any row pitch): CTA b owns rows [b M / G, (b + 1) M / G).
-// Short rows: a window holds several whole rows; each row goes to a group of
-// L lanes of one warp (as many lanes per row as the CTA's threads allow, a
-// power of two up to 32), which add the row's 16-byte chunks masked to the
-// row and finish with a shuffle tree: no rendezvous per window.  Long rows: a window
+// Rows of at most kFlatElemRowBytes: a window holds many whole rows and each
+// thread sums whole rows, element by element.  Other short rows: a window
+// holds several whole rows; each row goes to a group of L lanes of one warp
+// (as many lanes per row as the CTA's threads allow, a power of two up to 32),
+// which add the row's 16-byte chunks masked to the row and finish with a
+// shuffle tree: no rendezvous per window.  Long rows: a window
 // holds one piece of one row; every thread keeps its share of the row across
 // the row's pieces; at the row's last piece each warp's shuffle tree deposits
 // a partial, and warp 0 adds the partials in warp order (the other warps do
@@ -246,18 +248,100 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     return v;
 }
 
-// Sum of the elements of the 4-byte word `u` (at window byte offset wb) whose
-// bytes lie in [b0, b1).
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+// One element of the stage at shared address addr, widened exactly.
 template <int DT>
-__device__ __forceinline__ float word_sum(uint32_t u, int wb, int b0, int b1) {
-    if constexpr (DT == MBT_F32) {
-        return wb >= b0 && wb < b1 ? __uint_as_float(u) : 0.f;
-    } else {
-        const float lo = element_value<DT>(u & 0xffffu);
-        const float hi = element_value<DT>(u >> 16);
-        const bool in_lo = wb >= b0 && wb < b1, in_hi = wb + 2 >= b0 && wb + 2 < b1;
-        if (in_lo && in_hi) return lo + hi;
-        return in_lo ? lo : in_hi ? hi : 0.f;
+__device__ __forceinline__ float lds_element(uint32_t addr) {
+    if constexpr (DT == MBT_F32)
+        return __uint_as_float(lds32(addr));
+    else
+        return element_value<DT>(lds16(addr));
+}
+
+// Sum of the NN elements of a row starting at shared address addr, in column
+// order.
+template <int DT, int NN>
+__device__ __forceinline__ float row_sum_fixed(uint32_t addr) {
+    constexpr int es = DT == MBT_F32 ? 4 : 2;
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < NN; ++c) s += lds_element<DT>(addr + es * c);
+    return s;
+}
+
+// The same for a row of n elements (n at most kFlatElemRowBytes / element size).
+template <int DT>
+__device__ __forceinline__ float row_sum_elems(uint32_t addr, int n) {
+    constexpr int es = DT == MBT_F32 ? 4 : 2;
+    switch (n) {
+        case 1: return row_sum_fixed<DT, 1>(addr);
+        case 2: return row_sum_fixed<DT, 2>(addr);
+        case 3: return row_sum_fixed<DT, 3>(addr);
+        case 4: return row_sum_fixed<DT, 4>(addr);
+        case 5: return row_sum_fixed<DT, 5>(addr);
+        case 6: return row_sum_fixed<DT, 6>(addr);
+        case 7: return row_sum_fixed<DT, 7>(addr);
+        case 8: return row_sum_fixed<DT, 8>(addr);
+        default: {
+            float s = 0.f;
+            int c = 0;
+            for (; c + 4 <= n; c += 4) {
+                const float x0 = lds_element<DT>(addr + es * c);
+                const float x1 = lds_element<DT>(addr + es * (c + 1));
+                const float x2 = lds_element<DT>(addr + es * (c + 2));
+                const float x3 = lds_element<DT>(addr + es * (c + 3));
+                s += x0;
+                s += x1;
+                s += x2;
+                s += x3;
+            }
+            for (; c < n; ++c) s += lds_element<DT>(addr + es * c);
+            return s;
+        }
+    }
+}
+
+// Rows whose pitch is a whole number of 4-byte words sharing a factor with 32:
+// the sum from column r round to column r - 1 (r, r + 1, ..., NN - 1, 0, ...,
+// r - 1; 0 <= r < NN), lanes starting at different columns so that their
+// reads fall in different banks.
+template <int DT, int NN>
+__device__ __forceinline__ float row_sum_fixed_rot(uint32_t addr, int r) {
+    constexpr int es = DT == MBT_F32 ? 4 : 2;
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NN; ++k) {
+        const int c = k + r < NN ? k + r : k + r - NN;
+        s += lds_element<DT>(addr + es * c);
+    }
+    return s;
+}
+
+template <int DT>
+__device__ __forceinline__ float row_sum_elems_rot(uint32_t addr, int n, int r) {
+    constexpr int es = DT == MBT_F32 ? 4 : 2;
+    switch (n) {
+        case 1: return row_sum_fixed_rot<DT, 1>(addr, r);
+        case 2: return row_sum_fixed_rot<DT, 2>(addr, r);
+        case 3: return row_sum_fixed_rot<DT, 3>(addr, r);
+        case 4: return row_sum_fixed_rot<DT, 4>(addr, r);
+        case 5: return row_sum_fixed_rot<DT, 5>(addr, r);
+        case 6: return row_sum_fixed_rot<DT, 6>(addr, r);
+        case 7: return row_sum_fixed_rot<DT, 7>(addr, r);
+        case 8: return row_sum_fixed_rot<DT, 8>(addr, r);
+        default: {
+            float s = 0.f;
+            for (int k = 0; k < n; ++k) {
+                const int c = k + r < n ? k + r : k + r - n;
+                s += lds_element<DT>(addr + es * c);
+            }
+            return s;
+        }
     }
 }
 
@@ -342,10 +426,13 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     const int warp = ctid >> 5;
     const int nthr = p.consumer_warps * 32;
     const unsigned char *gsrc = reinterpret_cast<const unsigned char *>(a.src);
-    // One instantiation of the window loop for whole rows per window, one for
-    // pieces of long rows: neither carries the other's state.
-    auto run = [&](auto short_rows) {
-        constexpr bool kShort = decltype(short_rows)::value;
+    // One instantiation of the window loop per row shape -- pieces of long rows
+    // (0), whole rows summed by lane groups (1), whole rows of at most
+    // kFlatElemRowBytes summed element by element (2; 3 with the lanes'
+    // starting columns rotated): none carries another's state.
+    auto run = [&](auto mode) {
+        constexpr int kMode = decltype(mode)::value;
+        constexpr bool kShort = kMode != 0;
         float row_acc = 0.f;            // long rows: this thread's share of the current row
         // Short rows: every row of a window goes to a group of L lanes of one warp
         // (a power of two, 1..32: as many lanes per row as the threads allow for
@@ -362,7 +449,6 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
         const int pp_log = L < 8 ? 3 - (__ffs(L) - 1) : 0;
         const int sh = pp_log > 0 ? a.phase_shift : 0;
         const int blk = 1 << (pp_log + sh);
-        const bool tiny = p.N * p.esize <= 16;
         uint32_t stage = 0, phase = 0;
         RowWindow rw = rowsum_window(a, ra, rb, 0);
         for (int64_t j = 0; j < count; ++j, next_row_window(a, rb, rw)) {
@@ -380,7 +466,44 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
             const int64_t we = wj.ws + wj.size;
             const int chunks = static_cast<int>(wj.size >> 4);
             const uint32_t sbase = sm.base + stage * p.stage_stride;
-            if constexpr (kShort) {
+            if constexpr (kMode >= 2) {
+                // Rows of at most kFlatElemRowBytes: thread t sums rows t, t + nthr,
+                // ... of the window element by element, from its starting column
+                // round to the one before it.  Consecutive lanes take consecutive
+                // rows (nearby shared-memory addresses, and coalesced stores of the
+                // sums).
+                const int nrows = static_cast<int>(rw.r1 - rw.r0);
+                const int pitch_b = static_cast<int>(a.ld * p.esize);
+                const int off0 = static_cast<int>(rw.e0 * p.esize - wj.ws);
+                const int row_b = static_cast<int>(p.N) * p.esize;
+                const int n = static_cast<int>(p.N);
+                // Starting column of this lane's rows: lanes elem_period apart would
+                // otherwise read the same bank at every step.
+                const int rot = kMode == 3 ? (lane / a.elem_period) * (4 / p.esize) % n : 0;
+                for (int lr = ctid; lr < nrows; lr += nthr) {
+                    const int b0 = off0 + lr * pitch_b;
+                    float s;
+                    if (b0 + row_b <= wj.size) {
+                        const uint32_t ra = sbase + static_cast<uint32_t>(b0);
+                        if constexpr (kMode == 3)
+                            s = row_sum_elems_rot<DT>(ra, n, rot);
+                        else
+                            s = row_sum_elems<DT>(ra, n);
+                    } else {
+                        // The array's last row: bytes past its last 16-byte boundary
+                        // were not loaded.
+                        s = 0.f;
+                        for (int c = 0; c < n; ++c) {
+                            const int64_t bb = b0 + static_cast<int64_t>(c) * p.esize;
+                            s += bb < wj.size ? lds_element<DT>(sbase + static_cast<uint32_t>(bb))
+                                              : element_value<DT>(element_bits<DT>(gsrc + wj.ws + bb));
+                        }
+                    }
+                    a.out[rw.r0 + lr] = s;
+                }
+                __syncwarp();
+                if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
+            } else if constexpr (kShort) {
                 // Short rows: the group's lanes add the row's chunks, masked to
                 // the row, and a shuffle tree inside the group gives the row's sum.
                 // No thread needs another warp's results, so the window needs no
@@ -401,24 +524,14 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
                         const int64_t loaded = b1 < wj.size ? b1 : wj.size;
                         if (loaded > b0) {
                             const int rb0 = static_cast<int>(b0), rb1 = static_cast<int>(b1);
-                            if (tiny) {
-                                // Rows of at most 16 bytes: 4-byte reads (measured: rows of
-                                // 3 bf16 elements 1.23 -> 1.82 TB/s; rows of 17 elements or
-                                // more were 3-29 % slower this way, so they keep 16-byte
-                                // chunks despite the bank conflicts of rows ~128 bytes apart).
-                                const int we = static_cast<int>((loaded - 1) >> 2);
-                                for (int wd = (rb0 >> 2) + gl; wd <= we; wd += L)
-                                    s += word_sum<DT>(lds32(sbase + 4u * wd), 4 * wd, rb0, rb1);
-                            } else {
-                                const int cs = rb0 >> 4;
-                                const int ce = static_cast<int>((loaded - 1) >> 4);
-                                for (int c = cs + gl; c <= ce; c += L) {
-                                    const uint4 v = lds128(sbase + 16u * c);
-                                    const int cb = 16 * c;
-                                    s += (cb >= rb0 && cb + 16 <= rb1)
-                                             ? chunk_sum<DT>(v)
-                                             : masked_chunk_sum_rel<DT>(v, cb, rb0, rb1);
-                                }
+                            const int cs = rb0 >> 4;
+                            const int ce = static_cast<int>((loaded - 1) >> 4);
+                            for (int c = cs + gl; c <= ce; c += L) {
+                                const uint4 v = lds128(sbase + 16u * c);
+                                const int cb = 16 * c;
+                                s += (cb >= rb0 && cb + 16 <= rb1)
+                                         ? chunk_sum<DT>(v)
+                                         : masked_chunk_sum_rel<DT>(v, cb, rb0, rb1);
                             }
                         }
                         // Bytes past the array's last 16-byte boundary (never loaded).
@@ -506,8 +619,12 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
             }
         }
     };
-    if (a.rows_per_window > 0)
-        run(std::true_type{});
+    if (a.rows_per_window > 0 && a.elem_rows && a.elem_period > 0)
+        run(std::integral_constant<int, 3>{});
+    else if (a.rows_per_window > 0 && a.elem_rows)
+        run(std::integral_constant<int, 2>{});
+    else if (a.rows_per_window > 0)
+        run(std::integral_constant<int, 1>{});
     else
-        run(std::false_type{});
+        run(std::integral_constant<int, 0>{});
 }

@@ -77,7 +77,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // operation can still run (through the 1-D bulk-copy kernels).
 int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, int tile_m,
                int tile_n, int stages, int dtype, const mbt_opts &o, int64_t *ld_src,
-               int64_t *ld_dst, bool *flat = nullptr) {
+               int64_t *ld_dst, bool *flat = nullptr, bool narrow_rows_flat = true) {
     if (flat) *flat = false;
     const int es = esize_of(dtype);
     if (es == 0) return MBT_ERR_ARG;
@@ -142,6 +142,14 @@ int check_args(int op, const void *src, const void *dst, int64_t M, int64_t N, i
         return MBT_OK;
     }
     if (static_cast<uint64_t>(*ld_src) * es >= (1ull << 40)) return MBT_ERR_UNSUPPORTED;
+    // Row sums of rows of at most kFlatElemRowBytes take the 1-D kernels whatever
+    // the pitch: a tile at least 128 bytes wide would carry mostly zero fill
+    // (measured: bf16 rows of 8 elements, 64 x 256 tiles, 279 GB/s), while the
+    // 1-D kernels sum such rows one thread a row.
+    if (narrow_rows_flat && op == MBT_OP_ROWSUM && N * es <= mbt::kFlatElemRowBytes &&
+        o.consumer_warps <= mbt::kMaxConsumerWarps) {
+        if (flat) *flat = true;
+    }
     return MBT_OK;
 }
 
@@ -255,6 +263,8 @@ void flat_setup(int op, int64_t M, int64_t N, int64_t ld, int es, int tile_m, in
     f->t_floor = f->total_bytes & ~int64_t(15);
     f->cap_bytes = static_cast<int64_t>(tile_m) * tile_n * es;
     f->rows_per_window = 0;
+    f->elem_rows = 0;
+    f->elem_period = 0;
     f->piece_elems = 0;
     f->pieces_per_row = 0;
     if (op == MBT_OP_ROWSUM) {
@@ -280,6 +290,20 @@ void flat_setup(int op, int64_t M, int64_t N, int64_t ld, int es, int tile_m, in
         if (rows >= 32) rows -= rows % 32;
         if (rows >= kFlatMinRowsPerWindow) {
             f->rows_per_window = rows;
+            f->elem_rows = row_bytes <= mbt::kFlatElemRowBytes ? 1 : 0;
+            // Rows a whole number w of 4-byte words apart start in the same bank
+            // every 32 / gcd(w, 32) rows: the lanes that far apart read their
+            // rows from different starting columns (measured on bf16 rows of 16
+            // and 32 elements, dense: 8- and 16-way conflicts otherwise).
+            if (f->elem_rows && pitch % 4 == 0) {
+                int64_t g = pitch / 4, m = 32;
+                while (m != 0) {
+                    const int64_t t = g % m;
+                    g = m;
+                    m = t;
+                }
+                f->elem_period = g > 1 ? static_cast<int32_t>(32 / g) : 0;
+            }
         } else {
             const int64_t most = room / es;
             f->pieces_per_row = ceil_div(N, most);
@@ -314,7 +338,7 @@ int flat_lanes_per_row(int64_t rows, int nthr) {
 // gained 21 %.  0 when L >= 8 (a phase reads one row's consecutive chunks) or
 // the rows are read 4 bytes at a time.
 int flat_phase_shift(const mbt::FlatArgs &f, int64_t N, int es, int W) {
-    if (f.rows_per_window <= 0 || N * es <= 16) return 0;
+    if (f.rows_per_window <= 0 || f.elem_rows || N * es <= 16) return 0;
     const int L = flat_lanes_per_row(f.rows_per_window, 32 * W);
     if (L >= 8) return 0;
     const int64_t pitch = f.ld * es, rows = f.rows_per_window;
@@ -1067,7 +1091,7 @@ int tile_stage_image(const void *src, int64_t M, int64_t N, int64_t ld, int tile
     int64_t ld_src = 0, ld_dst = 0;
     bool flat = false;
     int rc = check_args(MBT_OP_ROWSUM, src, image, M, N, tile_m, tile_n, 1, dtype, o, &ld_src,
-                        &ld_dst, &flat);
+                        &ld_dst, &flat, false);
     if (rc != MBT_OK) return rc;
     if (flat || M == 0 || N == 0 || image == nullptr) return MBT_ERR_ARG;
     if (tile_row < 0 || tile_col < 0 || tile_row * tile_m >= M || tile_col * tile_n >= N)

@@ -57,7 +57,7 @@ def test_flat_copy_matches_oracle(dtype, M, N, tm, tn, st):
     ("f16", "normal", 300, 63, 70, 128, 64, 2),         # short rows, pitched (140 B)
     ("bf16", "normal", 2000, 33, 33, 64, 256, 2),
     ("f32", "uniform", 5, 3, 3, 128, 32, 1),
-    ("bf16", "normal", 3000, 3, 3, 64, 256, 2),         # rows of <= 16 bytes: 4-byte reads
+    ("bf16", "normal", 3000, 3, 3, 64, 256, 2),         # rows of <= 64 bytes: one thread a row
     ("f16", "uniform", 2500, 7, 9, 128, 64, 3),         # 14-byte rows, odd pitch
     ("f16", "normal", 777, 8, 11, 128, 64, 2),          # 16-byte rows starting mid-word
     ("f32", "normal", 999, 4, 5, 128, 32, 2),
@@ -72,6 +72,69 @@ def test_flat_rowsum_matches_oracle(dtype, dist, M, N, ld, tm, tn, st):
     assert code == 0, info
     worst, rel, _ = rowsum_errors(out, x[:, :N])
     assert worst <= ROWSUM_RTOL, (worst, rel)
+
+
+@pytest.mark.parametrize("dtype,M,N,ld", [
+    ("bf16", 100003, 1, 1),          # 2-byte rows
+    ("bf16", 50001, 3, 3),           # 6-byte rows, the array's last row past its last
+    ("f16", 1001, 3, 3),             #   16-byte boundary (read from global memory)
+    ("f16", 40000, 8, 11),           # 16-byte rows, odd pitch
+    ("f16", 30000, 9, 9),            # 18 bytes: the rolled loop
+    ("bf16", 20000, 17, 17),
+    ("bf16", 9999, 31, 33),          # 62-byte rows, pitched
+    ("bf16", 8191, 32, 35),          # 64 bytes: the largest of this path
+    ("f32", 60001, 1, 1),
+    ("f32", 12345, 3, 5),
+    ("f32", 7001, 15, 15),
+    ("f32", 5003, 16, 17),
+])
+def test_flat_rowsum_element_rows(dtype, M, N, ld):
+    """Rows of at most 64 bytes: each consumer thread sums whole rows element
+    by element (unrolled up to 8 elements, a loop beyond).  Every row is
+    written (the output starts as NaN) and matches the oracle; the planner
+    takes this path exactly up to 64-byte rows."""
+    es = synthetic.ESIZE[dtype]
+    assert (ld * es) % 16 != 0
+    info = mbt.tile_device_info()
+    plan = mbt.tile_plan(mbt.OP_ROWSUM, M, N, 64, 256 if es == 2 else 128, 2,
+                         synthetic.DTYPES[dtype], num_sms=info["num_sms"],
+                         smem_optin=info["smem_optin"], fit_per_sm=3, ld_src=ld)
+    assert plan["flat"] == 1 and plan["phase_shift"] == 0
+    x = synthetic.make_matrix(M, N, dtype, "normal", seed=M + 13 * N, ld=ld)
+    out = torch.full((M,), float("nan"), device="cuda")
+    mbt.tile_rowsum(x.cuda()[:, :N], out, 64, 256 if es == 2 else 128, 2)
+    code, info = mbt.tile_status()
+    assert code == 0, info
+    assert not bool(out.isnan().any())
+    worst, rel, _ = rowsum_errors(out, x[:, :N])
+    assert worst <= ROWSUM_RTOL, (worst, rel)
+
+
+@pytest.mark.parametrize("dtype,M,N,ld,tile", [
+    ("bf16", 600000, 8, 8, (64, 256)),       # 16-byte rows, dense: a 16-byte pitch
+    ("f32", 300001, 16, 16, (128, 32)),      # 64-byte rows, dense
+    ("bf16", 70000, 32, 40, (64, 64)),       # 64-byte rows in an 80-byte pitch
+    ("f16", 90000, 5, 8, (128, 64)),         # 10-byte rows in a 16-byte pitch
+])
+def test_narrow_aligned_rows_take_the_element_path(dtype, M, N, ld, tile):
+    """Row sums of rows of at most 64 bytes take the 1-D kernels even where the
+    pitch is a multiple of 16 bytes (a tiled plan would carry mostly zero
+    fill); with more than 8 consumer warps asked for, the tiled kernels."""
+    es = synthetic.ESIZE[dtype]
+    assert (ld * es) % 16 == 0 and N * es <= 64
+    dt = synthetic.DTYPES[dtype]
+    assert mbt.tile_plan_device(mbt.OP_ROWSUM, M, N, *tile, 2, dt, ld_src=ld)["flat"] == 1
+    assert mbt.tile_plan_device(mbt.OP_ROWSUM, M, N, *tile, 2, dt, ld_src=ld,
+                                consumer_warps=12)["flat"] == 0
+    x = synthetic.make_matrix(M, N, dtype, "normal", seed=M + N, ld=ld)
+    xd = x.cuda()[:, :N]
+    out = torch.full((M,), float("nan"), device="cuda")
+    mbt.tile_rowsum(xd, out, *tile, 2)
+    wide = mbt.tile_rowsum(xd, None, *tile, 2, consumer_warps=12)
+    code, info = mbt.tile_status()
+    assert code == 0, info
+    assert rowsum_errors(out, x[:, :N])[0] <= ROWSUM_RTOL
+    assert rowsum_errors(wide, x[:, :N])[0] <= ROWSUM_RTOL
 
 
 @pytest.mark.parametrize("dtype,M,N,warps,ctas", [
