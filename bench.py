@@ -660,11 +660,85 @@ def bench_e2e(args, mbt, x3, x4, world):
         step()
     ms = reduce_max((time.perf_counter() - t0) * 1e3, world)
     value = aggregate_gbs(copy_bytes() + rowsum_bytes(), steps, world, ms)
+    h2d = h3.numel() * h3.element_size() + h4.numel() * h4.element_size()
+    d2h = r3.numel() * r3.element_size() + r4.numel() * r4.element_size()
+    link = link_rates(x3.device)
+    bound = link_bound_gbs(h2d, d2h, copy_bytes() + rowsum_bytes(), link)
     return {"value": round(value, 1), "unit": "GB/s", "steps": steps,
             "api": "tile_copy_host + tile_rowsum_host (host buffers, pinned)",
             "host_threads": args.e2e_threads,
-            "h2d_bytes_per_step": h3.numel() * h3.element_size() + h4.numel() * h4.element_size(),
-            "d2h_bytes_per_step": r3.numel() * r3.element_size() + r4.numel() * r4.element_size()}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "link": link, "link_bound": round(bound, 1),
+            "frac_of_link_bound": round(value / world / bound, 4),
+            "link_note": ("link_bound: the step's algorithmic bytes over the shortest time "
+                          "the link allows for its host-to-device and device-to-host bytes: "
+                          "all device-to-host traffic overlapped with host-to-device traffic "
+                          "at the rates both directions reach together, the rest of the "
+                          "host-to-device traffic alone")}
+
+
+def link_rates(device, nbytes: int = 512 << 20) -> dict:
+    """GB/s of pinned-host <-> device copies of nbytes (best of 3): each
+    direction alone, then both at once on two streams (each direction's own
+    rate while the other runs)."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    d_b = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def best_ms(run):
+        best = float("inf")
+        for _ in range(3):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            torch.cuda.synchronize()
+            run(ev)
+            torch.cuda.synchronize()
+            best = min(best, run.ms(ev))
+        return best
+
+    def one(dst, src, stream):
+        def run(ev):
+            ev[0].record(stream)
+            with torch.cuda.stream(stream):
+                dst.copy_(src, non_blocking=True)
+            ev[1].record(stream)
+        run.ms = lambda ev: ev[0].elapsed_time(ev[1])
+        return run
+
+    h2d = nbytes / best_ms(one(d_a, h_in, s1)) / 1e6
+    d2h = nbytes / best_ms(one(h_out, d_b, s2)) / 1e6
+    both = {}
+    for _ in range(3):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        torch.cuda.synchronize()
+        ev[0].record(s1)
+        ev[2].record(s2)
+        with torch.cuda.stream(s1):
+            d_a.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_b, non_blocking=True)
+        ev[1].record(s1)
+        ev[3].record(s2)
+        torch.cuda.synchronize()
+        hb = nbytes / ev[0].elapsed_time(ev[1]) / 1e6
+        db = nbytes / ev[2].elapsed_time(ev[3]) / 1e6
+        if hb + db > both.get("h2d_gbs", 0) + both.get("d2h_gbs", 0):
+            both = {"h2d_gbs": round(hb, 1), "d2h_gbs": round(db, 1)}
+    return {"h2d_gbs": round(h2d, 1), "d2h_gbs": round(d2h, 1), "both": both,
+            "bytes": nbytes}
+
+
+def link_bound_gbs(h2d: int, d2h: int, alg: int, link: dict) -> float:
+    """Throughput bound of a step that moves h2d bytes in and d2h bytes out:
+    the out-going bytes overlapped with in-coming ones at the rates both
+    directions reach together, the remainder of either direction alone."""
+    hb, db = link["both"]["h2d_gbs"] * 1e9, link["both"]["d2h_gbs"] * 1e9
+    if d2h / db <= h2d / hb:
+        t = d2h / db + (h2d - hb * d2h / db) / (link["h2d_gbs"] * 1e9)
+    else:
+        t = h2d / hb + (d2h - db * h2d / hb) / (link["d2h_gbs"] * 1e9)
+    return alg / t / 1e9
 
 
 def bench_only(args):
