@@ -523,8 +523,11 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     const int64_t sums_per_group = cols ? tile_n : tile_m;
     if (with_workspace) {
         const int64_t G = std::min<int64_t>(plan->num_tiles, cap);
-        // (the wide column sum walks one strip at a time)
-        const int cg = !cols ? 0 : W > mbt::kMaxConsumerWarps ? 1 : col_group_for(tile_n, es);
+        // (the wide column sum walks one strip at a time; strip pairs need an
+        // even warp count: their threads per chunk column, 4 W, a multiple of 8)
+        const int cg = !cols ? 0
+                       : (W > mbt::kMaxConsumerWarps || W % 2 != 0) ? 1
+                                                                     : col_group_for(tile_n, es);
         const int32_t kmax =
             cols ? colsum_contributors(plan->tiles_m, plan->tiles_n, cg, plan->num_tiles, G)
                  : most_contributors(group_tiles, plan->num_tiles, G);
@@ -907,6 +910,9 @@ int colsum_launch(const void *src, float *out, int64_t M, int64_t N, int64_t ld_
     }
     a.kmax = plan.kmax;
     a.tile_n = tile_n;
+    // strip pairs: the consumers' row stride must keep the swizzle term
+    if (plan.col_group == 2 && (plan.consumer_warps * 32 / (plan.boxes * 8)) % 8 != 0)
+        return MBT_ERR_UNSUPPORTED;
     const cudaError_t e = mbt::launch_colsum(dtype, map, a, plan.grid, plan.threads,
                                              plan.smem_bytes, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MBT_OK : MBT_ERR_CUDA;

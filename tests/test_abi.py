@@ -297,6 +297,12 @@ def test_plan_default_grid_follows_bytes_in_flight():
     p = _plan(mbt.OP_COLSUM, 12289, 8191, 128, 32, 3, torch.float32, fit=1, ws=True,
               ld_src=8192, consumer_warps=12)   # more than 8 warps: one strip at a time
     assert p["col_group"] == 1 and p["consumer_warps"] == 12
+    # strip pairs only with an even warp count (4 W threads per chunk column, a
+    # multiple of 8, so each thread's rows share one swizzle term)
+    for W, cg in ((2, 2), (3, 1), (4, 2), (5, 1), (6, 2), (7, 1), (8, 2)):
+        p = _plan(mbt.OP_COLSUM, 12289, 8191, 128, 32, 3, torch.float32, fit=2, ws=True,
+                  ld_src=8192, consumer_warps=W)
+        assert p["col_group"] == cg, W
     p = _plan(mbt.OP_COPY_ROWSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True)
     assert p["consumer_warps"] <= 8
     assert _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 8, torch.float16)["consumer_warps"] == 4
