@@ -44,6 +44,7 @@ __device__ int32_t g_status[4];
 namespace {
 
 constexpr int kVec = 8;  // 16-byte chunks a consumer thread holds per round
+static_assert(kVec == 8, "the row-sum consumer's box-aligned addressing assumes 8 chunks a round");
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -1136,6 +1137,16 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
     const int most = (cpr + tpr - 1) / tpr;
     const int rounds = (most + kVec - 1) / kVec;
     const int box = boxed ? (ctid / p.tile_m) / (tpr / p.boxes) : 0;
+    // Where this thread's chunk block starts on a box boundary and takes one
+    // round (the default plans at 2 stages and of 128-byte tiles), chunk lo + u
+    // of its row lies at box_base + ((u ^ (row mod 8)) << 4): one base per
+    // thread instead of a chunk_offset per load.  Measured: +1.5-1.9 % on the
+    // ragged 128-byte tiles; with two rounds (4 warps at 3 stages) the general
+    // form was 1.7 % faster.
+    const bool box_aligned = (lo & 7) == 0 && rounds == 1;
+    const uint32_t box_base =
+        static_cast<uint32_t>(lo >> 3) * p.box_stride + static_cast<uint32_t>(row) * kBoxRowBytes;
+    const int rx = row & 7;
     float acc = 0.f;
     int64_t key = -1;   // band being summed
     uint32_t stage = 0, phase = 0;
@@ -1178,10 +1189,18 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
         float tsum = 0.f;
         for (int r = 0; r < rounds; ++r) {
             uint4 v[kVec];
+            if (box_aligned) {
 #pragma unroll
-            for (int u = 0; u < kVec; ++u) {
-                const int c = r * kVec + u;
-                if (c < mine) v[u] = lds128(rbase + chunk_offset(row, lo + c, p.box_stride));
+                for (int u = 0; u < kVec; ++u)
+                    if (r * kVec + u < mine)
+                        v[u] = lds128(rbase + box_base + r * p.box_stride +
+                                      (static_cast<uint32_t>(u ^ rx) << 4));
+            } else {
+#pragma unroll
+                for (int u = 0; u < kVec; ++u) {
+                    const int c = r * kVec + u;
+                    if (c < mine) v[u] = lds128(rbase + chunk_offset(row, lo + c, p.box_stride));
+                }
             }
             if (r == rounds - 1) {
                 __syncwarp();
