@@ -1142,8 +1142,10 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
     // of its row lies at box_base + ((u ^ (row mod 8)) << 4): one base per
     // thread instead of a chunk_offset per load.  Measured: +1.5-1.9 % on the
     // ragged 128-byte tiles; with two rounds (4 warps at 3 stages) the general
-    // form was 1.7 % faster.
-    const bool box_aligned = (lo & 7) == 0 && rounds == 1;
+    // form was 1.7 % faster, and the wide CTA's 4-chunk blocks (S=4) lost 4 %
+    // with both forms compiled in, so its kernel keeps the general form only.
+    constexpr bool kWide = CT > kMaxConsumerThreads;
+    const bool box_aligned = !kWide && (lo & 7) == 0 && rounds == 1;
     const uint32_t box_base =
         static_cast<uint32_t>(lo >> 3) * p.box_stride + static_cast<uint32_t>(row) * kBoxRowBytes;
     const int rx = row & 7;
