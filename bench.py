@@ -35,7 +35,8 @@ COPY = dict(name="copy", dtype="f16", M=16384, N=16384, tile_m=128, tile_n=64,
 ROWSUM = dict(name="rowsum", dtype="bf16", M=8192, N=65536, tile_m=64, tile_n=256,
               dist="normal", seed=1004)
 ESIZE = {"f16": 2, "bf16": 2, "f32": 4}
-# The ragged task shapes, stored with a 16-byte row pitch (--only --config).
+# The ragged fp32 12289 x 8191 and fp16 24577 x 16383 workloads, stored with a 16-byte row
+# pitch (--only --config).
 RAGGED = {
     "5a": dict(name="5a", dtype="f32", M=12289, N=8191, tile_m=128, tile_n=32, dist="uniform",
                seed=1005),
@@ -508,7 +509,7 @@ def bench_gpu(args, rank, world):
     ms_rowsum = ms_rowsum_graph if graph else ms_rowsum_stream
     ms_total = ms_total_graph if graph else ms_total_stream
     t1 = time.time()
-    # every configuration of the task's table and the stage sweep, each point
+    # every workload configuration and the stage sweep, each point
     # in its own clock window
     sweep = None
     read_ref = None if args.no_read_ref else read_reference(dev, clocks)
@@ -601,7 +602,7 @@ def bench_gpu(args, rank, world):
     if sweep is not None:
         out["sweep"] = sweep
         out["sweep_note"] = (
-            "every configuration of the task's table (1, 2: latency; 3: copy at 1/2/3/4/6 "
+            "every workload configuration (1, 2: latency; 3: copy at 1/2/3/4/6 "
             "stages with LSU and bulk stores; 4: row and column sums at 2/3/4 stages with a "
             "caller's workspace, and the plain calls with the library's own; 5a/5b: copy, "
             "row sum, column sum and fused copy + row sum at 3 stages), each timed by "
@@ -807,7 +808,7 @@ def bench_only(args):
                       "gbs": round(nbytes / ms / 1e6, 1)}), flush=True)
 
 
-# Every configuration of the task's table, each point timed in its own window
+# Every workload configuration (lesson shapes 1-2, streaming 3-4, ragged 5a-5b), each point timed in its own window
 # with the SM clocks sampled there.  (config, op, dtype, M, N, tile_m, tile_n,
 # stages, extra) -- extra: store_mode for copies, "caller" / "library" for the
 # sums' workspace.
@@ -1221,7 +1222,7 @@ def main(argv=None):
                     help="leave the read-bandwidth reference out of the default line")
     ap.add_argument("--only", choices=["copy", "rowsum", "copy_rowsum", "colsum"])
     ap.add_argument("--config", choices=sorted(RAGGED),
-                    help="--only: one of the ragged task shapes (pitched rows) instead of "
+                    help="--only: one of the ragged workloads (pitched rows) instead of "
                          "the bench workload")
     ap.add_argument("--trim-cols", type=int, default=0,
                     help="--only: drop this many columns (an odd count gives a dense matrix "

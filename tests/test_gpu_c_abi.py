@@ -65,7 +65,7 @@ int main(int argc, char **argv) {
     int32_t info[4];
     CHECK(tile_status(NULL, info));
 
-    /* dense matrix: the task's plain signatures, then the _ex forms with a
+    /* dense matrix: the plain signatures, then the _ex forms with a
        workspace of our own on the same plan */
     const int64_t M2 = atoll(argv[6]), N2 = atoll(argv[7]);
     const size_t bytes2 = (size_t)M2 * N2 * 2;

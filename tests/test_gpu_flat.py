@@ -172,7 +172,8 @@ def test_flat_rowsum_permuted_rows_each_written_once(dtype, M, N, warps, ctas):
 
 
 def test_flat_full_size_dense_ragged_configs():
-    """The ragged shapes of the task, stored dense (no pitch padding)."""
+    """The ragged fp32 12289 x 8191 and fp16 24577 x 16383 shapes, stored dense (no pitch
+    padding)."""
     for dtype, M, N, tm, tn, seed in (("f32", 12289, 8191, 128, 32, 1005),
                                       ("f16", 24577, 16383, 128, 64, 1006)):
         x = synthetic.make_matrix(M, N, dtype, "uniform", seed)
