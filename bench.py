@@ -513,6 +513,9 @@ def bench_gpu(args, rank, world):
     # in its own clock window
     sweep = None
     read_ref = None if args.no_read_ref else read_reference(dev, clocks)
+    # the same at the row-sum workload's size (the same per-launch ramp and tail)
+    read_same = (None if args.no_read_ref else
+                 read_reference(dev, clocks, nbytes=ROWSUM["M"] * ROWSUM["N"] * ESIZE[ROWSUM["dtype"]]))
     if not args.no_sweep:
         theo = mbt.tile_device_info()["hbm_gbs_theoretical"]
         sweep = config_sweep(dev, clocks, measured_peak()[0], theo,
@@ -571,7 +574,10 @@ def bench_gpu(args, rank, world):
                 "frac_of_read_peak": (round(dom["gbs"] / read_ref["gbs"], 4)
                                       if dom_name == "rowsum" and read_ref else None),
                 "rowsum_frac_of_read_peak": (round(kernels["rowsum"]["gbs"] / read_ref["gbs"], 4)
-                                             if read_ref else None)}
+                                             if read_ref else None),
+                "read_same_size": read_same,
+                "rowsum_frac_of_read_same_size": (round(kernels["rowsum"]["gbs"] / read_same["gbs"], 4)
+                                                  if read_same else None)}
     out = {
         "metric": "achieved HBM GB/s (read+write) for pipelined tile copy + rowsum",
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -750,6 +756,25 @@ def bench_only(args):
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
+    if args.only == "read":
+        # the read reference on a buffer of --rows MiB (default 1024)
+        nbytes = (args.rows or 1024) << 20
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        out = torch.empty(1, dtype=torch.int32, device=dev)
+        fn = lambda: mbt.tile_read_checksum(buf, out)  # noqa: E731
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(args.steps):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e) / args.steps
+        print(json.dumps({"only": "read", "bytes": nbytes, "ms": round(ms, 4),
+                          "gbs": round(nbytes / ms / 1e6, 1)}), flush=True)
+        return
     c = ROWSUM if args.only in ("rowsum", "colsum") else COPY
     if args.config:
         c = RAGGED[args.config]
@@ -839,9 +864,10 @@ POINT_TARGET_S = 0.25     # device time of each point's timed graph replays
 READ_REF_BYTES = 4 << 30   # the read reference's buffer: far larger than L2
 
 
-def read_reference(dev, clocks, target_s: float = POINT_TARGET_S) -> dict:
+def read_reference(dev, clocks, target_s: float = POINT_TARGET_S,
+                   nbytes: int = READ_REF_BYTES) -> dict:
     """The read-only ceiling of this device for the reductions: GB/s of
-    tile_read_checksum (one pass of 16-byte loads over a 4 GiB buffer, every
+    tile_read_checksum (one pass of 16-byte loads over an nbytes buffer, every
     32-bit word folded into an XOR checksum), replayed from a CUDA graph of 10
     launches for about `target_s`, one event pair around the replays, with
     the clocks sampled meanwhile."""
@@ -849,7 +875,7 @@ def read_reference(dev, clocks, target_s: float = POINT_TARGET_S) -> dict:
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
-    buf = torch.empty(READ_REF_BYTES, dtype=torch.uint8, device=dev)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     out = torch.empty(1, dtype=torch.int32, device=dev)
     side.wait_stream(torch.cuda.current_stream())
     for _ in range(3):
@@ -879,10 +905,10 @@ def read_reference(dev, clocks, target_s: float = POINT_TARGET_S) -> dict:
     del graph, buf
     torch.cuda.empty_cache()
     c = clocks.summary(t0, t1)
-    return {"gbs": round(READ_REF_BYTES / ms / 1e6, 1), "ms": round(ms, 4),
-            "bytes": READ_REF_BYTES, "kernel": "mbt_read_checksum_kernel",
-            "what": ("tile_read_checksum: one pass of 16-byte loads over a 4 GiB device buffer "
-                     "(XOR of every 32-bit word), graph replay, mean per launch"),
+    return {"gbs": round(nbytes / ms / 1e6, 1), "ms": round(ms, 4),
+            "bytes": nbytes, "kernel": "mbt_read_checksum_kernel",
+            "what": (f"tile_read_checksum: one pass of 16-byte loads over a {nbytes >> 20} MiB "
+                     "device buffer (XOR of every 32-bit word), graph replay, mean per launch"),
             "launches_timed": reps * n,
             "clocks": {"sm_mhz": c.get("sm_mhz"), "sm_max_mhz": c.get("sm_max_mhz"),
                        "reasons": c.get("reasons"), "samples": c.get("samples")}}
@@ -1220,7 +1246,7 @@ def main(argv=None):
                     help="leave the per-configuration sweep out of the default line")
     ap.add_argument("--no-read-ref", action="store_true",
                     help="leave the read-bandwidth reference out of the default line")
-    ap.add_argument("--only", choices=["copy", "rowsum", "copy_rowsum", "colsum"])
+    ap.add_argument("--only", choices=["copy", "rowsum", "copy_rowsum", "colsum", "read"])
     ap.add_argument("--config", choices=sorted(RAGGED),
                     help="--only: one of the ragged workloads (pitched rows) instead of "
                          "the bench workload")
