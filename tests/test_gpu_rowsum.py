@@ -242,3 +242,58 @@ def test_flush_ring_wraps_many_times(split):
     out = mbt.tile_rowsum(x.cuda(), None, 64, 256, 2, max_ctas=3, split=split)
     assert mbt.tile_status()[0] == 0
     assert rowsum_errors(out, x)[0] <= ROWSUM_RTOL
+
+
+def test_library_workspace_from_concurrent_host_threads():
+    """Host threads calling the plain row sum at once, each on a stream of its own
+    and each through the per-thread default stream (cudaStreamPerThread, one
+    handle for all threads, a different stream in each): every thread's
+    workspace is its own, and every result is the caller's-workspace bits."""
+    import ctypes
+    import threading
+
+    M, N = 3000, 20000
+    x = synthetic.make_matrix(M, N, "bf16", "normal", seed=23)
+    xd = x.cuda()
+    need = mbt.tile_rowsum_workspace_bytes(M, N, 64, 256, 2, torch.bfloat16)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    want = mbt.tile_rowsum(xd, None, 64, 256, 2, workspace=ws)
+    torch.cuda.synchronize()
+    per_thread_stream = 0x2   # cudaStreamPerThread
+    results, errors = {}, []
+
+    def worker(k):
+        try:
+            torch.cuda.set_device(0)
+            outs = []
+            if k % 2 == 0:
+                s = torch.cuda.Stream()
+                s.wait_stream(torch.cuda.current_stream())
+                for _ in range(6):
+                    outs.append(mbt.tile_rowsum(xd, None, 64, 256, 2, stream=s))
+                s.synchronize()
+            else:
+                for _ in range(6):
+                    o = torch.empty(M, dtype=torch.float32, device="cuda")
+                    torch.cuda.synchronize()
+                    rc = mbt.C.tile_rowsum(xd.data_ptr(), o.data_ptr(), M, N, 64, 256, 2,
+                                           mbt.DTYPE_CODE[xd.dtype], per_thread_stream)
+                    assert rc == 0, rc
+                    outs.append(o)
+                torch.cuda.synchronize()
+            results[k] = outs
+        except Exception as e:   # reported by the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(6)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert mbt.tile_status()[0] == 0
+    for k, outs in results.items():
+        for o in outs:
+            assert torch.equal(o.view(torch.int32), want.view(torch.int32)), k
+    assert rowsum_errors(want, x)[0] <= ROWSUM_RTOL
