@@ -105,6 +105,58 @@ __device__ bool post_group(const ColsumArgs &a, int64_t gstart, float (*acc)[EPC
     return true;
 }
 
+// The last contributor's addition for the strips of a pair that this CTA
+// completes (bit k of `lasts`: strip k of the pair; 128-byte tile rows, so at
+// most 2 x 64 columns).  Entry e = k tn + c (strip k, column c) belongs to
+// lane e % 32; for each entry the K_k partial slots are added in slot order
+// (as warp_add_slots does, so the same bits), the column sum is written and
+// the slots are left zero.  A lane's 4 entries and 8 slots are loaded
+// together, both strips at once: a pair of strips with 5 contributors each
+// costs one load round trip, not three per strip one strip after the other.
+__device__ __forceinline__ void combine_pair(const ColsumArgs &a, const int64_t *strip_k,
+                                             const int64_t *K_k, unsigned lasts, int tn) {
+    constexpr int PL = 4, B = 8;
+    const int lane = threadIdx.x & 31;
+    float *slot0[PL];
+    int kn[PL];
+    int kmax_all = 0;
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+        const int e = lane + 32 * i;
+        const int k = e >= tn ? 1 : 0;
+        const bool on = e < 2 * tn && ((lasts >> k) & 1u);
+        slot0[i] = a.partial + (k ? strip_k[1] : strip_k[0]) * a.kmax * tn + (e - k * tn);
+        kn[i] = on ? static_cast<int>(k ? K_k[1] : K_k[0]) : 0;
+        kmax_all = kn[i] > kmax_all ? kn[i] : kmax_all;
+    }
+    float acc[PL];
+#pragma unroll
+    for (int i = 0; i < PL; ++i) acc[i] = 0.f;
+    for (int k0 = 0; k0 < kmax_all; k0 += B) {
+        float v[B][PL];
+#pragma unroll
+        for (int u = 0; u < B; ++u)
+#pragma unroll
+            for (int i = 0; i < PL; ++i)
+                v[u][i] = k0 + u < kn[i] ? __ldcg(slot0[i] + static_cast<int64_t>(k0 + u) * tn)
+                                         : 0.f;
+#pragma unroll
+        for (int u = 0; u < B; ++u)
+#pragma unroll
+            for (int i = 0; i < PL; ++i)
+                if (k0 + u < kn[i]) acc[i] += v[u][i];
+    }
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+        if (kn[i] == 0) continue;
+        const int e = lane + 32 * i;
+        const int k = e >= tn ? 1 : 0;
+        const int64_t col = (k ? strip_k[1] : strip_k[0]) * tn + (e - k * tn);
+        if (col < a.p.N) a.out[col] = acc[i];
+        for (int j = 0; j < kn[i]; ++j) slot0[i][static_cast<int64_t>(j) * tn] = 0.f;
+    }
+}
+
 // The column sum's flush warp: takes the consumers' records in order until
 // the end mark (key -1).
 template <int GMAX>
@@ -133,6 +185,7 @@ __device__ void colsum_flush_warp(const ColsumArgs &a, const float *ring_data, F
         bool any_split = false;
 #pragma unroll
         for (int k = 0; k < GMAX; ++k) {
+            strip_k[k] = 0;
             K_k[k] = 0;
             if (k >= c0.wg) continue;
             const int64_t pos_first = gstart + k;
@@ -162,21 +215,28 @@ __device__ void colsum_flush_warp(const ColsumArgs &a, const float *ring_data, F
         __syncwarp();
         if (lane == 0) mbar_arrive(fr.empty0 + 8u * slot);   // data[] is no longer read
         ++fr.k;
+        if (!any_split) continue;
+        // The tickets of the group's split strips, taken together (lane k:
+        // strip k of the group).
+        int64_t my_strip = 0, my_K = 0;
 #pragma unroll
-        for (int k = 0; k < GMAX; ++k) {
-            if (K_k[k] <= 1) continue;
-            const int64_t strip = strip_k[k], K = K_k[k];
-            int is_last = 0;
-            if (lane == 0) is_last = atomicAdd(&a.ticket[strip], 1) == K - 1;
-            is_last = __shfl_sync(0xffffffffu, is_last, 0);
-            if (!is_last) continue;
-            fence_acq_rel_gpu();   // the other contributors' partials, before reading them
-            const int64_t col0 = strip * tn;
-            warp_add_slots<16, 2>(a.partial + strip * a.kmax * tn, K, tn, tn, a.out + col0,
-                                  p.N - col0);
-            __syncwarp();
-            if (lane == 0) a.ticket[strip] = 0;
+        for (int k = 0; k < GMAX; ++k)
+            if (lane == k) {
+                my_strip = strip_k[k];
+                my_K = K_k[k];
+            }
+        const bool my_last = my_K > 1 && atomicAdd(&a.ticket[my_strip], 1) == my_K - 1;
+        const unsigned lasts = __ballot_sync(0xffffffffu, my_last);
+        if (lasts == 0) continue;
+        fence_acq_rel_gpu();   // the other contributors' partials, before reading them
+        if constexpr (GMAX == 2) {
+            combine_pair(a, strip_k, K_k, lasts, tn);
+        } else {
+            warp_add_slots<16, 2>(a.partial + strip_k[0] * a.kmax * tn, K_k[0], tn, tn,
+                                  a.out + strip_k[0] * tn, p.N - strip_k[0] * tn);
         }
+        __syncwarp();
+        if (my_last) a.ticket[my_strip] = 0;
     }
 }
 
