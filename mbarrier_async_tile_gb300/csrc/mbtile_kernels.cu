@@ -1102,9 +1102,18 @@ __device__ void flush_warp(const RowsumArgs &a, const float *red, FlushRing fr,
         is_last = __shfl_sync(0xffffffffu, is_last, 0);
         if (is_last) {
             fence_acq_rel_gpu();   // the other contributors' partials, before reading them
-            warp_add_slots<8, 4>(a.partial + ft.band * a.kmax * p.tile_m, ft.K, p.tile_m,
-                                 p.tile_m, a.out + ft.band * p.tile_m,
-                                 p.M - ft.band * p.tile_m);
+            // Bands of at most 128 rows: 8 slots per load round trip (a band
+            // of the fp32 12289 x 8191 row sum has 5-6 contributors).  Not in
+            // the wide kernel, whose consumers lost speed when its register
+            // count went up.
+            if (CT <= kMaxConsumerThreads && p.tile_m <= 128)
+                warp_add_slots<4, 8>(a.partial + ft.band * a.kmax * p.tile_m, ft.K, p.tile_m,
+                                     p.tile_m, a.out + ft.band * p.tile_m,
+                                     p.M - ft.band * p.tile_m);
+            else
+                warp_add_slots<8, 4>(a.partial + ft.band * a.kmax * p.tile_m, ft.K, p.tile_m,
+                                     p.tile_m, a.out + ft.band * p.tile_m,
+                                     p.M - ft.band * p.tile_m);
             __syncwarp();
             if (lane == 0) a.ticket[ft.band] = 0;
         }
