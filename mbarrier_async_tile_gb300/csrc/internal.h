@@ -87,6 +87,16 @@ struct RowsumArgs {
 // strip (tile_n columns) reduced down the rows.
 constexpr int kMaxColGroup = 2;
 
+// Records the consumers of a row or column sum may post ahead of the flush warp.
+constexpr int kFlushSlots = 2;
+
+// Dynamic shared memory of the column sum's flush ring, after the stages:
+// kFlushSlots slots of one float per consumer thread, element of a 16-byte
+// chunk (16 / es) and strip of a group.
+constexpr int64_t colsum_ring_bytes(int consumer_warps, int es, int col_group) {
+    return static_cast<int64_t>(kFlushSlots) * 32 * consumer_warps * (16 / es) * col_group * 4;
+}
+
 // Position of tile t in the strip-group order (PipeArgs.col_group = g >= 1).
 struct ColPos {
     int64_t gstart;            // order position of the group's first tile

@@ -27,9 +27,6 @@
 // Included by mbtile_kernels.cu inside its anonymous namespace: it uses that
 // file's PTX wrappers, bounded waits, producer, status word and log.
 
-constexpr int kColsumRedFloats = 32 * kMaxConsumerWarps * 8;   // threads x EPC (max)
-constexpr int kColsumWideRedFloats = 32 * kMaxWideConsumerWarps * 8;
-
 template <int DT>
 __device__ __forceinline__ void chunk_accumulate(float *acc, const uint4 &v) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -53,22 +50,22 @@ __device__ __forceinline__ void chunk_accumulate(float *acc, const uint4 &v) {
     }
 }
 
-// Flush ring of the column sum: when a CTA leaves a group, its consumers add
-// the tpc partials of each column in g order (through red[]) and hand the
-// per-column sums of the group's strips -- with the group as key -- to the
-// flush warp, which does the global part: the column sums (sole contributor),
-// or the CTA's partials, fence, ticket, and for the last contributor the
-// addition of all contributors' partials in CTA order.  The consumers go on
-// at once.  (Measured on the row sum, whose flush works the same way: the
-// fence and ticket round trips of a band change had stalled the consumers of
-// the CTAs crossing one by ~3 us.)
-constexpr int kColsumSlotFloats = 512;   // group strips x tile_n, at most
-
+// Flush ring of the column sum: when a CTA leaves a group, each consumer
+// thread drops its accumulators into the next ring slot (in dynamic shared
+// memory after the stages: kFlushSlots slots of 32 W x EPC x GMAX floats,
+// thread (q, g)'s sums of strip k at g (GMAX tn) + k tn + q EPC) and its warp
+// arrives; no consumer waits for another.  The flush warp adds the tpc
+// partials of each column in g order and does the global part: the column
+// sums (sole contributor), or the CTA's partials, fence, ticket, and for the
+// last contributor the addition of all contributors' partials in CTA order.
+// Measured on the fp32 12289 x 8191 column sum with 128 x 32 tiles: adding
+// the partials in the consumers, between two rendezvous of all consumer
+// warps per strip, stalled the consumers of a CTA that changes strip pair
+// half way through its range by ~4 us.
 template <int EPC, int GMAX>
-__device__ bool post_group(const ColsumArgs &a, int64_t gstart, float (*acc)[EPC], bool active,
-                           int q, int g, int tpc, float *red, float *ring_data, FlushCtl &f,
-                           FlushRing &fr, const WaitCtl &w, int ctid, int nthr) {
-    const int tn = a.tile_n;
+__device__ bool post_group(int tn, int64_t gstart, float (*acc)[EPC], bool active, int q,
+                           int g, float *ring, int slot_floats, FlushRing &fr, const WaitCtl &w,
+                           int ctid) {
     const uint32_t slot = ring_slot(fr.k);
     bool ok = wait_bounded(fr.empty0 + 8u * slot, ring_parity(fr.k) ^ 1u, w, true);
     ok = __all_sync(0xffffffffu, ok);
@@ -79,24 +76,14 @@ __device__ bool post_group(const ColsumArgs &a, int64_t gstart, float (*acc)[EPC
         }
         return false;
     }
-    float *data = ring_data + slot * kColsumSlotFloats;
-    if (gstart >= 0) {
-        const ColPos c0 = col_pos(gstart, a.p.tiles_m, a.p.tiles_n, GMAX);
+    if (gstart >= 0 && active) {
+        float *dst = ring + slot * slot_floats + g * (GMAX * tn) + q * EPC;
 #pragma unroll
-        for (int k = 0; k < GMAX; ++k) {
-            if (k >= c0.wg) break;
-            if (active) {
+        for (int k = 0; k < GMAX; ++k)
 #pragma unroll
-                for (int e = 0; e < EPC; ++e) red[g * tn + q * EPC + e] = acc[k][e];
-            }
-            if (!consumers_sync(f, w)) return false;
-            for (int c = ctid; c < tn; c += nthr) {
-                float v = red[c];
-                for (int s = 1; s < tpc; ++s) v += red[s * tn + c];
-                data[k * tn + c] = v;
-            }
-            if (!consumers_sync(f, w)) return false;   // red[] may be rewritten after this
-        }
+            for (int e = 0; e < EPC; e += 4)
+                *reinterpret_cast<float4 *>(dst + k * tn + e) =
+                    make_float4(acc[k][e], acc[k][e + 1], acc[k][e + 2], acc[k][e + 3]);
     }
     if (ctid == 0) fr.key[slot] = gstart;
     __syncwarp();
@@ -160,11 +147,12 @@ __device__ __forceinline__ void combine_pair(const ColsumArgs &a, const int64_t 
 // The column sum's flush warp: takes the consumers' records in order until
 // the end mark (key -1).
 template <int GMAX>
-__device__ void colsum_flush_warp(const ColsumArgs &a, const float *ring_data, FlushRing fr,
-                                  const WaitCtl &w) {
+__device__ void colsum_flush_warp(const ColsumArgs &a, const float *ring, int slot_floats,
+                                  int tpc, FlushRing fr, const WaitCtl &w) {
     const PipeArgs &p = a.p;
     const int lane = threadIdx.x & 31;
     const int tn = a.tile_n;
+    const int gw = GMAX * tn;   // floats per partial row of a slot
     const int64_t G = gridDim.x;
     for (;;) {
         const uint32_t slot = ring_slot(fr.k);
@@ -179,7 +167,7 @@ __device__ void colsum_flush_warp(const ColsumArgs &a, const float *ring_data, F
         }
         const int64_t gstart = fr.key[slot];
         if (gstart < 0) return;   // the consumers are done
-        const float *data = ring_data + slot * kColsumSlotFloats;
+        const float *data = ring + slot * slot_floats;
         const ColPos c0 = col_pos(gstart, p.tiles_m, p.tiles_n, GMAX);
         int64_t strip_k[GMAX], K_k[GMAX];
         bool any_split = false;
@@ -202,7 +190,19 @@ __device__ void colsum_flush_warp(const ColsumArgs &a, const float *ring_data, F
             const int64_t col0 = strip * tn;
             float *part = a.partial + (strip * a.kmax + (blockIdx.x - b_first)) * tn;
             for (int c = lane; c < tn; c += 32) {
-                const float v = data[k * tn + c];
+                // the tpc partials of the column, in g order (4 loads at a time)
+                const float *col = data + k * tn + c;
+                float v = col[0];
+                int s = 1;
+                for (; s + 4 <= tpc; s += 4) {
+                    const float t0 = col[s * gw], t1 = col[(s + 1) * gw];
+                    const float t2 = col[(s + 2) * gw], t3 = col[(s + 3) * gw];
+                    v += t0;
+                    v += t1;
+                    v += t2;
+                    v += t3;
+                }
+                for (; s < tpc; ++s) v += col[s * gw];
                 if (K == 1) {
                     if (col0 + c < p.N) a.out[col0 + c] = v;
                 } else {
@@ -243,8 +243,8 @@ __device__ void colsum_flush_warp(const ColsumArgs &a, const float *ring_data, F
 // GMAX: strips per group (= p.col_group; the launch picks the instantiation).
 template <int DT, int GMAX>
 __device__ void consume_colsum(const ColsumArgs &a, const Smem &sm, const WaitCtl &w,
-                               int64_t first, int64_t count, float *red, float *ring_data,
-                               FlushCtl &f, FlushRing &fr) {
+                               int64_t first, int64_t count, float *ring, int slot_floats,
+                               FlushRing &fr) {
     constexpr int EPC = DT == MBT_F32 ? 4 : 8;
     const PipeArgs &p = a.p;
     const int ctid = static_cast<int>(threadIdx.x) - 64;   // warp 0 produces, warp 1 flushes
@@ -282,8 +282,8 @@ __device__ void consume_colsum(const ColsumArgs &a, const Smem &sm, const WaitCt
     for (int64_t j = 0; j < count; ++j, col_next(c, p.tiles_m, p.tiles_n, GMAX)) {
         const int64_t tile = first + j;
         if (c.gstart != group) {
-            if (group >= 0 && !post_group<EPC, GMAX>(a, group, acc, active, q, g, tpc, red,
-                                                     ring_data, f, fr, w, ctid, nthr)) {
+            if (group >= 0 && !post_group<EPC, GMAX>(a.tile_n, group, acc, active, q, g, ring,
+                                                     slot_floats, fr, w, ctid)) {
                 ok = false;
                 break;
             }
@@ -349,11 +349,10 @@ __device__ void consume_colsum(const ColsumArgs &a, const Smem &sm, const WaitCt
         }
     }
     if (ok && group >= 0)
-        ok = post_group<EPC, GMAX>(a, group, acc, active, q, g, tpc, red, ring_data, f, fr, w,
-                                   ctid, nthr);
+        ok = post_group<EPC, GMAX>(a.tile_n, group, acc, active, q, g, ring, slot_floats, fr,
+                                   w, ctid);
     if (ok)   // the end mark for the flush warp
-        post_group<EPC, GMAX>(a, -1, acc, active, q, g, tpc, red, ring_data, f, fr, w, ctid,
-                              nthr);
+        post_group<EPC, GMAX>(a.tile_n, -1, acc, active, q, g, ring, slot_floats, fr, w, ctid);
 }
 
 // WIDE: up to 16 consumer warps, one CTA per SM.
@@ -362,11 +361,7 @@ __global__ void __launch_bounds__(WIDE ? kMaxWideThreads : kMaxThreads + 32, WID
     mbt_colsum_kernel(const __grid_constant__ CUtensorMap map, const ColsumArgs a) {
     extern __shared__ __align__(1024) unsigned char dyn_smem[];
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
-    __shared__ __align__(8) uint64_t flush_bar;
     __shared__ __align__(8) uint64_t ring_bars[2 * kFlushSlots];   // flush ring: full, empty
-    // [tpc][tile_n] partial column sums
-    __shared__ float red[WIDE ? kColsumWideRedFloats : kColsumRedFloats];
-    __shared__ float ring_data[kFlushSlots * kColsumSlotFloats];
     __shared__ int64_t ring_key[kFlushSlots];
     __shared__ int abort_flag;
     Smem sm;
@@ -377,10 +372,15 @@ __global__ void __launch_bounds__(WIDE ? kMaxWideThreads : kMaxThreads + 32, WID
             mbar_init(fr.empty0 + 8u * k, 1);
         }
     }
-    init_pipeline(a.p, sm, bars, &abort_flag, &flush_bar,
-                  static_cast<uint32_t>(a.p.consumer_warps), dyn_smem);   // fences the inits
+    init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);   // fences the inits
     clear_next_tickets(a.clear_ticket, a.clear_n);
     WaitCtl w{a.p.wait_budget_ns, &abort_flag, status_of(a.p)};
+    // The flush ring's slots, after the stages (the host sized the dynamic
+    // shared memory for them: colsum_ring_bytes).
+    constexpr int EPC = DT == MBT_F32 ? 4 : 8;
+    const int slot_floats = 32 * a.p.consumer_warps * EPC * GMAX;
+    float *ring = reinterpret_cast<float *>(dyn_smem + (sm.base - smem_u32(dyn_smem)) +
+                                            a.p.stages * a.p.stage_stride);
     // Contiguous, evenly split range of scheduling units, in strip-major order.
     const int64_t G = gridDim.x;
     const int64_t b = blockIdx.x;
@@ -391,9 +391,9 @@ __global__ void __launch_bounds__(WIDE ? kMaxWideThreads : kMaxThreads + 32, WID
         return;
     }
     if (threadIdx.x < 64) {
-        colsum_flush_warp<GMAX>(a, ring_data, fr, w);
+        colsum_flush_warp<GMAX>(a, ring, slot_floats, a.p.consumer_warps * 32 / (a.p.boxes * 8),
+                                fr, w);
         return;
     }
-    FlushCtl f{smem_u32(&flush_bar), 0u};
-    consume_colsum<DT, GMAX>(a, sm, w, first, last - first, red, ring_data, f, fr);
+    consume_colsum<DT, GMAX>(a, sm, w, first, last - first, ring, slot_floats, fr);
 }

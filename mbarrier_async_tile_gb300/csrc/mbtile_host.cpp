@@ -482,7 +482,14 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
                              (op == MBT_OP_ROWSUM && !flat);
     plan->threads = 32 * ((o.pipeline == 1 ? 0 : 1) + W + (second_warp ? 1 : 0));
     plan->tx_bytes = plan->boxes * tile_m * mbt::kBoxRowBytes;
-    const int64_t smem = static_cast<int64_t>(stages) * plan->stage_bytes + mbt::kSwizzleAtomBytes;
+    int64_t smem = static_cast<int64_t>(stages) * plan->stage_bytes + mbt::kSwizzleAtomBytes;
+    if (op == MBT_OP_COLSUM) {
+        // the flush ring, sized for the widest strip group the plan may take
+        // (the same rule as the split plan's below)
+        const int cg_max =
+            (W > mbt::kMaxConsumerWarps || W % 2 != 0) ? 1 : col_group_for(tile_n, es);
+        smem += mbt::colsum_ring_bytes(W, es, cg_max);
+    }
     if (smem > smem_optin) return MBT_ERR_SMEM;
     plan->smem_bytes = static_cast<int32_t>(smem);
     plan->tiles_m = ceil_div(M, tile_m);

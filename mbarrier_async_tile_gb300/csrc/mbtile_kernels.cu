@@ -1021,7 +1021,6 @@ __device__ bool flush_band(const RowsumArgs &a, int64_t key, float acc, bool act
 // as flush_band.
 constexpr int kMaxConsumerThreads = 32 * kMaxConsumerWarps;
 constexpr int kMaxWideConsumerThreads = 32 * kMaxWideConsumerWarps;
-constexpr int kFlushSlots = 2;   // segments the consumers may run ahead
 
 struct FlushRing {
     uint32_t full0;    // full[slot] at + 8 slot, counts consumer warps
