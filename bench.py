@@ -519,7 +519,8 @@ def bench_gpu(args, rank, world):
     if not args.no_sweep:
         theo = mbt.tile_device_info()["hbm_gbs_theoretical"]
         sweep = config_sweep(dev, clocks, measured_peak()[0], theo,
-                             read_peak=read_ref["gbs"] if read_ref else None)
+                             read_peak=read_ref["gbs"] if read_ref else None,
+                             read_at_size=not args.no_read_ref)
     time.sleep(0.15)
     clocks.stop()
     step_bytes = copy_bytes() + rowsum_bytes()
@@ -915,7 +916,7 @@ def read_reference(dev, clocks, target_s: float = POINT_TARGET_S,
 
 
 def config_sweep(dev, clocks, peak: float, theo: float, target_s: float = POINT_TARGET_S,
-                 select=None, read_peak: float | None = None):
+                 select=None, read_peak: float | None = None, read_at_size: bool = False):
     """Time every CONFIG_POINTS entry (or those `select` keeps) on one side
     stream: the calls captured in a CUDA graph (20 launches, 200 for the
     latency-bound lesson shapes), replayed until about `target_s` of device
@@ -924,7 +925,10 @@ def config_sweep(dev, clocks, peak: float, theo: float, target_s: float = POINT_
     during each point's replays go with it.  Each point's output is checked
     once on the device first (copies bit for bit, sums on sampled rows or
     columns against a float64 reduction within 1e-5 of max(|sum|, sqrt(sum
-    of squares))).  Returns the list of point records."""
+    of squares))).  With `read_at_size`, each row or column sum is also
+    compared with the read reference over as many bytes as the sum reads
+    (measured once per size: a short launch pays the same ramp-up and tail).
+    Returns the list of point records."""
     import mbarrier_async_tile_gb300 as mbt
     import synthetic
 
@@ -932,6 +936,7 @@ def config_sweep(dev, clocks, peak: float, theo: float, target_s: float = POINT_
     side.wait_stream(torch.cuda.current_stream())
     out_points = []
     cache = {}
+    read_at = {}   # bytes -> read reference GB/s at that size
 
     def matrix(cfg, dt, M, N):
         key = (cfg, dt, M, N)
@@ -1067,6 +1072,12 @@ def config_sweep(dev, clocks, peak: float, theo: float, target_s: float = POINT_
         rec["launches_timed"] = reps * n_graph
         rec["parity_ok"] = bool(ok)
         c = clocks.summary(t0, t1)
+        if read_at_size and not latency and op in ("rowsum", "colsum"):
+            rb = (M * N * es + 15) // 16 * 16
+            if rb not in read_at:
+                read_at[rb] = read_reference(dev, clocks, target_s, rb)["gbs"]
+            rec["read_same_size_gbs"] = read_at[rb]
+            rec["frac_of_read_same_size"] = round(rec["gbs"] / read_at[rb], 4)
         rec["clocks"] = {"sm_mhz": c.get("sm_mhz"), "sm_max_mhz": c.get("sm_max_mhz"),
                          "reasons": c.get("reasons"), "samples": c.get("samples")}
         out_points.append(rec)

@@ -87,14 +87,21 @@ struct RowsumArgs {
 // strip (tile_n columns) reduced down the rows.
 constexpr int kMaxColGroup = 2;
 
-// Records the consumers of a row or column sum may post ahead of the flush warp.
+// Records the consumers of a row sum may post ahead of the flush warp.
 constexpr int kFlushSlots = 2;
 
+// The column sum's flush ring has one slot: its consumers post once per strip
+// group they leave (a few times per launch), and a second slot would cost the
+// bf16 8192 x 65536 column sum with 64 x 256 tiles, 3 stages and 8 consumer
+// warps its second CTA per SM (measured 6733 -> 5088 GB/s).
+constexpr int kColsumRingSlots = 1;
+
 // Dynamic shared memory of the column sum's flush ring, after the stages:
-// kFlushSlots slots of one float per consumer thread, element of a 16-byte
-// chunk (16 / es) and strip of a group.
+// kColsumRingSlots slots of one float per consumer thread, element of a
+// 16-byte chunk (16 / es) and strip of a group.
 constexpr int64_t colsum_ring_bytes(int consumer_warps, int es, int col_group) {
-    return static_cast<int64_t>(kFlushSlots) * 32 * consumer_warps * (16 / es) * col_group * 4;
+    return static_cast<int64_t>(kColsumRingSlots) * 32 * consumer_warps * (16 / es) * col_group *
+           4;
 }
 
 // Position of tile t in the strip-group order (PipeArgs.col_group = g >= 1).

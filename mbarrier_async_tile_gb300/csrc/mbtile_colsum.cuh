@@ -52,7 +52,7 @@ __device__ __forceinline__ void chunk_accumulate(float *acc, const uint4 &v) {
 
 // Flush ring of the column sum: when a CTA leaves a group, each consumer
 // thread drops its accumulators into the next ring slot (in dynamic shared
-// memory after the stages: kFlushSlots slots of 32 W x EPC x GMAX floats,
+// memory after the stages: kColsumRingSlots slots of 32 W x EPC x GMAX floats,
 // thread (q, g)'s sums of strip k at g (GMAX tn) + k tn + q EPC) and its warp
 // arrives; no consumer waits for another.  The flush warp adds the tpc
 // partials of each column in g order and does the global part: the column
@@ -66,8 +66,9 @@ template <int EPC, int GMAX>
 __device__ bool post_group(int tn, int64_t gstart, float (*acc)[EPC], bool active, int q,
                            int g, float *ring, int slot_floats, FlushRing &fr, const WaitCtl &w,
                            int ctid) {
-    const uint32_t slot = ring_slot(fr.k);
-    bool ok = wait_bounded(fr.empty0 + 8u * slot, ring_parity(fr.k) ^ 1u, w, true);
+    const uint32_t slot = ring_slot<kColsumRingSlots>(fr.k);
+    bool ok = wait_bounded(fr.empty0 + 8u * slot, ring_parity<kColsumRingSlots>(fr.k) ^ 1u, w,
+                           true);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) {
         if ((threadIdx.x & 31) == 0) {
@@ -155,8 +156,8 @@ __device__ void colsum_flush_warp(const ColsumArgs &a, const float *ring, int sl
     const int gw = GMAX * tn;   // floats per partial row of a slot
     const int64_t G = gridDim.x;
     for (;;) {
-        const uint32_t slot = ring_slot(fr.k);
-        bool ok = wait_bounded(fr.full0 + 8u * slot, ring_parity(fr.k), w, true);
+        const uint32_t slot = ring_slot<kColsumRingSlots>(fr.k);
+        bool ok = wait_bounded(fr.full0 + 8u * slot, ring_parity<kColsumRingSlots>(fr.k), w, true);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
             if (lane == 0) {
@@ -361,13 +362,13 @@ __global__ void __launch_bounds__(WIDE ? kMaxWideThreads : kMaxThreads + 32, WID
     mbt_colsum_kernel(const __grid_constant__ CUtensorMap map, const ColsumArgs a) {
     extern __shared__ __align__(1024) unsigned char dyn_smem[];
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
-    __shared__ __align__(8) uint64_t ring_bars[2 * kFlushSlots];   // flush ring: full, empty
-    __shared__ int64_t ring_key[kFlushSlots];
+    __shared__ __align__(8) uint64_t ring_bars[2 * kColsumRingSlots];   // flush ring: full, empty
+    __shared__ int64_t ring_key[kColsumRingSlots];
     __shared__ int abort_flag;
     Smem sm;
-    FlushRing fr{smem_u32(&ring_bars[0]), smem_u32(&ring_bars[kFlushSlots]), 0u, ring_key};
+    FlushRing fr{smem_u32(&ring_bars[0]), smem_u32(&ring_bars[kColsumRingSlots]), 0u, ring_key};
     if (threadIdx.x == 0) {
-        for (int k = 0; k < kFlushSlots; ++k) {
+        for (int k = 0; k < kColsumRingSlots; ++k) {
             mbar_init(fr.full0 + 8u * k, static_cast<uint32_t>(a.p.consumer_warps));
             mbar_init(fr.empty0 + 8u * k, 1);
         }

@@ -1029,8 +1029,15 @@ struct FlushRing {
     volatile int64_t *key;   // key[slot]: the segment's key, -1 = no more segments
 };
 
-__device__ __forceinline__ uint32_t ring_slot(uint32_t k) { return k % kFlushSlots; }
-__device__ __forceinline__ uint32_t ring_parity(uint32_t k) { return (k / kFlushSlots) & 1u; }
+// Slot and phase parity of record k in a ring of NS slots.
+template <int NS = kFlushSlots>
+__device__ __forceinline__ uint32_t ring_slot(uint32_t k) {
+    return k % NS;
+}
+template <int NS = kFlushSlots>
+__device__ __forceinline__ uint32_t ring_parity(uint32_t k) {
+    return (k / NS) & 1u;
+}
 
 // Post a segment (key >= 0, red: this thread's share) or the end (key < 0).
 // CT: consumer threads a ring slot holds.
