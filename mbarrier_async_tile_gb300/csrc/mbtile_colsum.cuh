@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(WIDE ? kMaxWideThreads : kMaxThreads + 32, WID
             mbar_init(fr.empty0 + 8u * k, 1);
         }
     }
-    init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);   // fences the inits
+    init_pipeline(a.p, sm, bars, &abort_flag, dyn_smem);   // fences the inits
     clear_next_tickets(a.clear_ticket, a.clear_n);
     WaitCtl w{a.p.wait_budget_ns, &abort_flag, status_of(a.p)};
     // The flush ring's slots, after the stages (the host sized the dynamic

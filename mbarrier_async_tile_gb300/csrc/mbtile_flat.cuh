@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
     __shared__ int abort_flag;
     Smem sm;
-    init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);
+    init_pipeline(a.p, sm, bars, &abort_flag, dyn_smem);
     const PipeArgs &p = a.p;
     WaitCtl w{p.wait_budget_ns, &abort_flag, status_of(p)};
     const int64_t G = gridDim.x;
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     if (threadIdx.x == 0)
         for (int k = 0; k < kFlatRowSlots; ++k)
             mbar_init(smem_u32(&row_bar[k]), static_cast<uint32_t>(a.p.consumer_warps));
-    init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);   // fences the inits
+    init_pipeline(a.p, sm, bars, &abort_flag, dyn_smem);   // fences the inits
     const PipeArgs &p = a.p;
     WaitCtl w{p.wait_budget_ns, &abort_flag, status_of(p)};
     const int64_t G = gridDim.x;

@@ -480,7 +480,8 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     // pipeline has no producer warp
     const bool second_warp = op == MBT_OP_COPY_ROWSUM || op == MBT_OP_COLSUM ||
                              (op == MBT_OP_ROWSUM && !flat);
-    plan->threads = 32 * ((o.pipeline == 1 ? 0 : 1) + W + (second_warp ? 1 : 0));
+    plan->threads = 32 * ((o.pipeline == 1 ? 0 : 1) + W + (second_warp ? 1 : 0) +
+                          (op == MBT_OP_COPY_ROWSUM ? 1 : 0));   // the fused flush warp
     plan->tx_bytes = plan->boxes * tile_m * mbt::kBoxRowBytes;
     int64_t smem = static_cast<int64_t>(stages) * plan->stage_bytes + mbt::kSwizzleAtomBytes;
     if (op == MBT_OP_COLSUM) {

@@ -455,7 +455,6 @@ __device__ void produce_rows(const CUtensorMap *map, const RowsumArgs &a, const 
 // them -- release.
 __device__ __forceinline__ void init_pipeline(const PipeArgs &p, Smem &sm,
                                               uint64_t *bars, volatile int *abort_flag,
-                                              uint64_t *extra_bar, uint32_t extra_count,
                                               unsigned char *dyn, bool boxed = false) {
     sm.base = (smem_u32(dyn) + (kSwizzleAtomBytes - 1)) & ~uint32_t(kSwizzleAtomBytes - 1);
     sm.full0 = smem_u32(&bars[0]);
@@ -478,7 +477,6 @@ __device__ __forceinline__ void init_pipeline(const PipeArgs &p, Smem &sm,
             mbar_init(sm.empty0 + 8u * s,
                       static_cast<uint32_t>(p.consumer_warps + p.empty_extra));
         }
-        if (extra_bar != nullptr) mbar_init(smem_u32(extra_bar), extra_count);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -749,7 +747,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
     __shared__ int abort_flag;
     Smem sm;
-    init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);
+    init_pipeline(a.p, sm, bars, &abort_flag, dyn_smem);
     WaitCtl w{a.p.wait_budget_ns, &abort_flag, status_of(a.p)};
     // Tiles b, b + G, b + 2G, ... in row-major tile order.
     const int64_t G = gridDim.x;
@@ -781,7 +779,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
     __shared__ int abort_flag;
     Smem sm;
-    init_pipeline(a.p, sm, bars, &abort_flag, nullptr, 0, dyn_smem);
+    init_pipeline(a.p, sm, bars, &abort_flag, dyn_smem);
     const PipeArgs &p = a.p;
     WaitCtl w{p.wait_budget_ns, &abort_flag, status_of(p)};
     const int64_t G = gridDim.x;
@@ -863,26 +861,6 @@ __device__ __forceinline__ int64_t unit_owner(int64_t x, int64_t gran, int64_t u
     return ((x / gran + 1) * G - 1) / units;
 }
 
-struct FlushCtl {
-    uint32_t bar;       // mbarrier counting consumer warps
-    uint32_t parity;    // next phase parity to wait for
-};
-
-// Bounded rendezvous of all consumer warps (replaces a named barrier so that a
-// consumer warp which gave up cannot leave the others blocked forever).
-__device__ bool consumers_sync(FlushCtl &f, const WaitCtl &w) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(f.bar);
-    bool ok = wait_bounded(f.bar, f.parity, w, true);
-    ok = __all_sync(0xffffffffu, ok);
-    f.parity ^= 1u;
-    if (!ok && (threadIdx.x & 31) == 0) {
-        report_timeout(w, 1, kMaxStages, f.parity ^ 1u);
-        *w.abort = 1;
-    }
-    return ok;
-}
-
 // Where a finished segment (a CTA's part of band `key`) goes: the band's K
 // contributors are the CTAs owning its units, this CTA's slot its rank among
 // them.
@@ -902,8 +880,8 @@ __device__ __forceinline__ FlushTarget flush_target(const RowsumArgs &a, int64_t
 }
 
 // One warp adds K partial slots (`stride` floats apart) for the entries
-// lane, lane + 32, ... < n: per entry in slot order, as combine_slots does,
-// so the same bits; writes dst[c] for c < valid and leaves the slots zero.
+// lane, lane + 32, ... < n: per entry in slot order (so the same bits for
+// every grid); writes dst[c] for c < valid and leaves the slots zero.
 // Each lane's entries (at most PL) and B slots are loaded together, so the
 // addition takes about K / B load round trips instead of one per entry.
 template <int PL, int B>
@@ -946,79 +924,17 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
-// The band's K partial slots of one row, added in slot order; the loads are
-// issued B at a time so that their latencies overlap.  Leaves the slots
-// zero-filled (a workspace may next serve a shape whose tickets lie there).
-template <int B>
-__device__ __forceinline__ float combine_slots(float *base, int64_t K, int64_t stride) {
-    float total = 0.f;
-    for (int64_t k0 = 0; k0 < K; k0 += B) {
-        float v[B];
-#pragma unroll
-        for (int u = 0; u < B; ++u) v[u] = k0 + u < K ? __ldcg(base + (k0 + u) * stride) : 0.f;
-#pragma unroll
-        for (int u = 0; u < B; ++u)
-            if (k0 + u < K) total += v[u];
-    }
-    for (int64_t k = 0; k < K; ++k) base[k * stride] = 0.f;   // leave the workspace zero-filled
-    return total;
-}
-
-
-
-// Finish one segment: combine the threads of each row, then either write the
-// row sums (sole contributor) or deposit the partials in the segment's slot
-// and let the last contributor to arrive add the band's slots in slot order.
-__device__ bool flush_band(const RowsumArgs &a, int64_t key, float acc, bool active,
-                           int row, int sub, int tpr, float *red, int *last_flag,
-                           FlushCtl &f, const WaitCtl &w, int ctid) {
-    const PipeArgs &p = a.p;
-    red[ctid] = acc;
-    if (!consumers_sync(f, w)) return false;
-    const FlushTarget ft = flush_target(a, key);
-    const int64_t grow = ft.band * p.tile_m + row;
-    float v = 0.f;
-    if (active && sub == 0) {
-        v = red[row];
-        for (int s = 1; s < tpr; ++s) v += red[row + s * p.tile_m];
-    }
-    if (ft.K == 1) {
-        if (active && sub == 0 && grow < p.M) a.out[grow] = v;
-        return consumers_sync(f, w);   // red[] may be rewritten after this
-    }
-    float *slot = a.partial + (ft.band * a.kmax + ft.slot) * p.tile_m;
-    if (active && sub == 0) {
-        slot[row] = v;
-        fence_acq_rel_gpu();
-    }
-    if (!consumers_sync(f, w)) return false;
-    if (ctid == 0) {
-        const int old = atomicAdd(&a.ticket[ft.band], 1);
-        *last_flag = (old == ft.K - 1);
-    }
-    if (!consumers_sync(f, w)) return false;
-    if (*last_flag) {
-        fence_acq_rel_gpu();
-        if (active && sub == 0) {
-            const float total = combine_slots<4>(a.partial + ft.band * a.kmax * p.tile_m + row,
-                                                 ft.K, p.tile_m);
-            if (grow < p.M) a.out[grow] = total;
-        }
-        if (ctid == 0) a.ticket[ft.band] = 0;
-    }
-    return true;
-}
-
-// Flush ring of the row sum without the fused store warp: the consumers hand
-// each finished segment (the CTA's part of a band) -- one fp32 per
-// consumer thread and the segment's key -- to a flush warp through a ring of
-// shared-memory slots (full: all consumer warps arrived; empty: the flush
-// warp has read the slot), and go on with the next segment at once.  The
-// flush warp combines each row's threads in `sub` order and does the global
-// part (the row sums, or the segment's partials, the band's ticket and the
-// last contributor's ordered addition), so the global round trips of a
-// segment change no longer stall the pipeline.  Same arithmetic, same order
-// as flush_band.
+// Flush ring of the row sum: the consumers hand each finished segment (the
+// CTA's part of a band) -- one fp32 per consumer thread and the segment's key
+// -- to a flush warp through a ring of shared-memory slots (full: all
+// consumer warps arrived; empty: the flush warp has read the slot), and go on
+// with the next segment at once.  The flush warp combines each row's threads
+// in `sub` order and does the global part (the row sums, or the segment's
+// partials, the band's ticket and the last contributor's ordered addition),
+// so the global round trips of a segment change never stall the pipeline.
+// (Measured when the consumers still did that part themselves, between
+// rendezvous of all consumer warps: the CTAs crossing a band change stalled
+// ~3 us; in the fused kernel, moving it to a flush warp gained 0.2-0.5 %.)
 constexpr int kMaxConsumerThreads = 32 * kMaxConsumerWarps;
 constexpr int kMaxWideConsumerThreads = 32 * kMaxWideConsumerWarps;
 
@@ -1065,7 +981,7 @@ __device__ bool flush_post(FlushRing &fr, float *red, float acc, int64_t key, in
 // The flush warp: takes the consumers' records in order until the end mark.
 // A band this CTA reduced alone gets its row sums written; otherwise the
 // CTA's partials go to its slot and the band's last contributor to arrive
-// adds the K slots in slot order (the order of flush_band).
+// adds the K slots in slot order.
 template <int CT>
 __device__ void flush_warp(const RowsumArgs &a, const float *red, FlushRing fr,
                            const WaitCtl &w) {
@@ -1134,10 +1050,10 @@ __device__ void flush_warp(const RowsumArgs &a, const float *red, FlushRing fr,
 // the per-box kernels give bit-identical sums.  With `boxed` (host-checked:
 // tpr a multiple of boxes, and the threads of one box whole warps) every warp
 // reads one box only, and waits for and releases that box alone.
-template <int DT, bool boxed, bool ring, int CT>
+template <int DT, bool boxed, int CT>
 __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCtl &w,
-                               const volatile StageInfo *info, float *red, int *last_flag,
-                               FlushCtl &f, FlushRing &fr, int cwarp0) {
+                               const volatile StageInfo *info, float *red, FlushRing &fr,
+                               int cwarp0) {
     const PipeArgs &p = a.p;
     const int ctid = static_cast<int>(threadIdx.x) - 32 * cwarp0;
     const int lane = threadIdx.x & 31;
@@ -1188,10 +1104,7 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
             break;
         }
         if (k != key) {
-            if (key >= 0 &&
-                !(ring ? flush_post<CT>(fr, red, acc, key, ctid, w)
-                       : flush_band(a, key, acc, active, row, sub, tpr, red, last_flag, f, w,
-                                    ctid))) {
+            if (key >= 0 && !flush_post<CT>(fr, red, acc, key, ctid, w)) {
                 ok = false;
                 break;
             }
@@ -1236,53 +1149,46 @@ __device__ void consume_rowsum(const RowsumArgs &a, const Smem &sm, const WaitCt
         }
     }
     if (!ok) return;
-    if (key >= 0) {
-        if (ring)
-            ok = flush_post<CT>(fr, red, acc, key, ctid, w);
-        else
-            flush_band(a, key, acc, active, row, sub, tpr, red, last_flag, f, w, ctid);
-    }
-    if (ring && ok) flush_post<CT>(fr, red, 0.f, -1, ctid, w);   // end mark for the flush warp
+    if (key >= 0) ok = flush_post<CT>(fr, red, acc, key, ctid, w);
+    if (ok) flush_post<CT>(fr, red, 0.f, -1, ctid, w);   // end mark for the flush warp
 }
 
 // FUSED: warp 1 writes every landed stage to dst (bulk tensor stores; LSU
 // stores for tiles with a partial 16-byte chunk at column N) and is the one
-// extra arrival on each empty barrier; the row-sum warps follow it.  Without
-// it, warp 1 is the flush warp (see flush_warp).
+// extra arrival on each empty barrier, warp 2 is the flush warp (see
+// flush_warp) and the row-sum warps follow.  Without it, warp 1 is the flush
+// warp.
 // BOXED: a full/empty pair per (stage, box) (never with FUSED).  Each barrier
 // layout is its own instantiation, so neither carries the other's code.
 // WIDE: up to 16 consumer warps, one CTA per SM (stage-wide pairs, no store
 // warp).
 template <int DT, bool FUSED, bool BOXED, bool WIDE = false>
-__global__ void __launch_bounds__(WIDE ? kMaxWideThreads : kMaxThreads + 32, WIDE ? 1 : 2)
+__global__ void __launch_bounds__(WIDE ? kMaxWideThreads : kMaxThreads + (FUSED ? 64 : 32),
+                                  WIDE ? 1 : 2)
     mbt_rowsum_kernel(const __grid_constant__ CUtensorMap map,
                       const __grid_constant__ CUtensorMap dst_map, const RowsumArgs a) {
     extern __shared__ __align__(1024) unsigned char dyn_smem[];
     // Per-box barrier pairs only without the store warp (which reads whole stages).
     static_assert(!(FUSED && BOXED), "the store warp reads whole stages");
     static_assert(!(WIDE && (FUSED || BOXED)), "wide CTAs: stage-wide pairs, no store warp");
-    constexpr bool ring = !FUSED;
     constexpr int CT = WIDE ? kMaxWideConsumerThreads : kMaxConsumerThreads;
     __shared__ __align__(8) uint64_t bars[BOXED ? 16 * kMaxStages : 2 * kMaxStages];
-    __shared__ __align__(8) uint64_t flush_bar;
     __shared__ __align__(8) uint64_t ring_bars[2 * kFlushSlots];   // flush ring: full, empty
-    // By row-sum consumer thread (one block per flush-ring slot without FUSED).
-    __shared__ float red[ring ? kFlushSlots * CT : CT];
+    // By row-sum consumer thread, one block per flush-ring slot.
+    __shared__ float red[kFlushSlots * CT];
     __shared__ int abort_flag;
-    __shared__ int last_flag;
     __shared__ StageInfo info[8 * kMaxStages];   // per (stage, box), from the producer
     __shared__ int64_t ring_key[kFlushSlots];
     Smem sm;
     constexpr bool boxed = BOXED;
     FlushRing fr{smem_u32(&ring_bars[0]), smem_u32(&ring_bars[kFlushSlots]), 0u, ring_key};
-    if (ring && threadIdx.x == 0) {
+    if (threadIdx.x == 0) {
         for (int k = 0; k < kFlushSlots; ++k) {
             mbar_init(fr.full0 + 8u * k, static_cast<uint32_t>(a.p.consumer_warps));
             mbar_init(fr.empty0 + 8u * k, 1);
         }
     }
-    init_pipeline(a.p, sm, bars, &abort_flag, &flush_bar,
-                  static_cast<uint32_t>(a.p.consumer_warps), dyn_smem, boxed);   // fences the inits
+    init_pipeline(a.p, sm, bars, &abort_flag, dyn_smem, boxed);   // fences the inits
     clear_next_tickets(a.clear_ticket, a.clear_n);
     WaitCtl w{a.p.wait_budget_ns, &abort_flag, status_of(a.p)};
     // Contiguous, evenly split range of scheduling units, in band-major order.
@@ -1307,8 +1213,11 @@ __global__ void __launch_bounds__(WIDE ? kMaxWideThreads : kMaxThreads + 32, WID
         }
         return;
     }
-    FlushCtl f{smem_u32(&flush_bar), 0u};
-    consume_rowsum<DT, boxed, ring, CT>(a, sm, w, info, red, &last_flag, f, fr, 2);
+    if (FUSED && threadIdx.x < 96) {   // the fused kernel's flush warp
+        flush_warp<CT>(a, red, fr, w);
+        return;
+    }
+    consume_rowsum<DT, boxed, CT>(a, sm, w, info, red, fr, FUSED ? 3 : 2);
 }
 
 __global__ void mbt_accumulate_kernel(float *acc, const float *part, int64_t n, int first) {

@@ -333,11 +333,12 @@ def test_plan_default_grid_follows_bytes_in_flight():
                  ctas_per_sm=5)["grid"] == 456
 
 
-def test_plan_fused_adds_a_store_warp():
+def test_plan_fused_adds_a_store_warp_and_a_flush_warp():
     p = _plan(mbt.OP_COPY_ROWSUM, 24577, 16383, 128, 64, 3, torch.float16, fit=2, ws=True,
               ld_src=16384, ld_dst=16384)
-    # 16 KB stages, one held by the store in flight: 2 live x 2 CTAs = 64 KB per SM
-    assert p["grid"] == 304 and p["consumer_warps"] == 8 and p["threads"] == 32 * 10
+    # 16 KB stages, one held by the store in flight: 2 live x 2 CTAs = 64 KB per SM;
+    # producer, store warp, flush warp and 8 consumer warps
+    assert p["grid"] == 304 and p["consumer_warps"] == 8 and p["threads"] == 32 * 11
 
 
 def test_plan_tiled_rowsum_adds_a_flush_warp():

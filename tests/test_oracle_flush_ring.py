@@ -2,8 +2,8 @@
 band or strip to a flush warp through a few shared-memory slots with the
 full/empty mbarrier protocol of the tile ring, run the other way round),
 checked on the oracle's discrete-event model under random interleavings:
-every record arrives in order and intact, for the kernels' 2 slots and other
-depths.  Planted mistakes -- the writers starting at the readers' parity, a
+every record arrives in order and intact, for the row sum's 2 slots, the
+column sum's 1 and other depths.  Planted mistakes -- the writers starting at the readers' parity, a
 full barrier expecting one arrival instead of one per writer warp, the
 reader starting at the writers' parity -- are each caught."""
 import pytest
