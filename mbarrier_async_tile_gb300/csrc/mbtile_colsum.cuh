@@ -10,9 +10,10 @@
 //
 // Order.  The column strips are taken in groups of col_group adjacent strips
 // (2 strips where a tile row is 128 bytes, so that the copies in flight read
-// 256 contiguous bytes of each row, not scattered 128-byte pieces); within a group the
-// tiles go band by band, left to right.  Each consumer thread keeps one set of
-// accumulators per strip of the group.
+// 256 contiguous bytes of each row, not scattered 128-byte pieces; and where one
+// CTA per SM streams alone, 2 strips of up to 512 bytes, 1 KB per row); within
+// a group the tiles go band by band, left to right.  Each consumer thread keeps
+// one set of accumulators per strip of the group.
 //
 // Consumer mapping.  A tile row holds cpr = boxes x 8 chunks of 16 bytes;
 // tpc = 32 W / cpr threads share each chunk column: thread (q, g) with
@@ -20,9 +21,9 @@
 // into EPC fp32 accumulators (EPC = elements per chunk: 8, or 4 for fp32).
 // Eight consecutive threads read eight consecutive rows of the same chunk,
 // which the 128-byte swizzle spreads over all banks.  When a CTA leaves a
-// group, the tpc partial sums of each column are added in g order; a strip
-// that several CTAs share is combined by the last of them in CTA order
-// (tickets and partials in the caller's workspace, left zeroed).
+// group, the tpc partial sums of each column are added in g order (by the
+// flush warp); a strip that several CTAs share is combined by the last of them
+// in CTA order (tickets and partials in the workspace, left zeroed).
 //
 // Included by mbtile_kernels.cu inside its anonymous namespace: it uses that
 // file's PTX wrappers, bounded waits, producer, status word and log.
@@ -94,54 +95,59 @@ __device__ bool post_group(int tn, int64_t gstart, float (*acc)[EPC], bool activ
 }
 
 // The last contributor's addition for the strips of a pair that this CTA
-// completes (bit k of `lasts`: strip k of the pair; 128-byte tile rows, so at
-// most 2 x 64 columns).  Entry e = k tn + c (strip k, column c) belongs to
-// lane e % 32; for each entry the K_k partial slots are added in slot order
-// (as warp_add_slots does, so the same bits), the column sum is written and
-// the slots are left zero.  A lane's 4 entries and 8 slots are loaded
-// together, both strips at once: a pair of strips with 5 contributors each
-// costs one load round trip, not three per strip one strip after the other.
+// completes (bit k of `lasts`: strip k of the pair).  Entry e = k tn + c
+// (strip k, column c) of a 128-entry chunk of the pair belongs to lane
+// e % 32; for each entry the K_k partial slots are added in slot order (as
+// warp_add_slots does, so the same bits), the column sum is written and the
+// slots are left zero.  A lane's 4 entries and 8 slots are loaded together,
+// both strips at once: a pair of 128-byte strips (at most 2 x 64 columns, one
+// chunk) with 5 contributors each costs one load round trip, not three per
+// strip one strip after the other.  Wider strips (pairs where one CTA per SM
+// runs) take one chunk after another.
 __device__ __forceinline__ void combine_pair(const ColsumArgs &a, const int64_t *strip_k,
                                              const int64_t *K_k, unsigned lasts, int tn) {
     constexpr int PL = 4, B = 8;
     const int lane = threadIdx.x & 31;
-    float *slot0[PL];
-    int kn[PL];
-    int kmax_all = 0;
+    for (int e0 = 0; e0 < 2 * tn; e0 += 32 * PL) {
+        float *slot0[PL];
+        int kn[PL];
+        int kmax_all = 0;
 #pragma unroll
-    for (int i = 0; i < PL; ++i) {
-        const int e = lane + 32 * i;
-        const int k = e >= tn ? 1 : 0;
-        const bool on = e < 2 * tn && ((lasts >> k) & 1u);
-        slot0[i] = a.partial + (k ? strip_k[1] : strip_k[0]) * a.kmax * tn + (e - k * tn);
-        kn[i] = on ? static_cast<int>(k ? K_k[1] : K_k[0]) : 0;
-        kmax_all = kn[i] > kmax_all ? kn[i] : kmax_all;
-    }
-    float acc[PL];
+        for (int i = 0; i < PL; ++i) {
+            const int e = e0 + lane + 32 * i;
+            const int k = e >= tn ? 1 : 0;
+            const bool on = e < 2 * tn && ((lasts >> k) & 1u);
+            slot0[i] = a.partial + (k ? strip_k[1] : strip_k[0]) * a.kmax * tn + (e - k * tn);
+            kn[i] = on ? static_cast<int>(k ? K_k[1] : K_k[0]) : 0;
+            kmax_all = kn[i] > kmax_all ? kn[i] : kmax_all;
+        }
+        float acc[PL];
 #pragma unroll
-    for (int i = 0; i < PL; ++i) acc[i] = 0.f;
-    for (int k0 = 0; k0 < kmax_all; k0 += B) {
-        float v[B][PL];
+        for (int i = 0; i < PL; ++i) acc[i] = 0.f;
+        for (int k0 = 0; k0 < kmax_all; k0 += B) {
+            float v[B][PL];
 #pragma unroll
-        for (int u = 0; u < B; ++u)
+            for (int u = 0; u < B; ++u)
 #pragma unroll
-            for (int i = 0; i < PL; ++i)
-                v[u][i] = k0 + u < kn[i] ? __ldcg(slot0[i] + static_cast<int64_t>(k0 + u) * tn)
-                                         : 0.f;
+                for (int i = 0; i < PL; ++i)
+                    v[u][i] = k0 + u < kn[i]
+                                  ? __ldcg(slot0[i] + static_cast<int64_t>(k0 + u) * tn)
+                                  : 0.f;
 #pragma unroll
-        for (int u = 0; u < B; ++u)
+            for (int u = 0; u < B; ++u)
 #pragma unroll
-            for (int i = 0; i < PL; ++i)
-                if (k0 + u < kn[i]) acc[i] += v[u][i];
-    }
+                for (int i = 0; i < PL; ++i)
+                    if (k0 + u < kn[i]) acc[i] += v[u][i];
+        }
 #pragma unroll
-    for (int i = 0; i < PL; ++i) {
-        if (kn[i] == 0) continue;
-        const int e = lane + 32 * i;
-        const int k = e >= tn ? 1 : 0;
-        const int64_t col = (k ? strip_k[1] : strip_k[0]) * tn + (e - k * tn);
-        if (col < a.p.N) a.out[col] = acc[i];
-        for (int j = 0; j < kn[i]; ++j) slot0[i][static_cast<int64_t>(j) * tn] = 0.f;
+        for (int i = 0; i < PL; ++i) {
+            if (kn[i] == 0) continue;
+            const int e = e0 + lane + 32 * i;
+            const int k = e >= tn ? 1 : 0;
+            const int64_t col = (k ? strip_k[1] : strip_k[0]) * tn + (e - k * tn);
+            if (col < a.p.N) a.out[col] = acc[i];
+            for (int j = 0; j < kn[i]; ++j) slot0[i][static_cast<int64_t>(j) * tn] = 0.f;
+        }
     }
 }
 
@@ -267,7 +273,7 @@ __device__ void consume_colsum(const ColsumArgs &a, const Smem &sm, const WaitCt
     int64_t group = -1;   // order position of the current group's first tile
     const int most = (p.tile_m + tpc - 1) / tpc;
     const int rounds = (most + CV - 1) / CV;
-    // Strip pairs (128-byte tile rows) are planned with tpc a multiple of 8, so
+    // Strip pairs are planned with tpc a multiple of 8, so
     // rows g, g + tpc, ... of chunk q share one swizzle term: their stage
     // offsets are one per-thread base plus k tpc 128 bytes, and a whole-height
     // tile gives every thread the same row count.  Measured on fp16 24577 x

@@ -177,11 +177,27 @@ int32_t most_contributors(int64_t tiles_n, int64_t num_tiles, int64_t G) {
 // span at least this much (narrow tiles otherwise read scattered 128-byte
 // pieces of each row: measured 4.1 against 5.7-6.2 TB/s for 256 bytes and up).
 constexpr int64_t kColGroupBytes = 256;
+// ... and at least this much where one CTA per SM streams alone: bf16
+// 8192 x 65536 with 64 x 256 tiles at 4 stages ran at 4983 GB/s with one
+// 512-byte strip at a time, 6219 with strip pairs (with two CTAs per SM, pairs
+// lost 1.3 % at 2 stages).
+constexpr int64_t kColGroupBytesOnePerSm = 1024;
 
-int col_group_for(int tile_n, int es) {
+int col_group_for(int tile_n, int es, bool one_per_sm = false) {
     const int64_t row = static_cast<int64_t>(tile_n) * es;
-    return static_cast<int>(std::min<int64_t>(mbt::kMaxColGroup,
-                                              std::max<int64_t>(1, kColGroupBytes / row)));
+    const int64_t want = one_per_sm ? kColGroupBytesOnePerSm : kColGroupBytes;
+    return static_cast<int>(
+        std::min<int64_t>(mbt::kMaxColGroup, std::max<int64_t>(1, want / row)));
+}
+
+// Strips per group of a split column sum with W consumer warps: one for the
+// wide CTA; a pair only where its tpc = 32 W / (8 boxes) threads per chunk
+// column are a multiple of 8, so that each thread's rows share one swizzle
+// term (the launch refuses other pairs).
+int colsum_group(int W, int tile_n, int es, int boxes, bool one_per_sm) {
+    if (W > mbt::kMaxConsumerWarps) return 1;
+    const int cg = col_group_for(tile_n, es, one_per_sm);
+    return cg > 1 && (32 * W / (8 * boxes)) % 8 != 0 ? 1 : cg;
 }
 
 // Most CTAs that share one column strip when num_tiles tiles in strip-group
@@ -487,8 +503,7 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     if (op == MBT_OP_COLSUM) {
         // the flush ring, sized for the widest strip group the plan may take
         // (the same rule as the split plan's below)
-        const int cg_max =
-            (W > mbt::kMaxConsumerWarps || W % 2 != 0) ? 1 : col_group_for(tile_n, es);
+        const int cg_max = colsum_group(W, tile_n, es, plan->boxes, one_per_sm);
         smem += mbt::colsum_ring_bytes(W, es, cg_max);
     }
     if (smem > smem_optin) return MBT_ERR_SMEM;
@@ -531,11 +546,7 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     const int64_t sums_per_group = cols ? tile_n : tile_m;
     if (with_workspace) {
         const int64_t G = std::min<int64_t>(plan->num_tiles, cap);
-        // (the wide column sum walks one strip at a time; strip pairs need an
-        // even warp count: their threads per chunk column, 4 W, a multiple of 8)
-        const int cg = !cols ? 0
-                       : (W > mbt::kMaxConsumerWarps || W % 2 != 0) ? 1
-                                                                     : col_group_for(tile_n, es);
+        const int cg = cols ? colsum_group(W, tile_n, es, plan->boxes, one_per_sm) : 0;
         const int32_t kmax =
             cols ? colsum_contributors(plan->tiles_m, plan->tiles_n, cg, plan->num_tiles, G)
                  : most_contributors(group_tiles, plan->num_tiles, G);

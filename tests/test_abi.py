@@ -281,8 +281,9 @@ def test_plan_default_grid_follows_bytes_in_flight():
     p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True)
     assert p["grid"] == 152 and p["consumer_warps"] == 16 and p["threads"] == 32 * 18
     assert p["box_barriers"] == 0
+    # (one CTA per SM: its 512-byte strips walked in pairs)
     p = _plan(mbt.OP_COLSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True)
-    assert p["grid"] == 152 and p["consumer_warps"] == 8 and p["col_group"] == 1
+    assert p["grid"] == 152 and p["consumer_warps"] == 8 and p["col_group"] == 2
     p = _plan(mbt.OP_COLSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True,
               consumer_warps=16)
     assert p["threads"] == 32 * 18 and p["col_group"] == 1
@@ -303,6 +304,14 @@ def test_plan_default_grid_follows_bytes_in_flight():
         p = _plan(mbt.OP_COLSUM, 12289, 8191, 128, 32, 3, torch.float32, fit=2, ws=True,
                   ld_src=8192, consumer_warps=W)
         assert p["col_group"] == cg, W
+    # wider strips in pairs only where one CTA per SM runs, and only with tpc =
+    # 32 W / (8 boxes) a multiple of 8 (512-byte rows: W = 8)
+    for fit, W, cg in ((2, 8, 1), (1, 8, 2), (1, 4, 1), (1, 6, 1)):
+        p = _plan(mbt.OP_COLSUM, 8192, 65536, 64, 256, 4 if fit == 1 else 2, torch.bfloat16,
+                  fit=fit, ws=True, consumer_warps=W)
+        assert p["col_group"] == cg, (fit, W)
+    p = _plan(mbt.OP_COLSUM, 8192, 65536, 128, 128, 4, torch.bfloat16, fit=1, ws=True)
+    assert p["col_group"] == 2 and p["consumer_warps"] == 8        # 256-byte rows: tpc 16
     p = _plan(mbt.OP_COPY_ROWSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True)
     assert p["consumer_warps"] <= 8
     assert _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 8, torch.float16)["consumer_warps"] == 4

@@ -181,10 +181,34 @@ def test_ragged_full_size_configs():
         assert worst <= ROWSUM_RTOL, (dtype, worst, rel)
 
 
+@pytest.mark.parametrize("case", [("bf16", 2048, 4096, 64, 256), ("bf16", 2048, 4096, 128, 128),
+                                  ("f32", 2048, 2048, 64, 64)],
+                         ids=["512-byte-strips", "256-byte-strips", "256-byte-f32-strips"])
+def test_wide_strip_pairs_where_one_cta_per_sm_runs(case):
+    """With one CTA per SM (here asked for: ctas_per_sm=1, 4 stages), strips of
+    256 and 512 bytes are walked in pairs.  The grid (one CTA per SM) is large
+    against these shapes, so each strip has 10-19 contributors: the last one
+    adds more than 8 slots per column, a pair's 512 or 256 columns in chunks of
+    128.  Every column against the oracle; repeat calls bit-identical."""
+    dtype, M, N, tm, tn = case
+    x = synthetic.make_matrix(M, N, dtype, "normal", seed=M + tn)
+    plan = mbt.tile_plan_device(mbt.OP_COLSUM, M, N, tm, tn, 4, synthetic.DTYPES[dtype],
+                                ctas_per_sm=1)
+    assert plan["split"] == 1 and plan["col_group"] == 2 and plan["kmax"] > 8, plan
+    xd = x.cuda()
+    out = mbt.tile_colsum(xd, None, tm, tn, 4, ctas_per_sm=1)
+    assert mbt.tile_status()[0] == 0
+    worst, rel, _ = colsum_errors(out, x)
+    assert worst <= ROWSUM_RTOL, (worst, rel)
+    again = mbt.tile_colsum(xd, None, tm, tn, 4, ctas_per_sm=1)
+    assert mbt.tile_status()[0] == 0
+    assert torch.equal(out.view(torch.int32), again.view(torch.int32))
+
+
 @pytest.mark.parametrize("split", [False, True])
 def test_flush_ring_wraps_many_times(split):
     """Three CTAs over 1024 one-tile strips (and 512 strip pairs): each CTA's
-    consumers post hundreds of strip groups through the two-slot flush ring."""
+    consumers post hundreds of strip groups through the one-slot flush ring."""
     for M, N, tm, tn in ((64, 262144, 64, 256), (100, 65536, 128, 64)):
         x = synthetic.make_matrix(M, N, "bf16", "normal", seed=M + 5)
         out = mbt.tile_colsum(x.cuda(), None, tm, tn, 2, max_ctas=3, split=split)
