@@ -260,13 +260,18 @@ int wanted_ctas_per_sm(int op, const mbt_opts &o, int stages, int64_t stage_byte
 // sum at ~4.9 TB/s, 2 % slower with 16 (so it keeps 8 unless asked).  Two
 // CTAs of 8 at 2 stages: 6.6-6.8 TB/s for both.  The one-CTA ceiling does not
 // move with stages, consumer warps or the form of the barrier wait.
-int consumer_warps_for(int op, int tile_m, int stages, const mbt_opts &o, int wanted_ctas,
-                       int64_t n_mod, bool flat, bool one_per_sm, bool wide_ok) {
+int consumer_warps_for(int op, int tile_m, int boxes, int stages, const mbt_opts &o,
+                       int wanted_ctas, int64_t n_mod, bool flat, bool one_per_sm, bool wide_ok) {
     if (bulk_stores(op, o, n_mod)) return 1;   // one thread issues the stores
     if (o.consumer_warps) return o.consumer_warps;
     if (flat && op == MBT_OP_ROWSUM) return wanted_ctas <= 2 ? 8 : 4;   // no tile rows
     if (op == MBT_OP_ROWSUM && one_per_sm && wide_ok) return mbt::kMaxWideConsumerWarps;
     if (op == MBT_OP_ROWSUM && wanted_ctas == 2 && stages == 3 && tile_m <= 128) return 4;
+    // The fused copy + row sum on tiles of one 128-byte box and at most 128
+    // rows: 4 row-sum warps, whose reads of the stage compete less with the
+    // store warp's (fp32 12289 x 8191 128 x 32, fp16 24577 x 16383 and 16384^2
+    // 128 x 64, 2 CTAs per SM: +0.5-0.8 % at 3 stages, +0.8-1.8 % at 4).
+    if (op == MBT_OP_COPY_ROWSUM && boxes == 1 && tile_m <= 128) return 4;
     if (op != MBT_OP_COPY) return (wanted_ctas <= 2 || tile_m > 128) ? 8 : 4;
     return kDefaultConsumerWarps;
 }
@@ -480,8 +485,8 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
     // wide column sums walk one strip at a time (a split plan of 128-byte tiles
     // walks two)
     const bool wide_ok = op == MBT_OP_ROWSUM || !with_workspace || col_group_for(tile_n, es) == 1;
-    const int W = consumer_warps_for(op, tile_m, stages, o, wanted, n_mod, flat, one_per_sm,
-                                     wide_ok);
+    const int W = consumer_warps_for(op, tile_m, plan->boxes, stages, o, wanted, n_mod, flat,
+                                     one_per_sm, wide_ok);
     plan->bulk_stores = bulk_stores(op, o, n_mod) || op == MBT_OP_COPY_ROWSUM ? 1 : 0;
     // Row sums: at least one thread per tile row; column sums: at least one
     // thread per 16-byte chunk column of a tile row.

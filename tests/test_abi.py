@@ -346,8 +346,10 @@ def test_plan_fused_adds_a_store_warp_and_a_flush_warp():
     p = _plan(mbt.OP_COPY_ROWSUM, 24577, 16383, 128, 64, 3, torch.float16, fit=2, ws=True,
               ld_src=16384, ld_dst=16384)
     # 16 KB stages, one held by the store in flight: 2 live x 2 CTAs = 64 KB per SM;
-    # producer, store warp, flush warp and 8 consumer warps
-    assert p["grid"] == 304 and p["consumer_warps"] == 8 and p["threads"] == 32 * 11
+    # producer, store warp, flush warp and (one-box tiles of 128 rows) 4 row-sum warps
+    assert p["grid"] == 304 and p["consumer_warps"] == 4 and p["threads"] == 32 * 7
+    p = _plan(mbt.OP_COPY_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16, fit=2, ws=True)
+    assert p["consumer_warps"] == 8 and p["threads"] == 32 * 11   # four-box tiles: 8
 
 
 def test_plan_tiled_rowsum_adds_a_flush_warp():
