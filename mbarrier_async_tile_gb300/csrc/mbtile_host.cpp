@@ -248,11 +248,14 @@ int wanted_ctas_per_sm(int op, const mbt_opts &o, int stages, int64_t stage_byte
 // Row sums: 8 consumer warps (256 threads: an even split of any power-of-two
 // tile_m <= 256) when at most two CTAs share an SM; 4 warps when three or more
 // do (then registers would not fit 8), unless the tile has more rows than 128
-// threads can own.  The tiled row sum also takes 4 at exactly 3 stages when
+// threads can own.  The tiled row sum also takes 4 at 3 or more stages when
 // two CTAs share an SM: measured on 32 KB tiles (bf16 64x256 and 32x512, fp16
-// 128x128), 4 warps beat 8 there by 1.5-2.9 %, while at 2 stages 8 beat 4 by
-// up to 4 %, and at 4 stages (wanted_ctas is never below 2, but only one such
-// CTA fits an SM) 4 warps lose a third.  Where only one CTA of the tiled row
+// 128x128) at 3 stages, 4 warps beat 8 by 1.5-2.9 %, and on 16 KB tiles (fp32
+// 128x32, fp16 128x64) at 4 stages by 3.0-5.0 %, while at 2 stages 8 beat 4
+// by up to 4 %, and where only one 4-stage CTA fits an SM 4 warps lose a
+// third.  Column sums that want four or more CTAs per SM take 2 warps, so that
+// four fit the registers (with 4 warps only three do): fp32 12289 x 8191
+// 128 x 32 and fp16 24577 x 16383 128 x 64 at 2 stages, +3.3-3.7 %.  Where only one CTA of the tiled row
 // sum runs on an SM (`one_per_sm`: its stages leave no room for a second, or
 // the caller asked for one), the wide kernel's 16 warps.  Measured on bf16
 // 64 x 256 tiles with one CTA per SM: the row sum runs at ~6.1 TB/s whatever
@@ -266,7 +269,8 @@ int consumer_warps_for(int op, int tile_m, int boxes, int stages, const mbt_opts
     if (o.consumer_warps) return o.consumer_warps;
     if (flat && op == MBT_OP_ROWSUM) return wanted_ctas <= 2 ? 8 : 4;   // no tile rows
     if (op == MBT_OP_ROWSUM && one_per_sm && wide_ok) return mbt::kMaxWideConsumerWarps;
-    if (op == MBT_OP_ROWSUM && wanted_ctas == 2 && stages == 3 && tile_m <= 128) return 4;
+    if (op == MBT_OP_ROWSUM && wanted_ctas == 2 && stages >= 3 && tile_m <= 128) return 4;
+    if (op == MBT_OP_COLSUM && wanted_ctas >= 4) return 2;
     // The fused copy + row sum on tiles of one 128-byte box and at most 128
     // rows: 4 row-sum warps, whose reads of the stage compete less with the
     // store warp's (fp32 12289 x 8191 128 x 32, fp16 24577 x 16383 and 16384^2
