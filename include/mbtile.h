@@ -112,13 +112,22 @@ typedef struct mbt_opts {
                                 at what fits); 0 => at least 2, and enough
                                 that the stages on one SM hold ~64 KB (copy)
                                 or ~128 KB (row sum) */
-    int32_t consumer_warps;  /* consumer warps per CTA, 1..8; 0 => 4 for
-                                tile_copy; for tile_rowsum 8, or 4 when the
+    int32_t consumer_warps;  /* consumer warps per CTA, 1..8 (up to 16 for
+                                tile_rowsum and tile_colsum, see the
+                                conventions above); 0 => tile_copy 4 (1 with
+                                bulk stores); tile_rowsum 8, or 4 when the
                                 default grid puts 3+ CTAs on an SM and
-                                tile_m <= 128 (and, with a 2-D tensor map,
-                                when it puts 2 on an SM at exactly 3 stages
-                                and tile_m <= 128).  The CTA has one more warp,
-                                the producer. */
+                                tile_m <= 128, or (with a 2-D tensor map) 2
+                                CTAs at 3+ stages and tile_m <= 128, or 16
+                                where one CTA per SM runs; tile_colsum 2
+                                where 4+ CTAs per SM are wanted, else 8, or
+                                4 at 3 CTAs per SM and tile_m <= 128;
+                                tile_copy_rowsum 4 for tiles of one 128-byte
+                                box and at most 128 rows, else 8, or 4 at 3+
+                                CTAs per SM and tile_m <= 128.  The CTA has
+                                one more warp, the
+                                producer, and the warps mbt_plan.threads
+                                lists. */
     int32_t store_mode;      /* tile_copy only (same result in every mode).
                                 1: one consumer thread writes each landed
                                 stage back with bulk tensor stores (same
@@ -195,12 +204,12 @@ typedef struct mbt_opts {
 typedef struct mbt_plan {
     int32_t grid;            /* CTAs launched */
     int32_t threads;         /* threads per CTA = 32 x (1 + consumer_warps),
-                                plus one warp for the fused operation's
-                                stores, or the flush warp of the tiled row
-                                sum and of the column sum (which finishes each
-                                band's / strip's sums while the consumers go
-                                on); none without a producer warp (unified
-                                copy) */
+                                plus the flush warp of the tiled row sums
+                                (the fused operation's too) and of the column
+                                sum (which finishes each band's / strip's
+                                sums while the consumers go on), plus the
+                                fused operation's store warp; none without a
+                                producer warp (unified copy) */
     int32_t consumer_warps;
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t boxes;           /* 128-byte boxes per tile row */
@@ -223,9 +232,13 @@ typedef struct mbt_plan {
                                 tpr / boxes a multiple of 32; see
                                 mbt_opts.pipeline for when it is chosen */
     int32_t col_group;       /* column sum: adjacent column strips taken
-                                together, band by band (2 where the tile row
-                                is 128 bytes and strips are split over CTAs,
-                                else 1); 0 for the other operations */
+                                together, band by band (2 where strips are
+                                split over CTAs and the tile row is 128
+                                bytes, or up to 512 bytes with one CTA per
+                                SM, and the pair's threads per 16-byte chunk
+                                column, 32 x consumer_warps / (8 x boxes),
+                                are a multiple of 8; else 1); 0 for the other
+                                operations */
     int32_t bulk_stores;     /* copy: 1 if stages are written back with bulk
                                 tensor stores (see mbt_opts.store_mode; always
                                 1 for tile_copy_rowsum) */
@@ -309,7 +322,8 @@ int tile_rowsum_ex(const void *src, float *out, int64_t M, int64_t N,
  * with bulk tensor stores ("cute(11) Hopper TMA copy" §6.3-6.4) while the
  * consumer warps reduce it.  The CTA has a producer warp, a store warp (bulk
  * tensor stores of each row's whole 16-byte chunks; its lanes store a row's
- * partial chunk at column N) and the row-sum warps; each stage is released
+ * partial chunk at column N), a flush warp (each band's sums, as in
+ * tile_rowsum) and the row-sum warps; each stage is released
  * when both the store and the row-sum warps are done with it.  Row sums are
  * bit-identical to tile_rowsum's with the same plan.  Workspace: as for
  * tile_rowsum (the library's own unless opts->workspace is given; size for a

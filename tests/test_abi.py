@@ -312,6 +312,25 @@ def test_plan_default_grid_follows_bytes_in_flight():
         assert p["col_group"] == cg, (fit, W)
     p = _plan(mbt.OP_COLSUM, 8192, 65536, 128, 128, 4, torch.bfloat16, fit=1, ws=True)
     assert p["col_group"] == 2 and p["consumer_warps"] == 8        # 256-byte rows: tpc 16
+
+
+def test_plan_warp_counts_on_16_kb_tiles():
+    """Defaults on the ragged shapes' one-box tiles of 128 rows: the row sum
+    takes 4 warps at 3 and 4 stages with two CTAs per SM; the column sum takes
+    2 where four CTAs per SM are wanted (2 stages), so that four fit."""
+    for st, fit, W, grid in ((3, 3, 4, 456), (4, 2, 4, 304), (2, 3, 4, 456)):
+        p = _plan(mbt.OP_ROWSUM, 24577, 16383, 128, 64, st, torch.float16, fit=fit, ws=True,
+                  ld_src=16384)
+        assert (p["consumer_warps"], p["grid"]) == (W, grid), (st, p)
+    p = _plan(mbt.OP_COLSUM, 24577, 16383, 128, 64, 2, torch.float16, fit=5, ws=True,
+              ld_src=16384)
+    assert (p["consumer_warps"], p["grid"], p["col_group"]) == (2, 608, 2)
+    p = _plan(mbt.OP_COLSUM, 24577, 16383, 128, 64, 3, torch.float16, fit=3, ws=True,
+              ld_src=16384)
+    assert (p["consumer_warps"], p["grid"]) == (4, 456)
+    p = _plan(mbt.OP_COLSUM, 24577, 16383, 128, 64, 4, torch.float16, fit=2, ws=True,
+              ld_src=16384)
+    assert (p["consumer_warps"], p["grid"]) == (8, 304)
     p = _plan(mbt.OP_COPY_ROWSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True)
     assert p["consumer_warps"] <= 8
     assert _plan(mbt.OP_COPY, 16384, 16384, 128, 64, 8, torch.float16)["consumer_warps"] == 4
