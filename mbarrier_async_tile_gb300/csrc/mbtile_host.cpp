@@ -255,20 +255,24 @@ int wanted_ctas_per_sm(int op, const mbt_opts &o, int stages, int64_t stage_byte
 // by up to 4 %, and where only one 4-stage CTA fits an SM 4 warps lose a
 // third.  Column sums that want four or more CTAs per SM take 2 warps, so that
 // four fit the registers (with 4 warps only three do): fp32 12289 x 8191
-// 128 x 32 and fp16 24577 x 16383 128 x 64 at 2 stages, +3.3-3.7 %.  Where only one CTA of the tiled row
-// sum runs on an SM (`one_per_sm`: its stages leave no room for a second, or
-// the caller asked for one), the wide kernel's 16 warps.  Measured on bf16
-// 64 x 256 tiles with one CTA per SM: the row sum runs at ~6.1 TB/s whatever
-// the stages (3 to 6) and 1 % faster with 16 warps than with 8; the column
-// sum at ~4.9 TB/s, 2 % slower with 16 (so it keeps 8 unless asked).  Two
-// CTAs of 8 at 2 stages: 6.6-6.8 TB/s for both.  The one-CTA ceiling does not
-// move with stages, consumer warps or the form of the barrier wait.
+// 128 x 32 and fp16 24577 x 16383 128 x 64 at 2 stages, +3.3-3.7 %.  Where
+// only one CTA of the tiled row sum runs on an SM (`one_per_sm`: its stages
+// leave no room for a second, or the caller asked for one): 8 warps where
+// each thread then reads at most one round of 8 chunks of a tile row (boxes x
+// tile_m <= 256; the 8-warp kernel then takes one base address per thread),
+// else the wide kernel's 16.  Measured with one CTA per SM, 8 against 16
+// warps: bf16 64 x 256 at 4 / 5 / 6 stages 6511 / 6641 / 6473 against 6102 /
+// 6108 / 6102 GB/s, and 1-7 % ahead on 9 of 10 other one-round tiles (32 x
+// 512, 256 x 64, 128 x 128, fp32 64 x 128 and 128 x 64); two-round tiles (fp32
+// 128 x 128, bf16 128 x 256) 2-4.5 % behind.  The column sum keeps 8 unless
+// asked (16 measured 2 % slower).
 int consumer_warps_for(int op, int tile_m, int boxes, int stages, const mbt_opts &o,
                        int wanted_ctas, int64_t n_mod, bool flat, bool one_per_sm, bool wide_ok) {
     if (bulk_stores(op, o, n_mod)) return 1;   // one thread issues the stores
     if (o.consumer_warps) return o.consumer_warps;
     if (flat && op == MBT_OP_ROWSUM) return wanted_ctas <= 2 ? 8 : 4;   // no tile rows
-    if (op == MBT_OP_ROWSUM && one_per_sm && wide_ok) return mbt::kMaxWideConsumerWarps;
+    if (op == MBT_OP_ROWSUM && one_per_sm)
+        return boxes * tile_m <= 256 || !wide_ok ? 8 : mbt::kMaxWideConsumerWarps;
     if (op == MBT_OP_ROWSUM && wanted_ctas == 2 && stages >= 3 && tile_m <= 128) return 4;
     if (op == MBT_OP_COLSUM && wanted_ctas >= 4) return 2;
     // The fused copy + row sum on tiles of one 128-byte box and at most 128

@@ -274,22 +274,30 @@ def test_plan_default_grid_follows_bytes_in_flight():
     p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16, fit=4, ws=True)
     assert p["grid"] == 304 and p["consumer_warps"] == 8
     # the same tiles at 3 stages (96 KB per CTA): still 2 CTAs, with 4 warps; at 4
-    # stages only one 128 KB CTA fits an SM: the row sum's wide CTA of 16 consumer
-    # warps (+ producer and flush warps); the column sum keeps 8 unless asked
+    # stages only one 128 KB CTA fits an SM: 8 consumer warps (each thread one
+    # round of 8 chunks; + producer and flush warps); the column sum keeps 8 too
     p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 3, torch.bfloat16, fit=2, ws=True)
     assert p["grid"] == 304 and p["consumer_warps"] == 4
     p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True)
-    assert p["grid"] == 152 and p["consumer_warps"] == 16 and p["threads"] == 32 * 18
+    assert p["grid"] == 152 and p["consumer_warps"] == 8 and p["threads"] == 32 * 10
     assert p["box_barriers"] == 0
+    # tiles whose rows would give each of 256 threads two rounds of 8 chunks
+    # (boxes x tile_m > 256): the wide CTA of 16 consumer warps
+    p = _plan(mbt.OP_ROWSUM, 8192, 32768, 128, 128, 3, torch.float32, fit=1, ws=True)
+    assert p["grid"] == 152 and p["consumer_warps"] == 16 and p["threads"] == 32 * 18
     # (one CTA per SM: its 512-byte strips walked in pairs)
     p = _plan(mbt.OP_COLSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True)
     assert p["grid"] == 152 and p["consumer_warps"] == 8 and p["col_group"] == 2
     p = _plan(mbt.OP_COLSUM, 8192, 65536, 64, 256, 4, torch.bfloat16, fit=1, ws=True,
               consumer_warps=16)
     assert p["threads"] == 32 * 18 and p["col_group"] == 1
-    # a caller's one CTA per SM gets the wide CTA too; 128-byte column-sum tiles
-    # walked in strip pairs, the fused operation and copies never do
+    # a caller's one CTA per SM is planned the same way; 128-byte column-sum
+    # tiles walked in strip pairs, the fused operation and copies never get the
+    # wide CTA
     p = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16, fit=4, ws=True,
+              ctas_per_sm=1)
+    assert p["consumer_warps"] == 8
+    p = _plan(mbt.OP_ROWSUM, 8192, 65536, 128, 256, 2, torch.bfloat16, fit=4, ws=True,
               ctas_per_sm=1)
     assert p["consumer_warps"] == 16
     p = _plan(mbt.OP_COLSUM, 12289, 8191, 128, 32, 8, torch.float32, fit=1, ws=True,
@@ -418,7 +426,9 @@ def test_plan_errors_and_limits():
     p = _plan(mbt.OP_ROWSUM, 1024, 1024, 256, 64, 2, torch.float16, fit=2)
     assert p["consumer_warps"] == 8
     p = _plan(mbt.OP_ROWSUM, 1024, 1024, 256, 64, 2, torch.float16, fit=1)
-    assert p["consumer_warps"] == 16                 # one CTA per SM: the wide CTA
+    assert p["consumer_warps"] == 8                  # one CTA per SM, one round a thread
+    p = _plan(mbt.OP_ROWSUM, 1024, 1024, 256, 128, 2, torch.float16, fit=1)
+    assert p["consumer_warps"] == 16                 # two rounds with 8 warps: the wide CTA
 
 
 def test_plan_rowsum_multibox_tile():

@@ -45,9 +45,9 @@ CASES = {
     "colsum": ("bf16", 512, 4096, lambda x, y, **o: mbt.tile_colsum(
         x, None, 64, 256, 3, split=False, **o), "cols"),
     "rowsum_wide": ("bf16", 512, 4096, lambda x, y, **o: mbt.tile_rowsum(
-        x, None, 64, 256, 4, split=False, **o), "rows"),
+        x, None, 64, 256, 4, consumer_warps=16, split=False, **o), "rows"),
     "colsum_wide": ("bf16", 512, 4096, lambda x, y, **o: mbt.tile_colsum(
-        x, None, 64, 256, 4, split=False, **o), "cols"),
+        x, None, 64, 256, 4, consumer_warps=16, split=False, **o), "cols"),
     "fused": ("bf16", 512, 4096, lambda x, y, **o: mbt.tile_copy_rowsum(
         x, y, None, 128, 64, 3, split=False, **o), "rows+copy"),
     "flat_copy": ("f16", 512, 1001, _copy(), "copy"),

@@ -1,9 +1,9 @@
 """The wide row- and column-sum kernels (more than 8 consumer warps, one CTA
-per SM): the row sum's default where only one CTA fits an SM (4 stages of 32
-KB tiles, or a caller's ctas_per_sm = 1), the column sum's when the caller
-asks for more than 8 warps.  GPU parity against the binary64 oracle on split
-and unsplit plans, ragged shapes and explicit warp counts above 8, sums
-bit-identical from call to call."""
+per SM): the row sum's default where only one CTA fits an SM and 8 warps would
+give each thread two rounds of a tile row's chunks (fp32 128 x 128 tiles),
+else when the caller asks for more than 8 warps, as for the column sum.  GPU
+parity against the binary64 oracle on split and unsplit plans, ragged shapes
+and explicit warp counts above 8, sums bit-identical from call to call."""
 import pytest
 import torch
 
@@ -30,11 +30,11 @@ def _plan(op, M, N, tm, tn, st, dtype, **opt):
 
 CASES = [
     # dtype, dist, M, N, tile_m, tile_n, stages, opts
-    ("bf16", "normal", 2048, 65536, 64, 256, 4, {}),
-    ("bf16", "normal", 2048, 65536, 64, 256, 4, {"split": False}),
-    ("f16", "uniform", 1000, 30001, 64, 256, 4, {}),            # ragged M and N
-    ("f32", "uniform", 777, 20000, 128, 128, 3, {}),            # 512-byte rows, 64 KB tiles
-    ("bf16", "uniform", 4097, 3000, 32, 512, 5, {}),            # 1 KB tile rows
+    ("bf16", "normal", 2048, 65536, 64, 256, 4, {"consumer_warps": 16}),
+    ("bf16", "normal", 2048, 65536, 64, 256, 4, {"consumer_warps": 16, "split": False}),
+    ("f16", "uniform", 1000, 30001, 64, 256, 4, {"consumer_warps": 16}),   # ragged M and N
+    ("f32", "uniform", 777, 20000, 128, 128, 3, {}),    # 512-byte rows, 64 KB tiles: the default
+    ("bf16", "uniform", 4097, 3000, 32, 512, 5, {"consumer_warps": 16}),   # 1 KB tile rows
     ("f16", "normal", 3000, 9000, 128, 64, 2, {"consumer_warps": 12}),
     ("bf16", "normal", 3000, 9000, 256, 64, 3, {"consumer_warps": 16, "ctas_per_sm": 1}),
     ("bf16", "normal", 3000, 9000, 64, 256, 2, {"consumer_warps": 10}),
@@ -97,11 +97,11 @@ def test_wide_full_size_colsum_sampled():
 
 def test_device_plan_of_the_sweep_points():
     """tile_plan_device on the bench's row-sum tiles: 2 CTAs of 8 consumer
-    warps per SM at 2 stages (bands split), one wide CTA per SM at 4."""
+    warps per SM at 2 stages (bands split), one CTA of 8 per SM at 4."""
     sms = mbt.tile_device_info()["num_sms"]
     p2 = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16)
     assert p2["grid"] == 2 * sms and p2["consumer_warps"] == 8 and p2["split"] == 1
     p4 = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 4, torch.bfloat16)
-    assert p4["grid"] == sms and p4["consumer_warps"] == 16
+    assert p4["grid"] == sms and p4["consumer_warps"] == 8
     whole = _plan(mbt.OP_ROWSUM, 8192, 65536, 64, 256, 2, torch.bfloat16, no_split=1)
     assert whole["split"] == 0 and whole["grid"] == 128
