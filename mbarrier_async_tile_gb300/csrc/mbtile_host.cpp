@@ -696,10 +696,12 @@ int plan_on_device(int op, int64_t M, int64_t N, int tile_m, int tile_n, int sta
     int fit = 0;
     rc = fit_of(*plan, &fit);
     if (rc != MBT_OK) return rc;
-    const int threads = plan->threads;
+    const int threads = plan->threads, smem = plan->smem_bytes;
     rc = plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, d.num_sms, d.smem_optin, fit,
                    with_workspace, plan, flat);
-    if (rc != MBT_OK || plan->threads == threads) return rc;
+    // (the second pass may change the warps, or the column sum's flush ring
+    // with its strip group: then the occupancy is asked again)
+    if (rc != MBT_OK || (plan->threads == threads && plan->smem_bytes == smem)) return rc;
     rc = fit_of(*plan, &fit);
     if (rc != MBT_OK) return rc;
     return plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, d.num_sms, d.smem_optin, fit,
