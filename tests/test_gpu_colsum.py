@@ -205,6 +205,30 @@ def test_wide_strip_pairs_where_one_cta_per_sm_runs(case):
     assert torch.equal(out.view(torch.int32), again.view(torch.int32))
 
 
+def test_default_warp_counts_on_16_kb_tiles():
+    """fp16 128 x 64 tiles: at 2 stages the column sum wants four CTAs per SM
+    and takes 2 consumer warps (so that four fit the registers), at 3 stages 4
+    warps; the row sum at 4 stages with two CTAs per SM takes 4.  Every sum
+    against the oracle."""
+    M, N = 4096, 4096
+    x = synthetic.make_matrix(M, N, "f16", "uniform", seed=4242)
+    xd = x.cuda()
+    sms = mbt.tile_device_info()["num_sms"]
+    p2 = mbt.tile_plan_device(mbt.OP_COLSUM, M, N, 128, 64, 2, torch.float16)
+    assert p2["consumer_warps"] == 2 and p2["grid"] == 4 * sms and p2["col_group"] == 2, p2
+    p3 = mbt.tile_plan_device(mbt.OP_COLSUM, M, N, 128, 64, 3, torch.float16)
+    assert p3["consumer_warps"] == 4, p3
+    for st in (2, 3):
+        out = mbt.tile_colsum(xd, None, 128, 64, st)
+        assert mbt.tile_status()[0] == 0
+        assert colsum_errors(out, x)[0] <= ROWSUM_RTOL, st
+    pr = mbt.tile_plan_device(mbt.OP_ROWSUM, M, N, 128, 64, 4, torch.float16)
+    assert pr["consumer_warps"] == 4 and pr["grid"] == 2 * sms, pr
+    rows = mbt.tile_rowsum(xd, None, 128, 64, 4)
+    assert mbt.tile_status()[0] == 0
+    assert rowsum_errors(rows, x)[0] <= ROWSUM_RTOL
+
+
 @pytest.mark.parametrize("split", [False, True])
 def test_flush_ring_wraps_many_times(split):
     """Three CTAs over 1024 one-tile strips (and 512 strip pairs): each CTA's
