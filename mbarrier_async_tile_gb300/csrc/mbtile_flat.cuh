@@ -345,6 +345,93 @@ __device__ __forceinline__ float row_sum_elems_rot(uint32_t addr, int n, int r) 
     }
 }
 
+// The two 16-bit elements of one 4-byte word of the stage, widened exactly
+// as element_value does (the lower address first).
+template <int DT>
+__device__ __forceinline__ float2 pair_value(uint32_t w) {
+    if constexpr (DT == MBT_BF16)
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    else
+        return make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(w))),
+                           __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16))));
+}
+
+// The sum of row_sum_fixed for 16-bit rows of NN elements on a 4-byte
+// boundary: the same elements in the same order, two per 32-bit load (an odd
+// row's last element alone).
+template <int DT, int NN>
+__device__ __forceinline__ float row_sum_pairs_fixed(uint32_t addr) {
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k + 1 < NN; k += 2) {
+        const float2 f = pair_value<DT>(lds32(addr + 2 * k));
+        s += f.x;
+        s += f.y;
+    }
+    if constexpr (NN % 2 == 1) s += lds_element<DT>(addr + 2 * (NN - 1));
+    return s;
+}
+
+template <int DT>
+__device__ __forceinline__ float row_sum_pairs(uint32_t addr, int n) {
+    float s = 0.f;
+    int c = 0;
+    for (; c + 4 <= n; c += 4) {
+        const uint32_t w0 = lds32(addr + 2 * c), w1 = lds32(addr + 2 * c + 4);
+        const float2 f0 = pair_value<DT>(w0), f1 = pair_value<DT>(w1);
+        s += f0.x;
+        s += f0.y;
+        s += f1.x;
+        s += f1.y;
+    }
+    for (; c + 2 <= n; c += 2) {
+        const float2 f = pair_value<DT>(lds32(addr + 2 * c));
+        s += f.x;
+        s += f.y;
+    }
+    if (c < n) s += lds_element<DT>(addr + 2 * c);
+    return s;
+}
+
+// The rotated sum of row_sum_fixed_rot for 16-bit rows of 2 NP elements on a
+// 4-byte boundary whose starting column is even (2 rp): the same elements in
+// the same order, two per 32-bit load, and one wrap test per pair.
+template <int DT, int NP>
+__device__ __forceinline__ float row_sum_pairs_rot_fixed(uint32_t addr, int rp) {
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        const int c = k + rp < NP ? k + rp : k + rp - NP;
+        const float2 f = pair_value<DT>(lds32(addr + 4 * c));
+        s += f.x;
+        s += f.y;
+    }
+    return s;
+}
+
+template <int DT>
+__device__ __forceinline__ float row_sum_pairs_rot(uint32_t addr, int np, int rp) {
+    float s = 0.f;
+    int c = rp;
+    int k = 0;
+    for (; k + 2 <= np; k += 2) {
+        const int c1 = c + 1 == np ? 0 : c + 1;
+        const uint32_t w0 = lds32(addr + 4 * c), w1 = lds32(addr + 4 * c1);
+        const float2 f0 = pair_value<DT>(w0), f1 = pair_value<DT>(w1);
+        s += f0.x;
+        s += f0.y;
+        s += f1.x;
+        s += f1.y;
+        c = c1 + 1 == np ? 0 : c1 + 1;
+    }
+    if (k < np) {
+        const float2 f = pair_value<DT>(lds32(addr + 4 * c));
+        s += f.x;
+        s += f.y;
+    }
+    return s;
+}
+
 // Sum of the elements of the 16-byte chunk `v` at window byte offset cb whose
 // bytes lie in [b0, b1) (window-relative offsets, so 32 bits do), in element order.
 template <int DT>
@@ -479,8 +566,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
                 const int n = static_cast<int>(p.N);
                 // Starting column of this lane's rows: lanes elem_period apart would
                 // otherwise read the same bank at every step.
-                const int rot = kMode == 3 ? (lane / a.elem_period) * (4 / p.esize) % n : 0;
-                // One row loop per row length up to 8 (the row's sum unrolled inside,
+                const int rot = kMode >= 3 ? (lane / a.elem_period) * (4 / p.esize) % n : 0;
+                // One row loop per row length up to 8 (and 10, 12 with two
+                // elements per load; the row's sum unrolled inside,
                 // no branch on the length per row), one for longer rows.  Measured,
                 // same box, bf16 dense: 1 / 3 / 8 columns 2377 -> 4437 / 3483 -> 5753
                 // / 5144 -> 6650 GB/s; 16-32 columns 2-3 % slower than with the
@@ -493,7 +581,15 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
                         float s;
                         if (b0 + row_b <= wj.size) {
                             const uint32_t ra = sbase + static_cast<uint32_t>(b0);
-                            if constexpr (kMode == 3 && NN > 0)
+                            if constexpr (kMode == 5 && NN > 0)
+                                s = row_sum_pairs_fixed<DT, NN>(ra);
+                            else if constexpr (kMode == 5)
+                                s = row_sum_pairs<DT>(ra, n);
+                            else if constexpr (kMode == 4 && NN > 0 && NN % 2 == 0)
+                                s = row_sum_pairs_rot_fixed<DT, NN / 2>(ra, rot / 2);
+                            else if constexpr (kMode == 4)
+                                s = row_sum_pairs_rot<DT>(ra, n / 2, rot / 2);
+                            else if constexpr (kMode == 3 && NN > 0)
                                 s = row_sum_fixed_rot<DT, NN>(ra, rot);
                             else if constexpr (kMode == 3)
                                 s = row_sum_elems_rot<DT>(ra, n, rot);
@@ -524,7 +620,19 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
                     case 6: rows(std::integral_constant<int, 6>{}); break;
                     case 7: rows(std::integral_constant<int, 7>{}); break;
                     case 8: rows(std::integral_constant<int, 8>{}); break;
-                    default: rows(std::integral_constant<int, 0>{}); break;
+                    default:
+                        // With two elements per load, rows of 10 and 12 elements
+                        // unrolled too (longer unrolled rows made the kernel spill).
+                        if constexpr (kMode >= 4) {
+                            switch (n) {
+                                case 10: rows(std::integral_constant<int, 10>{}); break;
+                                case 12: rows(std::integral_constant<int, 12>{}); break;
+                                default: rows(std::integral_constant<int, 0>{}); break;
+                            }
+                        } else {
+                            rows(std::integral_constant<int, 0>{});
+                        }
+                        break;
                 }
                 __syncwarp();
                 if (lane == 0 && p.fault != 2) mbar_arrive(sm.empty0 + 8u * stage);
@@ -644,6 +752,23 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
             }
         }
     };
+    // Mode 4: the rotated rows of mode 3 for 16-bit elements and an even row
+    // length, so that the starting column (a whole 4-byte word) is even and a
+    // pair never straddles the row's end: two elements per load.
+    // Mode 5: the rows of mode 2 for 16-bit elements where the pitch is a
+    // whole number of 4-byte words (so every row starts on one): two elements
+    // per load.
+    if constexpr (DT != MBT_F32) {
+        if (a.rows_per_window > 0 && a.elem_rows && a.elem_period > 0 && (a.p.N & 1) == 0) {
+            run(std::integral_constant<int, 4>{});
+            return;
+        }
+        if (a.rows_per_window > 0 && a.elem_rows && a.elem_period == 0 &&
+            (a.ld * a.p.esize) % 4 == 0) {
+            run(std::integral_constant<int, 5>{});
+            return;
+        }
+    }
     if (a.rows_per_window > 0 && a.elem_rows && a.elem_period > 0)
         run(std::integral_constant<int, 3>{});
     else if (a.rows_per_window > 0 && a.elem_rows)

@@ -4,6 +4,8 @@ bytes, e.g. dense fp16 rows of 16383 elements): 1-D bulk copies of
 (dense src and dst; bytes past the matrix untouched), row sums at any pitch
 within 1e-5 of the binary64 oracle, short rows (several per stage) and long
 rows (pieces of a row per stage)."""
+import math
+
 import pytest
 import torch
 
@@ -103,6 +105,45 @@ def test_flat_rowsum_element_rows(dtype, M, N, ld):
     x = synthetic.make_matrix(M, N, dtype, "normal", seed=M + 13 * N, ld=ld)
     out = torch.full((M,), float("nan"), device="cuda")
     mbt.tile_rowsum(x.cuda()[:, :N], out, 64, 256 if es == 2 else 128, 2)
+    code, info = mbt.tile_status()
+    assert code == 0, info
+    assert not bool(out.isnan().any())
+    worst, rel, _ = rowsum_errors(out, x[:, :N])
+    assert worst <= ROWSUM_RTOL, (worst, rel)
+
+
+@pytest.mark.parametrize("dtype,M,N,ld", [
+    ("bf16", 200000, 2, 8),      # 16-byte pitch: one pair per row
+    ("f16", 150000, 4, 4),       # 8-byte dense pitch
+    ("bf16", 100000, 6, 12),     # 24-byte pitch
+    ("f16", 80000, 10, 16),      # the loop over pairs: 5 pairs (one left after the pairs of pairs)
+    ("bf16", 70000, 16, 16),     # 32-byte dense pitch
+    ("f16", 60000, 24, 32),
+    ("bf16", 50000, 30, 32),     # 15 pairs
+    # pitches of an odd number of 4-byte words: no rotation, pairs from column 0
+    ("bf16", 120000, 6, 6),      # 12 bytes
+    ("f16", 100000, 10, 10),     # 20 bytes
+    ("bf16", 60000, 18, 18),     # 36 bytes: the loop over pairs
+    ("f16", 40000, 30, 30),      # 60 bytes
+    ("bf16", 70000, 17, 18),     # odd row length: the last element alone
+    ("f16", 90000, 1, 2),        # one element in a 4-byte pitch
+    ("bf16", 80000, 7, 10),      # 7 elements (unrolled) in a 20-byte pitch
+])
+def test_flat_rowsum_paired_rows(dtype, M, N, ld):
+    """16-bit rows whose pitch is a whole number of 4-byte words, so that every
+    row starts on one: two elements per 32-bit load.  Where the pitch in words
+    shares a factor with 32 (and the row length is even), lanes start their
+    rows at rotated, even columns; else from column 0, an odd row's last
+    element alone.  Every row is written and matches the oracle."""
+    es = synthetic.ESIZE[dtype]
+    pitch = ld * es
+    assert N * es <= 64 and pitch % 4 == 0
+    assert N % 2 == 0 or math.gcd(pitch // 4, 32) == 1
+    dt = synthetic.DTYPES[dtype]
+    assert mbt.tile_plan_device(mbt.OP_ROWSUM, M, N, 64, 256, 2, dt, ld_src=ld)["flat"] == 1
+    x = synthetic.make_matrix(M, N, dtype, "normal", seed=M + 7 * N, ld=ld)
+    out = torch.full((M,), float("nan"), device="cuda")
+    mbt.tile_rowsum(x.cuda()[:, :N], out, 64, 256, 2)
     code, info = mbt.tile_status()
     assert code == 0, info
     assert not bool(out.isnan().any())
