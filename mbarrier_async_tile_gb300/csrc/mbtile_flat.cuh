@@ -567,8 +567,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
                 // Starting column of this lane's rows: lanes elem_period apart would
                 // otherwise read the same bank at every step.
                 const int rot = kMode >= 3 ? (lane / a.elem_period) * (4 / p.esize) % n : 0;
-                // One row loop per row length up to 8 (and 10, 12 with two
-                // elements per load; the row's sum unrolled inside,
+                // One row loop per row length up to 12 (the row's sum unrolled inside,
                 // no branch on the length per row), one for longer rows.  Measured,
                 // same box, bf16 dense: 1 / 3 / 8 columns 2377 -> 4437 / 3483 -> 5753
                 // / 5144 -> 6650 GB/s; 16-32 columns 2-3 % slower than with the
@@ -621,11 +620,15 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
                     case 7: rows(std::integral_constant<int, 7>{}); break;
                     case 8: rows(std::integral_constant<int, 8>{}); break;
                     default:
-                        // With two elements per load, rows of 10 and 12 elements
-                        // unrolled too (longer unrolled rows made the kernel spill).
-                        if constexpr (kMode >= 4) {
+                        // Rows of 9-12 elements unrolled too (dense bf16 9 / 11
+                        // columns 4032 / 4194 -> 6832 / 6771 GB/s, fp32 10 / 12
+                        // columns 5045 / 5662 -> 6737 / 6748; longer unrolled rows
+                        // made the kernel spill).
+                        if constexpr (kMode >= 2) {
                             switch (n) {
+                                case 9: rows(std::integral_constant<int, 9>{}); break;
                                 case 10: rows(std::integral_constant<int, 10>{}); break;
+                                case 11: rows(std::integral_constant<int, 11>{}); break;
                                 case 12: rows(std::integral_constant<int, 12>{}); break;
                                 default: rows(std::integral_constant<int, 0>{}); break;
                             }
