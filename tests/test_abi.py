@@ -322,6 +322,21 @@ def test_plan_default_grid_follows_bytes_in_flight():
     assert p["col_group"] == 2 and p["consumer_warps"] == 8        # 256-byte rows: tpc 16
 
 
+def test_plan_colsum_shared_memory_holds_the_flush_ring():
+    """The column sum's dynamic shared memory: 1024 bytes of alignment slack,
+    the stages, then one flush-ring slot of one float per consumer thread,
+    element of a 16-byte chunk and strip of the group (32 W x 16 / es x g)."""
+    for dt, es, M, N, tm, tn, st, fit, ld, W, g in (
+            (torch.float32, 4, 12289, 8191, 128, 32, 3, 3, 8192, 4, 2),
+            (torch.float16, 2, 24577, 16383, 128, 64, 3, 3, 16384, 4, 2),
+            (torch.bfloat16, 2, 8192, 65536, 64, 256, 3, 2, 65536, 8, 1),
+            (torch.bfloat16, 2, 8192, 65536, 64, 256, 4, 1, 65536, 8, 2)):
+        p = _plan(mbt.OP_COLSUM, M, N, tm, tn, st, dt, fit=fit, ws=True, ld_src=ld)
+        assert (p["consumer_warps"], p["col_group"]) == (W, g), p
+        ring = 32 * W * (16 // es) * g * 4
+        assert p["smem_bytes"] == 1024 + st * p["stage_bytes"] + ring, (p, ring)
+
+
 def test_plan_warp_counts_on_16_kb_tiles():
     """Defaults on the ragged shapes' one-box tiles of 128 rows: the row sum
     takes 4 warps at 3 and 4 stages with two CTAs per SM; the column sum takes
