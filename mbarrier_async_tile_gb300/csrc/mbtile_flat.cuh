@@ -479,7 +479,11 @@ __device__ __forceinline__ void next_row_window(const FlatArgs &a, int64_t rb, R
 constexpr int kFlatRowSlots = 16;
 constexpr int kFlatVec = 4;   // chunks a thread holds per round (register budget)
 
-template <int DT>
+// ELEM: the instantiation launched for rows of at most kFlatElemRowBytes
+// summed whole by one thread each (modes 2-5: a.elem_rows and whole rows per
+// window); the other holds only the window modes (0, 1), which alone take 88
+// registers instead of 94-96 (bf16 rows of 100 / 2047 elements: +3.4 / +3.6 %).
+template <int DT, bool ELEM = false>
 __global__ void __launch_bounds__(kMaxThreads, 2)
     mbt_rowsum_flat_kernel(const FlatArgs a) {
     extern __shared__ __align__(1024) unsigned char dyn_smem[];
@@ -761,23 +765,33 @@ __global__ void __launch_bounds__(kMaxThreads, 2)
     // Mode 5: the rows of mode 2 for 16-bit elements where the pitch is a
     // whole number of 4-byte words (so every row starts on one): two elements
     // per load.
-    if constexpr (DT != MBT_F32) {
-        if (a.rows_per_window > 0 && a.elem_rows && a.elem_period > 0 && (a.p.N & 1) == 0) {
-            run(std::integral_constant<int, 4>{});
-            return;
+    if constexpr (ELEM) {
+        // (every mode: the element rows' code measured 6-10 % slower on rows of
+        // 13-31 elements when compiled without the window modes beside it)
+        if constexpr (DT != MBT_F32) {
+            if (a.rows_per_window > 0 && a.elem_rows && a.elem_period > 0 &&
+                (a.p.N & 1) == 0) {
+                run(std::integral_constant<int, 4>{});
+                return;
+            }
+            if (a.rows_per_window > 0 && a.elem_rows && a.elem_period == 0 &&
+                (a.ld * a.p.esize) % 4 == 0) {
+                run(std::integral_constant<int, 5>{});
+                return;
+            }
         }
-        if (a.rows_per_window > 0 && a.elem_rows && a.elem_period == 0 &&
-            (a.ld * a.p.esize) % 4 == 0) {
-            run(std::integral_constant<int, 5>{});
-            return;
-        }
+        if (a.rows_per_window > 0 && a.elem_rows && a.elem_period > 0)
+            run(std::integral_constant<int, 3>{});
+        else if (a.rows_per_window > 0 && a.elem_rows)
+            run(std::integral_constant<int, 2>{});
+        else if (a.rows_per_window > 0)
+            run(std::integral_constant<int, 1>{});
+        else
+            run(std::integral_constant<int, 0>{});
+    } else {
+        if (a.rows_per_window > 0)
+            run(std::integral_constant<int, 1>{});
+        else
+            run(std::integral_constant<int, 0>{});
     }
-    if (a.rows_per_window > 0 && a.elem_rows && a.elem_period > 0)
-        run(std::integral_constant<int, 3>{});
-    else if (a.rows_per_window > 0 && a.elem_rows)
-        run(std::integral_constant<int, 2>{});
-    else if (a.rows_per_window > 0)
-        run(std::integral_constant<int, 1>{});
-    else
-        run(std::integral_constant<int, 0>{});
 }

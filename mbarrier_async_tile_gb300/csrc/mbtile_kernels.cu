@@ -1375,17 +1375,30 @@ cudaError_t launch_copy_flat(const FlatArgs &a, int grid, int threads, int smem,
     return launch_pipeline(mbt_copy_flat_kernel, grid, threads, smem, stream, a);
 }
 
-cudaError_t launch_rowsum_flat(int dtype, const FlatArgs &a, int grid, int threads, int smem,
-                               cudaStream_t stream) {
+template <bool ELEM>
+cudaError_t launch_rowsum_flat_t(int dtype, const FlatArgs &a, int grid, int threads, int smem,
+                                 cudaStream_t stream) {
     switch (dtype) {
         case MBT_F16:
-            return launch_pipeline(mbt_rowsum_flat_kernel<MBT_F16>, grid, threads, smem, stream, a);
+            return launch_pipeline(mbt_rowsum_flat_kernel<MBT_F16, ELEM>, grid, threads, smem,
+                                   stream, a);
         case MBT_BF16:
-            return launch_pipeline(mbt_rowsum_flat_kernel<MBT_BF16>, grid, threads, smem, stream,
-                                   a);
+            return launch_pipeline(mbt_rowsum_flat_kernel<MBT_BF16, ELEM>, grid, threads, smem,
+                                   stream, a);
         default:
-            return launch_pipeline(mbt_rowsum_flat_kernel<MBT_F32>, grid, threads, smem, stream, a);
+            return launch_pipeline(mbt_rowsum_flat_kernel<MBT_F32, ELEM>, grid, threads, smem,
+                                   stream, a);
     }
+}
+
+// Rows of at most kFlatElemRowBytes, whole rows per window: the element
+// instantiation (same launch bound as the other, so the occupancy the planner
+// asked of the other holds for it).
+cudaError_t launch_rowsum_flat(int dtype, const FlatArgs &a, int grid, int threads, int smem,
+                               cudaStream_t stream) {
+    if (a.rows_per_window > 0 && a.elem_rows)
+        return launch_rowsum_flat_t<true>(dtype, a, grid, threads, smem, stream);
+    return launch_rowsum_flat_t<false>(dtype, a, grid, threads, smem, stream);
 }
 
 cudaError_t launch_stage_image(const CUtensorMap &map, int32_t row0, int32_t col0, int32_t boxes,
@@ -1427,6 +1440,9 @@ cudaError_t set_kernel_smem_limit(int optin, int *usable) {
                          reinterpret_cast<const void *>(mbt_rowsum_flat_kernel<MBT_F16>),
                          reinterpret_cast<const void *>(mbt_rowsum_flat_kernel<MBT_BF16>),
                          reinterpret_cast<const void *>(mbt_rowsum_flat_kernel<MBT_F32>),
+                         reinterpret_cast<const void *>(mbt_rowsum_flat_kernel<MBT_F16, true>),
+                         reinterpret_cast<const void *>(mbt_rowsum_flat_kernel<MBT_BF16, true>),
+                         reinterpret_cast<const void *>(mbt_rowsum_flat_kernel<MBT_F32, true>),
                          reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F16, false, false>),
                          reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_BF16, false, false>),
                          reinterpret_cast<const void *>(mbt_rowsum_kernel<MBT_F32, false, false>),
