@@ -107,6 +107,27 @@ def test_flat_rowsum_windows_follow_the_rows_not_the_tile():
                  fit=8)["flat"] == 1
 
 
+def test_flat_rowsum_pieces_fill_four_ctas_per_sm():
+    """Long rows in pieces: more than the fewest pieces only where that lets
+    four CTAs share an SM with at least 5 % more bytes of stages in flight."""
+    def pieces(dtype, M, N, S):
+        p = _plan(mbt.OP_ROWSUM, M, N, 64, 256, S, dtype, fit=4)
+        assert p["flat"] == 1 and p["num_tiles"] % M == 0
+        return p["num_tiles"] // M, p["stage_bytes"]
+    # 131070-byte rows: 3 pieces (two 2 x 43 KB CTAs per SM) become 5 of 26 KB
+    # (four CTAs: 208 KB in flight against 172 KB)
+    assert pieces(torch.bfloat16, 4096, 65535, 2) == (5, 26 * 1024)
+    # 80002-byte rows: 2 pieces of 40 KB become 3 of 27 KB
+    assert pieces(torch.float16, 8192, 40001, 2) == (3, 27 * 1024)
+    # 200006-byte rows: 8 pieces would add only 2 %, so 4 of 49 KB stay
+    assert pieces(torch.bfloat16, 2000, 100003, 2) == (4, 49 * 1024)
+    # at 3 stages one 3 x 43 KB CTA per SM gives way to four of 3 x 17 KB
+    assert pieces(torch.bfloat16, 4096, 65535, 3) == (8, 17 * 1024)
+    # whole rows per window are not cut
+    assert _plan(mbt.OP_ROWSUM, 16384, 16383, 64, 256, 2, torch.bfloat16,
+                 fit=4)["num_tiles"] == 16384
+
+
 def test_flat_rowsum_phase_shift_spreads_bank_groups():
     """Short unaligned rows: the 8 / L lane groups of one 8-lane shared-memory
     phase sum rows 2^phase_shift apart.  A 16-byte read's bank group is its
