@@ -340,33 +340,32 @@ void flat_setup(int op, int64_t M, int64_t N, int64_t ld, int es, int tile_m, in
                 f->elem_period = g > 1 ? static_cast<int32_t>(32 / g) : 0;
             }
         } else {
-            // Pieces of a long row: the fewest that fit the window, unless more
-            // of them let kFlatPiecesCtas CTAs share an SM with at least 5 %
-            // more bytes of stages in flight there (CTAs that fit its shared
-            // memory x stages x stage bytes).  Measured, dense rows, 2 stages:
-            // bf16 131 KB rows 3 pieces (2 CTAs per SM) 5434 -> 5 pieces (4)
-            // 6451 GB/s, fp16 80 KB rows 2 -> 3 pieces 5438 -> 6529; bf16
-            // 200 KB rows keep 4 pieces (2 CTAs, 6324 GB/s; 7 pieces on 3 CTAs
-            // 5833).
+            // Pieces of a long row: the count that puts the most bytes of stages
+            // in flight on an SM (CTAs that fit its shared memory, at most
+            // kFlatPiecesCtas, x stages x stage bytes), where that is at least
+            // 5 % more than with the fewest pieces that fit the window.
+            // Measured, dense rows, 2 stages, GB/s: bf16 131 KB rows 3 pieces
+            // (2 CTAs per SM) 5434 -> 5 pieces (4) 6451; fp16 80 KB rows 2 -> 3
+            // pieces 5438 -> 6529; bf16 60 KB rows 1 piece (1 CTA) 4605, 3
+            // pieces (4 CTAs) 6273, 2 pieces (3 CTAs) 6453; bf16 200 KB rows
+            // keep 4 pieces (2 CTAs, 6324; 7 pieces on 3 CTAs 5833).
             const int64_t most = room / es;
             const int64_t p_min = ceil_div(N, most);
-            auto in_flight = [&](int64_t P, int64_t *ctas) {
+            auto in_flight = [&](int64_t P) {
                 const int64_t stage_b =
                     round_up(ceil_div(N, P) * es + 32, mbt::kSwizzleAtomBytes);
                 const int64_t per_cta =
                     std::max(stages, 1) * stage_b + mbt::kSwizzleAtomBytes + kFlatCtaOverheadBytes;
-                *ctas = std::min<int64_t>(kFlatPiecesCtas, kSmemPerSmBytes / per_cta);
-                return *ctas * std::max(stages, 1) * stage_b;
+                const int64_t ctas = std::min<int64_t>(kFlatPiecesCtas, kSmemPerSmBytes / per_cta);
+                return ctas * std::max(stages, 1) * stage_b;
             };
-            int64_t c_min = 0;
-            const int64_t f_min = in_flight(p_min, &c_min);
-            int64_t pieces = p_min;
-            for (int64_t P = p_min + 1; c_min < kFlatPiecesCtas && P <= 4 * p_min; ++P) {
-                int64_t c = 0;
-                const int64_t fl = in_flight(P, &c);
-                if (c == kFlatPiecesCtas) {
+            const int64_t f_min = in_flight(p_min);
+            int64_t pieces = p_min, best = f_min;
+            for (int64_t P = p_min + 1; P <= 4 * p_min + 8 && P <= N; ++P) {
+                const int64_t fl = in_flight(P);
+                if (fl > best) {
+                    best = fl;
                     if (fl * 100 >= f_min * 105) pieces = P;
-                    break;
                 }
             }
             f->pieces_per_row = pieces;

@@ -107,9 +107,10 @@ def test_flat_rowsum_windows_follow_the_rows_not_the_tile():
                  fit=8)["flat"] == 1
 
 
-def test_flat_rowsum_pieces_fill_four_ctas_per_sm():
-    """Long rows in pieces: more than the fewest pieces only where that lets
-    four CTAs share an SM with at least 5 % more bytes of stages in flight."""
+def test_flat_rowsum_pieces_put_most_bytes_in_flight():
+    """Long rows in pieces: the piece count with the most bytes of stages in
+    flight on an SM (CTAs that fit, at most four, x stages x stage bytes), where
+    that beats the fewest pieces by at least 5 %."""
     def pieces(dtype, M, N, S):
         p = _plan(mbt.OP_ROWSUM, M, N, 64, 256, S, dtype, fit=4)
         assert p["flat"] == 1 and p["num_tiles"] % M == 0
@@ -123,6 +124,12 @@ def test_flat_rowsum_pieces_fill_four_ctas_per_sm():
     assert pieces(torch.bfloat16, 2000, 100003, 2) == (4, 49 * 1024)
     # at 3 stages one 3 x 43 KB CTA per SM gives way to four of 3 x 17 KB
     assert pieces(torch.bfloat16, 4096, 65535, 3) == (8, 17 * 1024)
+    # 60002-byte rows: one 59 KB piece leaves one CTA per SM (118 KB in
+    # flight); 2 pieces on 3 CTAs (180 KB) beat 3 on 4 (160 KB)
+    assert pieces(torch.bfloat16, 8192, 30001, 2) == (2, 30 * 1024)
+    assert pieces(torch.float32, 4096, 15001, 2) == (2, 30 * 1024)
+    # ... and at 3 stages 1 piece on one CTA holds as much as any split
+    assert pieces(torch.bfloat16, 8192, 30001, 3) == (1, 59 * 1024)
     # whole rows per window are not cut
     assert _plan(mbt.OP_ROWSUM, 16384, 16383, 64, 256, 2, torch.bfloat16,
                  fit=4)["num_tiles"] == 16384

@@ -63,8 +63,12 @@ def test_flat_copy_matches_oracle(dtype, M, N, tm, tn, st):
     ("f16", "uniform", 2500, 7, 9, 128, 64, 3),         # 14-byte rows, odd pitch
     ("f16", "normal", 777, 8, 11, 128, 64, 2),          # 16-byte rows starting mid-word
     ("f32", "normal", 999, 4, 5, 128, 32, 2),
-    ("f16", "uniform", 501, 16383, 16383, 128, 64, 3),  # long rows: 3 pieces each
-    ("bf16", "normal", 40, 100003, 100003, 64, 256, 2),
+    ("f16", "uniform", 501, 16383, 16383, 128, 64, 3),  # long rows, one piece each
+    ("bf16", "normal", 40, 100003, 100003, 64, 256, 2),  # 4 pieces
+    ("bf16", "uniform", 301, 30001, 30001, 64, 256, 2),  # 2 pieces
+    ("f32", "normal", 77, 15001, 15003, 128, 32, 2),     # 2 pieces, pitched
+    ("bf16", "normal", 65, 65535, 65535, 64, 256, 2),    # 5 pieces
+    ("bf16", "uniform", 33, 65535, 65535, 64, 256, 3),   # 8 pieces
     ("f32", "normal", 123, 8191, 8191, 128, 32, 4),
 ])
 def test_flat_rowsum_matches_oracle(dtype, dist, M, N, ld, tm, tn, st):
