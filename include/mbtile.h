@@ -53,8 +53,9 @@
  *     whole rows -- at most 32 KB while 8 rows fit in that, else at most 64
  *     KB -- or one of equal pieces (at most 64 KB) of a longer row, within
  *     what `stages` stages leave of the shared memory.  A longer row is cut
- *     into the fewest pieces that fit, or into more where that lets four CTAs
- *     share an SM with at least 5 % more bytes of stages in flight.
+ *     into the fewest pieces that fit, or into the count that puts the most
+ *     bytes of stages in flight on an SM (CTAs that fit, at most four, x
+ *     stages x stage bytes) where that is at least 5 % more.
  *   - A tile is tile_m rows by tile_n columns.  tile_n * element size must be
  *     128, 256, 512 or 1024 bytes (1, 2, 4 or 8 side-by-side 128-byte boxes,
  *     each one bulk copy with the 128-byte swizzle); 1 <= tile_m <= 256;
