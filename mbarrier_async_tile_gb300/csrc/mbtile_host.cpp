@@ -38,9 +38,10 @@ constexpr int64_t kRowsumBytesPerSm = 128 * 1024;
 constexpr int64_t kFlatShortWindowBytes = 32 * 1024;
 constexpr int64_t kFlatRowsumWindowBytes = 64 * 1024;
 constexpr int64_t kFlatRowsumBytesPerSm = 192 * 1024;
-// Long rows in pieces: the CTAs per SM that the row sum's consumers fill best
-// (4 of 4 warps: their registers allow no more), an SM's shared memory, and
-// what a CTA takes besides its stages (static memory, the per-block reserve).
+// Long rows in pieces (flat_setup): the most flat row-sum CTAs an SM holds
+// (with 4 consumer warps their registers allow no more), an SM's shared
+// memory, and what a CTA takes besides its stages (static memory, the
+// per-block reserve).
 constexpr int64_t kFlatPiecesCtas = 4;
 constexpr int64_t kSmemPerSmBytes = 228 * 1024;
 constexpr int64_t kFlatCtaOverheadBytes = 2 * 1024;
@@ -351,18 +352,20 @@ void flat_setup(int op, int64_t M, int64_t N, int64_t ld, int es, int tile_m, in
             // keep 4 pieces (2 CTAs, 6324; 7 pieces on 3 CTAs 5833).
             const int64_t most = room / es;
             const int64_t p_min = ceil_div(N, most);
-            auto in_flight = [&](int64_t P) {
+            auto in_flight = [&](int64_t P, int64_t *ctas) {
                 const int64_t stage_b =
                     round_up(ceil_div(N, P) * es + 32, mbt::kSwizzleAtomBytes);
                 const int64_t per_cta =
                     std::max(stages, 1) * stage_b + mbt::kSwizzleAtomBytes + kFlatCtaOverheadBytes;
-                const int64_t ctas = std::min<int64_t>(kFlatPiecesCtas, kSmemPerSmBytes / per_cta);
-                return ctas * std::max(stages, 1) * stage_b;
+                *ctas = std::min<int64_t>(kFlatPiecesCtas, kSmemPerSmBytes / per_cta);
+                return *ctas * std::max(stages, 1) * stage_b;
             };
-            const int64_t f_min = in_flight(p_min);
+            int64_t ctas = 0;
+            const int64_t f_min = in_flight(p_min, &ctas);
             int64_t pieces = p_min, best = f_min;
-            for (int64_t P = p_min + 1; P <= 4 * p_min + 8 && P <= N; ++P) {
-                const int64_t fl = in_flight(P);
+            // Once kFlatPiecesCtas CTAs fit, more pieces only shrink the stages.
+            for (int64_t P = p_min + 1; ctas < kFlatPiecesCtas && P <= N; ++P) {
+                const int64_t fl = in_flight(P, &ctas);
                 if (fl > best) {
                     best = fl;
                     if (fl * 100 >= f_min * 105) pieces = P;
