@@ -509,10 +509,10 @@ int plan_impl(int op, int64_t M, int64_t N, int tile_m, int tile_n, int stages, 
                                         mbt::kSwizzleAtomBytes);
     plan->stage_bytes = static_cast<int32_t>(plan->boxes * box_stride);
     if (flat && op == MBT_OP_ROWSUM) {
-        // The flat row sum loads windows of at most the tile's bytes (at most
-        // kFlatRowsumWindowBytes): whole rows, or equal pieces of a long row.
-        // Stages are sized to the largest window it really loads (+ 16-byte
-        // rounding at both ends), and the grid by those bytes in flight.
+        // The flat row sum's windows do not follow the tile (flat_setup):
+        // whole rows, or equal pieces of a long row.  Stages are sized to the
+        // largest window it really loads (+ 16-byte rounding at both ends),
+        // and the grid by those bytes in flight.
         mbt::FlatArgs f{};
         flat_setup(op, M, N, o.ld_src ? o.ld_src : N, es, tile_m, tile_n, stages, smem_optin, &f);
         const int64_t pitch = (o.ld_src ? o.ld_src : N) * es;
@@ -743,8 +743,6 @@ int plan_on_device(int op, int64_t M, int64_t N, int tile_m, int tile_n, int sta
     return plan_impl(op, M, N, tile_m, tile_n, stages, dtype, o, d.num_sms, d.smem_optin, fit,
                      with_workspace, plan, flat);
 }
-
-
 
 PipeArgs pipe_args(const mbt_plan &plan, int64_t M, int64_t N, int tile_m, int stages, int dtype,
                    const mbt_opts &o) {
