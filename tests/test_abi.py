@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import random
 import torch
 
 import mbarrier_async_tile_gb300 as mbt
@@ -133,6 +134,34 @@ def test_flat_rowsum_pieces_put_most_bytes_in_flight():
     # whole rows per window are not cut
     assert _plan(mbt.OP_ROWSUM, 16384, 16383, 64, 256, 2, torch.bfloat16,
                  fit=4)["num_tiles"] == 16384
+
+
+def test_flat_rowsum_piece_plans_cover_rows_and_fit():
+    """Seeded random long rows at any pitch and 1-8 stages: each row is cut
+    into equal pieces that cover it exactly, a piece (plus 16-byte rounding at
+    both ends) fits its stage, the stages fit shared memory, and the pieces
+    are never fewer than the window bound allows."""
+    rng = random.Random(20261202)
+    smem = 232448
+    for _ in range(400):
+        dtype = rng.choice([torch.bfloat16, torch.float16, torch.float32])
+        es = torch.tensor([], dtype=dtype).element_size()
+        N = rng.randint(8192, 1 << 20)               # rows of 16 KB and more
+        ld = N + rng.choice([0, 1, 3])
+        if ld * es % 16 == 0:
+            ld += 1                                  # a pitch the 1-D kernels take
+        st = rng.randint(1, 8)
+        M = rng.randint(1, 50)
+        p = _plan(mbt.OP_ROWSUM, M, N, 64, 256 if es == 2 else 128, st, dtype, smem=smem,
+                  fit=rng.randint(1, 4), ld_src=ld)
+        assert p["flat"] == 1 and p["smem_bytes"] <= smem
+        pieces = p["num_tiles"] // M
+        assert pieces * M == p["num_tiles"] and pieces >= 1
+        piece = -(-N // pieces)
+        assert (pieces - 1) * piece < N <= pieces * piece          # equal pieces, no empty one
+        assert piece * es + 32 <= p["stage_bytes"]
+        window_cap = min(64 * 1024, (smem - 1024) // st // 1024 * 1024) - 32
+        assert pieces >= -(-N // (window_cap // es))
 
 
 def test_flat_rowsum_phase_shift_spreads_bank_groups():
