@@ -511,7 +511,7 @@ def bench_gpu(args, rank, world):
     t1 = time.time()
     # every workload configuration and the stage sweep, each point
     # in its own clock window
-    sweep = None
+    sweep = flat = None
     read_ref = None if args.no_read_ref else read_reference(dev, clocks)
     # the same at the row-sum workload's size (the same per-launch ramp and tail)
     read_same = (None if args.no_read_ref else
@@ -521,6 +521,8 @@ def bench_gpu(args, rank, world):
         sweep = config_sweep(dev, clocks, measured_peak()[0], theo,
                              read_peak=read_ref["gbs"] if read_ref else None,
                              read_at_size=not args.no_read_ref)
+        flat = flat_points(dev, clocks, measured_peak()[0],
+                           read_peak=read_ref["gbs"] if read_ref else None)
     time.sleep(0.15)
     clocks.stop()
     step_bytes = copy_bytes() + rowsum_bytes()
@@ -617,6 +619,14 @@ def bench_gpu(args, rank, world):
             "(ms = mean per launch, gaps included; ms_host_launched: 20 host launches back "
             "to back), clocks sampled during its replays, output checked on the device "
             "before timing; frac = gbs / measured hbm_gbs")
+    if flat is not None:
+        out["flat_points"] = flat
+        out["flat_note"] = (
+            "the 1-D bulk-copy kernels (row pitches that are not a multiple of 16 bytes, "
+            "and row sums of rows of at most 64 bytes), dense matrices: each point checked "
+            f"on the device, then launched from the host back to back for about "
+            f"{POINT_TARGET_S} s between one event pair (no graph), clocks sampled in that "
+            "window; windows = the plan's bulk-copy windows (row pieces or groups of rows)")
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(x3, d3, x4, o4, args.cpu_budget)
     return out
@@ -860,6 +870,108 @@ CONFIG_POINTS = (
 CONFIG_SEEDS = {"1": 1001, "2": 1002, "3": 1003, "4": 1004, "5a": 1005, "5b": 1006}
 CONFIG_DIST = {"4": "normal"}
 POINT_TARGET_S = 0.25     # device time of each point's timed graph replays
+
+
+# The 1-D bulk-copy path: row pitches that are not a multiple of 16 bytes (a
+# 2-D tensor map cannot describe them) and row sums of rows of at most 64
+# bytes.  (op, dtype, M, N, tile_m, tile_n, stages); every matrix dense.
+FLAT_POINTS = (
+    ("rowsum", "bf16", 4096, 65535, 64, 256, 2),     # 131,070-byte rows, in pieces
+    ("rowsum", "f16", 24577, 16383, 128, 64, 2),     # 32,766-byte rows, one a window
+    ("rowsum", "f16", 4194304, 63, 128, 64, 2),      # 126-byte rows, lane groups
+    ("rowsum", "bf16", 8000000, 16, 64, 256, 2),     # 32-byte rows, one thread a row
+    ("copy", "f16", 24577, 16383, 128, 64, 3),       # one contiguous byte array
+)
+FLAT_SEED = 1007
+
+
+def flat_points(dev, clocks, peak: float, read_peak: float | None = None,
+                target_s: float = POINT_TARGET_S) -> list:
+    """Each FLAT_POINTS entry: run once and checked on the device (copies bit
+    for bit, row sums on 64 sampled rows against a float64 sum within 1e-5 of
+    max(|sum|, sqrt(sum of squares))), 20 launches to size the timed run,
+    then launches from the host back to back for about `target_s` between one
+    event pair on a side stream, with the SM clocks sampled in that window.
+    A point that raises is recorded with its error and the next one runs."""
+    import mbarrier_async_tile_gb300 as mbt
+    import synthetic
+
+    side = torch.cuda.Stream()
+    points = []
+    for op, dt, M, N, tm, tn, st in FLAT_POINTS:
+        rec = {"op": op, "dtype": dt, "shape": [M, N], "ld": N, "tile": [tm, tn],
+               "stages": st}
+        x = y = o = None
+        try:
+            es = ESIZE[dt]
+            x = synthetic.make_matrix(M, N, dt, "uniform", FLAT_SEED, draw_on=str(dev))
+            if op == "copy":
+                y = torch.full_like(x, float("nan"))
+                nbytes = 2 * M * N * es
+
+                def call(s, x=x, y=y):
+                    mbt.tile_copy(x, y, tm, tn, st, stream=s)
+            else:
+                o = torch.full((M,), float("nan"), dtype=torch.float32, device=dev)
+                nbytes = M * N * es + 4 * M
+
+                def call(s, x=x, o=o):
+                    mbt.tile_rowsum(x, o, tm, tn, st, stream=s)
+            plan = mbt.tile_plan_device(mbt.OP_COPY if op == "copy" else mbt.OP_ROWSUM,
+                                        M, N, tm, tn, st, x.dtype)
+            side.wait_stream(torch.cuda.current_stream())
+            call(side)
+            code, info = mbt.tile_status(side)
+            if code != 0:
+                raise RuntimeError(f"pipeline status {code} {info}")
+            if op == "copy":
+                iv = torch.int32 if es == 4 else torch.int16
+                ok = torch.equal(y.view(iv), x.view(iv))
+            else:
+                g = torch.Generator().manual_seed(5)
+                idx = torch.randperm(M, generator=g)[:64].to(dev)
+                part = x.index_select(0, idx).double()
+                ref = part.sum(1)
+                scale = torch.maximum(ref.abs(), part.pow(2).sum(1).sqrt())
+                ok = bool(((o[idx].double() - ref).abs() <= 1e-5 * scale).all())
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            for _ in range(3):
+                call(side)
+            e0.record(side)
+            for _ in range(20):
+                call(side)
+            e1.record(side)
+            torch.cuda.synchronize()
+            n = max(20, int(target_s / max(e0.elapsed_time(e1) / 20 / 1e3, 1e-6)))
+            t0 = time.time()
+            e0.record(side)
+            for _ in range(n):
+                call(side)
+            e1.record(side)
+            torch.cuda.synchronize()
+            t1 = time.time()
+            code, info = mbt.tile_status(side)
+            if code != 0:
+                raise RuntimeError(f"pipeline status {code} {info}")
+            ms = e0.elapsed_time(e1) / n
+            gbs = nbytes / ms / 1e6
+            c = clocks.summary(t0, t1)
+            rec.update(bytes=nbytes, ms=round(ms, 4), gbs=round(gbs, 1),
+                       frac=round(gbs / peak, 4),
+                       frac_of_read_peak=(round(gbs / read_peak, 4)
+                                          if read_peak and op == "rowsum" else None),
+                       grid=plan["grid"], threads=plan["threads"],
+                       stage_bytes=plan["stage_bytes"], windows=plan["num_tiles"],
+                       launches_timed=n, parity_ok=bool(ok),
+                       clocks={"sm_mhz": c.get("sm_mhz"), "sm_max_mhz": c.get("sm_max_mhz"),
+                               "reasons": c.get("reasons"), "samples": c.get("samples")})
+        except Exception as e:   # recorded; the other points and the line go on
+            rec["error"] = f"{type(e).__name__}: {e}"[:300]
+        del x, y, o
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        points.append(rec)
+    return points
 
 
 READ_REF_BYTES = 4 << 30   # the read reference's buffer: far larger than L2
