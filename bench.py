@@ -901,7 +901,7 @@ def flat_points(dev, clocks, peak: float, read_peak: float | None = None,
     for op, dt, M, N, tm, tn, st in FLAT_POINTS:
         rec = {"op": op, "dtype": dt, "shape": [M, N], "ld": N, "tile": [tm, tn],
                "stages": st}
-        x = y = o = None
+        x = y = o = call = None
         try:
             es = ESIZE[dt]
             x = synthetic.make_matrix(M, N, dt, "uniform", FLAT_SEED, draw_on=str(dev))
@@ -967,7 +967,7 @@ def flat_points(dev, clocks, peak: float, read_peak: float | None = None,
                                "reasons": c.get("reasons"), "samples": c.get("samples")})
         except Exception as e:   # recorded; the other points and the line go on
             rec["error"] = f"{type(e).__name__}: {e}"[:300]
-        del x, y, o
+        del x, y, o, call      # the closure holds the tensors too
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         points.append(rec)
