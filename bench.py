@@ -1200,8 +1200,8 @@ def config_sweep(dev, clocks, peak: float, theo: float, target_s: float = POINT_
 
 
 def bench_configs(args):
-    """One JSON line per configuration point (see config_sweep), then the
-    denominators."""
+    """One JSON line per configuration point (see config_sweep) and per
+    1-D bulk-copy point (flat_points), then the denominators."""
     import mbarrier_async_tile_gb300 as mbt
 
     dev = torch.device("cuda", 0)
@@ -1216,6 +1216,8 @@ def bench_configs(args):
         print(json.dumps({"read_reference": ref}), flush=True)
         for rec in config_sweep(dev, clocks, peak, theo, read_peak=ref["gbs"]):
             print(json.dumps(rec), flush=True)
+        for rec in flat_points(dev, clocks, peak, read_peak=ref["gbs"]):
+            print(json.dumps({"flat": rec}), flush=True)
     finally:
         clocks.stop()
     print(json.dumps({"peak_gbs": peak, "peak_source": peak_kind,
