@@ -365,7 +365,7 @@ def bench_gpu(args, rank, world):
         figure) and with an event pair around each launch (each launch then
         also pays its own start-up, which back-to-back launches overlap with
         the previous launch's tail).  Returns (ms back to back, ms per event
-        pair).  In the one-stream pass a row sum starts while L2 still writes
+        pair, (best, median) of the event pairs).  In the one-stream pass a row sum starts while L2 still writes
         back the dirty lines the copy before it left (up to ~126 MB), so that
         pass charges part of the copy's writes to the row sum; here every
         launch follows one of its own kind (steady state)."""
@@ -406,8 +406,10 @@ def bench_gpu(args, rank, world):
         torch.cuda.synchronize()
         barrier(world)
         check()
-        ms_pairs = reduce_max(sum(a.elapsed_time(b) for a, b in evs) / args.steps, world)
-        return ms_b2b, ms_pairs
+        per = [a.elapsed_time(b) for a, b in evs]
+        ms_pairs = reduce_max(sum(per) / len(per), world)
+        pairs_stats = (reduce_max(min(per), world), reduce_max(statistics.median(per), world))
+        return ms_b2b, ms_pairs, pairs_stats
 
     def copy_on(stream):
         mbt.tile_copy(x3, d3, COPY["tile_m"], COPY["tile_n"], args.copy_stages,
@@ -489,8 +491,8 @@ def bench_gpu(args, rank, world):
     # per-kernel passes: steady-state launch durations for the roofline,
     # launched one by one from the host (back to back, and with an event pair
     # around each launch), then replayed from CUDA graphs
-    ms_copy_stream, ms_copy_pairs = run_kernel_pass("copy")
-    ms_rowsum_stream, ms_rowsum_pairs = run_kernel_pass("rowsum")
+    ms_copy_stream, ms_copy_pairs, copy_pairs_stats = run_kernel_pass("copy")
+    ms_rowsum_stream, ms_rowsum_pairs, rowsum_pairs_stats = run_kernel_pass("rowsum")
     ms_copy_graph = time_graphed(graphed(kernel_chunk("copy"), args.steps)) / args.steps
     ms_rowsum_graph = time_graphed(graphed(kernel_chunk("rowsum"), args.steps)) / args.steps
     # sequential passes: both operations on one stream, then again with
@@ -543,6 +545,8 @@ def bench_gpu(args, rank, world):
                  "gbs_host_launched": round(copy_bytes() / ms_copy_stream / 1e6, 1),
                  "ms_event_pairs": round(ms_copy_pairs, 4),
                  "gbs_event_pairs": round(copy_bytes() / ms_copy_pairs / 1e6, 1),
+                 "ms_event_pairs_best": round(copy_pairs_stats[0], 4),
+                 "ms_event_pairs_median": round(copy_pairs_stats[1], 4),
                  "ms_in_one_stream_step": round(ms_copy_seq, 4),
                  "stages": args.copy_stages, "tile": [COPY["tile_m"], COPY["tile_n"]]},
         "rowsum": {"ms": round(ms_rowsum, 4), "bytes": rowsum_bytes(),
@@ -551,6 +555,8 @@ def bench_gpu(args, rank, world):
                    "gbs_host_launched": round(rowsum_bytes() / ms_rowsum_stream / 1e6, 1),
                    "ms_event_pairs": round(ms_rowsum_pairs, 4),
                    "gbs_event_pairs": round(rowsum_bytes() / ms_rowsum_pairs / 1e6, 1),
+                   "ms_event_pairs_best": round(rowsum_pairs_stats[0], 4),
+                   "ms_event_pairs_median": round(rowsum_pairs_stats[1], 4),
                    "ms_in_one_stream_step": round(ms_rowsum_seq, 4),
                    "stages": args.rowsum_stages, "tile": [ROWSUM["tile_m"], ROWSUM["tile_n"]]},
     }
@@ -570,7 +576,8 @@ def bench_gpu(args, rank, world):
                            ", back to back on one stream, one CUDA event pair around all "
                            "of them: mean per launch, gaps included; kernels.*."
                            "ms_host_launched: the same launches from the host; kernels.*."
-                           "ms_event_pairs: host launches with an event pair around each; "
+                           "ms_event_pairs: host launches with an event pair around each "
+                           "(mean; _best and _median of the same launches); "
                            "kernels.*.ms_in_one_stream_step: the two kernels alternating "
                            "on one stream, where each inherits the other's L2 write-back"),
                 "read_peak": read_ref,
