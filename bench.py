@@ -365,10 +365,11 @@ def bench_gpu(args, rank, world):
         figure) and with an event pair around each launch (each launch then
         also pays its own start-up, which back-to-back launches overlap with
         the previous launch's tail).  Returns (ms back to back, ms per event
-        pair, (best, median) of the event pairs).  In the one-stream pass a row sum starts while L2 still writes
-        back the dirty lines the copy before it left (up to ~126 MB), so that
-        pass charges part of the copy's writes to the row sum; here every
-        launch follows one of its own kind (steady state)."""
+        pair, (best, median) of the event pairs).  In the one-stream pass a
+        row sum starts while L2 still writes back the dirty lines the copy
+        before it left (up to ~126 MB), so that pass charges part of the
+        copy's writes to the row sum; here every launch follows one of its
+        own kind (steady state)."""
         def launch():
             if which == "copy":
                 mbt.tile_copy(x3, d3, COPY["tile_m"], COPY["tile_n"], args.copy_stages,
